@@ -1,0 +1,371 @@
+"""Plain CPU oracle for the DLite draft-and-verify round (numpy, float64).
+
+TEST INFRASTRUCTURE ONLY. This module is the slow, obviously-correct statement
+of what the round computes. Only tests/, the smoke check in __graft_entry__ and
+the bench's CPU-baseline / reference leg may import it; the product path never
+does, and it shares no code with the CUDA library.
+
+Sources (web pages on the method; cited by page, section and equation):
+  [P1] "DLite 完全拆解:面向智能体的无历史投机解码" (pinghaoyang.com.cn, 2026-10-19)
+  [P2] "DLite: History-free Speculative Decoding for Agentic AI" paper summary
+       (yomxxx.com, 2026-10-20)
+  [P3] "DFlash block diffusion speculative decoding" (charlestar.github.io)
+
+Every function works on ONE request (the method is per-request independent);
+batching is a loop in draft_round / verify_* callers.
+
+Two precision modes:
+  mirror=False  every value in float64 ("pure").
+  mirror=True   float64 arithmetic, but values are rounded to bfloat16 at the
+                points where the bf16 GPU path stores bf16 activations (listed
+                in `BF16_POINTS`). Weights are taken as given (already bf16).
+
+Readings where the pages are silent (each is restated beside the code):
+  * RMSNorm everywhere, eps from the config (1e-6), applied after adding the
+    depth embedding, before attention, before the FFN and at the end.
+  * Context slots are key/value-only rows: each layer projects the staged z
+    with that layer's W_k, W_v; they get no query, no RoPE (local position 0)
+    and no residual update.
+  * Anchor at local position 0, placeholder i at local position i; RoPE is
+    rotate-half with base theta from the config.
+  * One shared placeholder embedding e_ph; the anchor row is the tied E row.
+  * Sequential head, low-rank RNN form: h_0 = 0,
+        h_i = b_i + P tanh(Q^T [b_i; h_{i-1}]),  i = 1..K,
+    followed by ONE vocabulary projection l_i = E h_i.
+  * Argmax ties go to the lowest token id.
+  * Sampling draws d_i by Gumbel-max on l_i/T with Philox noise; the draft
+    distribution is q_i = softmax(l_i / T).
+"""
+import numpy as np
+
+from . import philox as _ph
+
+BF16_POINTS = ("z", "y_attn", "q", "k", "v", "o", "y_ffn", "a")
+
+
+# ---------------------------------------------------------------- precision
+
+def bf16_round(x):
+    """Round to the nearest bfloat16 (ties to even), returned as float64.
+
+    fp64 -> fp32 (round to nearest even), then fp32 -> bf16 on the bit
+    pattern: add 0x7FFF plus the lowest kept bit, clear the low 16 bits.
+    """
+    x32 = np.asarray(x, dtype=np.float32)
+    u = x32.view(np.uint32).astype(np.uint64)
+    u = (u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))) & np.uint64(0xFFFF0000)
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def _r(x, mirror):
+    return bf16_round(x) if mirror else x
+
+
+def f64(a):
+    """Any array-like (numpy, or a CPU torch tensor via numpy()) as float64."""
+    if hasattr(a, "detach"):
+        a = a.detach().cpu().float().numpy()
+    return np.asarray(a, dtype=np.float64)
+
+
+# ---------------------------------------------------------------- building blocks
+
+def rmsnorm(x, g, eps):
+    """RMSNorm over the last axis: g * x / sqrt(mean(x^2) + eps)."""
+    x = f64(x)
+    return f64(g) * x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+
+
+def rope_rotate_half(x, positions, theta):
+    """Rotary embedding, rotate-half form, on x[..., rows, heads, d_h].
+
+    Pair (j, j + d_h/2) is rotated by angle pos * theta^(-2j/d_h).
+    [P1] §"局部位置编码切断草稿端的全局位置增长": the drafter uses local
+    coordinates only (anchor at 0, placeholders 1, 2, 3, ...).
+    """
+    x = f64(x)
+    d = x.shape[-1]
+    half = d // 2
+    inv_freq = theta ** (-np.arange(half, dtype=np.float64) * 2.0 / d)
+    ang = np.asarray(positions, dtype=np.float64)[:, None] * inv_freq[None, :]   # [rows, half]
+    cos = np.cos(ang)[:, None, :]
+    sin = np.sin(ang)[:, None, :]
+    x1, x2 = x[..., :half], x[..., half:]
+    return np.concatenate([x1 * cos - x2 * sin, x2 * cos + x1 * sin], axis=-1)
+
+
+def block_attention(q, k, v, n_q, n_kv):
+    """Non-causal attention over the whole local block.
+
+    q: [Tq, n_q, d_h]; k, v: [Tk, n_kv, d_h]. Query head h reads key/value head
+    floor(h * n_kv / n_q). Scores q.k / sqrt(d_h), softmax over ALL keys (no
+    mask). [P1] §"锚点是已经确定、尚待目标前向处理的输入": the backbone runs
+    non-causal attention inside the short block so every placeholder is
+    computed at once.
+    """
+    q, k, v = f64(q), f64(k), f64(v)
+    d_h = q.shape[-1]
+    group = n_q // n_kv
+    out = np.empty_like(q)
+    for h in range(n_q):
+        g = h // group
+        s = q[:, h, :] @ k[:, g, :].T / np.sqrt(d_h)          # [Tq, Tk]
+        s = s - s.max(axis=1, keepdims=True)
+        p = np.exp(s)
+        p /= p.sum(axis=1, keepdims=True)
+        out[:, h, :] = p @ v[:, g, :]
+    return out.reshape(q.shape[0], n_q * d_h)
+
+
+def silu(x):
+    return x / (1.0 + np.exp(-x))
+
+
+# ---------------------------------------------------------------- the drafter
+
+def stage(hidden, anchor, W, cfg, mirror=False):
+    """Depth-embedding staging and the local rows of one request.
+
+    z_j = RMSNorm(h_j + e_depth_j) * g_stage for the m selected target layers
+    ([P1] §"History-Free 到底省掉了什么", eq. z_t = h_t + e_depth, "官方实现还
+    会对相加后的特征做归一化"). Local rows: x_0 = E[anchor] (tied embedding),
+    x_i = e_ph for the K placeholders ([P1] §"锚点是已经确定...").
+    Returns z [m, D] and the fp32-class residual stream x [K+1, D].
+    """
+    h = f64(hidden)                                          # [m, D]
+    z = _r(rmsnorm(h + f64(W["e_depth"]), W["g_stage"], cfg.eps), mirror)
+    D, K = cfg.D, cfg.K
+    x = np.empty((K + 1, D))
+    x[0] = f64(W["E"][int(anchor)])
+    x[1:] = f64(W["e_ph"])[None, :]
+    return z, x
+
+
+def backbone_layer(x, z, Wl, cfg, mirror=False):
+    """One pre-norm block over [m context slots | anchor | K placeholders].
+
+    Queries exist only for the anchor and placeholders; keys/values for the
+    context slots and the local rows ([P1] §"本轮临时 K/V 仍然需要计算").
+    Context slots are K/V-only rows projected from z with no extra norm and
+    sit at local position 0, where RoPE is the identity.
+    """
+    K1 = cfg.K + 1
+    n_q, n_kv, d_h = cfg.n_q, cfg.n_kv, cfg.d_h
+    y = _r(rmsnorm(x, Wl["g_attn"], cfg.eps), mirror)
+    pos = np.arange(K1)
+    q = y @ f64(Wl["Wq"]).T
+    k_loc = y @ f64(Wl["Wk"]).T
+    v_loc = y @ f64(Wl["Wv"]).T
+    q = _r(rope_rotate_half(q.reshape(K1, n_q, d_h), pos, cfg.theta), mirror)
+    k_loc = _r(rope_rotate_half(k_loc.reshape(K1, n_kv, d_h), pos, cfg.theta), mirror)
+    v_loc = _r(v_loc.reshape(K1, n_kv, d_h), mirror)
+    k_ctx = _r((z @ f64(Wl["Wk"]).T).reshape(-1, n_kv, d_h), mirror)
+    v_ctx = _r((z @ f64(Wl["Wv"]).T).reshape(-1, n_kv, d_h), mirror)
+    k_all = np.concatenate([k_ctx, k_loc], axis=0)
+    v_all = np.concatenate([v_ctx, v_loc], axis=0)
+    o = _r(block_attention(q, k_all, v_all, n_q, n_kv), mirror)
+    x = x + o @ f64(Wl["Wo"]).T
+    y2 = _r(rmsnorm(x, Wl["g_ffn"], cfg.eps), mirror)
+    a = _r(silu(y2 @ f64(Wl["Wg"]).T) * (y2 @ f64(Wl["Wu"]).T), mirror)
+    return x + a @ f64(Wl["Wd"]).T
+
+
+def backbone(hidden, anchor, W, cfg, mirror=False, taps=None):
+    """Parallel backbone: b_i = RMSNorm(x_i) * g_final for placeholders i=1..K.
+
+    [P1] §"主干并行输出的是表示,还不是有因果联系的完整候选": the backbone
+    emits one vector per draft position, u_1..u_K, all at once.
+    """
+    z, x = stage(hidden, anchor, W, cfg, mirror)
+    if taps is not None:
+        taps["z"] = z
+        taps["x"] = []
+    for Wl in W["layers"]:
+        x = backbone_layer(x, z, Wl, cfg, mirror)
+        if taps is not None:
+            taps["x"].append(x.copy())
+    return rmsnorm(x[1:], W["g_final"], cfg.eps)
+
+
+def sequential_head(b, Q, P):
+    """Low-rank RNN head, direct form, state reset at the start of the block.
+
+    h_0 = 0;  h_i = b_i + P tanh(Q^T [b_i ; h_{i-1}]).  Q is stored as the
+    [R, 2D] matrix that maps [b; h] to R values, P as [D, R].
+    [P2] §设计 (sequential head): a low-rank RNN integrates in-block
+    dependencies in hidden space; [P1] §"官方顺序头具体算了什么": the state is
+    initialised at the start of each block.
+    """
+    b = f64(b)
+    Q, P = f64(Q), f64(P)
+    h_prev = np.zeros(b.shape[1])
+    out = np.empty_like(b)
+    for i in range(b.shape[0]):
+        t = np.tanh(Q @ np.concatenate([b[i], h_prev]))
+        out[i] = b[i] + P @ t
+        h_prev = out[i]
+    return out
+
+
+def lm_logits(h, E, chunk=16384):
+    """The single vocabulary projection l = E h (tied E [V, D]), chunked over V.
+
+    [P2] §设计: the vocabulary projection is done once, after the block's
+    dependencies are integrated; [P1] §"避免的是昂贵的中间词表投影".
+    """
+    h = f64(h)
+    V = E.shape[0]
+    out = np.empty((h.shape[0], V))
+    for s in range(0, V, chunk):
+        out[:, s:s + chunk] = h @ f64(E[s:s + chunk]).T
+    return out
+
+
+def _top2_gap(s):
+    part = np.partition(s, -2, axis=-1)
+    return part[..., -1] - part[..., -2]
+
+
+def draft_request(hidden, anchor, W, cfg, temperature=0.0, seed=0, pos=0, request=0,
+                  mirror=False, taps=None):
+    """One request's draft: candidates d_1..d_K plus what verification needs.
+
+    Greedy (T = 0): d_i = argmax_v l_iv (lowest id on ties).
+    Sampling (T > 0): d_i = argmax_v (l_iv / T + G_iv), G Gumbel noise from
+    Philox(c0 = v >> 2, position = pos + i, request, TAG_GUMBEL), word v & 3.
+    That is an exact draw from q_i = softmax(l_i / T) ([P1] §"从 logits 经过
+    温度缩放和 softmax,得到草稿分布 q_i").
+    Returns dict(cand, logit_d, lse, gap, b, h).
+    """
+    b = backbone(hidden, anchor, W, cfg, mirror, taps)
+    h = sequential_head(b, W["Q"], W["P"])
+    ell = lm_logits(h, W["E"])
+    K = cfg.K
+    if temperature == 0.0:
+        cand = np.argmax(ell, axis=1)
+        gap = _top2_gap(ell)
+        logit_d = ell[np.arange(K), cand]
+        lse = np.full(K, np.nan)
+    else:
+        s = np.empty_like(ell)
+        for i in range(K):
+            s[i] = ell[i] / temperature + _ph.gumbel_row(seed, pos + i + 1, request, ell.shape[1])
+        cand = np.argmax(s, axis=1)
+        gap = _top2_gap(s)
+        logit_d = ell[np.arange(K), cand]
+        m = (ell / temperature).max(axis=1)
+        lse = m + np.log(np.exp(ell / temperature - m[:, None]).sum(axis=1))
+    if taps is not None:
+        taps["b"] = b
+        taps["h"] = h
+        taps["logits"] = ell
+    return dict(cand=cand.astype(np.int64), logit_d=logit_d, lse=lse, gap=gap, b=b, h=h)
+
+
+# ---------------------------------------------------------------- verification
+
+def verify_greedy(cand, target_tokens):
+    """Longest accepted prefix, greedy mode.
+
+    target_tokens[j] is the target's argmax at input index j of [a, d_1..d_K],
+    i.e. its choice for position j+1. Draft d_i passes iff d_i equals
+    target_tokens[i-1]; A is the length of the leading run of passes (the
+    cumulative product of the pass flags: "pass, pass, fail, pass" gives A = 2).
+    The round commits d_1..d_A then target_tokens[A] (correction, or the bonus
+    token when A = K); that token is the next anchor.
+    [P1] §"一次因果前向评估整条候选", §"贪心模式与随机模式要分别说明",
+    §"一轮执行后..." steps 4-5.
+    """
+    cand = [int(c) for c in cand]
+    K = len(cand)
+    A = 0
+    while A < K and cand[A] == int(target_tokens[A]):
+        A += 1
+    tok = int(target_tokens[A])
+    return dict(A=A, commits=cand[:A] + [tok], n_commit=A + 1, next_anchor=tok)
+
+
+def inverse_cdf(w, u):
+    """Smallest index v with sum_{w<=v} w > u * sum(w), prefix sums in float64."""
+    c = np.cumsum(np.asarray(w, dtype=np.float64))
+    return int(np.searchsorted(c, u * c[-1], side="right"))
+
+
+N_PROPOSALS = 32
+
+
+def verify_sample(cand, logit_d, lse, h, E, p, temperature, seed, pos, request):
+    """Speculative rejection sampling with residual resampling, one request.
+
+    For i = 1..K: q_i(d_i) = exp(l_{i,d_i}/T - lse_i); with
+    u_i = Philox(0, pos + i, request, TAG_ACCEPT) word 0, d_i is accepted iff
+    u_i * q_i(d_i) < p_{i-1}(d_i), i.e. with probability min(1, p/q)
+    ([P1] §"贪心模式与随机模式要分别说明", eq. alpha(d) = min(1, p(d)/q(d))).
+    A = index of the first rejection (K if none).
+    A < K: draw from p_res = [p_A - q_{A+1}]_+ / sum ([P1] eq. p_res) by
+      proposal-rejection: propose v ~ p_A by inverse CDF with
+      u = Philox(j, pos+A+1, request, TAG_RESID) word 0 and keep it iff
+      word 1 * p(v) < p(v) - q(v); this keeps v with probability
+      max(0, 1 - q(v)/p(v)), so kept draws follow p_res exactly. After
+      N_PROPOSALS misses, inverse CDF over [p - q]_+ itself with
+      u = Philox(N_PROPOSALS, ...) word 0 (over p if that mass is 0).
+    A = K: the bonus token is drawn from p_K by inverse CDF with
+      u = Philox(0, pos+K+1, request, TAG_BONUS) word 0.
+    q(v) for arbitrary v is recomputed from the head state: exp(E_v.h/T - lse).
+    """
+    T = float(temperature)
+    cand = [int(c) for c in cand]
+    K = len(cand)
+    p = f64(p)
+    A = K
+    for i in range(1, K + 1):
+        d = cand[i - 1]
+        q_d = np.exp(float(logit_d[i - 1]) / T - float(lse[i - 1]))
+        u = float(_ph.draw(seed, 0, pos + i, request, _ph.TAG_ACCEPT, 0))
+        if not (u * q_d < p[i - 1, d]):
+            A = i - 1
+            break
+    resampled = "bonus"
+    if A == K:
+        u = float(_ph.draw(seed, 0, pos + K + 1, request, _ph.TAG_BONUS, 0))
+        tok = inverse_cdf(p[K], u)
+    else:
+        row = p[A]
+        hrow = f64(h[A])
+        lse_a = float(lse[A])
+        tok = None
+        for j in range(N_PROPOSALS):
+            u1 = float(_ph.draw(seed, j, pos + A + 1, request, _ph.TAG_RESID, 0))
+            u2 = float(_ph.draw(seed, j, pos + A + 1, request, _ph.TAG_RESID, 1))
+            v = inverse_cdf(row, u1)
+            q_v = np.exp(float(f64(E[v]) @ hrow) / T - lse_a)
+            if u2 * row[v] < row[v] - q_v:
+                tok = v
+                resampled = "proposal"
+                break
+        if tok is None:
+            q_all = np.exp(lm_logits(hrow[None, :], E)[0] / T - lse_a)
+            r = np.maximum(row - q_all, 0.0)
+            u3 = float(_ph.draw(seed, N_PROPOSALS, pos + A + 1, request, _ph.TAG_RESID, 0))
+            tok = inverse_cdf(r if r.sum() > 0 else row, u3)
+            resampled = "fallback"
+    return dict(A=A, commits=cand[:A] + [tok], n_commit=A + 1, next_anchor=tok, how=resampled)
+
+
+# ---------------------------------------------------------------- batch drivers
+
+def draft_round(hidden, anchor, W, cfg, temperature=0.0, seed=0, pos=None, mirror=False,
+                requests=None):
+    """Draft for each request b in `requests` (default: all rows of `hidden`)."""
+    B = len(anchor)
+    pos = np.zeros(B, dtype=np.int64) if pos is None else np.asarray(pos)
+    reqs = range(B) if requests is None else requests
+    return {b: draft_request(hidden[b], anchor[b], W, cfg, temperature, seed, int(pos[b]), b, mirror)
+            for b in reqs}
+
+
+# ---------------------------------------------------------------- cost model
+
+def draft_kv_bytes(L_D, H, n_kv, d_h, bytes_per_elem):
+    """History draft-KV size M = 2 L_D H n_kv d_h b ([P1] §"本轮临时 K/V 仍然需要计算")."""
+    return 2 * L_D * H * n_kv * d_h * bytes_per_elem

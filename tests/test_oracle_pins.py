@@ -1,0 +1,397 @@
+"""Pins of the CPU oracle against facts fixed outside itself.
+
+Each check is chosen so that a plausible slip in the oracle (a dropped term, a
+wrong sign, a transposed operand, an off-by-one index) fails at least one:
+published known-answer vectors, closed forms, library routines on special
+cases, brute force on tiny inputs, and distributional identities checked by
+Monte Carlo.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import dlite_oracle as O
+from oracle import philox as ph
+from history_free_speculative_gb300 import workload as wk
+from history_free_speculative_gb300 import reporter as rp
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden_lines(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return [l.strip() for l in f if l.strip() and not l.startswith("#")]
+
+
+# ---------------------------------------------------------------- RNG
+
+def test_philox_known_answers():
+    for line in _golden_lines("philox4x32_10_kat.txt"):
+        lhs, rhs = line.split("->")
+        c0, c1, c2, c3, k0, k1 = (int(t, 16) for t in lhs.split())
+        want = [int(t, 16) for t in rhs.split()]
+        got = ph.philox4x32_10(c0, c1, c2, c3, k0, k1)
+        assert [int(g) for g in got] == want
+
+
+def test_uniform_open_interval_and_exact_in_fp32():
+    x = np.array([0, 1, 511, 512, 0x7FFFFFFF, 0xFFFFFFFF], dtype=np.uint64)
+    u = ph.uniform_open(x)
+    assert u[0] == 0.5 * 2.0 ** -23 and u[-1] == 1.0 - 0.5 * 2.0 ** -23
+    assert np.all((u > 0) & (u < 1))
+    assert np.all(u.astype(np.float32).astype(np.float64) == u)
+
+
+def test_gumbel_max_matches_softmax():
+    """Gumbel-max over l/T draws from softmax(l/T): chi-square over 8 ids."""
+    rng = np.random.default_rng(0)
+    V, T, N = 8, 0.7, 30000
+    ell = rng.normal(0, 1.0, V)
+    counts = np.zeros(V)
+    for n in range(N):
+        s = ell / T + ph.gumbel_row(77, n, 3, V)
+        counts[np.argmax(s)] += 1
+    p = np.exp(ell / T - ell.max() / T)
+    p /= p.sum()
+    chi2 = ((counts - N * p) ** 2 / (N * p)).sum()
+    assert chi2 < 30.0          # 7 dof; P(chi2 > 30) ~ 1e-4
+
+
+def test_draws_are_keyed_by_seed_request_position_tag():
+    base = ph.draw(5, 0, 10, 2, ph.TAG_ACCEPT, 0)
+    for args in [(6, 0, 10, 2, ph.TAG_ACCEPT), (5, 1, 10, 2, ph.TAG_ACCEPT),
+                 (5, 0, 11, 2, ph.TAG_ACCEPT), (5, 0, 10, 3, ph.TAG_ACCEPT),
+                 (5, 0, 10, 2, ph.TAG_RESID)]:
+        assert ph.draw(*args, 0) != base
+    assert ph.draw(5, 0, 10, 2, ph.TAG_ACCEPT, 0) == base
+
+
+# ---------------------------------------------------------------- precision helper
+
+def test_bf16_round_matches_torch():
+    rng = np.random.default_rng(1)
+    x = np.concatenate([rng.normal(0, 1, 10000), rng.normal(0, 1e-3, 1000), rng.normal(0, 1e4, 1000)])
+    x32 = x.astype(np.float32)
+    want = torch.from_numpy(x32).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(O.bf16_round(x32), want)
+
+
+# ---------------------------------------------------------------- building blocks
+
+def test_rmsnorm_closed_form():
+    y = O.rmsnorm(np.array([3.0, 4.0]), np.array([1.0, 2.0]), 0.0)
+    r = math.sqrt((9 + 16) / 2)
+    assert np.allclose(y, [3 / r, 8 / r], rtol=0, atol=1e-15)
+    x = np.random.default_rng(2).normal(0, 5, (6, 64))
+    y = O.rmsnorm(x, np.full(64, 1.5), 0.0)
+    assert np.allclose(np.sqrt((y ** 2).mean(axis=1)), 1.5, atol=1e-12)
+
+
+def test_rope_is_complex_rotation_and_identity_at_zero():
+    rng = np.random.default_rng(3)
+    d, theta = 16, 1e6
+    x = rng.normal(size=(5, 2, d))
+    pos = np.arange(5)
+    y = O.rope_rotate_half(x, pos, theta)
+    assert np.array_equal(y[0], x[0])                      # position 0 = identity
+    # independent statement: (x_j + i x_{j+d/2}) * exp(i * pos * theta^(-2j/d))
+    half = d // 2
+    z = x[..., :half] + 1j * x[..., half:]
+    freq = theta ** (-2.0 * np.arange(half) / d)
+    w = z * np.exp(1j * pos[:, None, None] * freq[None, None, :])
+    assert np.allclose(y[..., :half], w.real, atol=1e-12)
+    assert np.allclose(y[..., half:], w.imag, atol=1e-12)
+
+
+def test_attention_matches_sdpa_library():
+    rng = np.random.default_rng(4)
+    n_q, n_kv, d = 8, 2, 32
+    q = rng.normal(size=(5, n_q, d))
+    k = rng.normal(size=(9, n_kv, d))
+    v = rng.normal(size=(9, n_kv, d))
+    got = O.block_attention(q, k, v, n_q, n_kv)
+    tq = torch.from_numpy(q).permute(1, 0, 2)[None]
+    tk = torch.from_numpy(k).repeat_interleave(n_q // n_kv, dim=1).permute(1, 0, 2)[None]
+    tv = torch.from_numpy(v).repeat_interleave(n_q // n_kv, dim=1).permute(1, 0, 2)[None]
+    want = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=False)
+    want = want[0].permute(1, 0, 2).reshape(5, n_q * d).numpy()
+    assert np.allclose(got, want, atol=1e-12)
+
+
+def test_attention_zero_query_is_mean_of_values():
+    rng = np.random.default_rng(5)
+    v = rng.normal(size=(7, 1, 4))
+    o = O.block_attention(np.zeros((3, 2, 4)), rng.normal(size=(7, 1, 4)), v, 2, 1)
+    assert np.allclose(o.reshape(3, 2, 4), v.mean(axis=0)[None], atol=1e-14)
+
+
+# ---------------------------------------------------------------- drafter structure
+
+def _tiny(**kw):
+    return wk.shrink(wk.TINY, **kw)
+
+
+def _weights(cfg, seed=11, jitter=False):
+    W = wk.make_weights(cfg, seed, gain_jitter=jitter)
+    return W
+
+
+def test_layer_is_residual():
+    cfg = _tiny()
+    W = _weights(cfg)
+    Wl = dict(W["layers"][0])
+    Wl["Wo"] = torch.zeros_like(Wl["Wo"])
+    Wl["Wd"] = torch.zeros_like(Wl["Wd"])
+    rng = np.random.default_rng(6)
+    x = rng.normal(size=(cfg.K + 1, cfg.D))
+    z = rng.normal(size=(cfg.m, cfg.D))
+    assert np.array_equal(O.backbone_layer(x, z, Wl, cfg), x)
+
+
+def test_context_slots_are_an_unordered_set():
+    """Sequence-dim context slots all sit at local position 0: permuting
+    (hidden_j, e_depth_j) pairs together cannot change the draft."""
+    cfg = _tiny()
+    W = _weights(cfg)
+    hidden, anchor, _ = wk.make_round_inputs(wk.WORKLOADS["tiny"], B=1)
+    perm = torch.tensor([2, 0, 3, 1])
+    b0 = O.backbone(hidden[0], anchor[0], W, cfg)
+    W2 = dict(W)
+    W2["e_depth"] = W["e_depth"][perm]
+    b1 = O.backbone(hidden[0][perm], anchor[0], W2, cfg)
+    assert np.allclose(b0, b1, atol=1e-12)
+    # ... while moving one slot's feature to another depth does change it
+    hid3 = hidden[0].clone()
+    hid3[[0, 1]] = hid3[[1, 0]]
+    b3 = O.backbone(hid3, anchor[0], W, cfg)
+    assert np.abs(b3 - b0).max() > 1e-3
+
+
+def test_block_attention_is_non_causal():
+    """The anchor row (position 0) sees the placeholders: changing e_ph moves it."""
+    cfg = _tiny()
+    W = _weights(cfg)
+    hidden, anchor, _ = wk.make_round_inputs(wk.WORKLOADS["tiny"], B=1)
+    z, x = O.stage(hidden[0], anchor[0], W, cfg)
+    x_a = O.backbone_layer(x, z, W["layers"][0], cfg)
+    W2 = dict(W)
+    W2["e_ph"] = W["e_ph"] * 3.0
+    z2, x2 = O.stage(hidden[0], anchor[0], W2, cfg)
+    x_b = O.backbone_layer(x2, z2, W["layers"][0], cfg)
+    assert np.array_equal(x[0], x2[0])
+    assert np.abs(x_a[0] - x_b[0]).max() > 1e-4
+
+
+def test_gains_are_applied():
+    cfg = _tiny()
+    Wj = _weights(cfg, jitter=True)
+    W1 = _weights(cfg, jitter=False)
+    hidden, anchor, _ = wk.make_round_inputs(wk.WORKLOADS["tiny"], B=1)
+    b_j = O.backbone(hidden[0], anchor[0], Wj, cfg)
+    b_1 = O.backbone(hidden[0], anchor[0], W1, cfg)
+    g = O.f64(Wj["g_final"])
+    # b / g_final is the plain normalised stream: unit RMS up to the eps term
+    assert np.allclose(np.sqrt(((b_j / g) ** 2).mean(axis=1)), 1.0, atol=1e-3)
+    assert np.abs(b_j - b_1).max() > 0.05
+
+
+def test_staging_closed_form():
+    cfg = _tiny()
+    W = _weights(cfg, jitter=True)
+    hidden, anchor, _ = wk.make_round_inputs(wk.WORKLOADS["tiny"], B=1)
+    z, x = O.stage(hidden[0], anchor[0], W, cfg)
+    s = O.f64(hidden[0]) + O.f64(W["e_depth"])
+    j = 2
+    want = O.f64(W["g_stage"]) * s[j] / math.sqrt(float(np.dot(s[j], s[j])) / cfg.D + cfg.eps)
+    assert np.allclose(z[j], want, atol=1e-12)
+    assert np.array_equal(x[0], O.f64(W["E"][int(anchor[0])]))
+    assert all(np.array_equal(x[i], O.f64(W["e_ph"])) for i in range(1, cfg.K + 1))
+
+
+# ---------------------------------------------------------------- sequential head
+
+def test_head_with_zero_P_is_identity():
+    rng = np.random.default_rng(7)
+    b = rng.normal(size=(5, 16))
+    assert np.array_equal(O.sequential_head(b, rng.normal(size=(4, 32)), np.zeros((16, 4))), b)
+
+
+def test_head_first_step_closed_form():
+    """h_0 = 0 and the [b; h] order: h_1 = b_1 + P tanh(Q[:, :D] b_1)."""
+    rng = np.random.default_rng(8)
+    D, R = 16, 4
+    b = rng.normal(size=(1, D))
+    Q = rng.normal(size=(R, 2 * D)) * 0.3
+    P = rng.normal(size=(D, R))
+    h = O.sequential_head(b, Q, P)
+    assert np.allclose(h[0], b[0] + P @ np.tanh(Q[:, :D] @ b[0]), atol=1e-14)
+
+
+def test_head_low_rank_recurrence_identity():
+    """Feeding back h_{i-1} = b_{i-1} + P t_{i-1} gives the R x R recurrence
+    t_i = tanh(Q_b b_i + Q_h b_{i-1} + (Q_h P) t_{i-1}); the two forms agree."""
+    rng = np.random.default_rng(9)
+    D, R, K = 24, 6, 7
+    b = rng.normal(size=(K, D))
+    Q = rng.normal(size=(R, 2 * D)) * 0.2
+    P = rng.normal(size=(D, R)) * 0.5
+    Qb, Qh = Q[:, :D], Q[:, D:]
+    M = Qh @ P
+    t_prev = np.zeros(R)
+    e_prev = np.zeros(R)
+    want = np.empty_like(b)
+    for i in range(K):
+        t = np.tanh(Qb @ b[i] + e_prev + M @ t_prev)
+        want[i] = b[i] + P @ t
+        t_prev, e_prev = t, Qh @ b[i]
+    assert np.allclose(O.sequential_head(b, Q, P), want, atol=1e-12)
+
+
+# ---------------------------------------------------------------- LM head
+
+def test_greedy_ties_go_to_lowest_id():
+    cfg = _tiny(V=8, D=4, K=1)
+    h = np.array([[1.0, 0.0, 0.0, 0.0]])
+    E = np.zeros((8, 4))
+    E[[2, 5, 6], 0] = 1.0
+    ell = O.lm_logits(h, E)
+    assert int(np.argmax(ell[0])) == 2
+
+
+def test_lse_matches_library():
+    from scipy.special import logsumexp
+    cfg = _tiny()
+    W = _weights(cfg)
+    hidden, anchor, _ = wk.make_round_inputs(wk.WORKLOADS["tiny"], B=1)
+    r = O.draft_request(hidden[0], anchor[0], W, cfg, temperature=0.7, seed=3, pos=5, request=0)
+    ell = O.lm_logits(r["h"], W["E"])
+    assert np.allclose(r["lse"], logsumexp(ell / 0.7, axis=1), atol=1e-12)
+    assert np.allclose(r["logit_d"], ell[np.arange(cfg.K), r["cand"]], atol=0)
+
+
+# ---------------------------------------------------------------- verification
+
+def test_pages_prefix_example():
+    for line in _golden_lines("pages_examples.txt"):
+        if line.startswith("prefix_flags"):
+            flags = [int(t) for t in line.split("->")[0].split()[1:]]
+            want = int(line.split("->")[1].split()[1])
+            cand = [7, 8, 9, 10]
+            tgt = [c if f else c + 1 for c, f in zip(cand, flags)] + [99]
+            r = O.verify_greedy(cand, tgt)
+            assert r["A"] == want and r["n_commit"] == want + 1
+            assert r["commits"] == cand[:want] + [tgt[want]] and r["next_anchor"] == tgt[want]
+        if line.startswith("next_index"):
+            A = int(line.split()[2])
+            idx = int(line.split("->")[1])
+            cand = [1, 2, 3, 4]
+            tgt = [1, 2, 3, 4, 5]
+            tgt[A] = 0 if A < 4 else tgt[A]
+            r = O.verify_greedy(cand, tgt)
+            assert r["A"] == A == idx
+
+
+def test_greedy_prefix_brute_force_exhaustive():
+    """All candidate/target pairs for V = 3, K = 3 against the cumprod rule."""
+    import itertools
+    V, K = 3, 3
+    for cand in itertools.product(range(V), repeat=K):
+        for tgt in itertools.product(range(V), repeat=K + 1):
+            r = O.verify_greedy(cand, tgt)
+            passes = np.array([cand[i] == tgt[i] for i in range(K)], dtype=np.int64)
+            A = int(np.cumprod(passes).sum())
+            assert r["A"] == A and 0 <= A <= K
+            assert r["commits"] == list(cand[:A]) + [tgt[A]]
+
+
+def _q_setup(V, ell):
+    """E = I, h = l, so that E h = l exactly (D = V)."""
+    E = np.eye(V)
+    return E, np.asarray(ell, dtype=np.float64)
+
+
+@pytest.mark.parametrize("case", ["disjoint", "overlapping"])
+def test_speculative_sampling_preserves_target(case):
+    """Committed token ~ p and first-position acceptance ~ sum_v min(p, q)."""
+    rng = np.random.default_rng(12 if case == "disjoint" else 13)
+    V, T, N = 6, 0.7, 12000
+    ell = rng.normal(0, 1.0, V)
+    E, h = _q_setup(V, ell)
+    q = np.exp(ell / T - ell.max() / T)
+    q /= q.sum()
+    if case == "disjoint":
+        p = rng.dirichlet(np.ones(V) * 0.5)
+    else:                                  # p close to q: rejections rare, fallback exercised
+        p = 0.93 * q + 0.07 * rng.dirichlet(np.ones(V))
+    lse = float(np.log(np.exp(ell / T).sum()))
+    counts = np.zeros(V)
+    accepted = 0
+    hows = {}
+    for n in range(N):
+        s = ell / T + ph.gumbel_row(21, n + 1, 0, V)
+        d = int(np.argmax(s))
+        pp = np.stack([p, np.full(V, 1.0 / V)])          # K = 1: row 0 verifies, row 1 bonus
+        r = O.verify_sample([d], [ell[d]], [lse], h[None, :], E, pp, T, 21, n, 0)
+        if r["A"] == 1:
+            accepted += 1
+            counts[d] += 1
+        else:
+            counts[r["commits"][0]] += 1
+        hows[r["how"]] = hows.get(r["how"], 0) + 1
+    beta = np.minimum(p, q).sum()
+    assert abs(accepted / N - beta) < 5 * math.sqrt(beta * (1 - beta) / N)
+    chi2 = ((counts - N * p) ** 2 / (N * p)).sum()
+    assert chi2 < 35.0                                    # 5 dof
+    if case == "overlapping":
+        assert hows.get("fallback", 0) > 0
+
+
+def test_prefix_survival_is_product_of_conditionals():
+    """P(A >= k) = prod c_i, and E[A+1] = 1 + sum_k P(A >= k)."""
+    rng = np.random.default_rng(14)
+    K, N, V = 5, 40000, 50
+    c = np.array([0.9, 0.8, 0.85, 0.6, 0.95])
+    cand = rng.integers(0, V, size=(N, K))
+    agree = rng.random((N, K)) < c
+    tgt = np.where(agree, cand, (cand + 1 + rng.integers(0, V - 1, size=(N, K))) % V)
+    tgt = np.concatenate([tgt, rng.integers(0, V, size=(N, 1))], axis=1)
+    A = np.array([O.verify_greedy(cand[n], tgt[n])["A"] for n in range(N)])
+    want = np.cumprod(c)
+    for k in range(1, K + 1):
+        est = (A >= k).mean()
+        assert abs(est - want[k - 1]) < 5 * math.sqrt(want[k - 1] * (1 - want[k - 1]) / N)
+    assert abs((A + 1).mean() - rp.expected_advance(rp.prefix_survival(c))) < 0.03
+
+
+# ---------------------------------------------------------------- cost-model arithmetic
+
+def test_pages_time_model_examples():
+    for line in _golden_lines("pages_examples.txt"):
+        t = line.split()
+        if t[0] == "speedup":
+            assert rp.speedup(float(t[2]), float(t[4]), float(t[6])) == pytest.approx(float(t[-1]))
+        if t[0] == "relative":
+            assert rp.relative_rate(float(t[1]), float(t[2])) == pytest.approx(float(t[-1]), abs=0.005)
+        if t[0] == "time_saved":
+            assert rp.time_saved(float(t[1])) == pytest.approx(float(t[-1]), abs=0.005)
+        if t[0] == "workflow":
+            assert rp.workflow_speedup(float(t[2]), float(t[4])) == pytest.approx(float(t[-1]))
+
+
+def test_draft_kv_formula_and_history_control_sizes():
+    # 2 * L_D * H * n_kv * d_h * b with the 8B-shaped drafter, bf16
+    assert O.draft_kv_bytes(3, 8192, 8, 128, 2) == 100663296
+    assert O.draft_kv_bytes(3, 118000, 8, 128, 2) == 1449984000
+
+
+def test_mirror_differs_from_pure_by_bf16_scale():
+    cfg = _tiny()
+    W = _weights(cfg)
+    hidden, anchor, _ = wk.make_round_inputs(wk.WORKLOADS["tiny"], B=1)
+    b0 = O.backbone(hidden[0], anchor[0], W, cfg, mirror=False)
+    b1 = O.backbone(hidden[0], anchor[0], W, cfg, mirror=True)
+    rel = np.linalg.norm(b1 - b0) / np.linalg.norm(b0)
+    assert 1e-5 < rel < 2e-2
