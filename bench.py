@@ -1,0 +1,416 @@
+"""Benchmark of the DLite draft-and-verify round on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--workload NAME]
+
+One step = one whole round (draft: staging, backbone, sequential head, LM head
+with fused sampling; verify: speculative sampling with residual resampling;
+RNG-position bookkeeping) over one batch of synthetic requests, replayed from
+a captured CUDA graph. Inputs are resident in HBM when the timed region
+starts; each round streams all 2.4 GB of weights (> L2), and the per-round
+inputs cycle through a ring of 4 batches.
+
+--impl reference times the CPU oracle (float64, numpy) on the host cores on a
+bounded sample of the same workload. Under torchrun only rank 0 runs it.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from history_free_speculative_gb300 import reporter as rp  # noqa: E402
+from history_free_speculative_gb300 import workload as wk  # noqa: E402
+
+METRIC = "draft+verify rounds/s & committed tok/s, Qwen3-8B-shape drafter B=32; %roofline"
+RING = 4
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained", d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    from history_free_speculative_gb300 import binding
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device(dev))
+    wl = wk.WORKLOADS[args.workload]
+    cfg = wl.cfg
+    B = wl.B
+    T = wl.temperature
+    sampling = T > 0
+
+    W = wk.make_weights(cfg, wl.weight_seed, device=dev)
+    dr = binding.Drafter(cfg, W, B_max=B)
+    # ring of per-round inputs (each rank its own shard of requests: weak scaling)
+    ring = []
+    for k in range(RING):
+        hidden, anchor, pos = wk.make_round_inputs(wl, round_index=k + 1000 * rank, device=dev)
+        item = {"hidden": hidden}
+        if sampling:
+            item["probs"] = wk.make_target_probs(B, cfg.K, cfg.V, wl.rng_seed + 17 * k + 1000 * rank,
+                                                 device=dev)
+        ring.append(item)
+    _, anchor, pos = wk.make_round_inputs(wl, round_index=999 + 1000 * rank, device=dev)
+    out = dr.new_outputs(B, dev)
+    tgt = torch.randint(0, cfg.V, (B, cfg.K + 1), device=dev, dtype=torch.int32)
+
+    stream = torch.cuda.Stream(device=dev)
+
+    def enqueue(k):
+        it = ring[k]
+        dr.draft_round(it["hidden"], anchor, T, wl.rng_seed, pos, out["cand"], out["qstats"],
+                       stream=stream)
+        if sampling:
+            dr.verify_sample(out["cand"], out["qstats"], None, it["probs"], T, wl.rng_seed, pos,
+                             out["accepted"], out["commits"], out["n_commit"], anchor, stream=stream)
+        else:
+            dr.verify(out["cand"], tgt, out["accepted"], out["commits"], out["n_commit"], anchor,
+                      stream=stream)
+        dr.advance(out["n_commit"], pos, stream=stream)
+
+    # eager warm-up (also sets kernel attributes before capture)
+    with torch.cuda.stream(stream):
+        enqueue(0)
+    stream.synchronize()
+    graphs = []
+    for k in range(RING):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                enqueue(k)
+        graphs.append(g)
+    launches_per_step = dr.launch_count(B, T) + 1   # + the position bookkeeping kernel
+
+    for i in range(args.warmup):
+        graphs[i % RING].replay()
+    stream.synchronize()
+    ncommit_total = torch.zeros((), dtype=torch.int64, device=dev)
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    clocks.start()
+    time.sleep(0.3)
+    ev0.record(stream)
+    for i in range(args.steps):
+        graphs[i % RING].replay()
+        with torch.cuda.stream(stream):
+            ncommit_total += out["n_commit"].sum()
+    ev1.record(stream)
+    stream.synchronize()
+    clk = clocks.stop()
+    barrier()
+    ms = ev0.elapsed_time(ev1)
+    t_s = ms / 1e3
+    committed = int(ncommit_total.item())
+    if ws > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([t_s], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_s = float(tt.item())
+        cc = torch.tensor([committed], device=dev, dtype=torch.int64)
+        dist.all_reduce(cc)
+        committed = int(cc.item())
+    rounds_s = ws * args.steps / t_s
+    tok_s = committed / t_s
+
+    # ---- per-kernel CUDA-event times (eager, same inputs) for the roofline
+    per = {}
+    nprof = 5
+    for r in range(nprof):
+        it = ring[r % RING]
+        times = dr.stage_times(it["hidden"], anchor, T, wl.rng_seed, pos, out,
+                               target_tokens=None if sampling else tgt,
+                               target_probs=it.get("probs"), stream=stream)
+        for name, t in times:
+            per.setdefault(name, []).append(t)
+    per_launch = {n: sum(v) / len(v) for n, v in per.items()}   # ms per round (summed over launches)
+    counts = {}
+    for name, _ in times:
+        counts[name] = counts.get(name, 0) + 1
+    hbm, tf_burst, tf_sus, peak_src = measured_peaks()
+    lm_ms = per_launch.get("lm_head", float("nan")) / counts.get("lm_head", 1)
+    lm_bytes = rp.lm_head_bytes(cfg, B)
+    lm_flops = rp.lm_head_flops(cfg, B)
+    achieved_gbs = lm_bytes / (lm_ms / 1e3) / 1e9
+    achieved_tf = lm_flops / (lm_ms / 1e3) / 1e12
+    t_bytes = lm_bytes / (hbm * 1e9)
+    t_flops = lm_flops / (tf_sus * 1e12)
+    bound = "hbm" if t_bytes >= t_flops else "tensor"
+    if bound == "hbm":
+        roof = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved_gbs / hbm, 4)}
+    else:
+        roof = {"bound": "tensor", "achieved": round(achieved_tf, 1), "peak": tf_sus, "unit": "TFLOP/s",
+                "frac": round(achieved_tf / tf_sus, 4)}
+    roof.update({"kernel": "lm_head", "traffic": None, "peak_source": peak_src,
+                 "algorithmic_bytes_per_launch": lm_bytes, "algorithmic_flops_per_launch": lm_flops,
+                 "ms_per_launch": round(lm_ms, 4)})
+    round_bytes = rp.round_bytes(cfg, B)
+    round_flops = rp.round_flops(cfg, B)
+    floor = rp.roofline_floor_s(round_bytes, round_flops, hbm, tf_sus)
+    ms_step = t_s * 1e3 / args.steps
+
+    # ---- end to end through the public host-buffer call
+    e2e = None
+    if rank == 0 or ws > 1:
+        e2e = run_e2e(dr, wl, ring, anchor, pos, stream, max(3, min(args.steps, 20)))
+
+    result = {
+        "metric": METRIC, "value": round(rounds_s, 2), "unit": "rounds/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype,
+        "data": "synthetic (seeded random weights and inputs of the workload's shapes)",
+        "config": {"workload": wl.name, "B_per_gpu": B, "D": cfg.D, "m": cfg.m, "K": cfg.K,
+                   "L_D": cfg.L_D, "F": cfg.F, "R": cfg.R, "V": cfg.V, "temperature": T,
+                   "parallelism": f"replicas x{ws}", "l2": "inputs larger than L2 (2.4 GB of weights "
+                   "streamed per round, 4-batch input ring)"},
+        "committed_tok_s": round(tok_s, 1),
+        "round_roofline": {"floor_ms": round(floor * 1e3, 4), "frac": round(floor / (ms_step / 1e3), 4),
+                           "bytes": round_bytes, "flops": round_flops, "peak_source": peak_src},
+        "roofline": roof,
+        "per_kernel_ms": {n: round(v, 4) for n, v in per_launch.items()},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if rank == 0:
+        if ws == 1 and not args.no_cpu_baseline:
+            result["cpu_baseline"] = cpu_baseline(wl, W, ring, anchor, pos)
+        print(json.dumps(result), flush=True)
+    dr.close()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(dr, wl, ring, anchor, pos, stream, steps):
+    cfg, B, T = wl.cfg, wl.B, wl.temperature
+    host = []
+    for it in ring:
+        h = {"hidden": it["hidden"].cpu().pin_memory()}
+        if T > 0:
+            h["probs"] = it["probs"].cpu().pin_memory()
+            h["tgt"] = None
+        else:
+            h["probs"] = None
+            h["tgt"] = torch.randint(0, cfg.V, (B, cfg.K + 1), dtype=torch.int32).pin_memory()
+        host.append(h)
+    a_h = anchor.cpu().pin_memory()
+    p_h = pos.cpu().pin_memory()
+    out_h = {k: v.pin_memory() for k, v in dr.new_outputs(B, "cpu").items()}
+    for i in range(2):
+        hh = host[i % RING]
+        dr.round_host(hh["hidden"], a_h, p_h, hh["tgt"], hh["probs"], T, wl.rng_seed, out_h, stream=stream)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        hh = host[i % RING]
+        dr.round_host(hh["hidden"], a_h, p_h, hh["tgt"], hh["probs"], T, wl.rng_seed, out_h, stream=stream)
+        a_h.copy_(out_h["next_anchor"])
+        p_h += out_h["n_commit"].to(torch.int64)
+    dt = time.perf_counter() - t0
+    hb = host[0]
+    h2d = hb["hidden"].numel() * hb["hidden"].element_size() + B * 4 + B * 8
+    h2d += (hb["probs"].numel() * 4) if T > 0 else (B * (cfg.K + 1) * 4)
+    d2h = B * 4 * 3 + B * (cfg.K + 1) * 4
+    return {"value": round(steps / dt, 2), "unit": "rounds/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": steps}
+
+
+# ---------------------------------------------------------------- oracle (CPU) arm
+
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def oracle_request_seconds(wl, W64, hidden, anchor, pos, probs, b):
+    """Oracle time of ONE request's round (draft + verify)."""
+    from oracle import dlite_oracle as O
+    cfg, T = wl.cfg, wl.temperature
+    t0 = time.perf_counter()
+    r = O.draft_request(hidden, int(anchor), W64, cfg, temperature=T, seed=wl.rng_seed,
+                        pos=int(pos), request=b)
+    if T > 0:
+        O.verify_sample(r["cand"], r["logit_d"], r["lse"], r["h"], W64["E"], probs, T, wl.rng_seed,
+                        int(pos), b)
+    else:
+        O.verify_greedy(r["cand"], list(r["cand"]) + [0])
+    return time.perf_counter() - t0
+
+
+def _w64(W):
+    from oracle import dlite_oracle as O
+    out = {k: O.f64(v) for k, v in W.items() if k != "layers"}
+    out["layers"] = [{k: O.f64(v) for k, v in l.items()} for l in W["layers"]]
+    return out
+
+
+def cpu_baseline(wl, W, ring, anchor, pos, n_req=2):
+    W64 = _w64(W)
+    it = ring[0]
+    ts = []
+    for b in range(n_req):
+        probs = it["probs"][b].cpu().numpy() if wl.temperature > 0 else None
+        ts.append(oracle_request_seconds(wl, W64, it["hidden"][b].cpu(), anchor[b].item(),
+                                         pos[b].item(), probs, b))
+    t_req = sum(ts) / len(ts)
+    return {"value": round(1.0 / (t_req * wl.B), 6), "unit": "rounds/s", "cores": _blas_threads(),
+            "kind": "oracle",
+            "sample": f"{n_req} of the {wl.B} requests of one round (float64 numpy oracle, draft + "
+                      f"verify); rounds/s = 1 / (mean seconds per request x {wl.B})"}
+
+
+def run_reference(args):
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return
+    wl = wk.WORKLOADS[args.workload]
+    cfg, B = wl.cfg, wl.B
+    W = wk.make_weights(cfg, wl.weight_seed, device="cpu")
+    W64 = _w64(W)
+    del W
+    hidden, anchor, pos = wk.make_round_inputs(wl, round_index=1000)
+    probs = None
+    if wl.temperature > 0:
+        probs = wk.make_target_probs(B, cfg.K, cfg.V, wl.rng_seed, device="cpu")
+    for i in range(args.warmup):
+        b = i % B
+        oracle_request_seconds(wl, W64, hidden[b], anchor[b], pos[b],
+                               None if probs is None else probs[b].numpy(), b)
+    ts = []
+    for i in range(args.steps):
+        b = i % B
+        ts.append(oracle_request_seconds(wl, W64, hidden[b], anchor[b], pos[b],
+                                         None if probs is None else probs[b].numpy(), b))
+    t_req = sum(ts) / len(ts)
+    value = 1.0 / (t_req * B)
+    sample = (f"each step = one of the {B} requests of a round through the float64 oracle "
+              f"(draft + verify); rounds/s = 1 / (mean seconds per request x {B})")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "rounds/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(t_req * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "B_per_gpu": B, "D": cfg.D, "V": cfg.V,
+                   "temperature": wl.temperature},
+        "cpu_baseline": {"value": round(value, 6), "unit": "rounds/s", "cores": _blas_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "rounds/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="qwen3-8b-b32", choices=sorted(wk.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,718 @@
+// C ABI of the DLite round: handle lifetime, weight preparation, workspace
+// layout and the launch sequences of draft / verify.
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <vector>
+
+#include "kernels.h"
+
+using namespace dlite;
+
+struct LayerW {
+  const bf16* Wqkv[2];  // [qd + 2 kvd, D] = [Wq; Wk; Wv]
+  const bf16* Wo[2];    // [D, qd]
+  const bf16* Wgu[2];   // [2F, D] = [Wg; Wu]
+  const bf16* Wd[2];    // [D, F]
+  float* g_attn;
+  float* g_ffn;
+};
+
+struct dlite_handle {
+  dlite_config cfg;
+  bool f32 = false;
+  int np = 1;  // planes of weights and backbone activations (2 for fp32 weights)
+  int qd = 0, kvd = 0;
+  std::vector<void*> allocs;
+
+  // weights
+  float *e_depth = nullptr, *g_stage = nullptr, *e_ph = nullptr, *g_final = nullptr;
+  const void* E_src = nullptr;  // E in the weight dtype (anchor lookup, q(v) rows)
+  const bf16* E[2] = {nullptr, nullptr};
+  LayerW layer[DLITE_MAX_LAYERS];
+  const bf16* Wce[2] = {nullptr, nullptr};  // [2R, D] = [Q_b; Q_h]
+  const bf16* P[2] = {nullptr, nullptr};    // [D, R]
+  float* Mt = nullptr;                      // [R, R] transposed Q_h P
+  float *rope_cos = nullptr, *rope_sin = nullptr;
+
+  // workspace
+  float* x = nullptr;
+  bf16 *y[2] = {nullptr, nullptr}, *z[2] = {nullptr, nullptr}, *o[2] = {nullptr, nullptr},
+       *a[2] = {nullptr, nullptr};
+  float* b = nullptr;
+  bf16* bp[2] = {nullptr, nullptr};
+  float* t = nullptr;
+  bf16* tp[2] = {nullptr, nullptr};
+  float* hs = nullptr;
+  bf16* hp[2] = {nullptr, nullptr};
+  float *part = nullptr, *part2 = nullptr;
+  LmRec* lmrec = nullptr;
+  double* resid = nullptr;
+  int* status = nullptr;
+
+  // per-kernel event recording (dlite_stage_times)
+  cudaEvent_t prof_ev[128];
+  const char* prof_name[128];
+  int prof_n = -1;  // -1: not recording
+  bool prof_events_made = false;
+  cudaStream_t prof_stream = nullptr;
+
+  // staging for dlite_round_host
+  void* d_hidden = nullptr;
+  int32_t *d_anchor = nullptr, *d_tgt = nullptr, *d_cand = nullptr, *d_acc = nullptr,
+          *d_commits = nullptr, *d_ncommit = nullptr, *d_next = nullptr;
+  int64_t* d_pos = nullptr;
+  float* d_probs = nullptr;
+  dlite_qstats* d_qs = nullptr;
+};
+
+namespace {
+
+#define CK(call)                                   \
+  do {                                             \
+    cudaError_t e_ = (call);                       \
+    if (e_ != cudaSuccess) return DLITE_ERR_CUDA;  \
+  } while (0)
+
+// Record an event after a launch when the handle is in profiling mode.
+void mark(dlite_handle* h, const char* name) {
+  if (h->prof_n < 0 || h->prof_n >= 127) return;
+  h->prof_name[h->prof_n] = name;
+  cudaEventRecord(h->prof_ev[++h->prof_n], h->prof_stream);
+}
+
+template <typename T>
+int alloc(dlite_handle* h, T** p, size_t n) {
+  void* q = nullptr;
+  if (n == 0) n = 1;
+  if (cudaMalloc(&q, n * sizeof(T)) != cudaSuccess) return DLITE_ERR_OOM;
+  h->allocs.push_back(q);
+  *p = (T*)q;
+  return DLITE_OK;
+}
+
+#define AL(ptr, n)                          \
+  do {                                      \
+    int r_ = alloc(h, &(ptr), (size_t)(n)); \
+    if (r_) return r_;                      \
+  } while (0)
+
+int check_config(const dlite_config* c) {
+  if (!c) return DLITE_ERR_INVALID_ARG;
+  if (c->dtype != DLITE_F32 && c->dtype != DLITE_BF16) return DLITE_ERR_INVALID_ARG;
+  if (c->B_max < 1 || c->K < 1 || c->K > 31 || c->m < 1 || c->m + c->K + 1 > 32)
+    return DLITE_ERR_UNSUPPORTED_SHAPE;
+  if (c->L_D < 1 || c->L_D > DLITE_MAX_LAYERS) return DLITE_ERR_UNSUPPORTED_SHAPE;
+  if (c->n_q < 1 || c->n_kv < 1 || c->n_q % c->n_kv) return DLITE_ERR_UNSUPPORTED_SHAPE;
+  if (c->d_h != 64 && c->d_h != 128) return DLITE_ERR_UNSUPPORTED_SHAPE;
+  if (c->D % 64 || c->F % 64 || c->R % 32 || c->R > 1024 || c->V < 8 || c->V % 8)
+    return DLITE_ERR_UNSUPPORTED_SHAPE;
+  if ((c->n_q * c->d_h) % 64) return DLITE_ERR_UNSUPPORTED_SHAPE;
+  const int G = c->n_q / c->n_kv, Tk = c->m + c->K + 1;
+  if ((size_t)(G * (c->K + 1) + 2 * Tk) * (c->d_h + 1) * 4 > 96 * 1024) return DLITE_ERR_UNSUPPORTED_SHAPE;
+  if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return DLITE_ERR_INVALID_ARG;
+  return DLITE_OK;
+}
+
+// Copy a [rows, cols] slice of a weight (row stride src_ld, column offset off)
+// into bf16 planes and / or fp32.
+int repack(dlite_handle* h, const void* src, int rows, int cols, int src_ld, int off,
+           const bf16** planes_out, float** f32_out) {
+  bf16* p0 = nullptr;
+  bf16* p1 = nullptr;
+  const size_t n = (size_t)rows * cols;
+  if (planes_out) {
+    AL(p0, n);
+    if (h->np == 2) AL(p1, n);
+    planes_out[0] = p0;
+    planes_out[1] = p1;
+  }
+  float* f = nullptr;
+  if (f32_out) {
+    AL(f, n);
+    *f32_out = f;
+  }
+  CK(launch_repack(src, h->f32, rows, cols, src_ld, off, p0, p1, planes_out ? h->np : 0, f, 0));
+  return DLITE_OK;
+}
+
+// Stack several [rows_i, cols] weights into one planes buffer.
+int stack(dlite_handle* h, const void* const* srcs, const int* rows, int n, int cols,
+          const bf16** planes_out) {
+  int total = 0;
+  for (int i = 0; i < n; ++i) total += rows[i];
+  bf16* p0 = nullptr;
+  bf16* p1 = nullptr;
+  AL(p0, (size_t)total * cols);
+  if (h->np == 2) AL(p1, (size_t)total * cols);
+  size_t off = 0;
+  for (int i = 0; i < n; ++i) {
+    CK(launch_repack(srcs[i], h->f32, rows[i], cols, cols, 0, p0 + off, p1 ? p1 + off : nullptr,
+                     h->np, nullptr, 0));
+    off += (size_t)rows[i] * cols;
+  }
+  planes_out[0] = p0;
+  planes_out[1] = p1;
+  return DLITE_OK;
+}
+
+Planes planes(const bf16* const* p, int n, int ld) {
+  Planes r;
+  r.p[0] = p[0];
+  r.p[1] = n == 2 ? p[1] : nullptr;
+  r.n = n;
+  r.ld = ld;
+  return r;
+}
+
+int gemm(dlite_handle* h, const char* name, const Planes& X, const Planes& W, int rows, int outs,
+         int K, float* part, int* S_out, cudaStream_t s) {
+  GemmArgs g;
+  g.X = X;
+  g.W = W;
+  g.rows = rows;
+  g.outs = outs;
+  g.K = K;
+  g.splits = gemm_splits(rows, outs, K);
+  g.part = part;
+  if (S_out) *S_out = g.splits;
+  CK(launch_gemm(g, s));
+  mark(h, name);
+  return DLITE_OK;
+}
+
+#define RUN(call)          \
+  do {                     \
+    int r_ = (call);       \
+    if (r_) return r_;     \
+  } while (0)
+
+void seed_key(uint64_t seed, uint32_t* k0, uint32_t* k1) {
+  *k0 = (uint32_t)(seed & 0xffffffffu);
+  *k1 = (uint32_t)(seed >> 32);
+}
+
+// ---------------------------------------------------------------- stages
+
+int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anchor,
+                 const dlite_taps* taps, cudaStream_t s) {
+  const dlite_config& c = h->cfg;
+  const int L = B * (c.K + 1), C = B * c.m;
+  StageArgs st;
+  st.hidden = hidden;
+  st.anchor = anchor;
+  st.E = h->E_src;
+  st.e_depth = h->e_depth;
+  st.g_stage = h->g_stage;
+  st.e_ph = h->e_ph;
+  st.g_attn0 = h->layer[0].g_attn;
+  st.B = B;
+  st.m = c.m;
+  st.K = c.K;
+  st.D = c.D;
+  st.V = c.V;
+  st.eps = c.rms_eps;
+  st.z[0] = h->z[0];
+  st.z[1] = h->z[1];
+  st.nz = h->np;
+  st.x = h->x;
+  st.y[0] = h->y[0];
+  st.y[1] = h->y[1];
+  st.ny = h->np;
+  st.tap_z = taps ? taps->z : nullptr;
+  st.status = h->status;
+  CK(launch_stage(st, h->f32, s));
+  mark(h, "stage");
+
+  for (int l = 0; l < c.L_D; ++l) {
+    const LayerW& w = h->layer[l];
+    int S1 = 1, S2 = 1;
+    // local rows: y -> [q | k | v]; context rows: z -> [k | v] with the same bytes
+    RUN(gemm(h, "gemm_qkv", planes(h->y, h->np, c.D), planes(w.Wqkv, h->np, c.D), L, h->qd + 2 * h->kvd, c.D,
+             h->part, &S1, s));
+    const bf16* wkv[2] = {w.Wqkv[0] + (size_t)h->qd * c.D,
+                          w.Wqkv[1] ? w.Wqkv[1] + (size_t)h->qd * c.D : nullptr};
+    RUN(gemm(h, "gemm_ctx_kv", planes(h->z, h->np, c.D), planes(wkv, h->np, c.D), C, 2 * h->kvd, c.D, h->part2, &S2,
+             s));
+    AttnArgs at;
+    at.part_loc = h->part;
+    at.S_loc = S1;
+    at.part_ctx = h->part2;
+    at.S_ctx = S2;
+    at.rope_cos = h->rope_cos;
+    at.rope_sin = h->rope_sin;
+    at.B = B;
+    at.m = c.m;
+    at.K = c.K;
+    at.n_q = c.n_q;
+    at.n_kv = c.n_kv;
+    at.d_h = c.d_h;
+    at.scale = (float)(1.0 / sqrt((double)c.d_h));
+    at.round_bf16 = h->f32 ? 0 : 1;
+    at.o[0] = h->o[0];
+    at.o[1] = h->o[1];
+    at.no = h->np;
+    CK(launch_attention(at, s));
+    mark(h, "attention");
+    // O projection + residual, then the FFN pre-norm
+    RUN(gemm(h, "gemm_o", planes(h->o, h->np, h->qd), planes(w.Wo, h->np, h->qd), L, c.D, h->qd, h->part, &S1, s));
+    ResNormArgs rn;
+    rn.part = h->part;
+    rn.S = S1;
+    rn.rows = L;
+    rn.D = c.D;
+    rn.x = h->x;
+    rn.g = w.g_ffn;
+    rn.eps = c.rms_eps;
+    rn.y[0] = h->y[0];
+    rn.y[1] = h->y[1];
+    rn.ny = h->np;
+    CK(launch_resnorm(rn, s));
+    mark(h, "resnorm");
+    // gate/up + SwiGLU
+    RUN(gemm(h, "gemm_gate_up", planes(h->y, h->np, c.D), planes(w.Wgu, h->np, c.D), L, 2 * c.F, c.D, h->part, &S1, s));
+    CK(launch_swiglu(h->part, S1, L, c.F, h->a, h->np, s));
+    mark(h, "swiglu");
+    // down + residual, then the next layer's pre-norm (or the final norm)
+    RUN(gemm(h, "gemm_down", planes(h->a, h->np, c.F), planes(w.Wd, h->np, c.F), L, c.D, c.F, h->part, &S1, s));
+    ResNormArgs r2 = rn;
+    r2.S = S1;
+    r2.tap_x = (taps && taps->x) ? taps->x + (size_t)l * L * c.D : nullptr;
+    if (l + 1 < c.L_D) {
+      r2.g = h->layer[l + 1].g_attn;
+    } else {
+      r2.g = h->g_final;
+      r2.final_mode = 1;
+      r2.K1 = c.K + 1;
+      r2.bout = h->b;
+      r2.bp[0] = h->bp[0];
+      r2.bp[1] = h->bp[1];
+      r2.tap_b = taps ? taps->b : nullptr;
+    }
+    CK(launch_resnorm(r2, s));
+    mark(h, "resnorm");
+  }
+  return DLITE_OK;
+}
+
+// b (h->b, h->bp) -> hs (h->hs, h->hp)
+int run_seq_head(dlite_handle* h, int B, float* tap_hs, cudaStream_t s) {
+  const dlite_config& c = h->cfg;
+  const int rows = B * c.K;
+  int S = 1;
+  RUN(gemm(h, "gemm_head_ce", planes(h->bp, 2, c.D), planes(h->Wce, h->np, c.D), rows, 2 * c.R, c.D, h->part, &S, s));
+  ChainArgs ch;
+  ch.part = h->part;
+  ch.S = S;
+  ch.rows = rows;
+  ch.Mt = h->Mt;
+  ch.B = B;
+  ch.K = c.K;
+  ch.R = c.R;
+  ch.t = h->t;
+  ch.tp[0] = h->tp[0];
+  ch.tp[1] = h->tp[1];
+  CK(launch_head_chain(ch, s));
+  mark(h, "head_chain");
+  RUN(gemm(h, "gemm_head_p", planes(h->tp, 2, c.R), planes(h->P, h->np, c.R), rows, c.D, c.R, h->part, &S, s));
+  CK(launch_head_out(h->part, S, rows, c.D, h->b, h->hs, h->hp, tap_hs, s));
+  mark(h, "head_out");
+  return DLITE_OK;
+}
+
+int run_lm_head(dlite_handle* h, int B, float temperature, uint64_t seed, const int64_t* pos,
+                int32_t* cand, dlite_qstats* qs, cudaStream_t s) {
+  const dlite_config& c = h->cfg;
+  LmArgs la;
+  la.H = planes(h->hp, 2, c.D);
+  la.E = planes(h->E, h->np, c.D);
+  la.rows = B * c.K;
+  la.V = c.V;
+  la.D = c.D;
+  la.K = c.K;
+  la.inv_T = temperature > 0.f ? 1.f / temperature : 0.f;
+  seed_key(seed, &la.k0, &la.k1);
+  la.pos = pos;
+  la.rec = h->lmrec;
+  la.status = h->status;
+  CK(launch_lm_head(la, s));
+  mark(h, "lm_head");
+  CK(launch_lm_merge(h->lmrec, lm_tiles(c.V), la.rows, c.K, la.inv_T, cand, qs, s));
+  mark(h, "lm_merge");
+  return DLITE_OK;
+}
+
+int check_round_args(dlite_handle* h, int B, const void* hidden, const int32_t* anchor,
+                     float temperature, const int64_t* pos, int32_t* cand, dlite_qstats* qs) {
+  if (!h || !hidden || !anchor || !cand) return DLITE_ERR_INVALID_ARG;
+  if (B < 1 || B > h->cfg.B_max) return DLITE_ERR_INVALID_ARG;
+  if (!(temperature >= 0.f) || isinf(temperature)) return DLITE_ERR_INVALID_ARG;
+  if (temperature > 0.f && (!pos || !qs)) return DLITE_ERR_INVALID_ARG;
+  return DLITE_OK;
+}
+
+}  // namespace
+
+// ================================================================ C ABI
+
+extern "C" {
+
+const char* dlite_status_string(int st) {
+  switch (st) {
+    case DLITE_OK: return "ok";
+    case DLITE_ERR_INVALID_ARG: return "invalid argument";
+    case DLITE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case DLITE_ERR_CUDA: return "CUDA runtime error";
+    case DLITE_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case DLITE_ERR_BOUNDS: return "id out of range on the device";
+    case DLITE_ERR_OOM: return "device allocation failed";
+    default: return "unknown status";
+  }
+}
+
+void dlite_destroy(dlite_handle* h) {
+  if (!h) return;
+  cudaDeviceSynchronize();
+  if (h->prof_events_made)
+    for (int i = 0; i < 128; ++i) cudaEventDestroy(h->prof_ev[i]);
+  for (void* p : h->allocs) cudaFree(p);
+  delete h;
+}
+
+static int create_impl(dlite_handle* h, const dlite_weights* w) {
+  const dlite_config& c = h->cfg;
+  const int D = c.D, F = c.F, R = c.R, V = c.V;
+  // ---- weights
+  RUN(repack(h, w->e_depth, c.m, D, D, 0, nullptr, &h->e_depth));
+  RUN(repack(h, w->g_stage, 1, D, D, 0, nullptr, &h->g_stage));
+  RUN(repack(h, w->e_ph, 1, D, D, 0, nullptr, &h->e_ph));
+  RUN(repack(h, w->g_final, 1, D, D, 0, nullptr, &h->g_final));
+  if (h->f32) {
+    float* e32 = nullptr;
+    RUN(repack(h, w->E, V, D, D, 0, h->E, &e32));
+    h->E_src = e32;
+  } else {
+    RUN(repack(h, w->E, V, D, D, 0, h->E, nullptr));
+    h->E_src = h->E[0];
+  }
+  for (int l = 0; l < c.L_D; ++l) {
+    const dlite_layer_weights& lw = w->layer[l];
+    LayerW& L = h->layer[l];
+    if (!lw.g_attn || !lw.Wq || !lw.Wk || !lw.Wv || !lw.Wo || !lw.g_ffn || !lw.Wg || !lw.Wu || !lw.Wd)
+      return DLITE_ERR_INVALID_ARG;
+    const void* qkv[3] = {lw.Wq, lw.Wk, lw.Wv};
+    const int qkv_rows[3] = {h->qd, h->kvd, h->kvd};
+    RUN(stack(h, qkv, qkv_rows, 3, D, L.Wqkv));
+    RUN(repack(h, lw.Wo, D, h->qd, h->qd, 0, L.Wo, nullptr));
+    const void* gu[2] = {lw.Wg, lw.Wu};
+    const int gu_rows[2] = {F, F};
+    RUN(stack(h, gu, gu_rows, 2, D, L.Wgu));
+    RUN(repack(h, lw.Wd, D, F, F, 0, L.Wd, nullptr));
+    RUN(repack(h, lw.g_attn, 1, D, D, 0, nullptr, &L.g_attn));
+    RUN(repack(h, lw.g_ffn, 1, D, D, 0, nullptr, &L.g_ffn));
+  }
+  {  // Wce = [Q[:, :D]; Q[:, D:]]
+    bf16* p0 = nullptr;
+    bf16* p1 = nullptr;
+    AL(p0, (size_t)2 * R * D);
+    if (h->np == 2) AL(p1, (size_t)2 * R * D);
+    CK(launch_repack(w->Q, h->f32, R, D, 2 * D, 0, p0, p1, h->np, nullptr, 0));
+    CK(launch_repack(w->Q, h->f32, R, D, 2 * D, D, p0 + (size_t)R * D,
+                     p1 ? p1 + (size_t)R * D : nullptr, h->np, nullptr, 0));
+    h->Wce[0] = p0;
+    h->Wce[1] = p1;
+  }
+  RUN(repack(h, w->P, D, R, R, 0, h->P, nullptr));
+  AL(h->Mt, (size_t)R * R);
+  CK(launch_head_matrix(w->Q, w->P, h->f32, D, R, h->Mt, 0));
+  {  // RoPE table for local positions 0..K (float64 on the host)
+    const int half = c.d_h / 2;
+    std::vector<float> cs((size_t)(c.K + 1) * half), sn((size_t)(c.K + 1) * half);
+    for (int p = 0; p <= c.K; ++p)
+      for (int j = 0; j < half; ++j) {
+        const double ang = p * pow((double)c.rope_theta, -2.0 * j / c.d_h);
+        cs[(size_t)p * half + j] = (float)cos(ang);
+        sn[(size_t)p * half + j] = (float)sin(ang);
+      }
+    AL(h->rope_cos, cs.size());
+    AL(h->rope_sin, sn.size());
+    CK(cudaMemcpy(h->rope_cos, cs.data(), cs.size() * 4, cudaMemcpyHostToDevice));
+    CK(cudaMemcpy(h->rope_sin, sn.data(), sn.size() * 4, cudaMemcpyHostToDevice));
+  }
+  // ---- workspace (sized for B_max)
+  const int Bm = c.B_max;
+  const size_t Lr = (size_t)Bm * (c.K + 1), Cr = (size_t)Bm * c.m, Hr = (size_t)Bm * c.K;
+  AL(h->x, Lr * D);
+  for (int p = 0; p < h->np; ++p) {
+    AL(h->y[p], Lr * D);
+    AL(h->z[p], Cr * D);
+    AL(h->o[p], Lr * h->qd);
+    AL(h->a[p], Lr * F);
+  }
+  AL(h->b, Hr * D);
+  AL(h->t, Hr * R);
+  AL(h->hs, Hr * D);
+  for (int p = 0; p < 2; ++p) {
+    AL(h->bp[p], Hr * D);
+    AL(h->tp[p], Hr * R);
+    AL(h->hp[p], Hr * D);
+  }
+  size_t pe = 0, pe2 = 0;
+  for (int B = 1; B <= Bm; ++B) {
+    const int L = B * (c.K + 1), C = B * c.m, H = B * c.K;
+    const size_t cand[6] = {gemm_part_elems(L, h->qd + 2 * h->kvd, D), gemm_part_elems(L, D, h->qd),
+                            gemm_part_elems(L, 2 * F, D),           gemm_part_elems(L, D, F),
+                            gemm_part_elems(H, 2 * R, D),           gemm_part_elems(H, D, R)};
+    for (size_t v : cand) pe = v > pe ? v : pe;
+    const size_t v2 = gemm_part_elems(C, 2 * h->kvd, D);
+    pe2 = v2 > pe2 ? v2 : pe2;
+  }
+  AL(h->part, pe);
+  AL(h->part2, pe2);
+  AL(h->lmrec, (size_t)lm_tiles(V) * Hr);
+  AL(h->resid, (size_t)Bm * V);
+  AL(h->status, 1);
+  CK(cudaMemset(h->status, 0, sizeof(int)));
+  for (int i = 0; i < 128; ++i) CK(cudaEventCreate(&h->prof_ev[i]));
+  h->prof_events_made = true;
+  // ---- staging for dlite_round_host
+  {
+    void* q = nullptr;
+    if (cudaMalloc(&q, (size_t)Bm * c.m * D * (h->f32 ? 4 : 2)) != cudaSuccess) return DLITE_ERR_OOM;
+    h->allocs.push_back(q);
+    h->d_hidden = q;
+  }
+  AL(h->d_anchor, Bm);
+  AL(h->d_pos, Bm);
+  AL(h->d_tgt, (size_t)Bm * (c.K + 1));
+  AL(h->d_probs, (size_t)Bm * (c.K + 1) * V);
+  AL(h->d_cand, Hr);
+  AL(h->d_qs, Hr);
+  AL(h->d_acc, Bm);
+  AL(h->d_commits, (size_t)Bm * (c.K + 1));
+  AL(h->d_ncommit, Bm);
+  AL(h->d_next, Bm);
+  CK(cudaDeviceSynchronize());
+  return DLITE_OK;
+}
+
+int dlite_create(const dlite_config* cfg, const dlite_weights* w, dlite_handle** out) {
+  if (!out || !w) return DLITE_ERR_INVALID_ARG;
+  *out = nullptr;
+  const int rc = check_config(cfg);
+  if (rc) return rc;
+  if (!w->e_depth || !w->g_stage || !w->e_ph || !w->E || !w->g_final || !w->Q || !w->P)
+    return DLITE_ERR_INVALID_ARG;
+  dlite_handle* h = new dlite_handle();
+  h->cfg = *cfg;
+  h->f32 = cfg->dtype == DLITE_F32;
+  h->np = h->f32 ? 2 : 1;
+  h->qd = cfg->n_q * cfg->d_h;
+  h->kvd = cfg->n_kv * cfg->d_h;
+  const int r = create_impl(h, w);
+  if (r) {
+    dlite_destroy(h);
+    return r;
+  }
+  *out = h;
+  return DLITE_OK;
+}
+
+int dlite_draft_round_taps(dlite_handle* h, int B, const void* hidden, const int32_t* anchor,
+                           float temperature, uint64_t seed, const int64_t* pos, int32_t* cand,
+                           dlite_qstats* qs, const dlite_taps* taps, dlite_stream_t stream) {
+  RUN(check_round_args(h, B, hidden, anchor, temperature, pos, cand, qs));
+  cudaStream_t s = (cudaStream_t)stream;
+  RUN(run_backbone(h, B, hidden, anchor, taps, s));
+  RUN(run_seq_head(h, B, taps ? taps->hs : nullptr, s));
+  RUN(run_lm_head(h, B, temperature, seed, pos, cand, qs, s));
+  return DLITE_OK;
+}
+
+int dlite_draft_round(dlite_handle* h, int B, const void* hidden, const int32_t* anchor,
+                      float temperature, uint64_t seed, const int64_t* pos, int32_t* cand,
+                      dlite_qstats* qs, dlite_stream_t stream) {
+  return dlite_draft_round_taps(h, B, hidden, anchor, temperature, seed, pos, cand, qs, nullptr,
+                                stream);
+}
+
+int dlite_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anchor, float* b,
+                   dlite_stream_t stream) {
+  if (!h || !hidden || !anchor || !b || B < 1 || B > h->cfg.B_max) return DLITE_ERR_INVALID_ARG;
+  dlite_taps taps = {nullptr, nullptr, b, nullptr};
+  return run_backbone(h, B, hidden, anchor, &taps, (cudaStream_t)stream);
+}
+
+int dlite_seq_head(dlite_handle* h, int B, const float* b, float* hs, dlite_stream_t stream) {
+  if (!h || !b || !hs || B < 1 || B > h->cfg.B_max) return DLITE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t n = (size_t)B * h->cfg.K * h->cfg.D;
+  CK(launch_split(b, n, h->bp, h->b, s));
+  return run_seq_head(h, B, hs, s);
+}
+
+int dlite_lm_head(dlite_handle* h, int B, const float* hs, float temperature, uint64_t seed,
+                  const int64_t* pos, int32_t* cand, dlite_qstats* qs, dlite_stream_t stream) {
+  if (!h || !hs || !cand || B < 1 || B > h->cfg.B_max) return DLITE_ERR_INVALID_ARG;
+  if (!(temperature >= 0.f) || isinf(temperature)) return DLITE_ERR_INVALID_ARG;
+  if (temperature > 0.f && (!pos || !qs)) return DLITE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t n = (size_t)B * h->cfg.K * h->cfg.D;
+  CK(launch_split(hs, n, h->hp, h->hs, s));
+  return run_lm_head(h, B, temperature, seed, pos, cand, qs, s);
+}
+
+int dlite_verify(dlite_handle* h, int B, const int32_t* cand, const int32_t* tgt, int32_t* accepted,
+                 int32_t* commits, int32_t* n_commit, int32_t* next_anchor, dlite_stream_t stream) {
+  if (!h || !cand || !tgt || !accepted || !commits || !n_commit || !next_anchor)
+    return DLITE_ERR_INVALID_ARG;
+  if (B < 1 || B > h->cfg.B_max) return DLITE_ERR_INVALID_ARG;
+  VerifyArgs v;
+  v.B = B;
+  v.K = h->cfg.K;
+  v.V = h->cfg.V;
+  v.cand = cand;
+  v.tgt = tgt;
+  v.accepted = accepted;
+  v.commits = commits;
+  v.n_commit = n_commit;
+  v.next_anchor = next_anchor;
+  v.status = h->status;
+  CK(launch_verify_greedy(v, (cudaStream_t)stream));
+  mark(h, "verify_greedy");
+  return DLITE_OK;
+}
+
+int dlite_verify_sample(dlite_handle* h, int B, const int32_t* cand, const dlite_qstats* qs,
+                        const float* hs, const float* probs, float temperature, uint64_t seed,
+                        const int64_t* pos, int32_t* accepted, int32_t* commits, int32_t* n_commit,
+                        int32_t* next_anchor, dlite_stream_t stream) {
+  if (!h || !cand || !qs || !probs || !pos || !accepted || !commits || !n_commit || !next_anchor)
+    return DLITE_ERR_INVALID_ARG;
+  if (B < 1 || B > h->cfg.B_max) return DLITE_ERR_INVALID_ARG;
+  if (!(temperature > 0.f) || isinf(temperature)) return DLITE_ERR_INVALID_ARG;
+  VerifyArgs v;
+  v.B = B;
+  v.K = h->cfg.K;
+  v.V = h->cfg.V;
+  v.D = h->cfg.D;
+  v.cand = cand;
+  v.qs = qs;
+  v.hs = hs ? hs : h->hs;
+  v.probs = probs;
+  if (h->f32)
+    v.Ef = (const float*)h->E_src;
+  else
+    v.Eb = h->E[0];
+  v.resid = h->resid;
+  v.T = (double)temperature;
+  seed_key(seed, &v.k0, &v.k1);
+  v.pos = pos;
+  v.accepted = accepted;
+  v.commits = commits;
+  v.n_commit = n_commit;
+  v.next_anchor = next_anchor;
+  v.status = h->status;
+  CK(launch_verify_sample(v, (cudaStream_t)stream));
+  mark(h, "verify_sample");
+  return DLITE_OK;
+}
+
+int dlite_advance(dlite_handle* h, int B, const int32_t* n_commit, int64_t* pos,
+                  dlite_stream_t stream) {
+  if (!h || !n_commit || !pos || B < 1 || B > h->cfg.B_max) return DLITE_ERR_INVALID_ARG;
+  CK(launch_advance(B, n_commit, pos, (cudaStream_t)stream));
+  return DLITE_OK;
+}
+
+int dlite_round_host(dlite_handle* h, int B, const void* hidden_host, const int32_t* anchor_host,
+                     const int64_t* pos_host, const int32_t* tgt_host, const float* probs_host,
+                     float temperature, uint64_t seed, int32_t* accepted_host, int32_t* commits_host,
+                     int32_t* n_commit_host, int32_t* next_anchor_host, dlite_stream_t stream) {
+  if (!h || !hidden_host || !anchor_host || !accepted_host || !commits_host || !n_commit_host ||
+      !next_anchor_host)
+    return DLITE_ERR_INVALID_ARG;
+  if (B < 1 || B > h->cfg.B_max) return DLITE_ERR_INVALID_ARG;
+  const bool sampling = temperature > 0.f;
+  if (sampling ? (!probs_host || !pos_host) : !tgt_host) return DLITE_ERR_INVALID_ARG;
+  const dlite_config& c = h->cfg;
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t hb = (size_t)B * c.m * c.D * (h->f32 ? 4 : 2);
+  CK(cudaMemcpyAsync(h->d_hidden, hidden_host, hb, cudaMemcpyHostToDevice, s));
+  CK(cudaMemcpyAsync(h->d_anchor, anchor_host, (size_t)B * 4, cudaMemcpyHostToDevice, s));
+  if (pos_host) CK(cudaMemcpyAsync(h->d_pos, pos_host, (size_t)B * 8, cudaMemcpyHostToDevice, s));
+  if (sampling)
+    CK(cudaMemcpyAsync(h->d_probs, probs_host, (size_t)B * (c.K + 1) * c.V * 4,
+                       cudaMemcpyHostToDevice, s));
+  else
+    CK(cudaMemcpyAsync(h->d_tgt, tgt_host, (size_t)B * (c.K + 1) * 4, cudaMemcpyHostToDevice, s));
+  RUN(dlite_draft_round(h, B, h->d_hidden, h->d_anchor, temperature, seed,
+                        pos_host ? h->d_pos : nullptr, h->d_cand, h->d_qs, stream));
+  if (sampling)
+    RUN(dlite_verify_sample(h, B, h->d_cand, h->d_qs, nullptr, h->d_probs, temperature, seed,
+                            h->d_pos, h->d_acc, h->d_commits, h->d_ncommit, h->d_next, stream));
+  else
+    RUN(dlite_verify(h, B, h->d_cand, h->d_tgt, h->d_acc, h->d_commits, h->d_ncommit, h->d_next,
+                     stream));
+  CK(cudaMemcpyAsync(accepted_host, h->d_acc, (size_t)B * 4, cudaMemcpyDeviceToHost, s));
+  CK(cudaMemcpyAsync(commits_host, h->d_commits, (size_t)B * (c.K + 1) * 4, cudaMemcpyDeviceToHost, s));
+  CK(cudaMemcpyAsync(n_commit_host, h->d_ncommit, (size_t)B * 4, cudaMemcpyDeviceToHost, s));
+  CK(cudaMemcpyAsync(next_anchor_host, h->d_next, (size_t)B * 4, cudaMemcpyDeviceToHost, s));
+  CK(cudaStreamSynchronize(s));
+  return DLITE_OK;
+}
+
+int dlite_device_status(dlite_handle* h, int clear, int* status_out, dlite_stream_t stream) {
+  if (!h || !status_out) return DLITE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  int v = 0;
+  CK(cudaMemcpyAsync(&v, h->status, sizeof(int), cudaMemcpyDeviceToHost, s));
+  if (clear) CK(cudaMemsetAsync(h->status, 0, sizeof(int), s));
+  CK(cudaStreamSynchronize(s));
+  *status_out = v;
+  if (v & DLITE_DEV_TIMEOUT) return DLITE_ERR_DEVICE_TIMEOUT;
+  if (v & DLITE_DEV_BOUNDS) return DLITE_ERR_BOUNDS;
+  return DLITE_OK;
+}
+
+int dlite_stage_times(dlite_handle* h, int B, const void* hidden, const int32_t* anchor,
+                      float temperature, uint64_t seed, const int64_t* pos,
+                      const int32_t* target_tokens, const float* target_probs, int32_t* cand,
+                      dlite_qstats* qs, int32_t* accepted, int32_t* commits, int32_t* n_commit,
+                      int32_t* next_anchor, float* times_ms, const char** names, int cap,
+                      dlite_stream_t stream) {
+  RUN(check_round_args(h, B, hidden, anchor, temperature, pos, cand, qs));
+  if (!times_ms || cap < 1) return DLITE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  h->prof_stream = s;
+  h->prof_n = 0;
+  CK(cudaEventRecord(h->prof_ev[0], s));
+  int rc = dlite_draft_round(h, B, hidden, anchor, temperature, seed, pos, cand, qs, stream);
+  if (!rc && temperature > 0.f && target_probs)
+    rc = dlite_verify_sample(h, B, cand, qs, nullptr, target_probs, temperature, seed, pos,
+                             accepted, commits, n_commit, next_anchor, stream);
+  else if (!rc && temperature == 0.f && target_tokens)
+    rc = dlite_verify(h, B, cand, target_tokens, accepted, commits, n_commit, next_anchor, stream);
+  const int n = h->prof_n;
+  h->prof_n = -1;
+  if (rc) return rc;
+  CK(cudaStreamSynchronize(s));
+  for (int i = 0; i < n && i < cap; ++i) {
+    float ms = 0.f;
+    CK(cudaEventElapsedTime(&ms, h->prof_ev[i], h->prof_ev[i + 1]));
+    times_ms[i] = ms;
+    if (names) names[i] = h->prof_name[i];
+  }
+  return n;
+}
+
+int dlite_launch_count(dlite_handle* h, int B, float temperature) {
+  if (!h || B < 1) return -1;
+  (void)temperature;
+  // stage + per layer {qkv, ctx-kv, attention, o, resnorm, gate/up, swiglu, down, resnorm}
+  // + head {ce, chain, P, out} + lm {head, merge} + verify
+  return 1 + 9 * h->cfg.L_D + 4 + 2 + 1;
+}
+
+}  // extern "C"

@@ -1,0 +1,103 @@
+// Argument blocks and launchers of the non-GEMM kernels.
+#pragma once
+
+#include "internal.h"
+
+namespace dlite {
+
+struct StageArgs {
+  const void* hidden = nullptr;  // [B, m, D] (f32 or bf16)
+  const int32_t* anchor = nullptr;
+  const void* E = nullptr;       // [V, D] in the weight dtype (anchor row lookup)
+  const float* e_depth = nullptr;
+  const float* g_stage = nullptr;
+  const float* e_ph = nullptr;
+  const float* g_attn0 = nullptr;
+  int B = 0, m = 0, K = 0, D = 0, V = 0;
+  float eps = 1e-6f;
+  bf16* z[2] = {nullptr, nullptr};
+  int nz = 1;
+  float* x = nullptr;            // [B*(K+1), D]
+  bf16* y[2] = {nullptr, nullptr};
+  int ny = 1;
+  float* tap_z = nullptr;
+  int* status = nullptr;
+};
+
+struct AttnArgs {
+  const float* part_loc = nullptr;  // [S_loc][B*(K+1)][qd + 2 kvd]
+  int S_loc = 1;
+  const float* part_ctx = nullptr;  // [S_ctx][B*m][2 kvd]
+  int S_ctx = 1;
+  const float* rope_cos = nullptr;  // [K+1][d_h/2]
+  const float* rope_sin = nullptr;
+  int B = 0, m = 0, K = 0, n_q = 0, n_kv = 0, d_h = 0;
+  float scale = 1.f;
+  int round_bf16 = 0;
+  bf16* o[2] = {nullptr, nullptr};  // [B*(K+1), n_q*d_h]
+  int no = 1;
+};
+
+struct ResNormArgs {
+  const float* part = nullptr;  // [S][rows][D]
+  int S = 1, rows = 0, D = 0;
+  float* x = nullptr;           // [rows, D], updated in place
+  const float* g = nullptr;
+  float eps = 1e-6f;
+  bf16* y[2] = {nullptr, nullptr};
+  int ny = 1;
+  int final_mode = 0;
+  int K1 = 0;                   // rows per request (final mode)
+  float* bout = nullptr;        // [B*K, D] (final mode)
+  bf16* bp[2] = {nullptr, nullptr};
+  float* tap_x = nullptr;
+  float* tap_b = nullptr;
+};
+
+struct ChainArgs {
+  const float* part = nullptr;  // [S][B*K][2R]: c at [0, R), e at [R, 2R)
+  int S = 1, rows = 0;
+  const float* Mt = nullptr;    // [R][R], Mt[s][r] = M[r][s]
+  int B = 0, K = 0, R = 0;
+  float* t = nullptr;           // [B*K, R]
+  bf16* tp[2] = {nullptr, nullptr};
+};
+
+struct VerifyArgs {
+  int B = 0, K = 0, V = 0, D = 0;
+  const int32_t* cand = nullptr;
+  const int32_t* tgt = nullptr;        // greedy
+  const dlite_qstats* qs = nullptr;    // sampling
+  const float* hs = nullptr;           // [B*K, D]
+  const float* probs = nullptr;        // [B, K+1, V]
+  const bf16* Eb = nullptr;            // E rows for q(v) (bf16 weights)
+  const float* Ef = nullptr;           // ... or fp32 weights
+  double* resid = nullptr;             // [B, V] fallback scratch
+  double T = 0.0;
+  uint32_t k0 = 0, k1 = 0;
+  const int64_t* pos = nullptr;
+  int32_t* accepted = nullptr;
+  int32_t* commits = nullptr;
+  int32_t* n_commit = nullptr;
+  int32_t* next_anchor = nullptr;
+  int* status = nullptr;
+};
+
+cudaError_t launch_stage(const StageArgs& a, bool f32, cudaStream_t s);
+cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s);
+cudaError_t launch_resnorm(const ResNormArgs& a, cudaStream_t s);
+cudaError_t launch_swiglu(const float* part, int S, int rows, int F, bf16* const* o, int no,
+                          cudaStream_t s);
+cudaError_t launch_head_chain(const ChainArgs& a, cudaStream_t s);
+cudaError_t launch_head_out(const float* part, int S, int rows, int D, const float* b, float* hs,
+                            bf16* const* hp, float* tap, cudaStream_t s);
+cudaError_t launch_split(const float* src, size_t n, bf16* const* pl, float* copy, cudaStream_t s);
+cudaError_t launch_verify_greedy(const VerifyArgs& a, cudaStream_t s);
+cudaError_t launch_verify_sample(const VerifyArgs& a, cudaStream_t s);
+cudaError_t launch_advance(int B, const int32_t* n_commit, int64_t* pos, cudaStream_t s);
+cudaError_t launch_repack(const void* src, bool src_f32, int rows, int cols, int src_ld,
+                          int src_off, bf16* p0, bf16* p1, int np, float* f32, cudaStream_t s);
+cudaError_t launch_head_matrix(const void* Q, const void* P, bool f32, int D, int R, float* Mt,
+                               cudaStream_t s);
+
+}  // namespace dlite

@@ -1,0 +1,238 @@
+/*
+ * dlite.h — C ABI of the DLite draft-and-verify round on one GB300 GPU.
+ *
+ * The method (DLite: history-free speculative decoding) drafts K tokens from
+ * the target model's current pivot features alone — m selected target-layer
+ * hidden states at the last processed position plus the anchor token — with
+ * no draft-side history KV, then verifies them against the target.
+ * Sources, cited by page / section / equation:
+ *   [P1] "DLite 完全拆解:面向智能体的无历史投机解码" (pinghaoyang.com.cn)
+ *   [P2] "DLite: History-free Speculative Decoding for Agentic AI" summary (yomxxx.com)
+ *
+ * Conventions for every call below
+ *   - Array arguments are DEVICE pointers owned by the caller, unless the
+ *     name ends in _host. They must stay valid until the stream reaches the
+ *     call. Layouts are dense, row-major, in the shapes given.
+ *   - Calls are stream-ordered and asynchronous: they enqueue kernels on
+ *     `stream` and return; they never allocate device memory and never
+ *     synchronise (except dlite_create, dlite_destroy, dlite_device_status
+ *     and dlite_round_host, which say so).
+ *   - Return value: DLITE_OK (0) or a negative DLITE_ERR_* code. Arguments are
+ *     validated on the host before anything is launched; on an error nothing
+ *     is enqueued. Device-side problems (an out-of-range token id, a bounded
+ *     wait that ran out) set bits in the handle's sticky device status word,
+ *     read with dlite_device_status; kernels never trap.
+ *   - A handle may be used from one stream at a time; calls on one handle
+ *     share its workspace, so calls that overlap on the GPU race.
+ */
+#ifndef DLITE_H
+#define DLITE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *dlite_stream_t; /* same type as cudaStream_t; NULL = legacy default stream */
+
+enum dlite_dtype { DLITE_F32 = 0, DLITE_BF16 = 1 };
+
+enum dlite_status {
+    DLITE_OK = 0,
+    DLITE_ERR_INVALID_ARG = -1,       /* null pointer, B out of [1, B_max], bad enum */
+    DLITE_ERR_UNSUPPORTED_SHAPE = -2, /* config outside what the kernels handle */
+    DLITE_ERR_CUDA = -3,              /* a CUDA runtime call failed (launch, copy, ...) */
+    DLITE_ERR_DEVICE_TIMEOUT = -4,    /* device status: a bounded wait ran out */
+    DLITE_ERR_BOUNDS = -5,            /* device status: an id was out of range (clamped) */
+    DLITE_ERR_OOM = -6                /* dlite_create could not allocate */
+};
+
+/* Device status word bits (dlite_device_status). */
+#define DLITE_DEV_TIMEOUT 1
+#define DLITE_DEV_BOUNDS 2
+
+/* Drafter shape. Positions: block = anchor + K placeholders ([P1] §"草稿块长与
+ * 验证块长不是一个参数": block_size 8 = 1 anchor + 7 drafts). */
+typedef struct {
+    int B_max;        /* largest batch any call will pass */
+    int D;            /* hidden width; multiple of 64 */
+    int m;            /* selected target layers (context slots); m + K + 1 <= 32 */
+    int K;            /* draft positions, 1..31 */
+    int L_D;          /* backbone layers, 1..DLITE_MAX_LAYERS */
+    int n_q, n_kv, d_h; /* attention heads; n_q % n_kv == 0; d_h in {64, 128} */
+    int F;            /* SwiGLU inner width; multiple of 64 */
+    int R;            /* sequential-head rank; multiple of 32, <= 1024 */
+    int V;            /* vocabulary (tied embedding / LM head) */
+    int dtype;        /* DLITE_F32 or DLITE_BF16: type of all weights and of `hidden` */
+    float rms_eps;    /* RMSNorm epsilon (1e-6) */
+    float rope_theta; /* RoPE base (1e6) */
+} dlite_config;
+
+#define DLITE_MAX_LAYERS 8
+
+/* Weights of one backbone layer, nn.Linear layout W[out, in], element type
+ * cfg.dtype. Shapes: g_attn, g_ffn [D]; Wq [n_q*d_h, D]; Wk, Wv [n_kv*d_h, D];
+ * Wo [D, n_q*d_h]; Wg, Wu [F, D]; Wd [D, F]. */
+typedef struct {
+    const void *g_attn, *Wq, *Wk, *Wv, *Wo, *g_ffn, *Wg, *Wu, *Wd;
+} dlite_layer_weights;
+
+/* All drafter weights (device pointers, element type cfg.dtype):
+ *   e_depth [m, D]   depth embedding ([P1] §"History-Free 到底省掉了什么", eq. z_t)
+ *   g_stage [D]      RMSNorm gain after the depth embedding is added
+ *   e_ph [D]         placeholder embedding ([P1] §"锚点是已经确定...")
+ *   E [V, D]         tied token embedding / LM head
+ *   g_final [D]      final RMSNorm gain of the backbone
+ *   Q [R, 2D]        sequential head, acting on [b_i ; h_{i-1}]
+ *   P [D, R]         sequential head output map: h_i = b_i + P tanh(Q [b_i; h_{i-1}]) */
+typedef struct {
+    const void *e_depth, *g_stage, *e_ph, *E, *g_final, *Q, *P;
+    dlite_layer_weights layer[DLITE_MAX_LAYERS];
+} dlite_weights;
+
+/* Draft statistics of one draft slot for sampling verification: the logit of
+ * the drawn token and log-sum-exp of logits / T, so q(d) = exp(logit/T - lse). */
+typedef struct {
+    float logit;
+    float lse;
+} dlite_qstats;
+
+typedef struct dlite_handle dlite_handle;
+
+/* Create a drafter on the current CUDA device. Copies and repacks the weights
+ * into handle-owned device memory (caller buffers may be freed afterwards),
+ * precomputes the sequential head's R x R matrix Q_h P, and allocates the
+ * workspace for batches up to B_max. Synchronises the device.
+ * Errors: INVALID_ARG (null), UNSUPPORTED_SHAPE, OOM, CUDA. */
+int dlite_create(const dlite_config *cfg, const dlite_weights *w, dlite_handle **out);
+
+/* Free everything the handle owns. Synchronises the device. NULL is a no-op. */
+void dlite_destroy(dlite_handle *h);
+
+/* One history-free draft ([P1] §"从目标隐藏状态到并行草稿表示", Fig. 3;
+ * [P2] §设计).
+ *   hidden [B, m, D] (cfg.dtype)  pivot features: the current hidden states of
+ *                                 the m selected target layers (no KV, no history)
+ *   anchor [B] int32              the token already chosen but not yet run
+ *                                 through the target ([P1] §"锚点...")
+ *   temperature                   0 = greedy argmax; > 0 = Gumbel-max draw from
+ *                                 q_i = softmax(l_i / T)
+ *   seed, pos [B] int64           RNG key and per-request position offset; draft
+ *                                 slot i (1..K) uses position pos[b] + i
+ *                                 (ignored when temperature == 0; pos may be NULL then)
+ *   candidates [B, K] int32       out: d_1..d_K
+ *   qstats [B, K]                 out: draft statistics (may be NULL when T == 0)
+ * Local rows: anchor at local position 0, placeholders at 1..K; the context
+ * slots are key/value-only rows at position 0. Out-of-range anchors are
+ * clamped to 0 and flag DLITE_DEV_BOUNDS. */
+int dlite_draft_round(dlite_handle *h, int B, const void *hidden, const int32_t *anchor,
+                      float temperature, uint64_t seed, const int64_t *pos,
+                      int32_t *candidates, dlite_qstats *qstats, dlite_stream_t stream);
+
+/* Optional intermediate outputs of a draft (device pointers, float32; any may
+ * be NULL): z [B, m, D] staged context features; x [L_D, B, K+1, D] residual
+ * stream after each layer; b [B, K, D] backbone outputs; hs [B, K, D]
+ * sequential-head outputs. */
+typedef struct {
+    float *z, *x, *b, *hs;
+} dlite_taps;
+
+/* dlite_draft_round plus taps (for checking hidden representations). */
+int dlite_draft_round_taps(dlite_handle *h, int B, const void *hidden, const int32_t *anchor,
+                           float temperature, uint64_t seed, const int64_t *pos,
+                           int32_t *candidates, dlite_qstats *qstats, const dlite_taps *taps,
+                           dlite_stream_t stream);
+
+/* Stage entry points (the same kernels as dlite_draft_round, split at the
+ * stage boundaries, for stage-by-stage checks).
+ *   dlite_backbone:   hidden, anchor -> b [B, K, D] float32 (staging + L_D layers + final norm)
+ *   dlite_seq_head:   b [B, K, D] float32 -> hs [B, K, D] float32 (sequential head)
+ *   dlite_lm_head:    hs [B, K, D] float32 -> candidates, qstats (vocabulary
+ *                     projection with the fused argmax / Gumbel-max + LSE) */
+int dlite_backbone(dlite_handle *h, int B, const void *hidden, const int32_t *anchor, float *b,
+                   dlite_stream_t stream);
+int dlite_seq_head(dlite_handle *h, int B, const float *b, float *hs, dlite_stream_t stream);
+int dlite_lm_head(dlite_handle *h, int B, const float *hs, float temperature, uint64_t seed,
+                  const int64_t *pos, int32_t *candidates, dlite_qstats *qstats,
+                  dlite_stream_t stream);
+
+/* Greedy verification ([P1] §"一次因果前向评估整条候选", §"贪心模式与随机模式").
+ *   candidates [B, K], target_tokens [B, K+1] int32: target_tokens[b, j] is the
+ *   target's argmax at input index j of [a, d_1..d_K] (its choice for position j+1).
+ * Outputs: accepted [B] = A (leading matches, 0..K); commits [B, K+1] =
+ * d_1..d_A then target_tokens[b, A], entries past A set to -1;
+ * n_commit [B] = A + 1; next_anchor [B] = target_tokens[b, A].
+ * next_anchor may alias the anchor buffer of the draft that produced the
+ * candidates (it is written after the draft has read it). */
+int dlite_verify(dlite_handle *h, int B, const int32_t *candidates, const int32_t *target_tokens,
+                 int32_t *accepted, int32_t *commits, int32_t *n_commit, int32_t *next_anchor,
+                 dlite_stream_t stream);
+
+/* Speculative-sampling verification ([P1] §"贪心模式与随机模式要分别说明",
+ * eqs. alpha(d) = min(1, p(d)/q(d)) and p_res = [p - q]_+ / sum).
+ *   candidates [B, K], qstats [B, K]     from the draft (temperature T > 0)
+ *   hs [B, K, D] float32 or NULL         sequential-head outputs the candidates were
+ *                                        drawn from (NULL: the handle's copy from its
+ *                                        most recent dlite_draft_round)
+ *   target_probs [B, K+1, V] float32     p_j: target distribution at input index j
+ * d_i is accepted iff u_i * q_i(d_i) < p_{i-1}(d_i), u_i = Philox(seed, request b,
+ * position pos[b]+i). At the first rejection the replacement is drawn from the
+ * residual by proposal-rejection (v ~ p, kept w.p. max(0, 1 - q(v)/p(v)), 32
+ * proposals, then inverse CDF over [p - q]_+); with no rejection the bonus token
+ * is drawn from p_K. Decisions are taken in float64. Outputs as dlite_verify. */
+int dlite_verify_sample(dlite_handle *h, int B, const int32_t *candidates,
+                        const dlite_qstats *qstats, const float *hs, const float *target_probs,
+                        float temperature, uint64_t seed, const int64_t *pos, int32_t *accepted,
+                        int32_t *commits, int32_t *n_commit, int32_t *next_anchor,
+                        dlite_stream_t stream);
+
+/* Round bookkeeping: pos[b] += n_commit[b] (the RNG positions follow the
+ * committed tokens; [P1] §"一轮执行后..." — each round advances A+1). */
+int dlite_advance(dlite_handle *h, int B, const int32_t *n_commit, int64_t *pos,
+                  dlite_stream_t stream);
+
+/* One whole round from HOST buffers: copies hidden_host [B, m, D] (cfg.dtype),
+ * anchor_host [B], pos_host [B] and either target_tokens_host [B, K+1]
+ * (temperature == 0) or target_probs_host [B, K+1, V] (temperature > 0) to the
+ * device, runs draft + verify, copies accepted/commits/n_commit/next_anchor
+ * back into the *_host outputs, and synchronises `stream`. Host buffers should
+ * be pinned for asynchronous copies. Uses handle-owned device staging buffers. */
+int dlite_round_host(dlite_handle *h, int B, const void *hidden_host, const int32_t *anchor_host,
+                     const int64_t *pos_host, const int32_t *target_tokens_host,
+                     const float *target_probs_host, float temperature, uint64_t seed,
+                     int32_t *accepted_host, int32_t *commits_host, int32_t *n_commit_host,
+                     int32_t *next_anchor_host, dlite_stream_t stream);
+
+/* Read (and with clear != 0, reset) the sticky device status word.
+ * Synchronises `stream`. *status_out gets DLITE_DEV_* bits. Returns
+ * DLITE_ERR_DEVICE_TIMEOUT or DLITE_ERR_BOUNDS when those bits are set. */
+int dlite_device_status(dlite_handle *h, int clear, int *status_out, dlite_stream_t stream);
+
+/* Static description of a status code. */
+const char *dlite_status_string(int status);
+
+/* Profiling: run one draft (and, when target_tokens / target_probs is given,
+ * its greedy / sampling verification) eagerly on `stream`, recording a CUDA
+ * event after every kernel launch; synchronises `stream`. Writes the elapsed
+ * milliseconds of launch i into times_ms[i] and a static kernel name into
+ * names[i] (names may be NULL), for up to `cap` launches. Returns the number
+ * of launches (> 0) or a negative DLITE_ERR_*. Arguments as dlite_draft_round
+ * and dlite_verify / dlite_verify_sample. */
+int dlite_stage_times(dlite_handle *h, int B, const void *hidden, const int32_t *anchor,
+                      float temperature, uint64_t seed, const int64_t *pos,
+                      const int32_t *target_tokens, const float *target_probs, int32_t *candidates,
+                      dlite_qstats *qstats, int32_t *accepted, int32_t *commits, int32_t *n_commit,
+                      int32_t *next_anchor, float *times_ms, const char **names, int cap,
+                      dlite_stream_t stream);
+
+/* Number of kernels the last draft+verify path enqueues for batch B
+ * (greedy when temperature == 0), for launch accounting. */
+int dlite_launch_count(dlite_handle *h, int B, float temperature);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DLITE_H */

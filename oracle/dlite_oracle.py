@@ -237,6 +237,7 @@ def draft_request(hidden, anchor, W, cfg, temperature=0.0, seed=0, pos=0, reques
     温度缩放和 softmax,得到草稿分布 q_i").
     Returns dict(cand, logit_d, lse, gap, b, h).
     """
+    temperature = float(np.float32(temperature))   # a float32 quantity, as in the C ABI
     b = backbone(hidden, anchor, W, cfg, mirror, taps)
     h = sequential_head(b, W["Q"], W["P"])
     ell = lm_logits(h, W["E"])
@@ -313,7 +314,7 @@ def verify_sample(cand, logit_d, lse, h, E, p, temperature, seed, pos, request):
       u = Philox(0, pos+K+1, request, TAG_BONUS) word 0.
     q(v) for arbitrary v is recomputed from the head state: exp(E_v.h/T - lse).
     """
-    T = float(temperature)
+    T = float(np.float32(temperature))   # a float32 quantity, as in the C ABI
     cand = [int(c) for c in cand]
     K = len(cand)
     p = f64(p)

@@ -1,0 +1,67 @@
+"""The C ABI library builds, loads without a GPU and exports every declared symbol."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from history_free_speculative_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = []
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[\w\s\*]*?\b(dlite_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def so():
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def test_every_declared_symbol_is_exported(so):
+    names = _declared()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(so, n), n
+
+
+def test_binding_covers_declared_symbols():
+    assert sorted(binding.EXPORTED) == _declared()
+
+
+def test_missing_library_fails_loudly():
+    saved = binding._lib
+    binding._lib = None
+    try:
+        with pytest.raises(RuntimeError):
+            binding.load("/nonexistent/libdlite.so")
+    finally:
+        binding._lib = saved
+
+
+def test_host_side_validation_needs_no_gpu(so):
+    """Argument errors are returned before any CUDA call is made."""
+    lib = binding.load()
+    h = ctypes.c_void_p()
+    assert lib.dlite_create(None, None, ctypes.byref(h)) == -1
+    bad = binding.Config(B_max=1, D=100, m=4, K=4, L_D=1, n_q=4, n_kv=2, d_h=64, F=768, R=32,
+                         V=2048, dtype=0, rms_eps=1e-6, rope_theta=1e6)
+    w = binding.Weights()
+    for n in ("e_depth", "g_stage", "e_ph", "E", "g_final", "Q", "P"):
+        setattr(w, n, 1)
+    assert lib.dlite_create(ctypes.byref(bad), ctypes.byref(w), ctypes.byref(h)) == -2
+    bad.D = 256
+    bad.m = 30   # m + K + 1 > 32: block does not fit one warp of keys
+    assert lib.dlite_create(ctypes.byref(bad), ctypes.byref(w), ctypes.byref(h)) == -2
+    assert lib.dlite_draft_round(None, 1, None, None, 0.0, 0, None, None, None, None) == -1
+    assert lib.dlite_verify(None, 1, None, None, None, None, None, None, None) == -1
+    assert lib.dlite_status_string(-2) == b"unsupported shape"
+    lib.dlite_destroy(None)

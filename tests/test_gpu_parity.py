@@ -1,0 +1,394 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Tolerances (from the method's stated agreement bar):
+  * token ids, A and commits: bit-exact;
+  * hidden representations: relative L2 error <= 2e-2 per tensor against the
+    pure fp64 oracle (bf16 weights, fp32 accumulate);
+  * candidates: >= 99.9% identical, and every mismatch only where the
+    oracle's top-2 gap (logits, or perturbed scores when sampling) is < 1e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+from history_free_speculative_gb300 import binding
+from history_free_speculative_gb300 import workload as wk
+from oracle import dlite_oracle as O
+from oracle import philox as ph
+from parity import HIDDEN_REL_TOL, check_candidates, f64_weights, rel_err
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def _drafter(cfg, W, B_max):
+    return binding.Drafter(cfg, wk.weights_to(W, DEV), B_max=B_max)
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    wl = wk.WORKLOADS["tiny"]
+    W = wk.make_weights(wl.cfg, wl.weight_seed, gain_jitter=True)
+    dr = _drafter(wl.cfg, W, B_max=16)
+    yield wl, W, dr
+    dr.close()
+
+
+# ---------------------------------------------------------------- tiny fp32 round, greedy
+
+def test_tiny_round_hidden_and_candidates(tiny):
+    wl, W, dr = tiny
+    cfg = wl.cfg
+    B = 16
+    cands, ocands, gaps = [], [], []
+    for rnd in range(3):
+        hidden, anchor, pos = wk.make_round_inputs(wl, B=B, round_index=rnd)
+        out = dr.new_outputs(B, DEV)
+        taps = {"z": torch.empty(B, cfg.m, cfg.D, device=DEV),
+                "x": torch.empty(cfg.L_D, B, cfg.K + 1, cfg.D, device=DEV),
+                "b": torch.empty(B, cfg.K, cfg.D, device=DEV),
+                "hs": torch.empty(B, cfg.K, cfg.D, device=DEV)}
+        dr.draft_round(hidden.to(DEV), anchor.to(DEV), 0.0, 0, pos.to(DEV), out["cand"],
+                       out["qstats"], taps=taps)
+        torch.cuda.synchronize()
+        for b in range(B):
+            t = {}
+            r = O.draft_request(hidden[b], int(anchor[b]), W, cfg, taps=t)
+            assert rel_err(taps["z"][b].cpu(), t["z"]) < 1e-5
+            for l in range(cfg.L_D):
+                assert rel_err(taps["x"][l, b].cpu(), t["x"][l]) < 1e-4
+            assert rel_err(taps["b"][b].cpu(), t["b"]) < 1e-4
+            assert rel_err(taps["hs"][b].cpu(), t["h"]) < 1e-4
+            cands.append(out["cand"][b].cpu().numpy())
+            ocands.append(r["cand"])
+            gaps.append(r["gap"])
+    check_candidates(np.stack(cands), np.stack(ocands), np.stack(gaps))
+
+
+def test_tiny_round_verify_commits(tiny):
+    wl, W, dr = tiny
+    cfg = wl.cfg
+    B = 16
+    hidden, anchor, pos = wk.make_round_inputs(wl, B=B, round_index=7)
+    ref = O.draft_round(hidden, anchor.numpy(), W, cfg)
+    ocand = np.stack([ref[b]["cand"] for b in range(B)])
+    tgt = wk.make_target_tokens(ocand, wl.accept_c, cfg.V, wl.rng_seed)
+    out = dr.new_outputs(B, DEV)
+    dr.draft_round(hidden.to(DEV), anchor.to(DEV), 0.0, 0, pos.to(DEV), out["cand"], out["qstats"])
+    dr.verify(out["cand"], tgt.to(DEV), out["accepted"], out["commits"], out["n_commit"],
+              out["next_anchor"])
+    torch.cuda.synchronize()
+    assert np.array_equal(out["cand"].cpu().numpy(), ocand)
+    for b in range(B):
+        ov = O.verify_greedy(ocand[b], tgt[b].numpy())
+        assert int(out["accepted"][b]) == ov["A"]
+        assert int(out["n_commit"][b]) == ov["n_commit"]
+        assert out["commits"][b, :ov["n_commit"]].tolist() == ov["commits"]
+        assert int(out["next_anchor"][b]) == ov["next_anchor"]
+
+
+def test_tiny_round_sampling(tiny):
+    wl, W, dr = tiny
+    cfg = wl.cfg
+    B, T, seed = 16, 0.7, 4242
+    hidden, anchor, pos = wk.make_round_inputs(wl, B=B, round_index=3)
+    out = dr.new_outputs(B, DEV)
+    dr.draft_round(hidden.to(DEV), anchor.to(DEV), T, seed, pos.to(DEV), out["cand"], out["qstats"])
+    torch.cuda.synchronize()
+    qs = out["qstats"].cpu().numpy()
+    cands, ocands, gaps = [], [], []
+    for b in range(B):
+        r = O.draft_request(hidden[b], int(anchor[b]), W, cfg, temperature=T, seed=seed,
+                            pos=int(pos[b]), request=b)
+        cands.append(out["cand"][b].cpu().numpy())
+        ocands.append(r["cand"])
+        gaps.append(r["gap"])
+        same = out["cand"][b].cpu().numpy() == r["cand"]
+        assert np.allclose(qs[b, same, 0], r["logit_d"][same], rtol=1e-4, atol=1e-4)
+        assert np.allclose(qs[b, :, 1], r["lse"], rtol=1e-5, atol=1e-4)
+    check_candidates(np.stack(cands), np.stack(ocands), np.stack(gaps))
+
+
+# ---------------------------------------------------------------- stage checks on identical inputs
+
+def _rand_hs(cfg, B, seed, scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(B, cfg.K, cfg.D, generator=g) * scale
+
+
+@pytest.mark.parametrize("T", [0.0, 0.7])
+def test_lm_head_identical_inputs_tiny(tiny, T):
+    wl, W, dr = tiny
+    cfg = wl.cfg
+    B = 16
+    hs = _rand_hs(cfg, B, 5)
+    pos = torch.arange(B, dtype=torch.int64) * 100
+    cand = torch.empty(B, cfg.K, dtype=torch.int32, device=DEV)
+    qs = torch.empty(B, cfg.K, 2, device=DEV)
+    dr.lm_head(hs.to(DEV), T, 99, pos.to(DEV), cand, qs)
+    torch.cuda.synchronize()
+    E = O.f64(W["E"])
+    ell = O.lm_logits(hs.reshape(-1, cfg.D).numpy(), E).reshape(B, cfg.K, -1)
+    Tq = float(np.float32(T))
+    if T == 0.0:
+        s = ell
+    else:
+        s = ell / Tq + np.stack([[ph.gumbel_row(99, int(pos[b]) + i + 1, b, cfg.V)
+                                  for i in range(cfg.K)] for b in range(B)])
+    oc = s.argmax(axis=2)
+    part = np.partition(s, -2, axis=2)
+    check_candidates(cand.cpu().numpy(), oc, part[..., -1] - part[..., -2], gap_tol=1e-4)
+
+
+def test_seq_head_identical_inputs_tiny(tiny):
+    wl, W, dr = tiny
+    cfg = wl.cfg
+    B = 16
+    b = _rand_hs(cfg, B, 6)
+    hs = torch.empty(B, cfg.K, cfg.D, device=DEV)
+    dr.seq_head(b.to(DEV), hs)
+    torch.cuda.synchronize()
+    for r in range(B):
+        want = O.sequential_head(b[r].numpy(), W["Q"], W["P"])
+        assert rel_err(hs[r].cpu(), want) < 1e-5
+
+
+# ---------------------------------------------------------------- verify (K5)
+
+@pytest.fixture(scope="module")
+def small_v():
+    """A tiny-vocabulary drafter for exhaustive verify checks (V = 8, K = 3)."""
+    cfg = wk.shrink(wk.TINY, V=8, K=3, D=64, F=128, R=32, n_q=2, n_kv=1, m=2)
+    W = wk.make_weights(cfg, 7)
+    dr = _drafter(cfg, W, B_max=4096)
+    yield cfg, W, dr
+    dr.close()
+
+
+def test_verify_greedy_exhaustive(small_v):
+    """All candidate / target pairs over 3 ids with K = 3, against brute force."""
+    import itertools
+    cfg, W, dr = small_v
+    cands = np.array(list(itertools.product(range(3), repeat=3)), dtype=np.int32)
+    tgts = np.array(list(itertools.product(range(3), repeat=4)), dtype=np.int32)
+    C = np.repeat(cands, len(tgts), axis=0)
+    Tt = np.tile(tgts, (len(cands), 1))
+    B = len(C)
+    out = dr.new_outputs(B, DEV)
+    dr.verify(torch.from_numpy(C).to(DEV), torch.from_numpy(Tt).to(DEV), out["accepted"],
+              out["commits"], out["n_commit"], out["next_anchor"])
+    torch.cuda.synchronize()
+    acc = out["accepted"].cpu().numpy()
+    com = out["commits"].cpu().numpy()
+    for i in range(B):
+        passes = (C[i] == Tt[i, :3]).astype(np.int64)
+        A = int(np.cumprod(passes).sum())
+        assert acc[i] == A
+        assert list(com[i, :A + 1]) == list(C[i, :A]) + [Tt[i, A]]
+        assert all(com[i, A + 1:] == -1)
+    assert np.array_equal(out["n_commit"].cpu().numpy(), acc + 1)
+
+
+def _sample_inputs(cfg, W, B, seed, overlap):
+    """Candidates drawn from q, q statistics and target rows (oracle-computed)."""
+    rng = np.random.default_rng(seed)
+    hs = rng.normal(0, 1.0, (B, cfg.K, cfg.D))
+    E = O.f64(W["E"])
+    ell = O.lm_logits(hs.reshape(-1, cfg.D), E).reshape(B, cfg.K, cfg.V)
+    T = float(np.float32(0.7))
+    lse = np.log(np.exp(ell / T).sum(axis=2))
+    cand = np.empty((B, cfg.K), dtype=np.int64)
+    pos = rng.integers(0, 1 << 20, B)
+    for b in range(B):
+        for i in range(cfg.K):
+            cand[b, i] = np.argmax(ell[b, i] / T + ph.gumbel_row(1, pos[b] + i + 1, b, cfg.V))
+    q = np.exp(ell / T - lse[..., None])
+    p = np.empty((B, cfg.K + 1, cfg.V))
+    for b in range(B):
+        for j in range(cfg.K + 1):
+            d = rng.dirichlet(np.ones(cfg.V) * 0.7)
+            p[b, j] = (overlap * q[b, min(j, cfg.K - 1)] + (1 - overlap) * d) if overlap else d
+    p = (p / p.sum(axis=2, keepdims=True)).astype(np.float32)
+    logit_d = np.take_along_axis(ell, cand[..., None], 2)[..., 0]
+    return hs.astype(np.float32), cand, logit_d.astype(np.float32), lse.astype(np.float32), p, pos
+
+
+@pytest.mark.parametrize("overlap", [0.0, 0.97])
+def test_verify_sample_identical_inputs(small_v, overlap):
+    """Accept/reject, residual proposals and the inverse-CDF fallback: bit-exact."""
+    cfg, W, dr = small_v
+    B, T, seed = 2048, 0.7, 1
+    hs, cand, logit_d, lse, p, pos = _sample_inputs(cfg, W, B, 31 + int(overlap * 100), overlap)
+    qs = np.stack([logit_d, lse], axis=-1)
+    out = dr.new_outputs(B, DEV)
+    dr.verify_sample(torch.from_numpy(cand.astype(np.int32)).to(DEV), torch.from_numpy(qs).to(DEV),
+                     torch.from_numpy(hs).to(DEV), torch.from_numpy(p).to(DEV), T, seed,
+                     torch.from_numpy(pos).to(DEV), out["accepted"], out["commits"],
+                     out["n_commit"], out["next_anchor"])
+    torch.cuda.synchronize()
+    acc = out["accepted"].cpu().numpy()
+    com = out["commits"].cpu().numpy()
+    hows = {}
+    for b in range(B):
+        r = O.verify_sample(cand[b], logit_d[b], lse[b], hs[b], W["E"], p[b], T, seed, int(pos[b]), b)
+        hows[r["how"]] = hows.get(r["how"], 0) + 1
+        assert acc[b] == r["A"], (b, acc[b], r)
+        assert list(com[b, :r["n_commit"]]) == r["commits"], (b, com[b], r)
+    assert np.array_equal(out["next_anchor"].cpu().numpy(), com[np.arange(B), acc])
+    if overlap:
+        assert hows.get("fallback", 0) > 0, hows
+
+
+def test_verify_sample_preserves_target_distribution(small_v):
+    """GPU speculative sampling: the committed first token follows p (chi-square)."""
+    cfg, W, dr = small_v
+    V, N, T = cfg.V, 4096, 0.7
+    rng = np.random.default_rng(3)
+    h1 = rng.normal(0, 1.0, cfg.D)
+    E = O.f64(W["E"])
+    ell = E @ h1
+    Tq = float(np.float32(T))
+    q = np.exp(ell / Tq - ell.max() / Tq)
+    q /= q.sum()
+    lse = float(np.log(np.exp(ell / Tq).sum()))
+    p0 = rng.dirichlet(np.ones(V))
+    pos = np.arange(N, dtype=np.int64) * 16
+    cand = np.zeros((N, cfg.K), dtype=np.int64)
+    for n in range(N):
+        cand[n, 0] = np.argmax(ell / Tq + ph.gumbel_row(5, pos[n] + 1, n, V))
+    hs = np.tile(h1, (N, cfg.K, 1)).astype(np.float32)
+    p = np.tile(p0, (N, cfg.K + 1, 1)).astype(np.float32)
+    qs = np.zeros((N, cfg.K, 2), dtype=np.float32)
+    qs[:, :, 0] = ell[cand].astype(np.float32)
+    qs[:, :, 1] = lse
+    out = dr.new_outputs(N, DEV)
+    dr.verify_sample(torch.from_numpy(cand.astype(np.int32)).to(DEV), torch.from_numpy(qs).to(DEV),
+                     torch.from_numpy(hs).to(DEV), torch.from_numpy(p).to(DEV), T, 5,
+                     torch.from_numpy(pos).to(DEV), out["accepted"], out["commits"],
+                     out["n_commit"], out["next_anchor"])
+    torch.cuda.synchronize()
+    first = out["commits"][:, 0].cpu().numpy()
+    counts = np.bincount(first, minlength=V)
+    pp = p0.astype(np.float32).astype(np.float64)
+    pp /= pp.sum()
+    chi2 = ((counts - N * pp) ** 2 / (N * pp)).sum()
+    assert chi2 < 40.0, (chi2, counts, N * pp)     # 7 dof
+    beta = np.minimum(pp, q).sum()
+    acc1 = (out["accepted"].cpu().numpy() >= 1).mean()
+    assert abs(acc1 - beta) < 5 * np.sqrt(beta * (1 - beta) / N)
+
+
+# ---------------------------------------------------------------- invariants and robustness
+
+def test_history_free_and_deterministic(tiny):
+    """Same (hidden, anchor, key) -> bit-identical draft, whatever ran before."""
+    wl, W, dr = tiny
+    B = 16
+    hidden, anchor, pos = wk.make_round_inputs(wl, B=B, round_index=11)
+    args = (hidden.to(DEV), anchor.to(DEV))
+    o1 = dr.new_outputs(B, DEV)
+    dr.draft_round(*args, 0.7, 5, pos.to(DEV), o1["cand"], o1["qstats"])
+    for k in range(5):        # unrelated rounds in between
+        h2, a2, p2 = wk.make_round_inputs(wl, B=B, round_index=100 + k)
+        o = dr.new_outputs(B, DEV)
+        dr.draft_round(h2.to(DEV), a2.to(DEV), 0.7, 9, p2.to(DEV), o["cand"], o["qstats"])
+    o2 = dr.new_outputs(B, DEV)
+    dr.draft_round(*args, 0.7, 5, pos.to(DEV), o2["cand"], o2["qstats"])
+    torch.cuda.synchronize()
+    assert torch.equal(o1["cand"], o2["cand"])
+    assert torch.equal(o1["qstats"], o2["qstats"])
+
+
+def test_out_of_range_anchor_flags_status(tiny):
+    wl, W, dr = tiny
+    B = 2
+    hidden, anchor, pos = wk.make_round_inputs(wl, B=B, round_index=1)
+    anchor[1] = wl.cfg.V + 5
+    out = dr.new_outputs(B, DEV)
+    dr.draft_round(hidden.to(DEV), anchor.to(DEV), 0.0, 0, pos.to(DEV), out["cand"], out["qstats"])
+    rc, st = dr.device_status(clear=True)
+    assert st & 2 and rc == -5
+    rc, st = dr.device_status(clear=True)
+    assert rc == 0 and st == 0
+
+
+def test_graph_capture_matches_eager(tiny):
+    wl, W, dr = tiny
+    cfg = wl.cfg
+    B = 8
+    hidden, anchor, pos = wk.make_round_inputs(wl, B=B, round_index=2)
+    hd, ad, pd = hidden.to(DEV), anchor.to(DEV), pos.to(DEV)
+    tgt = wk.make_target_tokens(np.zeros((B, cfg.K), dtype=np.int64), 0.0, cfg.V, 3).to(DEV)
+    eager = dr.new_outputs(B, DEV)
+    dr.draft_round(hd, ad, 0.0, 0, pd, eager["cand"], eager["qstats"])
+    dr.verify(eager["cand"], tgt, eager["accepted"], eager["commits"], eager["n_commit"],
+              eager["next_anchor"])
+    g_out = dr.new_outputs(B, DEV)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            dr.draft_round(hd, ad, 0.0, 0, pd, g_out["cand"], g_out["qstats"], stream=s)
+            dr.verify(g_out["cand"], tgt, g_out["accepted"], g_out["commits"], g_out["n_commit"],
+                      g_out["next_anchor"], stream=s)
+    graph.replay()
+    torch.cuda.synchronize()
+    for k in ("cand", "accepted", "commits", "n_commit", "next_anchor"):
+        assert torch.equal(eager[k], g_out[k]), k
+
+
+def test_round_host_matches_device_path(tiny):
+    wl, W, dr = tiny
+    cfg = wl.cfg
+    B = 4
+    hidden, anchor, pos = wk.make_round_inputs(wl, B=B, round_index=4)
+    tgt = wk.make_target_tokens(np.zeros((B, cfg.K), dtype=np.int64), 0.0, cfg.V, 3)
+    dev = dr.new_outputs(B, DEV)
+    dr.draft_round(hidden.to(DEV), anchor.to(DEV), 0.0, 0, pos.to(DEV), dev["cand"], dev["qstats"])
+    dr.verify(dev["cand"], tgt.to(DEV), dev["accepted"], dev["commits"], dev["n_commit"],
+              dev["next_anchor"])
+    host = {k: v.cpu().pin_memory() for k, v in dr.new_outputs(B, "cpu").items()}
+    dr.round_host(hidden.pin_memory(), anchor.pin_memory(), pos.pin_memory(), tgt.pin_memory(),
+                  None, 0.0, 0, host)
+    for k in ("accepted", "commits", "n_commit", "next_anchor"):
+        assert torch.equal(dev[k].cpu(), host[k]), k
+
+
+# ---------------------------------------------------------------- full-size shapes, sampled
+
+@pytest.mark.parametrize("name", ["qwen3-4b-b1", "qwen3-8b-b32"])
+def test_full_size_round_sampled_requests(name):
+    """Full-size drafter in the bench's launch configuration; the oracle checks
+    two sampled requests end to end (pure for hidden states, mirror for tokens)."""
+    wl = wk.WORKLOADS[name]
+    cfg = wl.cfg
+    B = wl.B
+    W = wk.make_weights(cfg, wl.weight_seed, device=DEV)
+    dr = binding.Drafter(cfg, W, B_max=B)
+    hidden, anchor, pos = wk.make_round_inputs(wl, device=DEV)
+    out = dr.new_outputs(B, DEV)
+    taps = {"b": torch.empty(B, cfg.K, cfg.D, device=DEV),
+            "hs": torch.empty(B, cfg.K, cfg.D, device=DEV)}
+    T = wl.temperature
+    dr.draft_round(hidden, anchor, T, wl.rng_seed, pos, out["cand"], out["qstats"], taps=taps)
+    torch.cuda.synchronize()
+    rc, st = dr.device_status()
+    assert rc == 0
+    Wc = f64_weights(wk.weights_to(W, "cpu"))
+    del W
+    dr_cand = out["cand"].cpu().numpy()
+    sample = [0, B - 1] if B > 1 else [0]
+    cands, ocands, gaps = [], [], []
+    for b in sample:
+        pure = O.draft_request(hidden[b].cpu(), int(anchor[b]), Wc, cfg, temperature=T,
+                               seed=wl.rng_seed, pos=int(pos[b]), request=b, mirror=False)
+        mir = O.draft_request(hidden[b].cpu(), int(anchor[b]), Wc, cfg, temperature=T,
+                              seed=wl.rng_seed, pos=int(pos[b]), request=b, mirror=True)
+        assert rel_err(taps["b"][b].cpu(), pure["b"]) < HIDDEN_REL_TOL
+        assert rel_err(taps["hs"][b].cpu(), pure["h"]) < HIDDEN_REL_TOL
+        cands.append(dr_cand[b])
+        ocands.append(mir["cand"])
+        gaps.append(mir["gap"])
+    check_candidates(np.stack(cands), np.stack(ocands), np.stack(gaps))
+    dr.close()
