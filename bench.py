@@ -162,8 +162,9 @@ def run_gpu(args):
         graphs.append(g)
     launches_per_step = dr.launch_count(B, T) + 1   # + the position bookkeeping kernel
 
-    for i in range(args.warmup):
-        graphs[i % RING].replay()
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % RING].replay()
     stream.synchronize()
     ncommit_total = torch.zeros((), dtype=torch.int64, device=dev)
 
@@ -179,12 +180,12 @@ def run_gpu(args):
     barrier()
     clocks.start()
     time.sleep(0.3)
-    ev0.record(stream)
-    for i in range(args.steps):
-        graphs[i % RING].replay()
-        with torch.cuda.stream(stream):
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(args.steps):
+            graphs[i % RING].replay()
             ncommit_total += out["n_commit"].sum()
-    ev1.record(stream)
+        ev1.record(stream)
     stream.synchronize()
     clk = clocks.stop()
     barrier()

@@ -69,6 +69,7 @@ _SIGS = {
     "dlite_device_status": (_I, [_P, _I, ctypes.POINTER(_I), _P]),
     "dlite_status_string": (ctypes.c_char_p, [_I]),
     "dlite_launch_count": (_I, [_P, _I, _F]),
+    "dlite_selftest_gemm": (_I, [_I, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P]),
     "dlite_stage_times": (_I, [_P, _I, _P, _P, _F, _U64, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                _P, ctypes.POINTER(ctypes.c_char_p), _I, _P]),
 }
@@ -121,6 +122,26 @@ def _stream(stream):
 def _check(code, what):
     if code != 0:
         raise DliteError(code, what)
+
+
+def selftest_gemm(X, W, rows=None, stream=None):
+    """Tensor-core product X[:rows] @ W^T through the round's GEMM engine.
+
+    X, W: lists of 1 or 2 bf16 device planes ([x_rows, K] with x_rows a multiple
+    of 128; [outs, K]). Returns (fp32 [rows, outs] device tensor, status).
+    """
+    lib = load()
+    rows = X[0].shape[0] if rows is None else rows
+    outs, K = W[0].shape
+    part = torch.zeros(16 * rows * outs, dtype=torch.float32, device=X[0].device)
+    st = torch.zeros(1, dtype=torch.int32, device=X[0].device)
+    S = lib.dlite_selftest_gemm(rows, outs, K, len(X), len(W), _ptr(X[0]),
+                                _ptr(X[1]) if len(X) > 1 else None, X[0].shape[0], _ptr(W[0]),
+                                _ptr(W[1]) if len(W) > 1 else None, _ptr(part), _ptr(st),
+                                _stream(stream))
+    if S < 0:
+        raise DliteError(S, "dlite_selftest_gemm")
+    return part[:S * rows * outs].view(S, rows, outs).sum(0), st
 
 
 def config_struct(cfg, B_max):

@@ -7,6 +7,7 @@
 #include <vector>
 
 #include "kernels.h"
+#include "tc_gemm.h"
 
 using namespace dlite;
 
@@ -19,12 +20,22 @@ struct LayerW {
   float* g_ffn;
 };
 
+struct MapEntry {
+  const void* base;
+  int rows, K, box;
+  CUtensorMap map;
+};
+
 struct dlite_handle {
   dlite_config cfg;
   bool f32 = false;
   int np = 1;  // planes of weights and backbone activations (2 for fp32 weights)
   int qd = 0, kvd = 0;
+  int Rp = 0;                       // R padded to a multiple of 64 (GEMM k extent)
+  int Lcap = 0, Ccap = 0, Hcap = 0;  // activation row capacities (multiples of 128)
+  int lm_tiles = 0;
   std::vector<void*> allocs;
+  std::vector<MapEntry> maps;
 
   // weights
   float *e_depth = nullptr, *g_stage = nullptr, *e_ph = nullptr, *g_final = nullptr;
@@ -133,7 +144,7 @@ int repack(dlite_handle* h, const void* src, int rows, int cols, int src_ld, int
     AL(f, n);
     *f32_out = f;
   }
-  CK(launch_repack(src, h->f32, rows, cols, src_ld, off, p0, p1, planes_out ? h->np : 0, f, 0));
+  CK(launch_repack(src, h->f32, rows, cols, src_ld, off, p0, p1, planes_out ? h->np : 0, f, cols, 0));
   return DLITE_OK;
 }
 
@@ -149,7 +160,7 @@ int stack(dlite_handle* h, const void* const* srcs, const int* rows, int n, int 
   size_t off = 0;
   for (int i = 0; i < n; ++i) {
     CK(launch_repack(srcs[i], h->f32, rows[i], cols, cols, 0, p0 + off, p1 ? p1 + off : nullptr,
-                     h->np, nullptr, 0));
+                     h->np, nullptr, cols, 0));
     off += (size_t)rows[i] * cols;
   }
   planes_out[0] = p0;
@@ -157,27 +168,59 @@ int stack(dlite_handle* h, const void* const* srcs, const int* rows, int n, int 
   return DLITE_OK;
 }
 
-Planes planes(const bf16* const* p, int n, int ld) {
-  Planes r;
-  r.p[0] = p[0];
-  r.p[1] = n == 2 ? p[1] : nullptr;
-  r.n = n;
-  r.ld = ld;
-  return r;
+// A GEMM operand: one or two bf16 planes of a row-major [rows, K] buffer.
+struct Operand {
+  const bf16* p[2];
+  int n;     // planes
+  int rows;  // rows of the buffer (tensor-map extent)
+  int K;     // k extent = row length
+};
+
+Operand opnd(const bf16* const* p, int n, int rows, int K) {
+  Operand o;
+  o.p[0] = p[0];
+  o.p[1] = n == 2 ? p[1] : nullptr;
+  o.n = n;
+  o.rows = rows;
+  o.K = K;
+  return o;
 }
 
-int gemm(dlite_handle* h, const char* name, const Planes& X, const Planes& W, int rows, int outs,
-         int K, float* part, int* S_out, cudaStream_t s) {
-  GemmArgs g;
-  g.X = X;
-  g.W = W;
-  g.rows = rows;
-  g.outs = outs;
-  g.K = K;
-  g.splits = gemm_splits(rows, outs, K);
-  g.part = part;
-  if (S_out) *S_out = g.splits;
-  CK(launch_gemm(g, s));
+const CUtensorMap* get_map(dlite_handle* h, const void* base, int rows, int K, int box) {
+  for (const MapEntry& e : h->maps)
+    if (e.base == base && e.rows == rows && e.K == K && e.box == box) return &e.map;
+  MapEntry e;
+  e.base = base;
+  e.rows = rows;
+  e.K = K;
+  e.box = box;
+  if (!tc::make_map(&e.map, base, rows, K, box)) return nullptr;
+  h->maps.push_back(e);
+  return &h->maps.back().map;
+}
+
+// part[z][r][o] = sum over split z of X[r, :] . W[o, :], r < rows, o < outs.
+int gemm(dlite_handle* h, const char* name, const Operand& X, const Operand& W, int rows, int outs,
+         float* part, int* S_out, cudaStream_t s) {
+  const tc::Plan pl = tc::plan(rows, outs, X.K, X.n, W.n, false);
+  if (!pl.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
+  h->maps.reserve(h->maps.size() + 4);
+  const CUtensorMap* x0 = get_map(h, X.p[0], X.rows, X.K, 128);
+  const CUtensorMap* x1 = X.n == 2 ? get_map(h, X.p[1], X.rows, X.K, 128) : nullptr;
+  const CUtensorMap* w0 = get_map(h, W.p[0], W.rows, W.K, pl.N);
+  const CUtensorMap* w1 = W.n == 2 ? get_map(h, W.p[1], W.rows, W.K, pl.N) : nullptr;
+  if (!x0 || !w0 || (X.n == 2 && !x1) || (W.n == 2 && !w1)) return DLITE_ERR_CUDA;
+  tc::TcParams prm;
+  prm.rows = rows;
+  prm.outs = outs;
+  prm.K = X.K;
+  prm.xplanes = X.n;
+  prm.wplanes = W.n;
+  prm.mode = 0;
+  prm.part = part;
+  prm.status = h->status;
+  if (S_out) *S_out = pl.S;
+  CK(tc::launch(pl, x0, x1, w0, w1, prm, s));
   mark(h, name);
   return DLITE_OK;
 }
@@ -194,6 +237,10 @@ void seed_key(uint64_t seed, uint32_t* k0, uint32_t* k1) {
 }
 
 // ---------------------------------------------------------------- stages
+
+tc::Plan lm_plan(dlite_handle* h, int rows) {
+  return tc::plan(rows, h->cfg.V, h->cfg.D, 2, h->np, true);
+}
 
 int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anchor,
                  const dlite_taps* taps, cudaStream_t s) {
@@ -229,12 +276,12 @@ int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anch
     const LayerW& w = h->layer[l];
     int S1 = 1, S2 = 1;
     // local rows: y -> [q | k | v]; context rows: z -> [k | v] with the same bytes
-    RUN(gemm(h, "gemm_qkv", planes(h->y, h->np, c.D), planes(w.Wqkv, h->np, c.D), L, h->qd + 2 * h->kvd, c.D,
-             h->part, &S1, s));
+    RUN(gemm(h, "gemm_qkv", opnd(h->y, h->np, h->Lcap, c.D), opnd(w.Wqkv, h->np, h->qd + 2 * h->kvd, c.D),
+             L, h->qd + 2 * h->kvd, h->part, &S1, s));
     const bf16* wkv[2] = {w.Wqkv[0] + (size_t)h->qd * c.D,
                           w.Wqkv[1] ? w.Wqkv[1] + (size_t)h->qd * c.D : nullptr};
-    RUN(gemm(h, "gemm_ctx_kv", planes(h->z, h->np, c.D), planes(wkv, h->np, c.D), C, 2 * h->kvd, c.D, h->part2, &S2,
-             s));
+    RUN(gemm(h, "gemm_ctx_kv", opnd(h->z, h->np, h->Ccap, c.D), opnd(wkv, h->np, 2 * h->kvd, c.D), C,
+             2 * h->kvd, h->part2, &S2, s));
     AttnArgs at;
     at.part_loc = h->part;
     at.S_loc = S1;
@@ -256,7 +303,8 @@ int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anch
     CK(launch_attention(at, s));
     mark(h, "attention");
     // O projection + residual, then the FFN pre-norm
-    RUN(gemm(h, "gemm_o", planes(h->o, h->np, h->qd), planes(w.Wo, h->np, h->qd), L, c.D, h->qd, h->part, &S1, s));
+    RUN(gemm(h, "gemm_o", opnd(h->o, h->np, h->Lcap, h->qd), opnd(w.Wo, h->np, c.D, h->qd), L, c.D,
+             h->part, &S1, s));
     ResNormArgs rn;
     rn.part = h->part;
     rn.S = S1;
@@ -271,11 +319,13 @@ int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anch
     CK(launch_resnorm(rn, s));
     mark(h, "resnorm");
     // gate/up + SwiGLU
-    RUN(gemm(h, "gemm_gate_up", planes(h->y, h->np, c.D), planes(w.Wgu, h->np, c.D), L, 2 * c.F, c.D, h->part, &S1, s));
+    RUN(gemm(h, "gemm_gate_up", opnd(h->y, h->np, h->Lcap, c.D), opnd(w.Wgu, h->np, 2 * c.F, c.D), L,
+             2 * c.F, h->part, &S1, s));
     CK(launch_swiglu(h->part, S1, L, c.F, h->a, h->np, s));
     mark(h, "swiglu");
     // down + residual, then the next layer's pre-norm (or the final norm)
-    RUN(gemm(h, "gemm_down", planes(h->a, h->np, c.F), planes(w.Wd, h->np, c.F), L, c.D, c.F, h->part, &S1, s));
+    RUN(gemm(h, "gemm_down", opnd(h->a, h->np, h->Lcap, c.F), opnd(w.Wd, h->np, c.D, c.F), L, c.D,
+             h->part, &S1, s));
     ResNormArgs r2 = rn;
     r2.S = S1;
     r2.tap_x = (taps && taps->x) ? taps->x + (size_t)l * L * c.D : nullptr;
@@ -301,7 +351,8 @@ int run_seq_head(dlite_handle* h, int B, float* tap_hs, cudaStream_t s) {
   const dlite_config& c = h->cfg;
   const int rows = B * c.K;
   int S = 1;
-  RUN(gemm(h, "gemm_head_ce", planes(h->bp, 2, c.D), planes(h->Wce, h->np, c.D), rows, 2 * c.R, c.D, h->part, &S, s));
+  RUN(gemm(h, "gemm_head_ce", opnd(h->bp, 2, h->Hcap, c.D), opnd(h->Wce, h->np, 2 * c.R, c.D), rows,
+           2 * c.R, h->part, &S, s));
   ChainArgs ch;
   ch.part = h->part;
   ch.S = S;
@@ -313,9 +364,11 @@ int run_seq_head(dlite_handle* h, int B, float* tap_hs, cudaStream_t s) {
   ch.t = h->t;
   ch.tp[0] = h->tp[0];
   ch.tp[1] = h->tp[1];
+  ch.ldt = h->Rp;
   CK(launch_head_chain(ch, s));
   mark(h, "head_chain");
-  RUN(gemm(h, "gemm_head_p", planes(h->tp, 2, c.R), planes(h->P, h->np, c.R), rows, c.D, c.R, h->part, &S, s));
+  RUN(gemm(h, "gemm_head_p", opnd(h->tp, 2, h->Hcap, h->Rp), opnd(h->P, h->np, c.D, h->Rp), rows, c.D,
+           h->part, &S, s));
   CK(launch_head_out(h->part, S, rows, c.D, h->b, h->hs, h->hp, tap_hs, s));
   mark(h, "head_out");
   return DLITE_OK;
@@ -324,21 +377,32 @@ int run_seq_head(dlite_handle* h, int B, float* tap_hs, cudaStream_t s) {
 int run_lm_head(dlite_handle* h, int B, float temperature, uint64_t seed, const int64_t* pos,
                 int32_t* cand, dlite_qstats* qs, cudaStream_t s) {
   const dlite_config& c = h->cfg;
-  LmArgs la;
-  la.H = planes(h->hp, 2, c.D);
-  la.E = planes(h->E, h->np, c.D);
-  la.rows = B * c.K;
-  la.V = c.V;
-  la.D = c.D;
-  la.K = c.K;
-  la.inv_T = temperature > 0.f ? 1.f / temperature : 0.f;
-  seed_key(seed, &la.k0, &la.k1);
-  la.pos = pos;
-  la.rec = h->lmrec;
-  la.status = h->status;
-  CK(launch_lm_head(la, s));
+  const int rows = B * c.K;
+  const tc::Plan pl = lm_plan(h, rows);
+  if (!pl.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
+  h->maps.reserve(h->maps.size() + 4);
+  const CUtensorMap* x0 = get_map(h, h->hp[0], h->Hcap, c.D, 128);
+  const CUtensorMap* x1 = get_map(h, h->hp[1], h->Hcap, c.D, 128);
+  const CUtensorMap* w0 = get_map(h, h->E[0], c.V, c.D, pl.N);
+  const CUtensorMap* w1 = h->np == 2 ? get_map(h, h->E[1], c.V, c.D, pl.N) : nullptr;
+  if (!x0 || !x1 || !w0 || (h->np == 2 && !w1)) return DLITE_ERR_CUDA;
+  tc::TcParams prm;
+  prm.rows = rows;
+  prm.outs = c.V;
+  prm.K = c.D;
+  prm.xplanes = 2;
+  prm.wplanes = h->np;
+  prm.mode = 1;
+  prm.rec = h->lmrec;
+  prm.inv_T = temperature > 0.f ? 1.f / temperature : 0.f;
+  seed_key(seed, &prm.k0, &prm.k1);
+  prm.pos = pos;
+  prm.K_draft = c.K;
+  prm.status = h->status;
+  CK(tc::launch(pl, x0, x1, w0, w1, prm, s));
   mark(h, "lm_head");
-  CK(launch_lm_merge(h->lmrec, lm_tiles(c.V), la.rows, c.K, la.inv_T, cand, qs, s));
+  const int n_tiles = (c.V + pl.N - 1) / pl.N;
+  CK(launch_lm_merge(h->lmrec, n_tiles, rows, c.K, prm.inv_T, cand, qs, s));
   mark(h, "lm_merge");
   return DLITE_OK;
 }
@@ -417,13 +481,25 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
     bf16* p1 = nullptr;
     AL(p0, (size_t)2 * R * D);
     if (h->np == 2) AL(p1, (size_t)2 * R * D);
-    CK(launch_repack(w->Q, h->f32, R, D, 2 * D, 0, p0, p1, h->np, nullptr, 0));
+    CK(launch_repack(w->Q, h->f32, R, D, 2 * D, 0, p0, p1, h->np, nullptr, D, 0));
     CK(launch_repack(w->Q, h->f32, R, D, 2 * D, D, p0 + (size_t)R * D,
-                     p1 ? p1 + (size_t)R * D : nullptr, h->np, nullptr, 0));
+                     p1 ? p1 + (size_t)R * D : nullptr, h->np, nullptr, D, 0));
     h->Wce[0] = p0;
     h->Wce[1] = p1;
   }
-  RUN(repack(h, w->P, D, R, R, 0, h->P, nullptr));
+  {  // P as [D, Rp] with zero columns R..Rp (the GEMM k extent is a multiple of 64)
+    bf16* p0 = nullptr;
+    bf16* p1 = nullptr;
+    AL(p0, (size_t)D * h->Rp);
+    CK(cudaMemset(p0, 0, (size_t)D * h->Rp * 2));
+    if (h->np == 2) {
+      AL(p1, (size_t)D * h->Rp);
+      CK(cudaMemset(p1, 0, (size_t)D * h->Rp * 2));
+    }
+    CK(launch_repack(w->P, h->f32, D, R, R, 0, p0, p1, h->np, nullptr, h->Rp, 0));
+    h->P[0] = p0;
+    h->P[1] = p1;
+  }
   AL(h->Mt, (size_t)R * R);
   CK(launch_head_matrix(w->Q, w->P, h->f32, D, R, h->Mt, 0));
   {  // RoPE table for local positions 0..K (float64 on the host)
@@ -440,9 +516,9 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
     CK(cudaMemcpy(h->rope_cos, cs.data(), cs.size() * 4, cudaMemcpyHostToDevice));
     CK(cudaMemcpy(h->rope_sin, sn.data(), sn.size() * 4, cudaMemcpyHostToDevice));
   }
-  // ---- workspace (sized for B_max)
+  // ---- workspace (sized for B_max; GEMM A operands padded to 128-row multiples)
   const int Bm = c.B_max;
-  const size_t Lr = (size_t)Bm * (c.K + 1), Cr = (size_t)Bm * c.m, Hr = (size_t)Bm * c.K;
+  const size_t Lr = (size_t)h->Lcap, Cr = (size_t)h->Ccap, Hr = (size_t)h->Hcap;
   AL(h->x, Lr * D);
   for (int p = 0; p < h->np; ++p) {
     AL(h->y[p], Lr * D);
@@ -455,22 +531,34 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
   AL(h->hs, Hr * D);
   for (int p = 0; p < 2; ++p) {
     AL(h->bp[p], Hr * D);
-    AL(h->tp[p], Hr * R);
+    AL(h->tp[p], Hr * h->Rp);
+    CK(cudaMemset(h->tp[p], 0, Hr * h->Rp * 2));
     AL(h->hp[p], Hr * D);
   }
-  size_t pe = 0, pe2 = 0;
+  size_t pe = 0, pe2 = 0, lme = 0;
   for (int B = 1; B <= Bm; ++B) {
     const int L = B * (c.K + 1), C = B * c.m, H = B * c.K;
-    const size_t cand[6] = {gemm_part_elems(L, h->qd + 2 * h->kvd, D), gemm_part_elems(L, D, h->qd),
-                            gemm_part_elems(L, 2 * F, D),           gemm_part_elems(L, D, F),
-                            gemm_part_elems(H, 2 * R, D),           gemm_part_elems(H, D, R)};
-    for (size_t v : cand) pe = v > pe ? v : pe;
-    const size_t v2 = gemm_part_elems(C, 2 * h->kvd, D);
+    const int sites[6][4] = {{L, h->qd + 2 * h->kvd, D, h->np}, {L, D, h->qd, h->np},
+                             {L, 2 * F, D, h->np},               {L, D, F, h->np},
+                             {H, 2 * R, D, 2},                   {H, D, h->Rp, 2}};
+    for (auto& st : sites) {
+      const tc::Plan pl = tc::plan(st[0], st[1], st[2], st[3], h->np, false);
+      if (!pl.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
+      const size_t v = (size_t)pl.S * st[0] * st[1];
+      pe = v > pe ? v : pe;
+    }
+    const tc::Plan pc = tc::plan(C, 2 * h->kvd, D, h->np, h->np, false);
+    if (!pc.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
+    const size_t v2 = (size_t)pc.S * C * 2 * h->kvd;
     pe2 = v2 > pe2 ? v2 : pe2;
+    const tc::Plan pl = lm_plan(h, H);
+    if (!pl.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
+    const size_t v3 = (size_t)((V + pl.N - 1) / pl.N) * H;
+    lme = v3 > lme ? v3 : lme;
   }
   AL(h->part, pe);
   AL(h->part2, pe2);
-  AL(h->lmrec, (size_t)lm_tiles(V) * Hr);
+  AL(h->lmrec, lme);
   AL(h->resid, (size_t)Bm * V);
   AL(h->status, 1);
   CK(cudaMemset(h->status, 0, sizeof(int)));
@@ -510,6 +598,10 @@ int dlite_create(const dlite_config* cfg, const dlite_weights* w, dlite_handle**
   h->np = h->f32 ? 2 : 1;
   h->qd = cfg->n_q * cfg->d_h;
   h->kvd = cfg->n_kv * cfg->d_h;
+  h->Rp = (cfg->R + 63) / 64 * 64;
+  h->Lcap = (cfg->B_max * (cfg->K + 1) + 127) / 128 * 128;
+  h->Ccap = (cfg->B_max * cfg->m + 127) / 128 * 128;
+  h->Hcap = (cfg->B_max * cfg->K + 127) / 128 * 128;
   const int r = create_impl(h, w);
   if (r) {
     dlite_destroy(h);
@@ -705,6 +797,33 @@ int dlite_stage_times(dlite_handle* h, int B, const void* hidden, const int32_t*
     if (names) names[i] = h->prof_name[i];
   }
   return n;
+}
+
+int dlite_selftest_gemm(int rows, int outs, int K, int xplanes, int wplanes, const void* X0,
+                        const void* X1, int x_rows, const void* W0, const void* W1, float* part,
+                        int* status, dlite_stream_t stream) {
+  if (rows < 1 || outs < 8 || outs % 8 || K < 64 || K % 64 || xplanes < 1 || xplanes > 2 ||
+      wplanes < 1 || wplanes > 2 || !X0 || !W0 || !part || x_rows < rows || x_rows % 128)
+    return DLITE_ERR_INVALID_ARG;
+  if ((xplanes == 2 && !X1) || (wplanes == 2 && !W1)) return DLITE_ERR_INVALID_ARG;
+  const tc::Plan pl = tc::plan(rows, outs, K, xplanes, wplanes, false);
+  if (!pl.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
+  CUtensorMap mx0, mx1, mw0, mw1;
+  if (!tc::make_map(&mx0, X0, x_rows, K, 128) || !tc::make_map(&mw0, W0, outs, K, pl.N))
+    return DLITE_ERR_CUDA;
+  if (xplanes == 2 && !tc::make_map(&mx1, X1, x_rows, K, 128)) return DLITE_ERR_CUDA;
+  if (wplanes == 2 && !tc::make_map(&mw1, W1, outs, K, pl.N)) return DLITE_ERR_CUDA;
+  tc::TcParams prm;
+  prm.rows = rows;
+  prm.outs = outs;
+  prm.K = K;
+  prm.xplanes = xplanes;
+  prm.wplanes = wplanes;
+  prm.part = part;
+  prm.status = status;
+  CK(tc::launch(pl, &mx0, xplanes == 2 ? &mx1 : nullptr, &mw0, wplanes == 2 ? &mw1 : nullptr, prm,
+                (cudaStream_t)stream));
+  return pl.S;
 }
 
 int dlite_launch_count(dlite_handle* h, int B, float temperature) {

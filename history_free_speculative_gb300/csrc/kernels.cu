@@ -299,7 +299,7 @@ __global__ void head_chain_kernel(ChainArgs a) {
       tprev[r] = tv[cnt];
       eprev[r] = ev[cnt];
       a.t[(size_t)row * R + r] = tv[cnt];
-      store_planes(a.tp, 2, (size_t)row * R + r, tv[cnt]);
+      store_planes(a.tp, 2, (size_t)row * a.ldt + r, tv[cnt]);
     }
     __syncthreads();
   }
@@ -583,7 +583,7 @@ cudaError_t launch_advance(int B, const int32_t* n_commit, int64_t* pos, cudaStr
 // to bf16 planes (two planes: hi / lo) or to fp32.
 template <typename T>
 __global__ void repack_kernel(const T* src, int rows, int cols, int src_ld, int src_off,
-                              bf16* p0, bf16* p1, int np, float* f32) {
+                              bf16* p0, bf16* p1, int np, float* f32, int dst_ld) {
   const size_t n = (size_t)rows * cols;
   bf16* pl[2] = {p0, p1};
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
@@ -591,21 +591,23 @@ __global__ void repack_kernel(const T* src, int rows, int cols, int src_ld, int 
     const size_t r = i / cols, c = i % cols;
     const float v = to_f32(src[r * src_ld + src_off + c]);
     if (f32) f32[i] = v;
-    if (np) store_planes(pl, np, i, v);
+    if (np) store_planes(pl, np, r * dst_ld + c, v);
   }
 }
 
 cudaError_t launch_repack(const void* src, bool src_f32, int rows, int cols, int src_ld,
-                          int src_off, bf16* p0, bf16* p1, int np, float* f32, cudaStream_t s) {
+                          int src_off, bf16* p0, bf16* p1, int np, float* f32, int dst_ld,
+                          cudaStream_t s) {
   const size_t n = (size_t)rows * cols;
   int blocks = (int)((n + 255) / 256);
   if (blocks > 152 * 32) blocks = 152 * 32;
+  if (dst_ld <= 0) dst_ld = cols;
   if (src_f32)
     repack_kernel<float><<<blocks, 256, 0, s>>>((const float*)src, rows, cols, src_ld, src_off, p0,
-                                                 p1, np, f32);
+                                                 p1, np, f32, dst_ld);
   else
     repack_kernel<bf16><<<blocks, 256, 0, s>>>((const bf16*)src, rows, cols, src_ld, src_off, p0, p1,
-                                                np, f32);
+                                                np, f32, dst_ld);
   return cudaGetLastError();
 }
 

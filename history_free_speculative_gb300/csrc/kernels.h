@@ -60,7 +60,8 @@ struct ChainArgs {
   const float* Mt = nullptr;    // [R][R], Mt[s][r] = M[r][s]
   int B = 0, K = 0, R = 0;
   float* t = nullptr;           // [B*K, R]
-  bf16* tp[2] = {nullptr, nullptr};
+  bf16* tp[2] = {nullptr, nullptr};  // [B*K, ldt] planes (columns R..ldt stay zero)
+  int ldt = 0;
 };
 
 struct VerifyArgs {
@@ -96,7 +97,8 @@ cudaError_t launch_verify_greedy(const VerifyArgs& a, cudaStream_t s);
 cudaError_t launch_verify_sample(const VerifyArgs& a, cudaStream_t s);
 cudaError_t launch_advance(int B, const int32_t* n_commit, int64_t* pos, cudaStream_t s);
 cudaError_t launch_repack(const void* src, bool src_f32, int rows, int cols, int src_ld,
-                          int src_off, bf16* p0, bf16* p1, int np, float* f32, cudaStream_t s);
+                          int src_off, bf16* p0, bf16* p1, int np, float* f32, int dst_ld,
+                          cudaStream_t s);
 cudaError_t launch_head_matrix(const void* Q, const void* P, bool f32, int D, int R, float* Mt,
                                cudaStream_t s);
 

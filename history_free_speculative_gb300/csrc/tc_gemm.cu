@@ -1,0 +1,426 @@
+// Tensor-core GEMM engine for sm_103a: TMA -> shared memory (128B swizzle)
+// -> tcgen05.mma (bf16 x bf16 -> fp32 in TMEM) -> tcgen05.ld epilogue.
+//
+//   D[r, o] = sum_k X[r, k] * W[o, k]
+// X (activations, A operand): rows in M-tiles of 128 (TMEM lanes).
+// W (weights, B operand): one slab of N output features per CTA (TMEM columns).
+// Every CTA streams its weight slab exactly once; all M-tiles of its row
+// group are accumulated side by side in TMEM, so weights are never re-read.
+// Warp roles: warp 0 = TMA producer, warp 1 = TMEM owner + MMA issuer (one
+// thread), warps 2-5 = epilogue (warp w reads TMEM lanes 32*(w%4)..+31).
+// Every mbarrier wait is bounded (~2 s of %globaltimer); on expiry the kernel
+// flags the device status word and runs to its end instead of hanging.
+#include <cuda.h>
+
+#include "internal.h"
+#include "tc_gemm.h"
+
+namespace dlite {
+namespace tc {
+
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+
+__device__ __forceinline__ uint32_t su32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint64_t gtimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait on phase `parity`; false after kTimeoutNs (status flagged).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status) {
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = gtimer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 128; ++i)
+      if (mbar_try(bar, parity)) return true;
+    if (gtimer() - t0 > kTimeoutNs) {
+      flag_status(status, kDevTimeout);
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+      "%4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+// Shared-memory matrix descriptor: K-major tile, rows of 128 B, 128-byte
+// swizzle, 8-row groups 1024 B apart (stride byte offset), descriptor version 1.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accum)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
+      "[%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
+  return v > bv || (v == bv && i < bi);
+}
+__device__ __forceinline__ void lse_add(float& m, float& s, float x) {
+  if (x > m) {
+    s = s * expf(m - x) + 1.f;
+    m = x;
+  } else {
+    s += expf(x - m);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap mx0, const __grid_constant__ CUtensorMap mx1,
+                   const __grid_constant__ CUtensorMap mw0, const __grid_constant__ CUtensorMap mw1,
+                   const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = (uint64_t*)(smem + (size_t)p.stages * p.stage_bytes);
+  uint32_t* tmem_holder = (uint32_t*)(bars + 2 * p.stages + 1);
+  const uint32_t full0 = su32(bars), empty0 = su32(bars + p.stages), accf = su32(bars + 2 * p.stages);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int o0 = blockIdx.x * p.N;
+  const int split = blockIdx.y;
+  const int m0 = blockIdx.z * p.n_mt * 128;
+  const int kb0 = split * p.kb_per_split;
+  const int kb1 = min(kb0 + p.kb_per_split, p.kblocks);
+  const int nkb = kb1 - kb0;
+  const uint32_t wtile = (uint32_t)p.N * 128u;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    mbar_init(accf, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_holder)),
+                 "r"(p.tmem_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0) {
+    if (lane == 0) {  // ---------------- TMA producer
+      const uint32_t bytes = (uint32_t)p.wplanes * wtile + (uint32_t)(p.n_mt * p.xplanes) * 16384u;
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % p.stages;
+        const uint32_t it = (uint32_t)(i / p.stages);
+        if (i >= p.stages && !mbar_wait(empty0 + 8 * s, (it - 1) & 1, p.status)) break;
+        const uint32_t st = su32(smem + (size_t)s * p.stage_bytes);
+        const uint32_t fb = full0 + 8 * s;
+        mbar_expect_tx(fb, bytes);
+        const int kx = (kb0 + i) * 64;
+        tma_load_2d(st, &mw0, fb, kx, o0);
+        if (p.wplanes == 2) tma_load_2d(st + wtile, &mw1, fb, kx, o0);
+        for (int mt = 0; mt < p.n_mt; ++mt)
+          for (int pl = 0; pl < p.xplanes; ++pl)
+            tma_load_2d(st + p.wplanes * wtile + (uint32_t)(mt * p.xplanes + pl) * 16384u,
+                        pl ? &mx1 : &mx0, fb, kx, m0 + mt * 128);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // ---------------- MMA issuer
+      const uint32_t idesc = idesc_bf16(128, p.N);
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % p.stages;
+        const uint32_t it = (uint32_t)(i / p.stages);
+        if (!mbar_wait(full0 + 8 * s, it & 1, p.status)) break;
+        fence_after();
+        const uint32_t sb = su32(smem + (size_t)s * p.stage_bytes);
+#pragma unroll 1
+        for (int kk = 0; kk < 4; ++kk) {
+          for (int mt = 0; mt < p.n_mt; ++mt) {
+            const uint32_t d = tmem + (uint32_t)(mt * p.N);
+            for (int c = 0; c < 3; ++c) {
+              if (c == 1 && p.xplanes < 2) continue;
+              if (c == 2 && p.wplanes < 2) continue;
+              const int px = (c == 1), pw = (c == 2);
+              const uint64_t ad =
+                  sw128_desc(sb + p.wplanes * wtile + (uint32_t)(mt * p.xplanes + px) * 16384u + kk * 32);
+              const uint64_t bd = sw128_desc(sb + pw * wtile + kk * 32);
+              umma_bf16(d, ad, bd, idesc, (i > 0 || kk > 0 || c > 0) ? 1u : 0u);
+            }
+          }
+        }
+        umma_commit(empty0 + 8 * s);
+      }
+      umma_commit(accf);
+    }
+  } else {  // ---------------- epilogue warps 2..5
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const bool got = mbar_wait(accf, 0, p.status);
+    fence_after();
+    if (got) {
+      for (int mt = 0; mt < p.n_mt; ++mt) {
+        const int r = m0 + mt * 128 + q * 32 + lane;
+        const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(mt * p.N);
+        if (p.mode == 0) {
+          float* out = p.part + ((size_t)split * p.rows + r) * p.outs;
+          for (int c = 0; c < p.N; c += 16) {
+            float v[16];
+            tmem_ld16(tbase + c, v);
+            if (r < p.rows) {
+#pragma unroll
+              for (int j = 0; j < 16; j += 4) {
+                const int col = o0 + c + j;
+                if (col + 3 < p.outs)
+                  *reinterpret_cast<float4*>(out + col) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+              }
+            }
+          }
+        } else {
+          // LM head: best (score, id) and LSE partials of this vocabulary slab for row r
+          const bool sampling = p.inv_T > 0.f;
+          float best = -INFINITY, blogit = 0.f, m = -INFINITY, s = 0.f;
+          int bidx = 0x7fffffff;
+          uint32_t pos = 0, req = 0;
+          if (sampling && r < p.rows) {
+            req = (uint32_t)(r / p.K_draft);
+            pos = (uint32_t)(p.pos[req] + (r % p.K_draft) + 1);
+          }
+          const bool valid = r < p.rows;
+          for (int c = 0; c < p.N; c += 16) {
+            float v[16];
+            tmem_ld16(tbase + c, v);  // warp-collective: executed by every lane
+            if (valid) {
+#pragma unroll
+              for (int g = 0; g < 16; g += 4) {
+                const int v0 = o0 + c + g;  // multiple of 4: one Philox call per group
+                if (v0 < p.outs) {          // outs is a multiple of 8: whole groups only
+                  if (!sampling) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                      if (better(v[g + j], v0 + j, best, bidx)) {
+                        best = v[g + j];
+                        bidx = v0 + j;
+                        blogit = v[g + j];
+                      }
+                  } else {
+                    const uint4 w = philox((uint32_t)v0 >> 2, pos, req, kTagGumbel, p.k0, p.k1);
+                    const uint32_t wx[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                      const float lt = v[g + j] * p.inv_T;
+                      const float sc = lt + gumbel_from_bits(wx[j]);
+                      if (better(sc, v0 + j, best, bidx)) {
+                        best = sc;
+                        bidx = v0 + j;
+                        blogit = v[g + j];
+                      }
+                      lse_add(m, s, lt);
+                    }
+                  }
+                }
+              }
+            }
+          }
+          if (r < p.rows) {
+            LmRec rec;
+            rec.best = best;
+            rec.idx = bidx;
+            rec.logit = blogit;
+            rec.m = m;
+            rec.s = s;
+            p.rec[(size_t)blockIdx.x * p.rows + r] = rec;
+          }
+        }
+      }
+    }
+  }
+  fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(p.tmem_cols)
+                 : "memory");
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encoder() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiledFn)f;
+  }
+  return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows) {
+  EncodeTiledFn fn = encoder();
+  if (!fn || !base || ((uintptr_t)base & 15) || K % 64 || box_rows < 1 || box_rows > 256 ||
+      rows < box_rows)
+    return false;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static int next_pow2_cols(int c) {
+  int n = 32;
+  while (n < c) n <<= 1;
+  return n;
+}
+
+Plan plan(int rows, int outs, int K, int xplanes, int wplanes, bool lm) {
+  Plan best;
+  best.ok = false;
+  const int kblocks = K / 64;
+  const int mt_total = (rows + 127) / 128;
+  const double bw_total = 6.5e12, l2_total = 1.6e13, mma_sm = 1.8e15 / kNumSMs;
+  double best_t = 1e30;
+  const int combos = 1 + (xplanes == 2) + (wplanes == 2);
+  const int nmax_out = ((outs + 15) / 16) * 16;
+  for (int gmax = 4; gmax >= 1; gmax >>= 1) {
+    const int groups = (mt_total + gmax - 1) / gmax;
+    const int n_mt = (mt_total + groups - 1) / groups;
+    for (int N = 16; N <= 256; N += 16) {
+      if (N * n_mt > 512 || N > nmax_out) continue;
+      if (N > outs) continue;
+      const uint32_t sb = (uint32_t)wplanes * N * 128 + (uint32_t)n_mt * xplanes * 16384;
+      int stages = (int)((kSmemBudget - 2048) / sb);
+      if (stages > 8) stages = 8;
+      if (stages < 2) continue;
+      const int slabs = (outs + N - 1) / N;
+      const int smax = lm ? 1 : (kblocks < 16 ? kblocks : 16);
+      for (int S = 1; S <= smax; ++S) {
+        const int kbps = (kblocks + S - 1) / S;
+        const int Se = (kblocks + kbps - 1) / kbps;
+        if (Se != S) continue;
+        const long units = (long)slabs * Se * groups;
+        const long waves = (units + kNumSMs - 1) / kNumSMs;
+        const double active = units < kNumSMs ? (double)units : (double)kNumSMs;
+        double bw_sm = bw_total / active;
+        if (bw_sm > 1.2e11) bw_sm = 1.2e11;
+        double l2_sm = l2_total / active;  // activation tiles come from L2, shared by all CTAs
+        if (l2_sm > 1.5e11) l2_sm = 1.5e11;
+        const double t_load = (double)wplanes * N * 128 / bw_sm;
+        const double t_l2 = (double)n_mt * xplanes * 16384 / l2_sm;
+        const double t_mma = (double)n_mt * combos * 128.0 * N * 64 * 2 / mma_sm;
+        double t_kb = t_load > t_mma ? t_load : t_mma;
+        t_kb = (t_kb > t_l2 ? t_kb : t_l2) + 3.0e-8;
+        double t = waves * (kbps * t_kb + 2.0e-6);
+        if (Se > 1) t += (double)Se * rows * outs * 8.0 / bw_total;
+        if (t < best_t * 0.999) {
+          best_t = t;
+          best.ok = true;
+          best.N = N;
+          best.S = Se;
+          best.kb_per_split = kbps;
+          best.kblocks = kblocks;
+          best.n_mt = n_mt;
+          best.groups = groups;
+          best.stages = stages;
+          best.stage_bytes = sb;
+          best.tmem_cols = next_pow2_cols(N * n_mt);
+        }
+      }
+    }
+  }
+  return best;
+}
+
+size_t smem_bytes(const Plan& pl) {
+  return 1024 + (size_t)pl.stages * pl.stage_bytes + 8 * (2 * pl.stages + 1) + 16;
+}
+
+cudaError_t launch(const Plan& pl, const CUtensorMap* x0, const CUtensorMap* x1, const CUtensorMap* w0,
+                   const CUtensorMap* w1, TcParams prm, cudaStream_t s) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(kSmemBudget + 2048));
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  prm.N = pl.N;
+  prm.n_mt = pl.n_mt;
+  prm.kb_per_split = pl.kb_per_split;
+  prm.kblocks = pl.kblocks;
+  prm.stages = pl.stages;
+  prm.stage_bytes = pl.stage_bytes;
+  prm.tmem_cols = (uint32_t)pl.tmem_cols;
+  dim3 grid((prm.outs + pl.N - 1) / pl.N, pl.S, pl.groups);
+  tc_gemm_kernel<<<grid, kThreads, smem_bytes(pl), s>>>(*x0, x1 ? *x1 : *x0, *w0, w1 ? *w1 : *w0, prm);
+  return cudaGetLastError();
+}
+
+}  // namespace tc
+}  // namespace dlite

@@ -1,0 +1,50 @@
+// tcgen05 GEMM engine: plan, tensor maps and launch.
+#pragma once
+
+#include <cuda.h>
+
+#include "internal.h"
+
+namespace dlite {
+namespace tc {
+
+constexpr int kThreads = 192;
+constexpr int kNumSMs = 152;
+constexpr size_t kSmemBudget = 220 * 1024;
+
+struct Plan {
+  bool ok = false;
+  int N = 0;             // weight rows (output features) per CTA slab
+  int S = 1;             // K splits
+  int kb_per_split = 0;  // 64-wide k blocks per split
+  int kblocks = 0;
+  int n_mt = 1;          // 128-row M-tiles per CTA
+  int groups = 1;        // row groups (grid.z)
+  int stages = 2;
+  uint32_t stage_bytes = 0;
+  int tmem_cols = 32;
+};
+
+struct TcParams {
+  int rows = 0, outs = 0, K = 0;
+  int n_mt = 1, xplanes = 1, wplanes = 1, N = 0, kb_per_split = 0, kblocks = 0, stages = 0;
+  uint32_t stage_bytes = 0, tmem_cols = 32;
+  int mode = 0;            // 0: fp32 partials [split][rows][outs]; 1: LM-head records
+  float* part = nullptr;
+  LmRec* rec = nullptr;    // [slabs][rows]
+  float inv_T = 0.f;
+  uint32_t k0 = 0, k1 = 0;
+  const int64_t* pos = nullptr;
+  int K_draft = 1;
+  int* status = nullptr;
+};
+
+// Tensor map of a bf16 row-major [rows, K] matrix, box = 64 (k) x box_rows.
+bool make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows);
+Plan plan(int rows, int outs, int K, int xplanes, int wplanes, bool lm);
+size_t smem_bytes(const Plan& pl);
+cudaError_t launch(const Plan& pl, const CUtensorMap* x0, const CUtensorMap* x1, const CUtensorMap* w0,
+                   const CUtensorMap* w1, TcParams prm, cudaStream_t s);
+
+}  // namespace tc
+}  // namespace dlite

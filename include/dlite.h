@@ -227,6 +227,17 @@ int dlite_stage_times(dlite_handle *h, int B, const void *hidden, const int32_t 
                       int32_t *next_anchor, float *times_ms, const char **names, int cap,
                       dlite_stream_t stream);
 
+/* Diagnostic: one tensor-core product through the same engine the round uses,
+ * part[z][r][o] = sum over k-split z of X[r, :] . W[o, :], with X given as 1 or
+ * 2 bf16 planes [x_rows, K] (x_rows a multiple of 128, >= rows) and W as 1 or 2
+ * bf16 planes [outs, K]; K a multiple of 64, outs a multiple of 8. `part` must
+ * hold 16 * rows * outs floats; the sum over the returned number of splits
+ * (> 0) is the product. `status` is a device int receiving DLITE_DEV_* bits.
+ * Returns the split count or a negative DLITE_ERR_*. */
+int dlite_selftest_gemm(int rows, int outs, int K, int xplanes, int wplanes, const void *X0,
+                        const void *X1, int x_rows, const void *W0, const void *W1, float *part,
+                        int *status, dlite_stream_t stream);
+
 /* Number of kernels the last draft+verify path enqueues for batch B
  * (greedy when temperature == 0), for launch accounting. */
 int dlite_launch_count(dlite_handle *h, int B, float temperature);
