@@ -135,12 +135,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t full0 = su32(bars), empty0 = su32(bars + p.stages), accf = su32(bars + 2 * p.stages);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // After any bounded wait has expired on this device, later CTAs skip their
+  // work (and only allocate / free TMEM) so a broken launch ends quickly.
+  const bool aborted = p.status && (*(volatile int*)p.status & kDevTimeout);
   const int o0 = blockIdx.x * p.N;
   const int split = blockIdx.y;
   const int m0 = blockIdx.z * p.n_mt * 128;
   const int kb0 = split * p.kb_per_split;
   const int kb1 = min(kb0 + p.kb_per_split, p.kblocks);
-  const int nkb = kb1 - kb0;
+  const int nkb = aborted ? 0 : kb1 - kb0;
   const uint32_t wtile = (uint32_t)p.N * 128u;
 
   if (threadIdx.x == 0) {
