@@ -63,12 +63,17 @@ class ClockSampler:
         self.lines = []
 
     def start(self):
+        """Start sampling; returns once the sampler is up (its start-up is kept out of the timed region)."""
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
                  "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            t0 = time.time()
+            while len(self.lines) < 3 and time.time() - t0 < 10:
+                time.sleep(0.05)
+            self.skip = len(self.lines)
         except Exception:
             self.proc = None
 
@@ -86,7 +91,7 @@ class ClockSampler:
             self.proc.kill()
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in self.lines:
+        for l in self.lines[getattr(self, "skip", 0):]:
             f = [x.strip() for x in l.split(",")]
             if len(f) < 9:
                 continue
@@ -162,11 +167,13 @@ def run_gpu(args):
         graphs.append(g)
     launches_per_step = dr.launch_count(B, T) + 1   # + the position bookkeeping kernel
 
+    ncommit_total = torch.zeros((), dtype=torch.int64, device=dev)
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
             graphs[i % RING].replay()
+            ncommit_total += out["n_commit"].sum()   # the same ops as the timed loop
     stream.synchronize()
-    ncommit_total = torch.zeros((), dtype=torch.int64, device=dev)
+    ncommit_total.zero_()
 
     def barrier():
         if ws > 1:
@@ -174,20 +181,24 @@ def run_gpu(args):
             dist.barrier()
         torch.cuda.synchronize()
 
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(local) if not args.no_clock_sampler else None
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     barrier()
-    clocks.start()
-    time.sleep(0.3)
+    if clocks:
+        clocks.start()
+    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     with torch.cuda.stream(stream):
         ev0.record(stream)
+        step_ev[0].record(stream)
         for i in range(args.steps):
             graphs[i % RING].replay()
             ncommit_total += out["n_commit"].sum()
+            step_ev[i + 1].record(stream)
         ev1.record(stream)
     stream.synchronize()
-    clk = clocks.stop()
+    clk = clocks.stop() if clocks else {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["not sampled"]}
+    step_ms = sorted(step_ev[i].elapsed_time(step_ev[i + 1]) for i in range(args.steps))
     barrier()
     ms = ev0.elapsed_time(ev1)
     t_s = ms / 1e3
@@ -202,6 +213,7 @@ def run_gpu(args):
         committed = int(cc.item())
     rounds_s = ws * args.steps / t_s
     tok_s = committed / t_s
+    counters = dr.counters(reset=True)
 
     # ---- per-kernel CUDA-event times (eager, same inputs) for the roofline
     per = {}
@@ -260,6 +272,9 @@ def run_gpu(args):
         "roofline": roof,
         "per_kernel_ms": {n: round(v, 4) for n, v in per_launch.items()},
         "gpu_launches": launches_per_step * args.steps,
+        "counters": counters,
+        "step_ms": {"min": round(step_ms[0], 4), "median": round(step_ms[len(step_ms) // 2], 4),
+                    "max": round(step_ms[-1], 4)},
         "clocks": clk,
         "e2e": e2e,
     }
@@ -404,6 +419,7 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="qwen3-8b-b32", choices=sorted(wk.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clock-sampler", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

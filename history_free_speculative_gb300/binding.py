@@ -69,7 +69,9 @@ _SIGS = {
     "dlite_device_status": (_I, [_P, _I, ctypes.POINTER(_I), _P]),
     "dlite_status_string": (ctypes.c_char_p, [_I]),
     "dlite_launch_count": (_I, [_P, _I, _F]),
-    "dlite_selftest_gemm": (_I, [_I, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P, _P]),
+    "dlite_counters": (_I, [_P, _I, ctypes.POINTER(ctypes.c_int64), _P]),
+    "dlite_selftest_gemm": (_I, [_I, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P,
+                                 ctypes.POINTER(ctypes.c_int), _P]),
     "dlite_stage_times": (_I, [_P, _I, _P, _P, _F, _U64, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                _P, ctypes.POINTER(ctypes.c_char_p), _I, _P]),
 }
@@ -124,20 +126,24 @@ def _check(code, what):
         raise DliteError(code, what)
 
 
-def selftest_gemm(X, W, rows=None, stream=None):
+def selftest_gemm(X, W, rows=None, stream=None, plan=None, part=None, outs=None):
     """Tensor-core product X[:rows] @ W^T through the round's GEMM engine.
 
     X, W: lists of 1 or 2 bf16 device planes ([x_rows, K] with x_rows a multiple
-    of 128; [outs, K]). Returns (fp32 [rows, outs] device tensor, status).
+    of 128; W in the tiled weight layout, rows padded to 64). Returns
+    (fp32 [rows, outs] device tensor, status).
     """
     lib = load()
     rows = X[0].shape[0] if rows is None else rows
-    outs, K = W[0].shape
-    part = torch.zeros(16 * rows * outs, dtype=torch.float32, device=X[0].device)
+    wrows, K = W[0].shape
+    outs = wrows if outs is None else outs
+    if part is None:
+        part = torch.zeros(16 * rows * outs, dtype=torch.float32, device=X[0].device)
     st = torch.zeros(1, dtype=torch.int32, device=X[0].device)
+    ov = (ctypes.c_int * 3)(*plan) if plan is not None else None
     S = lib.dlite_selftest_gemm(rows, outs, K, len(X), len(W), _ptr(X[0]),
                                 _ptr(X[1]) if len(X) > 1 else None, X[0].shape[0], _ptr(W[0]),
-                                _ptr(W[1]) if len(W) > 1 else None, _ptr(part), _ptr(st),
+                                _ptr(W[1]) if len(W) > 1 else None, _ptr(part), _ptr(st), ov,
                                 _stream(stream))
     if S < 0:
         raise DliteError(S, "dlite_selftest_gemm")
@@ -265,6 +271,13 @@ class Drafter:
         if n < 0:
             raise DliteError(n, "dlite_stage_times")
         return [(names[i].decode(), times[i]) for i in range(min(n, cap))]
+
+    def counters(self, reset=False, stream=None):
+        """Sampling-verify counters: residual draws, proposals, fallbacks, bonus draws."""
+        out = (ctypes.c_int64 * 5)()
+        _check(self.lib.dlite_counters(self.h, 1 if reset else 0, out, _stream(stream)), "dlite_counters")
+        return dict(residual=out[0], proposals=out[1], fallback=out[2], bonus=out[3],
+                    lm_close_calls=out[4])
 
     def launch_count(self, B, temperature):
         return self.lib.dlite_launch_count(self.h, B, temperature)

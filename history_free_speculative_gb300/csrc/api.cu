@@ -23,6 +23,7 @@ struct LayerW {
 struct MapEntry {
   const void* base;
   int rows, K, box;
+  bool tiled;
   CUtensorMap map;
 };
 
@@ -59,7 +60,9 @@ struct dlite_handle {
   bf16* hp[2] = {nullptr, nullptr};
   float *part = nullptr, *part2 = nullptr;
   LmRec* lmrec = nullptr;
-  double* resid = nullptr;
+  unsigned long long* resid = nullptr;
+  unsigned long long* counters = nullptr;
+  int Vp = 0;  // V padded to a multiple of 64 (tiled LM-head weight rows)
   int* status = nullptr;
 
   // per-kernel event recording (dlite_stage_times)
@@ -117,11 +120,13 @@ int check_config(const dlite_config* c) {
   if (c->L_D < 1 || c->L_D > DLITE_MAX_LAYERS) return DLITE_ERR_UNSUPPORTED_SHAPE;
   if (c->n_q < 1 || c->n_kv < 1 || c->n_q % c->n_kv) return DLITE_ERR_UNSUPPORTED_SHAPE;
   if (c->d_h != 64 && c->d_h != 128) return DLITE_ERR_UNSUPPORTED_SHAPE;
-  if (c->D % 64 || c->F % 64 || c->R % 32 || c->R > 1024 || c->V < 8 || c->V % 8)
+  if (c->D % 64 || c->F % 64 || c->R % 32 || c->R > 1024 || c->V < 8 || c->V % 8 || c->V > 262144)
     return DLITE_ERR_UNSUPPORTED_SHAPE;
   if ((c->n_q * c->d_h) % 64) return DLITE_ERR_UNSUPPORTED_SHAPE;
   const int G = c->n_q / c->n_kv, Tk = c->m + c->K + 1;
   if ((size_t)(G * (c->K + 1) + 2 * Tk) * (c->d_h + 1) * 4 > 96 * 1024) return DLITE_ERR_UNSUPPORTED_SHAPE;
+  if (c->R < 32 || chain_smem_bytes(c->R, chain_group_size(c->R, c->B_max)) > 200 * 1024)
+    return DLITE_ERR_UNSUPPORTED_SHAPE;
   if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return DLITE_ERR_INVALID_ARG;
   return DLITE_OK;
 }
@@ -144,7 +149,8 @@ int repack(dlite_handle* h, const void* src, int rows, int cols, int src_ld, int
     AL(f, n);
     *f32_out = f;
   }
-  CK(launch_repack(src, h->f32, rows, cols, src_ld, off, p0, p1, planes_out ? h->np : 0, f, cols, 0));
+  // planes feed the tensor-core products: tiled layout (rows here are multiples of 64)
+  CK(launch_repack(src, h->f32, rows, cols, src_ld, off, p0, p1, planes_out ? h->np : 0, f, -cols, 0));
   return DLITE_OK;
 }
 
@@ -159,8 +165,9 @@ int stack(dlite_handle* h, const void* const* srcs, const int* rows, int n, int 
   if (h->np == 2) AL(p1, (size_t)total * cols);
   size_t off = 0;
   for (int i = 0; i < n; ++i) {
+    // every piece has a multiple of 64 rows, so the tiled pieces concatenate
     CK(launch_repack(srcs[i], h->f32, rows[i], cols, cols, 0, p0 + off, p1 ? p1 + off : nullptr,
-                     h->np, nullptr, cols, 0));
+                     h->np, nullptr, -cols, 0));
     off += (size_t)rows[i] * cols;
   }
   planes_out[0] = p0;
@@ -186,15 +193,18 @@ Operand opnd(const bf16* const* p, int n, int rows, int K) {
   return o;
 }
 
-const CUtensorMap* get_map(dlite_handle* h, const void* base, int rows, int K, int box) {
+const CUtensorMap* get_map(dlite_handle* h, const void* base, int rows, int K, int box,
+                           bool tiled = false) {
   for (const MapEntry& e : h->maps)
-    if (e.base == base && e.rows == rows && e.K == K && e.box == box) return &e.map;
+    if (e.base == base && e.rows == rows && e.K == K && e.box == box && e.tiled == tiled) return &e.map;
   MapEntry e;
   e.base = base;
   e.rows = rows;
   e.K = K;
   e.box = box;
-  if (!tc::make_map(&e.map, base, rows, K, box)) return nullptr;
+  e.tiled = tiled;
+  if (!(tiled ? tc::make_map_tiled(&e.map, base, rows, K, box) : tc::make_map(&e.map, base, rows, K, box)))
+    return nullptr;
   h->maps.push_back(e);
   return &h->maps.back().map;
 }
@@ -204,11 +214,12 @@ int gemm(dlite_handle* h, const char* name, const Operand& X, const Operand& W, 
          float* part, int* S_out, cudaStream_t s) {
   const tc::Plan pl = tc::plan(rows, outs, X.K, X.n, W.n, false);
   if (!pl.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
+  const int xb = tc::x_box_rows(rows);
   h->maps.reserve(h->maps.size() + 4);
-  const CUtensorMap* x0 = get_map(h, X.p[0], X.rows, X.K, 128);
-  const CUtensorMap* x1 = X.n == 2 ? get_map(h, X.p[1], X.rows, X.K, 128) : nullptr;
-  const CUtensorMap* w0 = get_map(h, W.p[0], W.rows, W.K, pl.N);
-  const CUtensorMap* w1 = W.n == 2 ? get_map(h, W.p[1], W.rows, W.K, pl.N) : nullptr;
+  const CUtensorMap* x0 = get_map(h, X.p[0], X.rows, X.K, xb);
+  const CUtensorMap* x1 = X.n == 2 ? get_map(h, X.p[1], X.rows, X.K, xb) : nullptr;
+  const CUtensorMap* w0 = get_map(h, W.p[0], W.rows, W.K, pl.N, true);
+  const CUtensorMap* w1 = W.n == 2 ? get_map(h, W.p[1], W.rows, W.K, pl.N, true) : nullptr;
   if (!x0 || !w0 || (X.n == 2 && !x1) || (W.n == 2 && !w1)) return DLITE_ERR_CUDA;
   tc::TcParams prm;
   prm.rows = rows;
@@ -217,6 +228,7 @@ int gemm(dlite_handle* h, const char* name, const Operand& X, const Operand& W, 
   prm.xplanes = X.n;
   prm.wplanes = W.n;
   prm.mode = 0;
+  prm.x_box = xb;
   prm.part = part;
   prm.status = h->status;
   if (S_out) *S_out = pl.S;
@@ -238,8 +250,9 @@ void seed_key(uint64_t seed, uint32_t* k0, uint32_t* k1) {
 
 // ---------------------------------------------------------------- stages
 
+// LM head: one bf16 plane of h and of E; the merge re-scores the finalists exactly.
 tc::Plan lm_plan(dlite_handle* h, int rows) {
-  return tc::plan(rows, h->cfg.V, h->cfg.D, 2, h->np, true);
+  return tc::plan(rows, h->cfg.V, h->cfg.D, 1, 1, true);
 }
 
 int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anchor,
@@ -250,6 +263,7 @@ int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anch
   st.hidden = hidden;
   st.anchor = anchor;
   st.E = h->E_src;
+  st.E_tiled = h->f32 ? 0 : 1;
   st.e_depth = h->e_depth;
   st.g_stage = h->g_stage;
   st.e_ph = h->e_ph;
@@ -351,8 +365,8 @@ int run_seq_head(dlite_handle* h, int B, float* tap_hs, cudaStream_t s) {
   const dlite_config& c = h->cfg;
   const int rows = B * c.K;
   int S = 1;
-  RUN(gemm(h, "gemm_head_ce", opnd(h->bp, 2, h->Hcap, c.D), opnd(h->Wce, h->np, 2 * c.R, c.D), rows,
-           2 * c.R, h->part, &S, s));
+  RUN(gemm(h, "gemm_head_ce", opnd(h->bp, 2, h->Hcap, c.D), opnd(h->Wce, h->np, 2 * h->Rp, c.D), rows,
+           2 * h->Rp, h->part, &S, s));
   ChainArgs ch;
   ch.part = h->part;
   ch.S = S;
@@ -365,6 +379,8 @@ int run_seq_head(dlite_handle* h, int B, float* tap_hs, cudaStream_t s) {
   ch.tp[0] = h->tp[0];
   ch.tp[1] = h->tp[1];
   ch.ldt = h->Rp;
+  ch.Rp = h->Rp;
+  ch.Bg = chain_group_size(c.R, B);
   CK(launch_head_chain(ch, s));
   mark(h, "head_chain");
   RUN(gemm(h, "gemm_head_p", opnd(h->tp, 2, h->Hcap, h->Rp), opnd(h->P, h->np, c.D, h->Rp), rows, c.D,
@@ -380,29 +396,47 @@ int run_lm_head(dlite_handle* h, int B, float temperature, uint64_t seed, const 
   const int rows = B * c.K;
   const tc::Plan pl = lm_plan(h, rows);
   if (!pl.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
+  const int xb = tc::x_box_rows(rows);
   h->maps.reserve(h->maps.size() + 4);
-  const CUtensorMap* x0 = get_map(h, h->hp[0], h->Hcap, c.D, 128);
-  const CUtensorMap* x1 = get_map(h, h->hp[1], h->Hcap, c.D, 128);
-  const CUtensorMap* w0 = get_map(h, h->E[0], c.V, c.D, pl.N);
-  const CUtensorMap* w1 = h->np == 2 ? get_map(h, h->E[1], c.V, c.D, pl.N) : nullptr;
-  if (!x0 || !x1 || !w0 || (h->np == 2 && !w1)) return DLITE_ERR_CUDA;
+  const CUtensorMap* x0 = get_map(h, h->hp[0], h->Hcap, c.D, xb);
+  const CUtensorMap* w0 = get_map(h, h->E[0], h->Vp, c.D, pl.N, true);
+  if (!x0 || !w0) return DLITE_ERR_CUDA;
   tc::TcParams prm;
   prm.rows = rows;
   prm.outs = c.V;
   prm.K = c.D;
-  prm.xplanes = 2;
-  prm.wplanes = h->np;
+  prm.xplanes = 1;
+  prm.wplanes = 1;
   prm.mode = 1;
+  prm.x_box = xb;
   prm.rec = h->lmrec;
   prm.inv_T = temperature > 0.f ? 1.f / temperature : 0.f;
   seed_key(seed, &prm.k0, &prm.k1);
   prm.pos = pos;
   prm.K_draft = c.K;
   prm.status = h->status;
-  CK(tc::launch(pl, x0, x1, w0, w1, prm, s));
+  CK(tc::launch(pl, x0, nullptr, w0, nullptr, prm, s));
   mark(h, "lm_head");
-  const int n_tiles = (c.V + pl.N - 1) / pl.N;
-  CK(launch_lm_merge(h->lmrec, n_tiles, rows, c.K, prm.inv_T, cand, qs, s));
+  LmMergeArgs mg;
+  mg.rec = h->lmrec;
+  mg.n_tiles = (c.V + pl.N - 1) / pl.N * tc::kEpiGroups;
+  mg.rows = rows;
+  mg.K = c.K;
+  mg.D = c.D;
+  mg.V = c.V;
+  mg.inv_T = prm.inv_T;
+  mg.k0 = prm.k0;
+  mg.k1 = prm.k1;
+  mg.pos = pos;
+  mg.h = h->hs;
+  if (h->f32)
+    mg.Ef = (const float*)h->E_src;
+  else
+    mg.Eb = h->E[0];
+  mg.cand = cand;
+  mg.qs = qs;
+  mg.counters = h->counters;
+  CK(launch_lm_merge(mg, s));
   mark(h, "lm_merge");
   return DLITE_OK;
 }
@@ -452,13 +486,21 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
   RUN(repack(h, w->g_stage, 1, D, D, 0, nullptr, &h->g_stage));
   RUN(repack(h, w->e_ph, 1, D, D, 0, nullptr, &h->e_ph));
   RUN(repack(h, w->g_final, 1, D, D, 0, nullptr, &h->g_final));
-  if (h->f32) {
+  {  // E planes padded to Vp rows (zero rows past V) for the LM-head tiles
+    bf16* p0 = nullptr;
+    bf16* p1 = nullptr;
+    AL(p0, (size_t)h->Vp * D);
+    CK(cudaMemset(p0, 0, (size_t)h->Vp * D * 2));
+    if (h->np == 2) {
+      AL(p1, (size_t)h->Vp * D);
+      CK(cudaMemset(p1, 0, (size_t)h->Vp * D * 2));
+    }
     float* e32 = nullptr;
-    RUN(repack(h, w->E, V, D, D, 0, h->E, &e32));
-    h->E_src = e32;
-  } else {
-    RUN(repack(h, w->E, V, D, D, 0, h->E, nullptr));
-    h->E_src = h->E[0];
+    if (h->f32) AL(e32, (size_t)V * D);
+    CK(launch_repack(w->E, h->f32, V, D, D, 0, p0, p1, h->np, e32, -D, 0));
+    h->E[0] = p0;
+    h->E[1] = p1;
+    h->E_src = h->f32 ? (const void*)e32 : (const void*)p0;
   }
   for (int l = 0; l < c.L_D; ++l) {
     const dlite_layer_weights& lw = w->layer[l];
@@ -476,14 +518,20 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
     RUN(repack(h, lw.g_attn, 1, D, D, 0, nullptr, &L.g_attn));
     RUN(repack(h, lw.g_ffn, 1, D, D, 0, nullptr, &L.g_ffn));
   }
-  {  // Wce = [Q[:, :D]; Q[:, D:]]
+  {  // Wce = [Q_b; 0; Q_h; 0] = [Q[:, :D] padded to Rp rows; Q[:, D:] padded to Rp rows], tiled
     bf16* p0 = nullptr;
     bf16* p1 = nullptr;
-    AL(p0, (size_t)2 * R * D);
-    if (h->np == 2) AL(p1, (size_t)2 * R * D);
-    CK(launch_repack(w->Q, h->f32, R, D, 2 * D, 0, p0, p1, h->np, nullptr, D, 0));
-    CK(launch_repack(w->Q, h->f32, R, D, 2 * D, D, p0 + (size_t)R * D,
-                     p1 ? p1 + (size_t)R * D : nullptr, h->np, nullptr, D, 0));
+    const size_t n = (size_t)2 * h->Rp * D;
+    AL(p0, n);
+    CK(cudaMemset(p0, 0, n * 2));
+    if (h->np == 2) {
+      AL(p1, n);
+      CK(cudaMemset(p1, 0, n * 2));
+    }
+    const size_t half = (size_t)h->Rp * D;  // Rp rows: a whole number of 64-row tile rows
+    CK(launch_repack(w->Q, h->f32, R, D, 2 * D, 0, p0, p1, h->np, nullptr, -D, 0));
+    CK(launch_repack(w->Q, h->f32, R, D, 2 * D, D, p0 + half, p1 ? p1 + half : nullptr, h->np, nullptr,
+                     -D, 0));
     h->Wce[0] = p0;
     h->Wce[1] = p1;
   }
@@ -496,7 +544,7 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
       AL(p1, (size_t)D * h->Rp);
       CK(cudaMemset(p1, 0, (size_t)D * h->Rp * 2));
     }
-    CK(launch_repack(w->P, h->f32, D, R, R, 0, p0, p1, h->np, nullptr, h->Rp, 0));
+    CK(launch_repack(w->P, h->f32, D, R, R, 0, p0, p1, h->np, nullptr, -h->Rp, 0));
     h->P[0] = p0;
     h->P[1] = p1;
   }
@@ -540,7 +588,7 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
     const int L = B * (c.K + 1), C = B * c.m, H = B * c.K;
     const int sites[6][4] = {{L, h->qd + 2 * h->kvd, D, h->np}, {L, D, h->qd, h->np},
                              {L, 2 * F, D, h->np},               {L, D, F, h->np},
-                             {H, 2 * R, D, 2},                   {H, D, h->Rp, 2}};
+                             {H, 2 * h->Rp, D, 2},               {H, D, h->Rp, 2}};
     for (auto& st : sites) {
       const tc::Plan pl = tc::plan(st[0], st[1], st[2], st[3], h->np, false);
       if (!pl.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
@@ -553,13 +601,15 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
     pe2 = v2 > pe2 ? v2 : pe2;
     const tc::Plan pl = lm_plan(h, H);
     if (!pl.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
-    const size_t v3 = (size_t)((V + pl.N - 1) / pl.N) * H;
+    const size_t v3 = (size_t)((V + pl.N - 1) / pl.N) * tc::kEpiGroups * H;
     lme = v3 > lme ? v3 : lme;
   }
   AL(h->part, pe);
   AL(h->part2, pe2);
   AL(h->lmrec, lme);
   AL(h->resid, (size_t)Bm * V);
+  AL(h->counters, 8);
+  CK(cudaMemset(h->counters, 0, 8 * sizeof(unsigned long long)));
   AL(h->status, 1);
   CK(cudaMemset(h->status, 0, sizeof(int)));
   for (int i = 0; i < 128; ++i) CK(cudaEventCreate(&h->prof_ev[i]));
@@ -599,6 +649,7 @@ int dlite_create(const dlite_config* cfg, const dlite_weights* w, dlite_handle**
   h->qd = cfg->n_q * cfg->d_h;
   h->kvd = cfg->n_kv * cfg->d_h;
   h->Rp = (cfg->R + 63) / 64 * 64;
+  h->Vp = (cfg->V + 63) / 64 * 64;
   h->Lcap = (cfg->B_max * (cfg->K + 1) + 127) / 128 * 128;
   h->Ccap = (cfg->B_max * cfg->m + 127) / 128 * 128;
   h->Hcap = (cfg->B_max * cfg->K + 127) / 128 * 128;
@@ -698,6 +749,7 @@ int dlite_verify_sample(dlite_handle* h, int B, const int32_t* cand, const dlite
   else
     v.Eb = h->E[0];
   v.resid = h->resid;
+  v.counters = h->counters;
   v.T = (double)temperature;
   seed_key(seed, &v.k0, &v.k1);
   v.pos = pos;
@@ -801,29 +853,60 @@ int dlite_stage_times(dlite_handle* h, int B, const void* hidden, const int32_t*
 
 int dlite_selftest_gemm(int rows, int outs, int K, int xplanes, int wplanes, const void* X0,
                         const void* X1, int x_rows, const void* W0, const void* W1, float* part,
-                        int* status, dlite_stream_t stream) {
+                        int* status, const int* plan_override, dlite_stream_t stream) {
   if (rows < 1 || outs < 8 || outs % 8 || K < 64 || K % 64 || xplanes < 1 || xplanes > 2 ||
       wplanes < 1 || wplanes > 2 || !X0 || !W0 || !part || x_rows < rows || x_rows % 128)
     return DLITE_ERR_INVALID_ARG;
   if ((xplanes == 2 && !X1) || (wplanes == 2 && !W1)) return DLITE_ERR_INVALID_ARG;
-  const tc::Plan pl = tc::plan(rows, outs, K, xplanes, wplanes, false);
+  if (xplanes == 1 && wplanes == 2) return DLITE_ERR_INVALID_ARG;  // plane products x0w0 (+x1w0) (+x0w1)
+  tc::Plan pl = tc::plan(rows, outs, K, xplanes, wplanes, false);
   if (!pl.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
+  if (plan_override) {  // {N, S, stages}; 0 keeps the planner's choice
+    if (plan_override[0]) pl.N = plan_override[0];
+    if (plan_override[1]) {
+      pl.S = plan_override[1];
+      pl.kb_per_split = (pl.kblocks + pl.S - 1) / pl.S;
+      pl.S = (pl.kblocks + pl.kb_per_split - 1) / pl.kb_per_split;
+    }
+    pl.stage_bytes = (uint32_t)wplanes * pl.N * 128 + (uint32_t)pl.n_mt * xplanes * tc::a_slot_bytes(tc::x_box_rows(rows));
+    int stmax = (int)((tc::kSmemBudget - 2048 - tc::kTailPad) / pl.stage_bytes);
+    pl.stages = plan_override[2] ? plan_override[2] : (stmax > 8 ? 8 : stmax);
+    int cols = 32;
+    while (cols < pl.N * pl.n_mt) cols <<= 1;
+    pl.tmem_cols = cols;
+    if (pl.N < 64 || pl.N > 256 || pl.N % 64 || pl.N > (outs + 63) / 64 * 64 || pl.N * pl.n_mt > 512 ||
+        pl.stages < 2 ||
+        pl.stages > stmax || pl.S > 16)
+      return DLITE_ERR_INVALID_ARG;
+  }
   CUtensorMap mx0, mx1, mw0, mw1;
-  if (!tc::make_map(&mx0, X0, x_rows, K, 128) || !tc::make_map(&mw0, W0, outs, K, pl.N))
+  const int xb = tc::x_box_rows(rows);
+  const int wrows = (outs + 63) / 64 * 64;
+  if (!tc::make_map(&mx0, X0, x_rows, K, xb) || !tc::make_map_tiled(&mw0, W0, wrows, K, pl.N))
     return DLITE_ERR_CUDA;
-  if (xplanes == 2 && !tc::make_map(&mx1, X1, x_rows, K, 128)) return DLITE_ERR_CUDA;
-  if (wplanes == 2 && !tc::make_map(&mw1, W1, outs, K, pl.N)) return DLITE_ERR_CUDA;
+  if (xplanes == 2 && !tc::make_map(&mx1, X1, x_rows, K, xb)) return DLITE_ERR_CUDA;
+  if (wplanes == 2 && !tc::make_map_tiled(&mw1, W1, wrows, K, pl.N)) return DLITE_ERR_CUDA;
   tc::TcParams prm;
   prm.rows = rows;
   prm.outs = outs;
   prm.K = K;
   prm.xplanes = xplanes;
   prm.wplanes = wplanes;
+  prm.x_box = xb;
   prm.part = part;
   prm.status = status;
   CK(tc::launch(pl, &mx0, xplanes == 2 ? &mx1 : nullptr, &mw0, wplanes == 2 ? &mw1 : nullptr, prm,
                 (cudaStream_t)stream));
   return pl.S;
+}
+
+int dlite_counters(dlite_handle* h, int reset, int64_t* out, dlite_stream_t stream) {
+  if (!h || !out) return DLITE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  CK(cudaMemcpyAsync(out, h->counters, 5 * sizeof(int64_t), cudaMemcpyDeviceToHost, s));
+  if (reset) CK(cudaMemsetAsync(h->counters, 0, 8 * sizeof(int64_t), s));
+  CK(cudaStreamSynchronize(s));
+  return DLITE_OK;
 }
 
 int dlite_launch_count(dlite_handle* h, int B, float temperature) {

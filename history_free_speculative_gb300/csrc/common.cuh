@@ -32,6 +32,17 @@ __device__ __forceinline__ float round_bf16(float x) {
   return __bfloat162float(__float2bfloat16_rn(x));
 }
 
+// ---------------------------------------------------------------- tiled weights
+// Weight matrices that feed the tensor-core products are stored as 64 x 64
+// tiles: element (r, c) of a [rows, cols] matrix (rows padded to a multiple of
+// 64, cols a multiple of 64) sits at tile (r/64, c/64), tiles ordered row-tile
+// major, each tile 64 rows x 64 columns row-major. One k block (64 columns) of
+// a 64-row slab is then one contiguous 8 KB chunk, so a CTA streams its slab
+// from HBM as long sequential runs.
+__host__ __device__ __forceinline__ size_t tiled_index(size_t r, size_t c, size_t cols) {
+  return ((r >> 6) * (cols >> 6) + (c >> 6)) * 4096 + (r & 63) * 64 + (c & 63);
+}
+
 // ---------------------------------------------------------------- Philox4x32-10
 // Salmon, Moraes, Dror & Shaw, "Parallel random numbers: as easy as 1, 2, 3"
 // (SC'11): ten rounds of the 4x32 Philox S-box with the key bumped by the two
@@ -55,8 +66,11 @@ __device__ __forceinline__ uint4 philox(uint32_t c0, uint32_t c1, uint32_t c2, u
       k0 += kPhiloxW0;
       k1 += kPhiloxW1;
     }
-    const uint32_t hi0 = __umulhi(kPhiloxM0, c0), lo0 = kPhiloxM0 * c0;
-    const uint32_t hi1 = __umulhi(kPhiloxM1, c2), lo1 = kPhiloxM1 * c2;
+    // one 32x32 -> 64-bit multiply gives both halves of each product
+    const uint64_t p0 = (uint64_t)kPhiloxM0 * c0;
+    const uint64_t p1 = (uint64_t)kPhiloxM1 * c2;
+    const uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+    const uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
     const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
     c0 = n0;
     c1 = lo1;
@@ -74,8 +88,10 @@ __device__ __forceinline__ double u01d(uint32_t x) {
   return ((double)(x >> 9) + 0.5) * 1.1920928955078125e-07;
 }
 
+// Gumbel noise -log(-log u); the hardware log2 path (relative error ~1e-7 here),
+// used identically by the LM-head pass and its finalist re-scoring.
 __device__ __forceinline__ float gumbel_from_bits(uint32_t x) {
-  return -logf(-logf(u01f(x)));
+  return -__logf(-__logf(u01f(x)));
 }
 
 // ---------------------------------------------------------------- reductions

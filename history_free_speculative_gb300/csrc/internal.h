@@ -9,17 +9,32 @@
 
 namespace dlite {
 
-// LM-head record: the best (score, id) and the LSE partials of one vocabulary
-// slab for one row.
+// LM-head record of one vocabulary slab for one row: the 4 best
+// (score, id) of the slab in descending order (greedy: logit; sampling:
+// logit/T + Gumbel), from the bf16 product, and the slab's LSE partials.
+constexpr int kTopK = 4;
 struct LmRec {
-  float best;   // best score (greedy: logit; sampling: logit/T + Gumbel)
-  int idx;      // its token id
-  float logit;  // the logit of that token
-  float m;      // max of logit/T over the slab (sampling)
-  float s;      // sum of exp(logit/T - m) over the slab (sampling)
+  float sc[kTopK];
+  int id[kTopK];
+  float m;  // max of logit/T over the slab (sampling)
+  float s;  // sum of exp(logit/T - m) over the slab (sampling)
 };
 
-cudaError_t launch_lm_merge(const LmRec* rec, int n_tiles, int rows, int K, float inv_T,
-                            int32_t* cand, dlite_qstats* qs, cudaStream_t s);
+// Merge of the LM-head records and exact re-scoring of the finalists.
+struct LmMergeArgs {
+  const LmRec* rec = nullptr;  // [n_tiles][rows]
+  int n_tiles = 0, rows = 0, K = 0, D = 0, V = 0;
+  float inv_T = 0.f;           // 0 = greedy
+  uint32_t k0 = 0, k1 = 0;
+  const int64_t* pos = nullptr;
+  const float* h = nullptr;    // [rows, D] fp32 head states
+  const bf16* Eb = nullptr;    // exact LM weights (bf16, tiled layout) ...
+  const float* Ef = nullptr;   // ... or fp32
+  int32_t* cand = nullptr;
+  dlite_qstats* qs = nullptr;
+  unsigned long long* counters = nullptr;  // [4] = finalist sets that were close calls
+};
+
+cudaError_t launch_lm_merge(const LmMergeArgs& a, cudaStream_t s);
 
 }  // namespace dlite

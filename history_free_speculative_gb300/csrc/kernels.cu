@@ -64,7 +64,8 @@ __global__ void stage_kernel(StageArgs a) {
     }
     float ss = 0.f;
     for (int d = threadIdx.x; d < D; d += blockDim.x) {
-      const float v = (i == 0) ? ld_elem<T>(a.E, (size_t)tok * D + d) : a.e_ph[d];
+      const float v = (i == 0) ? ld_elem<T>(a.E, a.E_tiled ? tiled_index(tok, d, D) : (size_t)tok * D + d)
+                               : a.e_ph[d];
       sv[d] = v;
       a.x[(size_t)lr * D + d] = v;
       ss += v * v;
@@ -264,50 +265,124 @@ cudaError_t launch_swiglu(const float* part, int S, int rows, int F, bf16* const
 // ---------------------------------------------------------------- K3: sequential head chain
 // With Q = [Q_b | Q_h] and M = Q_h P (R x R), the head h_i = b_i + P t_i has
 // t_1 = tanh(c_1), t_i = tanh(c_i + e_{i-1} + M t_{i-1}) where c_i = Q_b b_i
-// and e_i = Q_h b_i come from one product over all rows. One CTA per request
-// runs the K serial steps with the state t in shared memory.
-__global__ void head_chain_kernel(ChainArgs a) {
+// and e_i = Q_h b_i come from one product over all rows.
+// Persistent cluster kernel: a cluster of kChainCluster CTAs serves a group of
+// Bg requests; CTA k owns rows [k*R/C, (k+1)*R/C) of M, kept in shared memory
+// (transposed, so a warp reads consecutive rows), computes those entries of
+// t_i for every request of the group and writes them into the state buffer
+// of every CTA of the cluster (distributed shared memory). One hardware
+// cluster barrier per step; the state never leaves the chip.
+constexpr int kChainCluster = 8;
+constexpr int kChainThreads = 256;
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t local_addr, uint32_t rank, float v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+
+__global__ void __launch_bounds__(kChainThreads) head_chain_kernel(ChainArgs a) {
   extern __shared__ float sm[];
-  float* tprev = sm;        // [R]
-  float* eprev = sm + a.R;  // [R]
-  const int b = blockIdx.x, R = a.R;
-  const size_t stride = (size_t)a.rows * 2 * R;
+  const int R = a.R, rc = R / kChainCluster;
+  const int Bg = a.Bg;
+  float* Ms = sm;                      // [R][rc]: Ms[s][r] = M[r0 + r][s]
+  float* tbuf = Ms + (size_t)R * rc;   // [2][Bg][R]
+  const uint32_t rank = cluster_ctarank();
+  const int group = blockIdx.x / kChainCluster;
+  const int r0 = (int)rank * rc;
+  {  // this CTA's contiguous slice of M: R * rc floats, float4 loads
+    const float4* src = reinterpret_cast<const float4*>(a.Mt + (size_t)rank * R * rc);
+    float4* dst = reinterpret_cast<float4*>(Ms);
+    const int n4 = R * rc / 4;
+#pragma unroll 8
+    for (int i = threadIdx.x; i < n4; i += blockDim.x) dst[i] = src[i];
+  }
+  const int rl = threadIdx.x % rc, ql = threadIdx.x / rc;  // (row, request) of this thread
+  const int req = group * Bg + ql;
+  const bool active = threadIdx.x < rc * Bg && req < a.B;
+  const size_t stride = (size_t)a.rows * 2 * a.Rp;
+  float e_prev = 0.f;
+  cluster_sync_all();  // every CTA of the cluster is running before any remote store
   for (int i = 0; i < a.K; ++i) {
-    const int row = b * a.K + i;
-    const float* p = a.part + (size_t)row * 2 * R;
-    float tv[4], ev[4];
-    int cnt = 0;
-    for (int r = threadIdx.x; r < R; r += blockDim.x, ++cnt) {
+    float t = 0.f;
+    if (active) {
+      const int row = req * a.K + i;
+      const float* p = a.part + (size_t)row * 2 * a.Rp + r0 + rl;
       float c = 0.f, e = 0.f;
-      for (int s = 0; s < a.S; ++s) {
-        c += p[s * stride + r];
-        e += p[s * stride + R + r];
+      for (int sp = 0; sp < a.S; ++sp) {
+        c += p[sp * stride];
+        e += p[sp * stride + a.Rp];
       }
       float acc = c;
       if (i > 0) {
-        acc += eprev[r];
+        const float* tp = tbuf + ((size_t)((i - 1) & 1) * Bg + ql) * R;
         float mt = 0.f;
-        for (int k = 0; k < R; ++k) mt = fmaf(a.Mt[(size_t)k * R + r], tprev[k], mt);
-        acc += mt;
+#pragma unroll 4
+        for (int k = 0; k < R; k += 4) {
+          const float4 tv = *reinterpret_cast<const float4*>(tp + k);
+          mt = fmaf(Ms[(size_t)k * rc + rl], tv.x, mt);
+          mt = fmaf(Ms[(size_t)(k + 1) * rc + rl], tv.y, mt);
+          mt = fmaf(Ms[(size_t)(k + 2) * rc + rl], tv.z, mt);
+          mt = fmaf(Ms[(size_t)(k + 3) * rc + rl], tv.w, mt);
+        }
+        acc += e_prev + mt;
       }
-      tv[cnt] = tanhf(acc);
-      ev[cnt] = e;
+      t = tanhf(acc);
+      e_prev = e;
+      a.t[(size_t)row * R + r0 + rl] = t;
+      store_planes(a.tp, 2, (size_t)row * a.ldt + r0 + rl, t);
+      const uint32_t laddr = (uint32_t)__cvta_generic_to_shared(
+          tbuf + ((size_t)(i & 1) * Bg + ql) * R + r0 + rl);
+      for (int k = 0; k < kChainCluster; ++k) st_cluster_f32(laddr, (uint32_t)k, t);
     }
-    __syncthreads();
-    cnt = 0;
-    for (int r = threadIdx.x; r < R; r += blockDim.x, ++cnt) {
-      tprev[r] = tv[cnt];
-      eprev[r] = ev[cnt];
-      a.t[(size_t)row * R + r] = tv[cnt];
-      store_planes(a.tp, 2, (size_t)row * a.ldt + r, tv[cnt]);
-    }
-    __syncthreads();
+    cluster_sync_all();
   }
 }
 
 cudaError_t launch_head_chain(const ChainArgs& a, cudaStream_t s) {
-  head_chain_kernel<<<a.B, 256, 2 * a.R * sizeof(float), s>>>(a);
-  return cudaGetLastError();
+  const int rc = a.R / kChainCluster;
+  const int groups = (a.B + a.Bg - 1) / a.Bg;
+  const size_t smem = ((size_t)a.R * rc + 2 * (size_t)a.Bg * a.R) * sizeof(float);
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(head_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         200 * 1024);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(groups * kChainCluster, 1, 1);
+  cfg.blockDim = dim3(kChainThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attrs[1];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = kChainCluster;
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, head_chain_kernel, a);
+}
+
+int chain_group_size(int R, int B) {
+  const int rc = R / kChainCluster;
+  int bg = kChainThreads / rc;
+  if (bg < 1) bg = 1;
+  if (bg > B) bg = B;
+  return bg;
+}
+
+size_t chain_smem_bytes(int R, int Bg) {
+  return ((size_t)R * (R / kChainCluster) + 2 * (size_t)Bg * R) * sizeof(float);
 }
 
 // h = b + sum_s part[s] (the P t_i product), kept in fp32 and as two bf16 planes.
@@ -382,55 +457,132 @@ cudaError_t launch_verify_greedy(const VerifyArgs& a, cudaStream_t s) {
 }
 
 // ---------------------------------------------------------------- K5: sampling verify
+//
+// Inverse CDF by exact integer prefix sums: every weight w(v) >= 0 is taken as
+// the fixed-point integer floor(w(v) * 2^62) (exact for fp32 weights >= 2^-39),
+// so prefix sums are exact and independent of the summation order. The row is
+// cut into segments of 128 ids; segment sums and their prefix live in shared
+// memory; a threshold tau = floor(S * u) is located by a binary search over
+// the segment prefix, then one warp scans the 128 ids of that segment.
+// Result: the smallest v with prefix(v) > tau, i.e. the inverse CDF at u.
 
-// Block-wide inverse CDF over one row for up to 32 thresholds at once:
-// out[j] = smallest v with prefix(v) > u[j] * total, prefix sums in float64.
-// Each thread owns one contiguous chunk; chunk sums are scanned in float64.
-template <typename W>
-__device__ void block_inverse_cdf(W weight, int V, const double* u, int nthr, int* out,
-                                  double* scan) {
-  const int tid = threadIdx.x, nt = blockDim.x;
-  const int chunk = (V + nt - 1) / nt;
-  const int v0 = min(V, tid * chunk), v1 = min(V, v0 + chunk);
-  double mine = 0.0;
-  int lastpos = -1;
-  for (int v = v0; v < v1; ++v) {
-    const double w = weight(v);
-    mine += w;
-    if (w > 0.0) lastpos = v;
-  }
-  scan[tid] = mine;
-  __shared__ int last_any;
-  if (tid == 0) last_any = -1;
-  if (tid < 32) out[tid] = 0x7fffffff;
-  __syncthreads();
-  if (lastpos >= 0) atomicMax(&last_any, lastpos);
-  // inclusive Hillis-Steele scan of chunk sums (nt <= 1024), fixed order
-  for (int off = 1; off < nt; off <<= 1) {
-    const double v = (tid >= off) ? scan[tid - off] : 0.0;
-    __syncthreads();
-    scan[tid] += v;
-    __syncthreads();
-  }
-  const double total = scan[nt - 1];
-  const double start = scan[tid] - mine;
-  for (int j = 0; j < nthr; ++j) {
-    const double tau = u[j] * total;
-    if (start <= tau && tau < start + mine) {
-      double run = start;
-      int hit = lastpos;  // rounding guard: the chunk's last positive id
-      for (int v = v0; v < v1; ++v) {
-        run += weight(v);
-        if (run > tau) {
-          hit = v;
-          break;
-        }
-      }
-      if (hit >= 0) atomicMin(&out[j], hit);
+constexpr int kSeg = 128;
+constexpr int kVerifyThreads = 1024;
+constexpr int kMaxSegs = 2048;  // V <= 262144
+
+__device__ __forceinline__ unsigned long long fix62(float w) {
+  return w > 0.f ? __float2ull_rz(w * 4611686018427387904.0f) : 0ull;  // 2^62
+}
+__device__ __forceinline__ unsigned long long fix62d(double w) {
+  return w > 0.0 ? __double2ull_rz(w * 4611686018427387904.0) : 0ull;
+}
+
+// tau = floor(S * (2y + 1) / 2^24) for the uniform u = (y + 1/2) / 2^23.
+__device__ __forceinline__ unsigned long long scaled_threshold(unsigned long long S, uint32_t x) {
+  const unsigned long long m = 2ull * (x >> 9) + 1ull;
+  const unsigned long long lo = S * m, hi = __umul64hi(S, m);
+  return (hi << 40) | (lo >> 24);
+}
+
+// Loader of 4 consecutive fixed-point weights starting at v (v % 4 == 0).
+struct RowF32 {
+  const float* row;
+  int V;
+  __device__ __forceinline__ void get4(int v, unsigned long long (&w)[4]) const {
+    if (v + 3 < V) {
+      const float4 f = *reinterpret_cast<const float4*>(row + v);
+      w[0] = fix62(f.x); w[1] = fix62(f.y); w[2] = fix62(f.z); w[3] = fix62(f.w);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) w[j] = (v + j < V) ? fix62(row[v + j]) : 0ull;
     }
   }
+};
+struct RowFix {
+  const unsigned long long* row;
+  int V;
+  __device__ __forceinline__ void get4(int v, unsigned long long (&w)[4]) const {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) w[j] = (v + j < V) ? row[v + j] : 0ull;
+  }
+};
+
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// out[j] for thresholds given by 32-bit Philox words xs[j], j < nthr (<= 32).
+// incl: shared [kMaxSegs] scratch. Returns the row total through *total.
+template <typename Row>
+__device__ void block_icdf(const Row& row, int V, const uint32_t* xs, int nthr, int* out,
+                           unsigned long long* incl, unsigned long long* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int nseg = (V + kSeg - 1) / kSeg;
+  // 1) segment sums: one warp per segment, one float4 per lane
+  for (int sg = warp; sg < nseg; sg += nw) {
+    unsigned long long w[4];
+    row.get4(sg * kSeg + lane * 4, w);
+    const unsigned long long t = warp_sum_u64(w[0] + w[1] + w[2] + w[3]);
+    if (lane == 0) incl[sg] = t;
+  }
   __syncthreads();
-  if (tid < nthr && out[tid] == 0x7fffffff) out[tid] = last_any < 0 ? 0 : last_any;
+  // 2) inclusive scan of the segment sums (warp 0, sequential chunks of 32)
+  if (warp == 0) {
+    unsigned long long carry = 0;
+    for (int base = 0; base < nseg; base += 32) {
+      const int i = base + lane;
+      unsigned long long v = (i < nseg) ? incl[i] : 0ull;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+      }
+      if (i < nseg) incl[i] = v + carry;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane == 0) *total = carry;
+  }
+  __syncthreads();
+  const unsigned long long S = *total;
+  // 3) one warp per threshold
+  for (int j = warp; j < nthr; j += nw) {
+    const unsigned long long tau = scaled_threshold(S, xs[j]);
+    // first segment with incl > tau (exists when S > 0)
+    int lo = 0, hi = nseg - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (incl[mid] > tau) hi = mid; else lo = mid + 1;
+    }
+    const unsigned long long before = lo > 0 ? incl[lo - 1] : 0ull;
+    unsigned long long w[4];
+    row.get4(lo * kSeg + lane * 4, w);
+    const unsigned long long mine = w[0] + w[1] + w[2] + w[3];
+    unsigned long long pre = mine;  // inclusive scan over lanes
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long u = __shfl_up_sync(0xffffffffu, pre, o);
+      if (lane >= o) pre += u;
+    }
+    const unsigned long long start = before + pre - mine;
+    const unsigned ball = __ballot_sync(0xffffffffu, start + mine > tau);
+    int v = V - 1;
+    if (ball) {
+      const int L = __ffs(ball) - 1;
+      if (lane == L) {
+        unsigned long long c = start;
+        int k = 0;
+        for (; k < 3; ++k) {
+          c += w[k];
+          if (c > tau) break;
+        }
+        out[j] = min(lo * kSeg + lane * 4 + k, V - 1);
+      }
+    } else if (lane == 0) {
+      out[j] = v;  // unreachable when S > 0
+    }
+  }
   __syncthreads();
 }
 
@@ -439,23 +591,35 @@ __device__ __forceinline__ float row_dot(const VerifyArgs& a, int v, const float
   float acc = 0.f;
   if (a.Ef) {
     const float* e = a.Ef + (size_t)v * a.D;
-    for (int d = lane; d < a.D; d += 32) acc = fmaf(e[d], h[d], acc);
+    for (int d = lane * 4; d < a.D; d += 128) {
+      const float4 ev = *reinterpret_cast<const float4*>(e + d);
+      const float4 hv = *reinterpret_cast<const float4*>(h + d);
+      acc = fmaf(ev.x, hv.x, fmaf(ev.y, hv.y, fmaf(ev.z, hv.z, fmaf(ev.w, hv.w, acc))));
+    }
   } else {
-    const bf16* e = a.Eb + (size_t)v * a.D;
-    for (int d = lane; d < a.D; d += 32) acc = fmaf(__bfloat162float(e[d]), h[d], acc);
+    for (int d = lane * 4; d < a.D; d += 128) {
+      const uint2 raw = *reinterpret_cast<const uint2*>(a.Eb + tiled_index(v, d, a.D));
+      const __nv_bfloat162 e01 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+      const __nv_bfloat162 e23 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+      const float4 hv = *reinterpret_cast<const float4*>(h + d);
+      acc = fmaf(__low2float(e01), hv.x, acc);
+      acc = fmaf(__high2float(e01), hv.y, acc);
+      acc = fmaf(__low2float(e23), hv.z, acc);
+      acc = fmaf(__high2float(e23), hv.w, acc);
+    }
   }
   return warp_sum(acc);
 }
 
-// One CTA per request.
-__global__ void verify_sample_kernel(VerifyArgs a) {
-  extern __shared__ double dsm[];  // [blockDim.x] scan scratch
+// One CTA (1024 threads) per request.
+__global__ void __launch_bounds__(kVerifyThreads) verify_sample_kernel(VerifyArgs a) {
+  __shared__ unsigned long long incl[kMaxSegs];
+  __shared__ unsigned long long total;
+  __shared__ uint32_t xs[kProposals];      // inverse-CDF words of the proposals
+  __shared__ double sacc[kProposals];      // acceptance uniforms of the proposals
+  __shared__ double qv[kProposals];        // q(v_j) of the proposals
+  __shared__ int sv[kProposals];
   __shared__ int sA, stok;
-  __shared__ double su[kProposals];  // inverse-CDF uniforms (proposal draws)
-  __shared__ double sacc[kProposals];  // acceptance uniforms of the proposals
-  __shared__ double qv[kProposals];  // q(v_j) of the proposals
-  __shared__ int sv[32];
-  __shared__ double rs;
   const int b = blockIdx.x, K = a.K, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nwarps = blockDim.x >> 5;
   const double T = a.T;
@@ -483,23 +647,24 @@ __global__ void verify_sample_kernel(VerifyArgs a) {
   __syncthreads();
   const int A = sA;
   const float* prow = prow_base + (size_t)A * a.V;
+  const RowF32 prow_fix{prow, a.V};
   if (A == K) {
     if (threadIdx.x == 0) {
-      const uint4 w = philox(0u, pos0 + K + 1, (uint32_t)b, kTagBonus, a.k0, a.k1);
-      su[0] = u01d(w.x);
+      xs[0] = philox(0u, pos0 + K + 1, (uint32_t)b, kTagBonus, a.k0, a.k1).x;
+      if (a.counters) atomicAdd(a.counters + 3, 1ull);
     }
     __syncthreads();
-    block_inverse_cdf([&](int v) { return (double)prow[v]; }, a.V, su, 1, sv, dsm);
+    block_icdf(prow_fix, a.V, xs, 1, sv, incl, &total);
     if (threadIdx.x == 0) stok = sv[0];
   } else {
     const uint32_t posA = pos0 + A + 1;
     if (threadIdx.x < kProposals) {
       const uint4 w = philox((uint32_t)threadIdx.x, posA, (uint32_t)b, kTagResid, a.k0, a.k1);
-      su[threadIdx.x] = u01d(w.x);
+      xs[threadIdx.x] = w.x;
       sacc[threadIdx.x] = u01d(w.y);
     }
     __syncthreads();
-    block_inverse_cdf([&](int v) { return (double)prow[v]; }, a.V, su, kProposals, sv, dsm);
+    block_icdf(prow_fix, a.V, xs, kProposals, sv, incl, &total);
     const float* h = a.hs + (size_t)(b * K + A) * a.D;
     const double lse_a = (double)a.qs[b * K + A].lse;
     for (int j = warp; j < kProposals; j += nwarps) {  // one warp per proposal
@@ -508,8 +673,9 @@ __global__ void verify_sample_kernel(VerifyArgs a) {
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-      int tok = -1;
+      int tok = -1, tried = 0;
       for (int j = 0; j < kProposals; ++j) {
+        ++tried;
         const double p = (double)prow[sv[j]];
         if (sacc[j] * p < p - qv[j]) {
           tok = sv[j];
@@ -517,36 +683,27 @@ __global__ void verify_sample_kernel(VerifyArgs a) {
         }
       }
       stok = tok;
+      if (a.counters) {
+        atomicAdd(a.counters + 0, 1ull);
+        atomicAdd(a.counters + 1, (unsigned long long)tried);
+        if (tok < 0) atomicAdd(a.counters + 2, 1ull);
+      }
     }
     __syncthreads();
     if (stok < 0) {
-      // exact fallback: inverse CDF over r(v) = max(0, p(v) - q(v)) for all v
-      double* r = a.resid + (size_t)b * a.V;
+      // exact fallback: inverse CDF over r(v) = max(0, p(v) - q(v)) for all v (rare)
+      unsigned long long* r = a.resid + (size_t)b * a.V;
       for (int v = warp; v < a.V; v += nwarps) {
         const float l = row_dot(a, v, h);
-        if (lane == 0) {
-          const double q = exp((double)l / T - lse_a);
-          const double d = (double)prow[v] - q;
-          r[v] = d > 0.0 ? d : 0.0;
-        }
+        if (lane == 0) r[v] = fix62d((double)prow[v] - exp((double)l / T - lse_a));
       }
       __syncthreads();
-      double part = 0.0;
-      for (int v = threadIdx.x; v < a.V; v += blockDim.x) part += r[v];
-      dsm[threadIdx.x] = part;
+      if (threadIdx.x == 0)
+        xs[0] = philox((uint32_t)kProposals, posA, (uint32_t)b, kTagResid, a.k0, a.k1).x;
       __syncthreads();
-      if (threadIdx.x == 0) {
-        double t = 0.0;
-        for (int i = 0; i < (int)blockDim.x; ++i) t += dsm[i];
-        rs = t;
-        const uint4 w = philox((uint32_t)kProposals, posA, (uint32_t)b, kTagResid, a.k0, a.k1);
-        su[0] = u01d(w.x);
-      }
-      __syncthreads();
-      if (rs > 0.0)
-        block_inverse_cdf([&](int v) { return r[v]; }, a.V, su, 1, sv, dsm);
-      else
-        block_inverse_cdf([&](int v) { return (double)prow[v]; }, a.V, su, 1, sv, dsm);
+      const RowFix rfix{r, a.V};
+      block_icdf(rfix, a.V, xs, 1, sv, incl, &total);
+      if (total == 0ull) block_icdf(prow_fix, a.V, xs, 1, sv, incl, &total);
       if (threadIdx.x == 0) stok = sv[0];
     }
   }
@@ -562,8 +719,7 @@ __global__ void verify_sample_kernel(VerifyArgs a) {
 }
 
 cudaError_t launch_verify_sample(const VerifyArgs& a, cudaStream_t s) {
-  const int threads = 256;
-  verify_sample_kernel<<<a.B, threads, threads * sizeof(double), s>>>(a);
+  verify_sample_kernel<<<a.B, kVerifyThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -581,6 +737,8 @@ cudaError_t launch_advance(int B, const int32_t* n_commit, int64_t* pos, cudaStr
 
 // dst[r][c] = src[r * src_ld + src_off + c] for r < rows, c < cols, converted
 // to bf16 planes (two planes: hi / lo) or to fp32.
+// dst_ld > 0: row-major planes with row stride dst_ld; dst_ld < 0: tiled planes
+// (see tiled_index) with -dst_ld columns.
 template <typename T>
 __global__ void repack_kernel(const T* src, int rows, int cols, int src_ld, int src_off,
                               bf16* p0, bf16* p1, int np, float* f32, int dst_ld) {
@@ -591,7 +749,10 @@ __global__ void repack_kernel(const T* src, int rows, int cols, int src_ld, int 
     const size_t r = i / cols, c = i % cols;
     const float v = to_f32(src[r * src_ld + src_off + c]);
     if (f32) f32[i] = v;
-    if (np) store_planes(pl, np, r * dst_ld + c, v);
+    if (np) {
+      const size_t d = dst_ld > 0 ? r * dst_ld + c : tiled_index(r, c, (size_t)(-dst_ld));
+      store_planes(pl, np, d, v);
+    }
   }
 }
 
@@ -601,7 +762,7 @@ cudaError_t launch_repack(const void* src, bool src_f32, int rows, int cols, int
   const size_t n = (size_t)rows * cols;
   int blocks = (int)((n + 255) / 256);
   if (blocks > 152 * 32) blocks = 152 * 32;
-  if (dst_ld <= 0) dst_ld = cols;
+  if (dst_ld == 0) dst_ld = cols;
   if (src_f32)
     repack_kernel<float><<<blocks, 256, 0, s>>>((const float*)src, rows, cols, src_ld, src_off, p0,
                                                  p1, np, f32, dst_ld);
@@ -611,15 +772,19 @@ cudaError_t launch_repack(const void* src, bool src_f32, int rows, int cols, int
   return cudaGetLastError();
 }
 
-// Mt[s][r] = sum_d Q[r][D + d] * P[d][s]  (M = Q_h P, stored transposed), float64 accumulate.
+// M = Q_h P (R x R), float64 accumulate, stored as kChainCluster contiguous
+// slices: slice k holds rows [k*R/C, (k+1)*R/C) of M transposed,
+// Ms[k][s][r] = M[k*R/C + r][s], the shared-memory image of CTA k of the chain.
 template <typename T>
-__global__ void head_matrix_kernel(const T* Q, const T* P, int D, int R, float* Mt) {
-  const int s = blockIdx.x, r0 = threadIdx.x;
-  for (int r = r0; r < R; r += blockDim.x) {
+__global__ void head_matrix_kernel(const T* Q, const T* P, int D, int R, float* Ms) {
+  const int s = blockIdx.x;
+  const int rc = R / kChainCluster;
+  for (int r = threadIdx.x; r < R; r += blockDim.x) {
     double acc = 0.0;
     for (int d = 0; d < D; ++d)
       acc += (double)to_f32(Q[(size_t)r * 2 * D + D + d]) * (double)to_f32(P[(size_t)d * R + s]);
-    Mt[(size_t)s * R + r] = (float)acc;
+    const int k = r / rc, rl = r % rc;
+    Ms[((size_t)k * R + s) * rc + rl] = (float)acc;
   }
 }
 

@@ -9,6 +9,7 @@ struct StageArgs {
   const void* hidden = nullptr;  // [B, m, D] (f32 or bf16)
   const int32_t* anchor = nullptr;
   const void* E = nullptr;       // [V, D] in the weight dtype (anchor row lookup)
+  int E_tiled = 0;               // E stored in the tiled layout (bf16 weights)
   const float* e_depth = nullptr;
   const float* g_stage = nullptr;
   const float* e_ph = nullptr;
@@ -55,13 +56,15 @@ struct ResNormArgs {
 };
 
 struct ChainArgs {
-  const float* part = nullptr;  // [S][B*K][2R]: c at [0, R), e at [R, 2R)
+  const float* part = nullptr;  // [S][B*K][2Rp]: c at [0, R), e at [Rp, Rp + R)
   int S = 1, rows = 0;
-  const float* Mt = nullptr;    // [R][R], Mt[s][r] = M[r][s]
+  const float* Mt = nullptr;    // M = Q_h P as 8 per-CTA slices [8][R][R/8] (transposed rows)
   int B = 0, K = 0, R = 0;
   float* t = nullptr;           // [B*K, R]
   bf16* tp[2] = {nullptr, nullptr};  // [B*K, ldt] planes (columns R..ldt stay zero)
   int ldt = 0;
+  int Bg = 1;                   // requests per cluster (chain_group_size)
+  int Rp = 0;                   // R padded to 64
 };
 
 struct VerifyArgs {
@@ -71,9 +74,10 @@ struct VerifyArgs {
   const dlite_qstats* qs = nullptr;    // sampling
   const float* hs = nullptr;           // [B*K, D]
   const float* probs = nullptr;        // [B, K+1, V]
-  const bf16* Eb = nullptr;            // E rows for q(v) (bf16 weights)
+  const bf16* Eb = nullptr;            // E rows for q(v) (bf16 weights, tiled layout)
   const float* Ef = nullptr;           // ... or fp32 weights
-  double* resid = nullptr;             // [B, V] fallback scratch
+  unsigned long long* resid = nullptr; // [B, V] fallback scratch (fixed-point residual)
+  unsigned long long* counters = nullptr;  // [4]: residual draws, proposals, fallbacks, bonus
   double T = 0.0;
   uint32_t k0 = 0, k1 = 0;
   const int64_t* pos = nullptr;
@@ -90,6 +94,8 @@ cudaError_t launch_resnorm(const ResNormArgs& a, cudaStream_t s);
 cudaError_t launch_swiglu(const float* part, int S, int rows, int F, bf16* const* o, int no,
                           cudaStream_t s);
 cudaError_t launch_head_chain(const ChainArgs& a, cudaStream_t s);
+int chain_group_size(int R, int B);
+size_t chain_smem_bytes(int R, int Bg);
 cudaError_t launch_head_out(const float* part, int S, int rows, int D, const float* b, float* hs,
                             bf16* const* hp, float* tap, cudaStream_t s);
 cudaError_t launch_split(const float* src, size_t n, bf16* const* pl, float* copy, cudaStream_t s);

@@ -60,6 +60,23 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* st
     }
   }
 }
+// Warp-wide bounded wait: every lane polls, lane 0's view decides, so the
+// result is uniform across the warp.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, int* status) {
+  if (__shfl_sync(0xffffffffu, (int)mbar_try(bar, parity), 0)) return true;
+  const uint64_t t0 = gtimer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (__shfl_sync(0xffffffffu, (int)mbar_try(bar, parity), 0)) return true;
+    const int expired = __shfl_sync(0xffffffffu, (int)(gtimer() - t0 > kTimeoutNs), 0);
+    if (expired) {
+      if ((threadIdx.x & 31) == 0) flag_status(status, kDevTimeout);
+      return false;
+    }
+  }
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int x, int y) {
   asm volatile(
@@ -68,6 +85,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
       : "memory");
 }
+// Weight tile load from the tiled layout: coordinates (0, 0, k block, 64-row slab).
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+      "%4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(0), "r"(0), "r"(c2), "r"(c3)
+      : "memory");
+}
+
 // Shared-memory matrix descriptor: K-major tile, rows of 128 B, 128-byte
 // swizzle, 8-row groups 1024 B apart (stride byte offset), descriptor version 1.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
@@ -115,23 +142,53 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
   return v > bv || (v == bv && i < bi);
 }
+// Insert (x, v) into a descending top-k list (ties: lower id ranks first):
+// replace the last entry, then bubble it up with constant indices only.
+__device__ __forceinline__ void cswap(float (&sc)[kTopK], int (&id)[kTopK], int k) {
+  if (better(sc[k + 1], id[k + 1], sc[k], id[k])) {
+    const float ts = sc[k];
+    const int ti = id[k];
+    sc[k] = sc[k + 1];
+    id[k] = id[k + 1];
+    sc[k + 1] = ts;
+    id[k + 1] = ti;
+  }
+}
+__device__ __forceinline__ void topk_insert(float (&sc)[kTopK], int (&id)[kTopK], float x, int v) {
+  if (!better(x, v, sc[kTopK - 1], id[kTopK - 1])) return;
+  sc[kTopK - 1] = x;
+  id[kTopK - 1] = v;
+#pragma unroll
+  for (int k = kTopK - 2; k >= 0; --k) cswap(sc, id, k);
+}
+
 __device__ __forceinline__ void lse_add(float& m, float& s, float x) {
   if (x > m) {
-    s = s * expf(m - x) + 1.f;
+    s = s * __expf(m - x) + 1.f;
     m = x;
   } else {
-    s += expf(x - m);
+    s += __expf(x - m);
   }
 }
 
+// NMT: M-tiles per CTA; XP / WP: bf16 planes of X / W (products x0w0, + x1w0, + x0w1).
+// The MMA issue loop is fully unrolled over these so the issuing thread only
+// adds precomputed descriptor offsets between tcgen05.mma instructions.
+template <int NMT, int XP, int WP>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap mx0, const __grid_constant__ CUtensorMap mx1,
                    const __grid_constant__ CUtensorMap mw0, const __grid_constant__ CUtensorMap mw1,
                    const TcParams p) {
+  // Shared memory: [barriers | pad to 1 KB] [stage 0] ... [stage S-1] [kTailPad].
+  // Stage: [activation slots: NMT x XP x a_slot] [weight planes: WP x N rows x 128 B].
+  // An activation slot holds only the x_box loaded rows; the 128-row MMA operand
+  // overhangs into the following bytes (stale data feeding only unused TMEM lanes),
+  // and the tail pad keeps that overhang inside the allocation.
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint64_t* bars = (uint64_t*)(smem + (size_t)p.stages * p.stage_bytes);
+  uint8_t* base = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = (uint64_t*)base;
   uint32_t* tmem_holder = (uint32_t*)(bars + 2 * p.stages + 1);
+  uint8_t* smem = base + 1024;
   const uint32_t full0 = su32(bars), empty0 = su32(bars + p.stages), accf = su32(bars + 2 * p.stages);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -144,6 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kb0 = split * p.kb_per_split;
   const int kb1 = min(kb0 + p.kb_per_split, p.kblocks);
   const int nkb = aborted ? 0 : kb1 - kb0;
+  const int rot = nkb > 0 ? (int)(blockIdx.x % (unsigned)nkb) : 0;
   const uint32_t wtile = (uint32_t)p.N * 128u;
 
   if (threadIdx.x == 0) {
@@ -165,64 +223,93 @@ __global__ void __launch_bounds__(kThreads, 1)
   fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  if (warp == 0) {
-    if (lane == 0) {  // ---------------- TMA producer
-      const uint32_t bytes = (uint32_t)p.wplanes * wtile + (uint32_t)(p.n_mt * p.xplanes) * 16384u;
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i % p.stages;
-        const uint32_t it = (uint32_t)(i / p.stages);
-        if (i >= p.stages && !mbar_wait(empty0 + 8 * s, (it - 1) & 1, p.status)) break;
+  // Role loops run with the whole warp converged: every lane waits on the
+  // barrier, one lane issues (a lone active lane beside 31 lanes parked at a
+  // block barrier issues far more slowly).
+  if (warp == 0) {  // ---------------- TMA producer
+    // activation tiles are p.x_box rows tall (only the valid rows when rows < 128; the
+    // rest of the 128-row smem tile holds stale data that only feeds unused TMEM lanes)
+    const uint32_t bytes = (uint32_t)WP * wtile + (uint32_t)(NMT * XP) * (uint32_t)p.x_box * 128u;
+    const uint32_t a_slot = a_slot_bytes(p.x_box);
+    for (int i = 0; i < nkb; ++i) {
+      const int s = i % p.stages;
+      const uint32_t it = (uint32_t)(i / p.stages);
+      if (i >= p.stages && !mbar_wait_warp(empty0 + 8 * s, (it - 1) & 1, p.status)) break;
+      if (lane == 0) {
         const uint32_t st = su32(smem + (size_t)s * p.stage_bytes);
         const uint32_t fb = full0 + 8 * s;
         mbar_expect_tx(fb, bytes);
-        const int kx = (kb0 + i) * 64;
-        tma_load_2d(st, &mw0, fb, kx, o0);
-        if (p.wplanes == 2) tma_load_2d(st + wtile, &mw1, fb, kx, o0);
-        for (int mt = 0; mt < p.n_mt; ++mt)
-          for (int pl = 0; pl < p.xplanes; ++pl)
-            tma_load_2d(st + p.wplanes * wtile + (uint32_t)(mt * p.xplanes + pl) * 16384u,
-                        pl ? &mx1 : &mx0, fb, kx, m0 + mt * 128);
+        // k blocks in a per-CTA rotated order: concurrent CTAs fetch different
+        // activation tiles instead of all hitting the same L2 lines
+        const int kb = kb0 + (i + rot) % nkb;
+        const int kx = kb * 64;
+        const uint32_t wst = st + (uint32_t)(NMT * XP) * a_slot;
+        tma_load_4d(wst, &mw0, fb, kb, o0 >> 6);
+        if (WP == 2) tma_load_4d(wst + wtile, &mw1, fb, kb, o0 >> 6);
+#pragma unroll
+        for (int mt = 0; mt < NMT; ++mt)
+#pragma unroll
+          for (int pl = 0; pl < XP; ++pl)
+            tma_load_2d(st + (uint32_t)(mt * XP + pl) * a_slot, pl ? &mx1 : &mx0, fb, kx, m0 + mt * 128);
       }
+      __syncwarp();
     }
-  } else if (warp == 1) {
-    if (lane == 0) {  // ---------------- MMA issuer
-      const uint32_t idesc = idesc_bf16(128, p.N);
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i % p.stages;
-        const uint32_t it = (uint32_t)(i / p.stages);
-        if (!mbar_wait(full0 + 8 * s, it & 1, p.status)) break;
-        fence_after();
-        const uint32_t sb = su32(smem + (size_t)s * p.stage_bytes);
-#pragma unroll 1
+  } else if (warp == 1) {  // ---------------- MMA issuer
+    constexpr int kCombos = 1 + (XP == 2) + (WP == 2);
+    const uint32_t idesc = idesc_bf16(128, p.N);
+    uint32_t dcol[NMT];
+#pragma unroll
+    for (int mt = 0; mt < NMT; ++mt) dcol[mt] = tmem + (uint32_t)(mt * p.N);
+    const uint32_t a_slot = a_slot_bytes(p.x_box);
+    const uint64_t wdelta = (uint64_t)(wtile >> 4);                      // second weight plane
+    const uint64_t wbase = (uint64_t)(((uint32_t)(NMT * XP) * a_slot) >> 4);  // weights follow the activations
+    const uint64_t aslot = (uint64_t)(a_slot >> 4);
+    const uint64_t desc0 = sw128_desc(su32(smem));
+    const uint64_t sdelta = (uint64_t)(p.stage_bytes >> 4);
+    for (int i = 0; i < nkb; ++i) {
+      const int s = i % p.stages;
+      const uint32_t it = (uint32_t)(i / p.stages);
+      if (!mbar_wait_warp(full0 + 8 * s, it & 1, p.status)) break;
+      fence_after();
+      if (lane == 0) {
+        const uint64_t a0 = desc0 + sdelta * (uint64_t)s;
+        const uint64_t b0 = a0 + wbase;
+        const uint32_t first = i > 0 ? 1u : 0u;
+#pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          for (int mt = 0; mt < p.n_mt; ++mt) {
-            const uint32_t d = tmem + (uint32_t)(mt * p.N);
-            for (int c = 0; c < 3; ++c) {
-              if (c == 1 && p.xplanes < 2) continue;
-              if (c == 2 && p.wplanes < 2) continue;
-              const int px = (c == 1), pw = (c == 2);
-              const uint64_t ad =
-                  sw128_desc(sb + p.wplanes * wtile + (uint32_t)(mt * p.xplanes + px) * 16384u + kk * 32);
-              const uint64_t bd = sw128_desc(sb + pw * wtile + kk * 32);
-              umma_bf16(d, ad, bd, idesc, (i > 0 || kk > 0 || c > 0) ? 1u : 0u);
+#pragma unroll
+          for (int mt = 0; mt < NMT; ++mt) {
+#pragma unroll
+            for (int c = 0; c < kCombos; ++c) {
+              const int px = (XP == 2 && c == 1) ? 1 : 0;
+              const int pw = (WP == 2 && c == kCombos - 1 && c > 0) ? 1 : 0;
+              // +32 B along K inside the 128-byte swizzled row = +2 in the encoded start address
+              const uint64_t ad = a0 + (uint64_t)(kk * 2) + (uint64_t)(mt * XP + px) * aslot;
+              const uint64_t bd = b0 + (uint64_t)(kk * 2) + (pw ? wdelta : 0ull);
+              umma_bf16(dcol[mt], ad, bd, idesc, (kk > 0 || c > 0) ? 1u : first);
             }
           }
         }
         umma_commit(empty0 + 8 * s);
       }
-      umma_commit(accf);
+      __syncwarp();
     }
-  } else {  // ---------------- epilogue warps 2..5
+    if (lane == 0) umma_commit(accf);
+    __syncwarp();
+  } else {  // ---------------- epilogue warps 2 .. 2 + 4 * kEpiGroups - 1
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
-    const bool got = mbar_wait(accf, 0, p.status);
+    const int eg = (warp - 2) >> 2;                 // column group of this warp
+    const int ncol = p.N / kEpiGroups;              // columns per group (multiple of 32)
+    const int c_lo = eg * ncol, c_hi = c_lo + ncol;
+    const bool got = mbar_wait_warp(accf, 0, p.status);
     fence_after();
     if (got) {
-      for (int mt = 0; mt < p.n_mt; ++mt) {
+      for (int mt = 0; mt < NMT; ++mt) {
         const int r = m0 + mt * 128 + q * 32 + lane;
         const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(mt * p.N);
         if (p.mode == 0) {
           float* out = p.part + ((size_t)split * p.rows + r) * p.outs;
-          for (int c = 0; c < p.N; c += 16) {
+          for (int c = c_lo; c < c_hi; c += 16) {
             float v[16];
             tmem_ld16(tbase + c, v);
             if (r < p.rows) {
@@ -235,17 +322,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         } else {
-          // LM head: best (score, id) and LSE partials of this vocabulary slab for row r
+          // LM head: 4 best (score, id) and LSE partials of this vocabulary slab for row r
           const bool sampling = p.inv_T > 0.f;
-          float best = -INFINITY, blogit = 0.f, m = -INFINITY, s = 0.f;
-          int bidx = 0x7fffffff;
+          float sc[kTopK];
+          int id[kTopK];
+#pragma unroll
+          for (int j = 0; j < kTopK; ++j) {
+            sc[j] = -INFINITY;
+            id[j] = 0x7fffffff;
+          }
+          float m = -INFINITY, s = 0.f;
           uint32_t pos = 0, req = 0;
-          if (sampling && r < p.rows) {
+          const bool valid = r < p.rows;
+          if (sampling && valid) {
             req = (uint32_t)(r / p.K_draft);
             pos = (uint32_t)(p.pos[req] + (r % p.K_draft) + 1);
           }
-          const bool valid = r < p.rows;
-          for (int c = 0; c < p.N; c += 16) {
+          for (int c = c_lo; c < c_hi; c += 16) {
             float v[16];
             tmem_ld16(tbase + c, v);  // warp-collective: executed by every lane
             if (valid) {
@@ -253,41 +346,36 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int g = 0; g < 16; g += 4) {
                 const int v0 = o0 + c + g;  // multiple of 4: one Philox call per group
                 if (v0 < p.outs) {          // outs is a multiple of 8: whole groups only
-                  if (!sampling) {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                      if (better(v[g + j], v0 + j, best, bidx)) {
-                        best = v[g + j];
-                        bidx = v0 + j;
-                        blogit = v[g + j];
-                      }
-                  } else {
+                  float x[4];
+                  if (sampling) {
                     const uint4 w = philox((uint32_t)v0 >> 2, pos, req, kTagGumbel, p.k0, p.k1);
                     const uint32_t wx[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                       const float lt = v[g + j] * p.inv_T;
-                      const float sc = lt + gumbel_from_bits(wx[j]);
-                      if (better(sc, v0 + j, best, bidx)) {
-                        best = sc;
-                        bidx = v0 + j;
-                        blogit = v[g + j];
-                      }
+                      x[j] = lt + gumbel_from_bits(wx[j]);
                       lse_add(m, s, lt);
                     }
+                  } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) x[j] = v[g + j];
                   }
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) topk_insert(sc, id, x[j], v0 + j);
                 }
               }
             }
           }
-          if (r < p.rows) {
+          if (valid) {
             LmRec rec;
-            rec.best = best;
-            rec.idx = bidx;
-            rec.logit = blogit;
+#pragma unroll
+            for (int j = 0; j < kTopK; ++j) {
+              rec.sc[j] = sc[j];
+              rec.id[j] = id[j];
+            }
             rec.m = m;
             rec.s = s;
-            p.rec[(size_t)blockIdx.x * p.rows + r] = rec;
+            p.rec[((size_t)blockIdx.x * kEpiGroups + eg) * p.rows + r] = rec;
           }
         }
       }
@@ -336,6 +424,21 @@ bool make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_map_tiled(CUtensorMap* m, const void* base, int rows, int K, int box_rows) {
+  EncodeTiledFn fn = encoder();
+  if (!fn || !base || ((uintptr_t)base & 15) || K % 64 || rows % 64 || box_rows % 64 || box_rows < 64 ||
+      box_rows > 256 || rows < box_rows)
+    return false;
+  const int kb = K / 64;
+  cuuint64_t dims[4] = {64, 64, (cuuint64_t)kb, (cuuint64_t)(rows / 64)};
+  cuuint64_t strides[3] = {128, 8192, (cuuint64_t)kb * 8192};
+  cuuint32_t box[4] = {64, 64, 1, (cuuint32_t)(box_rows / 64)};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 static int next_pow2_cols(int c) {
   int n = 32;
   while (n < c) n <<= 1;
@@ -350,15 +453,14 @@ Plan plan(int rows, int outs, int K, int xplanes, int wplanes, bool lm) {
   const double bw_total = 6.5e12, l2_total = 1.6e13, mma_sm = 1.8e15 / kNumSMs;
   double best_t = 1e30;
   const int combos = 1 + (xplanes == 2) + (wplanes == 2);
-  const int nmax_out = ((outs + 15) / 16) * 16;
+  const int nmax_out = ((outs + 63) / 64) * 64;  // tiled weights: rows padded to 64
   for (int gmax = 4; gmax >= 1; gmax >>= 1) {
     const int groups = (mt_total + gmax - 1) / gmax;
     const int n_mt = (mt_total + groups - 1) / groups;
-    for (int N = 16; N <= 256; N += 16) {
-      if (N * n_mt > 512 || N > nmax_out) continue;
-      if (N > outs) continue;
-      const uint32_t sb = (uint32_t)wplanes * N * 128 + (uint32_t)n_mt * xplanes * 16384;
-      int stages = (int)((kSmemBudget - 2048) / sb);
+    for (int N = 64; N <= 256; N += 64) {
+      if (N * n_mt > 512 || N > nmax_out) continue;  // weight buffers hold >= nmax_out rows
+      const uint32_t sb = (uint32_t)wplanes * N * 128 + (uint32_t)n_mt * xplanes * a_slot_bytes(x_box_rows(rows));
+      int stages = (int)((kSmemBudget - 2048 - kTailPad) / sb);
       if (stages > 8) stages = 8;
       if (stages < 2) continue;
       const int slabs = (outs + N - 1) / N;
@@ -375,7 +477,7 @@ Plan plan(int rows, int outs, int K, int xplanes, int wplanes, bool lm) {
         double l2_sm = l2_total / active;  // activation tiles come from L2, shared by all CTAs
         if (l2_sm > 1.5e11) l2_sm = 1.5e11;
         const double t_load = (double)wplanes * N * 128 / bw_sm;
-        const double t_l2 = (double)n_mt * xplanes * 16384 / l2_sm;
+        const double t_l2 = (double)n_mt * xplanes * x_box_rows(rows) * 128 / l2_sm;
         const double t_mma = (double)n_mt * combos * 128.0 * N * 64 * 2 / mma_sm;
         double t_kb = t_load > t_mma ? t_load : t_mma;
         t_kb = (t_kb > t_l2 ? t_kb : t_l2) + 3.0e-8;
@@ -401,17 +503,42 @@ Plan plan(int rows, int outs, int K, int xplanes, int wplanes, bool lm) {
 }
 
 size_t smem_bytes(const Plan& pl) {
-  return 1024 + (size_t)pl.stages * pl.stage_bytes + 8 * (2 * pl.stages + 1) + 16;
+  return 1024 /* align */ + 1024 /* barriers */ + (size_t)pl.stages * pl.stage_bytes + kTailPad;
+}
+
+typedef void (*KernelFn)(const __grid_constant__ CUtensorMap, const __grid_constant__ CUtensorMap,
+                         const __grid_constant__ CUtensorMap, const __grid_constant__ CUtensorMap,
+                         const TcParams);
+
+template <int NMT>
+static KernelFn pick_planes(int xp, int wp) {
+  if (xp == 1 && wp == 1) return tc_gemm_kernel<NMT, 1, 1>;
+  if (xp == 2 && wp == 1) return tc_gemm_kernel<NMT, 2, 1>;
+  if (xp == 2 && wp == 2) return tc_gemm_kernel<NMT, 2, 2>;
+  return nullptr;
+}
+
+static KernelFn pick(int nmt, int xp, int wp) {
+  switch (nmt) {
+    case 1: return pick_planes<1>(xp, wp);
+    case 2: return pick_planes<2>(xp, wp);
+    case 3: return pick_planes<3>(xp, wp);
+    case 4: return pick_planes<4>(xp, wp);
+    default: return nullptr;
+  }
 }
 
 cudaError_t launch(const Plan& pl, const CUtensorMap* x0, const CUtensorMap* x1, const CUtensorMap* w0,
                    const CUtensorMap* w1, TcParams prm, cudaStream_t s) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(kSmemBudget + 2048));
+  KernelFn fn = pick(pl.n_mt, prm.xplanes, prm.wplanes);
+  if (!fn) return cudaErrorInvalidValue;
+  static bool attr[5][3] = {};
+  const int pi = prm.xplanes == 1 ? 0 : (prm.wplanes == 1 ? 1 : 2);
+  if (!attr[pl.n_mt][pi]) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBudget);
     if (e != cudaSuccess) return e;
-    attr = true;
+    attr[pl.n_mt][pi] = true;
   }
   prm.N = pl.N;
   prm.n_mt = pl.n_mt;
@@ -421,7 +548,7 @@ cudaError_t launch(const Plan& pl, const CUtensorMap* x0, const CUtensorMap* x1,
   prm.stage_bytes = pl.stage_bytes;
   prm.tmem_cols = (uint32_t)pl.tmem_cols;
   dim3 grid((prm.outs + pl.N - 1) / pl.N, pl.S, pl.groups);
-  tc_gemm_kernel<<<grid, kThreads, smem_bytes(pl), s>>>(*x0, x1 ? *x1 : *x0, *w0, w1 ? *w1 : *w0, prm);
+  fn<<<grid, kThreads, smem_bytes(pl), s>>>(*x0, x1 ? *x1 : *x0, *w0, w1 ? *w1 : *w0, prm);
   return cudaGetLastError();
 }
 

@@ -8,9 +8,11 @@
 namespace dlite {
 namespace tc {
 
-constexpr int kThreads = 192;
+constexpr int kEpiGroups = 2;                    // epilogue warp groups (each 4 warps)
+constexpr int kThreads = 64 + 128 * kEpiGroups;  // TMA warp, MMA warp, epilogue warps
 constexpr int kNumSMs = 152;
-constexpr size_t kSmemBudget = 220 * 1024;
+constexpr size_t kSmemBudget = 226 * 1024;  // dynamic shared memory per CTA (all of it)
+constexpr size_t kTailPad = 16 * 1024;      // overhang room for a 128-row operand read
 
 struct Plan {
   bool ok = false;
@@ -29,9 +31,10 @@ struct TcParams {
   int rows = 0, outs = 0, K = 0;
   int n_mt = 1, xplanes = 1, wplanes = 1, N = 0, kb_per_split = 0, kblocks = 0, stages = 0;
   uint32_t stage_bytes = 0, tmem_cols = 32;
+  int x_box = 128;         // rows of each activation tile load (<= 128, multiple of 8)
   int mode = 0;            // 0: fp32 partials [split][rows][outs]; 1: LM-head records
   float* part = nullptr;
-  LmRec* rec = nullptr;    // [slabs][rows]
+  LmRec* rec = nullptr;    // [slabs * kEpiGroups][rows]
   float inv_T = 0.f;
   uint32_t k0 = 0, k1 = 0;
   const int64_t* pos = nullptr;
@@ -41,7 +44,14 @@ struct TcParams {
 
 // Tensor map of a bf16 row-major [rows, K] matrix, box = 64 (k) x box_rows.
 bool make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows);
+// Tensor map of a bf16 weight in the tiled layout (rows a multiple of 64), box = one
+// k block of box_rows (a multiple of 64) rows.
+bool make_map_tiled(CUtensorMap* m, const void* base, int rows, int K, int box_rows);
 Plan plan(int rows, int outs, int K, int xplanes, int wplanes, bool lm);
+// Rows of the activation tile loads: the valid rows (rounded to 8) when they fit one tile.
+inline int x_box_rows(int rows) { return rows >= 128 ? 128 : ((rows + 7) / 8) * 8; }
+// Shared-memory slot of one activation tile: the loaded rows, rounded to a 1 KB swizzle atom group.
+__host__ __device__ inline uint32_t a_slot_bytes(int x_box) { return (uint32_t)((x_box * 128 + 1023) / 1024 * 1024); }
 size_t smem_bytes(const Plan& pl);
 cudaError_t launch(const Plan& pl, const CUtensorMap* x0, const CUtensorMap* x1, const CUtensorMap* w0,
                    const CUtensorMap* w1, TcParams prm, cudaStream_t s);

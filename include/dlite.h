@@ -64,7 +64,7 @@ typedef struct {
     int n_q, n_kv, d_h; /* attention heads; n_q % n_kv == 0; d_h in {64, 128} */
     int F;            /* SwiGLU inner width; multiple of 64 */
     int R;            /* sequential-head rank; multiple of 32, <= 1024 */
-    int V;            /* vocabulary (tied embedding / LM head) */
+    int V;            /* vocabulary (tied embedding / LM head); multiple of 8, <= 262144 */
     int dtype;        /* DLITE_F32 or DLITE_BF16: type of all weights and of `hidden` */
     float rms_eps;    /* RMSNorm epsilon (1e-6) */
     float rope_theta; /* RoPE base (1e6) */
@@ -230,13 +230,25 @@ int dlite_stage_times(dlite_handle *h, int B, const void *hidden, const int32_t 
 /* Diagnostic: one tensor-core product through the same engine the round uses,
  * part[z][r][o] = sum over k-split z of X[r, :] . W[o, :], with X given as 1 or
  * 2 bf16 planes [x_rows, K] (x_rows a multiple of 128, >= rows) and W as 1 or 2
- * bf16 planes [outs, K]; K a multiple of 64, outs a multiple of 8. `part` must
+ * bf16 planes of [outs, K] in the library's tiled weight layout: rows padded with
+ * zeros to a multiple of 64, stored as 64 x 64 tiles, tile (i, j) = rows 64i.., columns
+ * 64j.., tiles in row-tile-major order, each tile row-major (two W planes need two
+ * X planes); K a multiple of 64, outs a multiple of 8. `part` must
  * hold 16 * rows * outs floats; the sum over the returned number of splits
  * (> 0) is the product. `status` is a device int receiving DLITE_DEV_* bits.
+ * plan_override: NULL, or host int[3] {slab width N, k splits, pipeline
+ * stages} (0 = planner's choice) for tiling sweeps.
  * Returns the split count or a negative DLITE_ERR_*. */
 int dlite_selftest_gemm(int rows, int outs, int K, int xplanes, int wplanes, const void *X0,
                         const void *X1, int x_rows, const void *W0, const void *W1, float *part,
-                        int *status, dlite_stream_t stream);
+                        int *status, const int *plan_override, dlite_stream_t stream);
+
+/* Counters since creation or the last reset, copied to host memory out[5]:
+ * [0] residual draws, [1] proposals evaluated, [2] residual draws that needed
+ * the exact inverse-CDF fallback, [3] bonus draws (sampling verification);
+ * [4] LM-head rows whose 4 finalists were within 0.02 (score units) of each
+ * other. Synchronises `stream`; reset != 0 zeroes them. */
+int dlite_counters(dlite_handle *h, int reset, int64_t *out, dlite_stream_t stream);
 
 /* Number of kernels the last draft+verify path enqueues for batch B
  * (greedy when temperature == 0), for launch accounting. */

@@ -23,8 +23,17 @@ CASES = [
     (256, 2048, 1024, 1, 1),    # B=32 local rows
     (448, 512, 256, 1, 1),      # 4 M-tiles in one CTA
     (600, 264, 128, 1, 1),      # 5 M-tiles: two row groups; outs not a multiple of 16
-    (129, 200, 192, 1, 2),      # ragged rows / outs, k = 3 blocks, two weight planes
+    (129, 200, 192, 2, 2),      # ragged rows / outs, k = 3 blocks, two planes on both sides
 ]
+
+
+def _tiled(w):
+    """The library's tiled weight layout: rows padded to 64, 64 x 64 row-major tiles."""
+    rows, K = w.shape
+    rp = (rows + 63) // 64 * 64
+    wp = torch.zeros(rp, K, dtype=w.dtype, device=w.device)
+    wp[:rows] = w
+    return wp.view(rp // 64, 64, K // 64, 64).permute(0, 2, 1, 3).contiguous().view(rp, K)
 
 
 def _planes(x, n):
@@ -44,7 +53,7 @@ def test_engine_matches_float64(rows, outs, K, xp, wp):
     W = torch.randn(outs, K, generator=g) * 0.05
     Xp = [p.to(DEV) for p in _planes(X, xp)]
     Wp = [p.to(DEV) for p in _planes(W, wp)]
-    got, st = binding.selftest_gemm(Xp, Wp, rows=rows)
+    got, st = binding.selftest_gemm(Xp, [_tiled(p) for p in Wp], rows=rows, outs=outs)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     x64 = [p[:rows].double().cpu().numpy() for p in Xp]
