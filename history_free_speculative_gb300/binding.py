@@ -65,6 +65,8 @@ _SIGS = {
     "dlite_verify": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P]),
     "dlite_verify_sample": (_I, [_P, _I, _P, _P, _P, _P, _F, _U64, _P, _P, _P, _P, _P, _P]),
     "dlite_advance": (_I, [_P, _I, _P, _P, _P]),
+    "dlite_verify_sample_static": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _F, _U64, _P, _P, _P,
+                                        _P, _P, _P]),
     "dlite_round_host": (_I, [_P, _I, _P, _P, _P, _P, _P, _F, _U64, _P, _P, _P, _P, _P]),
     "dlite_device_status": (_I, [_P, _I, ctypes.POINTER(_I), _P]),
     "dlite_status_string": (ctypes.c_char_p, [_I]),
@@ -148,6 +150,18 @@ def selftest_gemm(X, W, rows=None, stream=None, plan=None, part=None, outs=None)
     if S < 0:
         raise DliteError(S, "dlite_selftest_gemm")
     return part[:S * rows * outs].view(S, rows, outs).sum(0), st
+
+
+def verify_sample_static(cand, qstats, hs, E, probs, temperature, seed, pos, accepted, commits,
+                         n_commit, next_anchor, stream=None):
+    """Allocation-free sampling verification (no handle; E float32 row-major [V, D])."""
+    lib = load()
+    B, K = cand.shape
+    V, D = E.shape
+    _check(lib.dlite_verify_sample_static(B, K, V, D, _ptr(cand), _ptr(qstats), _ptr(hs), _ptr(E),
+                                          _ptr(probs), temperature, seed, _ptr(pos), _ptr(accepted),
+                                          _ptr(commits), _ptr(n_commit), _ptr(next_anchor),
+                                          _stream(stream)), "dlite_verify_sample_static")
 
 
 def config_struct(cfg, B_max):

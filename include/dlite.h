@@ -188,6 +188,28 @@ int dlite_verify_sample(dlite_handle *h, int B, const int32_t *candidates,
                         int32_t *commits, int32_t *n_commit, int32_t *next_anchor,
                         dlite_stream_t stream);
 
+/* Allocation-free sampling verification (no counterpart on the method's pages;
+ * a library convenience). Same computation and outputs as dlite_verify_sample,
+ * without a handle and without allocating: for callers that cannot allocate
+ * device memory where they verify (allocator-less embedders, arena-owned
+ * memory, hot loops that forbid cudaMalloc because it synchronises).
+ *   K, V, D          draft positions, vocabulary (multiple of 8, <= 262144), width (multiple of 4)
+ *   hs [B, K, D]     float32 head states the candidates were drawn from
+ *   E [V, D]         float32 row-major LM-head weights (used for q(v) = exp(E_v . h / T - lse))
+ *   other arguments  as dlite_verify_sample.
+ * Scratch: the exact-fallback residual row lives in a static device array of
+ * 2^20 fixed-point entries (8 MiB) that every GPU loading the library holds
+ * until exit; B * V above 2^20 is rejected with DLITE_ERR_UNSUPPORTED_SHAPE.
+ * The first call on a device looks up that array's device address (no
+ * allocation); make that first call before any stream capture. All calls
+ * share the array, which keeps the last call's contents (each call rewrites
+ * what it reads), so calls that overlap on the GPU race. */
+int dlite_verify_sample_static(int B, int K, int V, int D, const int32_t *candidates,
+                               const dlite_qstats *qstats, const float *hs, const float *E,
+                               const float *target_probs, float temperature, uint64_t seed,
+                               const int64_t *pos, int32_t *accepted, int32_t *commits,
+                               int32_t *n_commit, int32_t *next_anchor, dlite_stream_t stream);
+
 /* Round bookkeeping: pos[b] += n_commit[b] (the RNG positions follow the
  * committed tokens; [P1] §"一轮执行后..." — each round advances A+1). */
 int dlite_advance(dlite_handle *h, int B, const int32_t *n_commit, int64_t *pos,
