@@ -13,6 +13,7 @@ inputs cycle through a ring of 4 batches.
 bounded sample of the same workload. Under torchrun only rank 0 runs it.
 """
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -120,6 +121,8 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device(dev))
     wl = wk.WORKLOADS[args.workload]
+    if args.batch:
+        wl = dataclasses.replace(wl, B=args.batch, name=f"{wl.name}-B{args.batch}")
     cfg = wl.cfg
     B = wl.B
     T = wl.temperature
@@ -420,6 +423,7 @@ def main():
     ap.add_argument("--workload", default="qwen3-8b-b32", choices=sorted(wk.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clock-sampler", action="store_true")
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (exploration)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

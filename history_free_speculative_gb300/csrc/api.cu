@@ -120,11 +120,11 @@ int check_config(const dlite_config* c) {
   if (c->L_D < 1 || c->L_D > DLITE_MAX_LAYERS) return DLITE_ERR_UNSUPPORTED_SHAPE;
   if (c->n_q < 1 || c->n_kv < 1 || c->n_q % c->n_kv) return DLITE_ERR_UNSUPPORTED_SHAPE;
   if (c->d_h != 64 && c->d_h != 128) return DLITE_ERR_UNSUPPORTED_SHAPE;
+  if (c->D > 16384) return DLITE_ERR_UNSUPPORTED_SHAPE;  // row kernels: 4 float4 per thread
   if (c->D % 64 || c->F % 64 || c->R % 32 || c->R > 1024 || c->V < 8 || c->V % 8 || c->V > 262144)
     return DLITE_ERR_UNSUPPORTED_SHAPE;
   if ((c->n_q * c->d_h) % 64) return DLITE_ERR_UNSUPPORTED_SHAPE;
-  const int G = c->n_q / c->n_kv, Tk = c->m + c->K + 1;
-  if ((size_t)(G * (c->K + 1) + 2 * Tk) * (c->d_h + 1) * 4 > 96 * 1024) return DLITE_ERR_UNSUPPORTED_SHAPE;
+  if (attention_smem(c->K, c->m, c->d_h) > 96 * 1024) return DLITE_ERR_UNSUPPORTED_SHAPE;
   if (c->R < 32 || chain_smem_bytes(c->R, chain_group_size(c->R, c->B_max)) > 200 * 1024)
     return DLITE_ERR_UNSUPPORTED_SHAPE;
   if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return DLITE_ERR_INVALID_ARG;

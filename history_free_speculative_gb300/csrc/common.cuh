@@ -94,6 +94,17 @@ __device__ __forceinline__ float gumbel_from_bits(uint32_t x) {
   return -__logf(-__logf(u01f(x)));
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Kernels of the round are launched with programmatic stream serialization:
+// a kernel may begin while its predecessor drains. pdl_trigger lets the next
+// kernel launch; pdl_wait blocks until the predecessor has completed and its
+// writes are visible, and must precede any access to data a predecessor
+// produces or consumes.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- reductions
 
 __device__ __forceinline__ float warp_sum(float v) {

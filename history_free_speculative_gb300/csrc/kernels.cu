@@ -24,161 +24,237 @@ __device__ __forceinline__ void store_planes(bf16* const* pl, int n, size_t i, f
   }
 }
 
+constexpr int kRowThreads = 1024;
+constexpr int kRowVec = 4;  // float4 chunks per thread at most
+
+__device__ __forceinline__ float4 f4add(float4 a, float4 b) {
+  return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+
+__device__ __forceinline__ float4 sum_splits4(const float* base, size_t stride, int S) {
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  int s = 0;
+  for (; s + 8 <= S; s += 8) {  // eight independent loads in flight
+    float4 t[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t[k] = *reinterpret_cast<const float4*>(base + (size_t)(s + k) * stride);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc = f4add(acc, t[k]);
+  }
+  for (; s + 4 <= S; s += 4) {  // four independent loads in flight
+    const float4 a = *reinterpret_cast<const float4*>(base + (size_t)s * stride);
+    const float4 b = *reinterpret_cast<const float4*>(base + (size_t)(s + 1) * stride);
+    const float4 c = *reinterpret_cast<const float4*>(base + (size_t)(s + 2) * stride);
+    const float4 d = *reinterpret_cast<const float4*>(base + (size_t)(s + 3) * stride);
+    acc = f4add(acc, a);
+    acc = f4add(acc, b);
+    acc = f4add(acc, c);
+    acc = f4add(acc, d);
+  }
+  for (; s < S; ++s) acc = f4add(acc, *reinterpret_cast<const float4*>(base + (size_t)s * stride));
+  return acc;
+}
+
+__device__ __forceinline__ void store4_planes(bf16* const* pl, int n, size_t i, float4 v) {
+  store_planes(pl, n, i, v.x);
+  store_planes(pl, n, i + 1, v.y);
+  store_planes(pl, n, i + 2, v.z);
+  store_planes(pl, n, i + 3, v.w);
+}
+
 // ---------------------------------------------------------------- K1: staging
 // Rows [0, B*m): z_{b,j} = RMSNorm(hidden_{b,j} + e_depth_j) * g_stage.
 // Rows [B*m, B*m + B*(K+1)): local rows x_{b,0} = E[anchor_b], x_{b,i} = e_ph,
 // and y = RMSNorm(x) * g_attn (layer 0 input of the QKV product).
+// One CTA of 1024 threads per row, 4 consecutive elements per thread and step.
+__device__ __forceinline__ float4 load4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 load4(const bf16* p) {
+  const uint2 raw = *reinterpret_cast<const uint2*>(p);
+  const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+  const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+  return make_float4(__low2float(a), __high2float(a), __low2float(b), __high2float(b));
+}
+
 template <typename T>
-__global__ void stage_kernel(StageArgs a) {
-  extern __shared__ float sv[];
+__global__ void __launch_bounds__(1024) stage_kernel(StageArgs a) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float red[32];
   const int row = blockIdx.x;
-  const int D = a.D;
+  const int D = a.D, n4 = D / 4;
   const int nz = a.B * a.m;
+  float4 v[4];
+  float ss = 0.f;
   if (row < nz) {
     const int b = row / a.m, j = row % a.m;
     const T* h = reinterpret_cast<const T*>(a.hidden) + ((size_t)b * a.m + j) * D;
-    float ss = 0.f;
-    for (int d = threadIdx.x; d < D; d += blockDim.x) {
-      const float v = to_f32(h[d]) + a.e_depth[(size_t)j * D + d];
-      sv[d] = v;
-      ss += v * v;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = threadIdx.x + k * 1024;
+      if (i < n4) {
+        v[k] = f4add(load4(h + 4 * i), load4(a.e_depth + (size_t)j * D + 4 * i));
+        ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+      }
     }
     ss = block_sum(ss, red);
     const float inv = rsqrtf(ss / D + a.eps);
-    for (int d = threadIdx.x; d < D; d += blockDim.x) {
-      const float zv = sv[d] * inv * a.g_stage[d];
-      store_planes(a.z, a.nz, (size_t)row * D + d, zv);
-      if (a.tap_z) a.tap_z[(size_t)row * D + d] = zv;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = threadIdx.x + k * 1024;
+      if (i < n4) {
+        const float4 g = load4(a.g_stage + 4 * i);
+        const float4 zv = make_float4(v[k].x * inv * g.x, v[k].y * inv * g.y, v[k].z * inv * g.z,
+                                      v[k].w * inv * g.w);
+        store4_planes(a.z, a.nz, (size_t)row * D + 4 * i, zv);
+        if (a.tap_z) *reinterpret_cast<float4*>(a.tap_z + (size_t)row * D + 4 * i) = zv;
+      }
     }
   } else {
     const int lr = row - nz;
-    const int b = lr / (a.K + 1), i = lr % (a.K + 1);
+    const int b = lr / (a.K + 1), i0 = lr % (a.K + 1);
     int tok = 0;
-    if (i == 0) {
+    if (i0 == 0) {
       tok = a.anchor[b];
       if (tok < 0 || tok >= a.V) {
         if (threadIdx.x == 0) flag_status(a.status, kDevBounds);
         tok = 0;
       }
     }
-    float ss = 0.f;
-    for (int d = threadIdx.x; d < D; d += blockDim.x) {
-      const float v = (i == 0) ? ld_elem<T>(a.E, a.E_tiled ? tiled_index(tok, d, D) : (size_t)tok * D + d)
-                               : a.e_ph[d];
-      sv[d] = v;
-      a.x[(size_t)lr * D + d] = v;
-      ss += v * v;
+    const T* E = reinterpret_cast<const T*>(a.E);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = threadIdx.x + k * 1024;
+      if (i < n4) {
+        v[k] = (i0 == 0) ? load4(E + (a.E_tiled ? tiled_index(tok, 4 * i, D) : (size_t)tok * D + 4 * i))
+                         : load4(a.e_ph + 4 * i);
+        *reinterpret_cast<float4*>(a.x + (size_t)lr * D + 4 * i) = v[k];
+        ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+      }
     }
     ss = block_sum(ss, red);
     const float inv = rsqrtf(ss / D + a.eps);
-    for (int d = threadIdx.x; d < D; d += blockDim.x)
-      store_planes(a.y, a.ny, (size_t)lr * D + d, sv[d] * inv * a.g_attn0[d]);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = threadIdx.x + k * 1024;
+      if (i < n4) {
+        const float4 g = load4(a.g_attn0 + 4 * i);
+        store4_planes(a.y, a.ny, (size_t)lr * D + 4 * i,
+                      make_float4(v[k].x * inv * g.x, v[k].y * inv * g.y, v[k].z * inv * g.z,
+                                  v[k].w * inv * g.w));
+      }
+    }
   }
 }
 
 cudaError_t launch_stage(const StageArgs& a, bool f32, cudaStream_t s) {
   const int rows = a.B * a.m + a.B * (a.K + 1);
-  const size_t smem = (size_t)a.D * sizeof(float);
-  if (f32)
-    stage_kernel<float><<<rows, 256, smem, s>>>(a);
-  else
-    stage_kernel<bf16><<<rows, 256, smem, s>>>(a);
-  return cudaGetLastError();
+  if (f32) return launch_pdl(stage_kernel<float>, dim3(rows), dim3(1024), 0, s, a);
+  return launch_pdl(stage_kernel<bf16>, dim3(rows), dim3(1024), 0, s, a);
 }
 
 // ---------------------------------------------------------------- K2b: block attention
-// One CTA per (kv head g, request b). Sums the QKV split-K partials of the
-// request's rows, applies RoPE to the local queries / keys (table [K+1][d_h/2]),
-// then runs non-causal softmax attention of the G*(K+1) query rows of this kv
-// head over all m + K + 1 keys, one lane per key, warp-shuffle max / sum.
-__global__ void attention_kernel(AttnArgs a) {
+// One CTA per (query head h, request b); its key/value head is g = h / (n_q/n_kv).
+// Sums the QKV split-K partials of the request's rows (4 columns per item),
+// applies RoPE to the local queries / keys (table [K+1][d_h/2]), then runs
+// non-causal softmax attention of the K+1 query rows over all m + K + 1 keys:
+// one warp per query row, one lane per key for the scores, warp-shuffle
+// max / sum, and 4 output columns per lane. Shared rows are d_h + 4 floats so
+// 16-byte accesses by 8 consecutive lanes hit distinct banks.
+constexpr int kAttnThreads = 512;
+
+__global__ void __launch_bounds__(kAttnThreads) attention_kernel(AttnArgs a) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ float sm[];
-  const int g = blockIdx.x, b = blockIdx.y;
-  const int K1 = a.K + 1, dh = a.d_h, half = dh / 2, G = a.n_q / a.n_kv;
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int K1 = a.K + 1, dh = a.d_h, half = dh / 2, G = a.n_q / a.n_kv, g = h / G;
   const int qd = a.n_q * dh, kvd = a.n_kv * dh;
   const int ldl = qd + 2 * kvd;  // local partial row width
   const int ldc = 2 * kvd;       // context partial row width
   const int Tk = a.m + K1;
-  const int LD = dh + 1;
-  float* qs = sm;                   // [G*K1][LD]
-  float* ks = qs + G * K1 * LD;     // [Tk][LD]
-  float* vs = ks + Tk * LD;         // [Tk][LD]
+  const int LD = dh + 4;
+  float* qs = sm;               // [K1][LD]
+  float* ks = qs + K1 * LD;     // [Tk][LD]
+  float* vs = ks + Tk * LD;     // [Tk][LD]
   const size_t sl = (size_t)a.B * K1 * ldl, sc = (size_t)a.B * a.m * ldc;
-
-  auto sum_loc = [&](int row, int col) {
-    const float* p = a.part_loc + (size_t)(b * K1 + row) * ldl + col;
-    float v = 0.f;
-    for (int s = 0; s < a.S_loc; ++s) v += p[s * sl];
-    return v;
+  auto loc4 = [&](int row, int col) {
+    return sum_splits4(a.part_loc + (size_t)(b * K1 + row) * ldl + col, sl, a.S_loc);
   };
-  auto sum_ctx = [&](int row, int col) {
-    const float* p = a.part_ctx + (size_t)(b * a.m + row) * ldc + col;
-    float v = 0.f;
-    for (int s = 0; s < a.S_ctx; ++s) v += p[s * sc];
-    return v;
+  auto ctx4 = [&](int row, int col) {
+    return sum_splits4(a.part_ctx + (size_t)(b * a.m + row) * ldc + col, sc, a.S_ctx);
   };
-  auto rnd = [&](float v) { return a.round_bf16 ? round_bf16(v) : v; };
-
-  // queries: (i, hh, j) pairs
-  for (int idx = threadIdx.x; idx < K1 * G * half; idx += blockDim.x) {
-    const int j = idx % half, hh = (idx / half) % G, i = idx / (half * G);
-    const int col = (g * G + hh) * dh;
-    const float x1 = sum_loc(i, col + j), x2 = sum_loc(i, col + j + half);
-    const float c = a.rope_cos[i * half + j], sn = a.rope_sin[i * half + j];
-    float* q = qs + (hh * K1 + i) * LD;
-    q[j] = rnd(x1 * c - x2 * sn);
-    q[j + half] = rnd(x2 * c + x1 * sn);
-  }
-  // local keys (rotated) and values
-  for (int idx = threadIdx.x; idx < K1 * half; idx += blockDim.x) {
-    const int j = idx % half, i = idx / half;
-    const int col = qd + g * dh;
-    const float x1 = sum_loc(i, col + j), x2 = sum_loc(i, col + j + half);
-    const float c = a.rope_cos[i * half + j], sn = a.rope_sin[i * half + j];
-    float* k = ks + (a.m + i) * LD;
-    k[j] = rnd(x1 * c - x2 * sn);
-    k[j + half] = rnd(x2 * c + x1 * sn);
-  }
-  for (int idx = threadIdx.x; idx < K1 * dh; idx += blockDim.x) {
-    const int d = idx % dh, i = idx / dh;
-    vs[(a.m + i) * LD + d] = rnd(sum_loc(i, qd + kvd + g * dh + d));
-  }
-  // context keys / values: local position 0, no rotation
-  for (int idx = threadIdx.x; idx < a.m * dh; idx += blockDim.x) {
-    const int d = idx % dh, j = idx / dh;
-    ks[j * LD + d] = rnd(sum_ctx(j, g * dh + d));
-    vs[j * LD + d] = rnd(sum_ctx(j, kvd + g * dh + d));
+  auto rnd4 = [&](float4 v) {
+    return a.round_bf16 ? make_float4(round_bf16(v.x), round_bf16(v.y), round_bf16(v.z), round_bf16(v.w)) : v;
+  };
+  auto rope = [&](float* dst, int i, int j, float4 x1, float4 x2) {
+    const float4 c = load4(a.rope_cos + i * half + j), sn = load4(a.rope_sin + i * half + j);
+    *reinterpret_cast<float4*>(dst + j) =
+        rnd4(make_float4(x1.x * c.x - x2.x * sn.x, x1.y * c.y - x2.y * sn.y, x1.z * c.z - x2.z * sn.z,
+                         x1.w * c.w - x2.w * sn.w));
+    *reinterpret_cast<float4*>(dst + j + half) =
+        rnd4(make_float4(x2.x * c.x + x1.x * sn.x, x2.y * c.y + x1.y * sn.y, x2.z * c.z + x1.z * sn.z,
+                         x2.w * c.w + x1.w * sn.w));
+  };
+  const int h4 = half / 4, d4 = dh / 4;
+  const int nq = K1 * h4, nk = K1 * h4, nv = K1 * d4, nc = a.m * d4;
+  for (int idx = threadIdx.x; idx < nq + nk + nv + 2 * nc; idx += blockDim.x) {
+    if (idx < nq) {  // queries of head h (rotated)
+      const int j = (idx % h4) * 4, i = idx / h4, col = h * dh;
+      rope(qs + i * LD, i, j, loc4(i, col + j), loc4(i, col + j + half));
+    } else if (idx < nq + nk) {  // local keys (rotated)
+      const int t = idx - nq, j = (t % h4) * 4, i = t / h4, col = qd + g * dh;
+      rope(ks + (a.m + i) * LD, i, j, loc4(i, col + j), loc4(i, col + j + half));
+    } else if (idx < nq + nk + nv) {  // local values
+      const int t = idx - nq - nk, d = (t % d4) * 4, i = t / d4;
+      *reinterpret_cast<float4*>(vs + (a.m + i) * LD + d) = rnd4(loc4(i, qd + kvd + g * dh + d));
+    } else {  // context keys / values: local position 0, no rotation
+      const int t = idx - nq - nk - nv, kv = t / nc, r = t % nc, d = (r % d4) * 4, j = r / d4;
+      float* dst = (kv ? vs : ks) + j * LD + d;
+      *reinterpret_cast<float4*>(dst) = rnd4(ctx4(j, kv * kvd + g * dh + d));
+    }
   }
   __syncthreads();
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  for (int qr = warp; qr < G * K1; qr += nw) {
-    const int hh = qr / K1, i = qr % K1;
-    const float* q = qs + qr * LD;
+  for (int i = warp; i < K1; i += nw) {
+    const float* q = qs + i * LD;
     float sc_ = -INFINITY;
     if (lane < Tk) {
       const float* k = ks + lane * LD;
-      float acc = 0.f;
-      for (int d = 0; d < dh; ++d) acc = fmaf(q[d], k[d], acc);
-      sc_ = acc * a.scale;
+      float acc0 = 0.f, acc1 = 0.f;
+      for (int d = 0; d < dh; d += 8) {
+        const float4 qa = *reinterpret_cast<const float4*>(q + d), ka = *reinterpret_cast<const float4*>(k + d);
+        const float4 qb = *reinterpret_cast<const float4*>(q + d + 4), kb = *reinterpret_cast<const float4*>(k + d + 4);
+        acc0 = fmaf(qa.x, ka.x, fmaf(qa.y, ka.y, fmaf(qa.z, ka.z, fmaf(qa.w, ka.w, acc0))));
+        acc1 = fmaf(qb.x, kb.x, fmaf(qb.y, kb.y, fmaf(qb.z, kb.z, fmaf(qb.w, kb.w, acc1))));
+      }
+      sc_ = (acc0 + acc1) * a.scale;
     }
     const float mx = warp_max(sc_);
     const float e = (lane < Tk) ? expf(sc_ - mx) : 0.f;
     const float den = warp_sum(e);
     const float pj = e / den;
-    const size_t orow = (size_t)(b * K1 + i) * qd + (g * G + hh) * dh;
-    for (int d = lane; d < dh; d += 32) {
-      float acc = 0.f;
-      for (int jk = 0; jk < Tk; ++jk) acc = fmaf(__shfl_sync(0xffffffffu, pj, jk), vs[jk * LD + d], acc);
-      store_planes(a.o, a.no, orow + d, acc);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int jk = 0; jk < Tk; ++jk) {
+      const float pk = __shfl_sync(0xffffffffu, pj, jk);  // whole warp
+      if (lane < d4) {
+        const float4 v = *reinterpret_cast<const float4*>(vs + jk * LD + 4 * lane);
+        acc.x = fmaf(pk, v.x, acc.x);
+        acc.y = fmaf(pk, v.y, acc.y);
+        acc.z = fmaf(pk, v.z, acc.z);
+        acc.w = fmaf(pk, v.w, acc.w);
+      }
     }
+    if (lane < d4) store4_planes(a.o, a.no, (size_t)(b * K1 + i) * qd + h * dh + 4 * lane, acc);
   }
 }
 
+size_t attention_smem(int K, int m, int d_h) {
+  return (size_t)((K + 1) + 2 * (m + K + 1)) * (d_h + 4) * sizeof(float);
+}
+
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s) {
-  const int K1 = a.K + 1, G = a.n_q / a.n_kv, Tk = a.m + K1;
-  const size_t smem = (size_t)(G * K1 + 2 * Tk) * (a.d_h + 1) * sizeof(float);
+  const size_t smem = attention_smem(a.K, a.m, a.d_h);
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -186,80 +262,95 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  attention_kernel<<<dim3(a.n_kv, a.B), 256, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(attention_kernel, dim3(a.n_q, a.B), dim3(kAttnThreads), smem, s, a);
 }
 
 // ---------------------------------------------------------------- residual + RMSNorm
 // x[r] += sum_s part[s][r]; then either y = RMSNorm(x) * g (next product's
 // input) or, after the last layer, b = RMSNorm(x) * g_final for the
-// placeholder rows (the anchor row is dropped).
-__global__ void resnorm_kernel(ResNormArgs a) {
-  extern __shared__ float sv[];
+// placeholder rows (the anchor row is dropped). One CTA of 1024 threads per
+// row, float4 per thread (D <= 16384), every split's load issued before use.
+__global__ void __launch_bounds__(kRowThreads) resnorm_kernel(ResNormArgs a) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float red[32];
-  const int r = blockIdx.x, D = a.D;
+  const int r = blockIdx.x, D = a.D, n4 = D / 4;
   const size_t stride = (size_t)a.rows * D;
+  float4 v[kRowVec];
   float ss = 0.f;
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
-    float v = a.x[(size_t)r * D + d];
-    const float* p = a.part + (size_t)r * D + d;
-    float acc = 0.f;
-    for (int s = 0; s < a.S; ++s) acc += p[s * stride];
-    v += acc;
-    a.x[(size_t)r * D + d] = v;
-    if (a.tap_x) a.tap_x[(size_t)r * D + d] = v;
-    sv[d] = v;
-    ss += v * v;
+#pragma unroll
+  for (int k = 0; k < kRowVec; ++k) {
+    const int i = threadIdx.x + k * kRowThreads;
+    if (i < n4) {
+      float4 x = *reinterpret_cast<const float4*>(a.x + (size_t)r * D + 4 * i);
+      x = f4add(x, sum_splits4(a.part + (size_t)r * D + 4 * i, stride, a.S));
+      *reinterpret_cast<float4*>(a.x + (size_t)r * D + 4 * i) = x;
+      if (a.tap_x) *reinterpret_cast<float4*>(a.tap_x + (size_t)r * D + 4 * i) = x;
+      v[k] = x;
+      ss += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+    }
   }
   ss = block_sum(ss, red);
   const float inv = rsqrtf(ss / D + a.eps);
-  if (!a.final_mode) {
-    for (int d = threadIdx.x; d < D; d += blockDim.x)
-      store_planes(a.y, a.ny, (size_t)r * D + d, sv[d] * inv * a.g[d]);
-  } else {
+  if (a.final_mode) {
     const int b = r / a.K1, i = r % a.K1;
     if (i == 0) return;
     const size_t orow = (size_t)(b * (a.K1 - 1) + (i - 1)) * D;
-    for (int d = threadIdx.x; d < D; d += blockDim.x) {
-      const float v = sv[d] * inv * a.g[d];
-      a.bout[orow + d] = v;
-      store_planes(a.bp, 2, orow + d, v);
-      if (a.tap_b) a.tap_b[orow + d] = v;
+#pragma unroll
+    for (int k = 0; k < kRowVec; ++k) {
+      const int j = threadIdx.x + k * kRowThreads;
+      if (j < n4) {
+        const float4 g = *reinterpret_cast<const float4*>(a.g + 4 * j);
+        const float4 o = make_float4(v[k].x * inv * g.x, v[k].y * inv * g.y, v[k].z * inv * g.z,
+                                     v[k].w * inv * g.w);
+        *reinterpret_cast<float4*>(a.bout + orow + 4 * j) = o;
+        store4_planes(a.bp, 2, orow + 4 * j, o);
+        if (a.tap_b) *reinterpret_cast<float4*>(a.tap_b + orow + 4 * j) = o;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < kRowVec; ++k) {
+      const int j = threadIdx.x + k * kRowThreads;
+      if (j < n4) {
+        const float4 g = *reinterpret_cast<const float4*>(a.g + 4 * j);
+        store4_planes(a.y, a.ny, (size_t)r * D + 4 * j,
+                      make_float4(v[k].x * inv * g.x, v[k].y * inv * g.y, v[k].z * inv * g.z,
+                                  v[k].w * inv * g.w));
+      }
     }
   }
 }
 
 cudaError_t launch_resnorm(const ResNormArgs& a, cudaStream_t s) {
-  resnorm_kernel<<<a.rows, 256, (size_t)a.D * sizeof(float), s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(resnorm_kernel, dim3(a.rows), dim3(kRowThreads), 0, s, a);
 }
 
 // ---------------------------------------------------------------- SwiGLU epilogue
-// a[r, f] = silu(sum_s part[s][r][f]) * sum_s part[s][r][F + f].
+// a[r, f] = silu(sum_s part[s][r][f]) * sum_s part[s][r][F + f], float4 per thread.
 __global__ void swiglu_kernel(const float* part, int S, int rows, int F, bf16* o0, bf16* o1, int no) {
-  const size_t n = (size_t)rows * F, stride = (size_t)rows * 2 * F;
+  pdl_trigger();
+  pdl_wait();
+  const size_t n4 = (size_t)rows * F / 4, stride = (size_t)rows * 2 * F;
   bf16* outs[2] = {o0, o1};
-  for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n;
-       idx += (size_t)gridDim.x * blockDim.x) {
-    const size_t r = idx / F, f = idx % F;
+  for (size_t q = (size_t)blockIdx.x * blockDim.x + threadIdx.x; q < n4;
+       q += (size_t)gridDim.x * blockDim.x) {
+    const size_t idx = 4 * q, r = idx / F, f = idx % F;
     const float* p = part + r * 2 * F + f;
-    float gs = 0.f, us = 0.f;
-    for (int s = 0; s < S; ++s) {
-      gs += p[s * stride];
-      us += p[s * stride + F];
-    }
-    const float v = gs / (1.f + expf(-gs)) * us;
-    store_planes(outs, no, idx, v);
+    const float4 g = sum_splits4(p, stride, S);
+    const float4 u = sum_splits4(p + F, stride, S);
+    const float4 v = make_float4(g.x / (1.f + expf(-g.x)) * u.x, g.y / (1.f + expf(-g.y)) * u.y,
+                                 g.z / (1.f + expf(-g.z)) * u.z, g.w / (1.f + expf(-g.w)) * u.w);
+    store4_planes(outs, no, idx, v);
   }
 }
 
 cudaError_t launch_swiglu(const float* part, int S, int rows, int F, bf16* const* o, int no,
                           cudaStream_t s) {
-  const size_t n = (size_t)rows * F;
-  int blocks = (int)((n + 255) / 256);
+  const size_t n4 = (size_t)rows * F / 4;
+  int blocks = (int)((n4 + 255) / 256);
   if (blocks > 152 * 16) blocks = 152 * 16;
-  swiglu_kernel<<<blocks, 256, 0, s>>>(part, S, rows, F, o[0], o[1], no);
-  return cudaGetLastError();
+  return launch_pdl(swiglu_kernel, dim3(blocks), dim3(256), 0, s, part, S, rows, F, o[0], o[1], no);
 }
 
 // ---------------------------------------------------------------- K3: sequential head chain
@@ -290,6 +381,8 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t local_addr, uint32_t ran
 }
 
 __global__ void __launch_bounds__(kChainThreads) head_chain_kernel(ChainArgs a) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ float sm[];
   const int R = a.R, rc = R / kChainCluster;
   const int Bg = a.Bg;
@@ -310,17 +403,34 @@ __global__ void __launch_bounds__(kChainThreads) head_chain_kernel(ChainArgs a) 
   const bool active = threadIdx.x < rc * Bg && req < a.B;
   const size_t stride = (size_t)a.rows * 2 * a.Rp;
   float e_prev = 0.f;
+  // c_i, e_i of this thread's (row, request) for every step, loaded up front
+  float cs[32], es[32];
+  if (active) {
+    for (int i = 0; i < a.K; ++i) {
+      const float* p = a.part + (size_t)(req * a.K + i) * 2 * a.Rp + r0 + rl;
+      float c[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
+      int sp = 0;
+      for (; sp + 4 <= a.S; sp += 4) {  // 8 independent loads in flight
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          c[k] += p[(size_t)(sp + k) * stride];
+          e[k] += p[(size_t)(sp + k) * stride + a.Rp];
+        }
+      }
+      for (; sp < a.S; ++sp) {
+        c[0] += p[(size_t)sp * stride];
+        e[0] += p[(size_t)sp * stride + a.Rp];
+      }
+      cs[i] = (c[0] + c[1]) + (c[2] + c[3]);
+      es[i] = (e[0] + e[1]) + (e[2] + e[3]);
+    }
+  }
   cluster_sync_all();  // every CTA of the cluster is running before any remote store
   for (int i = 0; i < a.K; ++i) {
     float t = 0.f;
     if (active) {
       const int row = req * a.K + i;
-      const float* p = a.part + (size_t)row * 2 * a.Rp + r0 + rl;
-      float c = 0.f, e = 0.f;
-      for (int sp = 0; sp < a.S; ++sp) {
-        c += p[sp * stride];
-        e += p[sp * stride + a.Rp];
-      }
+      const float c = cs[i], e = es[i];
       float acc = c;
       if (i > 0) {
         const float* tp = tbuf + ((size_t)((i - 1) & 1) * Bg + ql) * R;
@@ -363,13 +473,15 @@ cudaError_t launch_head_chain(const ChainArgs& a, cudaStream_t s) {
   cfg.blockDim = dim3(kChainThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attrs[1];
+  cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeClusterDimension;
   attrs[0].val.clusterDim.x = kChainCluster;
   attrs[0].val.clusterDim.y = 1;
   attrs[0].val.clusterDim.z = 1;
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, head_chain_kernel, a);
 }
 
@@ -388,29 +500,32 @@ size_t chain_smem_bytes(int R, int Bg) {
 // h = b + sum_s part[s] (the P t_i product), kept in fp32 and as two bf16 planes.
 __global__ void head_out_kernel(const float* part, int S, int rows, int D, const float* bsrc,
                                 float* hs, bf16* h0, bf16* h1, float* tap) {
-  const size_t n = (size_t)rows * D;
+  pdl_trigger();
+  pdl_wait();
+  const size_t n = (size_t)rows * D, n4 = n / 4;
   bf16* pl[2] = {h0, h1};
-  for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n;
-       idx += (size_t)gridDim.x * blockDim.x) {
-    float v = bsrc[idx];
-    for (int s = 0; s < S; ++s) v += part[s * n + idx];
-    hs[idx] = v;
-    store_planes(pl, 2, idx, v);
-    if (tap) tap[idx] = v;
+  for (size_t q = (size_t)blockIdx.x * blockDim.x + threadIdx.x; q < n4;
+       q += (size_t)gridDim.x * blockDim.x) {
+    const size_t idx = 4 * q;
+    const float4 v = f4add(*reinterpret_cast<const float4*>(bsrc + idx), sum_splits4(part + idx, n, S));
+    *reinterpret_cast<float4*>(hs + idx) = v;
+    store4_planes(pl, 2, idx, v);
+    if (tap) *reinterpret_cast<float4*>(tap + idx) = v;
   }
 }
 
 cudaError_t launch_head_out(const float* part, int S, int rows, int D, const float* b, float* hs,
                             bf16* const* hp, float* tap, cudaStream_t s) {
-  const size_t n = (size_t)rows * D;
-  int blocks = (int)((n + 255) / 256);
+  const size_t n4 = (size_t)rows * D / 4;
+  int blocks = (int)((n4 + 255) / 256);
   if (blocks > 152 * 8) blocks = 152 * 8;
-  head_out_kernel<<<blocks, 256, 0, s>>>(part, S, rows, D, b, hs, hp[0], hp[1], tap);
-  return cudaGetLastError();
+  return launch_pdl(head_out_kernel, dim3(blocks), dim3(256), 0, s, part, S, rows, D, b, hs, hp[0], hp[1], tap);
 }
 
 // Split an fp32 tensor into two bf16 planes (used for caller-provided b / hs).
 __global__ void split_kernel(const float* src, size_t n, bf16* h0, bf16* h1, float* copy) {
+  pdl_trigger();
+  pdl_wait();
   bf16* pl[2] = {h0, h1};
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (size_t)gridDim.x * blockDim.x) {
@@ -422,14 +537,15 @@ __global__ void split_kernel(const float* src, size_t n, bf16* h0, bf16* h1, flo
 cudaError_t launch_split(const float* src, size_t n, bf16* const* pl, float* copy, cudaStream_t s) {
   int blocks = (int)((n + 255) / 256);
   if (blocks > 152 * 8) blocks = 152 * 8;
-  split_kernel<<<blocks, 256, 0, s>>>(src, n, pl[0], pl[1], copy);
-  return cudaGetLastError();
+  return launch_pdl(split_kernel, dim3(blocks), dim3(256), 0, s, src, n, pl[0], pl[1], copy);
 }
 
 // ---------------------------------------------------------------- K5: greedy verify
 // One warp per request: lane i < K compares d_{i+1} with the target's choice at
 // input index i; A = position of the first zero in the ballot (K if none).
 __global__ void verify_greedy_kernel(VerifyArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (b >= a.B) return;
@@ -452,8 +568,7 @@ __global__ void verify_greedy_kernel(VerifyArgs a) {
 
 cudaError_t launch_verify_greedy(const VerifyArgs& a, cudaStream_t s) {
   const int wpb = 8;
-  verify_greedy_kernel<<<(a.B + wpb - 1) / wpb, wpb * 32, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(verify_greedy_kernel, dim3((a.B + wpb - 1) / wpb), dim3(wpb * 32), 0, s, a);
 }
 
 // ---------------------------------------------------------------- K5: sampling verify
@@ -521,11 +636,21 @@ __device__ void block_icdf(const Row& row, int V, const uint32_t* xs, int nthr, 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const int nseg = (V + kSeg - 1) / kSeg;
   // 1) segment sums: one warp per segment, one float4 per lane
-  for (int sg = warp; sg < nseg; sg += nw) {
-    unsigned long long w[4];
-    row.get4(sg * kSeg + lane * 4, w);
-    const unsigned long long t = warp_sum_u64(w[0] + w[1] + w[2] + w[3]);
-    if (lane == 0) incl[sg] = t;
+  for (int sg0 = warp; sg0 < nseg; sg0 += 4 * nw) {  // four segments' loads in flight per warp
+    unsigned long long w[4][4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int sg = sg0 + u * nw;
+      if (sg < nseg) row.get4(sg * kSeg + lane * 4, w[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int sg = sg0 + u * nw;
+      if (sg < nseg) {
+        const unsigned long long t = warp_sum_u64(w[u][0] + w[u][1] + w[u][2] + w[u][3]);
+        if (lane == 0) incl[sg] = t;
+      }
+    }
   }
   __syncthreads();
   // 2) inclusive scan of the segment sums (warp 0, sequential chunks of 32)
@@ -597,6 +722,7 @@ __device__ __forceinline__ float row_dot(const VerifyArgs& a, int v, const float
       acc = fmaf(ev.x, hv.x, fmaf(ev.y, hv.y, fmaf(ev.z, hv.z, fmaf(ev.w, hv.w, acc))));
     }
   } else {
+#pragma unroll 8
     for (int d = lane * 4; d < a.D; d += 128) {
       const uint2 raw = *reinterpret_cast<const uint2*>(a.Eb + tiled_index(v, d, a.D));
       const __nv_bfloat162 e01 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
@@ -613,6 +739,8 @@ __device__ __forceinline__ float row_dot(const VerifyArgs& a, int v, const float
 
 // One CTA (1024 threads) per request.
 __global__ void __launch_bounds__(kVerifyThreads) verify_sample_kernel(VerifyArgs a) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ unsigned long long incl[kMaxSegs];
   __shared__ unsigned long long total;
   __shared__ uint32_t xs[kProposals];      // inverse-CDF words of the proposals
@@ -719,18 +847,18 @@ __global__ void __launch_bounds__(kVerifyThreads) verify_sample_kernel(VerifyArg
 }
 
 cudaError_t launch_verify_sample(const VerifyArgs& a, cudaStream_t s) {
-  verify_sample_kernel<<<a.B, kVerifyThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(verify_sample_kernel, dim3(a.B), dim3(kVerifyThreads), 0, s, a);
 }
 
 __global__ void advance_kernel(int B, const int32_t* n_commit, int64_t* pos) {
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b < B) pos[b] += n_commit[b];
 }
 
 cudaError_t launch_advance(int B, const int32_t* n_commit, int64_t* pos, cudaStream_t s) {
-  advance_kernel<<<(B + 127) / 128, 128, 0, s>>>(B, n_commit, pos);
-  return cudaGetLastError();
+  return launch_pdl(advance_kernel, dim3((B + 127) / 128), dim3(128), 0, s, B, n_commit, pos);
 }
 
 // ---------------------------------------------------------------- weight preparation

@@ -32,32 +32,23 @@ __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2
   m = mm;
 }
 
-// Merge two descending top-k lists into (sc, id).
-__device__ __forceinline__ void topk_merge(float (&sc)[kTopK], int (&id)[kTopK],
-                                           const float (&sc2)[kTopK], const int (&id2)[kTopK]) {
-  float o[kTopK];
-  int oi[kTopK];
-  int a = 0, b = 0;  // a, b <= k at step k: every read below is in range
-#pragma unroll
-  for (int k = 0; k < kTopK; ++k) {
-    const bool take_a = better(sc[a], id[a], sc2[b], id2[b]) || (sc[a] == sc2[b] && id[a] == id2[b]);
-    if (take_a) {
-      o[k] = sc[a];
-      oi[k] = id[a];
-      // drop an identical entry in the other list (the same id cannot appear twice)
-      if (sc2[b] == sc[a] && id2[b] == id[a]) ++b;
-      ++a;
-    } else {
-      o[k] = sc2[b];
-      oi[k] = id2[b];
-      ++b;
-    }
+// Insert (x, v) into a descending top-k list held in registers (constant indices only).
+__device__ __forceinline__ void cswap(float (&sc)[kTopK], int (&id)[kTopK], int k) {
+  if (better(sc[k + 1], id[k + 1], sc[k], id[k])) {
+    const float ts = sc[k];
+    const int ti = id[k];
+    sc[k] = sc[k + 1];
+    id[k] = id[k + 1];
+    sc[k + 1] = ts;
+    id[k + 1] = ti;
   }
+}
+__device__ __forceinline__ void topk_insert(float (&sc)[kTopK], int (&id)[kTopK], float x, int v) {
+  if (!better(x, v, sc[kTopK - 1], id[kTopK - 1])) return;
+  sc[kTopK - 1] = x;
+  id[kTopK - 1] = v;
 #pragma unroll
-  for (int k = 0; k < kTopK; ++k) {
-    sc[k] = o[k];
-    id[k] = oi[k];
-  }
+  for (int k = kTopK - 2; k >= 0; --k) cswap(sc, id, k);
 }
 
 __device__ __forceinline__ float exact_logit(const LmMergeArgs& a, int v, const float* h) {
@@ -71,6 +62,7 @@ __device__ __forceinline__ float exact_logit(const LmMergeArgs& a, int v, const 
       acc = fmaf(ev.x, hv.x, fmaf(ev.y, hv.y, fmaf(ev.z, hv.z, fmaf(ev.w, hv.w, acc))));
     }
   } else {
+#pragma unroll 8
     for (int d = lane * 4; d < a.D; d += 128) {
       const uint2 raw = *reinterpret_cast<const uint2*>(a.Eb + tiled_index(v, d, a.D));
       const __nv_bfloat162 e01 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
@@ -85,11 +77,23 @@ __device__ __forceinline__ float exact_logit(const LmMergeArgs& a, int v, const 
   return warp_sum(acc);
 }
 
-// One warp per row.
-__global__ void lm_merge_kernel(const LmMergeArgs a) {
-  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (r >= a.rows) return;
+// One CTA of kMergeWarps warps per row: every thread folds a strided subset of
+// the slab records into a register top-k + LSE, the warps combine by butterfly,
+// warp 0 combines the warps in a fixed order, and 4 warps re-score the 4
+// finalists exactly in parallel.
+constexpr int kMergeWarps = 16;
+
+__global__ void __launch_bounds__(kMergeWarps * 32) lm_merge_kernel(const LmMergeArgs a) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float wsc[kMergeWarps][kTopK];
+  __shared__ int wid[kMergeWarps][kTopK];
+  __shared__ float wm[kMergeWarps], wsum[kMergeWarps];
+  __shared__ float fin_sc[kTopK], fin_logit[kTopK];
+  __shared__ int fin_id[kTopK];
+  __shared__ float row_m, row_s, row_sc0, row_sc3;
+  const int r = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bool sampling = a.inv_T > 0.f;
   float sc[kTopK];
   int id[kTopK];
@@ -99,13 +103,14 @@ __global__ void lm_merge_kernel(const LmMergeArgs a) {
     id[k] = 0x7fffffff;
   }
   float m = -INFINITY, s = 0.f;
-  for (int t = lane; t < a.n_tiles; t += 32) {
+  for (int t = threadIdx.x; t < a.n_tiles; t += blockDim.x) {
     const LmRec rec = a.rec[(size_t)t * a.rows + r];
-    topk_merge(sc, id, rec.sc, rec.id);
+#pragma unroll
+    for (int k = 0; k < kTopK; ++k) topk_insert(sc, id, rec.sc[k], rec.id[k]);
     if (sampling) lse_merge(m, s, rec.m, rec.s);
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
+  for (int o = 16; o > 0; o >>= 1) {  // both partners end with the same list (disjoint sets)
     float sc2[kTopK];
     int id2[kTopK];
 #pragma unroll
@@ -115,49 +120,79 @@ __global__ void lm_merge_kernel(const LmMergeArgs a) {
     }
     const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
     const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    topk_merge(sc, id, sc2, id2);
+#pragma unroll
+    for (int k = 0; k < kTopK; ++k) topk_insert(sc, id, sc2[k], id2[k]);
     if (sampling) lse_merge(m, s, m2, s2);
   }
-  // exact re-scoring of the finalists
-  const float* h = a.h + (size_t)r * a.D;
-  uint32_t pos = 0, req = 0;
-  if (sampling) {
-    req = (uint32_t)(r / a.K);
-    pos = (uint32_t)(a.pos[req] + (r % a.K) + 1);
-  }
-  float best = -INFINITY, blogit = 0.f;
-  int bid = 0x7fffffff;
-#pragma unroll
-  for (int k = 0; k < kTopK; ++k) {
-    const int v = id[k];
-    if (v < 0 || v >= a.V) continue;  // fewer than kTopK ids (tiny vocabularies)
-    const float l = exact_logit(a, v, h);
-    float x = l;
-    if (sampling) {
-      const uint4 w = philox((uint32_t)v >> 2, pos, req, kTagGumbel, a.k0, a.k1);
-      const uint32_t wx[4] = {w.x, w.y, w.z, w.w};
-      x = l * a.inv_T + gumbel_from_bits(wx[v & 3]);
-    }
-    if (better(x, v, best, bid)) {
-      best = x;
-      bid = v;
-      blogit = l;
-    }
-  }
   if (lane == 0) {
+#pragma unroll
+    for (int k = 0; k < kTopK; ++k) {
+      wsc[warp][k] = sc[k];
+      wid[warp][k] = id[k];
+    }
+    wm[warp] = m;
+    wsum[warp] = s;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kMergeWarps; ++w) {
+#pragma unroll
+      for (int k = 0; k < kTopK; ++k) topk_insert(sc, id, wsc[w][k], wid[w][k]);
+      if (sampling) lse_merge(m, s, wm[w], wsum[w]);
+    }
+#pragma unroll
+    for (int k = 0; k < kTopK; ++k) fin_id[k] = id[k];
+    row_m = m;
+    row_s = s;
+    row_sc0 = sc[0];
+    row_sc3 = sc[kTopK - 1];
+  }
+  __syncthreads();
+  // exact re-scoring: warp k < kTopK takes finalist k
+  const float* h = a.h + (size_t)r * a.D;
+  if (warp < kTopK) {
+    const int v = fin_id[warp];
+    float x = -INFINITY, l = 0.f;
+    if (v >= 0 && v < a.V) {  // fewer than kTopK ids on tiny vocabularies
+      l = exact_logit(a, v, h);
+      x = l;
+      if (sampling) {
+        const uint32_t req = (uint32_t)(r / a.K);
+        const uint32_t pos = (uint32_t)(a.pos[req] + (r % a.K) + 1);
+        const uint4 w = philox((uint32_t)v >> 2, pos, req, kTagGumbel, a.k0, a.k1);
+        const uint32_t wx[4] = {w.x, w.y, w.z, w.w};
+        x = l * a.inv_T + gumbel_from_bits(wx[v & 3]);
+      }
+    }
+    if (lane == 0) {
+      fin_sc[warp] = x;
+      fin_logit[warp] = l;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float best = -INFINITY, blogit = 0.f;
+    int bid = 0x7fffffff;
+    for (int k = 0; k < kTopK; ++k) {
+      const int v = fin_id[k];
+      if (v < 0 || v >= a.V) continue;
+      if (better(fin_sc[k], v, best, bid)) {
+        best = fin_sc[k];
+        bid = v;
+        blogit = fin_logit[k];
+      }
+    }
     a.cand[r] = bid;
     if (a.qs) {
       a.qs[r].logit = blogit;
-      a.qs[r].lse = sampling ? m + logf(s) : NAN;
+      a.qs[r].lse = sampling ? row_m + logf(row_s) : NAN;
     }
-    if (a.counters && sc[kTopK - 1] > sc[0] - kCloseCall) atomicAdd(a.counters + 4, 1ull);
+    if (a.counters && row_sc3 > row_sc0 - kCloseCall) atomicAdd(a.counters + 4, 1ull);
   }
 }
 
 cudaError_t launch_lm_merge(const LmMergeArgs& a, cudaStream_t s) {
-  const int wpb = 8;
-  lm_merge_kernel<<<(a.rows + wpb - 1) / wpb, wpb * 32, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(lm_merge_kernel, dim3(a.rows), dim3(kMergeWarps * 32), 0, s, a);
 }
 
 }  // namespace dlite

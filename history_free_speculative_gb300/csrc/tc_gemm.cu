@@ -222,6 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   fence_after();
   const uint32_t tmem = *tmem_holder;
+  pdl_trigger();
 
   // Role loops run with the whole warp converged: every lane waits on the
   // barrier, one lane issues (a lone active lane beside 31 lanes parked at a
@@ -231,26 +232,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     // rest of the 128-row smem tile holds stale data that only feeds unused TMEM lanes)
     const uint32_t bytes = (uint32_t)WP * wtile + (uint32_t)(NMT * XP) * (uint32_t)p.x_box * 128u;
     const uint32_t a_slot = a_slot_bytes(p.x_box);
-    for (int i = 0; i < nkb; ++i) {
+    // k blocks in a per-CTA rotated order: concurrent CTAs fetch different
+    // activation tiles instead of all hitting the same L2 lines
+    auto load_w = [&](int i, int s) {
+      const uint32_t st = su32(smem + (size_t)s * p.stage_bytes);
+      const uint32_t fb = full0 + 8 * s;
+      const int kb = kb0 + (i + rot) % nkb;
+      mbar_expect_tx(fb, bytes);
+      const uint32_t wst = st + (uint32_t)(NMT * XP) * a_slot;
+      tma_load_4d(wst, &mw0, fb, kb, o0 >> 6);
+      if (WP == 2) tma_load_4d(wst + wtile, &mw1, fb, kb, o0 >> 6);
+    };
+    auto load_x = [&](int i, int s) {
+      const uint32_t st = su32(smem + (size_t)s * p.stage_bytes);
+      const uint32_t fb = full0 + 8 * s;
+      const int kx = (kb0 + (i + rot) % nkb) * 64;
+#pragma unroll
+      for (int mt = 0; mt < NMT; ++mt)
+#pragma unroll
+        for (int pl = 0; pl < XP; ++pl)
+          tma_load_2d(st + (uint32_t)(mt * XP + pl) * a_slot, pl ? &mx1 : &mx0, fb, kx, m0 + mt * 128);
+    };
+    // Weights do not depend on the previous kernel: stream the first stages'
+    // weight tiles before waiting for it, then the activations.
+    const int pre = nkb < p.stages ? nkb : p.stages;
+    if (lane == 0)
+      for (int i = 0; i < pre; ++i) load_w(i, i);
+    __syncwarp();
+    pdl_wait();
+    if (lane == 0)
+      for (int i = 0; i < pre; ++i) load_x(i, i);
+    __syncwarp();
+    for (int i = pre; i < nkb; ++i) {
       const int s = i % p.stages;
       const uint32_t it = (uint32_t)(i / p.stages);
-      if (i >= p.stages && !mbar_wait_warp(empty0 + 8 * s, (it - 1) & 1, p.status)) break;
+      if (!mbar_wait_warp(empty0 + 8 * s, (it - 1) & 1, p.status)) break;
       if (lane == 0) {
-        const uint32_t st = su32(smem + (size_t)s * p.stage_bytes);
-        const uint32_t fb = full0 + 8 * s;
-        mbar_expect_tx(fb, bytes);
-        // k blocks in a per-CTA rotated order: concurrent CTAs fetch different
-        // activation tiles instead of all hitting the same L2 lines
-        const int kb = kb0 + (i + rot) % nkb;
-        const int kx = kb * 64;
-        const uint32_t wst = st + (uint32_t)(NMT * XP) * a_slot;
-        tma_load_4d(wst, &mw0, fb, kb, o0 >> 6);
-        if (WP == 2) tma_load_4d(wst + wtile, &mw1, fb, kb, o0 >> 6);
-#pragma unroll
-        for (int mt = 0; mt < NMT; ++mt)
-#pragma unroll
-          for (int pl = 0; pl < XP; ++pl)
-            tma_load_2d(st + (uint32_t)(mt * XP + pl) * a_slot, pl ? &mx1 : &mx0, fb, kx, m0 + mt * 128);
+        load_w(i, s);
+        load_x(i, s);
       }
       __syncwarp();
     }
@@ -303,6 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int c_lo = eg * ncol, c_hi = c_lo + ncol;
     const bool got = mbar_wait_warp(accf, 0, p.status);
     fence_after();
+    pdl_wait();  // outputs may still be read by the previous kernel
     if (got) {
       for (int mt = 0; mt < NMT; ++mt) {
         const int r = m0 + mt * 128 + q * 32 + lane;
@@ -464,7 +484,8 @@ Plan plan(int rows, int outs, int K, int xplanes, int wplanes, bool lm) {
       if (stages > 8) stages = 8;
       if (stages < 2) continue;
       const int slabs = (outs + N - 1) / N;
-      const int smax = lm ? 1 : (kblocks < 16 ? kblocks : 16);
+      // at most 4 k-splits: every consumer sums the splits on its critical path
+      const int smax = lm ? 1 : (kblocks < 4 ? kblocks : 4);
       for (int S = 1; S <= smax; ++S) {
         const int kbps = (kblocks + S - 1) / S;
         const int Se = (kblocks + kbps - 1) / kbps;
@@ -548,8 +569,8 @@ cudaError_t launch(const Plan& pl, const CUtensorMap* x0, const CUtensorMap* x1,
   prm.stage_bytes = pl.stage_bytes;
   prm.tmem_cols = (uint32_t)pl.tmem_cols;
   dim3 grid((prm.outs + pl.N - 1) / pl.N, pl.S, pl.groups);
-  fn<<<grid, kThreads, smem_bytes(pl), s>>>(*x0, x1 ? *x1 : *x0, *w0, w1 ? *w1 : *w0, prm);
-  return cudaGetLastError();
+  return launch_pdl(fn, grid, dim3(kThreads), smem_bytes(pl), s, *x0, x1 ? *x1 : *x0, *w0,
+                    w1 ? *w1 : *w0, prm);
 }
 
 }  // namespace tc
