@@ -42,6 +42,30 @@ def dist_env():
     return ws, rank, local
 
 
+KERNEL_SOURCES = ["tc_gemm.cu", "tc_gemm.h", "common.cuh", "internal.h"]
+
+
+def lm_head_traffic():
+    """DRAM bytes per LM-head launch from the committed ncu summary, or None when
+    the kernel sources changed since that capture."""
+    import hashlib
+    prof = os.path.join(ROOT, "profiles", "lm_head_tc_gemm_qwen3-8b-b32.md")
+    if not os.path.exists(prof):
+        return None
+    vals = {}
+    for line in open(prof):
+        if ":" in line and line.strip().split(":")[0] in ("traffic_bytes_per_launch", "kernel_sources_sha256"):
+            k, v = line.strip().split(":", 1)
+            vals[k] = v.strip()
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "history_free_speculative_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    if vals.get("kernel_sources_sha256") != h.hexdigest():
+        return None
+    return int(vals["traffic_bytes_per_launch"])
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -247,7 +271,8 @@ def run_gpu(args):
     else:
         roof = {"bound": "tensor", "achieved": round(achieved_tf, 1), "peak": tf_sus, "unit": "TFLOP/s",
                 "frac": round(achieved_tf / tf_sus, 4)}
-    roof.update({"kernel": "lm_head", "traffic": None, "peak_source": peak_src,
+    traffic = lm_head_traffic() if (cfg.D == 4096 and B == 32) else None
+    roof.update({"kernel": "lm_head", "traffic": traffic, "peak_source": peak_src,
                  "algorithmic_bytes_per_launch": lm_bytes, "algorithmic_flops_per_launch": lm_flops,
                  "ms_per_launch": round(lm_ms, 4)})
     round_bytes = rp.round_bytes(cfg, B)

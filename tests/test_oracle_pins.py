@@ -395,3 +395,22 @@ def test_mirror_differs_from_pure_by_bf16_scale():
     b1 = O.backbone(hidden[0], anchor[0], W, cfg, mirror=True)
     rel = np.linalg.norm(b1 - b0) / np.linalg.norm(b0)
     assert 1e-5 < rel < 2e-2
+
+
+def test_ffn_gate_goes_through_silu_up_is_linear():
+    """silu(y W_g^T) * (y W_u^T): the FFN increment is linear in W_u and W_d but not in W_g,
+    so a swapped gate / up matrix or a missing nonlinearity changes which scaling is linear."""
+    cfg = _tiny()
+    W = _weights(cfg, seed=23)
+    rng = np.random.default_rng(24)
+    x = rng.normal(size=(cfg.K + 1, cfg.D))
+    z = rng.normal(size=(cfg.m, cfg.D))
+    base = dict(W["layers"][0])
+    base["Wo"] = torch.zeros_like(base["Wo"])          # attention contributes nothing
+    delta = O.backbone_layer(x, z, base, cfg) - x
+    for name, linear in (("Wu", True), ("Wd", True), ("Wg", False)):
+        Wl = dict(base)
+        Wl[name] = base[name] * 2.0          # exact in binary floating point
+        d2 = O.backbone_layer(x, z, Wl, cfg) - x
+        close = np.allclose(d2, 2.0 * delta, rtol=1e-9, atol=1e-12)
+        assert close == linear, name
