@@ -92,21 +92,21 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
             t0 = time.time()
-            while len(self.lines) < 3 and time.time() - t0 < 10:
-                time.sleep(0.05)
-            self.skip = len(self.lines)
+            while len(self.lines) < 2 and time.time() - t0 < 10:
+                time.sleep(0.02)
         except Exception:
             self.proc = None
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
 
-    def stop(self):
+    def stop(self, t_begin, t_end):
+        """Summarise the samples taken between t_begin and t_end (wall clock)."""
         if not self.proc:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -116,7 +116,9 @@ class ClockSampler:
             self.proc.kill()
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in self.lines[getattr(self, "skip", 0):]:
+        for ts, l in self.lines:
+            if not (t_begin <= ts <= t_end):
+                continue
             f = [x.strip() for x in l.split(",")]
             if len(f) < 9:
                 continue
@@ -215,6 +217,7 @@ def run_gpu(args):
     if clocks:
         clocks.start()
     step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    t_begin = time.time()
     with torch.cuda.stream(stream):
         ev0.record(stream)
         step_ev[0].record(stream)
@@ -224,7 +227,8 @@ def run_gpu(args):
             step_ev[i + 1].record(stream)
         ev1.record(stream)
     stream.synchronize()
-    clk = clocks.stop() if clocks else {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["not sampled"]}
+    t_end = time.time()
+    clk = clocks.stop(t_begin, t_end) if clocks else {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["not sampled"]}
     step_ms = sorted(step_ev[i].elapsed_time(step_ev[i + 1]) for i in range(args.steps))
     barrier()
     ms = ev0.elapsed_time(ev1)
@@ -442,7 +446,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="qwen3-8b-b32", choices=sorted(wk.WORKLOADS))

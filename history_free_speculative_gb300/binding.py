@@ -70,6 +70,7 @@ _SIGS = {
     "dlite_round_host": (_I, [_P, _I, _P, _P, _P, _P, _P, _F, _U64, _P, _P, _P, _P, _P]),
     "dlite_device_status": (_I, [_P, _I, ctypes.POINTER(_I), _P]),
     "dlite_status_string": (ctypes.c_char_p, [_I]),
+    "dlite_last_cuda_error": (ctypes.c_char_p, []),
     "dlite_launch_count": (_I, [_P, _I, _F]),
     "dlite_counters": (_I, [_P, _I, ctypes.POINTER(ctypes.c_int64), _P]),
     "dlite_selftest_gemm": (_I, [_I, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P,
@@ -125,6 +126,8 @@ def _stream(stream):
 
 def _check(code, what):
     if code != 0:
+        if code == -3 and _lib is not None:   # DLITE_ERR_CUDA: name the runtime error
+            what = f"{what} [{_lib.dlite_last_cuda_error().decode()}]"
         raise DliteError(code, what)
 
 

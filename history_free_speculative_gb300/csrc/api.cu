@@ -34,7 +34,7 @@ struct dlite_handle {
   int qd = 0, kvd = 0;
   int Rp = 0;                       // R padded to a multiple of 64 (GEMM k extent)
   int Lcap = 0, Ccap = 0, Hcap = 0;  // activation row capacities (multiples of 128)
-  int lm_tiles = 0;
+  int num_sms = 0;  // SMs of the device (persistent LM-head grid)
   std::vector<void*> allocs;
   std::vector<MapEntry> maps;
 
@@ -83,10 +83,15 @@ struct dlite_handle {
 
 namespace {
 
-#define CK(call)                                   \
-  do {                                             \
-    cudaError_t e_ = (call);                       \
-    if (e_ != cudaSuccess) return DLITE_ERR_CUDA;  \
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+#define CK(call)                     \
+  do {                               \
+    cudaError_t e_ = (call);         \
+    if (e_ != cudaSuccess) {         \
+      g_last_cuda_error = e_;        \
+      return DLITE_ERR_CUDA;         \
+    }                                \
   } while (0)
 
 // Record an event after a launch when the handle is in profiling mode.
@@ -394,39 +399,66 @@ int run_lm_head(dlite_handle* h, int B, float temperature, uint64_t seed, const 
                 int32_t* cand, dlite_qstats* qs, cudaStream_t s) {
   const dlite_config& c = h->cfg;
   const int rows = B * c.K;
-  const tc::Plan pl = lm_plan(h, rows);
-  if (!pl.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
-  const int xb = tc::x_box_rows(rows);
-  h->maps.reserve(h->maps.size() + 4);
-  const CUtensorMap* x0 = get_map(h, h->hp[0], h->Hcap, c.D, xb);
-  const CUtensorMap* w0 = get_map(h, h->E[0], h->Vp, c.D, pl.N, true);
-  if (!x0 || !w0) return DLITE_ERR_CUDA;
-  tc::TcParams prm;
-  prm.rows = rows;
-  prm.outs = c.V;
-  prm.K = c.D;
-  prm.xplanes = 1;
-  prm.wplanes = 1;
-  prm.mode = 1;
-  prm.x_box = xb;
-  prm.rec = h->lmrec;
-  prm.inv_T = temperature > 0.f ? 1.f / temperature : 0.f;
-  seed_key(seed, &prm.k0, &prm.k1);
-  prm.pos = pos;
-  prm.K_draft = c.K;
-  prm.status = h->status;
-  CK(tc::launch(pl, x0, nullptr, w0, nullptr, prm, s));
+  const float inv_T = temperature > 0.f ? 1.f / temperature : 0.f;
+  uint32_t k0 = 0, k1 = 0;
+  seed_key(seed, &k0, &k1);
+  int n_tiles = 0;
+  const tc::LmPlan lp = tc::lm_plan_persistent(rows, c.V, c.D, h->num_sms);
+  if (lp.ok) {  // persistent kernel, epilogue overlapped with the E stream
+    h->maps.reserve(h->maps.size() + 4);
+    const CUtensorMap* x0 = get_map(h, h->hp[0], h->Hcap, c.D, lp.x_box);
+    const CUtensorMap* w0 = get_map(h, h->E[0], h->Vp, c.D, lp.N, true);
+    if (!x0 || !w0) return DLITE_ERR_CUDA;
+    tc::LmParams prm;
+    prm.rows = rows;
+    prm.outs = c.V;
+    prm.rec = h->lmrec;
+    prm.inv_T = inv_T;
+    prm.k0 = k0;
+    prm.k1 = k1;
+    prm.pos = pos;
+    prm.K_draft = c.K;
+    prm.status = h->status;
+    CK(tc::launch_lm_persistent(lp, x0, w0, prm, s));
+    n_tiles = lp.grid * lp.groups;
+  } else {  // one slab per CTA
+    const tc::Plan pl = lm_plan(h, rows);
+    if (!pl.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
+    const int xb = tc::x_box_rows(rows);
+    h->maps.reserve(h->maps.size() + 4);
+    const CUtensorMap* x0 = get_map(h, h->hp[0], h->Hcap, c.D, xb);
+    const CUtensorMap* w0 = get_map(h, h->E[0], h->Vp, c.D, pl.N, true);
+    if (!x0 || !w0) return DLITE_ERR_CUDA;
+    tc::TcParams prm;
+    prm.rows = rows;
+    prm.outs = c.V;
+    prm.K = c.D;
+    prm.xplanes = 1;
+    prm.wplanes = 1;
+    prm.mode = 1;
+    prm.x_box = xb;
+    prm.rec = h->lmrec;
+    prm.inv_T = inv_T;
+    prm.k0 = k0;
+    prm.k1 = k1;
+    prm.pos = pos;
+    prm.K_draft = c.K;
+    prm.status = h->status;
+    CK(tc::launch(pl, x0, nullptr, w0, nullptr, prm, s));
+    n_tiles = (c.V + pl.N - 1) / pl.N * tc::kEpiGroups;
+  }
   mark(h, "lm_head");
   LmMergeArgs mg;
   mg.rec = h->lmrec;
-  mg.n_tiles = (c.V + pl.N - 1) / pl.N * tc::kEpiGroups;
+  mg.n_tiles = n_tiles;
   mg.rows = rows;
   mg.K = c.K;
   mg.D = c.D;
   mg.V = c.V;
-  mg.inv_T = prm.inv_T;
-  mg.k0 = prm.k0;
-  mg.k1 = prm.k1;
+  mg.inv_T = inv_T;
+  mg.T = (double)temperature;
+  mg.k0 = k0;
+  mg.k1 = k1;
   mg.pos = pos;
   mg.h = h->hs;
   if (h->f32)
@@ -467,6 +499,13 @@ const char* dlite_status_string(int st) {
     case DLITE_ERR_OOM: return "device allocation failed";
     default: return "unknown status";
   }
+}
+
+const char* dlite_last_cuda_error(void) {
+  static thread_local char buf[256];
+  snprintf(buf, sizeof(buf), "%s: %s", cudaGetErrorName(g_last_cuda_error),
+           cudaGetErrorString(g_last_cuda_error));
+  return buf;
 }
 
 void dlite_destroy(dlite_handle* h) {
@@ -603,6 +642,11 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
     if (!pl.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
     const size_t v3 = (size_t)((V + pl.N - 1) / pl.N) * tc::kEpiGroups * H;
     lme = v3 > lme ? v3 : lme;
+    const tc::LmPlan lp = tc::lm_plan_persistent(H, V, D, h->num_sms);
+    if (lp.ok) {
+      const size_t v4 = (size_t)lp.grid * lp.groups * H;
+      lme = v4 > lme ? v4 : lme;
+    }
   }
   AL(h->part, pe);
   AL(h->part2, pe2);
@@ -653,6 +697,15 @@ int dlite_create(const dlite_config* cfg, const dlite_weights* w, dlite_handle**
   h->Lcap = (cfg->B_max * (cfg->K + 1) + 127) / 128 * 128;
   h->Ccap = (cfg->B_max * cfg->m + 127) / 128 * 128;
   h->Hcap = (cfg->B_max * cfg->K + 127) / 128 * 128;
+  {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        h->num_sms < 1) {
+      delete h;
+      return DLITE_ERR_CUDA;
+    }
+  }
   const int r = create_impl(h, w);
   if (r) {
     dlite_destroy(h);

@@ -28,15 +28,16 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-// LM-head record of one vocabulary slab for one row: the 4 best
-// (score, id) of the slab in descending order (greedy: logit; sampling:
-// logit/T + Gumbel), from the bf16 product, and the slab's LSE partials.
+// LM-head record of a set of vocabulary columns for one row: the 4 best
+// (score, id) in descending order (greedy: logit; sampling: the base-2
+// Gumbel-max score logit log2(e)/T - log2(-log2 u)), from the bf16 product,
+// and the LSE partials of those columns in base 2.
 constexpr int kTopK = 4;
 struct LmRec {
   float sc[kTopK];
   int id[kTopK];
-  float m;  // max of logit/T over the slab (sampling)
-  float s;  // sum of exp(logit/T - m) over the slab (sampling)
+  float m;  // max of logit log2(e) / T over the columns (sampling)
+  float s;  // sum of 2^(logit log2(e) / T - m) over the columns (sampling)
 };
 
 // Merge of the LM-head records and exact re-scoring of the finalists.
@@ -44,6 +45,7 @@ struct LmMergeArgs {
   const LmRec* rec = nullptr;  // [n_tiles][rows]
   int n_tiles = 0, rows = 0, K = 0, D = 0, V = 0;
   float inv_T = 0.f;           // 0 = greedy
+  double T = 0.0;              // the temperature (float32 value) for the re-scoring
   uint32_t k0 = 0, k1 = 0;
   const int64_t* pos = nullptr;
   const float* h = nullptr;    // [rows, D] fp32 head states

@@ -10,11 +10,19 @@
 // gap between the first and the fifth best score, so the re-scored winner is
 // the winner of the exact product; rows where the fourth finalist is within
 // kCloseCall of the first are counted as close calls.
+//
+// Sampling records are in base-2 units (score = logit log2(e) / T minus
+// log2(-log2 u), an increasing map of the Gumbel-max score; LSE partials
+// m = max logit log2(e) / T, s = sum 2^(. - m)); the finalists are re-scored
+// in natural units, logit / T - log(-log u), and the LSE is returned in
+// natural units.
 #include "internal.h"
 
 namespace dlite {
 
-constexpr float kCloseCall = 0.02f;  // score units (logit, or logit/T when sampling)
+constexpr float kCloseCall = 0.02f;  // natural score units (logit, or logit/T when sampling)
+constexpr float kLog2eM = 1.4426950408889634f;
+constexpr float kLn2M = 0.6931471805599453f;
 
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
   return v > bv || (v == bv && i < bi);
@@ -28,7 +36,7 @@ __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2
     return;
   }
   const float mm = fmaxf(m, m2);
-  s = s * __expf(m - mm) + s2 * __expf(m2 - mm);
+  s = s * exp2f(m - mm) + s2 * exp2f(m2 - mm);
   m = mm;
 }
 
@@ -89,7 +97,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lm_merge_kernel(const LmMerg
   __shared__ float wsc[kMergeWarps][kTopK];
   __shared__ int wid[kMergeWarps][kTopK];
   __shared__ float wm[kMergeWarps], wsum[kMergeWarps];
-  __shared__ float fin_sc[kTopK], fin_logit[kTopK];
+  __shared__ double fin_sc[kTopK];
+  __shared__ float fin_logit[kTopK];
   __shared__ int fin_id[kTopK];
   __shared__ float row_m, row_s, row_sc0, row_sc3;
   const int r = blockIdx.x;
@@ -152,7 +161,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lm_merge_kernel(const LmMerg
   const float* h = a.h + (size_t)r * a.D;
   if (warp < kTopK) {
     const int v = fin_id[warp];
-    float x = -INFINITY, l = 0.f;
+    double x = -INFINITY;
+    float l = 0.f;
     if (v >= 0 && v < a.V) {  // fewer than kTopK ids on tiny vocabularies
       l = exact_logit(a, v, h);
       x = l;
@@ -161,7 +171,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lm_merge_kernel(const LmMerg
         const uint32_t pos = (uint32_t)(a.pos[req] + (r % a.K) + 1);
         const uint4 w = philox((uint32_t)v >> 2, pos, req, kTagGumbel, a.k0, a.k1);
         const uint32_t wx[4] = {w.x, w.y, w.z, w.w};
-        x = l * a.inv_T + gumbel_from_bits(wx[v & 3]);
+        x = (double)l / a.T + gumbel_d(wx[v & 3]);
       }
     }
     if (lane == 0) {
@@ -171,12 +181,13 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lm_merge_kernel(const LmMerg
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    float best = -INFINITY, blogit = 0.f;
+    double best = -INFINITY;
+    float blogit = 0.f;
     int bid = 0x7fffffff;
     for (int k = 0; k < kTopK; ++k) {
       const int v = fin_id[k];
       if (v < 0 || v >= a.V) continue;
-      if (better(fin_sc[k], v, best, bid)) {
+      if (fin_sc[k] > best || (fin_sc[k] == best && v < bid)) {
         best = fin_sc[k];
         bid = v;
         blogit = fin_logit[k];
@@ -185,9 +196,10 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lm_merge_kernel(const LmMerg
     a.cand[r] = bid;
     if (a.qs) {
       a.qs[r].logit = blogit;
-      a.qs[r].lse = sampling ? row_m + logf(row_s) : NAN;
+      a.qs[r].lse = sampling ? (row_m + log2f(row_s)) * kLn2M : NAN;
     }
-    if (a.counters && row_sc3 > row_sc0 - kCloseCall) atomicAdd(a.counters + 4, 1ull);
+    const float band = sampling ? kCloseCall * kLog2eM : kCloseCall;
+    if (a.counters && row_sc3 > row_sc0 - band) atomicAdd(a.counters + 4, 1ull);
   }
 }
 

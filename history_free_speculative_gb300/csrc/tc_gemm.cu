@@ -10,166 +10,11 @@
 // thread), warps 2-5 = epilogue (warp w reads TMEM lanes 32*(w%4)..+31).
 // Every mbarrier wait is bounded (~2 s of %globaltimer); on expiry the kernel
 // flags the device status word and runs to its end instead of hanging.
-#include <cuda.h>
-
-#include "internal.h"
+#include "tc_device.cuh"
 #include "tc_gemm.h"
 
 namespace dlite {
 namespace tc {
-
-constexpr uint64_t kTimeoutNs = 2000000000ull;
-
-__device__ __forceinline__ uint32_t su32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ uint64_t gtimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait on phase `parity`; false after kTimeoutNs (status flagged).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status) {
-  if (mbar_try(bar, parity)) return true;
-  const uint64_t t0 = gtimer();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 128; ++i)
-      if (mbar_try(bar, parity)) return true;
-    if (gtimer() - t0 > kTimeoutNs) {
-      flag_status(status, kDevTimeout);
-      return false;
-    }
-  }
-}
-// Warp-wide bounded wait: every lane polls, lane 0's view decides, so the
-// result is uniform across the warp.
-__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, int* status) {
-  if (__shfl_sync(0xffffffffu, (int)mbar_try(bar, parity), 0)) return true;
-  const uint64_t t0 = gtimer();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 64; ++i)
-      if (__shfl_sync(0xffffffffu, (int)mbar_try(bar, parity), 0)) return true;
-    const int expired = __shfl_sync(0xffffffffu, (int)(gtimer() - t0 > kTimeoutNs), 0);
-    if (expired) {
-      if ((threadIdx.x & 31) == 0) flag_status(status, kDevTimeout);
-      return false;
-    }
-  }
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int x, int y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
-      "%4}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
-      : "memory");
-}
-// Weight tile load from the tiled layout: coordinates (0, 0, k block, 64-row slab).
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int c2, int c3) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
-      "%4, %5, %6}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(0), "r"(0), "r"(c2), "r"(c3)
-      : "memory");
-}
-
-// Shared-memory matrix descriptor: K-major tile, rows of 128 B, 128-byte
-// swizzle, 8-row groups 1024 B apart (stride byte offset), descriptor version 1.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, both K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
-}
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                          uint32_t accum) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accum)
-      : "memory");
-}
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
-}
-__device__ __forceinline__ void fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
-      "[%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
-  return v > bv || (v == bv && i < bi);
-}
-// Insert (x, v) into a descending top-k list (ties: lower id ranks first):
-// replace the last entry, then bubble it up with constant indices only.
-__device__ __forceinline__ void cswap(float (&sc)[kTopK], int (&id)[kTopK], int k) {
-  if (better(sc[k + 1], id[k + 1], sc[k], id[k])) {
-    const float ts = sc[k];
-    const int ti = id[k];
-    sc[k] = sc[k + 1];
-    id[k] = id[k + 1];
-    sc[k + 1] = ts;
-    id[k + 1] = ti;
-  }
-}
-__device__ __forceinline__ void topk_insert(float (&sc)[kTopK], int (&id)[kTopK], float x, int v) {
-  if (!better(x, v, sc[kTopK - 1], id[kTopK - 1])) return;
-  sc[kTopK - 1] = x;
-  id[kTopK - 1] = v;
-#pragma unroll
-  for (int k = kTopK - 2; k >= 0; --k) cswap(sc, id, k);
-}
-
-__device__ __forceinline__ void lse_add(float& m, float& s, float x) {
-  if (x > m) {
-    s = s * __expf(m - x) + 1.f;
-    m = x;
-  } else {
-    s += __expf(x - m);
-  }
-}
 
 // NMT: M-tiles per CTA; XP / WP: bf16 planes of X / W (products x0w0, + x1w0, + x0w1).
 // The MMA issue loop is fully unrolled over these so the issuing thread only
@@ -344,59 +189,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           // LM head: 4 best (score, id) and LSE partials of this vocabulary slab for row r
           const bool sampling = p.inv_T > 0.f;
-          float sc[kTopK];
-          int id[kTopK];
-#pragma unroll
-          for (int j = 0; j < kTopK; ++j) {
-            sc[j] = -INFINITY;
-            id[j] = 0x7fffffff;
-          }
-          float m = -INFINITY, s = 0.f;
-          uint32_t pos = 0, req = 0;
+          const float c2s = p.inv_T * kLog2e;
+          LmAcc acc;
+          lm_acc_init(acc);
           const bool valid = r < p.rows;
+          PhiloxRow pr = {0u, 0u, 0u};
           if (sampling && valid) {
-            req = (uint32_t)(r / p.K_draft);
-            pos = (uint32_t)(p.pos[req] + (r % p.K_draft) + 1);
+            const int req = r / p.K_draft;
+            const uint32_t pos = (uint32_t)(p.pos[req] + (r % p.K_draft) + 1);
+            pr = philox_row_init(pos, (uint32_t)req, kTagGumbel, p.k0, p.k1);
           }
           for (int c = c_lo; c < c_hi; c += 16) {
-            float v[16];
-            tmem_ld16(tbase + c, v);  // warp-collective: executed by every lane
-            if (valid) {
-#pragma unroll
-              for (int g = 0; g < 16; g += 4) {
-                const int v0 = o0 + c + g;  // multiple of 4: one Philox call per group
-                if (v0 < p.outs) {          // outs is a multiple of 8: whole groups only
-                  float x[4];
-                  if (sampling) {
-                    const uint4 w = philox((uint32_t)v0 >> 2, pos, req, kTagGumbel, p.k0, p.k1);
-                    const uint32_t wx[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                      const float lt = v[g + j] * p.inv_T;
-                      x[j] = lt + gumbel_from_bits(wx[j]);
-                      lse_add(m, s, lt);
-                    }
-                  } else {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) x[j] = v[g + j];
-                  }
-#pragma unroll
-                  for (int j = 0; j < 4; ++j) topk_insert(sc, id, x[j], v0 + j);
-                }
+            uint32_t raw[16];
+            tmem_ld16_nowait(tbase + c, raw);  // warp-collective: executed by every lane
+            tmem_wait_ld();
+            const int v0 = o0 + c;
+            const int nv = p.outs - v0;  // outs is a multiple of 8: whole groups of 4 only
+            if (valid && nv > 0) {
+              if (nv >= 16) {
+                if (sampling)
+                  lm_fold16<true, true>(acc, raw, v0, 16, c2s, pr, p.k0, p.k1);
+                else
+                  lm_fold16<false, true>(acc, raw, v0, 16, c2s, pr, p.k0, p.k1);
+              } else {
+                if (sampling)
+                  lm_fold16<true, false>(acc, raw, v0, nv, c2s, pr, p.k0, p.k1);
+                else
+                  lm_fold16<false, false>(acc, raw, v0, nv, c2s, pr, p.k0, p.k1);
               }
             }
           }
-          if (valid) {
-            LmRec rec;
-#pragma unroll
-            for (int j = 0; j < kTopK; ++j) {
-              rec.sc[j] = sc[j];
-              rec.id[j] = id[j];
-            }
-            rec.m = m;
-            rec.s = s;
-            p.rec[((size_t)blockIdx.x * kEpiGroups + eg) * p.rows + r] = rec;
-          }
+          if (valid) lm_acc_store(acc, p.rec + ((size_t)blockIdx.x * kEpiGroups + eg) * p.rows + r);
         }
       }
     }

@@ -53,6 +53,30 @@ inline int x_box_rows(int rows) { return rows >= 128 ? 128 : ((rows + 7) / 8) * 
 // Shared-memory slot of one activation tile: the loaded rows, rounded to a 1 KB swizzle atom group.
 __host__ __device__ inline uint32_t a_slot_bytes(int x_box) { return (uint32_t)((x_box * 128 + 1023) / 1024 * 1024); }
 size_t smem_bytes(const Plan& pl);
+
+// Persistent LM-head kernel (rows <= 256): one CTA per SM over the vocabulary
+// slabs, double-buffered TMEM accumulators, sampling epilogue overlapped with
+// the E stream; records are [grid * groups][rows].
+struct LmPlan {
+  bool ok = false;
+  int n_mt = 1, N = 0, x_box = 0, kblocks = 0, stages = 0, n_slabs = 0, grid = 0, groups = 0;
+  uint32_t stage_bytes = 0;
+};
+struct LmParams {
+  int rows = 0, outs = 0;
+  int n_slabs = 0, kblocks = 0, stages = 0, x_box = 0;
+  uint32_t stage_bytes = 0;
+  LmRec* rec = nullptr;
+  float inv_T = 0.f;  // 0 = greedy
+  uint32_t k0 = 0, k1 = 0;
+  const int64_t* pos = nullptr;
+  int K_draft = 1;
+  int* status = nullptr;
+};
+LmPlan lm_plan_persistent(int rows, int outs, int K, int num_sms);
+size_t lm_smem_bytes(const LmPlan& pl);
+cudaError_t launch_lm_persistent(const LmPlan& pl, const CUtensorMap* x, const CUtensorMap* w, LmParams prm,
+                                 cudaStream_t s);
 cudaError_t launch(const Plan& pl, const CUtensorMap* x0, const CUtensorMap* x1, const CUtensorMap* w0,
                    const CUtensorMap* w1, TcParams prm, cudaStream_t s);
 

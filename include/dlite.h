@@ -235,6 +235,11 @@ int dlite_device_status(dlite_handle *h, int clear, int *status_out, dlite_strea
 /* Static description of a status code. */
 const char *dlite_status_string(int status);
 
+/* Name and description of the CUDA runtime error behind the most recent
+ * DLITE_ERR_CUDA returned on the calling host thread ("no error" if none).
+ * The string is static; no GPU work is done. */
+const char *dlite_last_cuda_error(void);
+
 /* Profiling: run one draft (and, when target_tokens / target_probs is given,
  * its greedy / sampling verification) eagerly on `stream`, recording a CUDA
  * event after every kernel launch; synchronises `stream`. Writes the elapsed

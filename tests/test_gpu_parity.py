@@ -109,6 +109,49 @@ def test_tiny_round_sampling(tiny):
     check_candidates(np.stack(cands), np.stack(ocands), np.stack(gaps))
 
 
+@pytest.fixture(scope="module")
+def midvocab():
+    # bf16 drafter whose vocabulary spans several slabs per CTA with a ragged
+    # last slab (100000 is not a multiple of 128 or 256)
+    cfg = wk.shrink(wk.QWEN3_8B, D=512, F=1024, L_D=1, n_q=4, n_kv=2, R=64, V=100000, m=2)
+    W = wk.make_weights(cfg, 77)
+    dr = _drafter(cfg, W, B_max=40)
+    yield cfg, W, dr
+    dr.close()
+
+
+@pytest.mark.parametrize("B", [3, 20, 40])   # 21 rows (one M-tile), 140 (two), 280 (one-slab kernel)
+@pytest.mark.parametrize("T", [0.0, 0.7])
+def test_lm_head_identical_inputs_multislab(midvocab, B, T):
+    cfg, W, dr = midvocab
+    hs = _rand_hs(cfg, B, 6 + B)
+    pos = torch.arange(B, dtype=torch.int64) * 977 + 5
+    cand = torch.empty(B, cfg.K, dtype=torch.int32, device=DEV)
+    qs = torch.empty(B, cfg.K, 2, device=DEV)
+    dr.lm_head(hs.to(DEV), T, 123, pos.to(DEV), cand, qs)
+    torch.cuda.synchronize()
+    E = O.f64(W["E"])
+    ell = O.lm_logits(hs.reshape(-1, cfg.D).numpy().astype(np.float64), E).reshape(B, cfg.K, -1)
+    Tq = float(np.float32(T))
+    if T == 0.0:
+        s = ell
+    else:
+        s = ell / Tq + np.stack([[ph.gumbel_row(123, int(pos[b]) + i + 1, b, cfg.V)
+                                  for i in range(cfg.K)] for b in range(B)])
+    oc = s.argmax(axis=2)
+    part = np.partition(s, -2, axis=2)
+    c = cand.cpu().numpy()
+    check_candidates(c, oc, part[..., -1] - part[..., -2])
+    q = qs.cpu().numpy()
+    # the reported logit is the exact re-score of the chosen id
+    chosen = np.take_along_axis(ell, c[..., None].astype(np.int64), 2)[..., 0]
+    assert np.allclose(q[..., 0], chosen, rtol=1e-5, atol=1e-4)
+    if T > 0:
+        lse = np.log(np.exp(ell / Tq - (ell / Tq).max(axis=2, keepdims=True)).sum(axis=2)) + \
+            (ell / Tq).max(axis=2)
+        assert np.allclose(q[..., 1], lse, rtol=0, atol=2e-3)
+
+
 # ---------------------------------------------------------------- stage checks on identical inputs
 
 def _rand_hs(cfg, B, seed, scale=1.0):
