@@ -216,7 +216,25 @@ const CUtensorMap* get_map(dlite_handle* h, const void* base, int rows, int K, i
 
 // part[z][r][o] = sum over split z of X[r, :] . W[o, :], r < rows, o < outs.
 int gemm(dlite_handle* h, const char* name, const Operand& X, const Operand& W, int rows, int outs,
-         float* part, int* S_out, cudaStream_t s) {
+         float* part, Splits* sp_out, cudaStream_t s) {
+  if (tc::use_pair_engine(rows, X.n, W.n)) {  // 2-SM MMAs
+    const tc::PairPlan pp = tc::pair_plan(rows, outs, X.K, h->num_sms);
+    if (pp.ok) {
+      h->maps.reserve(h->maps.size() + 4);
+      const CUtensorMap* x0 = get_map(h, X.p[0], X.rows, X.K, 128);
+      const CUtensorMap* w0 = get_map(h, W.p[0], W.rows, W.K, 128, true);
+      if (!x0 || !w0) return DLITE_ERR_CUDA;
+      tc::PairParams prm;
+      prm.rows = rows;
+      prm.outs = outs;
+      prm.part = part;
+      prm.status = h->status;
+      if (sp_out) *sp_out = tc::pair_splits(pp);
+      CK(tc::launch_pair(pp, x0, w0, prm, s));
+      mark(h, name);
+      return DLITE_OK;
+    }
+  }
   const tc::Plan pl = tc::plan(rows, outs, X.K, X.n, W.n, false);
   if (!pl.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
   const int xb = tc::x_box_rows(rows);
@@ -236,7 +254,7 @@ int gemm(dlite_handle* h, const char* name, const Operand& X, const Operand& W, 
   prm.x_box = xb;
   prm.part = part;
   prm.status = h->status;
-  if (S_out) *S_out = pl.S;
+  if (sp_out) *sp_out = uniform_splits(pl.S);
   CK(tc::launch(pl, x0, x1, w0, w1, prm, s));
   mark(h, name);
   return DLITE_OK;
@@ -293,7 +311,7 @@ int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anch
 
   for (int l = 0; l < c.L_D; ++l) {
     const LayerW& w = h->layer[l];
-    int S1 = 1, S2 = 1;
+    Splits S1, S2;
     // local rows: y -> [q | k | v]; context rows: z -> [k | v] with the same bytes
     RUN(gemm(h, "gemm_qkv", opnd(h->y, h->np, h->Lcap, c.D), opnd(w.Wqkv, h->np, h->qd + 2 * h->kvd, c.D),
              L, h->qd + 2 * h->kvd, h->part, &S1, s));
@@ -303,9 +321,9 @@ int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anch
              2 * h->kvd, h->part2, &S2, s));
     AttnArgs at;
     at.part_loc = h->part;
-    at.S_loc = S1;
+    at.sp_loc = S1;
     at.part_ctx = h->part2;
-    at.S_ctx = S2;
+    at.sp_ctx = S2;
     at.rope_cos = h->rope_cos;
     at.rope_sin = h->rope_sin;
     at.B = B;
@@ -326,7 +344,7 @@ int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anch
              h->part, &S1, s));
     ResNormArgs rn;
     rn.part = h->part;
-    rn.S = S1;
+    rn.sp = S1;
     rn.rows = L;
     rn.D = c.D;
     rn.x = h->x;
@@ -346,7 +364,7 @@ int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anch
     RUN(gemm(h, "gemm_down", opnd(h->a, h->np, h->Lcap, c.F), opnd(w.Wd, h->np, c.D, c.F), L, c.D,
              h->part, &S1, s));
     ResNormArgs r2 = rn;
-    r2.S = S1;
+    r2.sp = S1;
     r2.tap_x = (taps && taps->x) ? taps->x + (size_t)l * L * c.D : nullptr;
     if (l + 1 < c.L_D) {
       r2.g = h->layer[l + 1].g_attn;
@@ -369,12 +387,12 @@ int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anch
 int run_seq_head(dlite_handle* h, int B, float* tap_hs, cudaStream_t s) {
   const dlite_config& c = h->cfg;
   const int rows = B * c.K;
-  int S = 1;
+  Splits S;
   RUN(gemm(h, "gemm_head_ce", opnd(h->bp, 2, h->Hcap, c.D), opnd(h->Wce, h->np, 2 * h->Rp, c.D), rows,
            2 * h->Rp, h->part, &S, s));
   ChainArgs ch;
   ch.part = h->part;
-  ch.S = S;
+  ch.S = S.S;  // the head products run on the one-CTA engine (uniform splits)
   ch.rows = rows;
   ch.Mt = h->Mt;
   ch.B = B;
@@ -390,7 +408,7 @@ int run_seq_head(dlite_handle* h, int B, float* tap_hs, cudaStream_t s) {
   mark(h, "head_chain");
   RUN(gemm(h, "gemm_head_p", opnd(h->tp, 2, h->Hcap, h->Rp), opnd(h->P, h->np, c.D, h->Rp), rows, c.D,
            h->part, &S, s));
-  CK(launch_head_out(h->part, S, rows, c.D, h->b, h->hs, h->hp, tap_hs, s));
+  CK(launch_head_out(h->part, S.S, rows, c.D, h->b, h->hs, h->hp, tap_hs, s));
   mark(h, "head_out");
   return DLITE_OK;
 }
@@ -406,9 +424,11 @@ int run_lm_head(dlite_handle* h, int B, float temperature, uint64_t seed, const 
   const tc::LmPlan lp = tc::lm_plan_persistent(rows, c.V, c.D, h->num_sms);
   if (lp.ok) {  // persistent kernel, epilogue overlapped with the E stream
     h->maps.reserve(h->maps.size() + 4);
-    const CUtensorMap* x0 = get_map(h, h->hp[0], h->Hcap, c.D, lp.x_box);
-    const CUtensorMap* w0 = get_map(h, h->E[0], h->Vp, c.D, lp.N, true);
-    if (!x0 || !w0) return DLITE_ERR_CUDA;
+    const CUtensorMap* x0 = get_map(h, h->hp[0], h->Hcap, c.D, lp.x_box0);
+    const CUtensorMap* x1 = lp.paired ? get_map(h, h->hp[0], h->Hcap, c.D, lp.x_box1) : nullptr;
+    // a pair's CTAs each load half of every slab
+    const CUtensorMap* w0 = get_map(h, h->E[0], h->Vp, c.D, lp.paired ? lp.N / 2 : lp.N, true);
+    if (!x0 || !w0 || (lp.paired && !x1)) return DLITE_ERR_CUDA;
     tc::LmParams prm;
     prm.rows = rows;
     prm.outs = c.V;
@@ -419,8 +439,8 @@ int run_lm_head(dlite_handle* h, int B, float temperature, uint64_t seed, const 
     prm.pos = pos;
     prm.K_draft = c.K;
     prm.status = h->status;
-    CK(tc::launch_lm_persistent(lp, x0, w0, prm, s));
-    n_tiles = lp.grid * lp.groups;
+    CK(tc::launch_lm_persistent(lp, x0, x1, w0, prm, s));
+    n_tiles = lp.n_units * lp.groups;
   } else {  // one slab per CTA
     const tc::Plan pl = lm_plan(h, rows);
     if (!pl.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
@@ -633,18 +653,22 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
       if (!pl.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
       const size_t v = (size_t)pl.S * st[0] * st[1];
       pe = v > pe ? v : pe;
+      const tc::PairPlan pp = tc::pair_plan(st[0], st[1], st[2], h->num_sms);
+      if (pp.ok && tc::use_pair_engine(st[0], st[3], h->np)) pe = (size_t)pp.S * st[0] * st[1] > pe ? (size_t)pp.S * st[0] * st[1] : pe;  // planes
     }
     const tc::Plan pc = tc::plan(C, 2 * h->kvd, D, h->np, h->np, false);
     if (!pc.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
     const size_t v2 = (size_t)pc.S * C * 2 * h->kvd;
     pe2 = v2 > pe2 ? v2 : pe2;
+    const tc::PairPlan pc2 = tc::pair_plan(C, 2 * h->kvd, D, h->num_sms);
+    if (pc2.ok && tc::use_pair_engine(C, h->np, h->np)) pe2 = (size_t)pc2.S * C * 2 * h->kvd > pe2 ? (size_t)pc2.S * C * 2 * h->kvd : pe2;
     const tc::Plan pl = lm_plan(h, H);
     if (!pl.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
     const size_t v3 = (size_t)((V + pl.N - 1) / pl.N) * tc::kEpiGroups * H;
     lme = v3 > lme ? v3 : lme;
     const tc::LmPlan lp = tc::lm_plan_persistent(H, V, D, h->num_sms);
     if (lp.ok) {
-      const size_t v4 = (size_t)lp.grid * lp.groups * H;
+      const size_t v4 = (size_t)lp.n_units * lp.groups * H;
       lme = v4 > lme ? v4 : lme;
     }
   }
@@ -912,6 +936,25 @@ int dlite_selftest_gemm(int rows, int outs, int K, int xplanes, int wplanes, con
     return DLITE_ERR_INVALID_ARG;
   if ((xplanes == 2 && !X1) || (wplanes == 2 && !W1)) return DLITE_ERR_INVALID_ARG;
   if (xplanes == 1 && wplanes == 2) return DLITE_ERR_INVALID_ARG;  // plane products x0w0 (+x1w0) (+x0w1)
+  const int wrows = (outs + 63) / 64 * 64;
+  if (!plan_override && tc::use_pair_engine(rows, xplanes, wplanes)) {  // the round's route
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return DLITE_ERR_CUDA;
+    const tc::PairPlan pp = tc::pair_plan(rows, outs, K, sms);
+    if (pp.ok && pp.S <= 16) {  // `part` holds 16 planes
+      CUtensorMap mx, mw;
+      if (!tc::make_map(&mx, X0, x_rows, K, 128) || !tc::make_map_tiled(&mw, W0, wrows, K, 128))
+        return DLITE_ERR_CUDA;
+      tc::PairParams prm;
+      prm.rows = rows;
+      prm.outs = outs;
+      prm.part = part;
+      prm.status = status;
+      CK(tc::launch_pair(pp, &mx, &mw, prm, (cudaStream_t)stream));
+      return pp.S;
+    }
+  }
   tc::Plan pl = tc::plan(rows, outs, K, xplanes, wplanes, false);
   if (!pl.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
   if (plan_override) {  // {N, S, stages}; 0 keeps the planner's choice
@@ -934,7 +977,6 @@ int dlite_selftest_gemm(int rows, int outs, int K, int xplanes, int wplanes, con
   }
   CUtensorMap mx0, mx1, mw0, mw1;
   const int xb = tc::x_box_rows(rows);
-  const int wrows = (outs + 63) / 64 * 64;
   if (!tc::make_map(&mx0, X0, x_rows, K, xb) || !tc::make_map_tiled(&mw0, W0, wrows, K, pl.N))
     return DLITE_ERR_CUDA;
   if (xplanes == 2 && !tc::make_map(&mx1, X1, x_rows, K, xb)) return DLITE_ERR_CUDA;

@@ -28,6 +28,34 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Layout of the fp32 partial products of one GEMM, part[s][rows][outs]: the
+// product is the sum of the first n(r, c) planes at (r, c). Uniform split-K
+// (N == 0): n = S everywhere. Stream-K (N > 0): tiles of 256 rows x N outputs
+// (tile index (r / 256) * slabs + c / N), each tile's kb k blocks in order
+// units tile * kb .. tile * kb + kb - 1 of U units shared by G workers, worker
+// p owning units [p U / G, (p + 1) U / G); the workers that share a tile write
+// planes 0, 1, ... in order.
+struct Splits {
+  int S = 1;
+  int N = 0;
+  int slabs = 0, kb = 0, G = 0;
+  long long U = 0;
+};
+__host__ __device__ __forceinline__ long long splits_owner(const Splits& s, long long u) {
+  return ((u + 1) * s.G - 1) / s.U;
+}
+__host__ __device__ __forceinline__ int splits_at(const Splits& s, int row, int col) {
+  if (!s.N) return s.S;
+  const long long tile = (long long)(row >> 8) * s.slabs + col / s.N;
+  const long long u0 = tile * s.kb;
+  return (int)(splits_owner(s, u0 + s.kb - 1) - splits_owner(s, u0) + 1);
+}
+inline Splits uniform_splits(int S) {
+  Splits sp;
+  sp.S = S;
+  return sp;
+}
+
 // LM-head record of a set of vocabulary columns for one row: the 4 best
 // (score, id) in descending order (greedy: logit; sampling: the base-2
 // Gumbel-max score logit log2(e)/T - log2(-log2 u)), from the bf16 product,

@@ -178,10 +178,10 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(AttnArgs a) {
   float* vs = ks + Tk * LD;     // [Tk][LD]
   const size_t sl = (size_t)a.B * K1 * ldl, sc = (size_t)a.B * a.m * ldc;
   auto loc4 = [&](int row, int col) {
-    return sum_splits4(a.part_loc + (size_t)(b * K1 + row) * ldl + col, sl, a.S_loc);
+    return sum_splits4(a.part_loc + (size_t)(b * K1 + row) * ldl + col, sl, splits_at(a.sp_loc, b * K1 + row, col));
   };
   auto ctx4 = [&](int row, int col) {
-    return sum_splits4(a.part_ctx + (size_t)(b * a.m + row) * ldc + col, sc, a.S_ctx);
+    return sum_splits4(a.part_ctx + (size_t)(b * a.m + row) * ldc + col, sc, splits_at(a.sp_ctx, b * a.m + row, col));
   };
   auto rnd4 = [&](float4 v) {
     return a.round_bf16 ? make_float4(round_bf16(v.x), round_bf16(v.y), round_bf16(v.z), round_bf16(v.w)) : v;
@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(kRowThreads) resnorm_kernel(ResNormArgs a) {
     const int i = threadIdx.x + k * kRowThreads;
     if (i < n4) {
       float4 x = *reinterpret_cast<const float4*>(a.x + (size_t)r * D + 4 * i);
-      x = f4add(x, sum_splits4(a.part + (size_t)r * D + 4 * i, stride, a.S));
+      x = f4add(x, sum_splits4(a.part + (size_t)r * D + 4 * i, stride, splits_at(a.sp, r, 4 * i)));
       *reinterpret_cast<float4*>(a.x + (size_t)r * D + 4 * i) = x;
       if (a.tap_x) *reinterpret_cast<float4*>(a.tap_x + (size_t)r * D + 4 * i) = x;
       v[k] = x;
@@ -328,7 +328,7 @@ cudaError_t launch_resnorm(const ResNormArgs& a, cudaStream_t s) {
 
 // ---------------------------------------------------------------- SwiGLU epilogue
 // a[r, f] = silu(sum_s part[s][r][f]) * sum_s part[s][r][F + f], float4 per thread.
-__global__ void swiglu_kernel(const float* part, int S, int rows, int F, bf16* o0, bf16* o1, int no) {
+__global__ void swiglu_kernel(const float* part, Splits sp, int rows, int F, bf16* o0, bf16* o1, int no) {
   pdl_trigger();
   pdl_wait();
   const size_t n4 = (size_t)rows * F / 4, stride = (size_t)rows * 2 * F;
@@ -337,20 +337,20 @@ __global__ void swiglu_kernel(const float* part, int S, int rows, int F, bf16* o
        q += (size_t)gridDim.x * blockDim.x) {
     const size_t idx = 4 * q, r = idx / F, f = idx % F;
     const float* p = part + r * 2 * F + f;
-    const float4 g = sum_splits4(p, stride, S);
-    const float4 u = sum_splits4(p + F, stride, S);
+    const float4 g = sum_splits4(p, stride, splits_at(sp, (int)r, (int)f));
+    const float4 u = sum_splits4(p + F, stride, splits_at(sp, (int)r, (int)(F + f)));
     const float4 v = make_float4(g.x / (1.f + expf(-g.x)) * u.x, g.y / (1.f + expf(-g.y)) * u.y,
                                  g.z / (1.f + expf(-g.z)) * u.z, g.w / (1.f + expf(-g.w)) * u.w);
     store4_planes(outs, no, idx, v);
   }
 }
 
-cudaError_t launch_swiglu(const float* part, int S, int rows, int F, bf16* const* o, int no,
+cudaError_t launch_swiglu(const float* part, const Splits& sp, int rows, int F, bf16* const* o, int no,
                           cudaStream_t s) {
   const size_t n4 = (size_t)rows * F / 4;
   int blocks = (int)((n4 + 255) / 256);
   if (blocks > 152 * 16) blocks = 152 * 16;
-  return launch_pdl(swiglu_kernel, dim3(blocks), dim3(256), 0, s, part, S, rows, F, o[0], o[1], no);
+  return launch_pdl(swiglu_kernel, dim3(blocks), dim3(256), 0, s, part, sp, rows, F, o[0], o[1], no);
 }
 
 // ---------------------------------------------------------------- K3: sequential head chain

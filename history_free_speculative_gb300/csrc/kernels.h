@@ -26,10 +26,10 @@ struct StageArgs {
 };
 
 struct AttnArgs {
-  const float* part_loc = nullptr;  // [S_loc][B*(K+1)][qd + 2 kvd]
-  int S_loc = 1;
-  const float* part_ctx = nullptr;  // [S_ctx][B*m][2 kvd]
-  int S_ctx = 1;
+  const float* part_loc = nullptr;  // [splits][B*(K+1)][qd + 2 kvd]
+  Splits sp_loc;
+  const float* part_ctx = nullptr;  // [splits][B*m][2 kvd]
+  Splits sp_ctx;
   const float* rope_cos = nullptr;  // [K+1][d_h/2]
   const float* rope_sin = nullptr;
   int B = 0, m = 0, K = 0, n_q = 0, n_kv = 0, d_h = 0;
@@ -40,8 +40,9 @@ struct AttnArgs {
 };
 
 struct ResNormArgs {
-  const float* part = nullptr;  // [S][rows][D]
-  int S = 1, rows = 0, D = 0;
+  const float* part = nullptr;  // [splits][rows][D]
+  Splits sp;
+  int rows = 0, D = 0;
   float* x = nullptr;           // [rows, D], updated in place
   const float* g = nullptr;
   float eps = 1e-6f;
@@ -92,7 +93,7 @@ cudaError_t launch_stage(const StageArgs& a, bool f32, cudaStream_t s);
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s);
 size_t attention_smem(int K, int m, int d_h);
 cudaError_t launch_resnorm(const ResNormArgs& a, cudaStream_t s);
-cudaError_t launch_swiglu(const float* part, int S, int rows, int F, bf16* const* o, int no,
+cudaError_t launch_swiglu(const float* part, const Splits& sp, int rows, int F, bf16* const* o, int no,
                           cudaStream_t s);
 cudaError_t launch_head_chain(const ChainArgs& a, cudaStream_t s);
 int chain_group_size(int R, int B);

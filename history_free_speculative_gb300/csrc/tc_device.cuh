@@ -88,6 +88,61 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// ---------------------------------------------------------------- CTA pairs (2-SM MMA)
+// A cluster of two CTAs on neighbouring SMs runs one M = 256 MMA: each CTA
+// holds its 128 rows of A and half of the N columns of B in its own shared
+// memory (same offsets in both), rank 0 issues the MMA, and each CTA's TMEM
+// receives its 128 rows of D over all N columns. TMA loads of either CTA
+// signal rank 0's barrier; rank 0's commits arrive on both CTAs' barriers.
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared-memory variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
+                                                 int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
+                                                 int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(0), "r"(0), "r"(c2), "r"(c3)
+      : "memory");
+}
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                               uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accum)
+      : "memory");
+}
+// Arrive on the barrier at this shared-memory offset in both CTAs of the pair
+// once every prior 2-SM MMA of this thread has completed.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          bar),
+      "h"((uint16_t)3)
+      : "memory");
+}
+
 // Shared-memory matrix descriptor: K-major tile, rows of 128 B, 128-byte
 // swizzle, 8-row groups 1024 B apart (stride byte offset), descriptor version 1.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
@@ -269,29 +324,56 @@ __device__ __forceinline__ uint4 philox_row(uint32_t c0, const PhiloxRow& pr, ui
   return make_uint4(x0, x1, x2, x3);
 }
 
+// Insert (x, v) into the descending list of a thread that scans ids in
+// increasing order: every id already held is lower than v, so on equal scores
+// the held entry stays first (the lower-id-first order) and only strictly
+// greater scores move. Branch-free: the 32 lanes of a warp hold 32 different
+// rows, and a branch taken by any one lane would cost the whole warp.
+__device__ __forceinline__ void topk_push_scan(LmAcc& a, float x, int v) {
+  static_assert(kTopK == 4, "unrolled for 4 entries");
+  const bool c0 = x > a.sc[0], c1 = x > a.sc[1], c2 = x > a.sc[2], c3 = x > a.sc[3];
+  const float s0 = a.sc[0], s1 = a.sc[1], s2 = a.sc[2];
+  const int i0 = a.id[0], i1 = a.id[1], i2 = a.id[2];
+  a.sc[3] = c2 ? s2 : (c3 ? x : a.sc[3]);
+  a.id[3] = c2 ? i2 : (c3 ? v : a.id[3]);
+  a.sc[2] = c1 ? s1 : (c2 ? x : s2);
+  a.id[2] = c1 ? i1 : (c2 ? v : i2);
+  a.sc[1] = c0 ? s0 : (c1 ? x : s1);
+  a.id[1] = c0 ? i0 : (c1 ? v : i1);
+  a.sc[0] = c0 ? x : s0;
+  a.id[0] = c0 ? v : i0;
+}
+
 // Fold 16 consecutive columns v0 .. v0+15 (v0 a multiple of 4) of one row, of
 // which the first nv (a multiple of 4) are vocabulary ids. c2s = log2(e) / T.
+// Must be called by all 32 lanes of a warp together (warp vote inside).
 template <bool kSampling, bool kFull>
 __device__ __forceinline__ void lm_fold16(LmAcc& a, const uint32_t (&raw)[16], int v0, int nv, float c2s,
-                                          const PhiloxRow& pr, uint32_t k0, uint32_t k1) {
-  float x[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const float l = __uint_as_float(raw[j]);
-    x[j] = (kFull || j < nv) ? (kSampling ? l * c2s : l) : -INFINITY;
-  }
+                                          const PhiloxRow& pr, uint32_t k0, uint32_t k1, bool active) {
   if (kSampling) {
-    float cm = x[0];
+    // LSE partials; the chunk maximum is taken on the raw logits (c2s > 0)
+    float lmax = __uint_as_float(raw[0]);
 #pragma unroll
-    for (int j = 1; j < 16; ++j) cm = fmaxf(cm, x[j]);
-    if (cm > a.m) {
-      a.s *= ex2_approx(a.m - cm);
-      a.m = cm;
+    for (int j = 1; j < 16; ++j)
+      if (kFull || j < nv) lmax = fmaxf(lmax, __uint_as_float(raw[j]));
+    const float cm = lmax * c2s;
+    if (active) {
+      if (cm > a.m) {
+        a.s *= ex2_approx(a.m - cm);
+        a.m = cm;
+      }
+      float s = 0.f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (kFull || j < nv) s += ex2_approx(fmaf(__uint_as_float(raw[j]), c2s, -a.m));
+      a.s += s;
     }
-    float s = 0.f;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) s += ex2_approx(x[j] - a.m);
-    a.s += s;
+    // Every 23-bit draw gives noise -log2(-log2 u) <= 23.47 in these units: a
+    // chunk whose best scaled logit is further than that below the 4th best
+    // score of every lane cannot change any list (frequent with the wide
+    // logit ranges of trained models).
+    const bool hopeless = !active || !(cm + 23.5f > a.sc[kTopK - 1]);
+    if (__all_sync(0xffffffffu, hopeless)) return;
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
       if (!kFull && 4 * g >= nv) break;
@@ -299,14 +381,15 @@ __device__ __forceinline__ void lm_fold16(LmAcc& a, const uint32_t (&raw)[16], i
       const uint32_t wx[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float sc = x[4 * g + j] - lg2_approx(neg_log2_u01(wx[j]));
-        if (sc > a.sc[kTopK - 1]) topk_insert(a.sc, a.id, sc, v0 + 4 * g + j);
+        const float sc = fmaf(__uint_as_float(raw[4 * g + j]), c2s, -lg2_approx(neg_log2_u01(wx[j])));
+        if (active) topk_push_scan(a, sc, v0 + 4 * g + j);
       }
     }
   } else {
+    if (!active) return;
 #pragma unroll
     for (int j = 0; j < 16; ++j)
-      if (x[j] > a.sc[kTopK - 1]) topk_insert(a.sc, a.id, x[j], v0 + j);
+      if (kFull || j < nv) topk_push_scan(a, __uint_as_float(raw[j]), v0 + j);
   }
 }
 

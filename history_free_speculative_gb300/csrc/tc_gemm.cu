@@ -205,17 +205,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_ld();
             const int v0 = o0 + c;
             const int nv = p.outs - v0;  // outs is a multiple of 8: whole groups of 4 only
-            if (valid && nv > 0) {
+            if (nv > 0) {                 // uniform across the warp; rows differ per lane
               if (nv >= 16) {
                 if (sampling)
-                  lm_fold16<true, true>(acc, raw, v0, 16, c2s, pr, p.k0, p.k1);
+                  lm_fold16<true, true>(acc, raw, v0, 16, c2s, pr, p.k0, p.k1, valid);
                 else
-                  lm_fold16<false, true>(acc, raw, v0, 16, c2s, pr, p.k0, p.k1);
+                  lm_fold16<false, true>(acc, raw, v0, 16, c2s, pr, p.k0, p.k1, valid);
               } else {
                 if (sampling)
-                  lm_fold16<true, false>(acc, raw, v0, nv, c2s, pr, p.k0, p.k1);
+                  lm_fold16<true, false>(acc, raw, v0, nv, c2s, pr, p.k0, p.k1, valid);
                 else
-                  lm_fold16<false, false>(acc, raw, v0, nv, c2s, pr, p.k0, p.k1);
+                  lm_fold16<false, false>(acc, raw, v0, nv, c2s, pr, p.k0, p.k1, valid);
               }
             }
           }

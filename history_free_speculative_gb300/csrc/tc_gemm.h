@@ -54,17 +54,21 @@ inline int x_box_rows(int rows) { return rows >= 128 ? 128 : ((rows + 7) / 8) * 
 __host__ __device__ inline uint32_t a_slot_bytes(int x_box) { return (uint32_t)((x_box * 128 + 1023) / 1024 * 1024); }
 size_t smem_bytes(const Plan& pl);
 
-// Persistent LM-head kernel (rows <= 256): one CTA per SM over the vocabulary
-// slabs, double-buffered TMEM accumulators, sampling epilogue overlapped with
-// the E stream; records are [grid * groups][rows].
+// Persistent LM-head kernel (rows <= 256): one CTA per SM walking the
+// vocabulary slabs with double-buffered TMEM accumulators (sampling epilogue
+// overlapped with the E stream); rows 129..256 use CTA pairs, one 128-row tile
+// of h each, on the same slabs. Records are [n_units * groups][rows].
 struct LmPlan {
   bool ok = false;
-  int n_mt = 1, N = 0, x_box = 0, kblocks = 0, stages = 0, n_slabs = 0, grid = 0, groups = 0;
+  bool paired = false;
+  int N = 0, x_box0 = 0, x_box1 = 0, kblocks = 0, stages = 0, n_slabs = 0, n_units = 0, grid = 0,
+      groups = 0;
   uint32_t stage_bytes = 0;
+  size_t tail_pad = 0;
 };
 struct LmParams {
   int rows = 0, outs = 0;
-  int n_slabs = 0, kblocks = 0, stages = 0, x_box = 0;
+  int n_slabs = 0, kblocks = 0, stages = 0, x_box0 = 0, x_box1 = 0, paired = 0;
   uint32_t stage_bytes = 0;
   LmRec* rec = nullptr;
   float inv_T = 0.f;  // 0 = greedy
@@ -73,10 +77,32 @@ struct LmParams {
   int K_draft = 1;
   int* status = nullptr;
 };
+// Pair GEMM (2-SM MMA, persistent stream-K; rows 129..4096, bf16 operands):
+// grid = 2 x G CTAs in clusters of two; W maps with 128-row boxes, X maps with
+// 128-row boxes; partials laid out as pair_splits() describes.
+struct PairPlan {
+  bool ok = false;
+  int kblocks = 0, slabs = 0, groups = 0, stages = 0, G = 0, S = 1;
+  long long U = 0;
+};
+struct PairParams {
+  int rows = 0, outs = 0;
+  int kblocks = 0, slabs = 0, stages = 0, G = 1;
+  long long U = 1;
+  float* part = nullptr;
+  int* status = nullptr;
+};
+bool use_pair_engine(int rows, int xplanes, int wplanes);
+PairPlan pair_plan(int rows, int outs, int K, int num_sms);
+Splits pair_splits(const PairPlan& pl);
+size_t pair_smem_bytes(const PairPlan& pl);
+cudaError_t launch_pair(const PairPlan& pl, const CUtensorMap* x, const CUtensorMap* w, PairParams prm,
+                        cudaStream_t s);
+
 LmPlan lm_plan_persistent(int rows, int outs, int K, int num_sms);
 size_t lm_smem_bytes(const LmPlan& pl);
-cudaError_t launch_lm_persistent(const LmPlan& pl, const CUtensorMap* x, const CUtensorMap* w, LmParams prm,
-                                 cudaStream_t s);
+cudaError_t launch_lm_persistent(const LmPlan& pl, const CUtensorMap* x0, const CUtensorMap* x1,
+                                 const CUtensorMap* w, LmParams prm, cudaStream_t s);
 cudaError_t launch(const Plan& pl, const CUtensorMap* x0, const CUtensorMap* x1, const CUtensorMap* w0,
                    const CUtensorMap* w1, TcParams prm, cudaStream_t s);
 

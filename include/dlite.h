@@ -263,8 +263,11 @@ int dlite_stage_times(dlite_handle *h, int B, const void *hidden, const int32_t 
  * X planes); K a multiple of 64, outs a multiple of 8. `part` must
  * hold 16 * rows * outs floats; the sum over the returned number of splits
  * (> 0) is the product. `status` is a device int receiving DLITE_DEV_* bits.
- * plan_override: NULL, or host int[3] {slab width N, k splits, pipeline
- * stages} (0 = planner's choice) for tiling sweeps.
+ * plan_override: NULL selects what the round uses (one bf16 plane on each side
+ * and more than 128 rows: the CTA-pair engine with 2-SM MMAs; otherwise the
+ * one-CTA engine with the planner's tiling); a host int[3] {slab width N,
+ * k splits, pipeline stages} (0 = planner's choice) forces the one-CTA engine
+ * with that tiling, for sweeps.
  * Returns the split count or a negative DLITE_ERR_*. */
 int dlite_selftest_gemm(int rows, int outs, int K, int xplanes, int wplanes, const void *X0,
                         const void *X1, int x_rows, const void *W0, const void *W1, float *part,
