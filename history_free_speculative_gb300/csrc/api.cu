@@ -129,7 +129,7 @@ int check_config(const dlite_config* c) {
   if (c->D % 64 || c->F % 64 || c->R % 32 || c->R > 1024 || c->V < 8 || c->V % 8 || c->V > 262144)
     return DLITE_ERR_UNSUPPORTED_SHAPE;
   if ((c->n_q * c->d_h) % 64) return DLITE_ERR_UNSUPPORTED_SHAPE;
-  if (attention_smem(c->K, c->m, c->d_h) > 96 * 1024) return DLITE_ERR_UNSUPPORTED_SHAPE;
+  if (attention_smem(c->K, c->m, c->d_h, c->n_q / c->n_kv) > 200 * 1024) return DLITE_ERR_UNSUPPORTED_SHAPE;
   if (c->R < 32 || chain_smem_bytes(c->R, chain_group_size(c->R, c->B_max)) > 200 * 1024)
     return DLITE_ERR_UNSUPPORTED_SHAPE;
   if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return DLITE_ERR_INVALID_ARG;

@@ -153,10 +153,11 @@ cudaError_t launch_stage(const StageArgs& a, bool f32, cudaStream_t s) {
 }
 
 // ---------------------------------------------------------------- K2b: block attention
-// One CTA per (query head h, request b); its key/value head is g = h / (n_q/n_kv).
-// Sums the QKV split-K partials of the request's rows (4 columns per item),
-// applies RoPE to the local queries / keys (table [K+1][d_h/2]), then runs
-// non-causal softmax attention of the K+1 query rows over all m + K + 1 keys:
+// One CTA per (key/value head g, request b) serving the n_q / n_kv query heads
+// of its group, so each head's keys and values are reduced from the split-K
+// partials once. Sums the QKV partials of the request's rows (4 columns per
+// item), applies RoPE to the local queries / keys (table [K+1][d_h/2]), then
+// runs non-causal softmax attention of each query row over all m + K + 1 keys:
 // one warp per query row, one lane per key for the scores, warp-shuffle
 // max / sum, and 4 output columns per lane. Shared rows are d_h + 4 floats so
 // 16-byte accesses by 8 consecutive lanes hit distinct banks.
@@ -166,16 +167,16 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(AttnArgs a) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ float sm[];
-  const int h = blockIdx.x, b = blockIdx.y;
-  const int K1 = a.K + 1, dh = a.d_h, half = dh / 2, G = a.n_q / a.n_kv, g = h / G;
+  const int g = blockIdx.x, b = blockIdx.y;
+  const int K1 = a.K + 1, dh = a.d_h, half = dh / 2, G = a.n_q / a.n_kv;
   const int qd = a.n_q * dh, kvd = a.n_kv * dh;
   const int ldl = qd + 2 * kvd;  // local partial row width
   const int ldc = 2 * kvd;       // context partial row width
   const int Tk = a.m + K1;
   const int LD = dh + 4;
-  float* qs = sm;               // [K1][LD]
-  float* ks = qs + K1 * LD;     // [Tk][LD]
-  float* vs = ks + Tk * LD;     // [Tk][LD]
+  float* qs = sm;               // [G * K1][LD]: query row i of head g G + hh at hh * K1 + i
+  float* ks = qs + G * K1 * LD;  // [Tk][LD]
+  float* vs = ks + Tk * LD;      // [Tk][LD]
   const size_t sl = (size_t)a.B * K1 * ldl, sc = (size_t)a.B * a.m * ldc;
   auto loc4 = [&](int row, int col) {
     return sum_splits4(a.part_loc + (size_t)(b * K1 + row) * ldl + col, sl, splits_at(a.sp_loc, b * K1 + row, col));
@@ -196,11 +197,11 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(AttnArgs a) {
                          x2.w * c.w + x1.w * sn.w));
   };
   const int h4 = half / 4, d4 = dh / 4;
-  const int nq = K1 * h4, nk = K1 * h4, nv = K1 * d4, nc = a.m * d4;
+  const int nq = G * K1 * h4, nk = K1 * h4, nv = K1 * d4, nc = a.m * d4;
   for (int idx = threadIdx.x; idx < nq + nk + nv + 2 * nc; idx += blockDim.x) {
-    if (idx < nq) {  // queries of head h (rotated)
-      const int j = (idx % h4) * 4, i = idx / h4, col = h * dh;
-      rope(qs + i * LD, i, j, loc4(i, col + j), loc4(i, col + j + half));
+    if (idx < nq) {  // queries of the group's heads (rotated)
+      const int j = (idx % h4) * 4, r = idx / h4, hh = r / K1, i = r % K1, col = (g * G + hh) * dh;
+      rope(qs + r * LD, i, j, loc4(i, col + j), loc4(i, col + j + half));
     } else if (idx < nq + nk) {  // local keys (rotated)
       const int t = idx - nq, j = (t % h4) * 4, i = t / h4, col = qd + g * dh;
       rope(ks + (a.m + i) * LD, i, j, loc4(i, col + j), loc4(i, col + j + half));
@@ -216,8 +217,9 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(AttnArgs a) {
   __syncthreads();
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  for (int i = warp; i < K1; i += nw) {
-    const float* q = qs + i * LD;
+  for (int r = warp; r < G * K1; r += nw) {
+    const int hh = r / K1, i = r % K1;
+    const float* q = qs + r * LD;
     float sc_ = -INFINITY;
     if (lane < Tk) {
       const float* k = ks + lane * LD;
@@ -245,24 +247,24 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(AttnArgs a) {
         acc.w = fmaf(pk, v.w, acc.w);
       }
     }
-    if (lane < d4) store4_planes(a.o, a.no, (size_t)(b * K1 + i) * qd + h * dh + 4 * lane, acc);
+    if (lane < d4) store4_planes(a.o, a.no, (size_t)(b * K1 + i) * qd + (g * G + hh) * dh + 4 * lane, acc);
   }
 }
 
-size_t attention_smem(int K, int m, int d_h) {
-  return (size_t)((K + 1) + 2 * (m + K + 1)) * (d_h + 4) * sizeof(float);
+size_t attention_smem(int K, int m, int d_h, int G) {
+  return (size_t)(G * (K + 1) + 2 * (m + K + 1)) * (d_h + 4) * sizeof(float);
 }
 
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s) {
-  const size_t smem = attention_smem(a.K, a.m, a.d_h);
+  const size_t smem = attention_smem(a.K, a.m, a.d_h, a.n_q / a.n_kv);
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         96 * 1024);
+                                         200 * 1024);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  return launch_pdl(attention_kernel, dim3(a.n_q, a.B), dim3(kAttnThreads), smem, s, a);
+  return launch_pdl(attention_kernel, dim3(a.n_kv, a.B), dim3(kAttnThreads), smem, s, a);
 }
 
 // ---------------------------------------------------------------- residual + RMSNorm

@@ -91,7 +91,7 @@ struct VerifyArgs {
 
 cudaError_t launch_stage(const StageArgs& a, bool f32, cudaStream_t s);
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s);
-size_t attention_smem(int K, int m, int d_h);
+size_t attention_smem(int K, int m, int d_h, int G);
 cudaError_t launch_resnorm(const ResNormArgs& a, cudaStream_t s);
 cudaError_t launch_swiglu(const float* part, const Splits& sp, int rows, int F, bf16* const* o, int no,
                           cudaStream_t s);
