@@ -579,12 +579,12 @@ cudaError_t launch_verify_greedy(const VerifyArgs& a, cudaStream_t s) {
 // the fixed-point integer floor(w(v) * 2^62) (exact for fp32 weights >= 2^-39),
 // so prefix sums are exact and independent of the summation order. The row is
 // cut into segments of 128 ids; segment sums and their prefix live in shared
-// memory; a threshold tau = floor(S * u) is located by a binary search over
-// the segment prefix, then one warp scans the 128 ids of that segment.
-// Result: the smallest v with prefix(v) > tau, i.e. the inverse CDF at u.
+// memory (each CTA of a cluster holding a contiguous range of segments); a
+// threshold tau = floor(S * u) is located by a binary search over the segment
+// prefix, then one warp scans the 128 ids of that segment. Result: the
+// smallest v with prefix(v) > tau, i.e. the inverse CDF at u.
 
 constexpr int kSeg = 128;
-constexpr int kVerifyThreads = 1024;
 constexpr int kMaxSegs = 2048;  // V <= 262144
 
 __device__ __forceinline__ unsigned long long fix62(float w) {
@@ -630,89 +630,6 @@ __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v)
   return v;
 }
 
-// out[j] for thresholds given by 32-bit Philox words xs[j], j < nthr (<= 32).
-// incl: shared [kMaxSegs] scratch. Returns the row total through *total.
-template <typename Row>
-__device__ void block_icdf(const Row& row, int V, const uint32_t* xs, int nthr, int* out,
-                           unsigned long long* incl, unsigned long long* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const int nseg = (V + kSeg - 1) / kSeg;
-  // 1) segment sums: one warp per segment, one float4 per lane
-  for (int sg0 = warp; sg0 < nseg; sg0 += 4 * nw) {  // four segments' loads in flight per warp
-    unsigned long long w[4][4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int sg = sg0 + u * nw;
-      if (sg < nseg) row.get4(sg * kSeg + lane * 4, w[u]);
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int sg = sg0 + u * nw;
-      if (sg < nseg) {
-        const unsigned long long t = warp_sum_u64(w[u][0] + w[u][1] + w[u][2] + w[u][3]);
-        if (lane == 0) incl[sg] = t;
-      }
-    }
-  }
-  __syncthreads();
-  // 2) inclusive scan of the segment sums (warp 0, sequential chunks of 32)
-  if (warp == 0) {
-    unsigned long long carry = 0;
-    for (int base = 0; base < nseg; base += 32) {
-      const int i = base + lane;
-      unsigned long long v = (i < nseg) ? incl[i] : 0ull;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const unsigned long long u = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += u;
-      }
-      if (i < nseg) incl[i] = v + carry;
-      carry += __shfl_sync(0xffffffffu, v, 31);
-    }
-    if (lane == 0) *total = carry;
-  }
-  __syncthreads();
-  const unsigned long long S = *total;
-  // 3) one warp per threshold
-  for (int j = warp; j < nthr; j += nw) {
-    const unsigned long long tau = scaled_threshold(S, xs[j]);
-    // first segment with incl > tau (exists when S > 0)
-    int lo = 0, hi = nseg - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (incl[mid] > tau) hi = mid; else lo = mid + 1;
-    }
-    const unsigned long long before = lo > 0 ? incl[lo - 1] : 0ull;
-    unsigned long long w[4];
-    row.get4(lo * kSeg + lane * 4, w);
-    const unsigned long long mine = w[0] + w[1] + w[2] + w[3];
-    unsigned long long pre = mine;  // inclusive scan over lanes
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const unsigned long long u = __shfl_up_sync(0xffffffffu, pre, o);
-      if (lane >= o) pre += u;
-    }
-    const unsigned long long start = before + pre - mine;
-    const unsigned ball = __ballot_sync(0xffffffffu, start + mine > tau);
-    int v = V - 1;
-    if (ball) {
-      const int L = __ffs(ball) - 1;
-      if (lane == L) {
-        unsigned long long c = start;
-        int k = 0;
-        for (; k < 3; ++k) {
-          c += w[k];
-          if (c > tau) break;
-        }
-        out[j] = min(lo * kSeg + lane * 4 + k, V - 1);
-      }
-    } else if (lane == 0) {
-      out[j] = v;  // unreachable when S > 0
-    }
-  }
-  __syncthreads();
-}
-
 __device__ __forceinline__ float row_dot(const VerifyArgs& a, int v, const float* h) {
   const int lane = threadIdx.x & 31;
   float acc = 0.f;
@@ -739,28 +656,152 @@ __device__ __forceinline__ float row_dot(const VerifyArgs& a, int v, const float
   return warp_sum(acc);
 }
 
-// One CTA (1024 threads) per request.
-__global__ void __launch_bounds__(kVerifyThreads) verify_sample_kernel(VerifyArgs a) {
+// ---- cluster form: the row of one request is cut among kVerifyCluster CTAs
+
+constexpr int kVerifyCluster = 8;
+constexpr int kVerifyCThreads = 512;
+constexpr int kSegsPerCta = kMaxSegs / kVerifyCluster;
+
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"((uint32_t)__cvta_generic_to_shared(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_cluster_u64(uint32_t addr, unsigned long long v) {
+  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+__device__ __forceinline__ void st_cluster_f64(uint32_t addr, double v) {
+  asm volatile("st.shared::cluster.f64 [%0], %1;" ::"r"(addr), "d"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// Inverse CDF of a row over the cluster: CTA `rank` owns segments
+// [rank nseg / C, (rank + 1) nseg / C); the CTAs exchange their totals, so each
+// knows S and the prefix before its range, and the CTA whose range holds a
+// threshold resolves it and writes the id into out[j] of cluster rank 0.
+// xs (nthr <= 32 words) must be identical in every CTA. Returns S. Must be
+// called by every thread of every CTA of the cluster.
+template <typename Row>
+__device__ unsigned long long cluster_icdf(const Row& row, int V, const uint32_t* xs, int nthr, int* out,
+                                           unsigned long long* incl, unsigned long long* tot, uint32_t rank) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int nseg = (V + kSeg - 1) / kSeg;
+  const int s0 = (int)rank * nseg / kVerifyCluster, s1 = ((int)rank + 1) * nseg / kVerifyCluster;
+  const int ns = s1 - s0;
+  // 1) segment sums of this CTA's range: one warp per segment, four segments' loads in flight
+  for (int i0 = warp; i0 < ns; i0 += 4 * nw) {
+    unsigned long long w[4][4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * nw;
+      if (i < ns) row.get4((s0 + i) * kSeg + lane * 4, w[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * nw;
+      if (i < ns) {
+        const unsigned long long t = warp_sum_u64(w[u][0] + w[u][1] + w[u][2] + w[u][3]);
+        if (lane == 0) incl[i] = t;
+      }
+    }
+  }
+  __syncthreads();
+  // 2) local inclusive scan; 3) the local total into every CTA's tot[rank]
+  if (warp == 0) {
+    unsigned long long carry = 0;
+    for (int base = 0; base < ns; base += 32) {
+      const int i = base + lane;
+      unsigned long long v = (i < ns) ? incl[i] : 0ull;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+      }
+      if (i < ns) incl[i] = v + carry;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane < kVerifyCluster) st_cluster_u64(cluster_addr(tot + rank, (uint32_t)lane), carry);
+  }
+  cluster_sync_all();
+  unsigned long long S = 0, off = 0;
+#pragma unroll
+  for (int r = 0; r < kVerifyCluster; ++r) {
+    if (r < (int)rank) off += tot[r];
+    S += tot[r];
+  }
+  const unsigned long long lt = tot[rank];
+  // 4) the thresholds that fall into this CTA's range
+  for (int j = warp; j < nthr; j += nw) {
+    const unsigned long long tau = scaled_threshold(S, xs[j]);
+    if (S == 0ull) {
+      if (rank == 0 && lane == 0) out[j] = V - 1;  // no mass: last id (as a plain inverse CDF)
+      continue;
+    }
+    if (tau < off || tau >= off + lt) continue;
+    const unsigned long long tl = tau - off;
+    int lo = 0, hi = ns - 1;  // first local segment with incl > tl
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (incl[mid] > tl) hi = mid; else lo = mid + 1;
+    }
+    const unsigned long long before = lo > 0 ? incl[lo - 1] : 0ull;
+    unsigned long long w[4];
+    row.get4((s0 + lo) * kSeg + lane * 4, w);
+    const unsigned long long mine = w[0] + w[1] + w[2] + w[3];
+    unsigned long long pre = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long u = __shfl_up_sync(0xffffffffu, pre, o);
+      if (lane >= o) pre += u;
+    }
+    const unsigned long long start = before + pre - mine;
+    const unsigned ball = __ballot_sync(0xffffffffu, start + mine > tl);
+    const int L = ball ? __ffs(ball) - 1 : 31;
+    if (lane == L) {
+      unsigned long long c = start;
+      int k = 0;
+      for (; k < 3; ++k) {
+        c += w[k];
+        if (c > tl) break;
+      }
+      st_cluster_u32(cluster_addr(out + j, 0), (uint32_t)min((s0 + lo) * kSeg + lane * 4 + k, V - 1));
+    }
+  }
+  cluster_sync_all();  // every id is in rank 0's out[]
+  return S;
+}
+
+// A cluster of kVerifyCluster CTAs per request.
+__global__ void __launch_bounds__(kVerifyCThreads) verify_sample_kernel(VerifyArgs a) {
   pdl_trigger();
   pdl_wait();
-  __shared__ unsigned long long incl[kMaxSegs];
-  __shared__ unsigned long long total;
+  __shared__ unsigned long long incl[kSegsPerCta];
+  __shared__ unsigned long long tot[kVerifyCluster];
   __shared__ uint32_t xs[kProposals];      // inverse-CDF words of the proposals
   __shared__ double sacc[kProposals];      // acceptance uniforms of the proposals
-  __shared__ double qv[kProposals];        // q(v_j) of the proposals
-  __shared__ int sv[kProposals];
+  __shared__ double qv[kProposals];        // q(v_j) of the proposals (rank 0)
+  __shared__ int sv[kProposals];           // proposal ids (rank 0)
   __shared__ int sA, stok;
-  const int b = blockIdx.x, K = a.K, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t rank = cluster_ctarank();
+  const int b = blockIdx.x / kVerifyCluster, K = a.K, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nwarps = blockDim.x >> 5;
+  const bool lead = rank == 0;
   const double T = a.T;
   const uint32_t pos0 = (uint32_t)a.pos[b];
   const float* prow_base = a.probs + (size_t)b * (K + 1) * a.V;
-  if (warp == 0) {
+  if (warp == 0) {  // the accept tests (the same in every CTA of the cluster)
     bool acc = false;
     if (lane < K) {
       int d = a.cand[b * K + lane];
       if (d < 0 || d >= a.V) {
-        flag_status(a.status, kDevBounds);
+        if (lead) flag_status(a.status, kDevBounds);
         d = 0;
       }
       const dlite_qstats qs = a.qs[b * K + lane];
@@ -778,14 +819,14 @@ __global__ void __launch_bounds__(kVerifyThreads) verify_sample_kernel(VerifyArg
   const int A = sA;
   const float* prow = prow_base + (size_t)A * a.V;
   const RowF32 prow_fix{prow, a.V};
-  if (A == K) {
+  if (A == K) {  // every draft token accepted: the bonus token from p_K
     if (threadIdx.x == 0) {
       xs[0] = philox(0u, pos0 + K + 1, (uint32_t)b, kTagBonus, a.k0, a.k1).x;
-      if (a.counters) atomicAdd(a.counters + 3, 1ull);
+      if (lead && a.counters) atomicAdd(a.counters + 3, 1ull);
     }
     __syncthreads();
-    block_icdf(prow_fix, a.V, xs, 1, sv, incl, &total);
-    if (threadIdx.x == 0) stok = sv[0];
+    cluster_icdf(prow_fix, a.V, xs, 1, sv, incl, tot, rank);
+    if (lead && threadIdx.x == 0) stok = sv[0];
   } else {
     const uint32_t posA = pos0 + A + 1;
     if (threadIdx.x < kProposals) {
@@ -794,15 +835,17 @@ __global__ void __launch_bounds__(kVerifyThreads) verify_sample_kernel(VerifyArg
       sacc[threadIdx.x] = u01d(w.y);
     }
     __syncthreads();
-    block_icdf(prow_fix, a.V, xs, kProposals, sv, incl, &total);
+    cluster_icdf(prow_fix, a.V, xs, kProposals, sv, incl, tot, rank);
+    // q(v_j) of the proposals, spread over the cluster (one warp per proposal)
     const float* h = a.hs + (size_t)(b * K + A) * a.D;
     const double lse_a = (double)a.qs[b * K + A].lse;
-    for (int j = warp; j < kProposals; j += nwarps) {  // one warp per proposal
-      const float l = row_dot(a, sv[j], h);
-      if (lane == 0) qv[j] = exp((double)l / T - lse_a);
+    for (int j = (int)rank + kVerifyCluster * warp; j < kProposals; j += kVerifyCluster * nwarps) {
+      const int v = (int)ld_cluster_u32(cluster_addr(sv + j, 0));
+      const float l = row_dot(a, v, h);
+      if (lane == 0) st_cluster_f64(cluster_addr(qv + j, 0), exp((double)l / T - lse_a));
     }
-    __syncthreads();
-    if (threadIdx.x == 0) {
+    cluster_sync_all();
+    if (lead && threadIdx.x == 0) {  // proposal-rejection sampling of the residual, in order
       int tok = -1, tried = 0;
       for (int j = 0; j < kProposals; ++j) {
         ++tried;
@@ -812,36 +855,42 @@ __global__ void __launch_bounds__(kVerifyThreads) verify_sample_kernel(VerifyArg
           break;
         }
       }
-      stok = tok;
       if (a.counters) {
         atomicAdd(a.counters + 0, 1ull);
         atomicAdd(a.counters + 1, (unsigned long long)tried);
         if (tok < 0) atomicAdd(a.counters + 2, 1ull);
       }
+      for (int r = 0; r < kVerifyCluster; ++r) st_cluster_u32(cluster_addr(&stok, (uint32_t)r), (uint32_t)tok);
     }
-    __syncthreads();
+    cluster_sync_all();
     if (stok < 0) {
-      // exact fallback: inverse CDF over r(v) = max(0, p(v) - q(v)) for all v (rare)
+      // exact fallback (rare): inverse CDF over r(v) = max(0, p(v) - q(v)) for all v,
+      // each CTA filling the fixed-point residual of its own range of ids
       unsigned long long* r = a.resid + (size_t)b * a.V;
-      for (int v = warp; v < a.V; v += nwarps) {
+      const int nseg = (a.V + kSeg - 1) / kSeg;
+      const int v0 = ((int)rank * nseg / kVerifyCluster) * kSeg;
+      const int v1 = min((((int)rank + 1) * nseg / kVerifyCluster) * kSeg, a.V);
+      for (int v = v0 + warp; v < v1; v += nwarps) {
         const float l = row_dot(a, v, h);
         if (lane == 0) r[v] = fix62d((double)prow[v] - exp((double)l / T - lse_a));
       }
-      __syncthreads();
+      __syncthreads();  // this CTA reads back only its own range
       if (threadIdx.x == 0)
         xs[0] = philox((uint32_t)kProposals, posA, (uint32_t)b, kTagResid, a.k0, a.k1).x;
       __syncthreads();
       const RowFix rfix{r, a.V};
-      block_icdf(rfix, a.V, xs, 1, sv, incl, &total);
-      if (total == 0ull) block_icdf(prow_fix, a.V, xs, 1, sv, incl, &total);
-      if (threadIdx.x == 0) stok = sv[0];
+      const unsigned long long S = cluster_icdf(rfix, a.V, xs, 1, sv, incl, tot, rank);
+      if (S == 0ull) cluster_icdf(prow_fix, a.V, xs, 1, sv, incl, tot, rank);
+      if (lead && threadIdx.x == 0) stok = sv[0];
     }
   }
   __syncthreads();
+  if (!lead) return;
   const int tok = stok;
   for (int i = threadIdx.x; i <= K; i += blockDim.x)
     a.commits[b * (K + 1) + i] = (i < A) ? a.cand[b * K + i] : (i == A ? tok : -1);
   if (threadIdx.x == 0) {
+    if (tok < 0 || tok >= a.V) flag_status(a.status, kDevBounds);
     a.accepted[b] = A;
     a.n_commit[b] = A + 1;
     a.next_anchor[b] = tok;
@@ -849,7 +898,21 @@ __global__ void __launch_bounds__(kVerifyThreads) verify_sample_kernel(VerifyArg
 }
 
 cudaError_t launch_verify_sample(const VerifyArgs& a, cudaStream_t s) {
-  return launch_pdl(verify_sample_kernel, dim3(a.B), dim3(kVerifyThreads), 0, s, a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.B * kVerifyCluster);
+  cfg.blockDim = dim3(kVerifyCThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = kVerifyCluster;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, verify_sample_kernel, a);
 }
 
 __global__ void advance_kernel(int B, const int32_t* n_commit, int64_t* pos) {
