@@ -88,17 +88,6 @@ __device__ __forceinline__ double u01d(uint32_t x) {
   return ((double)(x >> 9) + 0.5) * 1.1920928955078125e-07;
 }
 
-// Gumbel noise -log(-log u) of the uniform u01d(x), in double precision. For u
-// near 1, -log u is taken as -log1p(-w) with the exact complement
-// w = 1 - u = ((2^23 - 1 - (x >> 9)) + 1/2) 2^-23, so it keeps full relative
-// accuracy where the noise is largest.
-__device__ __forceinline__ double gumbel_d(uint32_t x) {
-  const uint32_t k = x >> 9;
-  const double w = ((double)(0x7fffffu - k) + 0.5) * 1.1920928955078125e-07;
-  const double nl = w < 0.25 ? -log1p(-w) : -log(u01d(x));
-  return -log(nl);
-}
-
 // ---------------------------------------------------------------- programmatic dependent launch
 // Kernels of the round are launched with programmatic stream serialization:
 // a kernel may begin while its predecessor drains. pdl_trigger lets the next

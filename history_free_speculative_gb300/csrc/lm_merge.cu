@@ -86,10 +86,21 @@ __device__ __forceinline__ float exact_logit(const LmMergeArgs& a, int v, const 
 }
 
 // One CTA of kMergeWarps warps per row: every thread folds a strided subset of
-// the slab records into a register top-k + LSE, the warps combine by butterfly,
-// warp 0 combines the warps in a fixed order, and 4 warps re-score the 4
+// the records into a register top-k + LSE, the warps combine by butterfly,
+// thread 0 combines the warps in a fixed order, and the 4 warps re-score the 4
 // finalists exactly in parallel.
-constexpr int kMergeWarps = 16;
+constexpr int kMergeWarps = 4;  // one finalist per warp in the re-scoring
+
+// Gumbel noise -log(-log u) of the uniform u01f(x) with full relative accuracy
+// where it matters: for u within 2^-8 of 1, -log u is formed from the exact
+// complement w = 1 - u by its series w + w^2/2 + w^3/3 (truncation < w^4/4,
+// relative < 2^-26); elsewhere from the library logf.
+__device__ __forceinline__ float gumbel_f(uint32_t x) {
+  const uint32_t k = x >> 9;
+  const float w = fmaf((float)(0x7fffffu - k), 1.1920928955078125e-07f, 5.9604644775390625e-08f);
+  const float nl = w < 0.00390625f ? w * fmaf(w, fmaf(w, 1.f / 3.f, 0.5f), 1.f) : -logf(1.f - w);
+  return -logf(nl);
+}
 
 __global__ void __launch_bounds__(kMergeWarps * 32) lm_merge_kernel(const LmMergeArgs a) {
   pdl_trigger();
@@ -171,7 +182,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lm_merge_kernel(const LmMerg
         const uint32_t pos = (uint32_t)(a.pos[req] + (r % a.K) + 1);
         const uint4 w = philox((uint32_t)v >> 2, pos, req, kTagGumbel, a.k0, a.k1);
         const uint32_t wx[4] = {w.x, w.y, w.z, w.w};
-        x = (double)l / a.T + gumbel_d(wx[v & 3]);
+        x = (double)l / a.T + (double)gumbel_f(wx[v & 3]);
       }
     }
     if (lane == 0) {
