@@ -14,7 +14,7 @@ using namespace dlite;
 struct LayerW {
   const bf16* Wqkv[2];  // [qd + 2 kvd, D] = [Wq; Wk; Wv]
   const bf16* Wo[2];    // [D, qd]
-  const bf16* Wgu[2];   // [2F, D] = [Wg; Wu]
+  const bf16* Wgu[2];   // [2F, D]: gate and up rows interleaved in blocks of 32 (fused SwiGLU)
   const bf16* Wd[2];    // [D, F]
   float* g_attn;
   float* g_ffn;
@@ -215,8 +215,14 @@ const CUtensorMap* get_map(dlite_handle* h, const void* base, int rows, int K, i
 }
 
 // part[z][r][o] = sum over split z of X[r, :] . W[o, :], r < rows, o < outs.
+// With act != nullptr the product is the gate / up one (columns interleaved in
+// blocks of 32): on the one-CTA engine the epilogue writes a = silu(gate) * up
+// to the act planes directly and *fused is set; otherwise the partials are
+// written as usual and the caller runs the SwiGLU kernel.
 int gemm(dlite_handle* h, const char* name, const Operand& X, const Operand& W, int rows, int outs,
-         float* part, Splits* sp_out, cudaStream_t s) {
+         float* part, Splits* sp_out, cudaStream_t s, bf16* const* act = nullptr, int act_planes = 1,
+         bool* fused = nullptr) {
+  if (fused) *fused = false;
   if (tc::use_pair_engine(rows, X.n, W.n)) {  // 2-SM MMAs
     const tc::PairPlan pp = tc::pair_plan(rows, outs, X.K, h->num_sms);
     if (pp.ok) {
@@ -235,7 +241,7 @@ int gemm(dlite_handle* h, const char* name, const Operand& X, const Operand& W, 
       return DLITE_OK;
     }
   }
-  const tc::Plan pl = tc::plan(rows, outs, X.K, X.n, W.n, false);
+  const tc::Plan pl = tc::plan(rows, outs, X.K, X.n, W.n, false, act != nullptr);
   if (!pl.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
   const int xb = tc::x_box_rows(rows);
   h->maps.reserve(h->maps.size() + 4);
@@ -254,6 +260,13 @@ int gemm(dlite_handle* h, const char* name, const Operand& X, const Operand& W, 
   prm.x_box = xb;
   prm.part = part;
   prm.status = h->status;
+  if (act) {
+    prm.mode = 2;
+    prm.act[0] = act[0];
+    prm.act[1] = act_planes == 2 ? act[1] : nullptr;
+    prm.act_planes = act_planes;
+    if (fused) *fused = true;
+  }
   if (sp_out) *sp_out = uniform_splits(pl.S);
   CK(tc::launch(pl, x0, x1, w0, w1, prm, s));
   mark(h, name);
@@ -356,10 +369,13 @@ int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anch
     CK(launch_resnorm(rn, s));
     mark(h, "resnorm");
     // gate/up + SwiGLU
+    bool fused = false;
     RUN(gemm(h, "gemm_gate_up", opnd(h->y, h->np, h->Lcap, c.D), opnd(w.Wgu, h->np, 2 * c.F, c.D), L,
-             2 * c.F, h->part, &S1, s));
-    CK(launch_swiglu(h->part, S1, L, c.F, h->a, h->np, s));
-    mark(h, "swiglu");
+             2 * c.F, h->part, &S1, s, h->a, h->np, &fused));
+    if (!fused) {
+      CK(launch_swiglu_interleaved(h->part, S1, L, c.F, h->a, h->np, s));
+      mark(h, "swiglu");
+    }
     // down + residual, then the next layer's pre-norm (or the final norm)
     RUN(gemm(h, "gemm_down", opnd(h->a, h->np, h->Lcap, c.F), opnd(w.Wd, h->np, c.D, c.F), L, c.D,
              h->part, &S1, s));
@@ -570,9 +586,15 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
     const int qkv_rows[3] = {h->qd, h->kvd, h->kvd};
     RUN(stack(h, qkv, qkv_rows, 3, D, L.Wqkv));
     RUN(repack(h, lw.Wo, D, h->qd, h->qd, 0, L.Wo, nullptr));
-    const void* gu[2] = {lw.Wg, lw.Wu};
-    const int gu_rows[2] = {F, F};
-    RUN(stack(h, gu, gu_rows, 2, D, L.Wgu));
+    {
+      bf16* p0 = nullptr;
+      bf16* p1 = nullptr;
+      AL(p0, (size_t)2 * F * D);
+      if (h->np == 2) AL(p1, (size_t)2 * F * D);
+      CK(launch_repack_gate_up(lw.Wg, lw.Wu, h->f32, F, D, p0, p1, h->np, 0));
+      L.Wgu[0] = p0;
+      L.Wgu[1] = p1;
+    }
     RUN(repack(h, lw.Wd, D, F, F, 0, L.Wd, nullptr));
     RUN(repack(h, lw.g_attn, 1, D, D, 0, nullptr, &L.g_attn));
     RUN(repack(h, lw.g_ffn, 1, D, D, 0, nullptr, &L.g_ffn));
@@ -1007,9 +1029,11 @@ int dlite_counters(dlite_handle* h, int reset, int64_t* out, dlite_stream_t stre
 int dlite_launch_count(dlite_handle* h, int B, float temperature) {
   if (!h || B < 1) return -1;
   (void)temperature;
-  // stage + per layer {qkv, ctx-kv, attention, o, resnorm, gate/up, swiglu, down, resnorm}
-  // + head {ce, chain, P, out} + lm {head, merge} + verify
-  return 1 + 9 * h->cfg.L_D + 4 + 2 + 1;
+  // stage + per layer {qkv, ctx-kv, attention, o, resnorm, gate/up (+ swiglu on the pair
+  // engine), down, resnorm} + head {ce, chain, P, out} + lm {head, merge} + verify
+  const int L = B * (h->cfg.K + 1);
+  const int per_layer = tc::use_pair_engine(L, h->np, h->np) ? 9 : 8;
+  return 1 + per_layer * h->cfg.L_D + 4 + 2 + 1;
 }
 
 }  // extern "C"

@@ -329,7 +329,10 @@ cudaError_t launch_resnorm(const ResNormArgs& a, cudaStream_t s) {
 }
 
 // ---------------------------------------------------------------- SwiGLU epilogue
-// a[r, f] = silu(sum_s part[s][r][f]) * sum_s part[s][r][F + f], float4 per thread.
+// For products on the pair engine (the one-CTA engine fuses this into its
+// epilogue). The gate / up columns are interleaved in blocks of 32: feature f
+// has its gate at column 64 (f / 32) + f % 32 and its up 32 columns later.
+// a[r, f] = silu(gate) * up, float4 (4 features) per thread.
 __global__ void swiglu_kernel(const float* part, Splits sp, int rows, int F, bf16* o0, bf16* o1, int no) {
   pdl_trigger();
   pdl_wait();
@@ -338,17 +341,18 @@ __global__ void swiglu_kernel(const float* part, Splits sp, int rows, int F, bf1
   for (size_t q = (size_t)blockIdx.x * blockDim.x + threadIdx.x; q < n4;
        q += (size_t)gridDim.x * blockDim.x) {
     const size_t idx = 4 * q, r = idx / F, f = idx % F;
-    const float* p = part + r * 2 * F + f;
-    const float4 g = sum_splits4(p, stride, splits_at(sp, (int)r, (int)f));
-    const float4 u = sum_splits4(p + F, stride, splits_at(sp, (int)r, (int)(F + f)));
+    const int cg = (int)(64 * (f / 32) + f % 32);
+    const float* p = part + r * 2 * F + cg;
+    const float4 g = sum_splits4(p, stride, splits_at(sp, (int)r, cg));
+    const float4 u = sum_splits4(p + 32, stride, splits_at(sp, (int)r, cg + 32));
     const float4 v = make_float4(g.x / (1.f + expf(-g.x)) * u.x, g.y / (1.f + expf(-g.y)) * u.y,
                                  g.z / (1.f + expf(-g.z)) * u.z, g.w / (1.f + expf(-g.w)) * u.w);
     store4_planes(outs, no, idx, v);
   }
 }
 
-cudaError_t launch_swiglu(const float* part, const Splits& sp, int rows, int F, bf16* const* o, int no,
-                          cudaStream_t s) {
+cudaError_t launch_swiglu_interleaved(const float* part, const Splits& sp, int rows, int F, bf16* const* o, int no,
+                                      cudaStream_t s) {
   const size_t n4 = (size_t)rows * F / 4;
   int blocks = (int)((n4 + 255) / 256);
   if (blocks > 152 * 16) blocks = 152 * 16;
@@ -962,6 +966,33 @@ cudaError_t launch_repack(const void* src, bool src_f32, int rows, int cols, int
   else
     repack_kernel<bf16><<<blocks, 256, 0, s>>>((const bf16*)src, rows, cols, src_ld, src_off, p0, p1,
                                                 np, f32, dst_ld);
+  return cudaGetLastError();
+}
+
+// The gate / up weights stacked for the fused SwiGLU epilogue: destination row r
+// of [2F, D] is gate row 32 (r / 64) + r % 32 when r % 64 < 32, else up row
+// 32 (r / 64) + r % 32; stored in the tiled layout as bf16 planes.
+template <typename T>
+__global__ void repack_gate_up_kernel(const T* Wg, const T* Wu, int F, int D, bf16* p0, bf16* p1, int np) {
+  const size_t n = (size_t)2 * F * D;
+  bf16* pl[2] = {p0, p1};
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t r = i / D, c = i % D;
+    const size_t src_row = 32 * (r / 64) + r % 32;
+    const float v = to_f32((r % 64 < 32 ? Wg : Wu)[src_row * D + c]);
+    store_planes(pl, np, tiled_index(r, c, (size_t)D), v);
+  }
+}
+
+cudaError_t launch_repack_gate_up(const void* Wg, const void* Wu, bool src_f32, int F, int D, bf16* p0, bf16* p1,
+                                  int np, cudaStream_t s) {
+  const size_t n = (size_t)2 * F * D;
+  int blocks = (int)((n + 255) / 256);
+  if (blocks > 152 * 32) blocks = 152 * 32;
+  if (src_f32)
+    repack_gate_up_kernel<float><<<blocks, 256, 0, s>>>((const float*)Wg, (const float*)Wu, F, D, p0, p1, np);
+  else
+    repack_gate_up_kernel<bf16><<<blocks, 256, 0, s>>>((const bf16*)Wg, (const bf16*)Wu, F, D, p0, p1, np);
   return cudaGetLastError();
 }
 

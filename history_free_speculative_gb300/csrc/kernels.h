@@ -93,8 +93,8 @@ cudaError_t launch_stage(const StageArgs& a, bool f32, cudaStream_t s);
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s);
 size_t attention_smem(int K, int m, int d_h, int G);
 cudaError_t launch_resnorm(const ResNormArgs& a, cudaStream_t s);
-cudaError_t launch_swiglu(const float* part, const Splits& sp, int rows, int F, bf16* const* o, int no,
-                          cudaStream_t s);
+cudaError_t launch_swiglu_interleaved(const float* part, const Splits& sp, int rows, int F, bf16* const* o, int no,
+                                      cudaStream_t s);
 cudaError_t launch_head_chain(const ChainArgs& a, cudaStream_t s);
 int chain_group_size(int R, int B);
 size_t chain_smem_bytes(int R, int Bg);
@@ -107,6 +107,8 @@ cudaError_t launch_advance(int B, const int32_t* n_commit, int64_t* pos, cudaStr
 cudaError_t launch_repack(const void* src, bool src_f32, int rows, int cols, int src_ld,
                           int src_off, bf16* p0, bf16* p1, int np, float* f32, int dst_ld,
                           cudaStream_t s);
+cudaError_t launch_repack_gate_up(const void* Wg, const void* Wu, bool src_f32, int F, int D, bf16* p0, bf16* p1,
+                                  int np, cudaStream_t s);
 cudaError_t launch_head_matrix(const void* Q, const void* P, bool f32, int D, int R, float* Mt,
                                cudaStream_t s);
 

@@ -167,24 +167,91 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int c_lo = eg * ncol, c_hi = c_lo + ncol;
     const bool got = mbar_wait_warp(accf, 0, p.status);
     fence_after();
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // stage memory is reused below
     pdl_wait();  // outputs may still be read by the previous kernel
     if (got) {
       for (int mt = 0; mt < NMT; ++mt) {
         const int r = m0 + mt * 128 + q * 32 + lane;
         const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(mt * p.N);
         if (p.mode == 0) {
-          float* out = p.part + ((size_t)split * p.rows + r) * p.outs;
-          for (int c = c_lo; c < c_hi; c += 16) {
-            float v[16];
-            tmem_ld16(tbase + c, v);
-            if (r < p.rows) {
+          // 32 rows x 32 columns at a time through shared memory (the pipeline
+          // stages are idle once the last product has completed): element (row i,
+          // column j) at i * 32 + (j ^ i), so lanes writing a row or reading a
+          // column hit 32 banks, and each global store writes 32 consecutive
+          // floats of one row instead of 16 bytes of 32 different rows
+          float* stg = reinterpret_cast<float*>(smem) + (warp - 2) * 1024;
+          float* out = p.part + (size_t)split * p.rows * p.outs;
+          const int row0 = m0 + mt * 128 + q * 32;
+          for (int c = c_lo; c < c_hi; c += 32) {
+            uint32_t v0[16], v1[16];
+            tmem_ld16_nowait(tbase + c, v0);
+            tmem_ld16_nowait(tbase + c + 16, v1);
+            tmem_wait_ld();
 #pragma unroll
-              for (int j = 0; j < 16; j += 4) {
-                const int col = o0 + c + j;
-                if (col + 3 < p.outs)
-                  *reinterpret_cast<float4*>(out + col) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            for (int j = 0; j < 16; ++j) {
+              stg[lane * 32 + (j ^ lane)] = __uint_as_float(v0[j]);
+              stg[lane * 32 + ((j + 16) ^ lane)] = __uint_as_float(v1[j]);
+            }
+            __syncwarp();
+            const int col = o0 + c + lane;
+            if (row0 < p.rows) {
+              // 16 shared-memory reads first: a read placed after a global store
+              // (which may alias it, as far as the compiler knows) would wait for it
+              for (int h = 0; h < 32; h += 16) {
+                float vals[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) vals[j] = stg[(h + j) * 32 + (lane ^ (h + j))];
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                  if (row0 + h + j < p.rows && col < p.outs) out[(size_t)(row0 + h + j) * p.outs + col] = vals[j];
               }
             }
+            __syncwarp();
+          }
+        } else if (p.mode == 2) {
+          // SwiGLU: the slab's columns come in blocks of 64, [32 gate | 32 up] of the
+          // same 32 features; a = silu(gate) * up goes through the shared-memory
+          // transpose and out as rows of 32 features
+          float* stg = reinterpret_cast<float*>(smem) + (warp - 2) * 1024;
+          const int row0 = m0 + mt * 128 + q * 32;
+          const int F = p.outs / 2;
+          for (int blk = eg; blk < p.N / 64; blk += kEpiGroups) {
+            uint32_t g0[16], g1[16], u0[16], u1[16];
+            tmem_ld16_nowait(tbase + blk * 64, g0);
+            tmem_ld16_nowait(tbase + blk * 64 + 16, g1);
+            tmem_ld16_nowait(tbase + blk * 64 + 32, u0);
+            tmem_ld16_nowait(tbase + blk * 64 + 48, u1);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float ga = __uint_as_float(g0[j]), gb = __uint_as_float(g1[j]);
+              stg[lane * 32 + (j ^ lane)] = ga / (1.f + expf(-ga)) * __uint_as_float(u0[j]);
+              stg[lane * 32 + ((j + 16) ^ lane)] = gb / (1.f + expf(-gb)) * __uint_as_float(u1[j]);
+            }
+            __syncwarp();
+            const int f = (o0 / 64 + blk) * 32 + lane;  // this lane's feature
+            if (row0 < p.rows) {
+              for (int h = 0; h < 32; h += 16) {
+                float vals[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) vals[j] = stg[(h + j) * 32 + (lane ^ (h + j))];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  if (row0 + h + j < p.rows && f < F) {
+                    const size_t idx = (size_t)(row0 + h + j) * F + f;
+                    if (p.act_planes == 2) {
+                      bf16 hi, lo;
+                      split_bf16(vals[j], hi, lo);
+                      p.act[0][idx] = hi;
+                      p.act[1][idx] = lo;
+                    } else {
+                      p.act[0][idx] = __float2bfloat16_rn(vals[j]);
+                    }
+                  }
+                }
+              }
+            }
+            __syncwarp();
           }
         } else {
           // LM head: 4 best (score, id) and LSE partials of this vocabulary slab for row r
@@ -288,7 +355,7 @@ static int next_pow2_cols(int c) {
   return n;
 }
 
-Plan plan(int rows, int outs, int K, int xplanes, int wplanes, bool lm) {
+Plan plan(int rows, int outs, int K, int xplanes, int wplanes, bool lm, bool one_split) {
   Plan best;
   best.ok = false;
   const int kblocks = K / 64;
@@ -308,7 +375,7 @@ Plan plan(int rows, int outs, int K, int xplanes, int wplanes, bool lm) {
       if (stages < 2) continue;
       const int slabs = (outs + N - 1) / N;
       // at most 4 k-splits: every consumer sums the splits on its critical path
-      const int smax = lm ? 1 : (kblocks < 4 ? kblocks : 4);
+      const int smax = (lm || one_split) ? 1 : (kblocks < 4 ? kblocks : 4);
       for (int S = 1; S <= smax; ++S) {
         const int kbps = (kblocks + S - 1) / S;
         const int Se = (kblocks + kbps - 1) / kbps;
@@ -347,7 +414,10 @@ Plan plan(int rows, int outs, int K, int xplanes, int wplanes, bool lm) {
 }
 
 size_t smem_bytes(const Plan& pl) {
-  return 1024 /* align */ + 1024 /* barriers */ + (size_t)pl.stages * pl.stage_bytes + kTailPad;
+  // the epilogue reuses the first 32 KB of the stage memory as transpose buffers
+  size_t stage_mem = (size_t)pl.stages * pl.stage_bytes + kTailPad;
+  if (stage_mem < 32768) stage_mem = 32768;
+  return 1024 /* align */ + 1024 /* barriers */ + stage_mem;
 }
 
 typedef void (*KernelFn)(const __grid_constant__ CUtensorMap, const __grid_constant__ CUtensorMap,

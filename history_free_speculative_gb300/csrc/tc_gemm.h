@@ -32,8 +32,11 @@ struct TcParams {
   int n_mt = 1, xplanes = 1, wplanes = 1, N = 0, kb_per_split = 0, kblocks = 0, stages = 0;
   uint32_t stage_bytes = 0, tmem_cols = 32;
   int x_box = 128;         // rows of each activation tile load (<= 128, multiple of 8)
-  int mode = 0;            // 0: fp32 partials [split][rows][outs]; 1: LM-head records
+  int mode = 0;            // 0: fp32 partials [split][rows][outs]; 1: LM-head records;
+                           // 2: SwiGLU of gate / up columns interleaved in blocks of 32 (one split)
   float* part = nullptr;
+  bf16* act[2] = {nullptr, nullptr};  // mode 2: a = silu(gate) * up, [rows, outs / 2] bf16 planes
+  int act_planes = 1;
   LmRec* rec = nullptr;    // [slabs * kEpiGroups][rows]
   float inv_T = 0.f;
   uint32_t k0 = 0, k1 = 0;
@@ -47,7 +50,8 @@ bool make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows);
 // Tensor map of a bf16 weight in the tiled layout (rows a multiple of 64), box = one
 // k block of box_rows (a multiple of 64) rows.
 bool make_map_tiled(CUtensorMap* m, const void* base, int rows, int K, int box_rows);
-Plan plan(int rows, int outs, int K, int xplanes, int wplanes, bool lm);
+// lm or one_split: no k splits (the LM head; products whose epilogue needs the full sums)
+Plan plan(int rows, int outs, int K, int xplanes, int wplanes, bool lm, bool one_split = false);
 // Rows of the activation tile loads: the valid rows (rounded to 8) when they fit one tile.
 inline int x_box_rows(int rows) { return rows >= 128 ? 128 : ((rows + 7) / 8) * 8; }
 // Shared-memory slot of one activation tile: the loaded rows, rounded to a 1 KB swizzle atom group.

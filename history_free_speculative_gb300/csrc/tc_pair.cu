@@ -224,10 +224,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         const int col = o0 + c + lane;
         if (row0 < p.rows) {
-#pragma unroll 8
-          for (int j = 0; j < 32; ++j) {
-            const float v = stg[j * 32 + (lane ^ j)];
-            if (row0 + j < p.rows && col < p.outs) out[(size_t)(row0 + j) * p.outs + col] = v;
+          // 16 shared-memory reads first: a read placed after a global store
+          // (which may alias it, as far as the compiler knows) would wait for it
+          for (int h = 0; h < 32; h += 16) {
+            float vals[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) vals[j] = stg[(h + j) * 32 + (lane ^ (h + j))];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (row0 + h + j < p.rows && col < p.outs) out[(size_t)(row0 + h + j) * p.outs + col] = vals[j];
           }
         }
         __syncwarp();
@@ -265,34 +270,69 @@ Splits pair_splits(const PairPlan& pl) {
 
 bool use_pair_engine(int rows, int xplanes, int wplanes) {
   // Up to 512 rows (4 TMEM-resident 128-row tiles) the one-CTA engine with
-  // uniform split-K measured as fast or faster on the drafter's products (fewer
-  // partial planes for the consumers, a cheaper launch); beyond that it has to
-  // split the rows into groups that each stream the weights again.
+  // uniform split-K measured as fast or faster on the drafter's products
+  // (fewer partial planes for the consumers, a cheaper launch); beyond that it
+  // has to split the rows into groups that each stream the weights again.
   return xplanes == 1 && wplanes == 1 && rows > 512;
 }
 
 PairPlan pair_plan(int rows, int outs, int K, int num_sms) {
-  PairPlan pl;
-  if (rows <= 128 || rows > 4096 || K % 64 || K < 64 || outs % 8 || outs <= 64 || num_sms < 2) return pl;
-  pl.kblocks = K / 64;
-  pl.slabs = (outs + kPairN - 1) / kPairN;
-  pl.groups = (rows + 255) / 256;
-  pl.U = (long long)pl.groups * pl.slabs * pl.kblocks;
+  PairPlan best;
+  if (rows <= 128 || rows > 4096 || K % 64 || K < 64 || outs % 8 || outs <= 64 || num_sms < 2) return best;
+  const int kblocks = K / 64;
+  const int slabs = (outs + kPairN - 1) / kPairN;
+  const int groups = (rows + 255) / 256;
+  const long long tiles = (long long)groups * slabs;
+  const long long U = tiles * kblocks;
   const long long pairs = num_sms / 2;
-  pl.G = (int)(pl.U < pairs ? pl.U : pairs);
-  const int stages = (int)((kSmemBudget - 2048 - kPairStaging) / kPairStage);
-  pl.stages = stages > 8 ? 8 : stages;
-  // the most workers sharing one tile = partial planes written
-  const Splits sp = pair_splits(pl);
-  int smax = 1;
-  for (long long tile = 0; tile < (long long)pl.groups * pl.slabs; ++tile) {
-    const long long u0 = tile * pl.kblocks;
-    const int n = (int)(splits_owner(sp, u0 + pl.kblocks - 1) - splits_owner(sp, u0) + 1);
-    smax = n > smax ? n : smax;
+  const int stages0 = (int)((kSmemBudget - 2048 - kPairStaging) / kPairStage);
+  // Cost model (seconds): a k block costs ~700 cycles of 2-SM MMA per SM; the
+  // weights stream at ~6.5 TB/s per row group; each partial plane is written
+  // and read back once; an epilogue drains 128 x 256 floats per CTA.
+  const double clk = 1.9e9, hbm = 6.5e12, t_kb = 700.0 / clk, t_epi = 1.5e-6, launch = 3.0e-6;
+  const double t_hbm = (double)outs * K * 2.0 * groups / hbm;
+  double best_t = 1e30;
+  // candidates: G = tiles * S workers (S dividing the k blocks: exactly S planes
+  // per tile, several waves if G > pairs), or stream-K with G = pairs
+  for (int cand = 0; cand <= 16; ++cand) {
+    long long G;
+    if (cand == 0) {
+      G = U < pairs ? U : pairs;
+    } else {
+      const int S = cand;
+      if (kblocks % S) continue;
+      G = tiles * S;
+    }
+    PairPlan pl;
+    pl.kblocks = kblocks;
+    pl.slabs = slabs;
+    pl.groups = groups;
+    pl.U = U;
+    pl.G = (int)G;
+    pl.stages = stages0 > 8 ? 8 : stages0;
+    const Splits sp = pair_splits(pl);
+    int smax = 1;
+    double mean = 0.0;
+    for (long long t = 0; t < tiles; ++t) {
+      const long long u0 = t * kblocks;
+      const int n = (int)(splits_owner(sp, u0 + kblocks - 1) - splits_owner(sp, u0) + 1);
+      smax = n > smax ? n : smax;
+      mean += n;
+    }
+    mean /= (double)tiles;
+    pl.S = smax;
+    if (smax > 16) continue;
+    const long long waves = (G + pairs - 1) / pairs;
+    const double per_pair = (double)((U + G - 1) / G) * t_kb + t_epi * (double)((U + G - 1) / G / kblocks + 1);
+    double t = (double)waves * per_pair;
+    t = (t > t_hbm ? t : t_hbm) + launch + mean * rows * (double)outs * 8.0 / hbm;
+    if (t < best_t * 0.999) {
+      best_t = t;
+      best = pl;
+      best.ok = true;
+    }
   }
-  pl.S = smax;
-  pl.ok = true;
-  return pl;
+  return best;
 }
 
 size_t pair_smem_bytes(const PairPlan& pl) {
