@@ -42,14 +42,14 @@ def dist_env():
     return ws, rank, local
 
 
-KERNEL_SOURCES = ["tc_gemm.cu", "tc_gemm.h", "common.cuh", "internal.h"]
+KERNEL_SOURCES = ["lm_head.cu", "tc_device.cuh", "tc_gemm.h", "internal.h", "common.cuh"]
 
 
 def lm_head_traffic():
     """DRAM bytes per LM-head launch from the committed ncu summary, or None when
     the kernel sources changed since that capture."""
     import hashlib
-    prof = os.path.join(ROOT, "profiles", "lm_head_tc_gemm_qwen3-8b-b32.md")
+    prof = os.path.join(ROOT, "profiles", "lm_head_kernel_qwen3-8b-b32.md")
     if not os.path.exists(prof):
         return None
     vals = {}
