@@ -223,6 +223,26 @@ int gemm(dlite_handle* h, const char* name, const Operand& X, const Operand& W, 
          float* part, Splits* sp_out, cudaStream_t s, bf16* const* act = nullptr, int act_planes = 1,
          bool* fused = nullptr) {
   if (fused) *fused = false;
+  // few rows: persistent stream-K over the weights (the gate/up product keeps
+  // the one-CTA engine, whose epilogue applies the SwiGLU)
+  if (!act && tc::use_stream_engine(rows, X.n, W.n)) {
+    const tc::StreamPlan sp = tc::stream_plan(rows, outs, X.K, h->num_sms);
+    if (sp.ok) {
+      h->maps.reserve(h->maps.size() + 4);
+      const CUtensorMap* x0 = get_map(h, X.p[0], X.rows, X.K, sp.x_box);
+      const CUtensorMap* w0 = get_map(h, W.p[0], W.rows, W.K, sp.N, true);
+      if (!x0 || !w0) return DLITE_ERR_CUDA;
+      tc::StreamParams prm;
+      prm.rows = rows;
+      prm.outs = outs;
+      prm.part = part;
+      prm.status = h->status;
+      if (sp_out) *sp_out = tc::stream_splits(sp);
+      CK(tc::launch_stream(sp, x0, w0, prm, s));
+      mark(h, name);
+      return DLITE_OK;
+    }
+  }
   if (tc::use_pair_engine(rows, X.n, W.n)) {  // 2-SM MMAs
     const tc::PairPlan pp = tc::pair_plan(rows, outs, X.K, h->num_sms);
     if (pp.ok) {
@@ -345,6 +365,7 @@ int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anch
     at.n_q = c.n_q;
     at.n_kv = c.n_kv;
     at.d_h = c.d_h;
+    at.hq = attention_heads_per_cta(c.n_q, c.n_kv, B);
     at.scale = (float)(1.0 / sqrt((double)c.d_h));
     at.round_bf16 = h->f32 ? 0 : 1;
     at.o[0] = h->o[0];
@@ -456,7 +477,7 @@ int run_lm_head(dlite_handle* h, int B, float temperature, uint64_t seed, const 
     prm.K_draft = c.K;
     prm.status = h->status;
     CK(tc::launch_lm_persistent(lp, x0, x1, w0, prm, s));
-    n_tiles = lp.n_units * lp.groups;
+    n_tiles = lp.n_units;  // one record per walk and row
   } else {  // one slab per CTA
     const tc::Plan pl = lm_plan(h, rows);
     if (!pl.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
@@ -676,6 +697,9 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
       const size_t v = (size_t)pl.S * st[0] * st[1];
       pe = v > pe ? v : pe;
       const tc::PairPlan pp = tc::pair_plan(st[0], st[1], st[2], h->num_sms);
+      const tc::StreamPlan sq = tc::stream_plan(st[0], st[1], st[2], h->num_sms);
+      if (sq.ok && tc::use_stream_engine(st[0], st[3], h->np))
+        pe = (size_t)sq.S * st[0] * st[1] > pe ? (size_t)sq.S * st[0] * st[1] : pe;
       if (pp.ok && tc::use_pair_engine(st[0], st[3], h->np)) pe = (size_t)pp.S * st[0] * st[1] > pe ? (size_t)pp.S * st[0] * st[1] : pe;  // planes
     }
     const tc::Plan pc = tc::plan(C, 2 * h->kvd, D, h->np, h->np, false);
@@ -683,6 +707,9 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
     const size_t v2 = (size_t)pc.S * C * 2 * h->kvd;
     pe2 = v2 > pe2 ? v2 : pe2;
     const tc::PairPlan pc2 = tc::pair_plan(C, 2 * h->kvd, D, h->num_sms);
+    const tc::StreamPlan sc2 = tc::stream_plan(C, 2 * h->kvd, D, h->num_sms);
+    if (sc2.ok && tc::use_stream_engine(C, h->np, h->np))
+      pe2 = (size_t)sc2.S * C * 2 * h->kvd > pe2 ? (size_t)sc2.S * C * 2 * h->kvd : pe2;
     if (pc2.ok && tc::use_pair_engine(C, h->np, h->np)) pe2 = (size_t)pc2.S * C * 2 * h->kvd > pe2 ? (size_t)pc2.S * C * 2 * h->kvd : pe2;
     const tc::Plan pl = lm_plan(h, H);
     if (!pl.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
@@ -690,7 +717,7 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
     lme = v3 > lme ? v3 : lme;
     const tc::LmPlan lp = tc::lm_plan_persistent(H, V, D, h->num_sms);
     if (lp.ok) {
-      const size_t v4 = (size_t)lp.n_units * lp.groups * H;
+      const size_t v4 = (size_t)lp.n_units * H;
       lme = v4 > lme ? v4 : lme;
     }
   }
@@ -959,6 +986,24 @@ int dlite_selftest_gemm(int rows, int outs, int K, int xplanes, int wplanes, con
   if ((xplanes == 2 && !X1) || (wplanes == 2 && !W1)) return DLITE_ERR_INVALID_ARG;
   if (xplanes == 1 && wplanes == 2) return DLITE_ERR_INVALID_ARG;  // plane products x0w0 (+x1w0) (+x0w1)
   const int wrows = (outs + 63) / 64 * 64;
+  if (!plan_override && tc::use_stream_engine(rows, xplanes, wplanes)) {  // the round's route
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return DLITE_ERR_CUDA;
+    const tc::StreamPlan sp = tc::stream_plan(rows, outs, K, sms);
+    if (sp.ok) {
+      CUtensorMap mx, mw;
+      if (!tc::make_map(&mx, X0, x_rows, K, sp.x_box) || !tc::make_map_tiled(&mw, W0, wrows, K, sp.N))
+        return DLITE_ERR_CUDA;
+      tc::StreamParams prm;
+      prm.rows = rows;
+      prm.outs = outs;
+      prm.part = part;
+      prm.status = status;
+      CK(tc::launch_stream(sp, &mx, &mw, prm, (cudaStream_t)stream));
+      return sp.S;
+    }
+  }
   if (!plan_override && tc::use_pair_engine(rows, xplanes, wplanes)) {  // the round's route
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -1030,9 +1075,11 @@ int dlite_launch_count(dlite_handle* h, int B, float temperature) {
   if (!h || B < 1) return -1;
   (void)temperature;
   // stage + per layer {qkv, ctx-kv, attention, o, resnorm, gate/up (+ swiglu on the pair
-  // engine), down, resnorm} + head {ce, chain, P, out} + lm {head, merge} + verify
+  // engine; the one-CTA engine fuses it), down, resnorm} + head {ce, chain, P, out}
+  // + lm {head, merge} + verify
   const int L = B * (h->cfg.K + 1);
-  const int per_layer = tc::use_pair_engine(L, h->np, h->np) ? 9 : 8;
+  const bool fused = !tc::use_pair_engine(L, h->np, h->np);
+  const int per_layer = fused ? 8 : 9;
   return 1 + per_layer * h->cfg.L_D + 4 + 2 + 1;
 }
 

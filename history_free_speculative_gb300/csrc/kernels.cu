@@ -153,9 +153,10 @@ cudaError_t launch_stage(const StageArgs& a, bool f32, cudaStream_t s) {
 }
 
 // ---------------------------------------------------------------- K2b: block attention
-// One CTA per (key/value head g, request b) serving the n_q / n_kv query heads
-// of its group, so each head's keys and values are reduced from the split-K
-// partials once. Sums the QKV partials of the request's rows (4 columns per
+// One CTA per (hq query heads of one key/value group, request b): with many
+// requests hq = n_q / n_kv, so each head's keys and values are reduced from the
+// split-K partials once; with few requests hq shrinks to spread the work over
+// more SMs (the keys and values are then reduced by each CTA of the group). Sums the QKV partials of the request's rows (4 columns per
 // item), applies RoPE to the local queries / keys (table [K+1][d_h/2]), then
 // runs non-causal softmax attention of each query row over all m + K + 1 keys:
 // one warp per query row, one lane per key for the scores, warp-shuffle
@@ -167,8 +168,8 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(AttnArgs a) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ float sm[];
-  const int g = blockIdx.x, b = blockIdx.y;
-  const int K1 = a.K + 1, dh = a.d_h, half = dh / 2, G = a.n_q / a.n_kv;
+  const int G = a.hq, g = (int)(blockIdx.x * G) / (a.n_q / a.n_kv), h0 = blockIdx.x * G, b = blockIdx.y;
+  const int K1 = a.K + 1, dh = a.d_h, half = dh / 2;
   const int qd = a.n_q * dh, kvd = a.n_kv * dh;
   const int ldl = qd + 2 * kvd;  // local partial row width
   const int ldc = 2 * kvd;       // context partial row width
@@ -200,7 +201,7 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(AttnArgs a) {
   const int nq = G * K1 * h4, nk = K1 * h4, nv = K1 * d4, nc = a.m * d4;
   for (int idx = threadIdx.x; idx < nq + nk + nv + 2 * nc; idx += blockDim.x) {
     if (idx < nq) {  // queries of the group's heads (rotated)
-      const int j = (idx % h4) * 4, r = idx / h4, hh = r / K1, i = r % K1, col = (g * G + hh) * dh;
+      const int j = (idx % h4) * 4, r = idx / h4, hh = r / K1, i = r % K1, col = (h0 + hh) * dh;
       rope(qs + r * LD, i, j, loc4(i, col + j), loc4(i, col + j + half));
     } else if (idx < nq + nk) {  // local keys (rotated)
       const int t = idx - nq, j = (t % h4) * 4, i = t / h4, col = qd + g * dh;
@@ -247,7 +248,7 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(AttnArgs a) {
         acc.w = fmaf(pk, v.w, acc.w);
       }
     }
-    if (lane < d4) store4_planes(a.o, a.no, (size_t)(b * K1 + i) * qd + (g * G + hh) * dh + 4 * lane, acc);
+    if (lane < d4) store4_planes(a.o, a.no, (size_t)(b * K1 + i) * qd + (h0 + hh) * dh + 4 * lane, acc);
   }
 }
 
@@ -255,8 +256,15 @@ size_t attention_smem(int K, int m, int d_h, int G) {
   return (size_t)(G * (K + 1) + 2 * (m + K + 1)) * (d_h + 4) * sizeof(float);
 }
 
+int attention_heads_per_cta(int n_q, int n_kv, int B) {
+  // aim for at least ~128 CTAs; hq divides the group size n_q / n_kv
+  int hq = n_q / n_kv;
+  while (hq > 1 && (n_q / hq) * B < 128 && (n_q / n_kv) % (hq / 2) == 0) hq /= 2;
+  return hq;
+}
+
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s) {
-  const size_t smem = attention_smem(a.K, a.m, a.d_h, a.n_q / a.n_kv);
+  const size_t smem = attention_smem(a.K, a.m, a.d_h, a.hq);
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -264,7 +272,7 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  return launch_pdl(attention_kernel, dim3(a.n_kv, a.B), dim3(kAttnThreads), smem, s, a);
+  return launch_pdl(attention_kernel, dim3(a.n_q / a.hq, a.B), dim3(kAttnThreads), smem, s, a);
 }
 
 // ---------------------------------------------------------------- residual + RMSNorm

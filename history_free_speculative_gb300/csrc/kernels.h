@@ -33,6 +33,7 @@ struct AttnArgs {
   const float* rope_cos = nullptr;  // [K+1][d_h/2]
   const float* rope_sin = nullptr;
   int B = 0, m = 0, K = 0, n_q = 0, n_kv = 0, d_h = 0;
+  int hq = 1;  // query heads per CTA (divides n_q / n_kv): attention_heads_per_cta
   float scale = 1.f;
   int round_bf16 = 0;
   bf16* o[2] = {nullptr, nullptr};  // [B*(K+1), n_q*d_h]
@@ -92,6 +93,7 @@ struct VerifyArgs {
 cudaError_t launch_stage(const StageArgs& a, bool f32, cudaStream_t s);
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s);
 size_t attention_smem(int K, int m, int d_h, int G);
+int attention_heads_per_cta(int n_q, int n_kv, int B);
 cudaError_t launch_resnorm(const ResNormArgs& a, cudaStream_t s);
 cudaError_t launch_swiglu_interleaved(const float* part, const Splits& sp, int rows, int F, bf16* const* o, int no,
                                       cudaStream_t s);

@@ -13,8 +13,8 @@
 // accumulates, the epilogue warps score slab t-1, so the sampling arithmetic
 // runs under the stream of E from HBM. Every epilogue thread owns one row and
 // keeps its running top-4 and LSE partials over all slabs of its CTA in
-// registers, writing one record per walk and column group at the end; the
-// merge kernel combines them.
+// registers; at the end the column groups of a row are combined in shared
+// memory and one record per walk is written; the merge kernel combines them.
 //
 // Warp roles: warp 0 TMA producer (E slab k block + h tile per 64-wide k
 // block, through a ring of shared-memory stages; in a pair every copy signals
@@ -289,7 +289,31 @@ __global__ void __launch_bounds__(kLmThreads, 1)
           mbar_arrive(acce0 + 8 * b);
       }
     }
-    if (valid) lm_acc_store(acc, p.rec + ((size_t)unit * kLmGroups + eg) * p.rows + row);
+    // combine the column groups of each row in shared memory (the stage memory
+    // is idle once every product has completed): one record per row and walk
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    LmRec* sm_rec = reinterpret_cast<LmRec*>(smem);  // [kLmGroups][128]
+    const int rl = q * 32 + lane;
+    lm_acc_store(acc, sm_rec + eg * 128 + rl);
+    asm volatile("bar.sync 1, %0;" ::"r"(4 * kLmGroups * 32) : "memory");  // the epilogue warps only
+    if (eg == 0 && valid) {
+      for (int g2 = 1; g2 < kLmGroups; ++g2) {
+        const LmRec o = sm_rec[g2 * 128 + rl];
+#pragma unroll
+        for (int k = 0; k < kTopK; ++k) topk_insert(acc.sc, acc.id, o.sc[k], o.id[k]);
+        if (o.m != -INFINITY) {  // base-2 LSE partials
+          if (acc.m == -INFINITY) {
+            acc.m = o.m;
+            acc.s = o.s;
+          } else {
+            const float mm = fmaxf(acc.m, o.m);
+            acc.s = acc.s * ex2_approx(acc.m - mm) + o.s * ex2_approx(o.m - mm);
+            acc.m = mm;
+          }
+        }
+      }
+      lm_acc_store(acc, p.rec + (size_t)unit * p.rows + row);
+    }
   }
   fence_before();
   __syncthreads();

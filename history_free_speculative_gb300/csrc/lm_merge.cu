@@ -85,11 +85,10 @@ __device__ __forceinline__ float exact_logit(const LmMergeArgs& a, int v, const 
   return warp_sum(acc);
 }
 
-// One CTA of kMergeWarps warps per row: every thread folds a strided subset of
-// the records into a register top-k + LSE, the warps combine by butterfly,
-// thread 0 combines the warps in a fixed order, and the 4 warps re-score the 4
-// finalists exactly in parallel.
-constexpr int kMergeWarps = 4;  // one finalist per warp in the re-scoring
+// One CTA of kMergeWarps warps per row: every thread folds a strided subset of the records
+// into a register top-k + LSE, the warps combine by butterfly, thread 0
+// combines the warps in a fixed order, and warps 0-3 re-score the 4 finalists
+// exactly in parallel.
 
 // Gumbel noise -log(-log u) of the uniform u01f(x) with full relative accuracy
 // where it matters: for u within 2^-8 of 1, -log u is formed from the exact
@@ -102,7 +101,9 @@ __device__ __forceinline__ float gumbel_f(uint32_t x) {
   return -logf(nl);
 }
 
+template <int kMergeWarps>
 __global__ void __launch_bounds__(kMergeWarps * 32) lm_merge_kernel(const LmMergeArgs a) {
+  static_assert(kMergeWarps >= kTopK, "one warp per finalist");
   pdl_trigger();
   pdl_wait();
   __shared__ float wsc[kMergeWarps][kTopK];
@@ -123,11 +124,21 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lm_merge_kernel(const LmMerg
     id[k] = 0x7fffffff;
   }
   float m = -INFINITY, s = 0.f;
-  for (int t = threadIdx.x; t < a.n_tiles; t += blockDim.x) {
-    const LmRec rec = a.rec[(size_t)t * a.rows + r];
+  constexpr int kBatch = 4;  // records loaded before any is folded
+  for (int t0 = threadIdx.x; t0 < a.n_tiles; t0 += blockDim.x * kBatch) {
+    LmRec rec[kBatch];
 #pragma unroll
-    for (int k = 0; k < kTopK; ++k) topk_insert(sc, id, rec.sc[k], rec.id[k]);
-    if (sampling) lse_merge(m, s, rec.m, rec.s);
+    for (int u = 0; u < kBatch; ++u) {
+      const int t = t0 + u * blockDim.x;
+      if (t < a.n_tiles) rec[u] = a.rec[(size_t)t * a.rows + r];
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      if (t0 + u * (int)blockDim.x >= a.n_tiles) break;
+#pragma unroll
+      for (int k = 0; k < kTopK; ++k) topk_insert(sc, id, rec[u].sc[k], rec[u].id[k]);
+      if (sampling) lse_merge(m, s, rec[u].m, rec[u].s);
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {  // both partners end with the same list (disjoint sets)
@@ -215,7 +226,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lm_merge_kernel(const LmMerg
 }
 
 cudaError_t launch_lm_merge(const LmMergeArgs& a, cudaStream_t s) {
-  return launch_pdl(lm_merge_kernel, dim3(a.rows), dim3(kMergeWarps * 32), 0, s, a);
+  return launch_pdl(lm_merge_kernel<4>, dim3(a.rows), dim3(4 * 32), 0, s, a);
 }
 
 }  // namespace dlite

@@ -61,7 +61,7 @@ size_t smem_bytes(const Plan& pl);
 // Persistent LM-head kernel (rows <= 256): one CTA per SM walking the
 // vocabulary slabs with double-buffered TMEM accumulators (sampling epilogue
 // overlapped with the E stream); rows 129..256 use CTA pairs, one 128-row tile
-// of h each, on the same slabs. Records are [n_units * groups][rows].
+// of h each, on the same slabs. Records are [n_units][rows].
 struct LmPlan {
   bool ok = false;
   bool paired = false;
@@ -96,6 +96,31 @@ struct PairParams {
   float* part = nullptr;
   int* status = nullptr;
 };
+// Persistent stream-K GEMM for <= 128 rows (bf16 operands): grid = G CTAs (one
+// per SM); W maps with N-row boxes, X maps with x_box-row boxes; partials laid
+// out as stream_splits() describes.
+struct StreamPlan {
+  bool ok = false;
+  int N = 0, x_box = 0, kblocks = 0, slabs = 0, stages = 0, G = 0, S = 1;
+  uint32_t stage_bytes = 0;
+  size_t tail_pad = 0;
+  long long U = 0;
+};
+struct StreamParams {
+  int rows = 0, outs = 0;
+  int kblocks = 0, stages = 0, x_box = 8, G = 1;
+  uint32_t stage_bytes = 0;
+  long long U = 1;
+  float* part = nullptr;
+  int* status = nullptr;
+};
+bool use_stream_engine(int rows, int xplanes, int wplanes);
+StreamPlan stream_plan(int rows, int outs, int K, int num_sms);
+Splits stream_splits(const StreamPlan& pl);
+size_t stream_smem_bytes(const StreamPlan& pl);
+cudaError_t launch_stream(const StreamPlan& pl, const CUtensorMap* x, const CUtensorMap* w, StreamParams prm,
+                          cudaStream_t s);
+
 bool use_pair_engine(int rows, int xplanes, int wplanes);
 PairPlan pair_plan(int rows, int outs, int K, int num_sms);
 Splits pair_splits(const PairPlan& pl);
