@@ -45,7 +45,7 @@ struct dlite_handle {
   LayerW layer[DLITE_MAX_LAYERS];
   const bf16* Wce[2] = {nullptr, nullptr};  // [2R, D] = [Q_b; Q_h]
   const bf16* P[2] = {nullptr, nullptr};    // [D, R]
-  float* Mt = nullptr;                      // [R, R] transposed Q_h P
+  float* Mt = nullptr;                      // [R, R] Q_h P in the chain's register image
   float *rope_cos = nullptr, *rope_sin = nullptr;
 
   // workspace
@@ -126,11 +126,11 @@ int check_config(const dlite_config* c) {
   if (c->n_q < 1 || c->n_kv < 1 || c->n_q % c->n_kv) return DLITE_ERR_UNSUPPORTED_SHAPE;
   if (c->d_h != 64 && c->d_h != 128) return DLITE_ERR_UNSUPPORTED_SHAPE;
   if (c->D > 16384) return DLITE_ERR_UNSUPPORTED_SHAPE;  // row kernels: 4 float4 per thread
-  if (c->D % 64 || c->F % 64 || c->R % 32 || c->R > 1024 || c->V < 8 || c->V % 8 || c->V > 262144)
+  if (c->D % 64 || c->F % 64 || c->R % 32 || c->R > 512 || c->V < 8 || c->V % 8 || c->V > 262144)
     return DLITE_ERR_UNSUPPORTED_SHAPE;
   if ((c->n_q * c->d_h) % 64) return DLITE_ERR_UNSUPPORTED_SHAPE;
   if (attention_smem(c->K, c->m, c->d_h, c->n_q / c->n_kv) > 200 * 1024) return DLITE_ERR_UNSUPPORTED_SHAPE;
-  if (c->R < 32 || chain_smem_bytes(c->R, chain_group_size(c->R, c->B_max)) > 200 * 1024)
+  if (c->R < 32 || chain_smem_bytes(c->R, c->K, chain_group_size(c->R, c->B_max)) > 200 * 1024)
     return DLITE_ERR_UNSUPPORTED_SHAPE;
   if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return DLITE_ERR_INVALID_ARG;
   return DLITE_OK;

@@ -371,14 +371,19 @@ cudaError_t launch_swiglu_interleaved(const float* part, const Splits& sp, int r
 // With Q = [Q_b | Q_h] and M = Q_h P (R x R), the head h_i = b_i + P t_i has
 // t_1 = tanh(c_1), t_i = tanh(c_i + e_{i-1} + M t_{i-1}) where c_i = Q_b b_i
 // and e_i = Q_h b_i come from one product over all rows.
-// Persistent cluster kernel: a cluster of kChainCluster CTAs serves a group of
-// Bg requests; CTA k owns rows [k*R/C, (k+1)*R/C) of M, kept in shared memory
-// (transposed, so a warp reads consecutive rows), computes those entries of
-// t_i for every request of the group and writes them into the state buffer
-// of every CTA of the cluster (distributed shared memory). One hardware
-// cluster barrier per step; the state never leaves the chip.
+// Persistent cluster kernel, M held in registers: a cluster of kChainCluster
+// CTAs serves a group of Bg requests; CTA k owns rows [k*rc, (k+1)*rc) of M
+// (rc = R/8) and runs R/32 warps. Warp w owns rows k*rc + 4w + rr (rr < 4);
+// its lane L holds M[k*rc + 4w + rr][L + 32j] for j < R/32. A step reads the
+// previous state once per warp with conflict-free 32-bit loads (lane L reads
+// entries L + 32j), does 4 R/32 FMAs per lane and a reduce-scatter over the
+// warp (six shuffles) that leaves row 2*bit4 + bit3 of the lane's index in
+// each group of eight lanes; lane L & 7 then sends the new entry to CTA L & 7
+// of the cluster (distributed shared memory). One hardware cluster barrier per
+// step; the state never leaves the chip.
 constexpr int kChainCluster = 8;
-constexpr int kChainThreads = 256;
+constexpr int kChainMaxJ = 16;        // R <= 512
+constexpr int kChainMaxClusters = 16;  // clusters per launch (128 CTAs)
 
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -394,97 +399,195 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t local_addr, uint32_t ran
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
 
-__global__ void __launch_bounds__(kChainThreads) head_chain_kernel(ChainArgs a) {
+template <int NJ>  // R = 32 NJ
+__global__ void __launch_bounds__(512, 1) head_chain_kernel(ChainArgs a) {
   pdl_trigger();
-  pdl_wait();
   extern __shared__ float sm[];
-  const int R = a.R, rc = R / kChainCluster;
-  const int Bg = a.Bg;
-  float* Ms = sm;                      // [R][rc]: Ms[s][r] = M[r0 + r][s]
-  float* tbuf = Ms + (size_t)R * rc;   // [2][Bg][R]
+  constexpr int R = 32 * NJ, rc = R / kChainCluster;
+  const int Bg = a.Bg, K = a.K;
+  float* tbuf = sm;                    // [2][Bg][R] state, written by every CTA of the cluster
+  float* ce = tbuf + 2 * (size_t)Bg * R;  // [Bg][K][rc] (c, e) pairs of this CTA's rows
   const uint32_t rank = cluster_ctarank();
   const int group = blockIdx.x / kChainCluster;
   const int r0 = (int)rank * rc;
-  {  // this CTA's contiguous slice of M: R * rc floats, float4 loads
-    const float4* src = reinterpret_cast<const float4*>(a.Mt + (size_t)rank * R * rc);
-    float4* dst = reinterpret_cast<float4*>(Ms);
-    const int n4 = R * rc / 4;
-#pragma unroll 8
-    for (int i = threadIdx.x; i < n4; i += blockDim.x) dst[i] = src[i];
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  // this lane's entries of M (constant: loaded before waiting for the previous kernel)
+  float m[4][NJ];
+  {
+    const float* src = a.Mt + (size_t)rank * 4 * NJ * R + tid;
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) m[rr][j] = src[(size_t)(rr * NJ + j) * R];
   }
-  const int rl = threadIdx.x % rc, ql = threadIdx.x / rc;  // (row, request) of this thread
-  const int req = group * Bg + ql;
-  const bool active = threadIdx.x < rc * Bg && req < a.B;
+  pdl_wait();
+  // c_i, e_i of this CTA's rows for every (request, step): sum of the split planes
   const size_t stride = (size_t)a.rows * 2 * a.Rp;
-  float e_prev = 0.f;
-  // c_i, e_i of this thread's (row, request) for every step, loaded up front
-  float cs[32], es[32];
-  if (active) {
-    for (int i = 0; i < a.K; ++i) {
-      const float* p = a.part + (size_t)(req * a.K + i) * 2 * a.Rp + r0 + rl;
-      float c[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
+  const int n_ce = Bg * K * rc;
+  for (int idx = tid; idx < n_ce; idx += blockDim.x) {
+    const int r = idx % rc, i = (idx / rc) % K, q = idx / (rc * K);
+    const int req = group * Bg + q;
+    float c = 0.f, e = 0.f;
+    if (req < a.B) {
+      const float* p = a.part + (size_t)(req * K + i) * 2 * a.Rp + r0 + r;
+      float cc[4] = {0.f, 0.f, 0.f, 0.f}, ee[4] = {0.f, 0.f, 0.f, 0.f};
       int sp = 0;
-      for (; sp + 4 <= a.S; sp += 4) {  // 8 independent loads in flight
+      for (; sp + 4 <= a.S; sp += 4) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          c[k] += p[(size_t)(sp + k) * stride];
-          e[k] += p[(size_t)(sp + k) * stride + a.Rp];
+          cc[k] += p[(size_t)(sp + k) * stride];
+          ee[k] += p[(size_t)(sp + k) * stride + a.Rp];
         }
       }
       for (; sp < a.S; ++sp) {
-        c[0] += p[(size_t)sp * stride];
-        e[0] += p[(size_t)sp * stride + a.Rp];
+        cc[0] += p[(size_t)sp * stride];
+        ee[0] += p[(size_t)sp * stride + a.Rp];
       }
-      cs[i] = (c[0] + c[1]) + (c[2] + c[3]);
-      es[i] = (e[0] + e[1]) + (e[2] + e[3]);
+      c = (cc[0] + cc[1]) + (cc[2] + cc[3]);
+      e = (ee[0] + ee[1]) + (ee[2] + ee[3]);
     }
+    ce[2 * (size_t)idx] = c;
+    ce[2 * (size_t)idx + 1] = e;
   }
-  cluster_sync_all();  // every CTA of the cluster is running before any remote store
-  for (int i = 0; i < a.K; ++i) {
-    float t = 0.f;
-    if (active) {
-      const int row = req * a.K + i;
-      const float c = cs[i], e = es[i];
-      float acc = c;
+  cluster_sync_all();  // every CTA of the cluster is running before any remote store; ce is visible
+  const int nq = min(Bg, a.B - group * Bg);  // live requests of this group
+  const bool hi = lane & 16, b3 = lane & 8;
+  const int rl = 4 * w + 2 * (int)hi + (int)b3;  // the row this lane's group of eight ends up with
+  const int dst = lane & 7;                        // the CTA this lane sends to
+  for (int i = 0; i < K; ++i) {
+    const float* tprev = tbuf + (size_t)((i - 1) & 1) * Bg * R;
+    for (int q0 = 0; q0 < nq; q0 += 4) {  // up to four requests interleaved
+      float dot[4] = {0.f, 0.f, 0.f, 0.f};
       if (i > 0) {
-        const float* tp = tbuf + ((size_t)((i - 1) & 1) * Bg + ql) * R;
-        float mt = 0.f;
-#pragma unroll 4
-        for (int k = 0; k < R; k += 4) {
-          const float4 tv = *reinterpret_cast<const float4*>(tp + k);
-          mt = fmaf(Ms[(size_t)k * rc + rl], tv.x, mt);
-          mt = fmaf(Ms[(size_t)(k + 1) * rc + rl], tv.y, mt);
-          mt = fmaf(Ms[(size_t)(k + 2) * rc + rl], tv.z, mt);
-          mt = fmaf(Ms[(size_t)(k + 3) * rc + rl], tv.w, mt);
+        float p[4][4];  // [request][row]
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr) p[q][rr] = 0.f;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (q0 + q < nq) {
+              const float tv = tprev[(size_t)(q0 + q) * R + lane + 32 * j];
+#pragma unroll
+              for (int rr = 0; rr < 4; ++rr) p[q][rr] = fmaf(m[rr][j], tv, p[q][rr]);
+            }
+          }
         }
-        acc += e_prev + mt;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (q0 + q >= nq) break;  // uniform across the warp
+          // reduce-scatter: halves of the warp keep rows {0,1} / {2,3}, then quarters one row
+          float k0 = hi ? p[q][2] : p[q][0], k1 = hi ? p[q][3] : p[q][1];
+          const float s0 = hi ? p[q][0] : p[q][2], s1 = hi ? p[q][1] : p[q][3];
+          k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+          k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+          float d = b3 ? k1 : k0;
+          d += __shfl_xor_sync(0xffffffffu, b3 ? k0 : k1, 8);
+          d += __shfl_xor_sync(0xffffffffu, d, 4);
+          d += __shfl_xor_sync(0xffffffffu, d, 2);
+          d += __shfl_xor_sync(0xffffffffu, d, 1);
+          dot[q] = d;
+        }
       }
-      t = tanhf(acc);
-      e_prev = e;
-      a.t[(size_t)row * R + r0 + rl] = t;
-      store_planes(a.tp, 2, (size_t)row * a.ldt + r0 + rl, t);
-      const uint32_t laddr = (uint32_t)__cvta_generic_to_shared(
-          tbuf + ((size_t)(i & 1) * Bg + ql) * R + r0 + rl);
-      for (int k = 0; k < kChainCluster; ++k) st_cluster_f32(laddr, (uint32_t)k, t);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (q0 + q >= nq) break;
+        const float* cq = ce + 2 * ((size_t)((q0 + q) * K + i) * rc + rl);
+        float acc = cq[0];
+        if (i > 0) acc += cq[1 - 2 * rc] + dot[q];  // e_{i-1} of the same row
+        const float t = tanhf(acc);
+        const int row = (group * Bg + q0 + q) * K + i;
+        if (dst == 0) a.t[(size_t)row * R + r0 + rl] = t;
+        if (dst == 1) store_planes(a.tp, 2, (size_t)row * a.ldt + r0 + rl, t);
+        const uint32_t laddr =
+            (uint32_t)__cvta_generic_to_shared(tbuf + ((size_t)(i & 1) * Bg + q0 + q) * R + r0 + rl);
+        st_cluster_f32(laddr, (uint32_t)dst, t);
+      }
     }
     cluster_sync_all();
   }
 }
 
-cudaError_t launch_head_chain(const ChainArgs& a, cudaStream_t s) {
-  const int rc = a.R / kChainCluster;
-  const int groups = (a.B + a.Bg - 1) / a.Bg;
-  const size_t smem = ((size_t)a.R * rc + 2 * (size_t)a.Bg * a.R) * sizeof(float);
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(head_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         200 * 1024);
-    if (e != cudaSuccess) return e;
-    attr = true;
+int chain_group_size(int R, int B) {
+  (void)R;
+  return (B + kChainMaxClusters - 1) / kChainMaxClusters;
+}
+
+size_t chain_smem_bytes(int R, int K, int Bg) {
+  return (2 * (size_t)Bg * R + 2 * (size_t)Bg * K * (R / kChainCluster)) * sizeof(float);
+}
+
+using ChainFn = void (*)(ChainArgs);
+static ChainFn chain_fn(int R) {
+  switch (R / 32) {
+    case 1: return head_chain_kernel<1>;
+    case 2: return head_chain_kernel<2>;
+    case 3: return head_chain_kernel<3>;
+    case 4: return head_chain_kernel<4>;
+    case 5: return head_chain_kernel<5>;
+    case 6: return head_chain_kernel<6>;
+    case 7: return head_chain_kernel<7>;
+    case 8: return head_chain_kernel<8>;
+    case 9: return head_chain_kernel<9>;
+    case 10: return head_chain_kernel<10>;
+    case 11: return head_chain_kernel<11>;
+    case 12: return head_chain_kernel<12>;
+    case 13: return head_chain_kernel<13>;
+    case 14: return head_chain_kernel<14>;
+    case 15: return head_chain_kernel<15>;
+    case 16: return head_chain_kernel<16>;
+    default: return nullptr;
   }
+}
+
+// Clusters of the chain that are resident at once (at most kChainMaxClusters):
+// more would run in a second wave and double the serial time.
+static int chain_resident_clusters(ChainFn fn, int R, size_t smem) {
+  static int cached[kChainMaxJ + 1] = {};
+  const int nj = R / 32;
+  if (cached[nj]) return cached[nj];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kChainMaxClusters * kChainCluster, 1, 1);
+  cfg.blockDim = dim3(R, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = kChainCluster;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess || n < 1) {
+    (void)cudaGetLastError();
+    n = kChainMaxClusters;
+  }
+  cached[nj] = n < kChainMaxClusters ? n : kChainMaxClusters;
+  return cached[nj];
+}
+
+cudaError_t launch_head_chain(const ChainArgs& a_in, cudaStream_t s) {
+  if (a_in.R % 32 || a_in.R < 32 || a_in.R > 32 * kChainMaxJ) return cudaErrorInvalidValue;
+  const ChainFn fn = chain_fn(a_in.R);
+  static uint32_t attr_done = 0;
+  const uint32_t bit = 1u << (a_in.R / 32);
+  if (!(attr_done & bit)) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (e != cudaSuccess) return e;
+    attr_done |= bit;
+  }
+  ChainArgs a = a_in;
+  // as many requests per cluster as it takes for every cluster to be resident
+  const int fit = chain_resident_clusters(fn, a.R, chain_smem_bytes(a.R, a.K, a.Bg));
+  const int bg = (a.B + fit - 1) / fit;
+  if (bg > a.Bg && chain_smem_bytes(a.R, a.K, bg) <= 200 * 1024) a.Bg = bg;
+  const int groups = (a.B + a.Bg - 1) / a.Bg;
+  const size_t smem = chain_smem_bytes(a.R, a.K, a.Bg);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(groups * kChainCluster, 1, 1);
-  cfg.blockDim = dim3(kChainThreads, 1, 1);
+  cfg.blockDim = dim3(a.R, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attrs[2];
@@ -496,19 +599,7 @@ cudaError_t launch_head_chain(const ChainArgs& a, cudaStream_t s) {
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, head_chain_kernel, a);
-}
-
-int chain_group_size(int R, int B) {
-  const int rc = R / kChainCluster;
-  int bg = kChainThreads / rc;
-  if (bg < 1) bg = 1;
-  if (bg > B) bg = B;
-  return bg;
-}
-
-size_t chain_smem_bytes(int R, int Bg) {
-  return ((size_t)R * (R / kChainCluster) + 2 * (size_t)Bg * R) * sizeof(float);
+  return cudaLaunchKernelEx(&cfg, fn, a);
 }
 
 // h = b + sum_s part[s] (the P t_i product), kept in fp32 and as two bf16 planes.
@@ -1006,17 +1097,19 @@ cudaError_t launch_repack_gate_up(const void* Wg, const void* Wu, bool src_f32, 
 
 // M = Q_h P (R x R), float64 accumulate, stored as kChainCluster contiguous
 // slices: slice k holds rows [k*R/C, (k+1)*R/C) of M transposed,
-// Ms[k][s][r] = M[k*R/C + r][s], the shared-memory image of CTA k of the chain.
+// The chain's register image of M: float ((k * 4 R/32 + rr * R/32 + j) * R + 32 w + L)
+// holds M[k*R/8 + 4w + rr][L + 32j] for CTA k of the cluster, warp w, lane L.
 template <typename T>
 __global__ void head_matrix_kernel(const T* Q, const T* P, int D, int R, float* Ms) {
   const int s = blockIdx.x;
-  const int rc = R / kChainCluster;
+  const int rc = R / kChainCluster, nj = R / 32;
+  const int L = s & 31, j = s >> 5;
   for (int r = threadIdx.x; r < R; r += blockDim.x) {
     double acc = 0.0;
     for (int d = 0; d < D; ++d)
       acc += (double)to_f32(Q[(size_t)r * 2 * D + D + d]) * (double)to_f32(P[(size_t)d * R + s]);
-    const int k = r / rc, rl = r % rc;
-    Ms[((size_t)k * R + s) * rc + rl] = (float)acc;
+    const int k = r / rc, rl = r % rc, w = rl >> 2, rr = rl & 3;
+    Ms[((size_t)k * 4 * nj + rr * nj + j) * R + 32 * w + L] = (float)acc;
   }
 }
 

@@ -60,7 +60,7 @@ struct ResNormArgs {
 struct ChainArgs {
   const float* part = nullptr;  // [S][B*K][2Rp]: c at [0, R), e at [Rp, Rp + R)
   int S = 1, rows = 0;
-  const float* Mt = nullptr;    // M = Q_h P as 8 per-CTA slices [8][R][R/8] (transposed rows)
+  const float* Mt = nullptr;    // M = Q_h P in the chain's register image (launch_head_matrix)
   int B = 0, K = 0, R = 0;
   float* t = nullptr;           // [B*K, R]
   bf16* tp[2] = {nullptr, nullptr};  // [B*K, ldt] planes (columns R..ldt stay zero)
@@ -99,7 +99,7 @@ cudaError_t launch_swiglu_interleaved(const float* part, const Splits& sp, int r
                                       cudaStream_t s);
 cudaError_t launch_head_chain(const ChainArgs& a, cudaStream_t s);
 int chain_group_size(int R, int B);
-size_t chain_smem_bytes(int R, int Bg);
+size_t chain_smem_bytes(int R, int K, int Bg);
 cudaError_t launch_head_out(const float* part, int S, int rows, int D, const float* b, float* hs,
                             bf16* const* hp, float* tap, cudaStream_t s);
 cudaError_t launch_split(const float* src, size_t n, bf16* const* pl, float* copy, cudaStream_t s);

@@ -63,7 +63,7 @@ typedef struct {
     int L_D;          /* backbone layers, 1..DLITE_MAX_LAYERS */
     int n_q, n_kv, d_h; /* attention heads; n_q % n_kv == 0; d_h in {64, 128} */
     int F;            /* SwiGLU inner width; multiple of 64 */
-    int R;            /* sequential-head rank; multiple of 32, <= 1024 */
+    int R;            /* sequential-head rank; multiple of 32, <= 512 */
     int V;            /* vocabulary (tied embedding / LM head); multiple of 8, <= 262144 */
     int dtype;        /* DLITE_F32 or DLITE_BF16: type of all weights and of `hidden` */
     float rms_eps;    /* RMSNorm epsilon (1e-6) */
