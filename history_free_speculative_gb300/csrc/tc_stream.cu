@@ -24,7 +24,7 @@
 namespace dlite {
 namespace tc {
 
-constexpr uint32_t kStreamStaging = 4 * kEpiGroups * 32 * 32 * 4;  // epilogue transpose buffers
+constexpr uint32_t kStreamOverhang = 128u * 128u;  // the 128-row MMA operand read from the last stage
 
 struct StreamSeg {
   int slab, kb_lo, n, plane;
@@ -190,7 +190,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ncol = N / kEpiGroups;
     const int c_lo = eg * ncol;
     const int row0 = q * 32;  // this warp's 32 rows
-    float* stg = reinterpret_cast<float*>(smem + (size_t)p.stages * p.stage_bytes) + (warp - 2) * 1024;
+    const int row = row0 + lane;
+    const bool live = row < p.rows;
     pdl_wait();  // the partial buffer may still be read by the previous kernel
     long long u = u_begin;
     StreamSeg sg;
@@ -202,27 +203,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (row0 < p.rows) {  // a warp whose rows are all past the end only keeps the protocol
         const int o0 = sg.slab * N;
         const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * N);
-        float* out = p.part + (size_t)sg.plane * p.rows * p.outs;
+        // lane = row: each live lane stores its row's 32 columns per chunk as
+        // eight 16-byte stores straight from the TMEM registers (few rows: a
+        // handful of instructions per warp instead of a shared-memory transpose)
+        float* orow = p.part + ((size_t)sg.plane * p.rows + (live ? row : 0)) * p.outs + o0;
         for (int c = c_lo; c < c_lo + ncol; c += 32) {
-          // 32 rows x 32 columns through shared memory (element (i, j) at
-          // i * 32 + (j ^ i): conflict-free both ways), then rows of 32 floats
           uint32_t v0[16], v1[16];
           tmem_ld16_nowait(tbase + c, v0);
           tmem_ld16_nowait(tbase + c + 16, v1);
           tmem_wait_ld();
+          auto v = [&](int k) { return __uint_as_float(k < 16 ? v0[k] : v1[k - 16]); };
+          if (live) {
+            if (o0 + c + 32 <= p.outs) {
+              float4* dst = reinterpret_cast<float4*>(orow + c);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            stg[lane * 32 + (j ^ lane)] = __uint_as_float(v0[j]);
-            stg[lane * 32 + ((j + 16) ^ lane)] = __uint_as_float(v1[j]);
+              for (int k = 0; k < 8; ++k)
+                dst[k] = make_float4(v(4 * k), v(4 * k + 1), v(4 * k + 2), v(4 * k + 3));
+            } else {
+#pragma unroll
+              for (int k = 0; k < 32; ++k)
+                if (o0 + c + k < p.outs) orow[c + k] = v(k);
+            }
           }
-          __syncwarp();
-          const int col = o0 + c + lane;
-          const int nr = p.rows - row0 < 32 ? p.rows - row0 : 32;
-          for (int j = 0; j < nr; ++j) {
-            const float v = stg[j * 32 + (lane ^ j)];
-            if (col < p.outs) out[(size_t)(row0 + j) * p.outs + col] = v;
-          }
-          __syncwarp();
         }
       }
       fence_before();
@@ -270,9 +272,9 @@ StreamPlan stream_plan(int rows, int outs, int K, int num_sms) {
   pl.stage_bytes = (uint32_t)pl.N * 128u + a_slot_bytes(pl.x_box);
   // the 128-row MMA operand of the x_box-row activation tile overhangs into the
   // weight tile behind it (stale bytes feeding unused TMEM lanes); behind the
-  // last stage the 32 KB epilogue staging area takes the overhang
-  pl.tail_pad = 0;
-  int stages = (int)((kSmemBudget - 2048 - kStreamStaging - pl.tail_pad) / pl.stage_bytes);
+  // last stage a pad takes the overhang
+  pl.tail_pad = kStreamOverhang;
+  int stages = (int)((kSmemBudget - 2048 - pl.tail_pad) / pl.stage_bytes);
   if (stages > 8) stages = 8;
   if (stages < 2) return pl;
   pl.stages = stages;
@@ -289,8 +291,7 @@ StreamPlan stream_plan(int rows, int outs, int K, int num_sms) {
 }
 
 size_t stream_smem_bytes(const StreamPlan& pl) {
-  return 1024 /* align */ + 1024 /* barriers */ + (size_t)pl.stages * pl.stage_bytes + pl.tail_pad +
-         kStreamStaging;
+  return 1024 /* align */ + 1024 /* barriers */ + (size_t)pl.stages * pl.stage_bytes + pl.tail_pad;
 }
 
 cudaError_t launch_stream(const StreamPlan& pl, const CUtensorMap* x, const CUtensorMap* w, StreamParams prm,
