@@ -182,11 +182,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           float* stg = reinterpret_cast<float*>(smem) + (warp - 2) * 1024;
           float* out = p.part + (size_t)split * p.rows * p.outs;
           const int row0 = m0 + mt * 128 + q * 32;
+          const bool few = p.rows - row0 < 32;  // a partly filled quadrant: lane = row, direct stores
           for (int c = c_lo; c < c_hi; c += 32) {
             uint32_t v0[16], v1[16];
             tmem_ld16_nowait(tbase + c, v0);
             tmem_ld16_nowait(tbase + c + 16, v1);
             tmem_wait_ld();
+            if (few) {
+              if (r < p.rows) {
+                float* orow = out + (size_t)r * p.outs + o0 + c;
+                auto v = [&](int k) { return __uint_as_float(k < 16 ? v0[k] : v1[k - 16]); };
+                if (o0 + c + 32 <= p.outs) {
+#pragma unroll
+                  for (int k = 0; k < 8; ++k)
+                    reinterpret_cast<float4*>(orow)[k] =
+                        make_float4(v(4 * k), v(4 * k + 1), v(4 * k + 2), v(4 * k + 3));
+                } else {
+#pragma unroll
+                  for (int k = 0; k < 32; ++k)
+                    if (o0 + c + k < p.outs) orow[k] = v(k);
+                }
+              }
+              continue;
+            }
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               stg[lane * 32 + (j ^ lane)] = __uint_as_float(v0[j]);
@@ -215,6 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float* stg = reinterpret_cast<float*>(smem) + (warp - 2) * 1024;
           const int row0 = m0 + mt * 128 + q * 32;
           const int F = p.outs / 2;
+          const bool few = p.rows - row0 < 32;  // a partly filled quadrant: lane = row, direct stores
           for (int blk = eg; blk < p.N / 64; blk += kEpiGroups) {
             uint32_t g0[16], g1[16], u0[16], u1[16];
             tmem_ld16_nowait(tbase + blk * 64, g0);
@@ -222,6 +241,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld16_nowait(tbase + blk * 64 + 32, u0);
             tmem_ld16_nowait(tbase + blk * 64 + 48, u1);
             tmem_wait_ld();
+            if (few) {
+              const int f0 = (o0 / 64 + blk) * 32;  // the block's first feature (F is a multiple of 32)
+              if (r < p.rows && f0 < F) {
+                const size_t idx = (size_t)r * F + f0;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {  // 8 features per 16-byte store
+                  uint32_t hw[4], lw[4];
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    float a2[2];
+#pragma unroll
+                    for (int t2 = 0; t2 < 2; ++t2) {
+                      const int j = 8 * k + 2 * e + t2;
+                      const float g = __uint_as_float(j < 16 ? g0[j] : g1[j - 16]);
+                      const float u = __uint_as_float(j < 16 ? u0[j] : u1[j - 16]);
+                      a2[t2] = g / (1.f + expf(-g)) * u;
+                    }
+                    bf16 h0, l0, h1, l1;
+                    if (p.act_planes == 2) {
+                      split_bf16(a2[0], h0, l0);
+                      split_bf16(a2[1], h1, l1);
+                    } else {
+                      h0 = __float2bfloat16_rn(a2[0]);
+                      h1 = __float2bfloat16_rn(a2[1]);
+                      l0 = l1 = h0;
+                    }
+                    hw[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+                    lw[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+                  }
+                  reinterpret_cast<uint4*>(p.act[0] + idx)[k] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                  if (p.act_planes == 2)
+                    reinterpret_cast<uint4*>(p.act[1] + idx)[k] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                }
+              }
+              continue;
+            }
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const float ga = __uint_as_float(g0[j]), gb = __uint_as_float(g1[j]);
