@@ -27,6 +27,29 @@ __device__ __forceinline__ void store_planes(bf16* const* pl, int n, size_t i, f
 constexpr int kRowThreads = 1024;
 constexpr int kRowVec = 4;  // float4 chunks per thread at most
 
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t rank) {
+  uint32_t remote;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(remote)
+               : "r"((uint32_t)__cvta_generic_to_shared(local)), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ float4 f4add(float4 a, float4 b) {
   return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
 }
@@ -278,20 +301,26 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s) {
 // ---------------------------------------------------------------- residual + RMSNorm
 // x[r] += sum_s part[s][r]; then either y = RMSNorm(x) * g (next product's
 // input) or, after the last layer, b = RMSNorm(x) * g_final for the
-// placeholder rows (the anchor row is dropped). One CTA of 1024 threads per
-// row, float4 per thread (D <= 16384), every split's load issued before use.
+// placeholder rows (the anchor row is dropped). A row is served by a cluster
+// of C CTAs (C = 8 when there are few rows, else 1), CTA c taking columns
+// [c D / C, (c + 1) D / C) with up to kRowVec float4 per thread and every
+// split's load issued before use; the C partial sums of squares are
+// exchanged through distributed shared memory and added in rank order, so
+// every CTA of the row applies the same scale.
 __global__ void __launch_bounds__(kRowThreads) resnorm_kernel(ResNormArgs a) {
   pdl_trigger();
   pdl_wait();
   __shared__ float red[32];
-  const int r = blockIdx.x, D = a.D, n4 = D / 4;
+  const uint32_t C = cluster_nctarank(), c = cluster_ctarank();
+  const int r = blockIdx.x / (int)C, D = a.D;
+  const int n4 = D / 4 / (int)C, i0 = n4 * (int)c;  // this CTA's float4 range [i0, i0 + n4)
   const size_t stride = (size_t)a.rows * D;
   float4 v[kRowVec];
   float ss = 0.f;
 #pragma unroll
   for (int k = 0; k < kRowVec; ++k) {
-    const int i = threadIdx.x + k * kRowThreads;
-    if (i < n4) {
+    const int i = i0 + threadIdx.x + k * blockDim.x;
+    if (i < i0 + n4) {
       float4 x = *reinterpret_cast<const float4*>(a.x + (size_t)r * D + 4 * i);
       x = f4add(x, sum_splits4(a.part + (size_t)r * D + 4 * i, stride, splits_at(a.sp, r, 4 * i)));
       *reinterpret_cast<float4*>(a.x + (size_t)r * D + 4 * i) = x;
@@ -300,7 +329,14 @@ __global__ void __launch_bounds__(kRowThreads) resnorm_kernel(ResNormArgs a) {
       ss += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
     }
   }
-  ss = block_sum(ss, red);
+  ss = block_sum(ss, red);  // red[0] = this CTA's partial
+  if (C > 1) {
+    cluster_sync_all();  // every CTA's partial is in its red[0]
+    float t = 0.f;
+    for (uint32_t q = 0; q < C; ++q) t += ld_cluster_f32(red, q);
+    ss = t;
+    cluster_sync_all();  // no CTA leaves while another reads its shared memory
+  }
   const float inv = rsqrtf(ss / D + a.eps);
   if (a.final_mode) {
     const int b = r / a.K1, i = r % a.K1;
@@ -308,8 +344,8 @@ __global__ void __launch_bounds__(kRowThreads) resnorm_kernel(ResNormArgs a) {
     const size_t orow = (size_t)(b * (a.K1 - 1) + (i - 1)) * D;
 #pragma unroll
     for (int k = 0; k < kRowVec; ++k) {
-      const int j = threadIdx.x + k * kRowThreads;
-      if (j < n4) {
+      const int j = i0 + threadIdx.x + k * blockDim.x;
+      if (j < i0 + n4) {
         const float4 g = *reinterpret_cast<const float4*>(a.g + 4 * j);
         const float4 o = make_float4(v[k].x * inv * g.x, v[k].y * inv * g.y, v[k].z * inv * g.z,
                                      v[k].w * inv * g.w);
@@ -321,8 +357,8 @@ __global__ void __launch_bounds__(kRowThreads) resnorm_kernel(ResNormArgs a) {
   } else {
 #pragma unroll
     for (int k = 0; k < kRowVec; ++k) {
-      const int j = threadIdx.x + k * kRowThreads;
-      if (j < n4) {
+      const int j = i0 + threadIdx.x + k * blockDim.x;
+      if (j < i0 + n4) {
         const float4 g = *reinterpret_cast<const float4*>(a.g + 4 * j);
         store4_planes(a.y, a.ny, (size_t)r * D + 4 * j,
                       make_float4(v[k].x * inv * g.x, v[k].y * inv * g.y, v[k].z * inv * g.z,
@@ -332,8 +368,28 @@ __global__ void __launch_bounds__(kRowThreads) resnorm_kernel(ResNormArgs a) {
   }
 }
 
+constexpr int kResNormCluster = 8;
+
 cudaError_t launch_resnorm(const ResNormArgs& a, cudaStream_t s) {
-  return launch_pdl(resnorm_kernel, dim3(a.rows), dim3(kRowThreads), 0, s, a);
+  // few rows: a cluster per row, so that more SMs pull the split partials
+  const int C = (a.rows * kResNormCluster <= 4 * 152 && (a.D / 4) % kResNormCluster == 0) ? kResNormCluster : 1;
+  const int n4 = a.D / 4 / C;
+  int threads = (n4 + 31) / 32 * 32;
+  if (threads > kRowThreads) threads = kRowThreads;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.rows * C, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[0].val.programmaticStreamSerializationAllowed = 1;
+  attrs[1].id = cudaLaunchAttributeClusterDimension;
+  attrs[1].val.clusterDim.x = C;
+  attrs[1].val.clusterDim.y = 1;
+  attrs[1].val.clusterDim.z = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, resnorm_kernel, a);
 }
 
 // ---------------------------------------------------------------- SwiGLU epilogue
@@ -385,14 +441,6 @@ constexpr int kChainCluster = 8;
 constexpr int kChainMaxJ = 16;        // R <= 512
 constexpr int kChainMaxClusters = 16;  // clusters per launch (128 CTAs)
 
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
 __device__ __forceinline__ void st_cluster_f32(uint32_t local_addr, uint32_t rank, float v) {
   uint32_t remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));

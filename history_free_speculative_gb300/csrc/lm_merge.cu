@@ -59,36 +59,87 @@ __device__ __forceinline__ void topk_insert(float (&sc)[kTopK], int (&id)[kTopK]
   for (int k = kTopK - 2; k >= 0; --k) cswap(sc, id, k);
 }
 
-__device__ __forceinline__ float exact_logit(const LmMergeArgs& a, int v, const float* h) {
+// Partial exact logit of id v over columns [lo, hi) (fp32 accumulation; the
+// warp's lanes take 4 columns each per 128, all loads issued before use).
+__device__ __forceinline__ float exact_logit_part(const LmMergeArgs& a, int v, const float* h, int lo, int hi) {
   const int lane = threadIdx.x & 31;
-  float acc = 0.f;
-  if (a.Ef) {
-    const float* e = a.Ef + (size_t)v * a.D;
-    for (int d = lane * 4; d < a.D; d += 128) {
-      const float4 ev = *reinterpret_cast<const float4*>(e + d);
-      const float4 hv = *reinterpret_cast<const float4*>(h + d);
-      acc = fmaf(ev.x, hv.x, fmaf(ev.y, hv.y, fmaf(ev.z, hv.z, fmaf(ev.w, hv.w, acc))));
+  float acc0 = 0.f, acc1 = 0.f;
+  constexpr int kU = 16;
+  for (int d0 = lo + lane * 4; d0 < hi; d0 += 128 * kU) {
+    float4 ev[kU], hv[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int d = d0 + 128 * u;
+      if (d < hi) {
+        hv[u] = *reinterpret_cast<const float4*>(h + d);
+        if (a.Ef) {
+          ev[u] = *reinterpret_cast<const float4*>(a.Ef + (size_t)v * a.D + d);
+        } else {
+          const uint2 raw = *reinterpret_cast<const uint2*>(a.Eb + tiled_index(v, d, a.D));
+          const __nv_bfloat162 e01 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+          const __nv_bfloat162 e23 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+          ev[u] = make_float4(__low2float(e01), __high2float(e01), __low2float(e23), __high2float(e23));
+        }
+      } else {
+        hv[u] = ev[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
-  } else {
-#pragma unroll 8
-    for (int d = lane * 4; d < a.D; d += 128) {
-      const uint2 raw = *reinterpret_cast<const uint2*>(a.Eb + tiled_index(v, d, a.D));
-      const __nv_bfloat162 e01 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-      const __nv_bfloat162 e23 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
-      const float4 hv = *reinterpret_cast<const float4*>(h + d);
-      acc = fmaf(__low2float(e01), hv.x, acc);
-      acc = fmaf(__high2float(e01), hv.y, acc);
-      acc = fmaf(__low2float(e23), hv.z, acc);
-      acc = fmaf(__high2float(e23), hv.w, acc);
+#pragma unroll
+    for (int u = 0; u < kU; u += 2) {
+      acc0 = fmaf(ev[u].x, hv[u].x, fmaf(ev[u].y, hv[u].y, fmaf(ev[u].z, hv[u].z, fmaf(ev[u].w, hv[u].w, acc0))));
+      acc1 = fmaf(ev[u + 1].x, hv[u + 1].x,
+                  fmaf(ev[u + 1].y, hv[u + 1].y, fmaf(ev[u + 1].z, hv[u + 1].z, fmaf(ev[u + 1].w, hv[u + 1].w, acc1))));
     }
   }
-  return warp_sum(acc);
+  return warp_sum(acc0 + acc1);
 }
 
-// One CTA of kMergeWarps warps per row: every thread folds a strided subset of the records
-// into a register top-k + LSE, the warps combine by butterfly, thread 0
-// combines the warps in a fixed order, and warps 0-3 re-score the 4 finalists
-// exactly in parallel.
+// The 4 best (score, id) over the lanes' descending lists by a tournament:
+// four warp-wide arg-max reductions, the owner of each winner popping it.
+// Every lane returns the same list; the lanes' lists are consumed.
+__device__ __forceinline__ void warp_top4(float (&sc)[kTopK], int (&id)[kTopK], float (&osc)[kTopK],
+                                          int (&oid)[kTopK]) {
+#pragma unroll
+  for (int k = 0; k < kTopK; ++k) {
+    float bv = sc[0];
+    int bi = id[0];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (better(v2, i2, bv, bi)) {
+        bv = v2;
+        bi = i2;
+      }
+    }
+    osc[k] = bv;
+    oid[k] = bi;
+    if (id[0] == bi && sc[0] == bv) {  // ids are unique, except the empty entries
+#pragma unroll
+      for (int j = 0; j + 1 < kTopK; ++j) {
+        sc[j] = sc[j + 1];
+        id[j] = id[j + 1];
+      }
+      sc[kTopK - 1] = -INFINITY;
+      id[kTopK - 1] = 0x7fffffff;
+    }
+  }
+}
+
+__device__ __forceinline__ void warp_lse(float& m, float& s) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {  // both partners form the same two terms
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    lse_merge(m, s, m2, s2);
+  }
+}
+
+// One CTA of kMergeWarps warps per row: each thread takes the records
+// t = tid, tid + blockDim, ... (normally one: its record's list is already
+// sorted), each warp reduces its lanes' lists by tournament, warp 0 reduces
+// the warps' lists the same way, and the warps re-score the 4 finalists
+// exactly, two warps (half of the columns each) per finalist.
 
 // Gumbel noise -log(-log u) of the uniform u01f(x) with full relative accuracy
 // where it matters: for u within 2^-8 of 1, -log u is formed from the exact
@@ -103,14 +154,14 @@ __device__ __forceinline__ float gumbel_f(uint32_t x) {
 
 template <int kMergeWarps>
 __global__ void __launch_bounds__(kMergeWarps * 32) lm_merge_kernel(const LmMergeArgs a) {
-  static_assert(kMergeWarps >= kTopK, "one warp per finalist");
-  pdl_trigger();
+  static_assert(kMergeWarps == 2 * kTopK, "two warps per finalist");
+  // no early trigger: the verification kernel that follows would wait on
+  // these SMs (its CTAs slowed this kernel by about 2x when launched early)
   pdl_wait();
   __shared__ float wsc[kMergeWarps][kTopK];
   __shared__ int wid[kMergeWarps][kTopK];
   __shared__ float wm[kMergeWarps], wsum[kMergeWarps];
-  __shared__ double fin_sc[kTopK];
-  __shared__ float fin_logit[kTopK];
+  __shared__ float part[kMergeWarps];
   __shared__ int fin_id[kTopK];
   __shared__ float row_m, row_s, row_sc0, row_sc3;
   const int r = blockIdx.x;
@@ -124,109 +175,111 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lm_merge_kernel(const LmMerg
     id[k] = 0x7fffffff;
   }
   float m = -INFINITY, s = 0.f;
-  constexpr int kBatch = 4;  // records loaded before any is folded
-  for (int t0 = threadIdx.x; t0 < a.n_tiles; t0 += blockDim.x * kBatch) {
-    LmRec rec[kBatch];
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int t = t0 + u * blockDim.x;
-      if (t < a.n_tiles) rec[u] = a.rec[(size_t)t * a.rows + r];
-    }
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      if (t0 + u * (int)blockDim.x >= a.n_tiles) break;
-#pragma unroll
-      for (int k = 0; k < kTopK; ++k) topk_insert(sc, id, rec[u].sc[k], rec[u].id[k]);
-      if (sampling) lse_merge(m, s, rec[u].m, rec[u].s);
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {  // both partners end with the same list (disjoint sets)
-    float sc2[kTopK];
-    int id2[kTopK];
+  if ((int)threadIdx.x < a.n_tiles) {  // the first record is this lane's list as it stands
+    const LmRec rec = a.rec[(size_t)threadIdx.x * a.rows + r];
 #pragma unroll
     for (int k = 0; k < kTopK; ++k) {
-      sc2[k] = __shfl_xor_sync(0xffffffffu, sc[k], o);
-      id2[k] = __shfl_xor_sync(0xffffffffu, id[k], o);
+      sc[k] = rec.sc[k];
+      id[k] = rec.id[k];
     }
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-#pragma unroll
-    for (int k = 0; k < kTopK; ++k) topk_insert(sc, id, sc2[k], id2[k]);
-    if (sampling) lse_merge(m, s, m2, s2);
+    m = rec.m;
+    s = rec.s;
   }
+  for (int t = threadIdx.x + blockDim.x; t < a.n_tiles; t += blockDim.x) {
+    const LmRec rec = a.rec[(size_t)t * a.rows + r];
+#pragma unroll
+    for (int k = 0; k < kTopK; ++k) topk_insert(sc, id, rec.sc[k], rec.id[k]);
+    if (sampling) lse_merge(m, s, rec.m, rec.s);
+  }
+  float osc[kTopK];
+  int oid[kTopK];
+  warp_top4(sc, id, osc, oid);
+  if (sampling) warp_lse(m, s);
   if (lane == 0) {
 #pragma unroll
     for (int k = 0; k < kTopK; ++k) {
-      wsc[warp][k] = sc[k];
-      wid[warp][k] = id[k];
+      wsc[warp][k] = osc[k];
+      wid[warp][k] = oid[k];
     }
     wm[warp] = m;
     wsum[warp] = s;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int w = 1; w < kMergeWarps; ++w) {
+  if (warp == 0) {  // the same reduction over the warps' lists, lane w holding warp w's
 #pragma unroll
-      for (int k = 0; k < kTopK; ++k) topk_insert(sc, id, wsc[w][k], wid[w][k]);
-      if (sampling) lse_merge(m, s, wm[w], wsum[w]);
+    for (int k = 0; k < kTopK; ++k) {
+      sc[k] = lane < kMergeWarps ? wsc[lane][k] : -INFINITY;
+      id[k] = lane < kMergeWarps ? wid[lane][k] : 0x7fffffff;
     }
+    m = lane < kMergeWarps ? wm[lane] : -INFINITY;
+    s = lane < kMergeWarps ? wsum[lane] : 0.f;
+    warp_top4(sc, id, osc, oid);
+    if (sampling) warp_lse(m, s);
+    if (lane == 0) {
 #pragma unroll
-    for (int k = 0; k < kTopK; ++k) fin_id[k] = id[k];
-    row_m = m;
-    row_s = s;
-    row_sc0 = sc[0];
-    row_sc3 = sc[kTopK - 1];
+      for (int k = 0; k < kTopK; ++k) fin_id[k] = oid[k];
+      row_m = m;
+      row_s = s;
+      row_sc0 = osc[0];
+      row_sc3 = osc[kTopK - 1];
+    }
   }
   __syncthreads();
-  // exact re-scoring: warp k < kTopK takes finalist k
+  // exact re-scoring: warps 2k and 2k + 1 take the two halves of finalist k
   const float* h = a.h + (size_t)r * a.D;
-  if (warp < kTopK) {
-    const int v = fin_id[warp];
+  {
+    const int v = fin_id[warp >> 1];
+    const int half = (a.D / 2 + 3) & ~3;
+    const int lo = (warp & 1) ? half : 0, hi = (warp & 1) ? a.D : half;
+    float p = 0.f;
+    if (v >= 0 && v < a.V) p = exact_logit_part(a, v, h, lo, hi);  // fewer than kTopK ids on tiny vocabularies
+    if (lane == 0) part[warp] = p;
+  }
+  __syncthreads();
+  if (warp == 0) {  // lane k scores finalist k; the best by a 4-lane reduction (ties -> lowest id)
     double x = -INFINITY;
     float l = 0.f;
-    if (v >= 0 && v < a.V) {  // fewer than kTopK ids on tiny vocabularies
-      l = exact_logit(a, v, h);
-      x = l;
-      if (sampling) {
-        const uint32_t req = (uint32_t)(r / a.K);
-        const uint32_t pos = (uint32_t)(a.pos[req] + (r % a.K) + 1);
-        const uint4 w = philox((uint32_t)v >> 2, pos, req, kTagGumbel, a.k0, a.k1);
-        const uint32_t wx[4] = {w.x, w.y, w.z, w.w};
-        x = (double)l / a.T + (double)gumbel_f(wx[v & 3]);
+    int v = 0x7fffffff;
+    if (lane < kTopK) {
+      const int fv = fin_id[lane];
+      if (fv >= 0 && fv < a.V) {
+        v = fv;
+        l = part[2 * lane] + part[2 * lane + 1];
+        x = l;
+        if (sampling) {
+          const uint32_t req = (uint32_t)(r / a.K);
+          const uint32_t pos = (uint32_t)(a.pos[req] + (r % a.K) + 1);
+          const uint4 w = philox((uint32_t)v >> 2, pos, req, kTagGumbel, a.k0, a.k1);
+          const uint32_t wx[4] = {w.x, w.y, w.z, w.w};
+          x = (double)l / a.T + (double)gumbel_f(wx[v & 3]);
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 1; o < kTopK; o <<= 1) {
+      const double x2 = __shfl_xor_sync(0xffffffffu, x, o);
+      const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
+      const int v2 = __shfl_xor_sync(0xffffffffu, v, o);
+      if (x2 > x || (x2 == x && v2 < v)) {
+        x = x2;
+        l = l2;
+        v = v2;
       }
     }
     if (lane == 0) {
-      fin_sc[warp] = x;
-      fin_logit[warp] = l;
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    double best = -INFINITY;
-    float blogit = 0.f;
-    int bid = 0x7fffffff;
-    for (int k = 0; k < kTopK; ++k) {
-      const int v = fin_id[k];
-      if (v < 0 || v >= a.V) continue;
-      if (fin_sc[k] > best || (fin_sc[k] == best && v < bid)) {
-        best = fin_sc[k];
-        bid = v;
-        blogit = fin_logit[k];
+      a.cand[r] = v;
+      if (a.qs) {
+        a.qs[r].logit = l;
+        a.qs[r].lse = sampling ? (row_m + log2f(row_s)) * kLn2M : NAN;
       }
+      const float band = sampling ? kCloseCall * kLog2eM : kCloseCall;
+      if (a.counters && row_sc3 > row_sc0 - band) atomicAdd(a.counters + 4, 1ull);
     }
-    a.cand[r] = bid;
-    if (a.qs) {
-      a.qs[r].logit = blogit;
-      a.qs[r].lse = sampling ? (row_m + log2f(row_s)) * kLn2M : NAN;
-    }
-    const float band = sampling ? kCloseCall * kLog2eM : kCloseCall;
-    if (a.counters && row_sc3 > row_sc0 - band) atomicAdd(a.counters + 4, 1ull);
   }
 }
 
 cudaError_t launch_lm_merge(const LmMergeArgs& a, cudaStream_t s) {
-  return launch_pdl(lm_merge_kernel<4>, dim3(a.rows), dim3(4 * 32), 0, s, a);
+  return launch_pdl(lm_merge_kernel<2 * kTopK>, dim3(a.rows), dim3(2 * kTopK * 32), 0, s, a);
 }
 
 }  // namespace dlite
