@@ -311,10 +311,21 @@ tc::Plan lm_plan(dlite_handle* h, int rows) {
   return tc::plan(rows, h->cfg.V, h->cfg.D, 1, 1, true);
 }
 
+// Few rows: the context rows z are stored behind the local rows y in one
+// buffer and a single product [y; z] W_qkv^T serves both (the query columns of
+// the context rows are computed and ignored), one launch instead of two.
+static bool fuse_ctx(const dlite_handle* h, int B) {
+  const dlite_config& c = h->cfg;
+  const int rows = B * (c.K + 1) + B * c.m;
+  return h->np == 1 && tc::use_stream_engine(rows, 1, 1) &&
+         tc::stream_plan(rows, h->qd + 2 * h->kvd, c.D, h->num_sms).ok;
+}
+
 int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anchor,
                  const dlite_taps* taps, cudaStream_t s) {
   const dlite_config& c = h->cfg;
   const int L = B * (c.K + 1), C = B * c.m;
+  const bool fused_ctx = fuse_ctx(h, B);
   StageArgs st;
   st.hidden = hidden;
   st.anchor = anchor;
@@ -330,7 +341,7 @@ int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anch
   st.D = c.D;
   st.V = c.V;
   st.eps = c.rms_eps;
-  st.z[0] = h->z[0];
+  st.z[0] = fused_ctx ? h->y[0] + (size_t)L * c.D : h->z[0];
   st.z[1] = h->z[1];
   st.nz = h->np;
   st.x = h->x;
@@ -345,18 +356,30 @@ int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anch
   for (int l = 0; l < c.L_D; ++l) {
     const LayerW& w = h->layer[l];
     Splits S1, S2;
-    // local rows: y -> [q | k | v]; context rows: z -> [k | v] with the same bytes
-    RUN(gemm(h, "gemm_qkv", opnd(h->y, h->np, h->Lcap, c.D), opnd(w.Wqkv, h->np, h->qd + 2 * h->kvd, c.D),
-             L, h->qd + 2 * h->kvd, h->part, &S1, s));
-    const bf16* wkv[2] = {w.Wqkv[0] + (size_t)h->qd * c.D,
-                          w.Wqkv[1] ? w.Wqkv[1] + (size_t)h->qd * c.D : nullptr};
-    RUN(gemm(h, "gemm_ctx_kv", opnd(h->z, h->np, h->Ccap, c.D), opnd(wkv, h->np, 2 * h->kvd, c.D), C,
-             2 * h->kvd, h->part2, &S2, s));
     AttnArgs at;
+    if (fused_ctx) {
+      RUN(gemm(h, "gemm_qkv", opnd(h->y, h->np, h->Lcap + h->Ccap, c.D),
+               opnd(w.Wqkv, h->np, h->qd + 2 * h->kvd, c.D), L + C, h->qd + 2 * h->kvd, h->part, &S1, s));
+      at.part_ctx = h->part;
+      at.sp_ctx = S1;
+      at.ctx_row0 = L;
+      at.ctx_col0 = h->qd;
+      at.ldc = h->qd + 2 * h->kvd;
+      at.ctx_rows = L + C;
+      at.loc_rows = L + C;
+    } else {
+      // local rows: y -> [q | k | v]; context rows: z -> [k | v] with the same bytes
+      RUN(gemm(h, "gemm_qkv", opnd(h->y, h->np, h->Lcap, c.D), opnd(w.Wqkv, h->np, h->qd + 2 * h->kvd, c.D),
+               L, h->qd + 2 * h->kvd, h->part, &S1, s));
+      const bf16* wkv[2] = {w.Wqkv[0] + (size_t)h->qd * c.D,
+                            w.Wqkv[1] ? w.Wqkv[1] + (size_t)h->qd * c.D : nullptr};
+      RUN(gemm(h, "gemm_ctx_kv", opnd(h->z, h->np, h->Ccap, c.D), opnd(wkv, h->np, 2 * h->kvd, c.D), C,
+               2 * h->kvd, h->part2, &S2, s));
+      at.part_ctx = h->part2;
+      at.sp_ctx = S2;
+    }
     at.part_loc = h->part;
     at.sp_loc = S1;
-    at.part_ctx = h->part2;
-    at.sp_ctx = S2;
     at.rope_cos = h->rope_cos;
     at.rope_sin = h->rope_sin;
     at.B = B;
@@ -671,7 +694,7 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
   const size_t Lr = (size_t)h->Lcap, Cr = (size_t)h->Ccap, Hr = (size_t)h->Hcap;
   AL(h->x, Lr * D);
   for (int p = 0; p < h->np; ++p) {
-    AL(h->y[p], Lr * D);
+    AL(h->y[p], (Lr + Cr) * D);  // context rows behind the local rows when fused (fuse_ctx)
     AL(h->z[p], Cr * D);
     AL(h->o[p], Lr * h->qd);
     AL(h->a[p], Lr * F);
@@ -701,6 +724,10 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
       if (sq.ok && tc::use_stream_engine(st[0], st[3], h->np))
         pe = (size_t)sq.S * st[0] * st[1] > pe ? (size_t)sq.S * st[0] * st[1] : pe;
       if (pp.ok && tc::use_pair_engine(st[0], st[3], h->np)) pe = (size_t)pp.S * st[0] * st[1] > pe ? (size_t)pp.S * st[0] * st[1] : pe;  // planes
+    }
+    if (fuse_ctx(h, B)) {
+      const tc::StreamPlan sf = tc::stream_plan(L + C, h->qd + 2 * h->kvd, D, h->num_sms);
+      pe = (size_t)sf.S * (L + C) * (h->qd + 2 * h->kvd) > pe ? (size_t)sf.S * (L + C) * (h->qd + 2 * h->kvd) : pe;
     }
     const tc::Plan pc = tc::plan(C, 2 * h->kvd, D, h->np, h->np, false);
     if (!pc.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
@@ -1079,7 +1106,7 @@ int dlite_launch_count(dlite_handle* h, int B, float temperature) {
   // + lm {head, merge} + verify
   const int L = B * (h->cfg.K + 1);
   const bool fused = !tc::use_pair_engine(L, h->np, h->np);
-  const int per_layer = fused ? 8 : 9;
+  const int per_layer = (fused ? 8 : 9) - (fuse_ctx(h, B) ? 1 : 0);  // one product for [y; z] when fused
   return 1 + per_layer * h->cfg.L_D + 4 + 2 + 1;
 }
 

@@ -194,19 +194,21 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(AttnArgs a) {
   const int G = a.hq, g = (int)(blockIdx.x * G) / (a.n_q / a.n_kv), h0 = blockIdx.x * G, b = blockIdx.y;
   const int K1 = a.K + 1, dh = a.d_h, half = dh / 2;
   const int qd = a.n_q * dh, kvd = a.n_kv * dh;
-  const int ldl = qd + 2 * kvd;  // local partial row width
-  const int ldc = 2 * kvd;       // context partial row width
+  const int ldl = qd + 2 * kvd;               // local partial row width
+  const int ldc = a.ldc ? a.ldc : 2 * kvd;     // context partial row width
   const int Tk = a.m + K1;
   const int LD = dh + 4;
   float* qs = sm;               // [G * K1][LD]: query row i of head g G + hh at hh * K1 + i
   float* ks = qs + G * K1 * LD;  // [Tk][LD]
   float* vs = ks + Tk * LD;      // [Tk][LD]
-  const size_t sl = (size_t)a.B * K1 * ldl, sc = (size_t)a.B * a.m * ldc;
+  const size_t sl = (size_t)(a.loc_rows ? a.loc_rows : a.B * K1) * ldl;
+  const size_t sc = (size_t)(a.ctx_rows ? a.ctx_rows : a.B * a.m) * ldc;
   auto loc4 = [&](int row, int col) {
     return sum_splits4(a.part_loc + (size_t)(b * K1 + row) * ldl + col, sl, splits_at(a.sp_loc, b * K1 + row, col));
   };
   auto ctx4 = [&](int row, int col) {
-    return sum_splits4(a.part_ctx + (size_t)(b * a.m + row) * ldc + col, sc, splits_at(a.sp_ctx, b * a.m + row, col));
+    const int r = a.ctx_row0 + b * a.m + row, c = a.ctx_col0 + col;
+    return sum_splits4(a.part_ctx + (size_t)r * ldc + c, sc, splits_at(a.sp_ctx, r, c));
   };
   auto rnd4 = [&](float4 v) {
     return a.round_bf16 ? make_float4(round_bf16(v.x), round_bf16(v.y), round_bf16(v.z), round_bf16(v.w)) : v;

@@ -28,8 +28,10 @@ struct StageArgs {
 struct AttnArgs {
   const float* part_loc = nullptr;  // [splits][B*(K+1)][qd + 2 kvd]
   Splits sp_loc;
-  const float* part_ctx = nullptr;  // [splits][B*m][2 kvd]
+  const float* part_ctx = nullptr;  // [splits][ctx_rows][ldc]: row ctx_row0 + b m + j, columns ctx_col0 ..
   Splits sp_ctx;
+  int ctx_row0 = 0, ctx_col0 = 0, ldc = 0, ctx_rows = 0;  // ldc = 0: 2 kvd; ctx_rows = 0: B m
+  int loc_rows = 0;  // rows of a local partial plane (0: B (K+1))
   const float* rope_cos = nullptr;  // [K+1][d_h/2]
   const float* rope_sin = nullptr;
   int B = 0, m = 0, K = 0, n_q = 0, n_kv = 0, d_h = 0;
