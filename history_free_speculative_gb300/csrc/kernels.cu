@@ -756,8 +756,30 @@ __device__ __forceinline__ unsigned long long scaled_threshold(unsigned long lon
 
 // Loader of 4 consecutive fixed-point weights starting at v (v % 4 == 0).
 struct RowF32 {
+  static constexpr int kInFlight = 4;
   const float* row;
   int V;
+  struct Raw {
+    float4 f;
+  };
+  __device__ __forceinline__ Raw load(int v) const {
+    Raw r;
+    if (v + 3 < V) {
+      r.f = *reinterpret_cast<const float4*>(row + v);
+    } else {
+      r.f.x = v < V ? row[v] : 0.f;
+      r.f.y = v + 1 < V ? row[v + 1] : 0.f;
+      r.f.z = v + 2 < V ? row[v + 2] : 0.f;
+      r.f.w = v + 3 < V ? row[v + 3] : 0.f;
+    }
+    return r;
+  }
+  __device__ __forceinline__ void fix(int v, const Raw& r, unsigned long long (&w)[4]) const {
+    w[0] = v < V ? fix62(r.f.x) : 0ull;
+    w[1] = v + 1 < V ? fix62(r.f.y) : 0ull;
+    w[2] = v + 2 < V ? fix62(r.f.z) : 0ull;
+    w[3] = v + 3 < V ? fix62(r.f.w) : 0ull;
+  }
   __device__ __forceinline__ void get4(int v, unsigned long long (&w)[4]) const {
     if (v + 3 < V) {
       const float4 f = *reinterpret_cast<const float4*>(row + v);
@@ -769,8 +791,22 @@ struct RowF32 {
   }
 };
 struct RowFix {
+  static constexpr int kInFlight = 2;
   const unsigned long long* row;
   int V;
+  struct Raw {
+    unsigned long long w[4];
+  };
+  __device__ __forceinline__ Raw load(int v) const {
+    Raw r;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) r.w[j] = (v + j < V) ? row[v + j] : 0ull;
+    return r;
+  }
+  __device__ __forceinline__ void fix(int, const Raw& r, unsigned long long (&w)[4]) const {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) w[j] = r.w[j];
+  }
   __device__ __forceinline__ void get4(int v, unsigned long long (&w)[4]) const {
 #pragma unroll
     for (int j = 0; j < 4; ++j) w[j] = (v + j < V) ? row[v + j] : 0ull;
@@ -804,6 +840,43 @@ __device__ __forceinline__ float row_dot(const VerifyArgs& a, int v, const float
       acc = fmaf(__high2float(e01), hv.y, acc);
       acc = fmaf(__low2float(e23), hv.z, acc);
       acc = fmaf(__high2float(e23), hv.w, acc);
+    }
+  }
+  return warp_sum(acc);
+}
+
+// The part of E[v] . h over columns [lo, hi) (lo % 4 == 0): one warp, 4
+// columns per lane per 128, up to 4 raw loads per lane in flight (few
+// registers: the verification kernel runs two CTAs per SM).
+__device__ __forceinline__ float row_dot_part(const VerifyArgs& a, int v, const float* h, int lo, int hi) {
+  const int lane = threadIdx.x & 31;
+  float acc = 0.f;
+  constexpr int kU = 4;
+  for (int d0 = lo + lane * 4; d0 < hi; d0 += 128 * kU) {
+    uint2 eb[kU];
+    float4 ef[kU], hv[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int d = d0 + 128 * u;
+      if (d < hi) {
+        hv[u] = *reinterpret_cast<const float4*>(h + d);
+        if (a.Ef) ef[u] = *reinterpret_cast<const float4*>(a.Ef + (size_t)v * a.D + d);
+        else eb[u] = *reinterpret_cast<const uint2*>(a.Eb + tiled_index(v, d, a.D));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      if (d0 + 128 * u < hi) {
+        float4 e;
+        if (a.Ef) {
+          e = ef[u];
+        } else {
+          const __nv_bfloat162 e01 = *reinterpret_cast<const __nv_bfloat162*>(&eb[u].x);
+          const __nv_bfloat162 e23 = *reinterpret_cast<const __nv_bfloat162*>(&eb[u].y);
+          e = make_float4(__low2float(e01), __high2float(e01), __low2float(e23), __high2float(e23));
+        }
+        acc = fmaf(e.x, hv[u].x, fmaf(e.y, hv[u].y, fmaf(e.z, hv[u].z, fmaf(e.w, hv[u].w, acc))));
+      }
     }
   }
   return warp_sum(acc);
@@ -848,19 +921,23 @@ __device__ unsigned long long cluster_icdf(const Row& row, int V, const uint32_t
   const int nseg = (V + kSeg - 1) / kSeg;
   const int s0 = (int)rank * nseg / kVerifyCluster, s1 = ((int)rank + 1) * nseg / kVerifyCluster;
   const int ns = s1 - s0;
-  // 1) segment sums of this CTA's range: one warp per segment, four segments' loads in flight
-  for (int i0 = warp; i0 < ns; i0 += 4 * nw) {
-    unsigned long long w[4][4];
+  // 1) segment sums of this CTA's range: one warp per segment, the raw loads
+  //    of several segments in flight before any is converted
+  constexpr int kInFlight = Row::kInFlight;
+  for (int i0 = warp; i0 < ns; i0 += kInFlight * nw) {
+    typename Row::Raw raw[kInFlight];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kInFlight; ++u) {
       const int i = i0 + u * nw;
-      if (i < ns) row.get4((s0 + i) * kSeg + lane * 4, w[u]);
+      if (i < ns) raw[u] = row.load((s0 + i) * kSeg + lane * 4);
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kInFlight; ++u) {
       const int i = i0 + u * nw;
       if (i < ns) {
-        const unsigned long long t = warp_sum_u64(w[u][0] + w[u][1] + w[u][2] + w[u][3]);
+        unsigned long long w[4];
+        row.fix((s0 + i) * kSeg + lane * 4, raw[u], w);
+        const unsigned long long t = warp_sum_u64(w[0] + w[1] + w[2] + w[3]);
         if (lane == 0) incl[i] = t;
       }
     }
@@ -932,7 +1009,7 @@ __device__ unsigned long long cluster_icdf(const Row& row, int V, const uint32_t
 }
 
 // A cluster of kVerifyCluster CTAs per request.
-__global__ void __launch_bounds__(kVerifyCThreads) verify_sample_kernel(VerifyArgs a) {
+__global__ void __launch_bounds__(kVerifyCThreads, 2) verify_sample_kernel(VerifyArgs a) {
   pdl_trigger();
   pdl_wait();
   __shared__ unsigned long long incl[kSegsPerCta];
@@ -942,6 +1019,7 @@ __global__ void __launch_bounds__(kVerifyCThreads) verify_sample_kernel(VerifyAr
   __shared__ double qv[kProposals];        // q(v_j) of the proposals (rank 0)
   __shared__ int sv[kProposals];           // proposal ids (rank 0)
   __shared__ int sA, stok;
+  __shared__ float qpart[kVerifyCThreads / 32];
   const uint32_t rank = cluster_ctarank();
   const int b = blockIdx.x / kVerifyCluster, K = a.K, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nwarps = blockDim.x >> 5;
@@ -989,13 +1067,27 @@ __global__ void __launch_bounds__(kVerifyCThreads) verify_sample_kernel(VerifyAr
     }
     __syncthreads();
     cluster_icdf(prow_fix, a.V, xs, kProposals, sv, incl, tot, rank);
-    // q(v_j) of the proposals, spread over the cluster (one warp per proposal)
+    // q(v_j) of the proposals, spread over the cluster: CTA r takes proposals
+    // r, r + 8, ..., four warps (a quarter of the columns each) per proposal
     const float* h = a.hs + (size_t)(b * K + A) * a.D;
     const double lse_a = (double)a.qs[b * K + A].lse;
-    for (int j = (int)rank + kVerifyCluster * warp; j < kProposals; j += kVerifyCluster * nwarps) {
+    {
+      constexpr int kPerCta = kProposals / kVerifyCluster;  // 4
+      static_assert(kPerCta * 4 * 32 == kVerifyCThreads, "four warps per proposal");
+      const int jj = warp >> 2, qtr = warp & 3;
+      const int j = (int)rank + kVerifyCluster * jj;
       const int v = (int)ld_cluster_u32(cluster_addr(sv + j, 0));
-      const float l = row_dot(a, v, h);
-      if (lane == 0) st_cluster_f64(cluster_addr(qv + j, 0), exp((double)l / T - lse_a));
+      const int qd = ((a.D / 4 + 3) / 4) * 4;  // columns per quarter (a multiple of 4)
+      const int lo = min(qtr * qd, a.D), hi = min(lo + qd, a.D);
+      const float p = row_dot_part(a, v, h, lo, hi);
+      if (lane == 0) qpart[warp] = p;
+      __syncthreads();
+      if (threadIdx.x < kPerCta) {
+        const int jt = (int)rank + kVerifyCluster * (int)threadIdx.x;
+        const float* qp = qpart + 4 * threadIdx.x;
+        const float l = (qp[0] + qp[1]) + (qp[2] + qp[3]);
+        st_cluster_f64(cluster_addr(qv + jt, 0), exp((double)l / T - lse_a));
+      }
     }
     cluster_sync_all();
     if (lead && threadIdx.x == 0) {  // proposal-rejection sampling of the residual, in order
