@@ -42,6 +42,8 @@ struct Splits {
   long long U = 0;
 };
 __host__ __device__ __forceinline__ long long splits_owner(const Splits& s, long long u) {
+  if (s.U * s.G < 0x7fffffffLL)  // the usual sizes: 32-bit arithmetic, the same quotient
+    return (long long)(((uint32_t)(u + 1) * (uint32_t)s.G - 1u) / (uint32_t)s.U);
   return ((u + 1) * s.G - 1) / s.U;
 }
 __host__ __device__ __forceinline__ int splits_at(const Splits& s, int row, int col) {

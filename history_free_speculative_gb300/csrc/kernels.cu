@@ -54,27 +54,18 @@ __device__ __forceinline__ float4 f4add(float4 a, float4 b) {
   return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
 }
 
+template <int kDepth = 4>
 __device__ __forceinline__ float4 sum_splits4(const float* base, size_t stride, int S) {
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  int s = 0;
-  for (; s + 8 <= S; s += 8) {  // eight independent loads in flight
-    float4 t[8];
+  for (int s = 0; s < S; s += kDepth) {  // up to kDepth loads in flight, added in plane order
+    float4 t[kDepth];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) t[k] = *reinterpret_cast<const float4*>(base + (size_t)(s + k) * stride);
+    for (int k = 0; k < kDepth; ++k)
+      if (s + k < S) t[k] = *reinterpret_cast<const float4*>(base + (size_t)(s + k) * stride);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) acc = f4add(acc, t[k]);
+    for (int k = 0; k < kDepth; ++k)
+      if (s + k < S) acc = f4add(acc, t[k]);
   }
-  for (; s + 4 <= S; s += 4) {  // four independent loads in flight
-    const float4 a = *reinterpret_cast<const float4*>(base + (size_t)s * stride);
-    const float4 b = *reinterpret_cast<const float4*>(base + (size_t)(s + 1) * stride);
-    const float4 c = *reinterpret_cast<const float4*>(base + (size_t)(s + 2) * stride);
-    const float4 d = *reinterpret_cast<const float4*>(base + (size_t)(s + 3) * stride);
-    acc = f4add(acc, a);
-    acc = f4add(acc, b);
-    acc = f4add(acc, c);
-    acc = f4add(acc, d);
-  }
-  for (; s < S; ++s) acc = f4add(acc, *reinterpret_cast<const float4*>(base + (size_t)s * stride));
   return acc;
 }
 
@@ -187,7 +178,10 @@ cudaError_t launch_stage(const StageArgs& a, bool f32, cudaStream_t s) {
 // 16-byte accesses by 8 consecutive lanes hit distinct banks.
 constexpr int kAttnThreads = 512;
 
-__global__ void __launch_bounds__(kAttnThreads) attention_kernel(AttnArgs a) {
+// kDepth split loads in flight per item; kMinCtas CTAs per SM (two when the
+// grid exceeds the SMs: fewer registers, shallower loads).
+template <int kDepth, int kMinCtas>
+__global__ void __launch_bounds__(kAttnThreads, kMinCtas) attention_kernel(AttnArgs a) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ float sm[];
@@ -204,33 +198,27 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(AttnArgs a) {
   const size_t sl = (size_t)(a.loc_rows ? a.loc_rows : a.B * K1) * ldl;
   const size_t sc = (size_t)(a.ctx_rows ? a.ctx_rows : a.B * a.m) * ldc;
   auto loc4 = [&](int row, int col) {
-    return sum_splits4(a.part_loc + (size_t)(b * K1 + row) * ldl + col, sl, splits_at(a.sp_loc, b * K1 + row, col));
+    return sum_splits4<kDepth>(a.part_loc + (size_t)(b * K1 + row) * ldl + col, sl,
+                               splits_at(a.sp_loc, b * K1 + row, col));
   };
   auto ctx4 = [&](int row, int col) {
     const int r = a.ctx_row0 + b * a.m + row, c = a.ctx_col0 + col;
-    return sum_splits4(a.part_ctx + (size_t)r * ldc + c, sc, splits_at(a.sp_ctx, r, c));
+    return sum_splits4<kDepth>(a.part_ctx + (size_t)r * ldc + c, sc, splits_at(a.sp_ctx, r, c));
   };
   auto rnd4 = [&](float4 v) {
     return a.round_bf16 ? make_float4(round_bf16(v.x), round_bf16(v.y), round_bf16(v.z), round_bf16(v.w)) : v;
   };
-  auto rope = [&](float* dst, int i, int j, float4 x1, float4 x2) {
-    const float4 c = load4(a.rope_cos + i * half + j), sn = load4(a.rope_sin + i * half + j);
-    *reinterpret_cast<float4*>(dst + j) =
-        rnd4(make_float4(x1.x * c.x - x2.x * sn.x, x1.y * c.y - x2.y * sn.y, x1.z * c.z - x2.z * sn.z,
-                         x1.w * c.w - x2.w * sn.w));
-    *reinterpret_cast<float4*>(dst + j + half) =
-        rnd4(make_float4(x2.x * c.x + x1.x * sn.x, x2.y * c.y + x1.y * sn.y, x2.z * c.z + x1.z * sn.z,
-                         x2.w * c.w + x1.w * sn.w));
-  };
   const int h4 = half / 4, d4 = dh / 4;
-  const int nq = G * K1 * h4, nk = K1 * h4, nv = K1 * d4, nc = a.m * d4;
+  const int nq = G * K1 * d4, nk = K1 * d4, nv = K1 * d4, nc = a.m * d4;
+  // 1) every float4 of the block's rows summed over the split planes (one
+  //    split sum per item keeps the registers low: two CTAs per SM)
   for (int idx = threadIdx.x; idx < nq + nk + nv + 2 * nc; idx += blockDim.x) {
-    if (idx < nq) {  // queries of the group's heads (rotated)
-      const int j = (idx % h4) * 4, r = idx / h4, hh = r / K1, i = r % K1, col = (h0 + hh) * dh;
-      rope(qs + r * LD, i, j, loc4(i, col + j), loc4(i, col + j + half));
-    } else if (idx < nq + nk) {  // local keys (rotated)
-      const int t = idx - nq, j = (t % h4) * 4, i = t / h4, col = qd + g * dh;
-      rope(ks + (a.m + i) * LD, i, j, loc4(i, col + j), loc4(i, col + j + half));
+    if (idx < nq) {  // queries of the group's heads (rotated below)
+      const int d = (idx % d4) * 4, r = idx / d4, hh = r / K1, i = r % K1;
+      *reinterpret_cast<float4*>(qs + r * LD + d) = loc4(i, (h0 + hh) * dh + d);
+    } else if (idx < nq + nk) {  // local keys (rotated below)
+      const int t = idx - nq, d = (t % d4) * 4, i = t / d4;
+      *reinterpret_cast<float4*>(ks + (a.m + i) * LD + d) = loc4(i, qd + g * dh + d);
     } else if (idx < nq + nk + nv) {  // local values
       const int t = idx - nq - nk, d = (t % d4) * 4, i = t / d4;
       *reinterpret_cast<float4*>(vs + (a.m + i) * LD + d) = rnd4(loc4(i, qd + kvd + g * dh + d));
@@ -239,6 +227,22 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(AttnArgs a) {
       float* dst = (kv ? vs : ks) + j * LD + d;
       *reinterpret_cast<float4*>(dst) = rnd4(ctx4(j, kv * kvd + g * dh + d));
     }
+  }
+  __syncthreads();
+  // 2) rotate-half RoPE of the local queries and keys in shared memory
+  const int rq = G * K1 * h4, rk = K1 * h4;
+  for (int idx = threadIdx.x; idx < rq + rk; idx += blockDim.x) {
+    const int t = idx < rq ? idx : idx - rq, j = (t % h4) * 4, r = t / h4;
+    const int i = idx < rq ? r % K1 : r;
+    float* row = idx < rq ? qs + r * LD : ks + (a.m + r) * LD;
+    const float4 x1 = *reinterpret_cast<const float4*>(row + j), x2 = *reinterpret_cast<const float4*>(row + j + half);
+    const float4 c = load4(a.rope_cos + i * half + j), sn = load4(a.rope_sin + i * half + j);
+    *reinterpret_cast<float4*>(row + j) =
+        rnd4(make_float4(x1.x * c.x - x2.x * sn.x, x1.y * c.y - x2.y * sn.y, x1.z * c.z - x2.z * sn.z,
+                         x1.w * c.w - x2.w * sn.w));
+    *reinterpret_cast<float4*>(row + j + half) =
+        rnd4(make_float4(x2.x * c.x + x1.x * sn.x, x2.y * c.y + x1.y * sn.y, x2.z * c.z + x1.z * sn.z,
+                         x2.w * c.w + x1.w * sn.w));
   }
   __syncthreads();
 
@@ -290,14 +294,19 @@ int attention_heads_per_cta(int n_q, int n_kv, int B) {
 
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s) {
   const size_t smem = attention_smem(a.K, a.m, a.d_h, a.hq);
+  const dim3 grid(a.n_q / a.hq, a.B);
+  const bool many = (int)(grid.x * grid.y) > 152;
+  void (*fn)(AttnArgs) = many ? attention_kernel<2, 2> : attention_kernel<4, 1>;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(attention_kernel<2, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          200 * 1024);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attention_kernel<4, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  return launch_pdl(attention_kernel, dim3(a.n_q / a.hq, a.B), dim3(kAttnThreads), smem, s, a);
+  return launch_pdl(fn, grid, dim3(kAttnThreads), smem, s, a);
 }
 
 // ---------------------------------------------------------------- residual + RMSNorm
@@ -481,17 +490,14 @@ __global__ void __launch_bounds__(512, 1) head_chain_kernel(ChainArgs a) {
     if (req < a.B) {
       const float* p = a.part + (size_t)(req * K + i) * 2 * a.Rp + r0 + r;
       float cc[4] = {0.f, 0.f, 0.f, 0.f}, ee[4] = {0.f, 0.f, 0.f, 0.f};
-      int sp = 0;
-      for (; sp + 4 <= a.S; sp += 4) {
+      for (int sp = 0; sp < a.S; sp += 4) {  // the loads of four planes in flight
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          cc[k] += p[(size_t)(sp + k) * stride];
-          ee[k] += p[(size_t)(sp + k) * stride + a.Rp];
+          if (sp + k < a.S) {
+            cc[k] += p[(size_t)(sp + k) * stride];
+            ee[k] += p[(size_t)(sp + k) * stride + a.Rp];
+          }
         }
-      }
-      for (; sp < a.S; ++sp) {
-        cc[0] += p[(size_t)sp * stride];
-        ee[0] += p[(size_t)sp * stride + a.Rp];
       }
       c = (cc[0] + cc[1]) + (cc[2] + cc[3]);
       e = (ee[0] + ee[1]) + (ee[2] + ee[3]);
