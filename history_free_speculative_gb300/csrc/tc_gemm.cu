@@ -174,66 +174,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = m0 + mt * 128 + q * 32 + lane;
         const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(mt * p.N);
         if (p.mode == 0) {
-          // 32 rows x 32 columns at a time through shared memory (the pipeline
-          // stages are idle once the last product has completed): element (row i,
-          // column j) at i * 32 + (j ^ i), so lanes writing a row or reading a
-          // column hit 32 banks, and each global store writes 32 consecutive
-          // floats of one row instead of 16 bytes of 32 different rows
-          float* stg = reinterpret_cast<float*>(smem) + (warp - 2) * 1024;
+          // lane = row: each lane stores its row's 32 columns per chunk as eight
+          // 16-byte stores straight from the TMEM registers (measured faster than
+          // a shared-memory transpose into full 128-byte rows: the epilogue is
+          // bound by its instruction latency, not by the store pattern)
           float* out = p.part + (size_t)split * p.rows * p.outs;
-          const int row0 = m0 + mt * 128 + q * 32;
-          const bool few = p.rows - row0 < 32;  // a partly filled quadrant: lane = row, direct stores
           for (int c = c_lo; c < c_hi; c += 32) {
             uint32_t v0[16], v1[16];
             tmem_ld16_nowait(tbase + c, v0);
             tmem_ld16_nowait(tbase + c + 16, v1);
             tmem_wait_ld();
-            if (few) {
-              if (r < p.rows) {
-                float* orow = out + (size_t)r * p.outs + o0 + c;
-                auto v = [&](int k) { return __uint_as_float(k < 16 ? v0[k] : v1[k - 16]); };
-                if (o0 + c + 32 <= p.outs) {
+            if (r < p.rows) {
+              float* orow = out + (size_t)r * p.outs + o0 + c;
+              auto v = [&](int k) { return __uint_as_float(k < 16 ? v0[k] : v1[k - 16]); };
+              if (o0 + c + 32 <= p.outs) {
 #pragma unroll
-                  for (int k = 0; k < 8; ++k)
-                    reinterpret_cast<float4*>(orow)[k] =
-                        make_float4(v(4 * k), v(4 * k + 1), v(4 * k + 2), v(4 * k + 3));
-                } else {
+                for (int k = 0; k < 8; ++k)
+                  reinterpret_cast<float4*>(orow)[k] =
+                      make_float4(v(4 * k), v(4 * k + 1), v(4 * k + 2), v(4 * k + 3));
+              } else {
 #pragma unroll
-                  for (int k = 0; k < 32; ++k)
-                    if (o0 + c + k < p.outs) orow[k] = v(k);
-                }
-              }
-              continue;
-            }
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              stg[lane * 32 + (j ^ lane)] = __uint_as_float(v0[j]);
-              stg[lane * 32 + ((j + 16) ^ lane)] = __uint_as_float(v1[j]);
-            }
-            __syncwarp();
-            const int col = o0 + c + lane;
-            if (row0 < p.rows) {
-              // 16 shared-memory reads first: a read placed after a global store
-              // (which may alias it, as far as the compiler knows) would wait for it
-              for (int h = 0; h < 32; h += 16) {
-                float vals[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) vals[j] = stg[(h + j) * 32 + (lane ^ (h + j))];
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                  if (row0 + h + j < p.rows && col < p.outs) out[(size_t)(row0 + h + j) * p.outs + col] = vals[j];
+                for (int k = 0; k < 32; ++k)
+                  if (o0 + c + k < p.outs) orow[k] = v(k);
               }
             }
-            __syncwarp();
           }
         } else if (p.mode == 2) {
           // SwiGLU: the slab's columns come in blocks of 64, [32 gate | 32 up] of the
-          // same 32 features; a = silu(gate) * up goes through the shared-memory
-          // transpose and out as rows of 32 features
-          float* stg = reinterpret_cast<float*>(smem) + (warp - 2) * 1024;
-          const int row0 = m0 + mt * 128 + q * 32;
+          // same 32 features; lane = row stores a = silu(gate) * up of its row's 32
+          // features as bf16 (16-byte stores straight from the registers)
           const int F = p.outs / 2;
-          const bool few = p.rows - row0 < 32;  // a partly filled quadrant: lane = row, direct stores
           for (int blk = eg; blk < p.N / 64; blk += kEpiGroups) {
             uint32_t g0[16], g1[16], u0[16], u1[16];
             tmem_ld16_nowait(tbase + blk * 64, g0);
@@ -241,72 +211,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld16_nowait(tbase + blk * 64 + 32, u0);
             tmem_ld16_nowait(tbase + blk * 64 + 48, u1);
             tmem_wait_ld();
-            if (few) {
-              const int f0 = (o0 / 64 + blk) * 32;  // the block's first feature (F is a multiple of 32)
-              if (r < p.rows && f0 < F) {
-                const size_t idx = (size_t)r * F + f0;
+            const int f0 = (o0 / 64 + blk) * 32;  // the block's first feature (F is a multiple of 32)
+            if (r < p.rows && f0 < F) {
+              const size_t idx = (size_t)r * F + f0;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {  // 8 features per 16-byte store
-                  uint32_t hw[4], lw[4];
+              for (int k = 0; k < 4; ++k) {  // 8 features per 16-byte store
+                uint32_t hw[4], lw[4];
 #pragma unroll
-                  for (int e = 0; e < 4; ++e) {
-                    float a2[2];
+                for (int e = 0; e < 4; ++e) {
+                  float a2[2];
 #pragma unroll
-                    for (int t2 = 0; t2 < 2; ++t2) {
-                      const int j = 8 * k + 2 * e + t2;
-                      const float g = __uint_as_float(j < 16 ? g0[j] : g1[j - 16]);
-                      const float u = __uint_as_float(j < 16 ? u0[j] : u1[j - 16]);
-                      a2[t2] = g / (1.f + expf(-g)) * u;
-                    }
-                    bf16 h0, l0, h1, l1;
-                    if (p.act_planes == 2) {
-                      split_bf16(a2[0], h0, l0);
-                      split_bf16(a2[1], h1, l1);
-                    } else {
-                      h0 = __float2bfloat16_rn(a2[0]);
-                      h1 = __float2bfloat16_rn(a2[1]);
-                      l0 = l1 = h0;
-                    }
-                    hw[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-                    lw[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+                  for (int t2 = 0; t2 < 2; ++t2) {
+                    const int j = 8 * k + 2 * e + t2;
+                    const float g = __uint_as_float(j < 16 ? g0[j] : g1[j - 16]);
+                    const float u = __uint_as_float(j < 16 ? u0[j] : u1[j - 16]);
+                    a2[t2] = g / (1.f + expf(-g)) * u;
                   }
-                  reinterpret_cast<uint4*>(p.act[0] + idx)[k] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                  if (p.act_planes == 2)
-                    reinterpret_cast<uint4*>(p.act[1] + idx)[k] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-                }
-              }
-              continue;
-            }
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float ga = __uint_as_float(g0[j]), gb = __uint_as_float(g1[j]);
-              stg[lane * 32 + (j ^ lane)] = ga / (1.f + expf(-ga)) * __uint_as_float(u0[j]);
-              stg[lane * 32 + ((j + 16) ^ lane)] = gb / (1.f + expf(-gb)) * __uint_as_float(u1[j]);
-            }
-            __syncwarp();
-            const int f = (o0 / 64 + blk) * 32 + lane;  // this lane's feature
-            if (row0 < p.rows) {
-              for (int h = 0; h < 32; h += 16) {
-                float vals[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) vals[j] = stg[(h + j) * 32 + (lane ^ (h + j))];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                  if (row0 + h + j < p.rows && f < F) {
-                    const size_t idx = (size_t)(row0 + h + j) * F + f;
-                    if (p.act_planes == 2) {
-                      bf16 hi, lo;
-                      split_bf16(vals[j], hi, lo);
-                      p.act[0][idx] = hi;
-                      p.act[1][idx] = lo;
-                    } else {
-                      p.act[0][idx] = __float2bfloat16_rn(vals[j]);
-                    }
+                  bf16 h0, l0, h1, l1;
+                  if (p.act_planes == 2) {
+                    split_bf16(a2[0], h0, l0);
+                    split_bf16(a2[1], h1, l1);
+                  } else {
+                    h0 = __float2bfloat16_rn(a2[0]);
+                    h1 = __float2bfloat16_rn(a2[1]);
+                    l0 = l1 = h0;
                   }
+                  hw[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+                  lw[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
                 }
+                reinterpret_cast<uint4*>(p.act[0] + idx)[k] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                if (p.act_planes == 2)
+                  reinterpret_cast<uint4*>(p.act[1] + idx)[k] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
               }
             }
-            __syncwarp();
           }
         } else {
           // LM head: 4 best (score, id) and LSE partials of this vocabulary slab for row r
