@@ -525,7 +525,7 @@ int run_lm_head(dlite_handle* h, int B, float temperature, uint64_t seed, const 
     prm.K_draft = c.K;
     prm.status = h->status;
     CK(tc::launch(pl, x0, nullptr, w0, nullptr, prm, s));
-    n_tiles = (c.V + pl.N - 1) / pl.N * tc::kEpiGroups;
+    n_tiles = (c.V + pl.N - 1) / pl.N * tc::kGemmEpiGroups;
   }
   mark(h, "lm_head");
   LmMergeArgs mg;
@@ -740,7 +740,7 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
     if (pc2.ok && tc::use_pair_engine(C, h->np, h->np)) pe2 = (size_t)pc2.S * C * 2 * h->kvd > pe2 ? (size_t)pc2.S * C * 2 * h->kvd : pe2;
     const tc::Plan pl = lm_plan(h, H);
     if (!pl.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
-    const size_t v3 = (size_t)((V + pl.N - 1) / pl.N) * tc::kEpiGroups * H;
+    const size_t v3 = (size_t)((V + pl.N - 1) / pl.N) * tc::kGemmEpiGroups * H;
     lme = v3 > lme ? v3 : lme;
     const tc::LmPlan lp = tc::lm_plan_persistent(H, V, D, h->num_sms);
     if (lp.ok) {

@@ -20,7 +20,7 @@ namespace tc {
 // The MMA issue loop is fully unrolled over these so the issuing thread only
 // adds precomputed descriptor offsets between tcgen05.mma instructions.
 template <int NMT, int XP, int WP>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kGemmThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap mx0, const __grid_constant__ CUtensorMap mx1,
                    const __grid_constant__ CUtensorMap mw0, const __grid_constant__ CUtensorMap mw1,
                    const TcParams p) {
@@ -160,10 +160,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (lane == 0) umma_commit(accf);
     __syncwarp();
-  } else {  // ---------------- epilogue warps 2 .. 2 + 4 * kEpiGroups - 1
+  } else {  // ---------------- epilogue warps 2 .. 2 + 4 * kGemmEpiGroups - 1
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     const int eg = (warp - 2) >> 2;                 // column group of this warp
-    const int ncol = p.N / kEpiGroups;              // columns per group (multiple of 32)
+    const int ncol = p.N / kGemmEpiGroups;          // columns per group (multiple of 16)
     const int c_lo = eg * ncol, c_hi = c_lo + ncol;
     const bool got = mbar_wait_warp(accf, 0, p.status);
     fence_after();
@@ -174,28 +174,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = m0 + mt * 128 + q * 32 + lane;
         const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(mt * p.N);
         if (p.mode == 0) {
-          // lane = row: each lane stores its row's 32 columns per chunk as eight
+          // lane = row: each lane stores its row's 16 columns per chunk as four
           // 16-byte stores straight from the TMEM registers (measured faster than
           // a shared-memory transpose into full 128-byte rows: the epilogue is
           // bound by its instruction latency, not by the store pattern)
           float* out = p.part + (size_t)split * p.rows * p.outs;
-          for (int c = c_lo; c < c_hi; c += 32) {
-            uint32_t v0[16], v1[16];
+          for (int c = c_lo; c < c_hi; c += 16) {
+            uint32_t v0[16];
             tmem_ld16_nowait(tbase + c, v0);
-            tmem_ld16_nowait(tbase + c + 16, v1);
             tmem_wait_ld();
             if (r < p.rows) {
               float* orow = out + (size_t)r * p.outs + o0 + c;
-              auto v = [&](int k) { return __uint_as_float(k < 16 ? v0[k] : v1[k - 16]); };
-              if (o0 + c + 32 <= p.outs) {
+              if (o0 + c + 16 <= p.outs) {
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
+                for (int k = 0; k < 4; ++k)
                   reinterpret_cast<float4*>(orow)[k] =
-                      make_float4(v(4 * k), v(4 * k + 1), v(4 * k + 2), v(4 * k + 3));
+                      make_float4(__uint_as_float(v0[4 * k]), __uint_as_float(v0[4 * k + 1]),
+                                  __uint_as_float(v0[4 * k + 2]), __uint_as_float(v0[4 * k + 3]));
               } else {
 #pragma unroll
-                for (int k = 0; k < 32; ++k)
-                  if (o0 + c + k < p.outs) orow[k] = v(k);
+                for (int k = 0; k < 16; ++k)
+                  if (o0 + c + k < p.outs) orow[k] = __uint_as_float(v0[k]);
               }
             }
           }
@@ -204,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // same 32 features; lane = row stores a = silu(gate) * up of its row's 32
           // features as bf16 (16-byte stores straight from the registers)
           const int F = p.outs / 2;
-          for (int blk = eg; blk < p.N / 64; blk += kEpiGroups) {
+          for (int blk = eg; blk < p.N / 64; blk += kGemmEpiGroups) {
             uint32_t g0[16], g1[16], u0[16], u1[16];
             tmem_ld16_nowait(tbase + blk * 64, g0);
             tmem_ld16_nowait(tbase + blk * 64 + 16, g1);
@@ -278,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           }
-          if (valid) lm_acc_store(acc, p.rec + ((size_t)blockIdx.x * kEpiGroups + eg) * p.rows + r);
+          if (valid) lm_acc_store(acc, p.rec + ((size_t)blockIdx.x * kGemmEpiGroups + eg) * p.rows + r);
         }
       }
     }
@@ -454,7 +453,7 @@ cudaError_t launch(const Plan& pl, const CUtensorMap* x0, const CUtensorMap* x1,
   prm.stage_bytes = pl.stage_bytes;
   prm.tmem_cols = (uint32_t)pl.tmem_cols;
   dim3 grid((prm.outs + pl.N - 1) / pl.N, pl.S, pl.groups);
-  return launch_pdl(fn, grid, dim3(kThreads), smem_bytes(pl), s, *x0, x1 ? *x1 : *x0, *w0,
+  return launch_pdl(fn, grid, dim3(kGemmThreads), smem_bytes(pl), s, *x0, x1 ? *x1 : *x0, *w0,
                     w1 ? *w1 : *w0, prm);
 }
 

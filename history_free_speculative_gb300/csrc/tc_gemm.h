@@ -10,6 +10,9 @@ namespace tc {
 
 constexpr int kEpiGroups = 2;                    // epilogue warp groups (each 4 warps)
 constexpr int kThreads = 64 + 128 * kEpiGroups;  // TMA warp, MMA warp, epilogue warps
+// the one-CTA engine: four epilogue groups (its epilogue is on the critical path)
+constexpr int kGemmEpiGroups = 4;
+constexpr int kGemmThreads = 64 + 128 * kGemmEpiGroups;
 constexpr int kNumSMs = 152;
 constexpr size_t kSmemBudget = 226 * 1024;  // dynamic shared memory per CTA (all of it)
 constexpr size_t kTailPad = 16 * 1024;      // overhang room for a 128-row operand read
@@ -37,7 +40,7 @@ struct TcParams {
   float* part = nullptr;
   bf16* act[2] = {nullptr, nullptr};  // mode 2: a = silu(gate) * up, [rows, outs / 2] bf16 planes
   int act_planes = 1;
-  LmRec* rec = nullptr;    // [slabs * kEpiGroups][rows]
+  LmRec* rec = nullptr;    // [slabs * kGemmEpiGroups][rows]
   float inv_T = 0.f;
   uint32_t k0 = 0, k1 = 0;
   const int64_t* pos = nullptr;
