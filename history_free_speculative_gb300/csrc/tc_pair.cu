@@ -32,7 +32,7 @@ namespace tc {
 constexpr uint32_t kATile = 128 * 128;       // one 128-row x 64-k bf16 tile (16 KB)
 constexpr int kPairN = 256;                  // output columns per tile
 constexpr uint32_t kPairStage = 2 * kATile;  // this CTA's X tile + W tile per k block
-constexpr uint32_t kPairStaging = 4 * kEpiGroups * 32 * 32 * 4;  // epilogue transpose buffers
+constexpr uint32_t kPairStaging = 0;  // the epilogue stores from registers: no staging area
 
 struct Segment {
   int tile, kb_lo, n, plane;
@@ -194,7 +194,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ncol = kPairN / kEpiGroups;
     const int c_lo = eg * ncol;
     const uint32_t acce_leader = map_to_rank(acce0, 0);
-    float* stg = reinterpret_cast<float*>(smem + (size_t)p.stages * kPairStage) + (warp - 2) * 1024;
     pdl_wait();  // the partial buffer may still be read by the previous kernel
     long long u = u_begin;
     Segment sg;
@@ -208,34 +207,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int o0 = slab * kPairN;
       const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * kPairN);
       float* out = p.part + (size_t)sg.plane * p.rows * p.outs;
+      // lane = row: each lane stores its row's 32 columns per chunk as eight 16-byte
+      // stores straight from the TMEM registers (a shared-memory transpose into full
+      // 128-byte rows was latency-bound)
+      const int r = row0 + lane;
       for (int c = c_lo; c < c_lo + ncol; c += 32) {
-        // 32 rows x 32 columns through shared memory: element (row i, column j) at
-        // i * 32 + (j ^ i), so lanes writing a row or reading a column hit 32 banks;
-        // each global store then writes one row's 32 consecutive floats
         uint32_t v0[16], v1[16];
         tmem_ld16_nowait(tbase + c, v0);
         tmem_ld16_nowait(tbase + c + 16, v1);
         tmem_wait_ld();
+        if (r < p.rows) {
+          float* orow = out + (size_t)r * p.outs + o0 + c;
+          auto v = [&](int k) { return __uint_as_float(k < 16 ? v0[k] : v1[k - 16]); };
+          if (o0 + c + 32 <= p.outs) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          stg[lane * 32 + (j ^ lane)] = __uint_as_float(v0[j]);
-          stg[lane * 32 + ((j + 16) ^ lane)] = __uint_as_float(v1[j]);
-        }
-        __syncwarp();
-        const int col = o0 + c + lane;
-        if (row0 < p.rows) {
-          // 16 shared-memory reads first: a read placed after a global store
-          // (which may alias it, as far as the compiler knows) would wait for it
-          for (int h = 0; h < 32; h += 16) {
-            float vals[16];
+            for (int k = 0; k < 8; ++k)
+              reinterpret_cast<float4*>(orow)[k] = make_float4(v(4 * k), v(4 * k + 1), v(4 * k + 2), v(4 * k + 3));
+          } else {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) vals[j] = stg[(h + j) * 32 + (lane ^ (h + j))];
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (row0 + h + j < p.rows && col < p.outs) out[(size_t)(row0 + h + j) * p.outs + col] = vals[j];
+            for (int k = 0; k < 32; ++k)
+              if (o0 + c + k < p.outs) orow[k] = v(k);
           }
         }
-        __syncwarp();
       }
       fence_before();
       __syncwarp();
