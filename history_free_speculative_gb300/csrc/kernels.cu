@@ -24,8 +24,8 @@ __device__ __forceinline__ void store_planes(bf16* const* pl, int n, size_t i, f
   }
 }
 
-constexpr int kRowThreads = 1024;
-constexpr int kRowVec = 4;  // float4 chunks per thread at most
+constexpr int kRowThreads = 512;  // two or more CTAs per SM (rows in one wave)
+constexpr int kRowVec = 8;        // float4 chunks per thread at most (D <= 16384)
 
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -97,14 +97,14 @@ __global__ void __launch_bounds__(1024) stage_kernel(StageArgs a) {
   const int row = blockIdx.x;
   const int D = a.D, n4 = D / 4;
   const int nz = a.B * a.m;
-  float4 v[4];
+  float4 v[kRowVec];
   float ss = 0.f;
   if (row < nz) {
     const int b = row / a.m, j = row % a.m;
     const T* h = reinterpret_cast<const T*>(a.hidden) + ((size_t)b * a.m + j) * D;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int i = threadIdx.x + k * 1024;
+    for (int k = 0; k < kRowVec; ++k) {
+      const int i = threadIdx.x + k * blockDim.x;
       if (i < n4) {
         v[k] = f4add(load4(h + 4 * i), load4(a.e_depth + (size_t)j * D + 4 * i));
         ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
@@ -113,8 +113,8 @@ __global__ void __launch_bounds__(1024) stage_kernel(StageArgs a) {
     ss = block_sum(ss, red);
     const float inv = rsqrtf(ss / D + a.eps);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int i = threadIdx.x + k * 1024;
+    for (int k = 0; k < kRowVec; ++k) {
+      const int i = threadIdx.x + k * blockDim.x;
       if (i < n4) {
         const float4 g = load4(a.g_stage + 4 * i);
         const float4 zv = make_float4(v[k].x * inv * g.x, v[k].y * inv * g.y, v[k].z * inv * g.z,
@@ -136,8 +136,8 @@ __global__ void __launch_bounds__(1024) stage_kernel(StageArgs a) {
     }
     const T* E = reinterpret_cast<const T*>(a.E);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int i = threadIdx.x + k * 1024;
+    for (int k = 0; k < kRowVec; ++k) {
+      const int i = threadIdx.x + k * blockDim.x;
       if (i < n4) {
         v[k] = (i0 == 0) ? load4(E + (a.E_tiled ? tiled_index(tok, 4 * i, D) : (size_t)tok * D + 4 * i))
                          : load4(a.e_ph + 4 * i);
@@ -148,8 +148,8 @@ __global__ void __launch_bounds__(1024) stage_kernel(StageArgs a) {
     ss = block_sum(ss, red);
     const float inv = rsqrtf(ss / D + a.eps);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int i = threadIdx.x + k * 1024;
+    for (int k = 0; k < kRowVec; ++k) {
+      const int i = threadIdx.x + k * blockDim.x;
       if (i < n4) {
         const float4 g = load4(a.g_attn0 + 4 * i);
         store4_planes(a.y, a.ny, (size_t)lr * D + 4 * i,
@@ -162,8 +162,11 @@ __global__ void __launch_bounds__(1024) stage_kernel(StageArgs a) {
 
 cudaError_t launch_stage(const StageArgs& a, bool f32, cudaStream_t s) {
   const int rows = a.B * a.m + a.B * (a.K + 1);
-  if (f32) return launch_pdl(stage_kernel<float>, dim3(rows), dim3(1024), 0, s, a);
-  return launch_pdl(stage_kernel<bf16>, dim3(rows), dim3(1024), 0, s, a);
+  // few rows: 1024 threads per row; many: 512 (several rows per SM at once)
+  const int threads = rows <= 2 * 152 ? 1024 : 512;
+  if (a.D / 4 > kRowVec * threads) return cudaErrorInvalidValue;
+  if (f32) return launch_pdl(stage_kernel<float>, dim3(rows), dim3(threads), 0, s, a);
+  return launch_pdl(stage_kernel<bf16>, dim3(rows), dim3(threads), 0, s, a);
 }
 
 // ---------------------------------------------------------------- K2b: block attention
@@ -318,7 +321,8 @@ cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s) {
 // split's load issued before use; the C partial sums of squares are
 // exchanged through distributed shared memory and added in rank order, so
 // every CTA of the row applies the same scale.
-__global__ void __launch_bounds__(kRowThreads) resnorm_kernel(ResNormArgs a) {
+template <int kDepth, int kMinCtas, int kVec>  // split loads in flight; CTAs per SM; float4 per thread
+__global__ void __launch_bounds__(kRowThreads, kMinCtas) resnorm_kernel(ResNormArgs a) {
   pdl_trigger();
   pdl_wait();
   __shared__ float red[32];
@@ -326,14 +330,14 @@ __global__ void __launch_bounds__(kRowThreads) resnorm_kernel(ResNormArgs a) {
   const int r = blockIdx.x / (int)C, D = a.D;
   const int n4 = D / 4 / (int)C, i0 = n4 * (int)c;  // this CTA's float4 range [i0, i0 + n4)
   const size_t stride = (size_t)a.rows * D;
-  float4 v[kRowVec];
+  float4 v[kVec];
   float ss = 0.f;
 #pragma unroll
-  for (int k = 0; k < kRowVec; ++k) {
+  for (int k = 0; k < kVec; ++k) {
     const int i = i0 + threadIdx.x + k * blockDim.x;
     if (i < i0 + n4) {
       float4 x = *reinterpret_cast<const float4*>(a.x + (size_t)r * D + 4 * i);
-      x = f4add(x, sum_splits4(a.part + (size_t)r * D + 4 * i, stride, splits_at(a.sp, r, 4 * i)));
+      x = f4add(x, sum_splits4<kDepth>(a.part + (size_t)r * D + 4 * i, stride, splits_at(a.sp, r, 4 * i)));
       *reinterpret_cast<float4*>(a.x + (size_t)r * D + 4 * i) = x;
       if (a.tap_x) *reinterpret_cast<float4*>(a.tap_x + (size_t)r * D + 4 * i) = x;
       v[k] = x;
@@ -354,7 +358,7 @@ __global__ void __launch_bounds__(kRowThreads) resnorm_kernel(ResNormArgs a) {
     if (i == 0) return;
     const size_t orow = (size_t)(b * (a.K1 - 1) + (i - 1)) * D;
 #pragma unroll
-    for (int k = 0; k < kRowVec; ++k) {
+    for (int k = 0; k < kVec; ++k) {
       const int j = i0 + threadIdx.x + k * blockDim.x;
       if (j < i0 + n4) {
         const float4 g = *reinterpret_cast<const float4*>(a.g + 4 * j);
@@ -367,7 +371,7 @@ __global__ void __launch_bounds__(kRowThreads) resnorm_kernel(ResNormArgs a) {
     }
   } else {
 #pragma unroll
-    for (int k = 0; k < kRowVec; ++k) {
+    for (int k = 0; k < kVec; ++k) {
       const int j = i0 + threadIdx.x + k * blockDim.x;
       if (j < i0 + n4) {
         const float4 g = *reinterpret_cast<const float4*>(a.g + 4 * j);
@@ -400,7 +404,10 @@ cudaError_t launch_resnorm(const ResNormArgs& a, cudaStream_t s) {
   attrs[1].val.clusterDim.z = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, resnorm_kernel, a);
+  // a cluster per row: few CTAs, deep loads; else two CTAs per SM (all rows in one wave)
+  if (n4 > threads * (C > 1 ? 1 : kRowVec)) return cudaErrorInvalidValue;
+  return C > 1 ? cudaLaunchKernelEx(&cfg, resnorm_kernel<4, 1, 1>, a)
+               : cudaLaunchKernelEx(&cfg, resnorm_kernel<2, 2, kRowVec>, a);
 }
 
 // ---------------------------------------------------------------- SwiGLU epilogue
