@@ -170,6 +170,22 @@ cudaError_t launch_stage(const StageArgs& a, bool f32, cudaStream_t s) {
 }
 
 // ---------------------------------------------------------------- K2b: block attention
+// One warp-wide bf16 tensor-core product D[16 x 8] += A[16 x 16] B[16 x 8]
+// (fp32 accumulation; lane (g, c) = (lane / 4, lane % 4) holds A rows g, g + 8
+// at columns 2c, 2c + 1 (+8), B columns g at rows 2c, 2c + 1 (+8), D rows
+// g, g + 8 at columns 2c, 2c + 1).
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
 // One CTA per (hq query heads of one key/value group, request b): with many
 // requests hq = n_q / n_kv, so each head's keys and values are reduced from the
 // split-K partials once; with few requests hq shrinks to spread the work over
@@ -194,10 +210,12 @@ __global__ void __launch_bounds__(kAttnThreads, kMinCtas) attention_kernel(AttnA
   const int ldl = qd + 2 * kvd;               // local partial row width
   const int ldc = a.ldc ? a.ldc : 2 * kvd;     // context partial row width
   const int Tk = a.m + K1;
-  const int LD = dh + 4;
-  float* qs = sm;               // [G * K1][LD]: query row i of head g G + hh at hh * K1 + i
-  float* ks = qs + G * K1 * LD;  // [Tk][LD]
-  float* vs = ks + Tk * LD;      // [Tk][LD]
+  const int LD = dh + 4, LP = 36;
+  const int QR = G * K1, QRp = (QR + 15) / 16 * 16, Tkp = (Tk + 15) / 16 * 16;  // padded to tensor-core tiles
+  float* qs = sm;              // [QRp][LD]: query row i of head g G + hh at hh * K1 + i
+  float* ks = qs + QRp * LD;   // [Tkp][LD]
+  float* vs = ks + Tkp * LD;   // [Tkp][LD]
+  float* ps = vs + Tkp * LD;   // [QRp][LP] scores, then probabilities
   const size_t sl = (size_t)(a.loc_rows ? a.loc_rows : a.B * K1) * ldl;
   const size_t sc = (size_t)(a.ctx_rows ? a.ctx_rows : a.B * a.m) * ldc;
   auto loc4 = [&](int row, int col) {
@@ -232,6 +250,15 @@ __global__ void __launch_bounds__(kAttnThreads, kMinCtas) attention_kernel(AttnA
     }
   }
   __syncthreads();
+  // padding rows of the tensor-core tiles hold zeros
+  const bool tensor = a.round_bf16 && QR >= 32;
+  for (int idx = threadIdx.x; tensor && idx < ((QRp - QR) + 2 * (Tkp - Tk)) * dh; idx += blockDim.x) {
+    const int r = idx / dh, d = idx % dh;
+    float* row = r < QRp - QR ? qs + (QR + r) * LD
+                              : (r < QRp - QR + Tkp - Tk ? ks + (Tk + r - (QRp - QR)) * LD
+                                                         : vs + (Tk + r - (QRp - QR) - (Tkp - Tk)) * LD);
+    row[d] = 0.f;
+  }
   // 2) rotate-half RoPE of the local queries and keys in shared memory
   const int rq = G * K1 * h4, rk = K1 * h4;
   for (int idx = threadIdx.x; idx < rq + rk; idx += blockDim.x) {
@@ -250,6 +277,76 @@ __global__ void __launch_bounds__(kAttnThreads, kMinCtas) attention_kernel(AttnA
   __syncthreads();
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  if (tensor) {
+    // 3) bf16 operands (every value here is a bf16 rounding) and enough query
+    //    rows to fill the tiles (with a few rows the scalar form below is as
+    //    fast): S = Q K^T on the
+    //    tensor cores, softmax per row, O = P V with P split into two bf16 parts
+    //    (P = hi + lo to ~2^-16), fp32 accumulation throughout
+    const int gq = lane >> 2, cq = lane & 3;
+    const int mtiles = QRp / 16, ntk = (Tk + 7) / 8;
+    for (int t = warp; t < mtiles * ntk; t += nw) {
+      const int mt = t / ntk, nt = t % ntk;
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      const float* qa = qs + (mt * 16 + gq) * LD + 2 * cq;
+      const float* kb = ks + (nt * 8 + gq) * LD + 2 * cq;
+      for (int k0 = 0; k0 < dh; k0 += 16) {
+        const uint32_t A[4] = {pack_bf16x2(qa[k0], qa[k0 + 1]), pack_bf16x2(qa[8 * LD + k0], qa[8 * LD + k0 + 1]),
+                               pack_bf16x2(qa[k0 + 8], qa[k0 + 9]),
+                               pack_bf16x2(qa[8 * LD + k0 + 8], qa[8 * LD + k0 + 9])};
+        mma16816(d, A, pack_bf16x2(kb[k0], kb[k0 + 1]), pack_bf16x2(kb[k0 + 8], kb[k0 + 9]));
+      }
+      const int r0 = mt * 16 + gq, c0 = nt * 8 + 2 * cq;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = r0 + 8 * (e >> 1), c = c0 + (e & 1);
+        ps[r * LP + c] = c < Tk ? d[e] * a.scale : -INFINITY;
+      }
+    }
+    __syncthreads();
+    for (int r = warp; r < QR; r += nw) {  // softmax over the Tk <= 32 keys, one warp per row
+      const float x = lane < Tk ? ps[r * LP + lane] : -INFINITY;
+      const float mx = warp_max(x);
+      const float e = lane < Tk ? expf(x - mx) : 0.f;
+      const float den = warp_sum(e);
+      if (lane < Tkp) ps[r * LP + lane] = e / den;
+    }
+    __syncthreads();
+    const int ntd = dh / 8;
+    for (int t = warp; t < mtiles * ntd; t += nw) {
+      const int mt = t / ntd, nt = t % ntd;
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      const float* pa = ps + (mt * 16 + gq) * LP + 2 * cq;
+      const float* vb = vs + 2 * cq * LD + nt * 8 + gq;
+      for (int k0 = 0; k0 < Tkp; k0 += 16) {
+        const float p[8] = {pa[k0], pa[k0 + 1], pa[8 * LP + k0], pa[8 * LP + k0 + 1],
+                            pa[k0 + 8], pa[k0 + 9], pa[8 * LP + k0 + 8], pa[8 * LP + k0 + 9]};
+        float lo[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) lo[j] = p[j] - __bfloat162float(__float2bfloat16_rn(p[j]));
+        const uint32_t Ahi[4] = {pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]), pack_bf16x2(p[4], p[5]),
+                                 pack_bf16x2(p[6], p[7])};
+        const uint32_t Alo[4] = {pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]), pack_bf16x2(lo[4], lo[5]),
+                                 pack_bf16x2(lo[6], lo[7])};
+        const float* v = vb + k0 * LD;
+        const uint32_t b0 = pack_bf16x2(v[0], v[LD]), b1 = pack_bf16x2(v[8 * LD], v[9 * LD]);
+        mma16816(d, Ahi, b0, b1);
+        mma16816(d, Alo, b0, b1);
+      }
+      const int r0 = mt * 16 + gq, col = nt * 8 + 2 * cq;
+#pragma unroll
+      for (int hh2 = 0; hh2 < 2; ++hh2) {
+        const int r = r0 + 8 * hh2;
+        if (r < QR) {
+          const int hh = r / K1, i = r % K1;
+          const size_t idx = (size_t)(b * K1 + i) * qd + (h0 + hh) * dh + col;
+          store_planes(a.o, a.no, idx, d[2 * hh2]);
+          store_planes(a.o, a.no, idx + 1, d[2 * hh2 + 1]);
+        }
+      }
+    }
+    return;
+  }
   for (int r = warp; r < G * K1; r += nw) {
     const int hh = r / K1, i = r % K1;
     const float* q = qs + r * LD;
@@ -285,7 +382,8 @@ __global__ void __launch_bounds__(kAttnThreads, kMinCtas) attention_kernel(AttnA
 }
 
 size_t attention_smem(int K, int m, int d_h, int G) {
-  return (size_t)(G * (K + 1) + 2 * (m + K + 1)) * (d_h + 4) * sizeof(float);
+  const int QRp = (G * (K + 1) + 15) / 16 * 16, Tkp = (m + K + 1 + 15) / 16 * 16;
+  return ((size_t)(QRp + 2 * Tkp) * (d_h + 4) + (size_t)QRp * 36) * sizeof(float);
 }
 
 int attention_heads_per_cta(int n_q, int n_kv, int B) {
