@@ -265,7 +265,18 @@ def draft_request(hidden, anchor, W, cfg, temperature=0.0, seed=0, pos=0, reques
 
 # ---------------------------------------------------------------- verification
 
-def verify_greedy(cand, target_tokens):
+def _n_verify(K, n_verify):
+    """Candidates handed to verification: all K by default, else the first
+    n_verify; the rest are dropped ([P1] §"草稿块长与验证块长不是一个参数":
+    a verification window of n_verify + 1 tokens including the anchor truncates
+    verification, not drafting)."""
+    kv = K if n_verify is None else int(n_verify)
+    if not 0 <= kv <= K:
+        raise ValueError("n_verify must lie in [0, K]")
+    return kv
+
+
+def verify_greedy(cand, target_tokens, n_verify=None):
     """Longest accepted prefix, greedy mode.
 
     target_tokens[j] is the target's argmax at input index j of [a, d_1..d_K],
@@ -276,9 +287,11 @@ def verify_greedy(cand, target_tokens):
     token when A = K); that token is the next anchor.
     [P1] §"一次因果前向评估整条候选", §"贪心模式与随机模式要分别说明",
     §"一轮执行后..." steps 4-5.
+    With n_verify = w < K only d_1..d_w are verified (A <= w) and the token
+    committed after them is target_tokens[A].
     """
     cand = [int(c) for c in cand]
-    K = len(cand)
+    K = _n_verify(len(cand), n_verify)
     A = 0
     while A < K and cand[A] == int(target_tokens[A]):
         A += 1
@@ -295,7 +308,7 @@ def inverse_cdf(w, u):
 N_PROPOSALS = 32
 
 
-def verify_sample(cand, logit_d, lse, h, E, p, temperature, seed, pos, request):
+def verify_sample(cand, logit_d, lse, h, E, p, temperature, seed, pos, request, n_verify=None):
     """Speculative rejection sampling with residual resampling, one request.
 
     For i = 1..K: q_i(d_i) = exp(l_{i,d_i}/T - lse_i); with
@@ -313,10 +326,12 @@ def verify_sample(cand, logit_d, lse, h, E, p, temperature, seed, pos, request):
     A = K: the bonus token is drawn from p_K by inverse CDF with
       u = Philox(0, pos+K+1, request, TAG_BONUS) word 0.
     q(v) for arbitrary v is recomputed from the head state: exp(E_v.h/T - lse).
+    With n_verify = w < K the round runs as if K were w (only d_1..d_w are
+    tested; the bonus comes from p_w at position pos + w + 1).
     """
     T = float(np.float32(temperature))   # a float32 quantity, as in the C ABI
     cand = [int(c) for c in cand]
-    K = len(cand)
+    K = _n_verify(len(cand), n_verify)
     p = f64(p)
     A = K
     for i in range(1, K + 1):
@@ -351,6 +366,34 @@ def verify_sample(cand, logit_d, lse, h, E, p, temperature, seed, pos, request):
             tok = inverse_cdf(r if r.sum() > 0 else row, u3)
             resampled = "fallback"
     return dict(A=A, commits=cand[:A] + [tok], n_commit=A + 1, next_anchor=tok, how=resampled)
+
+
+def match_target_token(p_row, seed, pos, request, j):
+    """The target's own sample at input index j (its choice for position j + 1):
+    inverse CDF over p_j with u = Philox(0, pos + j + 1, request, TAG_MATCH) word 0."""
+    u = float(_ph.draw(seed, 0, pos + j + 1, request, _ph.TAG_MATCH, 0))
+    return inverse_cdf(p_row, u)
+
+
+def verify_match(cand, p, seed, pos, request, n_verify=None):
+    """Match verification, one request ([P1] §"贪心模式与随机模式要分别说明",
+    the official `match` mode): the candidates are the draft's greedy choices,
+    the target samples every position from its own distribution p_j (rows given
+    at the target's temperature), A is the leading run of positions where the
+    candidate equals the target's sample, and the round commits d_1..d_A then
+    the target's sample at index A (at the first mismatch, or after the last
+    verified candidate). Unlike rejection sampling this is no p/q rule: for a
+    fixed candidate d the chance of a match at index j is p_j(d).
+    """
+    cand = [int(c) for c in cand]
+    K = _n_verify(len(cand), n_verify)
+    p = f64(p)
+    t = [match_target_token(p[j], seed, pos, request, j) for j in range(K + 1)]
+    A = 0
+    while A < K and cand[A] == t[A]:
+        A += 1
+    tok = t[A]
+    return dict(A=A, commits=cand[:A] + [tok], n_commit=A + 1, next_anchor=tok, targets=t)
 
 
 # ---------------------------------------------------------------- batch drivers

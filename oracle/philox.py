@@ -27,6 +27,7 @@ TAG_GUMBEL = 1
 TAG_ACCEPT = 2
 TAG_RESID = 3
 TAG_BONUS = 4
+TAG_MATCH = 5   # the target's own sample at each position (match verification)
 
 _MASK = np.uint64(0xFFFFFFFF)
 

@@ -366,6 +366,95 @@ def test_prefix_survival_is_product_of_conditionals():
     assert abs((A + 1).mean() - rp.expected_advance(rp.prefix_survival(c))) < 0.03
 
 
+# ---------------------------------------------------------------- verification window, match mode
+
+def test_verification_window_is_the_shorter_round():
+    """n_verify = w gives exactly the round of a drafter with K = w on the first
+    w candidates and target rows 0..w (greedy and sampling, including the
+    Philox positions of the bonus draw), and n_verify = K changes nothing."""
+    rng = np.random.default_rng(31)
+    V, K, T = 6, 4, 0.7
+    E = np.eye(V)
+    for trial in range(60):
+        cand = [int(c) for c in rng.integers(0, 3, size=K)]
+        tgt = [int(t) for t in rng.integers(0, 3, size=K + 1)]
+        ell = rng.normal(0, 1.0, (K, V))
+        lse = [float(np.log(np.exp(e / T).sum())) for e in ell]
+        logit_d = [float(ell[i, cand[i]]) for i in range(K)]
+        p = rng.dirichlet(np.ones(V), size=K + 1)
+        assert O.verify_greedy(cand, tgt, n_verify=K) == O.verify_greedy(cand, tgt)
+        full = O.verify_sample(cand, logit_d, lse, ell, E, p, T, 5, 100 + trial, 3)
+        assert O.verify_sample(cand, logit_d, lse, ell, E, p, T, 5, 100 + trial, 3, n_verify=K) == full
+        for w in range(K + 1):
+            g = O.verify_greedy(cand, tgt, n_verify=w)
+            assert g == O.verify_greedy(cand[:w], tgt[:w + 1])
+            assert g["A"] <= w
+            r = O.verify_sample(cand, logit_d, lse, ell, E, p, T, 5, 100 + trial, 3, n_verify=w)
+            assert r == O.verify_sample(cand[:w], logit_d[:w], lse[:w], ell[:w + 1], E, p[:w + 1], T, 5,
+                                        100 + trial, 3)
+    with pytest.raises(ValueError):
+        O.verify_greedy([1, 2], [1, 2, 3], n_verify=3)
+
+
+def test_match_with_deterministic_target_is_greedy():
+    """One-hot target rows: every sample is the row's id, so match verification
+    reduces to greedy verification against those ids (every window)."""
+    rng = np.random.default_rng(32)
+    V, K = 5, 4
+    for trial in range(50):
+        tgt = [int(t) for t in rng.integers(0, V, size=K + 1)]
+        cand = [t if rng.random() < 0.7 else int(rng.integers(0, V)) for t in tgt[:K]]
+        p = np.zeros((K + 1, V))
+        p[np.arange(K + 1), tgt] = 1.0
+        for w in range(K + 1):
+            r = O.verify_match(cand, p, 9, trial, 1, n_verify=w)
+            g = O.verify_greedy(cand, tgt, n_verify=w)
+            assert r["targets"] == tgt[:w + 1]
+            assert {k: r[k] for k in g} == g
+
+
+def test_match_statistics():
+    """P(A >= k) = prod_{j<k} p_j(d_{j+1}) (independent target samples), and at a
+    mismatch the committed token follows p_A restricted to ids other than the
+    candidate: p_A(v) / (1 - p_A(d)), v != d. Monte Carlo over positions."""
+    rng = np.random.default_rng(33)
+    V, K, N = 4, 3, 20000
+    p = rng.dirichlet(np.ones(V) * 2.0, size=K + 1)
+    cand = [int(np.argmax(p[j])) for j in range(K)]      # a greedy draft that guessed the argmax
+    A = np.zeros(N, dtype=np.int64)
+    first = np.zeros(V)
+    for n in range(N):
+        r = O.verify_match(cand, p, 44, 10 * n, 2)
+        A[n] = r["A"]
+        if r["A"] == 0:
+            first[r["commits"][0]] += 1
+    pm = np.array([p[j, cand[j]] for j in range(K)])
+    want = np.cumprod(pm)
+    for k in range(1, K + 1):
+        est = (A >= k).mean()
+        assert abs(est - want[k - 1]) < 5 * math.sqrt(want[k - 1] * (1 - want[k - 1]) / N)
+    n0 = first.sum()
+    cond = p[0].copy()
+    cond[cand[0]] = 0.0
+    cond /= cond.sum()
+    assert first[cand[0]] == 0
+    m = cond > 0
+    chi2 = ((first[m] - n0 * cond[m]) ** 2 / (n0 * cond[m])).sum()
+    assert chi2 < 25.0                                    # V - 2 dof
+
+
+def test_match_uses_its_own_stream():
+    """The target samples come from tag TAG_MATCH at position pos + j + 1 and
+    differ from the bonus stream of sampling verification."""
+    V = 64
+    p = np.full((2, V), 1.0 / V)
+    t = O.verify_match([0], p, 123, 40, 5)["targets"]
+    for j in range(2):
+        u = float(ph.draw(123, 0, 40 + j + 1, 5, ph.TAG_MATCH, 0))
+        assert t[j] == min(int(u * V), V - 1)            # uniform row: floor(u V)
+    assert ph.TAG_MATCH not in (ph.TAG_GUMBEL, ph.TAG_ACCEPT, ph.TAG_RESID, ph.TAG_BONUS)
+
+
 # ---------------------------------------------------------------- cost-model arithmetic
 
 def test_pages_time_model_examples():
