@@ -43,6 +43,19 @@ class Weights(ctypes.Structure):
                [("layer", LayerWeights * MAX_LAYERS)]
 
 
+VERIFY_GREEDY, VERIFY_SAMPLE, VERIFY_MATCH = 0, 1, 2
+
+
+class VerifyArgs(ctypes.Structure):
+    """dlite_verify_args (include/dlite.h)."""
+    _fields_ = [("mode", ctypes.c_int), ("B", ctypes.c_int), ("n_verify", ctypes.c_int),
+                ("candidates", ctypes.c_void_p), ("target_tokens", ctypes.c_void_p),
+                ("qstats", ctypes.c_void_p), ("hs", ctypes.c_void_p), ("target_probs", ctypes.c_void_p),
+                ("temperature", ctypes.c_float), ("seed", ctypes.c_uint64), ("pos", ctypes.c_void_p),
+                ("accepted", ctypes.c_void_p), ("commits", ctypes.c_void_p), ("n_commit", ctypes.c_void_p),
+                ("next_anchor", ctypes.c_void_p)]
+
+
 class Taps(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("z", "x", "b", "hs")]
 
@@ -64,6 +77,7 @@ _SIGS = {
     "dlite_lm_head": (_I, [_P, _I, _P, _F, _U64, _P, _P, _P, _P]),
     "dlite_verify": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P]),
     "dlite_verify_sample": (_I, [_P, _I, _P, _P, _P, _P, _F, _U64, _P, _P, _P, _P, _P, _P]),
+    "dlite_verify_ex": (_I, [_P, ctypes.POINTER(VerifyArgs), _P]),
     "dlite_advance": (_I, [_P, _I, _P, _P, _P]),
     "dlite_verify_sample_static": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _F, _U64, _P, _P, _P,
                                         _P, _P, _P]),
@@ -257,6 +271,18 @@ class Drafter:
                                             _ptr(accepted), _ptr(commits), _ptr(n_commit),
                                             _ptr(next_anchor), _stream(stream)),
                "dlite_verify_sample")
+
+    def verify_ex(self, mode, cand, accepted, commits, n_commit, next_anchor, n_verify=None,
+                  target_tokens=None, qstats=None, hs=None, probs=None, temperature=0.0, seed=0, pos=None,
+                  stream=None):
+        """dlite_verify_ex: greedy / sampling / match verification over the first
+        n_verify candidates (default all K)."""
+        a = VerifyArgs(mode=mode, B=cand.shape[0], n_verify=cand.shape[1] if n_verify is None else n_verify,
+                       candidates=_ptr(cand), target_tokens=_ptr(target_tokens), qstats=_ptr(qstats),
+                       hs=_ptr(hs), target_probs=_ptr(probs), temperature=temperature, seed=seed,
+                       pos=_ptr(pos), accepted=_ptr(accepted), commits=_ptr(commits),
+                       n_commit=_ptr(n_commit), next_anchor=_ptr(next_anchor))
+        _check(self.lib.dlite_verify_ex(self.h, ctypes.byref(a), _stream(stream)), "dlite_verify_ex")
 
     def advance(self, n_commit, pos, stream=None):
         _check(self.lib.dlite_advance(self.h, n_commit.shape[0], _ptr(n_commit), _ptr(pos),

@@ -61,6 +61,7 @@ struct dlite_handle {
   float *part = nullptr, *part2 = nullptr;
   LmRec* lmrec = nullptr;
   unsigned long long* resid = nullptr;
+  int32_t* tsamp = nullptr;                 // [B_max, K+1] the target's samples (match verification)
   unsigned long long* counters = nullptr;
   int Vp = 0;  // V padded to a multiple of 64 (tiled LM-head weight rows)
   int* status = nullptr;
@@ -752,6 +753,7 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
   AL(h->part2, pe2);
   AL(h->lmrec, lme);
   AL(h->resid, (size_t)Bm * V);
+  AL(h->tsamp, (size_t)Bm * (c.K + 1));
   AL(h->counters, 8);
   CK(cudaMemset(h->counters, 0, 8 * sizeof(unsigned long long)));
   AL(h->status, 1);
@@ -914,6 +916,67 @@ int dlite_verify_sample(dlite_handle* h, int B, const int32_t* cand, const dlite
   CK(launch_verify_sample(v, (cudaStream_t)stream));
   mark(h, "verify_sample");
   return DLITE_OK;
+}
+
+int dlite_verify_ex(dlite_handle* h, const dlite_verify_args* a, dlite_stream_t stream) {
+  if (!h || !a) return DLITE_ERR_INVALID_ARG;
+  const dlite_config& c = h->cfg;
+  if (a->B < 1 || a->B > c.B_max || a->n_verify < 0 || a->n_verify > c.K) return DLITE_ERR_INVALID_ARG;
+  if (!a->candidates || !a->accepted || !a->commits || !a->n_commit || !a->next_anchor)
+    return DLITE_ERR_INVALID_ARG;
+  const cudaStream_t s = (cudaStream_t)stream;
+  VerifyArgs v;
+  v.B = a->B;
+  v.K = c.K;
+  v.V = c.V;
+  v.D = c.D;
+  v.kv = a->n_verify;
+  v.cand = a->candidates;
+  v.accepted = a->accepted;
+  v.commits = a->commits;
+  v.n_commit = a->n_commit;
+  v.next_anchor = a->next_anchor;
+  v.status = h->status;
+  switch (a->mode) {
+    case DLITE_VERIFY_GREEDY:
+      if (!a->target_tokens) return DLITE_ERR_INVALID_ARG;
+      v.tgt = a->target_tokens;
+      CK(launch_verify_greedy(v, s));
+      mark(h, "verify_greedy");
+      return DLITE_OK;
+    case DLITE_VERIFY_SAMPLE:
+      if (!a->qstats || !a->target_probs || !a->pos) return DLITE_ERR_INVALID_ARG;
+      if (!(a->temperature > 0.f) || isinf(a->temperature)) return DLITE_ERR_INVALID_ARG;
+      v.qs = a->qstats;
+      v.hs = a->hs ? a->hs : h->hs;
+      v.probs = a->target_probs;
+      if (h->f32)
+        v.Ef = (const float*)h->E_src;
+      else
+        v.Eb = h->E[0];
+      v.resid = h->resid;
+      v.counters = h->counters;
+      v.T = (double)a->temperature;
+      seed_key(a->seed, &v.k0, &v.k1);
+      v.pos = a->pos;
+      CK(launch_verify_sample(v, s));
+      mark(h, "verify_sample");
+      return DLITE_OK;
+    case DLITE_VERIFY_MATCH:
+      if (!a->target_probs || !a->pos) return DLITE_ERR_INVALID_ARG;
+      v.probs = a->target_probs;
+      seed_key(a->seed, &v.k0, &v.k1);
+      v.pos = a->pos;
+      v.tsamp = h->tsamp;
+      CK(launch_match_sample(v, s));
+      mark(h, "match_sample");
+      v.tgt = h->tsamp;  // then greedy verification against the target's samples
+      CK(launch_verify_greedy(v, s));
+      mark(h, "verify_match");
+      return DLITE_OK;
+    default:
+      return DLITE_ERR_INVALID_ARG;
+  }
 }
 
 int dlite_advance(dlite_handle* h, int B, const int32_t* n_commit, int64_t* pos,

@@ -815,13 +815,13 @@ __global__ void verify_greedy_kernel(VerifyArgs a) {
   const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (b >= a.B) return;
-  const int K = a.K;
+  const int K = a.K, KV = a.kv < 0 ? K : a.kv;  // only the first KV candidates are verified
   const int c = (lane < K) ? a.cand[b * K + lane] : 0;
-  const int tk = (lane <= K) ? a.tgt[b * (K + 1) + lane] : 0;
-  const unsigned pass = __ballot_sync(0xffffffffu, lane < K && c == tk);
-  const unsigned kmask = (K >= 32) ? 0xffffffffu : ((1u << K) - 1u);
+  const int tk = (lane <= KV) ? a.tgt[b * (K + 1) + lane] : 0;
+  const unsigned pass = __ballot_sync(0xffffffffu, lane < KV && c == tk);
+  const unsigned kmask = (KV >= 32) ? 0xffffffffu : ((1u << KV) - 1u);
   const unsigned fail = ~pass & kmask;
-  const int A = fail ? (__ffs(fail) - 1) : K;
+  const int A = fail ? (__ffs(fail) - 1) : KV;
   const int tA = __shfl_sync(0xffffffffu, tk, A);
   if (lane <= K) a.commits[b * (K + 1) + lane] = (lane < A) ? c : (lane == A ? tA : -1);
   if (lane == 0) {
@@ -1133,6 +1133,7 @@ __global__ void __launch_bounds__(kVerifyCThreads, 2) verify_sample_kernel(Verif
   __shared__ float qpart[kVerifyCThreads / 32];
   const uint32_t rank = cluster_ctarank();
   const int b = blockIdx.x / kVerifyCluster, K = a.K, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int KV = a.kv < 0 ? K : a.kv;  // only the first KV candidates are verified
   const int nwarps = blockDim.x >> 5;
   const bool lead = rank == 0;
   const double T = a.T;
@@ -1140,7 +1141,7 @@ __global__ void __launch_bounds__(kVerifyCThreads, 2) verify_sample_kernel(Verif
   const float* prow_base = a.probs + (size_t)b * (K + 1) * a.V;
   if (warp == 0) {  // the accept tests (the same in every CTA of the cluster)
     bool acc = false;
-    if (lane < K) {
+    if (lane < KV) {
       int d = a.cand[b * K + lane];
       if (d < 0 || d >= a.V) {
         if (lead) flag_status(a.status, kDevBounds);
@@ -1153,17 +1154,17 @@ __global__ void __launch_bounds__(kVerifyCThreads, 2) verify_sample_kernel(Verif
       acc = u * q < (double)prow_base[(size_t)lane * a.V + d];
     }
     const unsigned pass = __ballot_sync(0xffffffffu, acc);
-    const unsigned kmask = (K >= 32) ? 0xffffffffu : ((1u << K) - 1u);
+    const unsigned kmask = (KV >= 32) ? 0xffffffffu : ((1u << KV) - 1u);
     const unsigned fail = ~pass & kmask;
-    if (lane == 0) sA = fail ? (__ffs(fail) - 1) : K;
+    if (lane == 0) sA = fail ? (__ffs(fail) - 1) : KV;
   }
   __syncthreads();
   const int A = sA;
   const float* prow = prow_base + (size_t)A * a.V;
   const RowF32 prow_fix{prow, a.V};
-  if (A == K) {  // every draft token accepted: the bonus token from p_K
+  if (A == KV) {  // every verified draft token accepted: the bonus token from p_KV
     if (threadIdx.x == 0) {
-      xs[0] = philox(0u, pos0 + K + 1, (uint32_t)b, kTagBonus, a.k0, a.k1).x;
+      xs[0] = philox(0u, pos0 + KV + 1, (uint32_t)b, kTagBonus, a.k0, a.k1).x;
       if (lead && a.counters) atomicAdd(a.counters + 3, 1ull);
     }
     __syncthreads();
@@ -1269,6 +1270,49 @@ cudaError_t launch_verify_sample(const VerifyArgs& a, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, verify_sample_kernel, a);
+}
+
+constexpr uint32_t kTagMatch = 5;  // Philox tag of the target's own samples (match verification)
+
+// Match verification, step 1: the target's own sample at input index j of
+// request b (its choice for position j + 1), for j = 0..kv: inverse CDF over
+// p_j with the uniform of Philox(0, pos + j + 1, b, kTagMatch) word 0, one
+// 8-CTA cluster per (request, index) (the same exact fixed-point inverse CDF as
+// the sampling verification).
+__global__ void __launch_bounds__(kVerifyCThreads, 2) match_sample_kernel(VerifyArgs a) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ unsigned long long incl[kSegsPerCta];
+  __shared__ unsigned long long tot[kVerifyCluster];
+  __shared__ uint32_t xs[1];
+  __shared__ int sv[1];
+  const uint32_t rank = cluster_ctarank();
+  const int K = a.K, KV = a.kv < 0 ? K : a.kv;
+  const int item = blockIdx.x / kVerifyCluster, b = item / (KV + 1), j = item % (KV + 1);
+  const uint32_t pos0 = (uint32_t)a.pos[b];
+  if (threadIdx.x == 0) xs[0] = philox(0u, pos0 + j + 1, (uint32_t)b, kTagMatch, a.k0, a.k1).x;
+  __syncthreads();
+  const RowF32 prow{a.probs + ((size_t)b * (K + 1) + j) * a.V, a.V};
+  cluster_icdf(prow, a.V, xs, 1, sv, incl, tot, rank);
+  if (rank == 0 && threadIdx.x == 0) a.tsamp[b * (K + 1) + j] = sv[0];
+}
+
+cudaError_t launch_match_sample(const VerifyArgs& a, cudaStream_t s) {
+  const int KV = a.kv < 0 ? a.K : a.kv;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.B * (KV + 1) * kVerifyCluster);
+  cfg.blockDim = dim3(kVerifyCThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = kVerifyCluster;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, match_sample_kernel, a);
 }
 
 __global__ void advance_kernel(int B, const int32_t* n_commit, int64_t* pos) {

@@ -90,6 +90,8 @@ struct VerifyArgs {
   int32_t* n_commit = nullptr;
   int32_t* next_anchor = nullptr;
   int* status = nullptr;
+  int kv = -1;                         // candidates verified (the first kv of K; -1: all K)
+  int32_t* tsamp = nullptr;            // match mode: the target's samples [B, K+1]
 };
 
 cudaError_t launch_stage(const StageArgs& a, bool f32, cudaStream_t s);
@@ -107,6 +109,9 @@ cudaError_t launch_head_out(const float* part, int S, int rows, int D, const flo
 cudaError_t launch_split(const float* src, size_t n, bf16* const* pl, float* copy, cudaStream_t s);
 cudaError_t launch_verify_greedy(const VerifyArgs& a, cudaStream_t s);
 cudaError_t launch_verify_sample(const VerifyArgs& a, cudaStream_t s);
+// match mode, step 1: the target's own samples t_j ~ p_j for j = 0..kv into a.tsamp
+// (step 2 is launch_verify_greedy with a.tgt = a.tsamp)
+cudaError_t launch_match_sample(const VerifyArgs& a, cudaStream_t s);
 cudaError_t launch_advance(int B, const int32_t* n_commit, int64_t* pos, cudaStream_t s);
 cudaError_t launch_repack(const void* src, bool src_f32, int rows, int cols, int src_ld,
                           int src_off, bf16* p0, bf16* p1, int np, float* f32, int dst_ld,

@@ -188,6 +188,43 @@ int dlite_verify_sample(dlite_handle *h, int B, const int32_t *candidates,
                         int32_t *commits, int32_t *n_commit, int32_t *next_anchor,
                         dlite_stream_t stream);
 
+/* Verification with a window and a choice of rule ([P1] §"草稿块长与验证块长不是
+ * 一个参数": the verification window counts the anchor and may be shorter than
+ * the drafted block, which is then truncated; §"贪心模式与随机模式要分别说明":
+ * the official `match` mode).
+ *   mode      DLITE_VERIFY_GREEDY: as dlite_verify (target_tokens)
+ *             DLITE_VERIFY_SAMPLE: as dlite_verify_sample (qstats, hs, target_probs,
+ *                                  temperature, seed, pos)
+ *             DLITE_VERIFY_MATCH:  the candidates (the draft's greedy choices) against
+ *                                  the target's own samples t_j ~ p_j: t_j = inverse CDF of
+ *                                  target_probs[b, j] at u = Philox(seed, request b, position
+ *                                  pos[b]+j+1, tag 5); A = leading run of d_{j+1} == t_j,
+ *                                  commits d_1..d_A then t_A (target_probs, seed, pos)
+ *   n_verify  candidates handed to verification, 0..K (K: all); the rest are dropped:
+ *             A <= n_verify and the token after the verified prefix comes from index
+ *             A (sampling: the bonus from p_{n_verify} at position pos[b]+n_verify+1)
+ * Outputs as dlite_verify (commits [B, K+1], entries past A set to -1). Fields a mode
+ * does not use may be NULL / 0. Match mode keeps its samples in handle workspace;
+ * everything is stream-ordered and allocation-free (graph-capturable).
+ * Errors: INVALID_ARG for a NULL the mode needs, B outside [1, B_max], n_verify
+ * outside [0, K] or an unknown mode. */
+enum dlite_verify_mode { DLITE_VERIFY_GREEDY = 0, DLITE_VERIFY_SAMPLE = 1, DLITE_VERIFY_MATCH = 2 };
+typedef struct {
+    int mode;                       /* dlite_verify_mode */
+    int B;
+    int n_verify;
+    const int32_t *candidates;      /* [B, K] */
+    const int32_t *target_tokens;   /* [B, K+1], GREEDY */
+    const dlite_qstats *qstats;     /* [B, K], SAMPLE */
+    const float *hs;                /* [B, K, D] or NULL, SAMPLE */
+    const float *target_probs;      /* [B, K+1, V], SAMPLE and MATCH */
+    float temperature;              /* SAMPLE */
+    uint64_t seed;                  /* SAMPLE and MATCH */
+    const int64_t *pos;             /* [B], SAMPLE and MATCH */
+    int32_t *accepted, *commits, *n_commit, *next_anchor;
+} dlite_verify_args;
+int dlite_verify_ex(dlite_handle *h, const dlite_verify_args *args, dlite_stream_t stream);
+
 /* Allocation-free sampling verification (no counterpart on the method's pages;
  * a library convenience). Same computation and outputs as dlite_verify_sample,
  * without a handle and without allocating: for callers that cannot allocate

@@ -321,6 +321,110 @@ def test_verify_sample_preserves_target_distribution(small_v):
     assert abs(acc1 - beta) < 5 * np.sqrt(beta * (1 - beta) / N)
 
 
+# ---------------------------------------------------------------- verification window and match mode
+
+def _t(x, dtype=None):
+    x = np.asarray(x)
+    return torch.from_numpy(x.astype(dtype) if dtype else x).to(DEV)
+
+
+@pytest.mark.parametrize("n_verify", [0, 1, 2, 3])
+def test_verify_window_identical_inputs(small_v, n_verify):
+    """dlite_verify_ex with a verification window: greedy and sampling bit-exact
+    against the oracle's truncated rounds (n_verify = K is the full round)."""
+    cfg, W, dr = small_v
+    B, T, seed = 1024, 0.7, 3
+    rng = np.random.default_rng(50 + n_verify)
+    C = rng.integers(0, 3, size=(B, cfg.K)).astype(np.int32)
+    Tt = rng.integers(0, 3, size=(B, cfg.K + 1)).astype(np.int32)
+    out = dr.new_outputs(B, DEV)
+    dr.verify_ex(binding.VERIFY_GREEDY, _t(C), out["accepted"], out["commits"], out["n_commit"],
+                 out["next_anchor"], n_verify=n_verify, target_tokens=_t(Tt))
+    torch.cuda.synchronize()
+    acc, com = out["accepted"].cpu().numpy(), out["commits"].cpu().numpy()
+    for b in range(B):
+        r = O.verify_greedy(C[b], Tt[b], n_verify=n_verify)
+        assert acc[b] == r["A"] and list(com[b, :r["n_commit"]]) == r["commits"]
+        assert all(com[b, r["n_commit"]:] == -1)
+    hs, cand, logit_d, lse, p, pos = _sample_inputs(cfg, W, B, 60 + n_verify, 0.6)
+    qs = np.stack([logit_d, lse], axis=-1)
+    out = dr.new_outputs(B, DEV)
+    dr.verify_ex(binding.VERIFY_SAMPLE, _t(cand, np.int32), out["accepted"], out["commits"], out["n_commit"],
+                 out["next_anchor"], n_verify=n_verify, qstats=_t(qs), hs=_t(hs), probs=_t(p),
+                 temperature=T, seed=seed, pos=_t(pos))
+    torch.cuda.synchronize()
+    acc, com = out["accepted"].cpu().numpy(), out["commits"].cpu().numpy()
+    for b in range(B):
+        r = O.verify_sample(cand[b], logit_d[b], lse[b], hs[b], W["E"], p[b], T, seed, int(pos[b]), b,
+                            n_verify=n_verify)
+        assert acc[b] == r["A"] <= n_verify, (b, acc[b], r)
+        assert list(com[b, :r["n_commit"]]) == r["commits"], (b, com[b], r)
+    assert np.array_equal(out["next_anchor"].cpu().numpy(), com[np.arange(B), acc])
+
+
+def _match_inputs(cfg, B, seed, agree):
+    """Target rows p_j and greedy candidates that equal the row's mode w.p. agree."""
+    rng = np.random.default_rng(seed)
+    p = rng.dirichlet(np.ones(cfg.V) * 0.3, size=(B, cfg.K + 1)).astype(np.float32)
+    mode = np.argmax(p[:, :cfg.K], axis=2)
+    rand = rng.integers(0, cfg.V, size=(B, cfg.K))
+    cand = np.where(rng.random((B, cfg.K)) < agree, mode, rand).astype(np.int32)
+    pos = rng.integers(0, 1 << 20, B)
+    return cand, p, pos
+
+
+@pytest.mark.parametrize("n_verify", [None, 1, 0])
+def test_verify_match_identical_inputs(small_v, n_verify):
+    """Match verification (the target's own samples, Philox tag 5): A, commits and
+    the next anchor bit-exact against the oracle, for several windows."""
+    cfg, W, dr = small_v
+    B, seed = 2048, 11
+    cand, p, pos = _match_inputs(cfg, B, 70, 0.8)
+    out = dr.new_outputs(B, DEV)
+    dr.verify_ex(binding.VERIFY_MATCH, _t(cand), out["accepted"], out["commits"], out["n_commit"],
+                 out["next_anchor"], n_verify=n_verify, probs=_t(p), seed=seed, pos=_t(pos))
+    torch.cuda.synchronize()
+    acc, com = out["accepted"].cpu().numpy(), out["commits"].cpu().numpy()
+    hist = np.zeros(cfg.K + 1, dtype=np.int64)
+    for b in range(B):
+        r = O.verify_match(cand[b], p[b], seed, int(pos[b]), b, n_verify=n_verify)
+        hist[r["A"]] += 1
+        assert acc[b] == r["A"], (b, acc[b], r)
+        assert list(com[b, :r["n_commit"]]) == r["commits"], (b, com[b], r)
+    assert np.array_equal(out["n_commit"].cpu().numpy(), acc + 1)
+    kv = cfg.K if n_verify is None else n_verify
+    assert hist[kv] > 0 and (kv == 0 or hist[0] > 0)        # both ends of the range occur
+
+
+def test_verify_match_large_vocabulary(midvocab):
+    """Match verification over a 100k vocabulary (multi-segment inverse CDF in
+    every CTA of the cluster), against the oracle."""
+    cfg, W, dr = midvocab
+    B, seed = 16, 5
+    cand, p, pos = _match_inputs(cfg, B, 71, 0.9)
+    out = dr.new_outputs(B, DEV)
+    dr.verify_ex(binding.VERIFY_MATCH, _t(cand), out["accepted"], out["commits"], out["n_commit"],
+                 out["next_anchor"], probs=_t(p), seed=seed, pos=_t(pos))
+    torch.cuda.synchronize()
+    acc, com = out["accepted"].cpu().numpy(), out["commits"].cpu().numpy()
+    for b in range(B):
+        r = O.verify_match(cand[b], p[b], seed, int(pos[b]), b)
+        assert acc[b] == r["A"] and list(com[b, :r["n_commit"]]) == r["commits"], (b, r)
+
+
+def test_verify_ex_rejects_bad_arguments(small_v):
+    cfg, W, dr = small_v
+    cand = torch.zeros(4, cfg.K, dtype=torch.int32, device=DEV)
+    out = dr.new_outputs(4, DEV)
+    for kw in (dict(n_verify=cfg.K + 1, target_tokens=cand), dict(n_verify=-1, target_tokens=cand),
+               dict(target_tokens=None)):
+        with pytest.raises(RuntimeError):
+            dr.verify_ex(binding.VERIFY_GREEDY, cand, out["accepted"], out["commits"], out["n_commit"],
+                         out["next_anchor"], **kw)
+    with pytest.raises(RuntimeError):
+        dr.verify_ex(7, cand, out["accepted"], out["commits"], out["n_commit"], out["next_anchor"])
+
+
 # ---------------------------------------------------------------- invariants and robustness
 
 def test_history_free_and_deterministic(tiny):
