@@ -149,9 +149,15 @@ def run_gpu(args):
     wl = wk.WORKLOADS[args.workload]
     if args.batch:
         wl = dataclasses.replace(wl, B=args.batch, name=f"{wl.name}-B{args.batch}")
+    match = args.verify == "match"
+    nv = None if args.n_verify < 0 else args.n_verify
+    if match:   # greedy draft against the target's own samples at the workload's temperature
+        wl = dataclasses.replace(wl, name=f"{wl.name}-match")
+    if nv is not None:
+        wl = dataclasses.replace(wl, name=f"{wl.name}-nv{nv}")
     cfg = wl.cfg
     B = wl.B
-    T = wl.temperature
+    T = 0.0 if match else wl.temperature
     sampling = T > 0
 
     W = wk.make_weights(cfg, wl.weight_seed, device=dev)
@@ -161,7 +167,7 @@ def run_gpu(args):
     for k in range(RING):
         hidden, anchor, pos = wk.make_round_inputs(wl, round_index=k + 1000 * rank, device=dev)
         item = {"hidden": hidden}
-        if sampling:
+        if sampling or match:
             item["probs"] = wk.make_target_probs(B, cfg.K, cfg.V, wl.rng_seed + 17 * k + 1000 * rank,
                                                  device=dev)
         ring.append(item)
@@ -175,7 +181,16 @@ def run_gpu(args):
         it = ring[k]
         dr.draft_round(it["hidden"], anchor, T, wl.rng_seed, pos, out["cand"], out["qstats"],
                        stream=stream)
-        if sampling:
+        if match:
+            dr.verify_ex(binding.VERIFY_MATCH, out["cand"], out["accepted"], out["commits"], out["n_commit"],
+                         anchor, n_verify=nv, probs=it["probs"], seed=wl.rng_seed, pos=pos, stream=stream)
+        elif nv is not None:
+            dr.verify_ex(binding.VERIFY_SAMPLE if sampling else binding.VERIFY_GREEDY, out["cand"],
+                         out["accepted"], out["commits"], out["n_commit"], anchor, n_verify=nv,
+                         target_tokens=None if sampling else tgt, qstats=out["qstats"] if sampling else None,
+                         probs=it.get("probs") if sampling else None, temperature=T, seed=wl.rng_seed,
+                         pos=pos, stream=stream)
+        elif sampling:
             dr.verify_sample(out["cand"], out["qstats"], None, it["probs"], T, wl.rng_seed, pos,
                              out["accepted"], out["commits"], out["n_commit"], anchor, stream=stream)
         else:
@@ -194,7 +209,7 @@ def run_gpu(args):
             with torch.cuda.graph(g, stream=stream):
                 enqueue(k)
         graphs.append(g)
-    launches_per_step = dr.launch_count(B, T) + 1   # + the position bookkeeping kernel
+    launches_per_step = dr.launch_count(B, T) + 1 + (1 if match else 0)  # + position update (+ match samples)
 
     ncommit_total = torch.zeros((), dtype=torch.int64, device=dev)
     with torch.cuda.stream(stream):
@@ -286,7 +301,7 @@ def run_gpu(args):
 
     # ---- end to end through the public host-buffer call
     e2e = None
-    if rank == 0 or ws > 1:
+    if (rank == 0 or ws > 1) and not match and nv is None:   # the host-buffer call runs the default verification
         e2e = run_e2e(dr, wl, ring, anchor, pos, stream, max(3, min(args.steps, 20)))
 
     result = {
@@ -453,6 +468,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clock-sampler", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (exploration)")
+    ap.add_argument("--verify", default="default", choices=["default", "match"],
+                    help="match: greedy draft verified against the target's own samples")
+    ap.add_argument("--n-verify", type=int, default=-1, help="verification window (candidates verified; -1: all)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -1025,12 +1025,12 @@ __device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
 // threshold resolves it and writes the id into out[j] of cluster rank 0.
 // xs (nthr <= 32 words) must be identical in every CTA. Returns S. Must be
 // called by every thread of every CTA of the cluster.
-template <typename Row>
+template <typename Row, int kC = kVerifyCluster>  // kC CTAs in the cluster
 __device__ unsigned long long cluster_icdf(const Row& row, int V, const uint32_t* xs, int nthr, int* out,
                                            unsigned long long* incl, unsigned long long* tot, uint32_t rank) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const int nseg = (V + kSeg - 1) / kSeg;
-  const int s0 = (int)rank * nseg / kVerifyCluster, s1 = ((int)rank + 1) * nseg / kVerifyCluster;
+  const int s0 = (int)rank * nseg / kC, s1 = ((int)rank + 1) * nseg / kC;
   const int ns = s1 - s0;
   // 1) segment sums of this CTA's range: one warp per segment, the raw loads
   //    of several segments in flight before any is converted
@@ -1068,12 +1068,12 @@ __device__ unsigned long long cluster_icdf(const Row& row, int V, const uint32_t
       if (i < ns) incl[i] = v + carry;
       carry += __shfl_sync(0xffffffffu, v, 31);
     }
-    if (lane < kVerifyCluster) st_cluster_u64(cluster_addr(tot + rank, (uint32_t)lane), carry);
+    if (lane < kC) st_cluster_u64(cluster_addr(tot + rank, (uint32_t)lane), carry);
   }
   cluster_sync_all();
   unsigned long long S = 0, off = 0;
 #pragma unroll
-  for (int r = 0; r < kVerifyCluster; ++r) {
+  for (int r = 0; r < kC; ++r) {
     if (r < (int)rank) off += tot[r];
     S += tot[r];
   }
@@ -1277,42 +1277,52 @@ constexpr uint32_t kTagMatch = 5;  // Philox tag of the target's own samples (ma
 // Match verification, step 1: the target's own sample at input index j of
 // request b (its choice for position j + 1), for j = 0..kv: inverse CDF over
 // p_j with the uniform of Philox(0, pos + j + 1, b, kTagMatch) word 0, one
-// 8-CTA cluster per (request, index) (the same exact fixed-point inverse CDF as
-// the sampling verification).
+// cluster of 1-8 CTAs per (request, index) (the same exact fixed-point inverse
+// CDF as the sampling verification).
+template <int kC>  // CTAs per cluster: fewer when many rows are sampled (one wave)
 __global__ void __launch_bounds__(kVerifyCThreads, 2) match_sample_kernel(VerifyArgs a) {
   pdl_trigger();
   pdl_wait();
-  __shared__ unsigned long long incl[kSegsPerCta];
-  __shared__ unsigned long long tot[kVerifyCluster];
+  __shared__ unsigned long long incl[kMaxSegs / kC];
+  __shared__ unsigned long long tot[kC];
   __shared__ uint32_t xs[1];
   __shared__ int sv[1];
   const uint32_t rank = cluster_ctarank();
   const int K = a.K, KV = a.kv < 0 ? K : a.kv;
-  const int item = blockIdx.x / kVerifyCluster, b = item / (KV + 1), j = item % (KV + 1);
+  const int item = blockIdx.x / kC, b = item / (KV + 1), j = item % (KV + 1);
   const uint32_t pos0 = (uint32_t)a.pos[b];
   if (threadIdx.x == 0) xs[0] = philox(0u, pos0 + j + 1, (uint32_t)b, kTagMatch, a.k0, a.k1).x;
   __syncthreads();
   const RowF32 prow{a.probs + ((size_t)b * (K + 1) + j) * a.V, a.V};
-  cluster_icdf(prow, a.V, xs, 1, sv, incl, tot, rank);
+  cluster_icdf<RowF32, kC>(prow, a.V, xs, 1, sv, incl, tot, rank);
   if (rank == 0 && threadIdx.x == 0) a.tsamp[b * (K + 1) + j] = sv[0];
 }
 
-cudaError_t launch_match_sample(const VerifyArgs& a, cudaStream_t s) {
-  const int KV = a.kv < 0 ? a.K : a.kv;
+template <int kC>
+static cudaError_t launch_match_c(const VerifyArgs& a, int items, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.B * (KV + 1) * kVerifyCluster);
+  cfg.gridDim = dim3(items * kC);
   cfg.blockDim = dim3(kVerifyCThreads);
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = kVerifyCluster;
+  attr[1].val.clusterDim.x = kC;
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, match_sample_kernel, a);
+  return cudaLaunchKernelEx(&cfg, match_sample_kernel<kC>, a);
+}
+
+cudaError_t launch_match_sample(const VerifyArgs& a, cudaStream_t s) {
+  const int items = a.B * ((a.kv < 0 ? a.K : a.kv) + 1);  // (request, index) rows to sample
+  // the largest cluster that keeps every row in one wave (two CTAs per SM)
+  if (items * 8 <= 2 * 152) return launch_match_c<8>(a, items, s);
+  if (items * 4 <= 2 * 152) return launch_match_c<4>(a, items, s);
+  if (items * 2 <= 2 * 152) return launch_match_c<2>(a, items, s);
+  return launch_match_c<1>(a, items, s);
 }
 
 __global__ void advance_kernel(int B, const int32_t* n_commit, int64_t* pos) {

@@ -396,11 +396,12 @@ def test_verify_match_identical_inputs(small_v, n_verify):
     assert hist[kv] > 0 and (kv == 0 or hist[0] > 0)        # both ends of the range occur
 
 
-def test_verify_match_large_vocabulary(midvocab):
+@pytest.mark.parametrize("B", [1, 8, 16, 40])   # clusters of 8, 4, 2 and 1 CTAs per sampled row
+def test_verify_match_large_vocabulary(midvocab, B):
     """Match verification over a 100k vocabulary (multi-segment inverse CDF in
-    every CTA of the cluster), against the oracle."""
+    every CTA of the cluster, for each cluster size), against the oracle."""
     cfg, W, dr = midvocab
-    B, seed = 16, 5
+    seed = 5
     cand, p, pos = _match_inputs(cfg, B, 71, 0.9)
     out = dr.new_outputs(B, DEV)
     dr.verify_ex(binding.VERIFY_MATCH, _t(cand), out["accepted"], out["commits"], out["n_commit"],
