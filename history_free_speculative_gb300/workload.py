@@ -31,6 +31,7 @@ class DraftConfig:
     dtype: str      # "f32" or "bf16" (weights, hidden inputs)
     eps: float = 1e-6
     theta: float = 1e6
+    G: int = 1      # local token group ending at the anchor (local positions 0..G-1)
 
     @property
     def torch_dtype(self):

@@ -123,6 +123,14 @@ def silu(x):
 
 # ---------------------------------------------------------------- the drafter
 
+def anchor_group(anchor, cfg):
+    """The request's local token group: G token ids ending at the anchor."""
+    g = [int(t) for t in np.atleast_1d(np.asarray(anchor))]
+    if len(g) != cfg.G:
+        raise ValueError("the anchor group holds G = %d tokens" % cfg.G)
+    return g
+
+
 def stage(hidden, anchor, W, cfg, mirror=False):
     """Depth-embedding staging and the local rows of one request.
 
@@ -130,26 +138,33 @@ def stage(hidden, anchor, W, cfg, mirror=False):
     ([P1] §"History-Free 到底省掉了什么", eq. z_t = h_t + e_depth, "官方实现还
     会对相加后的特征做归一化"). Local rows: x_0 = E[anchor] (tied embedding),
     x_i = e_ph for the K placeholders ([P1] §"锚点是已经确定...").
-    Returns z [m, D] and the fp32-class residual stream x [K+1, D].
+    With a local token group of G tokens ending at the anchor ([P1]
+    §"局部位置编码切断草稿端的全局位置增长": build_block_position_ids takes a
+    fixed-length local group, its start the origin) the first G rows are the
+    group's embeddings and the K placeholders follow.
+    Returns z [m, D] and the fp32-class residual stream x [G+K, D].
     """
     h = f64(hidden)                                          # [m, D]
     z = _r(rmsnorm(h + f64(W["e_depth"]), W["g_stage"], cfg.eps), mirror)
-    D, K = cfg.D, cfg.K
-    x = np.empty((K + 1, D))
-    x[0] = f64(W["E"][int(anchor)])
-    x[1:] = f64(W["e_ph"])[None, :]
+    D, K, G = cfg.D, cfg.K, cfg.G
+    group = anchor_group(anchor, cfg)
+    x = np.empty((G + K, D))
+    for i, t in enumerate(group):
+        x[i] = f64(W["E"][t])
+    x[G:] = f64(W["e_ph"])[None, :]
     return z, x
 
 
 def backbone_layer(x, z, Wl, cfg, mirror=False):
-    """One pre-norm block over [m context slots | anchor | K placeholders].
+    """One pre-norm block over [m context slots | anchor group | K placeholders].
 
     Queries exist only for the anchor and placeholders; keys/values for the
     context slots and the local rows ([P1] §"本轮临时 K/V 仍然需要计算").
     Context slots are K/V-only rows projected from z with no extra norm and
-    sit at local position 0, where RoPE is the identity.
+    sit at local position 0, where RoPE is the identity; the group rows sit at
+    0..G-1 (its start is the origin) and placeholder i at G-1+i.
     """
-    K1 = cfg.K + 1
+    K1 = cfg.G + cfg.K
     n_q, n_kv, d_h = cfg.n_q, cfg.n_kv, cfg.d_h
     y = _r(rmsnorm(x, Wl["g_attn"], cfg.eps), mirror)
     pos = np.arange(K1)
@@ -184,7 +199,7 @@ def backbone(hidden, anchor, W, cfg, mirror=False, taps=None):
         x = backbone_layer(x, z, Wl, cfg, mirror)
         if taps is not None:
             taps["x"].append(x.copy())
-    return rmsnorm(x[1:], W["g_final"], cfg.eps)
+    return rmsnorm(x[cfg.G:], W["g_final"], cfg.eps)
 
 
 def sequential_head(b, Q, P):

@@ -211,6 +211,63 @@ def test_staging_closed_form():
     assert all(np.array_equal(x[i], O.f64(W["e_ph"])) for i in range(1, cfg.K + 1))
 
 
+# ---------------------------------------------------------------- local token group
+
+def test_group_staging_layout():
+    """G tokens ending at the anchor fill the first G local rows (tied E rows),
+    the K placeholders follow; G = 1 with a list equals the scalar anchor."""
+    cfg = _tiny(G=3)
+    W = _weights(cfg)
+    hidden, _, _ = wk.make_round_inputs(wk.WORKLOADS["tiny"], B=1)
+    group = [5, 17, 3]
+    z, x = O.stage(hidden[0], group, W, cfg)
+    assert x.shape == (cfg.G + cfg.K, cfg.D)
+    for i, t in enumerate(group):
+        assert np.array_equal(x[i], O.f64(W["E"][t]))
+    assert all(np.array_equal(x[i], O.f64(W["e_ph"])) for i in range(cfg.G, cfg.G + cfg.K))
+    c1 = _tiny()
+    W1 = _weights(c1)
+    assert np.array_equal(O.backbone(hidden[0], [7], W1, c1), O.backbone(hidden[0], 7, W1, c1))
+    with pytest.raises(ValueError):
+        O.stage(hidden[0], [1, 2], W, cfg)
+
+
+def test_group_positions_follow_the_group():
+    """Local rows that enter with identical inputs differ only by their RoPE
+    positions. With every group token's embedding equal to e_ph, a G = 2 block
+    of K = 3 placeholders and a G = 1 block of K = 4 placeholders hold the same
+    5 identical rows at positions 0..4, so the last three outputs agree; a
+    slip in the positions (placeholders restarting at 1, say) breaks this."""
+    c2, c1 = _tiny(G=2, K=3), _tiny(G=1, K=4)
+    W = _weights(c2)
+    W = dict(W)
+    E = W["E"].clone()
+    E[[11, 12]] = W["e_ph"]
+    W["E"] = E
+    hidden, _, _ = wk.make_round_inputs(wk.WORKLOADS["tiny"], B=1)
+    b2 = O.backbone(hidden[0], [11, 12], W, c2)
+    b1 = O.backbone(hidden[0], 11, W, c1)
+    assert np.allclose(b2, b1[1:], rtol=0, atol=1e-12)
+    assert not np.allclose(b1[0], b1[1], atol=1e-6)        # positions do matter
+
+
+def test_group_zero_blocks_closed_form_and_dependence():
+    """With zero output projections (Wo = Wd = 0) the residual stream keeps its
+    staged rows, so every placeholder's b is RMSNorm(e_ph) g_final whatever the
+    group; with the real weights the group's first token changes the outputs."""
+    cfg = _tiny(G=2)
+    W = _weights(cfg, jitter=True)
+    hidden, _, _ = wk.make_round_inputs(wk.WORKLOADS["tiny"], B=1)
+    Wz = dict(W)
+    Wz["layers"] = [dict(l, Wo=np.zeros_like(l["Wo"]), Wd=np.zeros_like(l["Wd"])) for l in W["layers"]]
+    e = O.f64(W["e_ph"])
+    want = O.f64(W["g_final"]) * e / math.sqrt(float(e @ e) / cfg.D + cfg.eps)
+    for group in ([1, 2], [300, 9]):
+        b = O.backbone(hidden[0], group, Wz, cfg)
+        assert np.allclose(b, want[None, :], atol=1e-12)
+    assert not np.allclose(O.backbone(hidden[0], [1, 2], W, cfg), O.backbone(hidden[0], [3, 2], W, cfg))
+
+
 # ---------------------------------------------------------------- sequential head
 
 def test_head_with_zero_P_is_identity():
