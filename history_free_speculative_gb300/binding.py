@@ -30,7 +30,7 @@ class DliteError(RuntimeError):
 class Config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
                 ("B_max", "D", "m", "K", "L_D", "n_q", "n_kv", "d_h", "F", "R", "V", "dtype")] + \
-               [("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float)]
+               [("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float), ("anchor_group", ctypes.c_int)]
 
 
 class LayerWeights(ctypes.Structure):
@@ -79,6 +79,7 @@ _SIGS = {
     "dlite_verify_sample": (_I, [_P, _I, _P, _P, _P, _P, _F, _U64, _P, _P, _P, _P, _P, _P]),
     "dlite_verify_ex": (_I, [_P, ctypes.POINTER(VerifyArgs), _P]),
     "dlite_advance": (_I, [_P, _I, _P, _P, _P]),
+    "dlite_shift_group": (_I, [_P, _I, _P, _P, _P, _P]),
     "dlite_verify_sample_static": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _F, _U64, _P, _P, _P,
                                         _P, _P, _P]),
     "dlite_round_host": (_I, [_P, _I, _P, _P, _P, _P, _P, _F, _U64, _P, _P, _P, _P, _P]),
@@ -185,7 +186,7 @@ def config_struct(cfg, B_max):
     return Config(B_max=B_max, D=cfg.D, m=cfg.m, K=cfg.K, L_D=cfg.L_D, n_q=cfg.n_q,
                   n_kv=cfg.n_kv, d_h=cfg.d_h, F=cfg.F, R=cfg.R, V=cfg.V,
                   dtype=DLITE_F32 if cfg.dtype == "f32" else DLITE_BF16,
-                  rms_eps=cfg.eps, rope_theta=cfg.theta)
+                  rms_eps=cfg.eps, rope_theta=cfg.theta, anchor_group=getattr(cfg, "G", 1))
 
 
 class Drafter:
@@ -283,6 +284,10 @@ class Drafter:
                        pos=_ptr(pos), accepted=_ptr(accepted), commits=_ptr(commits),
                        n_commit=_ptr(n_commit), next_anchor=_ptr(next_anchor))
         _check(self.lib.dlite_verify_ex(self.h, ctypes.byref(a), _stream(stream)), "dlite_verify_ex")
+
+    def shift_group(self, commits, n_commit, group, stream=None):
+        _check(self.lib.dlite_shift_group(self.h, n_commit.shape[0], _ptr(commits), _ptr(n_commit), _ptr(group),
+                                          _stream(stream)), "dlite_shift_group")
 
     def advance(self, n_commit, pos, stream=None):
         _check(self.lib.dlite_advance(self.h, n_commit.shape[0], _ptr(n_commit), _ptr(pos),

@@ -118,10 +118,14 @@ int alloc(dlite_handle* h, T** p, size_t n) {
     if (r_) return r_;                      \
   } while (0)
 
+// local token group (anchor_group 0 or 1: the anchor alone)
+static int group_of(const dlite_config* c) { return c->anchor_group > 1 ? c->anchor_group : 1; }
+
 int check_config(const dlite_config* c) {
   if (!c) return DLITE_ERR_INVALID_ARG;
   if (c->dtype != DLITE_F32 && c->dtype != DLITE_BF16) return DLITE_ERR_INVALID_ARG;
-  if (c->B_max < 1 || c->K < 1 || c->K > 31 || c->m < 1 || c->m + c->K + 1 > 32)
+  if (c->B_max < 1 || c->K < 1 || c->K > 31 || c->m < 1 || c->anchor_group < 0 || c->anchor_group > 8 ||
+      c->m + c->K + group_of(c) > 32)
     return DLITE_ERR_UNSUPPORTED_SHAPE;
   if (c->L_D < 1 || c->L_D > DLITE_MAX_LAYERS) return DLITE_ERR_UNSUPPORTED_SHAPE;
   if (c->n_q < 1 || c->n_kv < 1 || c->n_q % c->n_kv) return DLITE_ERR_UNSUPPORTED_SHAPE;
@@ -130,7 +134,8 @@ int check_config(const dlite_config* c) {
   if (c->D % 64 || c->F % 64 || c->R % 32 || c->R > 512 || c->V < 8 || c->V % 8 || c->V > 262144)
     return DLITE_ERR_UNSUPPORTED_SHAPE;
   if ((c->n_q * c->d_h) % 64) return DLITE_ERR_UNSUPPORTED_SHAPE;
-  if (attention_smem(c->K, c->m, c->d_h, c->n_q / c->n_kv) > 200 * 1024) return DLITE_ERR_UNSUPPORTED_SHAPE;
+  if (attention_smem(group_of(c) + c->K, c->m, c->d_h, c->n_q / c->n_kv) > 200 * 1024)
+    return DLITE_ERR_UNSUPPORTED_SHAPE;
   if (c->R < 32 || chain_smem_bytes(c->R, c->K, chain_group_size(c->R, c->B_max)) > 200 * 1024)
     return DLITE_ERR_UNSUPPORTED_SHAPE;
   if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return DLITE_ERR_INVALID_ARG;
@@ -317,7 +322,7 @@ tc::Plan lm_plan(dlite_handle* h, int rows) {
 // the context rows are computed and ignored), one launch instead of two.
 static bool fuse_ctx(const dlite_handle* h, int B) {
   const dlite_config& c = h->cfg;
-  const int rows = B * (c.K + 1) + B * c.m;
+  const int rows = B * (group_of(&c) + c.K) + B * c.m;
   return h->np == 1 && tc::use_stream_engine(rows, 1, 1) &&
          tc::stream_plan(rows, h->qd + 2 * h->kvd, c.D, h->num_sms).ok;
 }
@@ -325,7 +330,7 @@ static bool fuse_ctx(const dlite_handle* h, int B) {
 int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anchor,
                  const dlite_taps* taps, cudaStream_t s) {
   const dlite_config& c = h->cfg;
-  const int L = B * (c.K + 1), C = B * c.m;
+  const int G = group_of(&c), L = B * (G + c.K), C = B * c.m;
   const bool fused_ctx = fuse_ctx(h, B);
   StageArgs st;
   st.hidden = hidden;
@@ -339,6 +344,7 @@ int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anch
   st.B = B;
   st.m = c.m;
   st.K = c.K;
+  st.G = G;
   st.D = c.D;
   st.V = c.V;
   st.eps = c.rms_eps;
@@ -386,6 +392,7 @@ int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anch
     at.B = B;
     at.m = c.m;
     at.K = c.K;
+    at.K1 = G + c.K;
     at.n_q = c.n_q;
     at.n_kv = c.n_kv;
     at.d_h = c.d_h;
@@ -432,7 +439,8 @@ int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anch
     } else {
       r2.g = h->g_final;
       r2.final_mode = 1;
-      r2.K1 = c.K + 1;
+      r2.K1 = G + c.K;
+      r2.G = G;
       r2.bout = h->b;
       r2.bp[0] = h->bp[0];
       r2.bp[1] = h->bp[1];
@@ -676,10 +684,10 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
   }
   AL(h->Mt, (size_t)R * R);
   CK(launch_head_matrix(w->Q, w->P, h->f32, D, R, h->Mt, 0));
-  {  // RoPE table for local positions 0..K (float64 on the host)
-    const int half = c.d_h / 2;
-    std::vector<float> cs((size_t)(c.K + 1) * half), sn((size_t)(c.K + 1) * half);
-    for (int p = 0; p <= c.K; ++p)
+  {  // RoPE table for local positions 0..G+K-1 (float64 on the host)
+    const int half = c.d_h / 2, npos = group_of(&c) + c.K;
+    std::vector<float> cs((size_t)npos * half), sn((size_t)npos * half);
+    for (int p = 0; p < npos; ++p)
       for (int j = 0; j < half; ++j) {
         const double ang = p * pow((double)c.rope_theta, -2.0 * j / c.d_h);
         cs[(size_t)p * half + j] = (float)cos(ang);
@@ -711,7 +719,7 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
   }
   size_t pe = 0, pe2 = 0, lme = 0;
   for (int B = 1; B <= Bm; ++B) {
-    const int L = B * (c.K + 1), C = B * c.m, H = B * c.K;
+    const int L = B * (group_of(&c) + c.K), C = B * c.m, H = B * c.K;
     const int sites[6][4] = {{L, h->qd + 2 * h->kvd, D, h->np}, {L, D, h->qd, h->np},
                              {L, 2 * F, D, h->np},               {L, D, F, h->np},
                              {H, 2 * h->Rp, D, 2},               {H, D, h->Rp, 2}};
@@ -767,7 +775,7 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
     h->allocs.push_back(q);
     h->d_hidden = q;
   }
-  AL(h->d_anchor, Bm);
+  AL(h->d_anchor, (size_t)Bm * group_of(&c));
   AL(h->d_pos, Bm);
   AL(h->d_tgt, (size_t)Bm * (c.K + 1));
   AL(h->d_probs, (size_t)Bm * (c.K + 1) * V);
@@ -796,7 +804,7 @@ int dlite_create(const dlite_config* cfg, const dlite_weights* w, dlite_handle**
   h->kvd = cfg->n_kv * cfg->d_h;
   h->Rp = (cfg->R + 63) / 64 * 64;
   h->Vp = (cfg->V + 63) / 64 * 64;
-  h->Lcap = (cfg->B_max * (cfg->K + 1) + 127) / 128 * 128;
+  h->Lcap = (cfg->B_max * (group_of(cfg) + cfg->K) + 127) / 128 * 128;
   h->Ccap = (cfg->B_max * cfg->m + 127) / 128 * 128;
   h->Hcap = (cfg->B_max * cfg->K + 127) / 128 * 128;
   {
@@ -979,6 +987,13 @@ int dlite_verify_ex(dlite_handle* h, const dlite_verify_args* a, dlite_stream_t 
   }
 }
 
+int dlite_shift_group(dlite_handle* h, int B, const int32_t* commits, const int32_t* n_commit,
+                      int32_t* group, dlite_stream_t stream) {
+  if (!h || !commits || !n_commit || !group || B < 1 || B > h->cfg.B_max) return DLITE_ERR_INVALID_ARG;
+  CK(launch_shift_group(B, group_of(&h->cfg), h->cfg.K + 1, commits, n_commit, group, (cudaStream_t)stream));
+  return DLITE_OK;
+}
+
 int dlite_advance(dlite_handle* h, int B, const int32_t* n_commit, int64_t* pos,
                   dlite_stream_t stream) {
   if (!h || !n_commit || !pos || B < 1 || B > h->cfg.B_max) return DLITE_ERR_INVALID_ARG;
@@ -1000,7 +1015,7 @@ int dlite_round_host(dlite_handle* h, int B, const void* hidden_host, const int3
   cudaStream_t s = (cudaStream_t)stream;
   const size_t hb = (size_t)B * c.m * c.D * (h->f32 ? 4 : 2);
   CK(cudaMemcpyAsync(h->d_hidden, hidden_host, hb, cudaMemcpyHostToDevice, s));
-  CK(cudaMemcpyAsync(h->d_anchor, anchor_host, (size_t)B * 4, cudaMemcpyHostToDevice, s));
+  CK(cudaMemcpyAsync(h->d_anchor, anchor_host, (size_t)B * group_of(&c) * 4, cudaMemcpyHostToDevice, s));
   if (pos_host) CK(cudaMemcpyAsync(h->d_pos, pos_host, (size_t)B * 8, cudaMemcpyHostToDevice, s));
   if (sampling)
     CK(cudaMemcpyAsync(h->d_probs, probs_host, (size_t)B * (c.K + 1) * c.V * 4,
@@ -1167,7 +1182,7 @@ int dlite_launch_count(dlite_handle* h, int B, float temperature) {
   // stage + per layer {qkv, ctx-kv, attention, o, resnorm, gate/up (+ swiglu on the pair
   // engine; the one-CTA engine fuses it), down, resnorm} + head {ce, chain, P, out}
   // + lm {head, merge} + verify
-  const int L = B * (h->cfg.K + 1);
+  const int L = B * (group_of(&h->cfg) + h->cfg.K);
   const bool fused = !tc::use_pair_engine(L, h->np, h->np);
   const int per_layer = (fused ? 8 : 9) - (fuse_ctx(h, B) ? 1 : 0);  // one product for [y; z] when fused
   return 1 + per_layer * h->cfg.L_D + 4 + 2 + 1;

@@ -125,10 +125,10 @@ __global__ void __launch_bounds__(1024) stage_kernel(StageArgs a) {
     }
   } else {
     const int lr = row - nz;
-    const int b = lr / (a.K + 1), i0 = lr % (a.K + 1);
+    const int b = lr / (a.G + a.K), i0 = lr % (a.G + a.K);  // rows 0..G-1: the group, then placeholders
     int tok = 0;
-    if (i0 == 0) {
-      tok = a.anchor[b];
+    if (i0 < a.G) {
+      tok = a.anchor[b * a.G + i0];
       if (tok < 0 || tok >= a.V) {
         if (threadIdx.x == 0) flag_status(a.status, kDevBounds);
         tok = 0;
@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(1024) stage_kernel(StageArgs a) {
     for (int k = 0; k < kRowVec; ++k) {
       const int i = threadIdx.x + k * blockDim.x;
       if (i < n4) {
-        v[k] = (i0 == 0) ? load4(E + (a.E_tiled ? tiled_index(tok, 4 * i, D) : (size_t)tok * D + 4 * i))
+        v[k] = (i0 < a.G) ? load4(E + (a.E_tiled ? tiled_index(tok, 4 * i, D) : (size_t)tok * D + 4 * i))
                          : load4(a.e_ph + 4 * i);
         *reinterpret_cast<float4*>(a.x + (size_t)lr * D + 4 * i) = v[k];
         ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(1024) stage_kernel(StageArgs a) {
 }
 
 cudaError_t launch_stage(const StageArgs& a, bool f32, cudaStream_t s) {
-  const int rows = a.B * a.m + a.B * (a.K + 1);
+  const int rows = a.B * a.m + a.B * (a.G + a.K);
   // few rows: 1024 threads per row; many: 512 (several rows per SM at once)
   const int threads = rows <= 2 * 152 ? 1024 : 512;
   if (a.D / 4 > kRowVec * threads) return cudaErrorInvalidValue;
@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(kAttnThreads, kMinCtas) attention_kernel(AttnA
   pdl_wait();
   extern __shared__ float sm[];
   const int G = a.hq, g = (int)(blockIdx.x * G) / (a.n_q / a.n_kv), h0 = blockIdx.x * G, b = blockIdx.y;
-  const int K1 = a.K + 1, dh = a.d_h, half = dh / 2;
+  const int K1 = a.K1 ? a.K1 : a.K + 1, dh = a.d_h, half = dh / 2;  // local rows (group + placeholders)
   const int qd = a.n_q * dh, kvd = a.n_kv * dh;
   const int ldl = qd + 2 * kvd;               // local partial row width
   const int ldc = a.ldc ? a.ldc : 2 * kvd;     // context partial row width
@@ -381,8 +381,8 @@ __global__ void __launch_bounds__(kAttnThreads, kMinCtas) attention_kernel(AttnA
   }
 }
 
-size_t attention_smem(int K, int m, int d_h, int G) {
-  const int QRp = (G * (K + 1) + 15) / 16 * 16, Tkp = (m + K + 1 + 15) / 16 * 16;
+size_t attention_smem(int K1, int m, int d_h, int G) {  // K1 local rows per request
+  const int QRp = (G * K1 + 15) / 16 * 16, Tkp = (m + K1 + 15) / 16 * 16;
   return ((size_t)(QRp + 2 * Tkp) * (d_h + 4) + (size_t)QRp * 36) * sizeof(float);
 }
 
@@ -394,7 +394,7 @@ int attention_heads_per_cta(int n_q, int n_kv, int B) {
 }
 
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s) {
-  const size_t smem = attention_smem(a.K, a.m, a.d_h, a.hq);
+  const size_t smem = attention_smem(a.K1 ? a.K1 : a.K + 1, a.m, a.d_h, a.hq);
   const dim3 grid(a.n_q / a.hq, a.B);
   const bool many = (int)(grid.x * grid.y) > 152;
   void (*fn)(AttnArgs) = many ? attention_kernel<2, 2> : attention_kernel<4, 1>;
@@ -453,8 +453,8 @@ __global__ void __launch_bounds__(kRowThreads, kMinCtas) resnorm_kernel(ResNormA
   const float inv = rsqrtf(ss / D + a.eps);
   if (a.final_mode) {
     const int b = r / a.K1, i = r % a.K1;
-    if (i == 0) return;
-    const size_t orow = (size_t)(b * (a.K1 - 1) + (i - 1)) * D;
+    if (i < a.G) return;  // the group rows give no output
+    const size_t orow = (size_t)(b * (a.K1 - a.G) + (i - a.G)) * D;
 #pragma unroll
     for (int k = 0; k < kVec; ++k) {
       const int j = i0 + threadIdx.x + k * blockDim.x;
@@ -1334,6 +1334,30 @@ __global__ void advance_kernel(int B, const int32_t* n_commit, int64_t* pos) {
 
 cudaError_t launch_advance(int B, const int32_t* n_commit, int64_t* pos, cudaStream_t s) {
   return launch_pdl(advance_kernel, dim3((B + 127) / 128), dim3(128), 0, s, B, n_commit, pos);
+}
+
+// The next round's local group: the last G tokens of (group ++ commits[0..n_commit-1]).
+__global__ void shift_group_kernel(int B, int G, int K1, const int32_t* commits, const int32_t* n_commit,
+                                   int32_t* group) {
+  pdl_trigger();
+  pdl_wait();
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  const int n = n_commit[b];
+  int32_t* g = group + (size_t)b * G;
+  int32_t old[8];
+  for (int i = 0; i < G; ++i) old[i] = g[i];
+  for (int i = 0; i < G; ++i) {
+    const int src = n + i;  // index into (old ++ commits) of length G + n; keep the last G
+    g[i] = src < G ? old[src] : commits[(size_t)b * K1 + (src - G)];
+  }
+}
+
+cudaError_t launch_shift_group(int B, int G, int K1, const int32_t* commits, const int32_t* n_commit,
+                               int32_t* group, cudaStream_t s) {
+  if (G < 1 || G > 8) return cudaErrorInvalidValue;
+  return launch_pdl(shift_group_kernel, dim3((B + 127) / 128), dim3(128), 0, s, B, G, K1, commits, n_commit,
+                    group);
 }
 
 // ---------------------------------------------------------------- weight preparation

@@ -7,18 +7,18 @@ namespace dlite {
 
 struct StageArgs {
   const void* hidden = nullptr;  // [B, m, D] (f32 or bf16)
-  const int32_t* anchor = nullptr;
+  const int32_t* anchor = nullptr;  // [B, G]: the local token group, the anchor last
   const void* E = nullptr;       // [V, D] in the weight dtype (anchor row lookup)
   int E_tiled = 0;               // E stored in the tiled layout (bf16 weights)
   const float* e_depth = nullptr;
   const float* g_stage = nullptr;
   const float* e_ph = nullptr;
   const float* g_attn0 = nullptr;
-  int B = 0, m = 0, K = 0, D = 0, V = 0;
+  int B = 0, m = 0, K = 0, D = 0, V = 0, G = 1;
   float eps = 1e-6f;
   bf16* z[2] = {nullptr, nullptr};
   int nz = 1;
-  float* x = nullptr;            // [B*(K+1), D]
+  float* x = nullptr;            // [B*(G+K), D]
   bf16* y[2] = {nullptr, nullptr};
   int ny = 1;
   float* tap_z = nullptr;
@@ -35,6 +35,7 @@ struct AttnArgs {
   const float* rope_cos = nullptr;  // [K+1][d_h/2]
   const float* rope_sin = nullptr;
   int B = 0, m = 0, K = 0, n_q = 0, n_kv = 0, d_h = 0;
+  int K1 = 0;  // local rows per request (G + K; 0: K + 1)
   int hq = 1;  // query heads per CTA (divides n_q / n_kv): attention_heads_per_cta
   float scale = 1.f;
   int round_bf16 = 0;
@@ -53,6 +54,7 @@ struct ResNormArgs {
   int ny = 1;
   int final_mode = 0;
   int K1 = 0;                   // rows per request (final mode)
+  int G = 1;                    // leading group rows per request, dropped in final mode
   float* bout = nullptr;        // [B*K, D] (final mode)
   bf16* bp[2] = {nullptr, nullptr};
   float* tap_x = nullptr;
@@ -96,7 +98,7 @@ struct VerifyArgs {
 
 cudaError_t launch_stage(const StageArgs& a, bool f32, cudaStream_t s);
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s);
-size_t attention_smem(int K, int m, int d_h, int G);
+size_t attention_smem(int K1, int m, int d_h, int G);  // K1 local rows per request
 int attention_heads_per_cta(int n_q, int n_kv, int B);
 cudaError_t launch_resnorm(const ResNormArgs& a, cudaStream_t s);
 cudaError_t launch_swiglu_interleaved(const float* part, const Splits& sp, int rows, int F, bf16* const* o, int no,
@@ -113,6 +115,8 @@ cudaError_t launch_verify_sample(const VerifyArgs& a, cudaStream_t s);
 // (step 2 is launch_verify_greedy with a.tgt = a.tsamp)
 cudaError_t launch_match_sample(const VerifyArgs& a, cudaStream_t s);
 cudaError_t launch_advance(int B, const int32_t* n_commit, int64_t* pos, cudaStream_t s);
+cudaError_t launch_shift_group(int B, int G, int K1, const int32_t* commits, const int32_t* n_commit,
+                               int32_t* group, cudaStream_t s);
 cudaError_t launch_repack(const void* src, bool src_f32, int rows, int cols, int src_ld,
                           int src_off, bf16* p0, bf16* p1, int np, float* f32, int dst_ld,
                           cudaStream_t s);

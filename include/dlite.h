@@ -58,7 +58,7 @@ enum dlite_status {
 typedef struct {
     int B_max;        /* largest batch any call will pass */
     int D;            /* hidden width; multiple of 64 */
-    int m;            /* selected target layers (context slots); m + K + 1 <= 32 */
+    int m;            /* selected target layers (context slots); m + K + max(1, anchor_group) <= 32 */
     int K;            /* draft positions, 1..31 */
     int L_D;          /* backbone layers, 1..DLITE_MAX_LAYERS */
     int n_q, n_kv, d_h; /* attention heads; n_q % n_kv == 0; d_h in {64, 128} */
@@ -68,6 +68,12 @@ typedef struct {
     int dtype;        /* DLITE_F32 or DLITE_BF16: type of all weights and of `hidden` */
     float rms_eps;    /* RMSNorm epsilon (1e-6) */
     float rope_theta; /* RoPE base (1e6) */
+    int anchor_group; /* G: local token group ending at the anchor ([P1] §"局部位置编码切断草稿端的
+                       * 全局位置增长": a fixed-length local group whose start is the origin);
+                       * 0 or 1 = the anchor alone; m + K + G <= 32, G <= 8. The group rows sit at
+                       * local positions 0..G-1, the placeholders at G..G+K-1, and the `anchor`
+                       * argument of the draft calls is then [B, G] int32 (oldest first, the anchor
+                       * last) */
 } dlite_config;
 
 #define DLITE_MAX_LAYERS 8
@@ -116,6 +122,7 @@ void dlite_destroy(dlite_handle *h);
  *   hidden [B, m, D] (cfg.dtype)  pivot features: the current hidden states of
  *                                 the m selected target layers (no KV, no history)
  *   anchor [B] int32              the token already chosen but not yet run
+ *                                 ([B, G] with anchor_group G > 1: the local group, anchor last)
  *                                 through the target ([P1] §"锚点...")
  *   temperature                   0 = greedy argmax; > 0 = Gumbel-max draw from
  *                                 q_i = softmax(l_i / T)
@@ -124,7 +131,8 @@ void dlite_destroy(dlite_handle *h);
  *                                 (ignored when temperature == 0; pos may be NULL then)
  *   candidates [B, K] int32       out: d_1..d_K
  *   qstats [B, K]                 out: draft statistics (may be NULL when T == 0)
- * Local rows: anchor at local position 0, placeholders at 1..K; the context
+ * Local rows: anchor at local position 0, placeholders at 1..K (with a group:
+ * group tokens at 0..G-1, placeholders at G..G+K-1); the context
  * slots are key/value-only rows at position 0. Out-of-range anchors are
  * clamped to 0 and flag DLITE_DEV_BOUNDS. */
 int dlite_draft_round(dlite_handle *h, int B, const void *hidden, const int32_t *anchor,
@@ -247,13 +255,20 @@ int dlite_verify_sample_static(int B, int K, int V, int D, const int32_t *candid
                                const int64_t *pos, int32_t *accepted, int32_t *commits,
                                int32_t *n_commit, int32_t *next_anchor, dlite_stream_t stream);
 
+/* Round bookkeeping for a local token group (anchor_group G): group [B, G] becomes the
+ * last G tokens of (group ++ commits[b, 0..n_commit[b]-1]), i.e. the G most recent
+ * tokens ending at the new anchor. commits [B, K+1] and n_commit [B] as written by the
+ * verification calls; with G = 1 this is the next anchor. In place, stream-ordered. */
+int dlite_shift_group(dlite_handle *h, int B, const int32_t *commits, const int32_t *n_commit,
+                      int32_t *group, dlite_stream_t stream);
+
 /* Round bookkeeping: pos[b] += n_commit[b] (the RNG positions follow the
  * committed tokens; [P1] §"一轮执行后..." — each round advances A+1). */
 int dlite_advance(dlite_handle *h, int B, const int32_t *n_commit, int64_t *pos,
                   dlite_stream_t stream);
 
 /* One whole round from HOST buffers: copies hidden_host [B, m, D] (cfg.dtype),
- * anchor_host [B], pos_host [B] and either target_tokens_host [B, K+1]
+ * anchor_host [B, G], pos_host [B] and either target_tokens_host [B, K+1]
  * (temperature == 0) or target_probs_host [B, K+1, V] (temperature > 0) to the
  * device, runs draft + verify, copies accepted/commits/n_commit/next_anchor
  * back into the *_host outputs, and synchronises `stream`. Host buffers should

@@ -314,6 +314,14 @@ def verify_greedy(cand, target_tokens, n_verify=None):
     return dict(A=A, commits=cand[:A] + [tok], n_commit=A + 1, next_anchor=tok)
 
 
+def next_group(group, commits):
+    """The next round's local token group: the G most recent tokens, i.e. the
+    last G of the current group followed by the committed tokens (the last
+    committed token is the new anchor; [P1] §"一轮执行后..." step 5)."""
+    seq = [int(t) for t in np.atleast_1d(group)] + [int(c) for c in commits]
+    return seq[-len(np.atleast_1d(group)):]
+
+
 def inverse_cdf(w, u):
     """Smallest index v with sum_{w<=v} w > u * sum(w), prefix sums in float64."""
     c = np.cumsum(np.asarray(w, dtype=np.float64))

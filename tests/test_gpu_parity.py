@@ -426,6 +426,72 @@ def test_verify_ex_rejects_bad_arguments(small_v):
         dr.verify_ex(7, cand, out["accepted"], out["commits"], out["n_commit"], out["next_anchor"])
 
 
+# ---------------------------------------------------------------- local token group
+
+@pytest.mark.parametrize("name,G", [("tiny", 2), ("bf16", 3)])
+def test_group_round_parity(name, G):
+    """A local token group of G tokens: staging, attention over G + K local rows
+    at positions 0..G+K-1 and the placeholder outputs, against the oracle."""
+    if name == "tiny":
+        cfg = wk.shrink(wk.TINY, G=G)
+        W = wk.make_weights(cfg, 21, gain_jitter=True)
+        tol = 1e-4
+    else:
+        cfg = wk.shrink(wk.QWEN3_8B, D=512, F=1024, L_D=2, n_q=4, n_kv=2, R=64, V=4096, m=6, G=G)
+        W = wk.make_weights(cfg, 22)
+        tol = HIDDEN_REL_TOL
+    wl = wk.WORKLOADS["tiny"]
+    B = 12
+    dr = _drafter(cfg, W, B_max=B)
+    try:
+        hidden, _, pos = wk.make_round_inputs(wl, B=B, cfg=cfg)
+        rng = np.random.default_rng(G)
+        groups = torch.from_numpy(rng.integers(0, cfg.V, size=(B, G)).astype(np.int32))
+        out = dr.new_outputs(B, DEV)
+        taps = {"z": torch.empty(B, cfg.m, cfg.D, device=DEV),
+                "x": torch.empty(cfg.L_D, B, G + cfg.K, cfg.D, device=DEV),
+                "b": torch.empty(B, cfg.K, cfg.D, device=DEV),
+                "hs": torch.empty(B, cfg.K, cfg.D, device=DEV)}
+        dr.draft_round(hidden.to(DEV), groups.to(DEV), 0.0, 0, pos.to(DEV), out["cand"], out["qstats"], taps=taps)
+        torch.cuda.synchronize()
+        cands, ocands, gaps = [], [], []
+        for b in range(B):
+            t = {}
+            r = O.draft_request(hidden[b], groups[b].numpy(), W, cfg, taps=t, mirror=(cfg.dtype == "bf16"))
+            for l in range(cfg.L_D):
+                assert rel_err(taps["x"][l, b].cpu(), t["x"][l]) < tol
+            assert rel_err(taps["b"][b].cpu(), t["b"]) < tol
+            cands.append(out["cand"][b].cpu().numpy())
+            ocands.append(r["cand"])
+            gaps.append(r["gap"])
+        check_candidates(np.stack(cands), np.stack(ocands), np.stack(gaps))
+    finally:
+        dr.close()
+
+
+def test_shift_group_matches_oracle(small_v):
+    """dlite_shift_group against the oracle's next_group (G = 1 in this drafter:
+    the next anchor), and a G = 4 drafter over random commit lengths."""
+    for G in (1, 4):
+        cfg = wk.shrink(wk.TINY, V=8, K=3, D=64, F=128, R=32, n_q=2, n_kv=1, m=2, G=G)
+        dr = _drafter(cfg, wk.make_weights(cfg, 7), B_max=64)
+        try:
+            rng = np.random.default_rng(90 + G)
+            B = 64
+            group = rng.integers(0, 8, size=(B, G)).astype(np.int32)
+            n = rng.integers(1, cfg.K + 2, size=B).astype(np.int32)
+            commits = np.where(np.arange(cfg.K + 1)[None, :] < n[:, None],
+                               rng.integers(0, 8, size=(B, cfg.K + 1)), -1).astype(np.int32)
+            g = _t(group)
+            dr.shift_group(_t(commits), _t(n), g)
+            torch.cuda.synchronize()
+            got = g.cpu().numpy()
+            for b in range(B):
+                assert list(got[b]) == O.next_group(group[b], commits[b, :n[b]])
+        finally:
+            dr.close()
+
+
 # ---------------------------------------------------------------- invariants and robustness
 
 def test_history_free_and_deterministic(tiny):

@@ -268,6 +268,23 @@ def test_group_zero_blocks_closed_form_and_dependence():
     assert not np.allclose(O.backbone(hidden[0], [1, 2], W, cfg), O.backbone(hidden[0], [3, 2], W, cfg))
 
 
+def test_next_group_is_the_most_recent_tokens():
+    """G = 1: the next group is the verification's next anchor; generally the
+    last G tokens of the group followed by the commits (brute force)."""
+    rng = np.random.default_rng(41)
+    for _ in range(200):
+        G = int(rng.integers(1, 6))
+        group = [int(t) for t in rng.integers(0, 100, G)]
+        n = int(rng.integers(1, 9))
+        commits = [int(t) for t in rng.integers(100, 200, n)]
+        ng = O.next_group(group, commits)
+        assert len(ng) == G and ng[-1] == commits[-1]
+        full = group + commits
+        assert ng == full[len(full) - G:]
+    r = O.verify_greedy([1, 2, 3], [1, 2, 9, 4])
+    assert O.next_group([5], r["commits"]) == [r["next_anchor"]]
+
+
 # ---------------------------------------------------------------- sequential head
 
 def test_head_with_zero_P_is_identity():
