@@ -155,6 +155,9 @@ def run_gpu(args):
         wl = dataclasses.replace(wl, name=f"{wl.name}-match")
     if nv is not None:
         wl = dataclasses.replace(wl, name=f"{wl.name}-nv{nv}")
+    grp = max(1, args.group)
+    if grp > 1:   # a local token group of G tokens ending at the anchor
+        wl = dataclasses.replace(wl, cfg=dataclasses.replace(wl.cfg, G=grp), name=f"{wl.name}-G{grp}")
     cfg = wl.cfg
     B = wl.B
     T = 0.0 if match else wl.temperature
@@ -172,6 +175,9 @@ def run_gpu(args):
                                                  device=dev)
         ring.append(item)
     _, anchor, pos = wk.make_round_inputs(wl, round_index=999 + 1000 * rank, device=dev)
+    if grp > 1:   # the group [B, G] (anchor last); the verification writes its next anchor aside
+        group = torch.randint(0, cfg.V, (B, grp), device=dev, dtype=torch.int32)
+        next_tok = torch.empty(B, device=dev, dtype=torch.int32)
     out = dr.new_outputs(B, dev)
     tgt = torch.randint(0, cfg.V, (B, cfg.K + 1), device=dev, dtype=torch.int32)
 
@@ -179,23 +185,26 @@ def run_gpu(args):
 
     def enqueue(k):
         it = ring[k]
-        dr.draft_round(it["hidden"], anchor, T, wl.rng_seed, pos, out["cand"], out["qstats"],
-                       stream=stream)
+        dr.draft_round(it["hidden"], group if grp > 1 else anchor, T, wl.rng_seed, pos, out["cand"],
+                       out["qstats"], stream=stream)
+        nxt = next_tok if grp > 1 else anchor
         if match:
             dr.verify_ex(binding.VERIFY_MATCH, out["cand"], out["accepted"], out["commits"], out["n_commit"],
-                         anchor, n_verify=nv, probs=it["probs"], seed=wl.rng_seed, pos=pos, stream=stream)
+                         nxt, n_verify=nv, probs=it["probs"], seed=wl.rng_seed, pos=pos, stream=stream)
         elif nv is not None:
             dr.verify_ex(binding.VERIFY_SAMPLE if sampling else binding.VERIFY_GREEDY, out["cand"],
-                         out["accepted"], out["commits"], out["n_commit"], anchor, n_verify=nv,
+                         out["accepted"], out["commits"], out["n_commit"], nxt, n_verify=nv,
                          target_tokens=None if sampling else tgt, qstats=out["qstats"] if sampling else None,
                          probs=it.get("probs") if sampling else None, temperature=T, seed=wl.rng_seed,
                          pos=pos, stream=stream)
         elif sampling:
             dr.verify_sample(out["cand"], out["qstats"], None, it["probs"], T, wl.rng_seed, pos,
-                             out["accepted"], out["commits"], out["n_commit"], anchor, stream=stream)
+                             out["accepted"], out["commits"], out["n_commit"], nxt, stream=stream)
         else:
-            dr.verify(out["cand"], tgt, out["accepted"], out["commits"], out["n_commit"], anchor,
+            dr.verify(out["cand"], tgt, out["accepted"], out["commits"], out["n_commit"], nxt,
                       stream=stream)
+        if grp > 1:
+            dr.shift_group(out["commits"], out["n_commit"], group, stream=stream)
         dr.advance(out["n_commit"], pos, stream=stream)
 
     # eager warm-up (also sets kernel attributes before capture)
@@ -209,7 +218,7 @@ def run_gpu(args):
             with torch.cuda.graph(g, stream=stream):
                 enqueue(k)
         graphs.append(g)
-    launches_per_step = dr.launch_count(B, T) + 1 + (1 if match else 0)  # + position update (+ match samples)
+    launches_per_step = dr.launch_count(B, T) + 1 + (1 if match else 0) + (1 if grp > 1 else 0)
 
     ncommit_total = torch.zeros((), dtype=torch.int64, device=dev)
     with torch.cuda.stream(stream):
@@ -266,7 +275,7 @@ def run_gpu(args):
     nprof = 5
     for r in range(nprof):
         it = ring[r % RING]
-        times = dr.stage_times(it["hidden"], anchor, T, wl.rng_seed, pos, out,
+        times = dr.stage_times(it["hidden"], group if grp > 1 else anchor, T, wl.rng_seed, pos, out,
                                target_tokens=None if sampling else tgt,
                                target_probs=it.get("probs"), stream=stream)
         for name, t in times:
@@ -301,7 +310,7 @@ def run_gpu(args):
 
     # ---- end to end through the public host-buffer call
     e2e = None
-    if (rank == 0 or ws > 1) and not match and nv is None:   # the host-buffer call runs the default verification
+    if (rank == 0 or ws > 1) and not match and nv is None and grp == 1:   # the host call: default verification
         e2e = run_e2e(dr, wl, ring, anchor, pos, stream, max(3, min(args.steps, 20)))
 
     result = {
@@ -471,6 +480,7 @@ def main():
     ap.add_argument("--verify", default="default", choices=["default", "match"],
                     help="match: greedy draft verified against the target's own samples")
     ap.add_argument("--n-verify", type=int, default=-1, help="verification window (candidates verified; -1: all)")
+    ap.add_argument("--group", type=int, default=1, help="local token group size G (anchor last)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
