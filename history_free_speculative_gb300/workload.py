@@ -32,6 +32,7 @@ class DraftConfig:
     eps: float = 1e-6
     theta: float = 1e6
     G: int = 1      # local token group ending at the anchor (local positions 0..G-1)
+    head: str = "rnn"   # "rnn": low-rank RNN head + tied D->V projection; "gated": token-feedback head
 
     @property
     def torch_dtype(self):
@@ -143,6 +144,13 @@ def make_weights(cfg, seed, device="cpu", gain_jitter=False):
     W["g_final"] = gain()
     W["Q"] = mat(R, 2 * D)
     W["P"] = mat(D, R)
+    if cfg.head == "gated":   # the token-feedback head: E_R [V, R], W_s [2R, 2R], W_h [R, R + D], W_o [V, R]
+        W["E_R"] = mat(V, R)
+        W["W_s"] = mat(2 * R, 2 * R)
+        W["b_s"] = mat(2 * R)
+        W["W_h"] = mat(R, R + D)
+        W["b_h"] = mat(R)
+        W["W_o"] = mat(V, R)
     return W
 
 

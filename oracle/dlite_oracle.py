@@ -222,6 +222,59 @@ def sequential_head(b, Q, P):
     return out
 
 
+def _pick(ell_i, temperature, seed, position, request):
+    """d from one row of logits: argmax (T = 0) or Gumbel-max on l/T with the
+    Philox noise of (position, request); returns (d, gap, lse)."""
+    if temperature == 0.0:
+        d = int(np.argmax(ell_i))
+        return d, float(_top2_gap(ell_i[None, :])[0]), float("nan")
+    s = ell_i / temperature + _ph.gumbel_row(seed, position, request, ell_i.shape[0])
+    m = float((ell_i / temperature).max())
+    lse = m + float(np.log(np.exp(ell_i / temperature - m).sum()))
+    return int(np.argmax(s)), float(_top2_gap(s[None, :])[0]), lse
+
+
+def gated_head(b, anchor_token, W, temperature=0.0, seed=0, pos=0, request=0):
+    """The official gated token-feedback head, direct form ([P1] §"官方顺序头具体
+    算了什么", eq. block), one request:
+        v_i = E_R(d_{i-1}), d_0 = the anchor;
+        [g_i, c_i] = W_s [s_{i-1}; v_i] + b_s;   f_i = sigmoid(g_i);
+        s_i = f_i * s_{i-1} + (1 - f_i) * tanh(c_i),  s_0 = 0 (the state starts
+              with the block);
+        r_i = W_h [s_i; u_i] + b_h;   l_i = W_o r_i,
+    and d_i is drawn from l_i like the main head's candidates (argmax, or
+    Gumbel-max on l_i / T at position pos + i) before step i + 1 reads it.
+    g is the first R outputs of W_s, c the last R; W_h acts on [s; u].
+    Returns dict(cand, logit_d, lse, gap, r [K, R], logits [K, V]).
+    """
+    u = f64(b)
+    K = u.shape[0]
+    E_R, W_s, b_s = f64(W["E_R"]), f64(W["W_s"]), f64(W["b_s"])
+    W_h, b_h, W_o = f64(W["W_h"]), f64(W["b_h"]), f64(W["W_o"])
+    R = E_R.shape[1]
+    temperature = float(np.float32(temperature))
+    s_prev = np.zeros(R)
+    d_prev = int(anchor_token)
+    cand, logit_d, lse, gap = [], [], [], []
+    rs, ells = np.empty((K, R)), []
+    for i in range(K):
+        gc = W_s @ np.concatenate([s_prev, E_R[d_prev]]) + b_s
+        f = 1.0 / (1.0 + np.exp(-gc[:R]))
+        s_i = f * s_prev + (1.0 - f) * np.tanh(gc[R:])
+        r = W_h @ np.concatenate([s_i, u[i]]) + b_h
+        ell = W_o @ r
+        d, gp, l = _pick(ell, temperature, seed, pos + i + 1, request)
+        cand.append(d)
+        logit_d.append(float(ell[d]))
+        lse.append(l)
+        gap.append(gp)
+        rs[i] = r
+        ells.append(ell)
+        s_prev, d_prev = s_i, d
+    return dict(cand=np.array(cand, dtype=np.int64), logit_d=np.array(logit_d), lse=np.array(lse),
+                gap=np.array(gap), r=rs, logits=np.stack(ells))
+
+
 def lm_logits(h, E, chunk=16384):
     """The single vocabulary projection l = E h (tied E [V, D]), chunked over V.
 
@@ -254,6 +307,13 @@ def draft_request(hidden, anchor, W, cfg, temperature=0.0, seed=0, pos=0, reques
     """
     temperature = float(np.float32(temperature))   # a float32 quantity, as in the C ABI
     b = backbone(hidden, anchor, W, cfg, mirror, taps)
+    if getattr(cfg, "head", "rnn") == "gated":   # token feedback: vocabulary projection inside each step
+        r = gated_head(b, anchor_group(anchor, cfg)[-1], W, temperature, seed, pos, request)
+        if taps is not None:
+            taps["b"] = b
+            taps["h"] = r["r"]
+            taps["logits"] = r["logits"]
+        return dict(cand=r["cand"], logit_d=r["logit_d"], lse=r["lse"], gap=r["gap"], b=b, h=r["r"])
     h = sequential_head(b, W["Q"], W["P"])
     ell = lm_logits(h, W["E"])
     K = cfg.K

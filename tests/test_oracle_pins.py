@@ -285,6 +285,72 @@ def test_next_group_is_the_most_recent_tokens():
     assert O.next_group([5], r["commits"]) == [r["next_anchor"]]
 
 
+# ---------------------------------------------------------------- gated token-feedback head
+
+def _gated_setup(seed=5, V=64, R=16, D=32, K=5):
+    rng = np.random.default_rng(seed)
+    W = {"E_R": rng.normal(0, 0.5, (V, R)), "W_s": rng.normal(0, 0.3, (2 * R, 2 * R)),
+         "b_s": rng.normal(0, 0.3, 2 * R), "W_h": rng.normal(0, 0.3, (R, R + D)),
+         "b_h": rng.normal(0, 0.3, R), "W_o": rng.normal(0, 0.5, (V, R))}
+    u = rng.normal(0, 1.0, (K, D))
+    return W, u, R
+
+
+def test_gated_head_saturated_gate_ignores_feedback():
+    """f = sigmoid(g) -> 1 (large gate bias): the state stays at s_0 = 0, so
+    r_i = W_h[:, R:] u_i + b_h and l_i = W_o r_i whatever the tokens fed back."""
+    W, u, R = _gated_setup()
+    W["b_s"] = W["b_s"].copy()
+    W["b_s"][:R] = 60.0
+    want_r = u @ W["W_h"][:, R:].T + W["b_h"]
+    for anchor in (0, 17, 63):
+        out = O.gated_head(u, anchor, W)
+        assert np.allclose(out["r"], want_r, atol=1e-12)
+        assert np.allclose(out["logits"], want_r @ W["W_o"].T, atol=1e-12)
+        assert list(out["cand"]) == list(np.argmax(want_r @ W["W_o"].T, axis=1))
+
+
+def test_gated_head_open_gate_reads_the_previous_token():
+    """f -> 0 and no state-to-candidate weights: s_i = tanh(W_s[R:, R:] E_R[d_{i-1}]
+    + b_s[R:]), so each step depends on the previous token only (d_0 = anchor);
+    swapping the g / c halves, feeding d_i instead of d_{i-1} or the [s; u]
+    order of W_h would all break this."""
+    W, u, R = _gated_setup(6)
+    W["b_s"] = W["b_s"].copy()
+    W["b_s"][:R] = -60.0
+    W["W_s"] = W["W_s"].copy()
+    W["W_s"][R:, :R] = 0.0
+    anchor = 9
+    out = O.gated_head(u, anchor, W)
+    prev = anchor
+    for i in range(u.shape[0]):
+        s_i = np.tanh(W["W_s"][R:, R:] @ W["E_R"][prev] + W["b_s"][R:])
+        r = W["W_h"][:, :R] @ s_i + W["W_h"][:, R:] @ u[i] + W["b_h"]
+        assert np.allclose(out["r"][i], r, atol=1e-12)
+        prev = int(out["cand"][i])
+        assert prev == int(np.argmax(W["W_o"] @ r))
+    other = O.gated_head(u, 10, W)
+    assert not np.allclose(other["r"][0], out["r"][0])   # the anchor is fed back
+
+
+def test_gated_head_sampling_follows_softmax():
+    """T > 0: the first candidate is a draw from softmax(l_1 / T) (chi-square
+    over positions), and lse is the log-sum-exp of l_1 / T."""
+    W, u, R = _gated_setup(7, V=8)
+    T, N = 0.8, 12000
+    ell = O.gated_head(u, 3, W)["logits"][0]
+    p = np.exp(ell / np.float32(T) - (ell / np.float32(T)).max())
+    p /= p.sum()
+    counts = np.zeros(8)
+    for n in range(N):
+        out = O.gated_head(u[:1], 3, W, temperature=T, seed=2, pos=10 * n, request=1)
+        counts[out["cand"][0]] += 1
+    chi2 = ((counts - N * p) ** 2 / (N * p)).sum()
+    assert chi2 < 30.0                                    # 7 dof
+    want = float(torch.logsumexp(torch.tensor(ell / float(np.float32(T))), 0))
+    assert abs(out["lse"][0] - want) < 1e-9
+
+
 # ---------------------------------------------------------------- sequential head
 
 def test_head_with_zero_P_is_identity():
