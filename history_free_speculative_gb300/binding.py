@@ -30,7 +30,8 @@ class DliteError(RuntimeError):
 class Config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
                 ("B_max", "D", "m", "K", "L_D", "n_q", "n_kv", "d_h", "F", "R", "V", "dtype")] + \
-               [("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float), ("anchor_group", ctypes.c_int)]
+               [("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float), ("anchor_group", ctypes.c_int),
+                ("head_type", ctypes.c_int)]
 
 
 class LayerWeights(ctypes.Structure):
@@ -38,9 +39,16 @@ class LayerWeights(ctypes.Structure):
                 ("g_attn", "Wq", "Wk", "Wv", "Wo", "g_ffn", "Wg", "Wu", "Wd")]
 
 
+GATED_FIELDS = ("E_R", "W_s", "b_s", "W_h", "b_h", "W_o")
+
+
+class GatedWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in GATED_FIELDS]
+
+
 class Weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("e_depth", "g_stage", "e_ph", "E", "g_final", "Q", "P")] + \
-               [("layer", LayerWeights * MAX_LAYERS)]
+               [("layer", LayerWeights * MAX_LAYERS), ("gated", GatedWeights)]
 
 
 VERIFY_GREEDY, VERIFY_SAMPLE, VERIFY_MATCH = 0, 1, 2
@@ -186,7 +194,8 @@ def config_struct(cfg, B_max):
     return Config(B_max=B_max, D=cfg.D, m=cfg.m, K=cfg.K, L_D=cfg.L_D, n_q=cfg.n_q,
                   n_kv=cfg.n_kv, d_h=cfg.d_h, F=cfg.F, R=cfg.R, V=cfg.V,
                   dtype=DLITE_F32 if cfg.dtype == "f32" else DLITE_BF16,
-                  rms_eps=cfg.eps, rope_theta=cfg.theta, anchor_group=getattr(cfg, "G", 1))
+                  rms_eps=cfg.eps, rope_theta=cfg.theta, anchor_group=getattr(cfg, "G", 1),
+                  head_type=1 if getattr(cfg, "head", "rnn") == "gated" else 0)
 
 
 class Drafter:
@@ -207,6 +216,9 @@ class Drafter:
         for i, L in enumerate(W["layers"]):
             for n in ("g_attn", "Wq", "Wk", "Wv", "Wo", "g_ffn", "Wg", "Wu", "Wd"):
                 setattr(w.layer[i], n, _ptr(L[n]).value)
+        if getattr(cfg, "head", "rnn") == "gated":
+            for n in GATED_FIELDS:
+                setattr(w.gated, n, _ptr(W[n]).value)
         h = ctypes.c_void_p()
         _check(self.lib.dlite_create(ctypes.byref(c), ctypes.byref(w), ctypes.byref(h)), "dlite_create")
         self.h = h

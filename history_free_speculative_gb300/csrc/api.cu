@@ -46,6 +46,17 @@ struct dlite_handle {
   const bf16* Wce[2] = {nullptr, nullptr};  // [2R, D] = [Q_b; Q_h]
   const bf16* P[2] = {nullptr, nullptr};    // [D, R]
   float* Mt = nullptr;                      // [R, R] Q_h P in the chain's register image
+  // gated token-feedback head (head_type 1)
+  bool gated = false;
+  const bf16 *Ws[2] = {nullptr, nullptr}, *Whs[2] = {nullptr, nullptr}, *Whu[2] = {nullptr, nullptr},
+             *Wo[2] = {nullptr, nullptr};     // tiled planes: [2R, 2R], [R, R], [R, D], [Vp, R]
+  float *ER32 = nullptr, *bs32 = nullptr, *bh32 = nullptr, *Wo32 = nullptr;  // fp32 (Wo32: fp32 drafters)
+  int Bcap = 0;                             // B_max padded to 128 (activation rows of the step products)
+  float *g_s = nullptr, *g_hu = nullptr, *g_r = nullptr, *g_rstep = nullptr;
+  bf16 *g_xp[2] = {nullptr, nullptr}, *g_sp[2] = {nullptr, nullptr}, *g_rp = nullptr;
+  int32_t* g_cand = nullptr;
+  dlite_qstats* g_qs = nullptr;
+  int64_t* g_pos = nullptr;
   float *rope_cos = nullptr, *rope_sin = nullptr;
 
   // workspace
@@ -139,6 +150,8 @@ int check_config(const dlite_config* c) {
   if (c->R < 32 || chain_smem_bytes(c->R, c->K, chain_group_size(c->R, c->B_max)) > 200 * 1024)
     return DLITE_ERR_UNSUPPORTED_SHAPE;
   if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return DLITE_ERR_INVALID_ARG;
+  if (c->head_type != DLITE_HEAD_RNN && c->head_type != DLITE_HEAD_GATED) return DLITE_ERR_INVALID_ARG;
+  if (c->head_type == DLITE_HEAD_GATED && c->R % 64) return DLITE_ERR_UNSUPPORTED_SHAPE;
   return DLITE_OK;
 }
 
@@ -482,21 +495,35 @@ int run_seq_head(dlite_handle* h, int B, float* tap_hs, cudaStream_t s) {
   return DLITE_OK;
 }
 
-int run_lm_head(dlite_handle* h, int B, float temperature, uint64_t seed, const int64_t* pos,
-                int32_t* cand, dlite_qstats* qs, cudaStream_t s) {
+// The vocabulary projection with the fused choice: logits = W x for `rows`
+// rows of the bf16 activation x [x_cap rows, Kd] (tiled weight w [Vp, Kd]);
+// records, then the merge re-scores the finalists with the fp32 vectors vec
+// [rows, Kd] against the weight (bf16 tiled w, or w32 fp32 row-major) and
+// writes cand / qs per row. Row r draws its Gumbel noise at position
+// pos[r / K_draft] + r % K_draft + 1.
+struct LmOperands {
+  const bf16* x;
+  int x_cap, Kd;
+  const bf16* w;
+  const float* w32;
+  const float* vec;
+  int K_draft;
+};
+
+int run_lm_core(dlite_handle* h, int rows, const LmOperands& op, float temperature, uint64_t seed,
+                const int64_t* pos, int32_t* cand, dlite_qstats* qs, cudaStream_t s) {
   const dlite_config& c = h->cfg;
-  const int rows = B * c.K;
   const float inv_T = temperature > 0.f ? 1.f / temperature : 0.f;
   uint32_t k0 = 0, k1 = 0;
   seed_key(seed, &k0, &k1);
   int n_tiles = 0;
-  const tc::LmPlan lp = tc::lm_plan_persistent(rows, c.V, c.D, h->num_sms);
+  const tc::LmPlan lp = tc::lm_plan_persistent(rows, c.V, op.Kd, h->num_sms);
   if (lp.ok) {  // persistent kernel, epilogue overlapped with the E stream
     h->maps.reserve(h->maps.size() + 4);
-    const CUtensorMap* x0 = get_map(h, h->hp[0], h->Hcap, c.D, lp.x_box0);
-    const CUtensorMap* x1 = lp.paired ? get_map(h, h->hp[0], h->Hcap, c.D, lp.x_box1) : nullptr;
+    const CUtensorMap* x0 = get_map(h, op.x, op.x_cap, op.Kd, lp.x_box0);
+    const CUtensorMap* x1 = lp.paired ? get_map(h, op.x, op.x_cap, op.Kd, lp.x_box1) : nullptr;
     // a pair's CTAs each load half of every slab
-    const CUtensorMap* w0 = get_map(h, h->E[0], h->Vp, c.D, lp.paired ? lp.N / 2 : lp.N, true);
+    const CUtensorMap* w0 = get_map(h, op.w, h->Vp, op.Kd, lp.paired ? lp.N / 2 : lp.N, true);
     if (!x0 || !w0 || (lp.paired && !x1)) return DLITE_ERR_CUDA;
     tc::LmParams prm;
     prm.rows = rows;
@@ -506,22 +533,22 @@ int run_lm_head(dlite_handle* h, int B, float temperature, uint64_t seed, const 
     prm.k0 = k0;
     prm.k1 = k1;
     prm.pos = pos;
-    prm.K_draft = c.K;
+    prm.K_draft = op.K_draft;
     prm.status = h->status;
     CK(tc::launch_lm_persistent(lp, x0, x1, w0, prm, s));
     n_tiles = lp.n_units;  // one record per walk and row
   } else {  // one slab per CTA
-    const tc::Plan pl = lm_plan(h, rows);
+    const tc::Plan pl = tc::plan(rows, c.V, op.Kd, 1, 1, true);
     if (!pl.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
     const int xb = tc::x_box_rows(rows);
     h->maps.reserve(h->maps.size() + 4);
-    const CUtensorMap* x0 = get_map(h, h->hp[0], h->Hcap, c.D, xb);
-    const CUtensorMap* w0 = get_map(h, h->E[0], h->Vp, c.D, pl.N, true);
+    const CUtensorMap* x0 = get_map(h, op.x, op.x_cap, op.Kd, xb);
+    const CUtensorMap* w0 = get_map(h, op.w, h->Vp, op.Kd, pl.N, true);
     if (!x0 || !w0) return DLITE_ERR_CUDA;
     tc::TcParams prm;
     prm.rows = rows;
     prm.outs = c.V;
-    prm.K = c.D;
+    prm.K = op.Kd;
     prm.xplanes = 1;
     prm.wplanes = 1;
     prm.mode = 1;
@@ -531,7 +558,7 @@ int run_lm_head(dlite_handle* h, int B, float temperature, uint64_t seed, const 
     prm.k0 = k0;
     prm.k1 = k1;
     prm.pos = pos;
-    prm.K_draft = c.K;
+    prm.K_draft = op.K_draft;
     prm.status = h->status;
     CK(tc::launch(pl, x0, nullptr, w0, nullptr, prm, s));
     n_tiles = (c.V + pl.N - 1) / pl.N * tc::kGemmEpiGroups;
@@ -541,24 +568,103 @@ int run_lm_head(dlite_handle* h, int B, float temperature, uint64_t seed, const 
   mg.rec = h->lmrec;
   mg.n_tiles = n_tiles;
   mg.rows = rows;
-  mg.K = c.K;
-  mg.D = c.D;
+  mg.K = op.K_draft;
+  mg.D = op.Kd;
   mg.V = c.V;
   mg.inv_T = inv_T;
   mg.T = (double)temperature;
   mg.k0 = k0;
   mg.k1 = k1;
   mg.pos = pos;
-  mg.h = h->hs;
-  if (h->f32)
-    mg.Ef = (const float*)h->E_src;
+  mg.h = op.vec;
+  if (op.w32)
+    mg.Ef = op.w32;
   else
-    mg.Eb = h->E[0];
+    mg.Eb = op.w;
   mg.cand = cand;
   mg.qs = qs;
   mg.counters = h->counters;
   CK(launch_lm_merge(mg, s));
   mark(h, "lm_merge");
+  return DLITE_OK;
+}
+
+int run_lm_head(dlite_handle* h, int B, float temperature, uint64_t seed, const int64_t* pos,
+                int32_t* cand, dlite_qstats* qs, cudaStream_t s) {
+  const dlite_config& c = h->cfg;
+  LmOperands op;
+  op.x = h->hp[0];
+  op.x_cap = h->Hcap;
+  op.Kd = c.D;
+  op.w = h->E[0];
+  op.w32 = h->f32 ? (const float*)h->E_src : nullptr;
+  op.vec = h->hs;
+  op.K_draft = c.K;
+  return run_lm_core(h, B * c.K, op, temperature, seed, pos, cand, qs, s);
+}
+
+// The gated token-feedback head after the backbone (b, h->bp): per step i the
+// input [s_{i-1}; E_R[d_{i-1}]], the state product and gate, the r product,
+// then the vocabulary projection over W_o with the fused choice, whose token
+// the next step feeds back. r [B, K, R] stays in h->g_r (verification's q(v)).
+int run_gated_head(dlite_handle* h, int B, const int32_t* anchor, float temperature, uint64_t seed,
+                   const int64_t* pos, int32_t* cand, dlite_qstats* qs, float* tap_r, cudaStream_t s) {
+  const dlite_config& c = h->cfg;
+  const int R = c.R, K = c.K;
+  Splits S;
+  RUN(gemm(h, "gemm_gated_hu", opnd(h->bp, 2, h->Hcap, c.D), opnd(h->Whu, h->np, R, c.D), B * K, R, h->part,
+           &S, s));
+  CK(launch_gated_sum(h->part, S, B * K, R, h->g_hu, s));
+  mark(h, "gated_hu");
+  GatedArgs g;
+  g.B = B;
+  g.K = K;
+  g.R = R;
+  g.G = group_of(&c);
+  g.V = c.V;
+  g.anchor = anchor;
+  g.cand_tmp = h->g_cand;
+  g.qs_tmp = qs ? h->g_qs : nullptr;
+  g.cand = cand;
+  g.qs = qs;
+  g.pos = pos;
+  g.pos_i = h->g_pos;
+  g.ER = h->ER32;
+  g.bs = h->bs32;
+  g.bh = h->bh32;
+  g.hu = h->g_hu;
+  g.s = h->g_s;
+  g.xp[0] = h->g_xp[0];
+  g.xp[1] = h->g_xp[1];
+  g.sp[0] = h->g_sp[0];
+  g.sp[1] = h->g_sp[1];
+  g.r_all = h->g_r;
+  g.r_step = h->g_rstep;
+  g.rp = h->g_rp;
+  g.status = h->status;
+  LmOperands op;
+  op.x = h->g_rp;
+  op.x_cap = h->Bcap;
+  op.Kd = R;
+  op.w = h->Wo[0];
+  op.w32 = h->f32 ? h->Wo32 : nullptr;
+  op.vec = h->g_rstep;
+  op.K_draft = 1;
+  for (int i = 1; i <= K; ++i) {
+    CK(launch_gated_prep(g, i, s));
+    mark(h, "gated_prep");
+    RUN(gemm(h, "gemm_gated_s", opnd(h->g_xp, 2, h->Bcap, 2 * R), opnd(h->Ws, h->np, 2 * R, 2 * R), B, 2 * R,
+             h->part, &S, s));
+    CK(launch_gated_gate(g, h->part, S, s));
+    mark(h, "gated_gate");
+    RUN(gemm(h, "gemm_gated_r", opnd(h->g_sp, 2, h->Bcap, R), opnd(h->Whs, h->np, R, R), B, R, h->part, &S, s));
+    CK(launch_gated_r(g, i, h->part, S, s));
+    mark(h, "gated_r");
+    RUN(run_lm_core(h, B, op, temperature, seed, pos ? h->g_pos : nullptr, h->g_cand, qs ? h->g_qs : nullptr, s));
+  }
+  CK(launch_gated_final(g, s));
+  mark(h, "gated_final");
+  if (tap_r) CK(cudaMemcpyAsync(tap_r, h->g_r, (size_t)B * K * R * 4, cudaMemcpyDeviceToDevice, s));
   return DLITE_OK;
 }
 
@@ -682,6 +788,26 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
     h->P[0] = p0;
     h->P[1] = p1;
   }
+  if (h->gated) {  // the gated token-feedback head's weights (R is a multiple of 64)
+    RUN(repack(h, w->gated.W_s, 2 * R, 2 * R, 2 * R, 0, h->Ws, nullptr));
+    RUN(repack(h, w->gated.W_h, R, R, R + D, 0, h->Whs, nullptr));
+    RUN(repack(h, w->gated.W_h, R, D, R + D, R, h->Whu, nullptr));
+    RUN(repack(h, w->gated.E_R, V, R, R, 0, nullptr, &h->ER32));
+    RUN(repack(h, w->gated.b_s, 1, 2 * R, 2 * R, 0, nullptr, &h->bs32));
+    RUN(repack(h, w->gated.b_h, 1, R, R, 0, nullptr, &h->bh32));
+    bf16* p0 = nullptr;
+    bf16* p1 = nullptr;
+    AL(p0, (size_t)h->Vp * R);
+    CK(cudaMemset(p0, 0, (size_t)h->Vp * R * 2));
+    if (h->np == 2) {
+      AL(p1, (size_t)h->Vp * R);
+      CK(cudaMemset(p1, 0, (size_t)h->Vp * R * 2));
+    }
+    if (h->f32) AL(h->Wo32, (size_t)V * R);
+    CK(launch_repack(w->gated.W_o, h->f32, V, R, R, 0, p0, p1, h->np, h->Wo32, -R, 0));
+    h->Wo[0] = p0;
+    h->Wo[1] = p1;
+  }
   AL(h->Mt, (size_t)R * R);
   CK(launch_head_matrix(w->Q, w->P, h->f32, D, R, h->Mt, 0));
   {  // RoPE table for local positions 0..G+K-1 (float64 on the host)
@@ -720,9 +846,12 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
   size_t pe = 0, pe2 = 0, lme = 0;
   for (int B = 1; B <= Bm; ++B) {
     const int L = B * (group_of(&c) + c.K), C = B * c.m, H = B * c.K;
-    const int sites[6][4] = {{L, h->qd + 2 * h->kvd, D, h->np}, {L, D, h->qd, h->np},
+    const int sites[9][4] = {{L, h->qd + 2 * h->kvd, D, h->np}, {L, D, h->qd, h->np},
                              {L, 2 * F, D, h->np},               {L, D, F, h->np},
-                             {H, 2 * h->Rp, D, 2},               {H, D, h->Rp, 2}};
+                             {H, 2 * h->Rp, D, 2},               {H, D, h->Rp, 2},
+                             // the gated head's products (sized whatever the head type)
+                             {H, h->Rp, D, 2},                   {B, 2 * h->Rp, 2 * h->Rp, 2},
+                             {B, h->Rp, h->Rp, 2}};
     for (auto& st : sites) {
       const tc::Plan pl = tc::plan(st[0], st[1], st[2], st[3], h->np, false);
       if (!pl.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
@@ -762,6 +891,24 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
   AL(h->lmrec, lme);
   AL(h->resid, (size_t)Bm * V);
   AL(h->tsamp, (size_t)Bm * (c.K + 1));
+  if (h->gated) {
+    const size_t Bc = (size_t)h->Bcap;
+    AL(h->g_s, (size_t)Bm * R);
+    AL(h->g_hu, (size_t)Bm * c.K * R);
+    AL(h->g_r, (size_t)Bm * c.K * R);
+    AL(h->g_rstep, (size_t)Bm * R);
+    for (int p = 0; p < 2; ++p) {
+      AL(h->g_xp[p], Bc * 2 * R);
+      CK(cudaMemset(h->g_xp[p], 0, Bc * 2 * R * 2));
+      AL(h->g_sp[p], Bc * R);
+      CK(cudaMemset(h->g_sp[p], 0, Bc * R * 2));
+    }
+    AL(h->g_rp, Bc * R);
+    CK(cudaMemset(h->g_rp, 0, Bc * R * 2));
+    AL(h->g_cand, (size_t)Bm);
+    AL(h->g_qs, (size_t)Bm);
+    AL(h->g_pos, (size_t)Bm);
+  }
   AL(h->counters, 8);
   CK(cudaMemset(h->counters, 0, 8 * sizeof(unsigned long long)));
   AL(h->status, 1);
@@ -794,6 +941,9 @@ int dlite_create(const dlite_config* cfg, const dlite_weights* w, dlite_handle**
   *out = nullptr;
   const int rc = check_config(cfg);
   if (rc) return rc;
+  if (cfg->head_type == DLITE_HEAD_GATED &&
+      (!w->gated.E_R || !w->gated.W_s || !w->gated.b_s || !w->gated.W_h || !w->gated.b_h || !w->gated.W_o))
+    return DLITE_ERR_INVALID_ARG;
   if (!w->e_depth || !w->g_stage || !w->e_ph || !w->E || !w->g_final || !w->Q || !w->P)
     return DLITE_ERR_INVALID_ARG;
   dlite_handle* h = new dlite_handle();
@@ -807,6 +957,8 @@ int dlite_create(const dlite_config* cfg, const dlite_weights* w, dlite_handle**
   h->Lcap = (cfg->B_max * (group_of(cfg) + cfg->K) + 127) / 128 * 128;
   h->Ccap = (cfg->B_max * cfg->m + 127) / 128 * 128;
   h->Hcap = (cfg->B_max * cfg->K + 127) / 128 * 128;
+  h->Bcap = (cfg->B_max + 127) / 128 * 128;
+  h->gated = cfg->head_type == DLITE_HEAD_GATED;
   {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -831,6 +983,8 @@ int dlite_draft_round_taps(dlite_handle* h, int B, const void* hidden, const int
   RUN(check_round_args(h, B, hidden, anchor, temperature, pos, cand, qs));
   cudaStream_t s = (cudaStream_t)stream;
   RUN(run_backbone(h, B, hidden, anchor, taps, s));
+  if (h->gated)  // the head's vectors (r) go to the hs tap
+    return run_gated_head(h, B, anchor, temperature, seed, pos, cand, qs, taps ? taps->hs : nullptr, s);
   RUN(run_seq_head(h, B, taps ? taps->hs : nullptr, s));
   RUN(run_lm_head(h, B, temperature, seed, pos, cand, qs, s));
   return DLITE_OK;
@@ -852,6 +1006,7 @@ int dlite_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* an
 
 int dlite_seq_head(dlite_handle* h, int B, const float* b, float* hs, dlite_stream_t stream) {
   if (!h || !b || !hs || B < 1 || B > h->cfg.B_max) return DLITE_ERR_INVALID_ARG;
+  if (h->gated) return DLITE_ERR_UNSUPPORTED_SHAPE;  // the gated head runs inside dlite_draft_round
   cudaStream_t s = (cudaStream_t)stream;
   const size_t n = (size_t)B * h->cfg.K * h->cfg.D;
   CK(launch_split(b, n, h->bp, h->b, s));
@@ -861,12 +1016,33 @@ int dlite_seq_head(dlite_handle* h, int B, const float* b, float* hs, dlite_stre
 int dlite_lm_head(dlite_handle* h, int B, const float* hs, float temperature, uint64_t seed,
                   const int64_t* pos, int32_t* cand, dlite_qstats* qs, dlite_stream_t stream) {
   if (!h || !hs || !cand || B < 1 || B > h->cfg.B_max) return DLITE_ERR_INVALID_ARG;
+  if (h->gated) return DLITE_ERR_UNSUPPORTED_SHAPE;  // the gated head runs inside dlite_draft_round
   if (!(temperature >= 0.f) || isinf(temperature)) return DLITE_ERR_INVALID_ARG;
   if (temperature > 0.f && (!pos || !qs)) return DLITE_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   const size_t n = (size_t)B * h->cfg.K * h->cfg.D;
   CK(launch_split(hs, n, h->hp, h->hs, s));
   return run_lm_head(h, B, temperature, seed, pos, cand, qs, s);
+}
+
+// Where verification recomputes q(v) = exp(w_v . x_i / T - lse_i): the tied E and
+// the head outputs h_i (D wide), or, for the gated head, W_o and r_i (R wide).
+void set_q_source(dlite_handle* h, VerifyArgs* v, const float* vec) {
+  if (h->gated) {
+    v->D = h->cfg.R;
+    v->hs = vec ? vec : h->g_r;
+    if (h->f32)
+      v->Ef = h->Wo32;
+    else
+      v->Eb = h->Wo[0];
+    return;
+  }
+  v->D = h->cfg.D;
+  v->hs = vec ? vec : h->hs;
+  if (h->f32)
+    v->Ef = (const float*)h->E_src;
+  else
+    v->Eb = h->E[0];
 }
 
 int dlite_verify(dlite_handle* h, int B, const int32_t* cand, const int32_t* tgt, int32_t* accepted,
@@ -905,12 +1081,8 @@ int dlite_verify_sample(dlite_handle* h, int B, const int32_t* cand, const dlite
   v.D = h->cfg.D;
   v.cand = cand;
   v.qs = qs;
-  v.hs = hs ? hs : h->hs;
   v.probs = probs;
-  if (h->f32)
-    v.Ef = (const float*)h->E_src;
-  else
-    v.Eb = h->E[0];
+  set_q_source(h, &v, hs);
   v.resid = h->resid;
   v.counters = h->counters;
   v.T = (double)temperature;
@@ -956,12 +1128,8 @@ int dlite_verify_ex(dlite_handle* h, const dlite_verify_args* a, dlite_stream_t 
       if (!a->qstats || !a->target_probs || !a->pos) return DLITE_ERR_INVALID_ARG;
       if (!(a->temperature > 0.f) || isinf(a->temperature)) return DLITE_ERR_INVALID_ARG;
       v.qs = a->qstats;
-      v.hs = a->hs ? a->hs : h->hs;
       v.probs = a->target_probs;
-      if (h->f32)
-        v.Ef = (const float*)h->E_src;
-      else
-        v.Eb = h->E[0];
+      set_q_source(h, &v, a->hs);
       v.resid = h->resid;
       v.counters = h->counters;
       v.T = (double)a->temperature;
@@ -1185,6 +1353,8 @@ int dlite_launch_count(dlite_handle* h, int B, float temperature) {
   const int L = B * (group_of(&h->cfg) + h->cfg.K);
   const bool fused = !tc::use_pair_engine(L, h->np, h->np);
   const int per_layer = (fused ? 8 : 9) - (fuse_ctx(h, B) ? 1 : 0);  // one product for [y; z] when fused
+  if (h->gated)  // head: {W_h u product, sum} + K x {prep, state product, gate, r product, r, lm, merge} + final
+    return 1 + per_layer * h->cfg.L_D + 2 + 7 * h->cfg.K + 1 + 1;
   return 1 + per_layer * h->cfg.L_D + 4 + 2 + 1;
 }
 

@@ -96,6 +96,35 @@ struct VerifyArgs {
   int32_t* tsamp = nullptr;            // match mode: the target's samples [B, K+1]
 };
 
+// The gated token-feedback head's per-step state (gated.cu).
+struct GatedArgs {
+  int B = 0, K = 0, R = 0, G = 1, V = 0;
+  const int32_t* anchor = nullptr;   // [B, G]: d_0 is the last
+  int32_t* cand_tmp = nullptr;       // [B] this step's choice (written by the LM merge)
+  dlite_qstats* qs_tmp = nullptr;    // [B]
+  int32_t* cand = nullptr;           // [B, K]
+  dlite_qstats* qs = nullptr;        // [B, K] or null
+  const int64_t* pos = nullptr;      // [B] or null
+  int64_t* pos_i = nullptr;          // [B] pos + i - 1 (the LM head's positions at step i)
+  const float* ER = nullptr;         // [V, R] fp32
+  const float* bs = nullptr;         // [2R]
+  const float* bh = nullptr;         // [R]
+  const float* hu = nullptr;         // [B*K, R] W_h[:, R:] u_i
+  float* s = nullptr;                // [B, R] state
+  bf16* xp[2] = {nullptr, nullptr};  // [B, 2R] planes of [s; v]
+  bf16* sp[2] = {nullptr, nullptr};  // [B, R] planes of s
+  float* r_all = nullptr;            // [B*K, R]
+  float* r_step = nullptr;           // [B, R]
+  bf16* rp = nullptr;                // [B, R] bf16(r) (the vocabulary product's activation)
+  int* status = nullptr;
+};
+cudaError_t launch_gated_prep(const GatedArgs& a, int i, cudaStream_t s);
+cudaError_t launch_gated_gate(const GatedArgs& a, const float* part, const Splits& sp, cudaStream_t s);
+cudaError_t launch_gated_r(const GatedArgs& a, int i, const float* part, const Splits& sp, cudaStream_t s);
+cudaError_t launch_gated_sum(const float* part, const Splits& sp, int rows, int cols, float* out,
+                             cudaStream_t s);
+cudaError_t launch_gated_final(const GatedArgs& a, cudaStream_t s);
+
 cudaError_t launch_stage(const StageArgs& a, bool f32, cudaStream_t s);
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s);
 size_t attention_smem(int K1, int m, int d_h, int G);  // K1 local rows per request

@@ -74,7 +74,12 @@ typedef struct {
                        * local positions 0..G-1, the placeholders at G..G+K-1, and the `anchor`
                        * argument of the draft calls is then [B, G] int32 (oldest first, the anchor
                        * last) */
+    int head_type;    /* DLITE_HEAD_RNN (0): the low-rank RNN head with one tied D->V projection;
+                       * DLITE_HEAD_GATED (1): the official gated token-feedback head (weights in
+                       * dlite_weights.gated; R a multiple of 64) */
 } dlite_config;
+
+enum dlite_head_type { DLITE_HEAD_RNN = 0, DLITE_HEAD_GATED = 1 };
 
 #define DLITE_MAX_LAYERS 8
 
@@ -96,6 +101,13 @@ typedef struct {
 typedef struct {
     const void *e_depth, *g_stage, *e_ph, *E, *g_final, *Q, *P;
     dlite_layer_weights layer[DLITE_MAX_LAYERS];
+    /* the gated token-feedback head ([P1] §"官方顺序头具体算了什么"), head_type 1 only:
+     *   E_R [V, R] token embedding of the head;  W_s [2R, 2R], b_s [2R] acting on
+     *   [s_{i-1}; v_i] (outputs g first, then c);  W_h [R, R + D], b_h [R] acting on
+     *   [s_i; u_i];  W_o [V, R] vocabulary projection. Q and P are then unused. */
+    struct {
+        const void *E_R, *W_s, *b_s, *W_h, *b_h, *W_o;
+    } gated;
 } dlite_weights;
 
 /* Draft statistics of one draft slot for sampling verification: the logit of
@@ -140,9 +152,9 @@ int dlite_draft_round(dlite_handle *h, int B, const void *hidden, const int32_t 
                       int32_t *candidates, dlite_qstats *qstats, dlite_stream_t stream);
 
 /* Optional intermediate outputs of a draft (device pointers, float32; any may
- * be NULL): z [B, m, D] staged context features; x [L_D, B, K+1, D] residual
+ * be NULL): z [B, m, D] staged context features; x [L_D, B, G+K, D] residual
  * stream after each layer; b [B, K, D] backbone outputs; hs [B, K, D]
- * sequential-head outputs. */
+ * sequential-head outputs (gated head: its vectors r_i, [B, K, R]). */
 typedef struct {
     float *z, *x, *b, *hs;
 } dlite_taps;

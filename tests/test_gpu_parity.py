@@ -492,6 +492,84 @@ def test_shift_group_matches_oracle(small_v):
             dr.close()
 
 
+# ---------------------------------------------------------------- gated token-feedback head
+
+@pytest.mark.parametrize("name", ["tiny", "bf16"])
+@pytest.mark.parametrize("T", [0.0, 0.7])
+def test_gated_head_round_parity(name, T):
+    """The official gated head: per-step vectors r_i and candidates (greedy and
+    sampled, token fed back each step) against the oracle."""
+    if name == "tiny":
+        cfg = wk.shrink(wk.TINY, R=64, head="gated")
+        W = wk.make_weights(cfg, 31, gain_jitter=True)
+        tol = 1e-4
+    else:
+        cfg = wk.shrink(wk.QWEN3_8B, D=512, F=1024, L_D=2, n_q=4, n_kv=2, R=128, V=4096, m=6, head="gated")
+        W = wk.make_weights(cfg, 32)
+        tol = HIDDEN_REL_TOL
+    wl = wk.WORKLOADS["tiny"]
+    B, seed = 12, 77
+    dr = _drafter(cfg, W, B_max=B)
+    try:
+        hidden, anchor, pos = wk.make_round_inputs(wl, B=B, cfg=cfg)
+        anchor = anchor % cfg.V
+        out = dr.new_outputs(B, DEV)
+        taps = {"z": torch.empty(B, cfg.m, cfg.D, device=DEV),
+                "x": torch.empty(cfg.L_D, B, cfg.K + 1, cfg.D, device=DEV),
+                "b": torch.empty(B, cfg.K, cfg.D, device=DEV),
+                "hs": torch.empty(B, cfg.K, cfg.R, device=DEV)}
+        dr.draft_round(hidden.to(DEV), anchor.to(DEV), T, seed, pos.to(DEV), out["cand"], out["qstats"],
+                       taps=taps)
+        torch.cuda.synchronize()
+        cand = out["cand"].cpu().numpy()
+        qs = out["qstats"].cpu().numpy()
+        cands, ocands, gaps = [], [], []
+        for b in range(B):
+            r = O.draft_request(hidden[b], int(anchor[b]), W, cfg, temperature=T, seed=seed, pos=int(pos[b]),
+                                request=b, mirror=(cfg.dtype == "bf16"))
+            if np.array_equal(cand[b], r["cand"]):   # same tokens fed back: the vectors agree
+                assert rel_err(taps["hs"][b].cpu(), r["h"]) < tol
+                if T > 0:
+                    assert np.allclose(qs[b, :, 1], r["lse"], rtol=1e-5, atol=1e-3)
+            else:                                    # a near-tie flipped a token: earlier steps still agree
+                k = int(np.argmax(cand[b] != r["cand"]))
+                assert rel_err(taps["hs"][b, :k + 1].cpu(), r["h"][:k + 1]) < tol
+            cands.append(cand[b])
+            ocands.append(r["cand"])
+            gaps.append(r["gap"])
+        check_candidates(np.stack(cands), np.stack(ocands), np.stack(gaps))
+    finally:
+        dr.close()
+
+
+def test_gated_head_sampling_verification():
+    """Sampling verification with the gated head: q(v) from W_o and the head's
+    r vectors kept by the handle; bit-exact against the oracle on identical inputs."""
+    cfg = wk.shrink(wk.TINY, R=64, V=512, head="gated")
+    W = wk.make_weights(cfg, 33)
+    B, T, seed = 64, 0.7, 5
+    dr = _drafter(cfg, W, B_max=B)
+    try:
+        wl = wk.WORKLOADS["tiny"]
+        hidden, anchor, pos = wk.make_round_inputs(wl, B=B, cfg=cfg)
+        anchor = anchor % cfg.V
+        out = dr.new_outputs(B, DEV)
+        rvec = torch.empty(B, cfg.K, cfg.R, device=DEV)
+        taps = {"z": None, "x": None, "b": None, "hs": rvec}
+        dr.draft_round(hidden.to(DEV), anchor.to(DEV), T, seed, pos.to(DEV), out["cand"], out["qstats"], taps=taps)
+        p = wk.make_target_probs(B, cfg.K, cfg.V, 9, device=DEV)
+        dr.verify_sample(out["cand"], out["qstats"], None, p, T, seed, pos.to(DEV), out["accepted"],
+                         out["commits"], out["n_commit"], out["next_anchor"])
+        torch.cuda.synchronize()
+        cand, qs, rv = out["cand"].cpu().numpy(), out["qstats"].cpu().numpy(), rvec.cpu().numpy()
+        acc, com, pn = out["accepted"].cpu().numpy(), out["commits"].cpu().numpy(), p.cpu().numpy()
+        for b in range(B):
+            o = O.verify_sample(cand[b], qs[b, :, 0], qs[b, :, 1], rv[b], W["W_o"], pn[b], T, seed, int(pos[b]), b)
+            assert acc[b] == o["A"] and list(com[b, :o["n_commit"]]) == o["commits"], (b, o)
+    finally:
+        dr.close()
+
+
 # ---------------------------------------------------------------- invariants and robustness
 
 def test_history_free_and_deterministic(tiny):
