@@ -155,6 +155,8 @@ def run_gpu(args):
         wl = dataclasses.replace(wl, name=f"{wl.name}-match")
     if nv is not None:
         wl = dataclasses.replace(wl, name=f"{wl.name}-nv{nv}")
+    if args.head == "gated":   # the official gated token-feedback head
+        wl = dataclasses.replace(wl, cfg=dataclasses.replace(wl.cfg, head="gated"), name=f"{wl.name}-gated")
     grp = max(1, args.group)
     if grp > 1:   # a local token group of G tokens ending at the anchor
         wl = dataclasses.replace(wl, cfg=dataclasses.replace(wl.cfg, G=grp), name=f"{wl.name}-G{grp}")
@@ -398,7 +400,8 @@ def oracle_request_seconds(wl, W64, hidden, anchor, pos, probs, b):
     r = O.draft_request(hidden, int(anchor), W64, cfg, temperature=T, seed=wl.rng_seed,
                         pos=int(pos), request=b)
     if T > 0:
-        O.verify_sample(r["cand"], r["logit_d"], r["lse"], r["h"], W64["E"], probs, T, wl.rng_seed,
+        w_q = W64["W_o"] if getattr(cfg, "head", "rnn") == "gated" else W64["E"]   # q(v) weights
+        O.verify_sample(r["cand"], r["logit_d"], r["lse"], r["h"], w_q, probs, T, wl.rng_seed,
                         int(pos), b)
     else:
         O.verify_greedy(r["cand"], list(r["cand"]) + [0])
@@ -481,6 +484,7 @@ def main():
                     help="match: greedy draft verified against the target's own samples")
     ap.add_argument("--n-verify", type=int, default=-1, help="verification window (candidates verified; -1: all)")
     ap.add_argument("--group", type=int, default=1, help="local token group size G (anchor last)")
+    ap.add_argument("--head", default="rnn", choices=["rnn", "gated"], help="sequential head")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
