@@ -117,6 +117,56 @@ def block_attention(q, k, v, n_q, n_kv):
     return out.reshape(q.shape[0], n_q * d_h)
 
 
+# ---------------------------------------------------------------- history-KV control
+
+def history_values(H, n_kv, d_h, layer, request, which):
+    """Synthetic history rows of the control drafter, [H, n_kv, d_h], bf16 values.
+
+    Element (slot t, head g, column d) of K (which = 0) or V (which = 1) of a
+    layer and request: with the four uniforms u0..u3 of Philox(counter =
+    (t d_h + d, (2 layer + which) n_kv + g, request, TAG_HIST), key = HIST_SEED),
+    bf16(float32((u0 + u1 + u2 + u3 - 2) * sqrt(3))) -- mean 0, variance 1, a
+    stand-in for the N(0, 1) history of the control workload; every step is
+    computed in float32 so that the GPU forms the same bits.
+    """
+    t = np.arange(H, dtype=np.int64)[:, None, None]
+    g = np.arange(n_kv, dtype=np.int64)[None, :, None]
+    d = np.arange(d_h, dtype=np.int64)[None, None, :]
+    k0, k1 = _ph.seed_key(_ph.HIST_SEED)
+    w = _ph.philox4x32_10(t * d_h + d, (2 * layer + which) * n_kv + g, request, _ph.TAG_HIST, k0, k1)
+    u = [_ph.uniform_open(x).astype(np.float32) for x in w]
+    acc = ((u[0] + u[1]) + u[2]) + u[3]
+    val = (acc - np.float32(2.0)) * np.float32(1.7320508075688772)
+    return bf16_round(val.astype(np.float64))
+
+
+class HistoryCache:
+    """The control drafter's per-layer draft KV of one request: a ring of the
+    last H local K/V rows ([P1] §"本轮临时 K/V 仍然需要计算": a conventional
+    drafter keeps its own KV and it grows with the history; here a window of
+    H rows), initially the synthetic history_values. Each round attends over
+    the H cached rows beside the block, then writes its G + K local rows at
+    slots (cursor + j) mod H and advances the cursor."""
+
+    def __init__(self, cfg, H, request):
+        self.H = H
+        self.cursor = 0
+        self.k = [history_values(H, cfg.n_kv, cfg.d_h, l, request, 0) for l in range(cfg.L_D)]
+        self.v = [history_values(H, cfg.n_kv, cfg.d_h, l, request, 1) for l in range(cfg.L_D)]
+
+    def layer(self, l):
+        return self.k[l], self.v[l]
+
+    def append(self, local):
+        """local: per layer (k_loc, v_loc) [G+K, n_kv, d_h] of the finished round."""
+        n = local[0][0].shape[0]
+        slots = (self.cursor + np.arange(n)) % self.H
+        for l, (k_loc, v_loc) in enumerate(local):
+            self.k[l][slots] = k_loc
+            self.v[l][slots] = v_loc
+        self.cursor = (self.cursor + n) % self.H
+
+
 def silu(x):
     return x / (1.0 + np.exp(-x))
 
@@ -155,7 +205,7 @@ def stage(hidden, anchor, W, cfg, mirror=False):
     return z, x
 
 
-def backbone_layer(x, z, Wl, cfg, mirror=False):
+def backbone_layer(x, z, Wl, cfg, mirror=False, hist=None, local_out=None):
     """One pre-norm block over [m context slots | anchor group | K placeholders].
 
     Queries exist only for the anchor and placeholders; keys/values for the
@@ -178,6 +228,11 @@ def backbone_layer(x, z, Wl, cfg, mirror=False):
     v_ctx = _r((z @ f64(Wl["Wv"]).T).reshape(-1, n_kv, d_h), mirror)
     k_all = np.concatenate([k_ctx, k_loc], axis=0)
     v_all = np.concatenate([v_ctx, v_loc], axis=0)
+    if hist is not None:   # the control's draft KV: H more keys / values beside the block
+        k_all = np.concatenate([hist[0], k_all], axis=0)
+        v_all = np.concatenate([hist[1], v_all], axis=0)
+    if local_out is not None:
+        local_out.append((k_loc, v_loc))
     o = _r(block_attention(q, k_all, v_all, n_q, n_kv), mirror)
     x = x + o @ f64(Wl["Wo"]).T
     y2 = _r(rmsnorm(x, Wl["g_ffn"], cfg.eps), mirror)
@@ -185,7 +240,7 @@ def backbone_layer(x, z, Wl, cfg, mirror=False):
     return x + a @ f64(Wl["Wd"]).T
 
 
-def backbone(hidden, anchor, W, cfg, mirror=False, taps=None):
+def backbone(hidden, anchor, W, cfg, mirror=False, taps=None, history=None, local_out=None):
     """Parallel backbone: b_i = RMSNorm(x_i) * g_final for placeholders i=1..K.
 
     [P1] §"主干并行输出的是表示,还不是有因果联系的完整候选": the backbone
@@ -195,8 +250,8 @@ def backbone(hidden, anchor, W, cfg, mirror=False, taps=None):
     if taps is not None:
         taps["z"] = z
         taps["x"] = []
-    for Wl in W["layers"]:
-        x = backbone_layer(x, z, Wl, cfg, mirror)
+    for l, Wl in enumerate(W["layers"]):
+        x = backbone_layer(x, z, Wl, cfg, mirror, history.layer(l) if history is not None else None, local_out)
         if taps is not None:
             taps["x"].append(x.copy())
     return rmsnorm(x[cfg.G:], W["g_final"], cfg.eps)
@@ -295,7 +350,7 @@ def _top2_gap(s):
 
 
 def draft_request(hidden, anchor, W, cfg, temperature=0.0, seed=0, pos=0, request=0,
-                  mirror=False, taps=None):
+                  mirror=False, taps=None, history=None):
     """One request's draft: candidates d_1..d_K plus what verification needs.
 
     Greedy (T = 0): d_i = argmax_v l_iv (lowest id on ties).
@@ -306,7 +361,10 @@ def draft_request(hidden, anchor, W, cfg, temperature=0.0, seed=0, pos=0, reques
     Returns dict(cand, logit_d, lse, gap, b, h).
     """
     temperature = float(np.float32(temperature))   # a float32 quantity, as in the C ABI
-    b = backbone(hidden, anchor, W, cfg, mirror, taps)
+    local = [] if history is not None else None
+    b = backbone(hidden, anchor, W, cfg, mirror, taps, history, local)
+    if history is not None:   # the round's local rows join the draft KV afterwards
+        history.append(local)
     if getattr(cfg, "head", "rnn") == "gated":   # token feedback: vocabulary projection inside each step
         r = gated_head(b, anchor_group(anchor, cfg)[-1], W, temperature, seed, pos, request)
         if taps is not None:

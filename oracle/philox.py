@@ -28,6 +28,8 @@ TAG_ACCEPT = 2
 TAG_RESID = 3
 TAG_BONUS = 4
 TAG_MATCH = 5   # the target's own sample at each position (match verification)
+TAG_HIST = 6    # synthetic history K/V of the history-KV control
+HIST_SEED = 0x4849535400000001   # fixed key of the synthetic history
 
 _MASK = np.uint64(0xFFFFFFFF)
 

@@ -351,6 +351,82 @@ def test_gated_head_sampling_follows_softmax():
     assert abs(out["lse"][0] - want) < 1e-9
 
 
+# ---------------------------------------------------------------- history-KV control
+
+def test_history_values_statistics_and_keying():
+    """Synthetic history: bf16 values with mean 0, variance 1 (a sum of four
+    uniforms), different for every (layer, request, K/V) key."""
+    a = O.history_values(512, 2, 64, 0, 0, 0)
+    assert np.array_equal(a, O.bf16_round(a))
+    assert abs(a.mean()) < 0.02 and abs(a.var() - 1.0) < 0.03
+    assert abs(a.max()) <= 2 * math.sqrt(3.0) + 1e-6
+    others = [O.history_values(512, 2, 64, 1, 0, 0), O.history_values(512, 2, 64, 0, 1, 0),
+              O.history_values(512, 2, 64, 0, 0, 1)]
+    for b in others:
+        assert np.corrcoef(a.ravel(), b.ravel())[0, 1] < 0.05
+
+
+def test_history_is_an_unordered_set_of_extra_keys():
+    """The history rows are plain extra keys / values (no position): permuting
+    the ring's slots changes nothing, while the history does change the round;
+    and a zero-key history with constant values c mixes c in with weight
+    H / (H + sum_j exp(s_j)) per query."""
+    cfg = _tiny(L_D=1)
+    W = _weights(cfg)
+    hidden, _, _ = wk.make_round_inputs(wk.WORKLOADS["tiny"], B=1)
+    H = 40
+    h1 = O.HistoryCache(cfg, H, 0)
+    h2 = O.HistoryCache(cfg, H, 0)
+    perm = np.random.default_rng(3).permutation(H)
+    h2.k[0], h2.v[0] = h2.k[0][perm], h2.v[0][perm]
+    b1 = O.backbone(hidden[0], 5, W, cfg, history=h1)
+    b2 = O.backbone(hidden[0], 5, W, cfg, history=h2)
+    assert np.allclose(b1, b2, atol=1e-12)
+    assert not np.allclose(b1, O.backbone(hidden[0], 5, W, cfg), atol=1e-6)
+    rng = np.random.default_rng(4)
+    n_q, n_kv, d_h, T = 4, 2, 8, 6
+    q, k, v = rng.normal(size=(3, n_q, d_h)), rng.normal(size=(T, n_kv, d_h)), rng.normal(size=(T, n_kv, d_h))
+    c = rng.normal(size=(n_kv, d_h))
+    kh = np.zeros((H, n_kv, d_h))
+    vh = np.broadcast_to(c, (H, n_kv, d_h))
+    got = O.block_attention(q, np.concatenate([kh, k]), np.concatenate([vh, v]), n_q, n_kv).reshape(3, n_q, d_h)
+    base = O.block_attention(q, k, v, n_q, n_kv).reshape(3, n_q, d_h)
+    for h in range(n_q):
+        g = h // (n_q // n_kv)
+        Z = np.exp(q[:, h] @ k[:, g].T / math.sqrt(d_h)).sum(axis=1)
+        want = (base[:, h] * Z[:, None] + H * c[g][None, :]) / (Z + H)[:, None]
+        assert np.allclose(got[:, h], want, atol=1e-12)
+
+
+def test_history_ring_holds_the_last_rounds():
+    """After each round the ring holds that round's local K/V rows at slots
+    (cursor + j) mod H; older rows survive until overwritten."""
+    cfg = _tiny(L_D=2)
+    W = _weights(cfg)
+    hidden, _, _ = wk.make_round_inputs(wk.WORKLOADS["tiny"], B=1)
+    H, K1 = 12, cfg.K + 1
+    hc = O.HistoryCache(cfg, H, 2)
+    init_k1 = hc.k[1].copy()
+    seen = []
+    for rnd in range(4):
+        local = []
+        O.backbone(hidden[0], rnd + 1, W, cfg, history=hc, local_out=local)
+        before = hc.cursor
+        hc.append(local)
+        seen.append((before, local))
+    for rnd, (cur, local) in enumerate(seen):
+        for j in range(K1):
+            slot = (cur + j) % H
+            newer = any(((slot - c2) % H) < K1 for c2, _ in seen[rnd + 1:])
+            if not newer:
+                assert np.array_equal(hc.k[1][slot], local[1][0][j])
+                assert np.array_equal(hc.v[0][slot], local[0][1][j])
+    untouched = set(range(H)) - {(c + j) % H for c, _ in seen for j in range(K1)}
+    for slot in untouched:
+        assert np.array_equal(hc.k[1][slot], init_k1[slot])
+    assert hc.cursor == (4 * K1) % H
+
+
 # ---------------------------------------------------------------- sequential head
 
 def test_head_with_zero_P_is_identity():
