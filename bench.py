@@ -160,6 +160,9 @@ def run_gpu(args):
     grp = max(1, args.group)
     if grp > 1:   # a local token group of G tokens ending at the anchor
         wl = dataclasses.replace(wl, cfg=dataclasses.replace(wl.cfg, G=grp), name=f"{wl.name}-G{grp}")
+    if args.history > 0:   # the history-KV control: a ring of the last H draft K/V rows per layer
+        wl = dataclasses.replace(wl, cfg=dataclasses.replace(wl.cfg, history=args.history),
+                                 name=f"{wl.name}-H{args.history}")
     cfg = wl.cfg
     B = wl.B
     T = 0.0 if match else wl.temperature
@@ -282,14 +285,15 @@ def run_gpu(args):
                                target_probs=it.get("probs"), stream=stream)
         for name, t in times:
             per.setdefault(name, []).append(t)
-    per_launch = {n: sum(v) / len(v) for n, v in per.items()}   # ms per round (summed over launches)
+    per_launch = {n: sum(v) / len(v) for n, v in per.items()}   # ms per launch (mean over a name's launches)
     counts = {}
     for name, _ in times:
         counts[name] = counts.get(name, 0) + 1
     hbm, tf_burst, tf_sus, peak_src = measured_peaks()
-    lm_ms = per_launch.get("lm_head", float("nan")) / counts.get("lm_head", 1)
-    lm_bytes = rp.lm_head_bytes(cfg, B)
-    lm_flops = rp.lm_head_flops(cfg, B)
+    lm_ms = per_launch.get("lm_head", float("nan"))
+    gated = getattr(cfg, "head", "rnn") == "gated"   # one W_o projection per step
+    lm_bytes = rp.gated_lm_bytes(cfg, B) if gated else rp.lm_head_bytes(cfg, B)
+    lm_flops = rp.gated_lm_flops(cfg, B) if gated else rp.lm_head_flops(cfg, B)
     achieved_gbs = lm_bytes / (lm_ms / 1e3) / 1e9
     achieved_tf = lm_flops / (lm_ms / 1e3) / 1e12
     t_bytes = lm_bytes / (hbm * 1e9)
@@ -301,10 +305,18 @@ def run_gpu(args):
     else:
         roof = {"bound": "tensor", "achieved": round(achieved_tf, 1), "peak": tf_sus, "unit": "TFLOP/s",
                 "frac": round(achieved_tf / tf_sus, 4)}
-    traffic = lm_head_traffic() if (cfg.D == 4096 and B == 32) else None
+    traffic = lm_head_traffic() if (cfg.D == 4096 and B == 32 and not cfg.history) else None
     roof.update({"kernel": "lm_head", "traffic": traffic, "peak_source": peak_src,
                  "algorithmic_bytes_per_launch": lm_bytes, "algorithmic_flops_per_launch": lm_flops,
                  "ms_per_launch": round(lm_ms, 4)})
+    if cfg.history:   # the control's dominant kernel: the history attention (one launch per layer)
+        h_ms = per_launch.get("hist_attn", float("nan"))
+        h_bytes = rp.hist_attn_bytes(cfg, B)
+        h_gbs = h_bytes / (h_ms / 1e3) / 1e9
+        lm_roof = roof
+        roof = {"bound": "hbm", "achieved": round(h_gbs, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(h_gbs / hbm, 4), "kernel": "hist_attn", "traffic": None, "peak_source": peak_src,
+                "algorithmic_bytes_per_launch": h_bytes, "ms_per_launch": round(h_ms, 4), "lm_head": lm_roof}
     round_bytes = rp.round_bytes(cfg, B)
     round_flops = rp.round_flops(cfg, B)
     floor = rp.roofline_floor_s(round_bytes, round_flops, hbm, tf_sus)
@@ -323,7 +335,8 @@ def run_gpu(args):
         "config": {"workload": wl.name, "B_per_gpu": B, "D": cfg.D, "m": cfg.m, "K": cfg.K,
                    "L_D": cfg.L_D, "F": cfg.F, "R": cfg.R, "V": cfg.V, "temperature": T,
                    "parallelism": f"replicas x{ws}", "l2": "inputs larger than L2 (2.4 GB of weights "
-                   "streamed per round, 4-batch input ring)"},
+                   "streamed per round, 4-batch input ring)", "history": cfg.history,
+                   "draft_kv_bytes": 2 * cfg.L_D * cfg.history * cfg.n_kv * cfg.d_h * 2 * B},
         "committed_tok_s": round(tok_s, 1),
         "round_roofline": {"floor_ms": round(floor * 1e3, 4), "frac": round(floor / (ms_step / 1e3), 4),
                            "bytes": round_bytes, "flops": round_flops, "peak_source": peak_src},
@@ -337,7 +350,7 @@ def run_gpu(args):
         "e2e": e2e,
     }
     if rank == 0:
-        if ws == 1 and not args.no_cpu_baseline:
+        if ws == 1 and not args.no_cpu_baseline and not cfg.history:
             result["cpu_baseline"] = cpu_baseline(wl, W, ring, anchor, pos)
         print(json.dumps(result), flush=True)
     dr.close()
@@ -485,6 +498,8 @@ def main():
     ap.add_argument("--n-verify", type=int, default=-1, help="verification window (candidates verified; -1: all)")
     ap.add_argument("--group", type=int, default=1, help="local token group size G (anchor last)")
     ap.add_argument("--head", default="rnn", choices=["rnn", "gated"], help="sequential head")
+    ap.add_argument("--history", type=int, default=0,
+                    help="history-KV control: ring of the last H draft K/V rows per layer (0: history-free)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -31,7 +31,7 @@ class Config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
                 ("B_max", "D", "m", "K", "L_D", "n_q", "n_kv", "d_h", "F", "R", "V", "dtype")] + \
                [("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float), ("anchor_group", ctypes.c_int),
-                ("head_type", ctypes.c_int)]
+                ("head_type", ctypes.c_int), ("history", ctypes.c_int)]
 
 
 class LayerWeights(ctypes.Structure):
@@ -88,6 +88,8 @@ _SIGS = {
     "dlite_verify_ex": (_I, [_P, ctypes.POINTER(VerifyArgs), _P]),
     "dlite_advance": (_I, [_P, _I, _P, _P, _P]),
     "dlite_shift_group": (_I, [_P, _I, _P, _P, _P, _P]),
+    "dlite_history_reset": (_I, [_P, _P]),
+    "dlite_history_read": (_I, [_P, _I, _I, _I, _P, ctypes.POINTER(ctypes.c_int32), _P]),
     "dlite_verify_sample_static": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _F, _U64, _P, _P, _P,
                                         _P, _P, _P]),
     "dlite_round_host": (_I, [_P, _I, _P, _P, _P, _P, _P, _F, _U64, _P, _P, _P, _P, _P]),
@@ -195,7 +197,8 @@ def config_struct(cfg, B_max):
                   n_kv=cfg.n_kv, d_h=cfg.d_h, F=cfg.F, R=cfg.R, V=cfg.V,
                   dtype=DLITE_F32 if cfg.dtype == "f32" else DLITE_BF16,
                   rms_eps=cfg.eps, rope_theta=cfg.theta, anchor_group=getattr(cfg, "G", 1),
-                  head_type=1 if getattr(cfg, "head", "rnn") == "gated" else 0)
+                  head_type=1 if getattr(cfg, "head", "rnn") == "gated" else 0,
+                  history=getattr(cfg, "history", 0))
 
 
 class Drafter:
@@ -296,6 +299,19 @@ class Drafter:
                        pos=_ptr(pos), accepted=_ptr(accepted), commits=_ptr(commits),
                        n_commit=_ptr(n_commit), next_anchor=_ptr(next_anchor))
         _check(self.lib.dlite_verify_ex(self.h, ctypes.byref(a), _stream(stream)), "dlite_verify_ex")
+
+    def history_reset(self, stream=None):
+        """Refill every draft-KV ring with the synthetic history; cursors to 0."""
+        _check(self.lib.dlite_history_reset(self.h, _stream(stream)), "dlite_history_reset")
+
+    def history_read(self, layer, request, which, stream=None):
+        """One ring of the history-KV control: ([n_kv, H, d_h] bf16 on the device, cursor)."""
+        c = self.cfg
+        dst = torch.empty(c.n_kv, c.history, c.d_h, dtype=torch.bfloat16, device="cuda")
+        cur = ctypes.c_int32(0)
+        _check(self.lib.dlite_history_read(self.h, layer, request, which, _ptr(dst), ctypes.byref(cur),
+                                           _stream(stream)), "dlite_history_read")
+        return dst, int(cur.value)
 
     def shift_group(self, commits, n_commit, group, stream=None):
         _check(self.lib.dlite_shift_group(self.h, n_commit.shape[0], _ptr(commits), _ptr(n_commit), _ptr(group),

@@ -4,6 +4,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <vector>
 
 #include "kernels.h"
@@ -58,6 +59,14 @@ struct dlite_handle {
   dlite_qstats* g_qs = nullptr;
   int64_t* g_pos = nullptr;
   float *rope_cos = nullptr, *rope_sin = nullptr;
+  // history-KV control (cfg.history = H > 0)
+  int H = 0, hQR = 0, hTk = 0, hHx = 0;  // Hx = H + m + G + K rows per (request, head)
+  size_t hrows = 0;                       // rows of one layer's key (value) tensor
+  bf16 *hk_ring = nullptr, *hv_ring = nullptr;   // [L_D][hrows][d_h]: ring, then the block's rows
+  CUtensorMap hmap_k[DLITE_MAX_LAYERS], hmap_v[DLITE_MAX_LAYERS];  // 64-row x 64-column boxes
+  int* hcursor = nullptr;                        // [B_max]
+  bf16* hst_q = nullptr;                         // the rotated block queries of one layer
+  float *hpart_o = nullptr, *hpart_ml = nullptr;  // chunk partials
 
   // workspace
   float* x = nullptr;
@@ -152,6 +161,10 @@ int check_config(const dlite_config* c) {
   if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return DLITE_ERR_INVALID_ARG;
   if (c->head_type != DLITE_HEAD_RNN && c->head_type != DLITE_HEAD_GATED) return DLITE_ERR_INVALID_ARG;
   if (c->head_type == DLITE_HEAD_GATED && c->R % 64) return DLITE_ERR_UNSUPPORTED_SHAPE;
+  if (c->history < 0) return DLITE_ERR_INVALID_ARG;
+  if (c->history > 0 && (c->dtype != DLITE_BF16 || c->history < group_of(c) + c->K || c->history > (1 << 20) ||
+                         (c->n_q / c->n_kv) * (group_of(c) + c->K) > 128))
+    return DLITE_ERR_UNSUPPORTED_SHAPE;
   return DLITE_OK;
 }
 
@@ -340,6 +353,50 @@ static bool fuse_ctx(const dlite_handle* h, int B) {
          tc::stream_plan(rows, h->qd + 2 * h->kvd, c.D, h->num_sms).ok;
 }
 
+// History-KV control, layer l: split-KV attention of the block's queries over
+// the ring and the block, then the merge into h->o and the ring append.
+int run_history_attention(dlite_handle* h, int B, int l, cudaStream_t s) {
+  const dlite_config& c = h->cfg;
+  const HistPlan hp = hist_plan(B, c.n_kv, h->H, h->hTk, h->hQR, c.d_h, h->num_sms);
+  const size_t ring_l = (size_t)l * h->hrows * c.d_h;
+  HistAttnArgs ha;
+  ha.q = h->hst_q;
+  ha.B = B;
+  ha.n_kv = c.n_kv;
+  ha.H = h->H;
+  ha.Hx = h->hHx;
+  ha.Tk = h->hTk;
+  ha.QR = h->hQR;
+  ha.sub_per_chunk = hp.sub_per_chunk;
+  ha.nchunk = hp.nchunk;
+  ha.scale_log2 = (float)(1.4426950408889634 / sqrt((double)c.d_h));
+  ha.part_o = h->hpart_o;
+  ha.part_ml = h->hpart_ml;
+  ha.status = h->status;
+  CK(launch_hist_attn(&h->hmap_k[l], &h->hmap_v[l], ha, c.d_h, s));
+  mark(h, "hist_attn");
+  HistCombineArgs hc;
+  hc.part_o = h->hpart_o;
+  hc.part_ml = h->hpart_ml;
+  hc.B = B;
+  hc.n_q = c.n_q;
+  hc.n_kv = c.n_kv;
+  hc.d_h = c.d_h;
+  hc.QR = h->hQR;
+  hc.K1 = group_of(&c) + c.K;
+  hc.m = c.m;
+  hc.H = h->H;
+  hc.Hx = h->hHx;
+  hc.nchunk = hp.nchunk * hist_key_splits(h->hQR);
+  hc.o = h->o[0];
+  hc.kc = h->hk_ring + ring_l;
+  hc.vc = h->hv_ring + ring_l;
+  hc.cursor = h->hcursor;
+  CK(launch_hist_combine(hc, s));
+  mark(h, "hist_combine");
+  return DLITE_OK;
+}
+
 int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anchor,
                  const dlite_taps* taps, cudaStream_t s) {
   const dlite_config& c = h->cfg;
@@ -415,8 +472,16 @@ int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anch
     at.o[0] = h->o[0];
     at.o[1] = h->o[1];
     at.no = h->np;
+    if (h->H) {
+      at.hist_q = h->hst_q;
+      at.hist_k = h->hk_ring + (size_t)l * h->hrows * c.d_h;
+      at.hist_v = h->hv_ring + (size_t)l * h->hrows * c.d_h;
+      at.hist_ld = h->hHx;
+      at.hist_off = h->H;
+    }
     CK(launch_attention(at, s));
     mark(h, "attention");
+    if (h->H) RUN(run_history_attention(h, B, l, s));
     // O projection + residual, then the FFN pre-norm
     RUN(gemm(h, "gemm_o", opnd(h->o, h->np, h->Lcap, h->qd), opnd(w.Wo, h->np, c.D, h->qd), L, c.D,
              h->part, &S1, s));
@@ -461,6 +526,10 @@ int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anch
     }
     CK(launch_resnorm(r2, s));
     mark(h, "resnorm");
+  }
+  if (h->H) {  // the round's rows are in every layer's ring: move the cursors on
+    CK(launch_hist_advance(h->hcursor, B, G + c.K, h->H, s));
+    mark(h, "hist_advance");
   }
   return DLITE_OK;
 }
@@ -932,6 +1001,28 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
   AL(h->d_commits, (size_t)Bm * (c.K + 1));
   AL(h->d_ncommit, Bm);
   AL(h->d_next, Bm);
+  if (c.history > 0) {  // the conventional drafter's draft KV and the history kernels' buffers
+    const int K1 = group_of(&c) + c.K;
+    h->H = c.history;
+    h->hQR = (c.n_q / c.n_kv) * K1;
+    h->hTk = c.m + K1;
+    h->hHx = h->H + h->hTk;
+    h->hrows = std::max<size_t>((size_t)Bm * c.n_kv * h->hHx, 64);
+    const size_t ring = (size_t)c.L_D * h->hrows * c.d_h;
+    AL(h->hk_ring, ring);
+    AL(h->hv_ring, ring);
+    for (int l = 0; l < c.L_D; ++l)
+      if (!tc::make_map(&h->hmap_k[l], h->hk_ring + (size_t)l * h->hrows * c.d_h, (int)h->hrows, c.d_h, 64) ||
+          !tc::make_map(&h->hmap_v[l], h->hv_ring + (size_t)l * h->hrows * c.d_h, (int)h->hrows, c.d_h, 64))
+        return DLITE_ERR_CUDA;
+    AL(h->hcursor, Bm);
+    AL(h->hst_q, (size_t)Bm * c.n_kv * h->hQR * c.d_h);
+    const size_t prow =
+        (size_t)(hist_max_ctas(h->num_sms) + (long long)Bm * c.n_kv) * hist_key_splits(h->hQR) * h->hQR;
+    AL(h->hpart_o, prow * c.d_h);
+    AL(h->hpart_ml, prow * 2);
+    RUN(dlite_history_reset(h, nullptr));
+  }
   CK(cudaDeviceSynchronize());
   return DLITE_OK;
 }
@@ -1344,6 +1435,41 @@ int dlite_counters(dlite_handle* h, int reset, int64_t* out, dlite_stream_t stre
   return DLITE_OK;
 }
 
+int dlite_history_reset(dlite_handle* h, dlite_stream_t stream) {
+  if (!h || !h->H) return DLITE_ERR_INVALID_ARG;
+  HistFillArgs f;
+  f.k = h->hk_ring;
+  f.v = h->hv_ring;
+  f.cursor = h->hcursor;
+  f.L = h->cfg.L_D;
+  f.Bm = h->cfg.B_max;
+  f.n_kv = h->cfg.n_kv;
+  f.H = h->H;
+  f.Hx = h->hHx;
+  f.rows = h->hrows;
+  f.d_h = h->cfg.d_h;
+  CK(launch_hist_fill(f, (cudaStream_t)stream));
+  return DLITE_OK;
+}
+
+int dlite_history_read(dlite_handle* h, int layer, int request, int which, void* dst, int32_t* cursor,
+                       dlite_stream_t stream) {
+  if (!h || !h->H || !dst || layer < 0 || layer >= h->cfg.L_D || request < 0 || request >= h->cfg.B_max ||
+      (which != 0 && which != 1))
+    return DLITE_ERR_INVALID_ARG;
+  const dlite_config& c = h->cfg;
+  const size_t row = (size_t)c.d_h * sizeof(bf16);
+  const bf16* src = (which ? h->hv_ring : h->hk_ring) + (size_t)layer * h->hrows * c.d_h +
+                    (size_t)request * c.n_kv * h->hHx * c.d_h;
+  cudaStream_t s = (cudaStream_t)stream;
+  CK(cudaMemcpy2DAsync(dst, h->H * row, src, h->hHx * row, h->H * row, c.n_kv, cudaMemcpyDeviceToDevice, s));
+  if (cursor) {
+    CK(cudaMemcpyAsync(cursor, h->hcursor + request, sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+    CK(cudaStreamSynchronize(s));
+  }
+  return DLITE_OK;
+}
+
 int dlite_launch_count(dlite_handle* h, int B, float temperature) {
   if (!h || B < 1) return -1;
   (void)temperature;
@@ -1353,9 +1479,11 @@ int dlite_launch_count(dlite_handle* h, int B, float temperature) {
   const int L = B * (group_of(&h->cfg) + h->cfg.K);
   const bool fused = !tc::use_pair_engine(L, h->np, h->np);
   const int per_layer = (fused ? 8 : 9) - (fuse_ctx(h, B) ? 1 : 0);  // one product for [y; z] when fused
+  // history-KV control: + {history attention, combine} per layer + the cursor advance
+  const int hist = h->H ? 2 * h->cfg.L_D + 1 : 0;
   if (h->gated)  // head: {W_h u product, sum} + K x {prep, state product, gate, r product, r, lm, merge} + final
-    return 1 + per_layer * h->cfg.L_D + 2 + 7 * h->cfg.K + 1 + 1;
-  return 1 + per_layer * h->cfg.L_D + 4 + 2 + 1;
+    return 1 + per_layer * h->cfg.L_D + hist + 2 + 7 * h->cfg.K + 1 + 1;
+  return 1 + per_layer * h->cfg.L_D + hist + 4 + 2 + 1;
 }
 
 }  // extern "C"

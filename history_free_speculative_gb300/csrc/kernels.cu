@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(kAttnThreads, kMinCtas) attention_kernel(AttnA
   }
   __syncthreads();
   // padding rows of the tensor-core tiles hold zeros
-  const bool tensor = a.round_bf16 && QR >= 32;
+  const bool tensor = a.round_bf16 && QR >= 32 && !a.hist_q;
   for (int idx = threadIdx.x; tensor && idx < ((QRp - QR) + 2 * (Tkp - Tk)) * dh; idx += blockDim.x) {
     const int r = idx / dh, d = idx % dh;
     float* row = r < QRp - QR ? qs + (QR + r) * LD
@@ -275,6 +275,24 @@ __global__ void __launch_bounds__(kAttnThreads, kMinCtas) attention_kernel(AttnA
                          x2.w * c.w + x1.w * sn.w));
   }
   __syncthreads();
+  if (a.hist_q) {  // history mode: the rotated, bf16-rounded block goes to the history kernels
+    const int hpg = a.n_q / a.n_kv, hh0 = h0 - g * hpg;
+    const size_t bg = (size_t)b * a.n_kv + g;
+    auto put4 = [](bf16* dst, const float* src) {
+      const float4 v = *reinterpret_cast<const float4*>(src);
+      __nv_bfloat162 p[2] = {__floats2bfloat162_rn(v.x, v.y), __floats2bfloat162_rn(v.z, v.w)};
+      *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<uint2*>(p);
+    };
+    for (int idx = threadIdx.x; idx < QR * d4; idx += blockDim.x) {
+      const int r = idx / d4, d = (idx % d4) * 4, hh = r / K1, i = r % K1;
+      put4(a.hist_q + (bg * hpg * K1 + (size_t)(hh0 + hh) * K1 + i) * dh + d, qs + r * LD + d);
+    }
+    for (int idx = threadIdx.x; hh0 == 0 && idx < 2 * Tk * d4; idx += blockDim.x) {
+      const int kv = idx / (Tk * d4), t = idx % (Tk * d4), j = t / d4, d = (t % d4) * 4;
+      put4((kv ? a.hist_v : a.hist_k) + (bg * a.hist_ld + a.hist_off + j) * dh + d, (kv ? vs : ks) + j * LD + d);
+    }
+    return;
+  }
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   if (tensor) {

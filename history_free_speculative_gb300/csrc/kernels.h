@@ -1,6 +1,8 @@
 // Argument blocks and launchers of the non-GEMM kernels.
 #pragma once
 
+#include <cuda.h>
+
 #include "internal.h"
 
 namespace dlite {
@@ -41,6 +43,14 @@ struct AttnArgs {
   int round_bf16 = 0;
   bf16* o[2] = {nullptr, nullptr};  // [B*(K+1), n_q*d_h]
   int no = 1;
+  // history mode (bf16 values): instead of attending, hand the rotated block to
+  // the history kernels: queries [B][n_kv][(n_q/n_kv) K1][d_h] (row hh K1 + i);
+  // block keys / values (context rows, then local rows) at rows
+  // (b n_kv + g) hist_ld + hist_off + j of the layer's key / value tensors
+  bf16* hist_q = nullptr;
+  bf16* hist_k = nullptr;
+  bf16* hist_v = nullptr;
+  int hist_ld = 0, hist_off = 0;
 };
 
 struct ResNormArgs {
@@ -153,5 +163,49 @@ cudaError_t launch_repack_gate_up(const void* Wg, const void* Wu, bool src_f32, 
                                   int np, cudaStream_t s);
 cudaError_t launch_head_matrix(const void* Q, const void* P, bool f32, int D, int R, float* Mt,
                                cudaStream_t s);
+
+// ---------------------------------------------------------------- history-KV control
+// Per layer one key and one value tensor of `rows` rows x d_h bf16: row
+// (b n_kv + g) Hx + t holds ring slot t < H of request slot b, head g, and
+// rows H .. H + m + G + K - 1 behind it the current block's rows (so a head's
+// keys are one contiguous run); rows past B_max n_kv Hx are padding.
+struct HistFillArgs {
+  bf16* k = nullptr;  // [L][rows][d_h]
+  bf16* v = nullptr;
+  int* cursor = nullptr;  // [B_max], zeroed
+  int L = 0, Bm = 0, n_kv = 0, H = 0, Hx = 0, d_h = 0;
+  size_t rows = 0;
+};
+struct HistAttnArgs {
+  const bf16* q = nullptr;   // [B][n_kv][QR][d_h] the block's rotated queries
+  int B = 0, n_kv = 0, H = 0, Hx = 0, Tk = 0, QR = 0;
+  int sub_per_chunk = 1, nchunk = 1;  // 64-key sub-tiles per chunk; chunks
+  float scale_log2 = 1.f;             // softmax scale x log2(e)
+  float* part_o = nullptr;            // [B][n_kv][nchunk][KS][QR][d_h] (KS = hist_key_splits(QR))
+  float* part_ml = nullptr;           // [B][n_kv][nchunk][KS][QR][2]: running max (log2 domain), sum
+  int* status = nullptr;              // copy timeouts
+};
+struct HistCombineArgs {
+  const float* part_o = nullptr;
+  const float* part_ml = nullptr;
+  int B = 0, n_q = 0, n_kv = 0, d_h = 0, QR = 0, K1 = 0, m = 0, H = 0, Hx = 0;
+  int nchunk = 1;             // partials per row: chunks x key splits
+  bf16* o = nullptr;          // [B K1][n_q d_h]
+  bf16* kc = nullptr;         // this layer's key / value tensors (block rows appended into the ring)
+  bf16* vc = nullptr;
+  const int* cursor = nullptr;
+};
+struct HistPlan {
+  int sub_per_chunk = 1, nchunk = 1;
+};
+size_t hist_attn_smem(int d_h, int QR);
+int hist_key_splits(int QR);           // key halves per tile (partials per chunk)
+long long hist_max_ctas(int num_sms);  // bound on chunks x heads x requests (partial buffer sizing)
+HistPlan hist_plan(int B, int n_kv, int H, int Tk, int QR, int d_h, int num_sms);
+cudaError_t launch_hist_fill(const HistFillArgs& a, cudaStream_t s);
+cudaError_t launch_hist_attn(const CUtensorMap* mk, const CUtensorMap* mv, const HistAttnArgs& a, int d_h,
+                             cudaStream_t s);
+cudaError_t launch_hist_combine(const HistCombineArgs& a, cudaStream_t s);
+cudaError_t launch_hist_advance(int* cursor, int B, int n, int H, cudaStream_t s);
 
 }  // namespace dlite

@@ -64,7 +64,26 @@ def round_bytes(cfg, B):
     small = (cfg.m * D + cfg.L_D * 2 * D + 3 * D) * wb
     hidden = B * cfg.m * D * wb
     io = B * (4 + 4 * cfg.K * 2 + 4 * (cfg.K + 1) + 16)
-    return weights * wb + small + hidden + io
+    return weights * wb + small + hidden + io + history_bytes(cfg, B)
+
+
+def history_bytes(cfg, B):
+    """History-KV control: per layer every ring read once (bf16 keys and values)
+    and the round's G + K rows written into it; 0 for the history-free drafter."""
+    H = getattr(cfg, "history", 0)
+    if not H:
+        return 0
+    K1 = getattr(cfg, "G", 1) + cfg.K
+    return cfg.L_D * B * cfg.n_kv * cfg.d_h * 2 * 2 * (H + K1)
+
+
+def hist_attn_bytes(cfg, B):
+    """One launch of the history attention (one layer): the ring and the block's
+    keys / values read once, the block's queries read once (bf16)."""
+    K1 = getattr(cfg, "G", 1) + cfg.K
+    Tk = cfg.m + K1
+    QR = cfg.n_q // cfg.n_kv * K1
+    return B * cfg.n_kv * cfg.d_h * 2 * (2 * (cfg.history + Tk) + QR)
 
 
 def round_flops(cfg, B):
@@ -78,7 +97,8 @@ def round_flops(cfg, B):
     attn = 2 * 2 * loc * cfg.n_q * (m + K + 1) * cfg.d_h
     head = 2 * B * K * D * 2 * R + 2 * B * K * R * R + 2 * B * K * R * D
     lm = 2 * B * K * D * V
-    return cfg.L_D * (per_layer + attn) + head + lm
+    hist = 2 * 2 * B * cfg.n_q * (getattr(cfg, "G", 1) + K) * getattr(cfg, "history", 0) * cfg.d_h
+    return cfg.L_D * (per_layer + attn + hist) + head + lm
 
 
 def lm_head_bytes(cfg, B):
@@ -88,6 +108,16 @@ def lm_head_bytes(cfg, B):
 
 def lm_head_flops(cfg, B):
     return 2 * B * cfg.K * cfg.D * cfg.V
+
+
+def gated_lm_bytes(cfg, B):
+    """One step's vocabulary projection of the gated head: W_o [V, R] once, r [B, R] (bf16)."""
+    wb = 4 if cfg.dtype == "f32" else 2
+    return cfg.V * cfg.R * wb + B * cfg.R * 2
+
+
+def gated_lm_flops(cfg, B):
+    return 2 * B * cfg.R * cfg.V
 
 
 def roofline_floor_s(nbytes, flops, hbm_gbs, tflops):

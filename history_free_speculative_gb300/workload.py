@@ -33,6 +33,7 @@ class DraftConfig:
     theta: float = 1e6
     G: int = 1      # local token group ending at the anchor (local positions 0..G-1)
     head: str = "rnn"   # "rnn": low-rank RNN head + tied D->V projection; "gated": token-feedback head
+    history: int = 0    # H > 0: history-KV control (a ring of the last H draft K/V rows per layer)
 
     @property
     def torch_dtype(self):

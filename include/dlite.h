@@ -77,6 +77,17 @@ typedef struct {
     int head_type;    /* DLITE_HEAD_RNN (0): the low-rank RNN head with one tied D->V projection;
                        * DLITE_HEAD_GATED (1): the official gated token-feedback head (weights in
                        * dlite_weights.gated; R a multiple of 64) */
+    int history;      /* H: history-KV control of the history-cost comparison. 0 (the method):
+                       * history-free, no draft KV. H > 0: the conventional drafter the method is
+                       * measured against ([P1] §"本轮临时 K/V 仍然需要计算"; [P2] "Cost of the
+                       * history"): every backbone layer keeps a ring of the last H local key /
+                       * value rows of each request slot (bf16, 2 L_D H n_kv d_h values per slot,
+                       * allocated by dlite_create and filled with the synthetic history that
+                       * dlite_history_reset describes); each backbone pass attends over the H
+                       * ring rows beside the block, then writes its G + K local rows at slots
+                       * (cursor + j) mod H and advances the slot's cursor by G + K. A 512-row
+                       * ring is the sliding-window variant. Requires DLITE_BF16,
+                       * G + K <= H <= 2^20 and (n_q / n_kv) (G + K) <= 128 */
 } dlite_config;
 
 enum dlite_head_type { DLITE_HEAD_RNN = 0, DLITE_HEAD_GATED = 1 };
@@ -266,6 +277,21 @@ int dlite_verify_sample_static(int B, int K, int V, int D, const int32_t *candid
                                const float *target_probs, float temperature, uint64_t seed,
                                const int64_t *pos, int32_t *accepted, int32_t *commits,
                                int32_t *n_commit, int32_t *next_anchor, dlite_stream_t stream);
+
+/* History-KV control (cfg.history = H > 0). dlite_history_reset refills every
+ * ring with the synthetic history and sets every cursor to 0 (dlite_create has
+ * done so): element (slot t, head g, column d) of layer l, request slot b, keys
+ * (which = 0) or values (which = 1) is bf16((u0 + u1 + u2 + u3 - 2) sqrt(3)),
+ * every step in fp32, u_i the four uniforms ((x >> 9) + 1/2) 2^-23 of
+ * Philox4x32-10(counter = (t d_h + d, (2 l + which) n_kv + g, b, 6),
+ * key = (0x00000001, 0x48495354)): mean 0, variance 1.
+ * dlite_history_read copies one ring, [n_kv][H][d_h] bf16 (slot-major per
+ * head), to the device buffer dst on `stream` and, when cursor is non-null,
+ * the slot's cursor to host memory (synchronising the stream).
+ * Errors: INVALID_ARG (no history, layer / request / which out of range, null dst), CUDA. */
+int dlite_history_reset(dlite_handle *h, dlite_stream_t stream);
+int dlite_history_read(dlite_handle *h, int layer, int request, int which, void *dst, int32_t *cursor,
+                       dlite_stream_t stream);
 
 /* Round bookkeeping for a local token group (anchor_group G): group [B, G] becomes the
  * last G tokens of (group ++ commits[b, 0..n_commit[b]-1]), i.e. the G most recent

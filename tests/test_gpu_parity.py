@@ -684,3 +684,89 @@ def test_full_size_round_sampled_requests(name):
         gaps.append(mir["gap"])
     check_candidates(np.stack(cands), np.stack(ocands), np.stack(gaps))
     dr.close()
+
+
+# ---------------------------------------------------------------- history-KV control
+
+def _history_cfg(name, H):
+    if name == "d128":   # 4 query heads per key/value head, as in the 8B shape: 32 query rows per head
+        return wk.shrink(wk.QWEN3_8B, D=512, F=1024, L_D=2, n_q=8, n_kv=2, R=64, V=4096, m=6, history=H)
+    return wk.shrink(wk.TINY, dtype="bf16", history=H)   # d_h = 64, 2 heads per group
+
+
+@pytest.mark.parametrize("name", ["d128", "d64"])
+def test_history_fill_matches_oracle(name):
+    """The synthetic history in every ring, bit for bit, and the cursors at 0."""
+    H = 80
+    cfg = _history_cfg(name, H)
+    dr = _drafter(cfg, wk.make_weights(cfg, 41), B_max=3)
+    try:
+        for l in range(cfg.L_D):
+            for b in range(3):
+                for which in (0, 1):
+                    ring, cur = dr.history_read(l, b, which)
+                    got = ring.float().cpu().numpy().transpose(1, 0, 2)
+                    ref = O.history_values(H, cfg.n_kv, cfg.d_h, l, b, which)
+                    assert np.array_equal(got, ref), (l, b, which)
+                    assert cur == 0
+    finally:
+        dr.close()
+
+
+@pytest.mark.parametrize("name,H", [("d128", 300), ("d128", 64), ("d64", 200), ("d64", 12)])
+def test_history_round_parity(name, H):
+    """Three rounds of the history-KV control (the 12-row ring wraps): hidden rows and candidates against
+    the oracle drafter attending over its own ring, then each ring after the
+    append (slots no round has written bit-exact, the written rows within the
+    hidden tolerance: the appended rows are the drafter's own) and the cursors."""
+    cfg = _history_cfg(name, H)
+    W = wk.make_weights(cfg, 42)
+    wl = wk.WORKLOADS["tiny"]
+    B = 4
+    dr = _drafter(cfg, W, B_max=B)
+    K1 = cfg.G + cfg.K
+    try:
+        hist = [O.HistoryCache(cfg, H, b) for b in range(B)]
+        written = np.zeros((B, H), dtype=bool)
+        for rnd in range(3):
+            hidden, anchor, pos = wk.make_round_inputs(wl, B=B, round_index=rnd, cfg=cfg)
+            anchor = anchor % cfg.V
+            out = dr.new_outputs(B, DEV)
+            taps = {"z": torch.empty(B, cfg.m, cfg.D, device=DEV),
+                    "x": torch.empty(cfg.L_D, B, K1, cfg.D, device=DEV),
+                    "b": torch.empty(B, cfg.K, cfg.D, device=DEV),
+                    "hs": torch.empty(B, cfg.K, cfg.D, device=DEV)}
+            dr.draft_round(hidden.to(DEV), anchor.to(DEV), 0.0, 0, pos.to(DEV), out["cand"], out["qstats"],
+                           taps=taps)
+            torch.cuda.synchronize()
+            cursor0 = [hc.cursor for hc in hist]
+            cands, ocands, gaps = [], [], []
+            for b in range(B):
+                t = {}
+                r = O.draft_request(hidden[b], int(anchor[b]), W, cfg, taps=t, mirror=True, history=hist[b])
+                for l in range(cfg.L_D):
+                    assert rel_err(taps["x"][l, b].cpu(), t["x"][l]) < HIDDEN_REL_TOL, (rnd, b, l)
+                assert rel_err(taps["b"][b].cpu(), t["b"]) < HIDDEN_REL_TOL
+                cands.append(out["cand"][b].cpu().numpy())
+                ocands.append(r["cand"])
+                gaps.append(r["gap"])
+            check_candidates(np.stack(cands), np.stack(ocands), np.stack(gaps))
+            for b in range(B):
+                written[b, (cursor0[b] + np.arange(K1)) % H] = True   # rows of this and earlier rounds
+                slots, keep = written[b], ~written[b]
+                for l in range(cfg.L_D):
+                    for which, ref in ((0, hist[b].k[l]), (1, hist[b].v[l])):
+                        ring, cur = dr.history_read(l, b, which)
+                        got = ring.float().cpu().numpy().transpose(1, 0, 2)
+                        assert np.array_equal(got[keep], ref[keep]), (rnd, b, l, which)
+                        assert rel_err(got[slots], ref[slots]) < HIDDEN_REL_TOL, (rnd, b, l, which)
+                        assert cur == hist[b].cursor == (cursor0[b] + K1) % H
+    finally:
+        dr.close()
+
+
+def test_history_calls_need_a_ring(tiny):
+    """A drafter built with history = 0 keeps no ring: the history calls refuse it."""
+    wl, W, dr = tiny
+    with pytest.raises(binding.DliteError):
+        dr.history_reset()
