@@ -770,3 +770,44 @@ def test_history_calls_need_a_ring(tiny):
     wl, W, dr = tiny
     with pytest.raises(binding.DliteError):
         dr.history_reset()
+
+
+def test_full_size_history_round_sampled_requests():
+    """The 8B-shape history-KV control at B = 8 with an 8192-row ring, in the
+    bench's launch configuration: two sampled requests against the oracle
+    drafter attending over its own ring (pure for hidden states, mirror for
+    tokens), and their rings after the append."""
+    H = 8192
+    wl = wk.WORKLOADS["qwen3-8b-history"]
+    cfg = wk.shrink(wl.cfg, history=H)
+    B = wl.B
+    K1 = cfg.G + cfg.K
+    W = wk.make_weights(cfg, wl.weight_seed, device=DEV)
+    dr = binding.Drafter(cfg, W, B_max=B)
+    hidden, anchor, pos = wk.make_round_inputs(wl, device=DEV)
+    out = dr.new_outputs(B, DEV)
+    taps = {"b": torch.empty(B, cfg.K, cfg.D, device=DEV)}
+    dr.draft_round(hidden, anchor, 0.0, wl.rng_seed, pos, out["cand"], out["qstats"], taps=taps)
+    torch.cuda.synchronize()
+    rc, st = dr.device_status()
+    assert rc == 0 and st == 0
+    Wc = f64_weights(wk.weights_to(W, "cpu"))
+    del W
+    cands, ocands, gaps = [], [], []
+    for b in (1, B - 1):
+        hp = O.HistoryCache(cfg, H, b)
+        hm = O.HistoryCache(cfg, H, b)
+        pure = O.draft_request(hidden[b].cpu(), int(anchor[b]), Wc, cfg, mirror=False, history=hp)
+        mir = O.draft_request(hidden[b].cpu(), int(anchor[b]), Wc, cfg, mirror=True, history=hm)
+        assert rel_err(taps["b"][b].cpu(), pure["b"]) < HIDDEN_REL_TOL
+        cands.append(out["cand"][b].cpu().numpy())
+        ocands.append(mir["cand"])
+        gaps.append(mir["gap"])
+        for l in range(cfg.L_D):
+            ring, cur = dr.history_read(l, b, 0)
+            got = ring.float().cpu().numpy().transpose(1, 0, 2)
+            assert cur == K1 and hm.cursor == K1
+            assert np.array_equal(got[K1:], hm.k[l][K1:])
+            assert rel_err(got[:K1], hm.k[l][:K1]) < HIDDEN_REL_TOL
+    check_candidates(np.stack(cands), np.stack(ocands), np.stack(gaps))
+    dr.close()
