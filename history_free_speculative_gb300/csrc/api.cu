@@ -253,11 +253,12 @@ const CUtensorMap* get_map(dlite_handle* h, const void* base, int rows, int K, i
 // written as usual and the caller runs the SwiGLU kernel.
 int gemm(dlite_handle* h, const char* name, const Operand& X, const Operand& W, int rows, int outs,
          float* part, Splits* sp_out, cudaStream_t s, bf16* const* act = nullptr, int act_planes = 1,
-         bool* fused = nullptr) {
+         bool* fused = nullptr, int skip_row0 = 0, int skip_cols = 0) {
   if (fused) *fused = false;
+  const bool skipping = skip_row0 > 0;  // tiles to skip: the one-CTA engine
   // few rows: persistent stream-K over the weights (the gate/up product keeps
   // the one-CTA engine, whose epilogue applies the SwiGLU)
-  if (!act && tc::use_stream_engine(rows, X.n, W.n)) {
+  if (!act && !skipping && tc::use_stream_engine(rows, X.n, W.n)) {
     const tc::StreamPlan sp = tc::stream_plan(rows, outs, X.K, h->num_sms);
     if (sp.ok) {
       h->maps.reserve(h->maps.size() + 4);
@@ -275,7 +276,7 @@ int gemm(dlite_handle* h, const char* name, const Operand& X, const Operand& W, 
       return DLITE_OK;
     }
   }
-  if (tc::use_pair_engine(rows, X.n, W.n)) {  // 2-SM MMAs
+  if (!skipping && tc::use_pair_engine(rows, X.n, W.n)) {  // 2-SM MMAs
     const tc::PairPlan pp = tc::pair_plan(rows, outs, X.K, h->num_sms);
     if (pp.ok) {
       h->maps.reserve(h->maps.size() + 4);
@@ -312,6 +313,8 @@ int gemm(dlite_handle* h, const char* name, const Operand& X, const Operand& W, 
   prm.x_box = xb;
   prm.part = part;
   prm.status = h->status;
+  prm.skip_row0 = skip_row0;
+  prm.skip_cols = skip_cols;
   if (act) {
     prm.mode = 2;
     prm.act[0] = act[0];
@@ -343,15 +346,20 @@ tc::Plan lm_plan(dlite_handle* h, int rows) {
   return tc::plan(rows, h->cfg.V, h->cfg.D, 1, 1, true);
 }
 
-// Few rows: the context rows z are stored behind the local rows y in one
-// buffer and a single product [y; z] W_qkv^T serves both (the query columns of
-// the context rows are computed and ignored), one launch instead of two.
-static bool fuse_ctx(const dlite_handle* h, int B) {
+// bf16 drafters store the context rows z behind the local rows y in one
+// buffer, and a single product [y; z] W_qkv^T serves both, one launch instead
+// of two: 1 = few rows, on the stream-K engine (the query columns of the
+// context rows are computed and ignored); 2 = more rows, on the one-CTA
+// engine, whose tiles of context rows x query columns are skipped.
+// 0 = two products (fp32 drafters).
+static int ctx_route(const dlite_handle* h, int B) {
   const dlite_config& c = h->cfg;
   const int rows = B * (group_of(&c) + c.K) + B * c.m;
-  return h->np == 1 && tc::use_stream_engine(rows, 1, 1) &&
-         tc::stream_plan(rows, h->qd + 2 * h->kvd, c.D, h->num_sms).ok;
+  if (h->np != 1) return 0;
+  if (tc::use_stream_engine(rows, 1, 1)) return tc::stream_plan(rows, h->qd + 2 * h->kvd, c.D, h->num_sms).ok;
+  return tc::plan(rows, h->qd + 2 * h->kvd, c.D, 1, 1, false).ok ? 2 : 0;
 }
+static bool fuse_ctx(const dlite_handle* h, int B) { return ctx_route(h, B) != 0; }
 
 // History-KV control, layer l: split-KV attention of the block's queries over
 // the ring and the block, then the merge into h->o and the ring append.
@@ -435,8 +443,10 @@ int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anch
     Splits S1, S2;
     AttnArgs at;
     if (fused_ctx) {
+      const bool skip = ctx_route(h, B) == 2;
       RUN(gemm(h, "gemm_qkv", opnd(h->y, h->np, h->Lcap + h->Ccap, c.D),
-               opnd(w.Wqkv, h->np, h->qd + 2 * h->kvd, c.D), L + C, h->qd + 2 * h->kvd, h->part, &S1, s));
+               opnd(w.Wqkv, h->np, h->qd + 2 * h->kvd, c.D), L + C, h->qd + 2 * h->kvd, h->part, &S1, s,
+               nullptr, 1, nullptr, skip ? L : 0, skip ? h->qd : 0));
       at.part_ctx = h->part;
       at.sp_ctx = S1;
       at.ctx_row0 = L;
@@ -932,9 +942,12 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
         pe = (size_t)sq.S * st[0] * st[1] > pe ? (size_t)sq.S * st[0] * st[1] : pe;
       if (pp.ok && tc::use_pair_engine(st[0], st[3], h->np)) pe = (size_t)pp.S * st[0] * st[1] > pe ? (size_t)pp.S * st[0] * st[1] : pe;  // planes
     }
-    if (fuse_ctx(h, B)) {
+    if (ctx_route(h, B) == 1) {
       const tc::StreamPlan sf = tc::stream_plan(L + C, h->qd + 2 * h->kvd, D, h->num_sms);
       pe = (size_t)sf.S * (L + C) * (h->qd + 2 * h->kvd) > pe ? (size_t)sf.S * (L + C) * (h->qd + 2 * h->kvd) : pe;
+    } else if (ctx_route(h, B) == 2) {
+      const tc::Plan pf = tc::plan(L + C, h->qd + 2 * h->kvd, D, 1, 1, false);
+      pe = std::max(pe, (size_t)pf.S * (L + C) * (h->qd + 2 * h->kvd));
     }
     const tc::Plan pc = tc::plan(C, 2 * h->kvd, D, h->np, h->np, false);
     if (!pc.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;

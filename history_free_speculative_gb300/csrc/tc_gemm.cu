@@ -37,12 +37,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t full0 = su32(bars), empty0 = su32(bars + p.stages), accf = su32(bars + 2 * p.stages);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // After any bounded wait has expired on this device, later CTAs skip their
-  // work (and only allocate / free TMEM) so a broken launch ends quickly.
-  const bool aborted = p.status && (*(volatile int*)p.status & kDevTimeout);
   const int o0 = blockIdx.x * p.N;
   const int split = blockIdx.y;
   const int m0 = blockIdx.z * p.n_mt * 128;
+  if (p.skip_row0 > 0 && m0 >= p.skip_row0 && o0 + p.N <= p.skip_cols) {  // a tile nobody reads
+    pdl_trigger();
+    return;
+  }
+  // After any bounded wait has expired on this device, later CTAs skip their
+  // work (and only allocate / free TMEM) so a broken launch ends quickly.
+  const bool aborted = p.status && (*(volatile int*)p.status & kDevTimeout);
   const int kb0 = split * p.kb_per_split;
   const int kb1 = min(kb0 + p.kb_per_split, p.kblocks);
   const int nkb = aborted ? 0 : kb1 - kb0;

@@ -46,6 +46,10 @@ struct TcParams {
   const int64_t* pos = nullptr;
   int K_draft = 1;
   int* status = nullptr;
+  // mode 0: a CTA whose rows all lie at or past skip_row0 (> 0) and whose
+  // columns all lie before skip_cols does nothing (a product over stacked
+  // operands whose lower rows need only the upper columns)
+  int skip_row0 = 0, skip_cols = 0;
 };
 
 // Tensor map of a bf16 row-major [rows, K] matrix, box = 64 (k) x box_rows.
