@@ -21,6 +21,12 @@ struct LayerW {
   float* g_ffn;
 };
 
+// A one-CTA-engine product shape and the plan chosen for it by timing at create.
+struct TunedPlan {
+  int rows, outs, K, xp, wp, act, skip_row0, skip_cols;
+  tc::Plan pl;
+};
+
 struct MapEntry {
   const void* base;
   int rows, K, box;
@@ -38,6 +44,8 @@ struct dlite_handle {
   int num_sms = 0;  // SMs of the device (persistent LM-head grid)
   std::vector<void*> allocs;
   std::vector<MapEntry> maps;
+  std::vector<TunedPlan> tuned;  // plans of the B_max products, chosen by timing (tune_products)
+  size_t part_cap = 0;           // floats in part
 
   // weights
   float *e_depth = nullptr, *g_stage = nullptr, *e_ph = nullptr, *g_final = nullptr;
@@ -246,6 +254,44 @@ const CUtensorMap* get_map(dlite_handle* h, const void* base, int rows, int K, i
   return &h->maps.back().map;
 }
 
+// One launch of the one-CTA engine with plan pl (partials, or the SwiGLU output when act is set).
+int launch_onecta(dlite_handle* h, const tc::Plan& pl, const Operand& X, const Operand& W, int rows, int outs,
+                  float* part, cudaStream_t s, bf16* const* act, int act_planes, int skip_row0, int skip_cols) {
+  const int xb = tc::x_box_rows(rows);
+  h->maps.reserve(h->maps.size() + 4);
+  const CUtensorMap* x0 = get_map(h, X.p[0], X.rows, X.K, xb);
+  const CUtensorMap* x1 = X.n == 2 ? get_map(h, X.p[1], X.rows, X.K, xb) : nullptr;
+  const CUtensorMap* w0 = get_map(h, W.p[0], W.rows, W.K, pl.N, true);
+  const CUtensorMap* w1 = W.n == 2 ? get_map(h, W.p[1], W.rows, W.K, pl.N, true) : nullptr;
+  if (!x0 || !w0 || (X.n == 2 && !x1) || (W.n == 2 && !w1)) return DLITE_ERR_CUDA;
+  tc::TcParams prm;
+  prm.rows = rows;
+  prm.outs = outs;
+  prm.K = X.K;
+  prm.xplanes = X.n;
+  prm.wplanes = W.n;
+  prm.mode = 0;
+  prm.x_box = xb;
+  prm.part = part;
+  prm.status = h->status;
+  prm.skip_row0 = skip_row0;
+  prm.skip_cols = skip_cols;
+  if (act) {
+    prm.mode = 2;
+    prm.act[0] = act[0];
+    prm.act[1] = act_planes == 2 ? act[1] : nullptr;
+    prm.act_planes = act_planes;
+  }
+  CK(tc::launch(pl, x0, x1, w0, w1, prm, s));
+  return DLITE_OK;
+}
+
+#define RUN(call)          \
+  do {                     \
+    int r_ = (call);       \
+    if (r_) return r_;     \
+  } while (0)
+
 // part[z][r][o] = sum over split z of X[r, :] . W[o, :], r < rows, o < outs.
 // With act != nullptr the product is the gate / up one (columns interleaved in
 // blocks of 32): on the one-CTA engine the epilogue writes a = silu(gate) * up
@@ -294,45 +340,20 @@ int gemm(dlite_handle* h, const char* name, const Operand& X, const Operand& W, 
       return DLITE_OK;
     }
   }
-  const tc::Plan pl = tc::plan(rows, outs, X.K, X.n, W.n, false, act != nullptr);
+  tc::Plan pl = tc::plan(rows, outs, X.K, X.n, W.n, false, act != nullptr, skip_row0, skip_cols);
+  for (const TunedPlan& t : h->tuned)
+    if (t.rows == rows && t.outs == outs && t.K == X.K && t.xp == X.n && t.wp == W.n && t.act == (act != nullptr) &&
+        t.skip_row0 == skip_row0 && t.skip_cols == skip_cols) {
+      pl = t.pl;
+      break;
+    }
   if (!pl.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
-  const int xb = tc::x_box_rows(rows);
-  h->maps.reserve(h->maps.size() + 4);
-  const CUtensorMap* x0 = get_map(h, X.p[0], X.rows, X.K, xb);
-  const CUtensorMap* x1 = X.n == 2 ? get_map(h, X.p[1], X.rows, X.K, xb) : nullptr;
-  const CUtensorMap* w0 = get_map(h, W.p[0], W.rows, W.K, pl.N, true);
-  const CUtensorMap* w1 = W.n == 2 ? get_map(h, W.p[1], W.rows, W.K, pl.N, true) : nullptr;
-  if (!x0 || !w0 || (X.n == 2 && !x1) || (W.n == 2 && !w1)) return DLITE_ERR_CUDA;
-  tc::TcParams prm;
-  prm.rows = rows;
-  prm.outs = outs;
-  prm.K = X.K;
-  prm.xplanes = X.n;
-  prm.wplanes = W.n;
-  prm.mode = 0;
-  prm.x_box = xb;
-  prm.part = part;
-  prm.status = h->status;
-  prm.skip_row0 = skip_row0;
-  prm.skip_cols = skip_cols;
-  if (act) {
-    prm.mode = 2;
-    prm.act[0] = act[0];
-    prm.act[1] = act_planes == 2 ? act[1] : nullptr;
-    prm.act_planes = act_planes;
-    if (fused) *fused = true;
-  }
+  if (act && fused) *fused = true;
   if (sp_out) *sp_out = uniform_splits(pl.S);
-  CK(tc::launch(pl, x0, x1, w0, w1, prm, s));
+  RUN(launch_onecta(h, pl, X, W, rows, outs, part, s, act, act_planes, skip_row0, skip_cols));
   mark(h, name);
   return DLITE_OK;
 }
-
-#define RUN(call)          \
-  do {                     \
-    int r_ = (call);       \
-    if (r_) return r_;     \
-  } while (0)
 
 void seed_key(uint64_t seed, uint32_t* k0, uint32_t* k1) {
   *k0 = (uint32_t)(seed & 0xffffffffu);
@@ -791,6 +812,90 @@ void dlite_destroy(dlite_handle* h) {
   delete h;
 }
 
+// Plans of the one-CTA-engine products at B = B_max, chosen by timing every
+// feasible plan on the device (CUDA events; L2 flushed before each launch, so
+// the weights stream from HBM as in a round; best of two). Other batch sizes
+// keep the analytical planner's choice. bf16 drafters only.
+static int tune_products(dlite_handle* h) {
+  const dlite_config& c = h->cfg;
+  if (h->np != 1) return DLITE_OK;
+  const int B = c.B_max, L = B * (group_of(&c) + c.K), C = B * c.m, Hr = B * c.K;
+  struct Site {
+    Operand X, W;
+    int rows, outs;
+    bf16* const* act;
+    int skip_row0, skip_cols;
+  };
+  std::vector<Site> sites;
+  const LayerW& w = h->layer[0];
+  const int qkv = h->qd + 2 * h->kvd;
+  if (ctx_route(h, B) == 2)
+    sites.push_back({opnd(h->y, 1, h->Lcap + h->Ccap, c.D), opnd(w.Wqkv, 1, qkv, c.D), L + C, qkv, nullptr, L, h->qd});
+  sites.push_back({opnd(h->o, 1, h->Lcap, h->qd), opnd(w.Wo, 1, c.D, h->qd), L, c.D, nullptr, 0, 0});
+  sites.push_back({opnd(h->y, 1, h->Lcap, c.D), opnd(w.Wgu, 1, 2 * c.F, c.D), L, 2 * c.F, h->a, 0, 0});
+  sites.push_back({opnd(h->a, 1, h->Lcap, c.F), opnd(w.Wd, 1, c.D, c.F), L, c.D, nullptr, 0, 0});
+  if (!h->gated) {
+    sites.push_back({opnd(h->bp, 2, h->Hcap, c.D), opnd(h->Wce, 1, 2 * h->Rp, c.D), Hr, 2 * h->Rp, nullptr, 0, 0});
+    sites.push_back({opnd(h->tp, 2, h->Hcap, h->Rp), opnd(h->P, 1, c.D, h->Rp), Hr, c.D, nullptr, 0, 0});
+  }
+  const size_t flush_bytes = (size_t)256 << 20;  // twice the L2
+  void* flush = nullptr;
+  if (cudaMalloc(&flush, flush_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return DLITE_OK;  // no room to time: the analytical plans stay
+  }
+  cudaStream_t s = nullptr;
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  int rc = DLITE_OK;
+  if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess || cudaEventCreate(&e0) != cudaSuccess ||
+      cudaEventCreate(&e1) != cudaSuccess)
+    rc = DLITE_ERR_CUDA;
+  for (const Site& st : sites) {
+    if (rc) break;
+    const bool skipping = st.skip_row0 > 0;
+    const bool stream = !st.act && !skipping && tc::use_stream_engine(st.rows, st.X.n, st.W.n) &&
+                        tc::stream_plan(st.rows, st.outs, st.X.K, h->num_sms).ok;
+    const bool pair = !stream && !skipping && tc::use_pair_engine(st.rows, st.X.n, st.W.n) &&
+                      tc::pair_plan(st.rows, st.outs, st.X.K, h->num_sms).ok;
+    if (stream || pair) continue;  // another engine serves this product
+    TunedPlan best;
+    float best_ms = 1e30f;
+    for (const tc::Plan& pl : tc::plan_candidates(st.rows, st.outs, st.X.K, st.X.n, st.W.n, st.act != nullptr)) {
+      if (!st.act && (size_t)pl.S * st.rows * st.outs > h->part_cap) continue;
+      float t = 1e30f;
+      for (int rep = 0; rep < 2 && !rc; ++rep) {
+        float ms = 0.f;
+        if (cudaMemsetAsync(flush, rep, flush_bytes, s) != cudaSuccess || cudaEventRecord(e0, s) != cudaSuccess) {
+          rc = DLITE_ERR_CUDA;
+          break;
+        }
+        rc = launch_onecta(h, pl, st.X, st.W, st.rows, st.outs, h->part, s, st.act, 1, st.skip_row0, st.skip_cols);
+        if (rc || cudaEventRecord(e1, s) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess ||
+            cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess) {
+          rc = rc ? rc : DLITE_ERR_CUDA;
+          break;
+        }
+        t = std::min(t, ms);
+      }
+      if (!rc && t < best_ms) {
+        best_ms = t;
+        best = {st.rows, st.outs, st.X.K, st.X.n, st.W.n, st.act != nullptr, st.skip_row0, st.skip_cols, pl};
+      }
+    }
+    if (!rc && best_ms < 1e29f) h->tuned.push_back(best);
+  }
+  if (e0) cudaEventDestroy(e0);
+  if (e1) cudaEventDestroy(e1);
+  if (s) cudaStreamDestroy(s);
+  cudaFree(flush);
+  if (!rc) {  // a timed launch must not have tripped a bounded wait
+    int st = 0;
+    if (cudaMemcpy(&st, h->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return DLITE_ERR_CUDA;
+    if (st) return DLITE_ERR_DEVICE_TIMEOUT;
+  }
+  return rc;
+}
+
 static int create_impl(dlite_handle* h, const dlite_weights* w) {
   const dlite_config& c = h->cfg;
   const int D = c.D, F = c.F, R = c.R, V = c.V;
@@ -946,7 +1051,7 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
       const tc::StreamPlan sf = tc::stream_plan(L + C, h->qd + 2 * h->kvd, D, h->num_sms);
       pe = (size_t)sf.S * (L + C) * (h->qd + 2 * h->kvd) > pe ? (size_t)sf.S * (L + C) * (h->qd + 2 * h->kvd) : pe;
     } else if (ctx_route(h, B) == 2) {
-      const tc::Plan pf = tc::plan(L + C, h->qd + 2 * h->kvd, D, 1, 1, false);
+      const tc::Plan pf = tc::plan(L + C, h->qd + 2 * h->kvd, D, 1, 1, false, false, L, h->qd);
       pe = std::max(pe, (size_t)pf.S * (L + C) * (h->qd + 2 * h->kvd));
     }
     const tc::Plan pc = tc::plan(C, 2 * h->kvd, D, h->np, h->np, false);
@@ -968,7 +1073,13 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
       lme = v4 > lme ? v4 : lme;
     }
   }
+  {  // the timed plan selection at B_max may pick up to 4 splits for the layer products
+    const int L = Bm * (group_of(&c) + c.K), C = Bm * c.m;
+    pe = std::max(pe, (size_t)4 * L * std::max(h->qd + 2 * h->kvd, D));
+    if (ctx_route(h, Bm) == 2) pe = std::max(pe, (size_t)4 * (L + C) * (h->qd + 2 * h->kvd));
+  }
   AL(h->part, pe);
+  h->part_cap = pe;
   AL(h->part2, pe2);
   AL(h->lmrec, lme);
   AL(h->resid, (size_t)Bm * V);
@@ -1036,6 +1147,8 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
     AL(h->hpart_ml, prow * 2);
     RUN(dlite_history_reset(h, nullptr));
   }
+  CK(cudaDeviceSynchronize());
+  RUN(tune_products(h));
   CK(cudaDeviceSynchronize());
   return DLITE_OK;
 }

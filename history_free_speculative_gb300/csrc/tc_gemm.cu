@@ -11,6 +11,7 @@
 // Every mbarrier wait is bounded (~2 s of %globaltimer); on expiry the kernel
 // flags the device status word and runs to its end instead of hanging.
 #include "tc_device.cuh"
+
 #include "tc_gemm.h"
 
 namespace dlite {
@@ -350,7 +351,8 @@ static int next_pow2_cols(int c) {
   return n;
 }
 
-Plan plan(int rows, int outs, int K, int xplanes, int wplanes, bool lm, bool one_split) {
+Plan plan(int rows, int outs, int K, int xplanes, int wplanes, bool lm, bool one_split, int skip_row0,
+          int skip_cols) {
   Plan best;
   best.ok = false;
   const int kblocks = K / 64;
@@ -375,7 +377,9 @@ Plan plan(int rows, int outs, int K, int xplanes, int wplanes, bool lm, bool one
         const int kbps = (kblocks + S - 1) / S;
         const int Se = (kblocks + kbps - 1) / kbps;
         if (Se != S) continue;
-        const long units = (long)slabs * Se * groups;
+        long units = 0;  // CTAs with work (tiles past skip_row0 x before skip_cols are skipped)
+        for (int g = 0; g < groups; ++g)
+          units += (long)Se * (skip_row0 > 0 && g * n_mt * 128 >= skip_row0 ? slabs - skip_cols / N : slabs);
         const long waves = (units + kNumSMs - 1) / kNumSMs;
         const double active = units < kNumSMs ? (double)units : (double)kNumSMs;
         double bw_sm = bw_total / active;
@@ -406,6 +410,45 @@ Plan plan(int rows, int outs, int K, int xplanes, int wplanes, bool lm, bool one
     }
   }
   return best;
+}
+
+std::vector<Plan> plan_candidates(int rows, int outs, int K, int xplanes, int wplanes, bool one_split) {
+  std::vector<Plan> out;
+  const int kblocks = K / 64;
+  const int mt_total = (rows + 127) / 128;
+  const int nmax_out = ((outs + 63) / 64) * 64;
+  int prev_nmt = 0;
+  for (int gmax = 4; gmax >= 1; gmax >>= 1) {
+    const int groups = (mt_total + gmax - 1) / gmax;
+    const int n_mt = (mt_total + groups - 1) / groups;
+    if (n_mt == prev_nmt) continue;  // the same split of the M-tiles
+    prev_nmt = n_mt;
+    for (int N = 64; N <= 256; N += 64) {
+      if (N * n_mt > 512 || N > nmax_out) continue;
+      const uint32_t sb = (uint32_t)wplanes * N * 128 + (uint32_t)n_mt * xplanes * a_slot_bytes(x_box_rows(rows));
+      int stages = (int)((kSmemBudget - 2048 - kTailPad) / sb);
+      if (stages > 8) stages = 8;
+      if (stages < 2) continue;
+      const int smax = one_split ? 1 : (kblocks < 4 ? kblocks : 4);
+      for (int S = 1; S <= smax; ++S) {
+        const int kbps = (kblocks + S - 1) / S;
+        if ((kblocks + kbps - 1) / kbps != S) continue;
+        Plan p;
+        p.ok = true;
+        p.N = N;
+        p.S = S;
+        p.kb_per_split = kbps;
+        p.kblocks = kblocks;
+        p.n_mt = n_mt;
+        p.groups = groups;
+        p.stages = stages;
+        p.stage_bytes = sb;
+        p.tmem_cols = next_pow2_cols(N * n_mt);
+        out.push_back(p);
+      }
+    }
+  }
+  return out;
 }
 
 size_t smem_bytes(const Plan& pl) {

@@ -3,6 +3,8 @@
 
 #include <cuda.h>
 
+#include <vector>
+
 #include "internal.h"
 
 namespace dlite {
@@ -58,12 +60,16 @@ bool make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows);
 // k block of box_rows (a multiple of 64) rows.
 bool make_map_tiled(CUtensorMap* m, const void* base, int rows, int K, int box_rows);
 // lm or one_split: no k splits (the LM head; products whose epilogue needs the full sums)
-Plan plan(int rows, int outs, int K, int xplanes, int wplanes, bool lm, bool one_split = false);
+// skip_row0 / skip_cols: the tiles TcParams::skip_row0 / skip_cols describe do no work
+Plan plan(int rows, int outs, int K, int xplanes, int wplanes, bool lm, bool one_split = false, int skip_row0 = 0,
+          int skip_cols = 0);
 // Rows of the activation tile loads: the valid rows (rounded to 8) when they fit one tile.
 inline int x_box_rows(int rows) { return rows >= 128 ? 128 : ((rows + 7) / 8) * 8; }
 // Shared-memory slot of one activation tile: the loaded rows, rounded to a 1 KB swizzle atom group.
 __host__ __device__ inline uint32_t a_slot_bytes(int x_box) { return (uint32_t)((x_box * 128 + 1023) / 1024 * 1024); }
 size_t smem_bytes(const Plan& pl);
+// Every feasible plan of a one-CTA-engine product (for timing-based selection).
+std::vector<Plan> plan_candidates(int rows, int outs, int K, int xplanes, int wplanes, bool one_split);
 
 // Persistent LM-head kernel (rows <= 256): one CTA per SM walking the
 // vocabulary slabs with double-buffered TMEM accumulators (sampling epilogue
