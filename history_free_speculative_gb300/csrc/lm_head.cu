@@ -16,6 +16,14 @@
 // registers; at the end the column groups of a row are combined in shared
 // memory and one record per walk is written; the merge kernel combines them.
 //
+// With at most 32 rows and a short k extent (the gated head's per-step W_o
+// product: 8 k blocks per slab) scoring, not the E stream, paces a slab, and
+// rows 0..31 sit in TMEM lane quadrant 0, which only the warps of one SM
+// sub-partition can read. Then (`rep`) the h tile is loaded four times, at
+// rows 0, 32, 64 and 96, so every quadrant holds the same logits, and the
+// warp of quadrant q scores a quarter of its column group: four times the
+// epilogue warps, a quarter of the columns each.
+//
 // Warp roles: warp 0 TMA producer (E slab k block + h tile per 64-wide k
 // block, through a ring of shared-memory stages; in a pair every copy signals
 // rank 0's barrier), warp 1 TMEM owner and MMA issuer (rank 0 of a pair),
@@ -116,10 +124,10 @@ __global__ void __launch_bounds__(kLmThreads, 1)
 
   if (warp == 0) {  // ---------------- TMA producer
     // stage: [h tile: x_box rows in a slot of x_box0 rows][E slab k block: kWRows rows]
-    const uint32_t wofs = a_slot_bytes(p.x_box0);
+    const uint32_t wofs = a_slot_bytes(p.rep ? 128 : p.x_box0);
     // bytes landing per stage: in a pair, rank 0's barrier counts both CTAs' copies
     const uint32_t bytes = PAIR ? 2u * kWTile + (uint32_t)(p.x_box0 + p.x_box1) * 128u
-                                : kWTile + (uint32_t)x_box * 128u;
+                                : kWTile + (uint32_t)x_box * 128u * (p.rep ? 4u : 1u);
     const uint32_t fullb = PAIR ? map_to_rank(full0, 0) : full0;
     const CUtensorMap* mx = tile ? &mx1 : &mx0;
     auto load_w = [&](int i, int s) {
@@ -137,6 +145,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       const int kx = ((i % nkb + rot) % nkb) * 64;
       if (PAIR)
         tma_load_2d_pair(st, mx, fullb + 8 * s, kx, tile * 128);
+      else if (p.rep)  // one copy of the rows per TMEM lane quadrant
+        for (int q4 = 0; q4 < 4; ++q4) tma_load_2d(st + q4 * 32 * 128, mx, fullb + 8 * s, kx, 0);
       else
         tma_load_2d(st, mx, fullb + 8 * s, kx, tile * 128);
     };
@@ -174,7 +184,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     if (PAIR && tile != 0) goto mma_done;
     {
     const uint32_t idesc = idesc_bf16(PAIR ? 256 : 128, N);
-    const uint64_t wbase = (uint64_t)(a_slot_bytes(p.x_box0) >> 4);
+    const uint64_t wbase = (uint64_t)(a_slot_bytes(p.rep ? 128 : p.x_box0) >> 4);
     const uint64_t desc0 = sw128_desc(su32(smem));
     const uint64_t sdelta = (uint64_t)(p.stage_bytes >> 4);
     int i = 0;
@@ -232,11 +242,13 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   } else {  // ---------------- epilogue warps
     const int q = warp & 3;
     const int eg = (warp - 2) >> 2;
-    const int c_lo = eg * kColsPerGroup;
+    const bool rep = !PAIR && p.rep && kColsPerGroup == 64;
+    const int width = rep ? kColsPerGroup / 4 : kColsPerGroup;  // columns this warp scores per slab
+    const int c_lo = eg * kColsPerGroup + (rep ? q * width : 0);
     const bool sampling = p.inv_T > 0.f;
     const float c2s = p.inv_T * kLog2e;
     pdl_wait();  // positions are read below; records are written at the end
-    const int row = tile * 128 + q * 32 + lane;
+    const int row = rep ? lane : tile * 128 + q * 32 + lane;
     const bool valid = row < p.rows;
     LmAcc acc;
     lm_acc_init(acc);
@@ -257,7 +269,13 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       fence_after();
       if (any_valid) {
         const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)b * kAccCols + (uint32_t)c_lo;
-        if constexpr (kColsPerGroup % 32 == 0) {
+        if (rep) {  // one 16-column chunk
+          uint32_t r0[16];
+          tmem_ld16_nowait(tbase, r0);
+          tmem_wait_ld();
+          const int v0 = slab * N + c_lo;
+          fold_cols(acc, r0, v0, p.outs - v0, sampling, c2s, pr, p.k0, p.k1, valid);
+        } else if constexpr (kColsPerGroup % 32 == 0) {
 #pragma unroll 1
           for (int c = 0; c < kColsPerGroup; c += 32) {
             uint32_t r0[16], r1[16];
@@ -296,9 +314,9 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     const int rl = q * 32 + lane;
     lm_acc_store(acc, sm_rec + eg * 128 + rl);
     asm volatile("bar.sync 1, %0;" ::"r"(4 * kLmGroups * 32) : "memory");  // the epilogue warps only
-    if (eg == 0 && valid) {
-      for (int g2 = 1; g2 < kLmGroups; ++g2) {
-        const LmRec o = sm_rec[g2 * 128 + rl];
+    if (eg == 0 && valid && (!rep || q == 0)) {
+      for (int g2 = 1; g2 < kLmGroups * (rep ? 4 : 1); ++g2) {  // rep: every (group, quadrant) of the row
+        const LmRec o = sm_rec[rep ? (g2 % kLmGroups) * 128 + (g2 / kLmGroups) * 32 + lane : g2 * 128 + rl];
 #pragma unroll
         for (int k = 0; k < kTopK; ++k) topk_insert(acc.sc, acc.id, o.sc[k], o.id[k]);
         if (o.m != -INFINITY) {  // base-2 LSE partials
@@ -346,9 +364,10 @@ LmPlan lm_plan_persistent(int rows, int outs, int K, int num_sms) {
   pl.x_box0 = rows >= 128 ? 128 : (rows + 7) / 8 * 8;
   pl.x_box1 = pl.paired ? (rows - 128 + 7) / 8 * 8 : 0;
   pl.kblocks = K / 64;
+  pl.rep = !pl.paired && rows <= 32 && pl.N == 256 && pl.kblocks <= 16;
   const uint32_t wrows = pl.paired ? (uint32_t)pl.N / 2 : (uint32_t)pl.N;
-  pl.stage_bytes = wrows * 128u + a_slot_bytes(pl.x_box0);
-  pl.tail_pad = !pl.paired && (uint32_t)(128 - pl.x_box0) * 128u > wrows * 128u ? kTailPad : 0;
+  pl.stage_bytes = wrows * 128u + a_slot_bytes(pl.rep ? 128 : pl.x_box0);  // rep: four 32-row copies
+  pl.tail_pad = !pl.paired && !pl.rep && (uint32_t)(128 - pl.x_box0) * 128u > wrows * 128u ? kTailPad : 0;
   int stages = (int)((kSmemBudget - 2048 - pl.tail_pad) / pl.stage_bytes);
   if (stages > 8) stages = 8;
   if (stages < 2) return pl;
@@ -394,6 +413,7 @@ cudaError_t launch_lm_persistent(const LmPlan& pl, const CUtensorMap* x0, const 
   prm.x_box0 = pl.x_box0;
   prm.x_box1 = pl.x_box1;
   prm.paired = pl.paired ? 1 : 0;
+  prm.rep = pl.rep ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(pl.grid);
   cfg.blockDim = dim3(kLmThreads);

@@ -78,6 +78,7 @@ std::vector<Plan> plan_candidates(int rows, int outs, int K, int xplanes, int wp
 struct LmPlan {
   bool ok = false;
   bool paired = false;
+  bool rep = false;  // rows <= 32 copied into all four TMEM lane quadrants (short k: the epilogue paces a slab)
   int N = 0, x_box0 = 0, x_box1 = 0, kblocks = 0, stages = 0, n_slabs = 0, n_units = 0, grid = 0,
       groups = 0;
   uint32_t stage_bytes = 0;
@@ -85,7 +86,7 @@ struct LmPlan {
 };
 struct LmParams {
   int rows = 0, outs = 0;
-  int n_slabs = 0, kblocks = 0, stages = 0, x_box0 = 0, x_box1 = 0, paired = 0;
+  int n_slabs = 0, kblocks = 0, stages = 0, x_box0 = 0, x_box1 = 0, paired = 0, rep = 0;
   uint32_t stage_bytes = 0;
   LmRec* rec = nullptr;
   float inv_T = 0.f;  // 0 = greedy
