@@ -386,10 +386,17 @@ def run_e2e(dr, wl, ring, anchor, pos, stream, steps):
     dt = time.perf_counter() - t0
     hb = host[0]
     h2d = hb["hidden"].numel() * hb["hidden"].element_size() + B * 4 + B * 8
-    h2d += (hb["probs"].numel() * 4) if T > 0 else (B * (cfg.K + 1) * 4)
+    out = {}
+    if T > 0:   # pinned probabilities are read in place: each request's K draft entries and one full row
+        h2d += B * cfg.K * 4 + B * cfg.V * 4
+        out["target_probs"] = (f"read in place from pinned host memory by the verification "
+                               f"({hb['probs'].numel() * 4} B per step resident on the host; "
+                               f"counted: the K entries and the one row each request reads)")
+    else:
+        h2d += B * (cfg.K + 1) * 4
     d2h = B * 4 * 3 + B * (cfg.K + 1) * 4
     return {"value": round(steps / dt, 2), "unit": "rounds/s", "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "steps": steps}
+            "d2h_bytes_per_step": int(d2h), "steps": steps, **out}
 
 
 # ---------------------------------------------------------------- oracle (CPU) arm

@@ -108,6 +108,9 @@ struct dlite_handle {
   int64_t* d_pos = nullptr;
   float* d_probs = nullptr;
   dlite_qstats* d_qs = nullptr;
+  // dlite_round_host copies the target rows on its own stream, under the draft
+  cudaStream_t cstream = nullptr;
+  cudaEvent_t ev_in = nullptr, ev_cp = nullptr;
 };
 
 namespace {
@@ -808,6 +811,9 @@ void dlite_destroy(dlite_handle* h) {
   cudaDeviceSynchronize();
   if (h->prof_events_made)
     for (int i = 0; i < 128; ++i) cudaEventDestroy(h->prof_ev[i]);
+  if (h->ev_in) cudaEventDestroy(h->ev_in);
+  if (h->ev_cp) cudaEventDestroy(h->ev_cp);
+  if (h->cstream) cudaStreamDestroy(h->cstream);
   for (void* p : h->allocs) cudaFree(p);
   delete h;
 }
@@ -1130,6 +1136,9 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
   AL(h->d_commits, (size_t)Bm * (c.K + 1));
   AL(h->d_ncommit, Bm);
   AL(h->d_next, Bm);
+  CK(cudaStreamCreateWithFlags(&h->cstream, cudaStreamNonBlocking));
+  CK(cudaEventCreateWithFlags(&h->ev_in, cudaEventDisableTiming));
+  CK(cudaEventCreateWithFlags(&h->ev_cp, cudaEventDisableTiming));
   if (c.history > 0) {  // the conventional drafter's draft KV and the history kernels' buffers
     const int K1 = group_of(&c) + c.K;
     h->H = c.history;
@@ -1404,18 +1413,38 @@ int dlite_round_host(dlite_handle* h, int B, const void* hidden_host, const int3
   const dlite_config& c = h->cfg;
   cudaStream_t s = (cudaStream_t)stream;
   const size_t hb = (size_t)B * c.m * c.D * (h->f32 ? 4 : 2);
+  // the target rows (155 MB of probabilities at B = 32, V = 151936) are only
+  // read by the verification: they cross on the handle's copy stream while the
+  // draft runs, after whatever `stream` had queued (an earlier verification
+  // may still read the staging buffer)
+  // Pinned, device-mapped probabilities are not copied at all: the
+  // verification reads the entries and rows it uses in place (over the
+  // CPU-GPU link), a few percent of the tensor.
+  const float* probs_dev = h->d_probs;
+  if (sampling) {
+    cudaPointerAttributes pa;
+    if (cudaPointerGetAttributes(&pa, probs_host) == cudaSuccess && pa.type == cudaMemoryTypeHost &&
+        pa.devicePointer)
+      probs_dev = (const float*)pa.devicePointer;
+    else
+      cudaGetLastError();  // not a CUDA allocation: copied below
+  }
+  CK(cudaEventRecord(h->ev_in, s));
+  CK(cudaStreamWaitEvent(h->cstream, h->ev_in, 0));
+  if (sampling && probs_dev == h->d_probs)
+    CK(cudaMemcpyAsync(h->d_probs, probs_host, (size_t)B * (c.K + 1) * c.V * 4,
+                       cudaMemcpyHostToDevice, h->cstream));
+  else if (!sampling)
+    CK(cudaMemcpyAsync(h->d_tgt, tgt_host, (size_t)B * (c.K + 1) * 4, cudaMemcpyHostToDevice, h->cstream));
+  CK(cudaEventRecord(h->ev_cp, h->cstream));
   CK(cudaMemcpyAsync(h->d_hidden, hidden_host, hb, cudaMemcpyHostToDevice, s));
   CK(cudaMemcpyAsync(h->d_anchor, anchor_host, (size_t)B * group_of(&c) * 4, cudaMemcpyHostToDevice, s));
   if (pos_host) CK(cudaMemcpyAsync(h->d_pos, pos_host, (size_t)B * 8, cudaMemcpyHostToDevice, s));
-  if (sampling)
-    CK(cudaMemcpyAsync(h->d_probs, probs_host, (size_t)B * (c.K + 1) * c.V * 4,
-                       cudaMemcpyHostToDevice, s));
-  else
-    CK(cudaMemcpyAsync(h->d_tgt, tgt_host, (size_t)B * (c.K + 1) * 4, cudaMemcpyHostToDevice, s));
   RUN(dlite_draft_round(h, B, h->d_hidden, h->d_anchor, temperature, seed,
                         pos_host ? h->d_pos : nullptr, h->d_cand, h->d_qs, stream));
+  CK(cudaStreamWaitEvent(s, h->ev_cp, 0));
   if (sampling)
-    RUN(dlite_verify_sample(h, B, h->d_cand, h->d_qs, nullptr, h->d_probs, temperature, seed,
+    RUN(dlite_verify_sample(h, B, h->d_cand, h->d_qs, nullptr, probs_dev, temperature, seed,
                             h->d_pos, h->d_acc, h->d_commits, h->d_ncommit, h->d_next, stream));
   else
     RUN(dlite_verify(h, B, h->d_cand, h->d_tgt, h->d_acc, h->d_commits, h->d_ncommit, h->d_next,

@@ -310,7 +310,12 @@ int dlite_advance(dlite_handle *h, int B, const int32_t *n_commit, int64_t *pos,
  * (temperature == 0) or target_probs_host [B, K+1, V] (temperature > 0) to the
  * device, runs draft + verify, copies accepted/commits/n_commit/next_anchor
  * back into the *_host outputs, and synchronises `stream`. Host buffers should
- * be pinned for asynchronous copies. Uses handle-owned device staging buffers. */
+ * be pinned for asynchronous copies. Uses handle-owned device staging buffers;
+ * the target rows cross on a handle-owned copy stream while the draft runs on
+ * `stream` (the verification waits for them). Target probabilities in pinned,
+ * device-mapped host memory (cudaHostAlloc / pinned tensors on a unified-address
+ * system) are not copied: the verification reads the entries and rows it uses
+ * in place, so only those cross the CPU-GPU link. */
 int dlite_round_host(dlite_handle *h, int B, const void *hidden_host, const int32_t *anchor_host,
                      const int64_t *pos_host, const int32_t *target_tokens_host,
                      const float *target_probs_host, float temperature, uint64_t seed,

@@ -647,6 +647,27 @@ def test_round_host_matches_device_path(tiny):
         assert torch.equal(dev[k].cpu(), host[k]), k
 
 
+def test_round_host_sampling_matches_device_path(tiny):
+    """Sampling through the host-buffer call: target probabilities in pinned
+    (device-mapped, read in place) and in pageable (copied) host memory both
+    give the device path's accepted lengths and commits."""
+    wl, W, dr = tiny
+    cfg = wl.cfg
+    B, T, seed = 4, 0.7, 99
+    hidden, anchor, pos = wk.make_round_inputs(wl, B=B, round_index=5)
+    probs = wk.make_target_probs(B, cfg.K, cfg.V, 5)
+    dev = dr.new_outputs(B, DEV)
+    dr.draft_round(hidden.to(DEV), anchor.to(DEV), T, seed, pos.to(DEV), dev["cand"], dev["qstats"])
+    dr.verify_sample(dev["cand"], dev["qstats"], None, probs.to(DEV), T, seed, pos.to(DEV), dev["accepted"],
+                     dev["commits"], dev["n_commit"], dev["next_anchor"])
+    for pinned in (True, False):
+        host = {k: v.cpu().pin_memory() for k, v in dr.new_outputs(B, "cpu").items()}
+        p_h = probs.pin_memory() if pinned else probs.clone()
+        dr.round_host(hidden.pin_memory(), anchor.pin_memory(), pos.pin_memory(), None, p_h, T, seed, host)
+        for k in ("accepted", "commits", "n_commit", "next_anchor"):
+            assert torch.equal(dev[k].cpu(), host[k]), (pinned, k)
+
+
 # ---------------------------------------------------------------- full-size shapes, sampled
 
 @pytest.mark.parametrize("name", ["qwen3-4b-b1", "qwen3-8b-b32"])
