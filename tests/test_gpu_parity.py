@@ -712,6 +712,8 @@ def test_full_size_round_sampled_requests(name):
 def _history_cfg(name, H):
     if name == "d128":   # 4 query heads per key/value head, as in the 8B shape: 32 query rows per head
         return wk.shrink(wk.QWEN3_8B, D=512, F=1024, L_D=2, n_q=8, n_kv=2, R=64, V=4096, m=6, history=H)
+    if name == "d128wide":   # 8 query heads x 9 local rows = 72 query rows per head: one key split per tile
+        return wk.shrink(wk.QWEN3_8B, D=512, F=1024, L_D=1, n_q=16, n_kv=2, K=8, R=64, V=4096, m=6, history=H)
     return wk.shrink(wk.TINY, dtype="bf16", history=H)   # d_h = 64, 2 heads per group
 
 
@@ -734,7 +736,7 @@ def test_history_fill_matches_oracle(name):
         dr.close()
 
 
-@pytest.mark.parametrize("name,H", [("d128", 300), ("d128", 64), ("d64", 200), ("d64", 12)])
+@pytest.mark.parametrize("name,H", [("d128", 300), ("d128", 64), ("d64", 200), ("d64", 12), ("d128wide", 150)])
 def test_history_round_parity(name, H):
     """Three rounds of the history-KV control (the 12-row ring wraps): hidden rows and candidates against
     the oracle drafter attending over its own ring, then each ring after the
