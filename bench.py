@@ -42,6 +42,23 @@ def dist_env():
     return ws, rank, local
 
 
+def shard_round_index(k, rank):
+    """Input slot k of rank `rank`: every replica drafts its own requests (weak scaling)."""
+    return k + 1000 * rank
+
+
+def reduce_over_ranks(t_s, committed, device):
+    """The job's time (the slowest rank) and its committed tokens (all ranks)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return t_s, committed
+    tt = torch.tensor([t_s], device=device, dtype=torch.float64)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    cc = torch.tensor([committed], device=device, dtype=torch.int64)
+    dist.all_reduce(cc)
+    return float(tt.item()), int(cc.item())
+
+
 KERNEL_SOURCES = ["lm_head.cu", "tc_device.cuh", "tc_gemm.h", "internal.h", "common.cuh"]
 
 
@@ -173,13 +190,13 @@ def run_gpu(args):
     # ring of per-round inputs (each rank its own shard of requests: weak scaling)
     ring = []
     for k in range(RING):
-        hidden, anchor, pos = wk.make_round_inputs(wl, round_index=k + 1000 * rank, device=dev)
+        hidden, anchor, pos = wk.make_round_inputs(wl, round_index=shard_round_index(k, rank), device=dev)
         item = {"hidden": hidden}
         if sampling or match:
             item["probs"] = wk.make_target_probs(B, cfg.K, cfg.V, wl.rng_seed + 17 * k + 1000 * rank,
                                                  device=dev)
         ring.append(item)
-    _, anchor, pos = wk.make_round_inputs(wl, round_index=999 + 1000 * rank, device=dev)
+    _, anchor, pos = wk.make_round_inputs(wl, round_index=shard_round_index(999, rank), device=dev)
     if grp > 1:   # the group [B, G] (anchor last); the verification writes its next anchor aside
         group = torch.randint(0, cfg.V, (B, grp), device=dev, dtype=torch.int32)
         next_tok = torch.empty(B, device=dev, dtype=torch.int32)
@@ -263,14 +280,7 @@ def run_gpu(args):
     ms = ev0.elapsed_time(ev1)
     t_s = ms / 1e3
     committed = int(ncommit_total.item())
-    if ws > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([t_s], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_s = float(tt.item())
-        cc = torch.tensor([committed], device=dev, dtype=torch.int64)
-        dist.all_reduce(cc)
-        committed = int(cc.item())
+    t_s, committed = reduce_over_ranks(t_s, committed, dev)
     rounds_s = ws * args.steps / t_s
     tok_s = committed / t_s
     counters = dr.counters(reset=True)
