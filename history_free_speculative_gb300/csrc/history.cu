@@ -2,8 +2,9 @@
 // that the history-free one is compared against keeps its own draft KV, a ring
 // of the last H local key / value rows per layer and request, and attends over
 // it beside the block ([P1] §"本轮临时 K/V 仍然需要计算": the draft KV of a
-// conventional drafter grows with the history; [P2] "Cost of the history" table:
-// draft memory 2 L_D H n_kv d_h per request). Kernels:
+// conventional drafter grows with the history, M_draftKV ≈ 2 L_D H n_kv d_h b;
+// [P2] §"实验：三类负载，逐项看数字", ablation: 128- and 512-token
+// sliding-window KV variants). Kernels:
 //   hist_fill      the synthetic history (Philox, tag 6), bit-identical to the
 //                  CPU definition: four uniforms summed in fp32, centred and
 //                  scaled to unit variance, rounded to bf16;

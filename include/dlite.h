@@ -79,8 +79,9 @@ typedef struct {
                        * dlite_weights.gated; R a multiple of 64) */
     int history;      /* H: history-KV control of the history-cost comparison. 0 (the method):
                        * history-free, no draft KV. H > 0: the conventional drafter the method is
-                       * measured against ([P1] §"本轮临时 K/V 仍然需要计算"; [P2] "Cost of the
-                       * history"): every backbone layer keeps a ring of the last H local key /
+                       * measured against ([P1] §"本轮临时 K/V 仍然需要计算", eq. M_draftKV; [P2]
+                       * §"实验：三类负载，逐项看数字", the sliding-window ablation): every backbone
+                       * layer keeps a ring of the last H local key /
                        * value rows of each request slot (bf16, 2 L_D H n_kv d_h values per slot,
                        * allocated by dlite_create and filled with the synthetic history that
                        * dlite_history_reset describes); each backbone pass attends over the H

@@ -2,7 +2,7 @@
 history-cost workload and the per-launch bytes of the history attention.
 
 The draft KV of the control drafter is 2 L_D H n_kv d_h values per request
-("Cost of the history": 2 * layers * history * KV heads * head width, bf16):
+(DLite 完全拆解, §"本轮临时 K/V 仍然需要计算", eq. M_draftKV ≈ 2 L_D H n_kv d_h b; bf16):
 at the 8B shape (L_D 3, 8 KV heads of 128) 100.7 MB at H = 8192, 503.3 MB at
 H = 40960 and 1.450 GB at H = 118000, per request.
 """
