@@ -68,3 +68,29 @@ def test_engine_matches_float64(rows, outs, K, xp, wp):
     err = np.abs(got - ref).max()
     assert np.isfinite(got).all()
     assert err <= 1e-5 * scale, (err, scale)
+
+
+@pytest.mark.parametrize("N", [64, 128, 192, 256])
+@pytest.mark.parametrize("S", [1, 2, 4])
+@pytest.mark.parametrize("rows", [256, 100])
+def test_engine_plans_match_float64(N, S, rows):
+    """Every slab width and k split the create-time plan timing may pick, on a
+    two-tile and a one-tile row count: the same product as the float64 one."""
+    outs, K = 768, 512
+    g = torch.Generator().manual_seed(N * 31 + S * 7 + rows)
+    x_rows = (rows + 127) // 128 * 128
+    X = torch.randn(x_rows, K, generator=g)
+    X[rows:] = float("nan")
+    W = torch.randn(outs, K, generator=g) * 0.05
+    Xp = [p.to(DEV) for p in _planes(X, 1)]
+    Wp = [p.to(DEV) for p in _planes(W, 1)]
+    got, st = binding.selftest_gemm(Xp, [_tiled(p) for p in Wp], rows=rows, outs=outs, plan=(N, S, 0))
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    x64 = Xp[0][:rows].double().cpu().numpy()
+    w64 = Wp[0].double().cpu().numpy()
+    ref = x64 @ w64.T
+    got = got.double().cpu().numpy()
+    scale = np.sqrt(K) * np.abs(w64).max() * np.abs(x64).max()
+    assert np.isfinite(got).all()
+    assert np.abs(got - ref).max() <= 1e-5 * scale
