@@ -834,3 +834,30 @@ def test_full_size_history_round_sampled_requests():
             assert rel_err(got[:K1], hm.k[l][:K1]) < HIDDEN_REL_TOL
     check_candidates(np.stack(cands), np.stack(ocands), np.stack(gaps))
     dr.close()
+
+
+def test_history_ring_memory_matches_draft_kv_formula():
+    """The control's device memory grows by the draft-KV formula 2 L_D H n_kv d_h b
+    per request slot (DLite 完全拆解, §"本轮临时 K/V 仍然需要计算", eq. M_draftKV), plus a
+    fixed workspace (the block rows behind each ring, staged queries and chunk
+    partials bounded by 8 CTAs per SM) that does not grow with H."""
+    H, Bm = 65536, 4
+    cfg = _history_cfg("d128", H)
+    cfg0 = _history_cfg("d128", 0)
+    W = wk.make_weights(cfg, 43)
+    Wd = wk.weights_to(W, DEV)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    d0 = binding.Drafter(cfg0, Wd, B_max=Bm)
+    torch.cuda.synchronize()
+    free1 = torch.cuda.mem_get_info()[0]
+    d1 = binding.Drafter(cfg, Wd, B_max=Bm)
+    torch.cuda.synchronize()
+    free2 = torch.cuda.mem_get_info()[0]
+    try:
+        extra = (free1 - free2) - (free0 - free1)
+        formula = 2 * cfg.L_D * H * cfg.n_kv * cfg.d_h * 2 * Bm
+        assert formula <= extra <= formula + (64 << 20), (extra, formula)
+    finally:
+        d0.close()
+        d1.close()
