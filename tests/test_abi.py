@@ -65,3 +65,45 @@ def test_host_side_validation_needs_no_gpu(so):
     assert lib.dlite_verify(None, 1, None, None, None, None, None, None, None) == -1
     assert lib.dlite_status_string(-2) == b"unsupported shape"
     lib.dlite_destroy(None)
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("history", -1, -1),            # negative history: invalid
+    ("history", 2, -2),             # a ring shorter than the round's G + K rows
+    ("history", (1 << 20) + 1, -2),  # past the synthetic history's counter range
+    ("anchor_group", 9, -2),        # local token group longer than 8
+    ("head_type", 2, -1),           # no such head
+    ("R", 96, -2),                  # gated head: R must be a multiple of 64 (with head_type 1 below)
+])
+def test_config_checks_need_no_gpu(so, field, value, code):
+    """The history, group and head fields of dlite_config are checked before any CUDA call."""
+    lib = binding.load()
+    h = ctypes.c_void_p()
+    cfg = binding.Config(B_max=1, D=256, m=4, K=4, L_D=1, n_q=4, n_kv=2, d_h=64, F=768, R=64,
+                         V=2048, dtype=1, rms_eps=1e-6, rope_theta=1e6, anchor_group=1, head_type=0,
+                         history=0)
+    setattr(cfg, field, value)
+    if field == "R":
+        cfg.head_type = 1
+    w = binding.Weights()
+    for n in ("e_depth", "g_stage", "e_ph", "E", "g_final", "Q", "P"):
+        setattr(w, n, 1)
+    for n in binding.GATED_FIELDS:
+        setattr(w.gated, n, 1)
+    assert lib.dlite_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == code
+
+
+def test_history_needs_bf16_and_few_query_rows(so):
+    lib = binding.load()
+    h = ctypes.c_void_p()
+    w = binding.Weights()
+    for n in ("e_depth", "g_stage", "e_ph", "E", "g_final", "Q", "P"):
+        setattr(w, n, 1)
+    cfg = binding.Config(B_max=1, D=256, m=4, K=4, L_D=1, n_q=4, n_kv=2, d_h=64, F=768, R=64,
+                         V=2048, dtype=0, rms_eps=1e-6, rope_theta=1e6, history=64)
+    assert lib.dlite_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == -2   # fp32 drafter
+    cfg.dtype = 1
+    cfg.n_q, cfg.n_kv, cfg.K = 32, 1, 7   # 32 heads x 8 rows = 256 query rows per KV head
+    assert lib.dlite_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == -2
+    assert lib.dlite_history_reset(None, None) == -1
+    assert lib.dlite_history_read(None, 0, 0, 0, None, None, None) == -1
