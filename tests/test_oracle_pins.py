@@ -719,3 +719,86 @@ def test_ffn_gate_goes_through_silu_up_is_linear():
         d2 = O.backbone_layer(x, z, Wl, cfg) - x
         close = np.allclose(d2, 2.0 * delta, rtol=1e-9, atol=1e-12)
         assert close == linear, name
+
+
+# ---------------------------------------------------------------- attention wiring of a layer
+
+def _wiring_setup(G=1, seed=31):
+    # jittered gains: the staged z is then far from unit RMS, so a context row
+    # taken through the pre-attention norm differs from z itself
+    cfg = _tiny(G=G)
+    W = _weights(cfg, seed=seed, jitter=True)
+    rng = np.random.default_rng(seed + 1)
+    x = rng.normal(size=(cfg.G + cfg.K, cfg.D))
+    hidden = torch.from_numpy(rng.normal(size=(cfg.m, cfg.D)))
+    z, _ = O.stage(hidden, [0] * cfg.G if G > 1 else 0, W, cfg)
+    return cfg, W, x, z
+
+
+def test_layer_with_zero_queries_averages_the_value_rows():
+    """W_q = 0 makes every score zero, so each query head returns the plain mean
+    of its KV group's value rows over all m + G + K keys: the context rows
+    projected from the staged z as it is, the local rows from the normed
+    y = RMSNorm(x) g_attn, neither rotated. With W_d = 0 the layer output is
+    then x + mean W_o^T in closed form ([P1] §"本轮临时 K/V 仍然需要计算":
+    context and local rows both give keys / values)."""
+    cfg, W, x, z = _wiring_setup()
+    Wl = dict(W["layers"][0])
+    Wl["Wq"] = torch.zeros_like(Wl["Wq"])
+    Wl["Wd"] = torch.zeros_like(Wl["Wd"])
+    g = O.f64(Wl["g_attn"])
+    y = g * x / np.sqrt((x * x).mean(axis=1, keepdims=True) + cfg.eps)
+    Wv = O.f64(Wl["Wv"])
+    rows = np.concatenate([z, y]) @ Wv.T                       # [m + K1, n_kv d_h]
+    mean = rows.mean(axis=0).reshape(cfg.n_kv, cfg.d_h)
+    group = cfg.n_q // cfg.n_kv
+    o = np.concatenate([mean[h // group] for h in range(cfg.n_q)])
+    want = x + (o @ O.f64(Wl["Wo"]).T)[None, :]
+    got = O.backbone_layer(x, z, Wl, cfg)
+    assert np.allclose(got, want, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("G", [1, 2])
+def test_layer_attention_inputs_follow_the_local_positions(G, monkeypatch):
+    """What a layer hands to the attention, against an independent statement in
+    complex form: local row i (position i: the group at 0..G-1, placeholders
+    after it) gives q_i = rot_i(W_q y_i) and k_i = rot_i(W_k y_i), where rot_p
+    multiplies the pair (j, j + d_h/2), read as one complex number, by
+    exp(i p theta^(-2j/d_h)); context row j gives k = W_k z_j with no rotation
+    (position 0) and no norm; values are never rotated. The score matrix
+    q k^T / sqrt(d_h) and the values are compared ([P1]
+    §"局部位置编码切断草稿端的全局位置增长")."""
+    cfg, W, x, z = _wiring_setup(G=G, seed=37 + G)
+    Wl = W["layers"][0]
+    seen = {}
+    real = O.block_attention
+
+    def spy(q, k, v, n_q, n_kv):
+        seen.update(q=np.array(q), k=np.array(k), v=np.array(v))
+        return real(q, k, v, n_q, n_kv)
+
+    monkeypatch.setattr(O, "block_attention", spy)
+    O.backbone_layer(x, z, Wl, cfg)
+    K1, d = cfg.G + cfg.K, cfg.d_h
+    g = O.f64(Wl["g_attn"])
+    y = g * x / np.sqrt((x * x).mean(axis=1, keepdims=True) + cfg.eps)
+
+    def rot(rows, pos):   # rows [T, heads, d]
+        half = d // 2
+        c = rows[..., :half] + 1j * rows[..., half:]
+        w = np.exp(1j * np.outer(pos, cfg.theta ** (-2.0 * np.arange(half) / d)))[:, None, :]
+        c = c * w
+        return np.concatenate([c.real, c.imag], axis=-1)
+
+    pos = np.arange(K1, dtype=np.float64)
+    q = rot((y @ O.f64(Wl["Wq"]).T).reshape(K1, cfg.n_q, d), pos)
+    k_loc = rot((y @ O.f64(Wl["Wk"]).T).reshape(K1, cfg.n_kv, d), pos)
+    k_ctx = (z @ O.f64(Wl["Wk"]).T).reshape(cfg.m, cfg.n_kv, d)
+    v = (np.concatenate([z, y]) @ O.f64(Wl["Wv"]).T).reshape(cfg.m + K1, cfg.n_kv, d)
+    k = np.concatenate([k_ctx, k_loc])
+    group = cfg.n_q // cfg.n_kv
+    for h in range(cfg.n_q):
+        want = q[:, h] @ k[:, h // group].T / math.sqrt(d)
+        got = seen["q"][:, h] @ seen["k"][:, h // group].T / math.sqrt(d)
+        assert np.allclose(got, want, rtol=0, atol=1e-10), h
+    assert np.allclose(seen["v"], v, rtol=0, atol=1e-12)
