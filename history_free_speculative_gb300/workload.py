@@ -34,6 +34,8 @@ class DraftConfig:
     G: int = 1      # local token group ending at the anchor (local positions 0..G-1)
     head: str = "rnn"   # "rnn": low-rank RNN head + tied D->V projection; "gated": token-feedback head
     history: int = 0    # H > 0: history-KV control (a ring of the last H draft K/V rows per layer)
+    act_planes: int = 1  # bf16 drafters: 1 = bf16 activations; 2 = fp32-class (two bf16 planes)
+    warmup: int = 0     # gated head: warm the state up on the token before the anchor (needs G >= 2)
 
     @property
     def torch_dtype(self):
@@ -64,6 +66,7 @@ class Workload:
     index: int                 # seeds are 1234/1235/1236 + 100 * index
     accept_c: float = 0.0      # greedy: per-position agreement probability
     scaled_hidden: bool = True
+    accept_classes: bool = False   # greedy: two request classes, c ~ Beta(6, 4) / Beta(18, 2)
 
     @property
     def weight_seed(self):
@@ -86,9 +89,9 @@ WORKLOADS = {
     "qwen3-8b-b32": Workload("qwen3-8b-shape-b32-sample-t0.7", QWEN3_8B, B=32,
                              temperature=0.7, index=2),
     "qwen3-8b-sweep": Workload("qwen3-8b-shape-sweep", QWEN3_8B, B=64, temperature=0.0,
-                               index=3),
+                               index=3, accept_classes=True),
     "qwen3-8b-history": Workload("qwen3-8b-shape-b8-history-control", QWEN3_8B, B=8,
-                                 temperature=0.0, index=4),
+                                 temperature=0.0, index=4, accept_classes=True),
 }
 
 SWEEP_BATCHES = (1, 2, 4, 8, 16, 32, 64)
@@ -200,16 +203,25 @@ def make_target_tokens(ref_cand, accept_p, V, seed, device="cpu"):
     return tgt.to(torch.int32)
 
 
-def make_beta_accept(B, K, seed, device="cpu"):
+def make_beta_accept(B, K, seed, device="cpu", n_tables=None):
     """Per-position agreement probabilities for the two-class sweep.
 
     Even requests: c ~ Beta(6, 4) (agentic-like); odd: c ~ Beta(18, 2)
-    (structured-output-like); drawn iid per (request, position).
+    (structured-output-like); drawn iid per (table, request, position). With
+    n_tables the result is [n_tables, B, K] (one table per round, cycled by the
+    synthetic target's round counter), else [B, K]. float64.
     """
     rng = np.random.default_rng(int(seed))
-    a = np.array([6.0 if b % 2 == 0 else 18.0 for b in range(B)])[:, None] * np.ones((1, K))
-    bb = np.array([4.0 if b % 2 == 0 else 2.0 for b in range(B)])[:, None] * np.ones((1, K))
-    return torch.from_numpy(rng.beta(a, bb)).to(device)
+    n = 1 if n_tables is None else int(n_tables)
+    a = np.array([6.0 if b % 2 == 0 else 18.0 for b in range(B)])[None, :, None] * np.ones((n, 1, K))
+    bb = np.array([4.0 if b % 2 == 0 else 2.0 for b in range(B)])[None, :, None] * np.ones((n, 1, K))
+    c = torch.from_numpy(rng.beta(a, bb)).to(device)
+    return c if n_tables is not None else c[0]
+
+
+def make_const_accept(B, K, c, n_tables=1, device="cpu"):
+    """A constant agreement probability c for every (table, request, position): [n_tables, B, K]."""
+    return torch.full((n_tables, B, K), float(c), dtype=torch.float64, device=device)
 
 
 def make_target_probs(B, K, V, seed, device="cpu", support=64, logit_std=3.0, tail=1e-3,

@@ -289,7 +289,18 @@ def _pick(ell_i, temperature, seed, position, request):
     return int(np.argmax(s)), float(_top2_gap(s[None, :])[0]), lse
 
 
-def gated_head(b, anchor_token, W, temperature=0.0, seed=0, pos=0, request=0):
+def gated_state_step(s_prev, token, W):
+    """One state update of the gated head on the previous token's embedding:
+    [g, c] = W_s [s_prev; E_R(token)] + b_s;  f = sigmoid(g);
+    s = f * s_prev + (1 - f) * tanh(c)  ([P1] §"官方顺序头具体算了什么", eq. block)."""
+    E_R, W_s, b_s = f64(W["E_R"]), f64(W["W_s"]), f64(W["b_s"])
+    R = E_R.shape[1]
+    gc = W_s @ np.concatenate([s_prev, E_R[int(token)]]) + b_s
+    f = 1.0 / (1.0 + np.exp(-gc[:R]))
+    return f * s_prev + (1.0 - f) * np.tanh(gc[R:])
+
+
+def gated_head(b, anchor_token, W, temperature=0.0, seed=0, pos=0, request=0, warm_token=None):
     """The official gated token-feedback head, direct form ([P1] §"官方顺序头具体
     算了什么", eq. block), one request:
         v_i = E_R(d_{i-1}), d_0 = the anchor;
@@ -300,6 +311,10 @@ def gated_head(b, anchor_token, W, temperature=0.0, seed=0, pos=0, request=0):
     and d_i is drawn from l_i like the main head's candidates (argmax, or
     Gumbel-max on l_i / T at position pos + i) before step i + 1 reads it.
     g is the first R outputs of W_s, c the last R; W_h acts on [s; u].
+    Warm-up (the same passage: when the configuration allows, the one token
+    before the anchor warms the state up for a fixed length): with warm_token,
+    s_0 is one state update from the zero state on E_R(warm_token), with no
+    output; step 1 then reads s_0 and the anchor as before.
     Returns dict(cand, logit_d, lse, gap, r [K, R], logits [K, V]).
     """
     u = f64(b)
@@ -309,6 +324,8 @@ def gated_head(b, anchor_token, W, temperature=0.0, seed=0, pos=0, request=0):
     R = E_R.shape[1]
     temperature = float(np.float32(temperature))
     s_prev = np.zeros(R)
+    if warm_token is not None:
+        s_prev = gated_state_step(s_prev, warm_token, W)
     d_prev = int(anchor_token)
     cand, logit_d, lse, gap = [], [], [], []
     rs, ells = np.empty((K, R)), []
@@ -366,7 +383,9 @@ def draft_request(hidden, anchor, W, cfg, temperature=0.0, seed=0, pos=0, reques
     if history is not None:   # the round's local rows join the draft KV afterwards
         history.append(local)
     if getattr(cfg, "head", "rnn") == "gated":   # token feedback: vocabulary projection inside each step
-        r = gated_head(b, anchor_group(anchor, cfg)[-1], W, temperature, seed, pos, request)
+        group = anchor_group(anchor, cfg)
+        warm = group[-2] if getattr(cfg, "warmup", 0) else None   # the token before the anchor
+        r = gated_head(b, group[-1], W, temperature, seed, pos, request, warm_token=warm)
         if taps is not None:
             taps["b"] = b
             taps["h"] = r["r"]
@@ -535,6 +554,42 @@ def verify_match(cand, p, seed, pos, request, n_verify=None):
         A += 1
     tok = t[A]
     return dict(A=A, commits=cand[:A] + [tok], n_commit=A + 1, next_anchor=tok, targets=t)
+
+
+# ---------------------------------------------------------------- synthetic target
+
+def synthetic_target_tokens(cand, c, seed, pos, request, V):
+    """Target choices [K+1] of one request that stand in for the target model
+    in the acceptance workloads.
+
+    The acceptance model is the per-position conditional acceptance c_i of
+    [P1] §"分布重叠怎样影响平均推进量" and of the DFlash page's prefix-survival
+    formula P(A >= k) = prod_{i<=k} c_i: the target's choice at input index j
+    (its choice for position j + 1) equals the candidate d_{j+1} with
+    probability c_j, independently per position, and is otherwise a uniform
+    id different from it; the choice at index K (the bonus position) is a
+    uniform id.
+    Draws: the words (w0, w1, w2, w3) of Philox(counter = (0, pos + j + 1,
+    request, TAG_TARGET), key = seed). Agreement iff uniform_open(w0) < c_j
+    (c_j a float32 value; both sides exact in float64). A disagreeing choice
+    is (d_{j+1} + 1 + floor(w1 (V - 1) / 2^32)) mod V; the bonus choice is
+    floor(w1 V / 2^32). Integer arithmetic throughout, so both sides agree
+    bit for bit.
+    """
+    cand = [int(x) for x in cand]
+    K = len(cand)
+    c = np.asarray(c, dtype=np.float32).astype(np.float64)
+    out = []
+    for j in range(K + 1):
+        w = _ph.words(seed, 0, pos + j + 1, request, _ph.TAG_TARGET)
+        if j == K:
+            out.append((int(w[1]) * V) >> 32)
+            break
+        if float(_ph.uniform_open(w[0])) < c[j]:
+            out.append(cand[j])
+        else:
+            out.append((cand[j] + 1 + ((int(w[1]) * (V - 1)) >> 32)) % V)
+    return out
 
 
 # ---------------------------------------------------------------- batch drivers

@@ -333,6 +333,50 @@ def test_gated_head_open_gate_reads_the_previous_token():
     assert not np.allclose(other["r"][0], out["r"][0])   # the anchor is fed back
 
 
+def test_gated_head_warmup_saturated_gate_is_a_no_op():
+    """Warm-up on the token before the anchor ([P1] §"官方顺序头具体算了什么"): with
+    f -> 1 the warm-up step keeps the zero state (s_0 = 1 * 0 + 0 * tanh c), so
+    the head's outputs equal those without warm-up, whatever the token."""
+    W, u, R = _gated_setup(8)
+    W["b_s"] = W["b_s"].copy()
+    W["b_s"][:R] = 60.0
+    base = O.gated_head(u, 5, W)
+    for w in (0, 31, 63):
+        out = O.gated_head(u, 5, W, warm_token=w)
+        assert np.array_equal(out["r"], base["r"]) and list(out["cand"]) == list(base["cand"])
+
+
+def test_gated_head_warmup_open_gate_closed_form():
+    """With f -> 0 the warm-up state is s_0 = tanh(W_s^c [0; E_R(w)] + b_s^c) (c the
+    last R outputs of W_s); step 1 then updates from s_0 on the anchor's
+    embedding: s_1 = tanh(W_s^c [s_0; E_R(a)] + b_s^c), r_1 = W_h [s_1; u_1] + b_h.
+    A warm-up that read the anchor, skipped the zero start, or fed its state to
+    r (an output for the warm-up token) fails this."""
+    W, u, R = _gated_setup(9)
+    W["b_s"] = W["b_s"].copy()
+    W["b_s"][:R] = -60.0
+    a, w = 12, 40
+    s0 = np.tanh(W["W_s"][R:, R:] @ W["E_R"][w] + W["b_s"][R:])
+    s1 = np.tanh(W["W_s"][R:, :R] @ s0 + W["W_s"][R:, R:] @ W["E_R"][a] + W["b_s"][R:])
+    r1 = W["W_h"][:, :R] @ s1 + W["W_h"][:, R:] @ u[0] + W["b_h"]
+    out = O.gated_head(u, a, W, warm_token=w)
+    assert np.allclose(out["r"][0], r1, atol=1e-12)
+    assert out["r"].shape[0] == u.shape[0]                       # K outputs, none for the warm-up
+    assert not np.allclose(O.gated_head(u, a, W, warm_token=w + 1)["r"][0], r1)   # the token matters
+
+
+def test_draft_warmup_takes_the_token_before_the_anchor():
+    """In a drafted round the warm-up token is the group's second-to-last token."""
+    cfg = _tiny(G=3, head="gated", warmup=1, R=64)
+    W = _weights(cfg, seed=13)
+    hidden, _, _ = wk.make_round_inputs(wk.WORKLOADS["tiny"], B=1, cfg=cfg)
+    group = [7, 21, 9]
+    r = O.draft_request(hidden[0], group, W, cfg)
+    b = O.backbone(hidden[0], group, W, cfg)
+    want = O.gated_head(b, 9, W, warm_token=21)
+    assert list(r["cand"]) == list(want["cand"]) and np.allclose(r["h"], want["r"], atol=1e-12)
+
+
 def test_gated_head_sampling_follows_softmax():
     """T > 0: the first candidate is a draw from softmax(l_1 / T) (chi-square
     over positions), and lse is the log-sum-exp of l_1 / T."""
@@ -802,3 +846,66 @@ def test_layer_attention_inputs_follow_the_local_positions(G, monkeypatch):
         got = seen["q"][:, h] @ seen["k"][:, h // group].T / math.sqrt(d)
         assert np.allclose(got, want, rtol=0, atol=1e-10), h
     assert np.allclose(seen["v"], v, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- synthetic target of the acceptance workloads
+
+def test_synthetic_target_extremes():
+    """c = 1: the target agrees everywhere (A = K); c = 0: it never agrees and
+    every disagreeing id differs from the candidate (A = 0)."""
+    rng = np.random.default_rng(51)
+    V, K = 37, 6
+    for r in range(300):
+        cand = [int(t) for t in rng.integers(0, V, K)]
+        t1 = O.synthetic_target_tokens(cand, np.ones(K), 9, r, 2, V)
+        assert t1[:K] == cand and 0 <= t1[K] < V
+        t0 = O.synthetic_target_tokens(cand, np.zeros(K), 9, r, 2, V)
+        assert all(a != b and 0 <= a < V for a, b in zip(t0[:K], cand))
+        assert O.verify_greedy(cand, t1)["A"] == K and O.verify_greedy(cand, t0)["A"] == 0
+
+
+def test_synthetic_target_other_ids_are_uniform():
+    """A disagreeing choice is uniform over the V - 1 other ids and the bonus
+    choice uniform over all V (chi-square)."""
+    V, K, N = 5, 3, 6000
+    other = np.zeros(V)
+    bonus = np.zeros(V)
+    for r in range(N):
+        t = O.synthetic_target_tokens([2] * K, np.zeros(K), 17, 10 * r, 1, V)
+        for x in t[:K]:
+            other[x] += 1
+        bonus[t[K]] += 1
+    assert other[2] == 0
+    e = K * N / (V - 1)
+    chi_o = (((other - e) ** 2) / e)[[0, 1, 3, 4]].sum()
+    chi_b = (((bonus - N / V) ** 2) / (N / V)).sum()
+    assert chi_o < 25.0 and chi_b < 25.0        # 3 and 4 dof; P(> 25) < 1e-4
+
+
+def test_synthetic_target_prefix_survival():
+    """Greedy verification against the synthetic target: P(A >= k) = prod c_i
+    (DFlash page, prefix survival; [P1] §"分布重叠怎样影响平均推进量"), within
+    5 sigma binomial bands, and E[A + 1] = 1 + sum_k P(A >= k)."""
+    c = np.array([0.9, 0.8, 0.7, 0.95, 0.6], dtype=np.float32)
+    K, V, N = len(c), 1000, 20000
+    cand = [3, 1, 4, 1, 5]
+    A = np.array([O.verify_greedy(cand, O.synthetic_target_tokens(cand, c, 23, 8 * n, n % 7, V))["A"]
+                  for n in range(N)])
+    surv = np.cumprod(c.astype(np.float64))
+    for k in range(1, K + 1):
+        p = surv[k - 1]
+        assert abs((A >= k).mean() - p) < 5 * math.sqrt(p * (1 - p) / N), k
+    assert abs((A + 1).mean() - rp.expected_advance(surv)) < 5 * (A + 1).std() / math.sqrt(N)
+
+
+def test_synthetic_target_is_keyed():
+    """Different seeds, positions and requests give different draws; the same
+    key gives the same tokens."""
+    cand = list(range(10, 17))
+    c = np.full(7, 0.5)
+    base = O.synthetic_target_tokens(cand, c, 5, 100, 3, 151936)
+    assert base == O.synthetic_target_tokens(cand, c, 5, 100, 3, 151936)
+    for kw in ({"seed": 6}, {"pos": 101}, {"request": 4}):
+        args = dict(seed=5, pos=100, request=3)
+        args.update(kw)
+        assert O.synthetic_target_tokens(cand, c, args["seed"], args["pos"], args["request"], 151936) != base
