@@ -31,7 +31,8 @@ class Config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in
                 ("B_max", "D", "m", "K", "L_D", "n_q", "n_kv", "d_h", "F", "R", "V", "dtype")] + \
                [("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float), ("anchor_group", ctypes.c_int),
-                ("head_type", ctypes.c_int), ("history", ctypes.c_int)]
+                ("head_type", ctypes.c_int), ("history", ctypes.c_int), ("act_planes", ctypes.c_int),
+                ("head_warmup", ctypes.c_int)]
 
 
 class LayerWeights(ctypes.Structure):
@@ -93,6 +94,8 @@ _SIGS = {
     "dlite_verify_sample_static": (_I, [_I, _I, _I, _I, _P, _P, _P, _P, _P, _F, _U64, _P, _P, _P,
                                         _P, _P, _P]),
     "dlite_round_host": (_I, [_P, _I, _P, _P, _P, _P, _P, _F, _U64, _P, _P, _P, _P, _P]),
+    "dlite_synthetic_target": (_I, [_I, _I, _I, _P, _P, _I, _P, _U64, _P, _P, _P]),
+    "dlite_selftest_wait": (_I, [_P, _U64, _P, _P]),
     "dlite_device_status": (_I, [_P, _I, ctypes.POINTER(_I), _P]),
     "dlite_status_string": (ctypes.c_char_p, [_I]),
     "dlite_last_cuda_error": (ctypes.c_char_p, []),
@@ -186,10 +189,35 @@ def verify_sample_static(cand, qstats, hs, E, probs, temperature, seed, pos, acc
     lib = load()
     B, K = cand.shape
     V, D = E.shape
+    want = ((cand, torch.int32, (B, K)), (qstats, torch.float32, (B, K, 2)), (hs, torch.float32, (B, K, D)),
+            (E, torch.float32, (V, D)), (probs, torch.float32, (B, K + 1, V)), (pos, torch.int64, (B,)),
+            (accepted, torch.int32, (B,)), (commits, torch.int32, (B, K + 1)), (n_commit, torch.int32, (B,)),
+            (next_anchor, torch.int32, (B,)))
+    for t, dt, shape in want:
+        if t.dtype != dt or tuple(t.shape) != shape:
+            raise ValueError(f"verify_sample_static: expected {dt} {shape}, got {t.dtype} {tuple(t.shape)}")
     _check(lib.dlite_verify_sample_static(B, K, V, D, _ptr(cand), _ptr(qstats), _ptr(hs), _ptr(E),
                                           _ptr(probs), temperature, seed, _ptr(pos), _ptr(accepted),
                                           _ptr(commits), _ptr(n_commit), _ptr(next_anchor),
                                           _stream(stream)), "dlite_verify_sample_static")
+
+
+def synthetic_target(cand, accept_c, seed, pos, target_tokens, V, round_counter=None, stream=None):
+    """Synthetic target tokens [B, K+1] (dlite_synthetic_target): accept_c is
+    [n_tables, B, K] float32 on the device, round_counter a device int32 (or None)."""
+    lib = load()
+    B, K = cand.shape
+    if accept_c.dtype != torch.float32 or accept_c.dim() != 3 or tuple(accept_c.shape[1:]) != (B, K):
+        raise ValueError("accept_c must be float32 [n_tables, B, K]")
+    if cand.dtype != torch.int32 or pos.dtype != torch.int64 or target_tokens.dtype != torch.int32:
+        raise ValueError("candidates / target_tokens int32, pos int64 expected")
+    if tuple(target_tokens.shape) != (B, K + 1) or tuple(pos.shape) != (B,):
+        raise ValueError("target_tokens [B, K+1] and pos [B] expected")
+    if round_counter is not None and round_counter.dtype != torch.int32:
+        raise ValueError("round_counter must be a device int32")
+    _check(lib.dlite_synthetic_target(B, K, V, _ptr(cand), _ptr(accept_c), accept_c.shape[0],
+                                      _ptr(round_counter), seed, _ptr(pos), _ptr(target_tokens),
+                                      _stream(stream)), "dlite_synthetic_target")
 
 
 def config_struct(cfg, B_max):
@@ -198,7 +226,8 @@ def config_struct(cfg, B_max):
                   dtype=DLITE_F32 if cfg.dtype == "f32" else DLITE_BF16,
                   rms_eps=cfg.eps, rope_theta=cfg.theta, anchor_group=getattr(cfg, "G", 1),
                   head_type=1 if getattr(cfg, "head", "rnn") == "gated" else 0,
-                  history=getattr(cfg, "history", 0))
+                  history=getattr(cfg, "history", 0), act_planes=getattr(cfg, "act_planes", 1),
+                  head_warmup=getattr(cfg, "warmup", 0))
 
 
 class Drafter:
@@ -347,6 +376,11 @@ class Drafter:
         if n < 0:
             raise DliteError(n, "dlite_stage_times")
         return [(names[i].decode(), times[i]) for i in range(min(n, cap))]
+
+    def selftest_wait(self, limit_ns, result, stream=None):
+        """Bounded-wait probe (dlite_selftest_wait): result is a device int32 [3]."""
+        _check(self.lib.dlite_selftest_wait(self.h, int(limit_ns), _ptr(result), _stream(stream)),
+               "dlite_selftest_wait")
 
     def counters(self, reset=False, stream=None):
         """Sampling-verify counters: residual draws, proposals, fallbacks, bonus draws."""

@@ -37,7 +37,8 @@ struct MapEntry {
 struct dlite_handle {
   dlite_config cfg;
   bool f32 = false;
-  int np = 1;  // planes of weights and backbone activations (2 for fp32 weights)
+  int np = 1;  // planes of the weights (2 for fp32 weights)
+  int xp = 1;  // planes of the backbone activations (2: fp32-class, cfg.act_planes or fp32 weights)
   int qd = 0, kvd = 0;
   int Rp = 0;                       // R padded to a multiple of 64 (GEMM k extent)
   int Lcap = 0, Ccap = 0, Hcap = 0;  // activation row capacities (multiples of 128)
@@ -172,6 +173,11 @@ int check_config(const dlite_config* c) {
   if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return DLITE_ERR_INVALID_ARG;
   if (c->head_type != DLITE_HEAD_RNN && c->head_type != DLITE_HEAD_GATED) return DLITE_ERR_INVALID_ARG;
   if (c->head_type == DLITE_HEAD_GATED && c->R % 64) return DLITE_ERR_UNSUPPORTED_SHAPE;
+  if (c->act_planes < 0 || c->act_planes > 2) return DLITE_ERR_INVALID_ARG;
+  if (c->act_planes == 2 && c->history > 0) return DLITE_ERR_UNSUPPORTED_SHAPE;  // the history kernels are bf16
+  if (c->head_warmup < 0 || c->head_warmup > 1) return DLITE_ERR_INVALID_ARG;
+  if (c->head_warmup && (c->head_type != DLITE_HEAD_GATED || group_of(c) < 2))
+    return DLITE_ERR_UNSUPPORTED_SHAPE;  // the warm-up token is the group's second-to-last
   if (c->history < 0) return DLITE_ERR_INVALID_ARG;
   if (c->history > 0 && (c->dtype != DLITE_BF16 || c->history < group_of(c) + c->K || c->history > (1 << 20) ||
                          (c->n_q / c->n_kv) * (group_of(c) + c->K) > 128))
@@ -379,7 +385,7 @@ tc::Plan lm_plan(dlite_handle* h, int rows) {
 static int ctx_route(const dlite_handle* h, int B) {
   const dlite_config& c = h->cfg;
   const int rows = B * (group_of(&c) + c.K) + B * c.m;
-  if (h->np != 1) return 0;
+  if (h->np != 1 || h->xp != 1) return 0;
   if (tc::use_stream_engine(rows, 1, 1)) return tc::stream_plan(rows, h->qd + 2 * h->kvd, c.D, h->num_sms).ok;
   return tc::plan(rows, h->qd + 2 * h->kvd, c.D, 1, 1, false).ok ? 2 : 0;
 }
@@ -452,11 +458,11 @@ int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anch
   st.eps = c.rms_eps;
   st.z[0] = fused_ctx ? h->y[0] + (size_t)L * c.D : h->z[0];
   st.z[1] = h->z[1];
-  st.nz = h->np;
+  st.nz = h->xp;
   st.x = h->x;
   st.y[0] = h->y[0];
   st.y[1] = h->y[1];
-  st.ny = h->np;
+  st.ny = h->xp;
   st.tap_z = taps ? taps->z : nullptr;
   st.status = h->status;
   CK(launch_stage(st, h->f32, s));
@@ -468,7 +474,7 @@ int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anch
     AttnArgs at;
     if (fused_ctx) {
       const bool skip = ctx_route(h, B) == 2;
-      RUN(gemm(h, "gemm_qkv", opnd(h->y, h->np, h->Lcap + h->Ccap, c.D),
+      RUN(gemm(h, "gemm_qkv", opnd(h->y, h->xp, h->Lcap + h->Ccap, c.D),
                opnd(w.Wqkv, h->np, h->qd + 2 * h->kvd, c.D), L + C, h->qd + 2 * h->kvd, h->part, &S1, s,
                nullptr, 1, nullptr, skip ? L : 0, skip ? h->qd : 0));
       at.part_ctx = h->part;
@@ -480,11 +486,11 @@ int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anch
       at.loc_rows = L + C;
     } else {
       // local rows: y -> [q | k | v]; context rows: z -> [k | v] with the same bytes
-      RUN(gemm(h, "gemm_qkv", opnd(h->y, h->np, h->Lcap, c.D), opnd(w.Wqkv, h->np, h->qd + 2 * h->kvd, c.D),
+      RUN(gemm(h, "gemm_qkv", opnd(h->y, h->xp, h->Lcap, c.D), opnd(w.Wqkv, h->np, h->qd + 2 * h->kvd, c.D),
                L, h->qd + 2 * h->kvd, h->part, &S1, s));
       const bf16* wkv[2] = {w.Wqkv[0] + (size_t)h->qd * c.D,
                             w.Wqkv[1] ? w.Wqkv[1] + (size_t)h->qd * c.D : nullptr};
-      RUN(gemm(h, "gemm_ctx_kv", opnd(h->z, h->np, h->Ccap, c.D), opnd(wkv, h->np, 2 * h->kvd, c.D), C,
+      RUN(gemm(h, "gemm_ctx_kv", opnd(h->z, h->xp, h->Ccap, c.D), opnd(wkv, h->np, 2 * h->kvd, c.D), C,
                2 * h->kvd, h->part2, &S2, s));
       at.part_ctx = h->part2;
       at.sp_ctx = S2;
@@ -502,10 +508,10 @@ int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anch
     at.d_h = c.d_h;
     at.hq = attention_heads_per_cta(c.n_q, c.n_kv, B);
     at.scale = (float)(1.0 / sqrt((double)c.d_h));
-    at.round_bf16 = h->f32 ? 0 : 1;
+    at.round_bf16 = h->xp == 1 ? 1 : 0;
     at.o[0] = h->o[0];
     at.o[1] = h->o[1];
-    at.no = h->np;
+    at.no = h->xp;
     if (h->H) {
       at.hist_q = h->hst_q;
       at.hist_k = h->hk_ring + (size_t)l * h->hrows * c.d_h;
@@ -517,7 +523,7 @@ int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anch
     mark(h, "attention");
     if (h->H) RUN(run_history_attention(h, B, l, s));
     // O projection + residual, then the FFN pre-norm
-    RUN(gemm(h, "gemm_o", opnd(h->o, h->np, h->Lcap, h->qd), opnd(w.Wo, h->np, c.D, h->qd), L, c.D,
+    RUN(gemm(h, "gemm_o", opnd(h->o, h->xp, h->Lcap, h->qd), opnd(w.Wo, h->np, c.D, h->qd), L, c.D,
              h->part, &S1, s));
     ResNormArgs rn;
     rn.part = h->part;
@@ -529,19 +535,19 @@ int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anch
     rn.eps = c.rms_eps;
     rn.y[0] = h->y[0];
     rn.y[1] = h->y[1];
-    rn.ny = h->np;
+    rn.ny = h->xp;
     CK(launch_resnorm(rn, s));
     mark(h, "resnorm");
     // gate/up + SwiGLU
     bool fused = false;
-    RUN(gemm(h, "gemm_gate_up", opnd(h->y, h->np, h->Lcap, c.D), opnd(w.Wgu, h->np, 2 * c.F, c.D), L,
-             2 * c.F, h->part, &S1, s, h->a, h->np, &fused));
+    RUN(gemm(h, "gemm_gate_up", opnd(h->y, h->xp, h->Lcap, c.D), opnd(w.Wgu, h->np, 2 * c.F, c.D), L,
+             2 * c.F, h->part, &S1, s, h->a, h->xp, &fused));
     if (!fused) {
-      CK(launch_swiglu_interleaved(h->part, S1, L, c.F, h->a, h->np, s));
+      CK(launch_swiglu_interleaved(h->part, S1, L, c.F, h->a, h->xp, s));
       mark(h, "swiglu");
     }
     // down + residual, then the next layer's pre-norm (or the final norm)
-    RUN(gemm(h, "gemm_down", opnd(h->a, h->np, h->Lcap, c.F), opnd(w.Wd, h->np, c.D, c.F), L, c.D,
+    RUN(gemm(h, "gemm_down", opnd(h->a, h->xp, h->Lcap, c.F), opnd(w.Wd, h->np, c.D, c.F), L, c.D,
              h->part, &S1, s));
     ResNormArgs r2 = rn;
     r2.sp = S1;
@@ -753,6 +759,15 @@ int run_gated_head(dlite_handle* h, int B, const int32_t* anchor, float temperat
   op.w32 = h->f32 ? h->Wo32 : nullptr;
   op.vec = h->g_rstep;
   op.K_draft = 1;
+  g.warm = c.head_warmup;
+  if (c.head_warmup) {  // s_0: one state update from zero on the token before the anchor, no output
+    CK(launch_gated_prep(g, 0, s));
+    mark(h, "gated_prep");
+    RUN(gemm(h, "gemm_gated_s", opnd(h->g_xp, 2, h->Bcap, 2 * R), opnd(h->Ws, h->np, 2 * R, 2 * R), B, 2 * R,
+             h->part, &S, s));
+    CK(launch_gated_gate(g, h->part, S, s));
+    mark(h, "gated_gate");
+  }
   for (int i = 1; i <= K; ++i) {
     CK(launch_gated_prep(g, i, s));
     mark(h, "gated_prep");
@@ -825,7 +840,7 @@ void dlite_destroy(dlite_handle* h) {
 // keep the analytical planner's choice. bf16 drafters only.
 static int tune_products(dlite_handle* h) {
   const dlite_config& c = h->cfg;
-  if (h->np != 1) return DLITE_OK;
+  if (h->np != 1 || h->xp != 1) return DLITE_OK;
   const int B = c.B_max, L = B * (group_of(&c) + c.K), C = B * c.m, Hr = B * c.K;
   struct Site {
     Operand X, W;
@@ -1023,7 +1038,7 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
   const int Bm = c.B_max;
   const size_t Lr = (size_t)h->Lcap, Cr = (size_t)h->Ccap, Hr = (size_t)h->Hcap;
   AL(h->x, Lr * D);
-  for (int p = 0; p < h->np; ++p) {
+  for (int p = 0; p < h->xp; ++p) {
     AL(h->y[p], (Lr + Cr) * D);  // context rows behind the local rows when fused (fuse_ctx)
     AL(h->z[p], Cr * D);
     AL(h->o[p], Lr * h->qd);
@@ -1041,8 +1056,8 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
   size_t pe = 0, pe2 = 0, lme = 0;
   for (int B = 1; B <= Bm; ++B) {
     const int L = B * (group_of(&c) + c.K), C = B * c.m, H = B * c.K;
-    const int sites[9][4] = {{L, h->qd + 2 * h->kvd, D, h->np}, {L, D, h->qd, h->np},
-                             {L, 2 * F, D, h->np},               {L, D, F, h->np},
+    const int sites[9][4] = {{L, h->qd + 2 * h->kvd, D, h->xp}, {L, D, h->qd, h->xp},
+                             {L, 2 * F, D, h->xp},               {L, D, F, h->xp},
                              {H, 2 * h->Rp, D, 2},               {H, D, h->Rp, 2},
                              // the gated head's products (sized whatever the head type)
                              {H, h->Rp, D, 2},                   {B, 2 * h->Rp, 2 * h->Rp, 2},
@@ -1065,15 +1080,15 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
       const tc::Plan pf = tc::plan(L + C, h->qd + 2 * h->kvd, D, 1, 1, false, false, L, h->qd);
       pe = std::max(pe, (size_t)pf.S * (L + C) * (h->qd + 2 * h->kvd));
     }
-    const tc::Plan pc = tc::plan(C, 2 * h->kvd, D, h->np, h->np, false);
+    const tc::Plan pc = tc::plan(C, 2 * h->kvd, D, h->xp, h->np, false);
     if (!pc.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
     const size_t v2 = (size_t)pc.S * C * 2 * h->kvd;
     pe2 = v2 > pe2 ? v2 : pe2;
     const tc::PairPlan pc2 = tc::pair_plan(C, 2 * h->kvd, D, h->num_sms);
     const tc::StreamPlan sc2 = tc::stream_plan(C, 2 * h->kvd, D, h->num_sms);
-    if (sc2.ok && tc::use_stream_engine(C, h->np, h->np))
+    if (sc2.ok && tc::use_stream_engine(C, h->xp, h->np))
       pe2 = (size_t)sc2.S * C * 2 * h->kvd > pe2 ? (size_t)sc2.S * C * 2 * h->kvd : pe2;
-    if (pc2.ok && tc::use_pair_engine(C, h->np, h->np)) pe2 = (size_t)pc2.S * C * 2 * h->kvd > pe2 ? (size_t)pc2.S * C * 2 * h->kvd : pe2;
+    if (pc2.ok && tc::use_pair_engine(C, h->xp, h->np)) pe2 = (size_t)pc2.S * C * 2 * h->kvd > pe2 ? (size_t)pc2.S * C * 2 * h->kvd : pe2;
     const tc::Plan pl = lm_plan(h, H);
     if (!pl.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
     const size_t v3 = (size_t)((V + pl.N - 1) / pl.N) * tc::kGemmEpiGroups * H;
@@ -1181,6 +1196,7 @@ int dlite_create(const dlite_config* cfg, const dlite_weights* w, dlite_handle**
   h->cfg = *cfg;
   h->f32 = cfg->dtype == DLITE_F32;
   h->np = h->f32 ? 2 : 1;
+  h->xp = (h->f32 || cfg->act_planes == 2) ? 2 : 1;
   h->qd = cfg->n_q * cfg->d_h;
   h->kvd = cfg->n_kv * cfg->d_h;
   h->Rp = (cfg->R + 63) / 64 * 64;
@@ -1630,6 +1646,12 @@ int dlite_history_read(dlite_handle* h, int layer, int request, int which, void*
   return DLITE_OK;
 }
 
+int dlite_selftest_wait(dlite_handle* h, uint64_t limit_ns, int32_t* result, dlite_stream_t stream) {
+  if (!h || !result || limit_ns < 1 || limit_ns > 1000000000ull) return DLITE_ERR_INVALID_ARG;
+  CK(launch_wait_probe(limit_ns, h->status, result, (cudaStream_t)stream));
+  return DLITE_OK;
+}
+
 int dlite_launch_count(dlite_handle* h, int B, float temperature) {
   if (!h || B < 1) return -1;
   (void)temperature;
@@ -1637,12 +1659,13 @@ int dlite_launch_count(dlite_handle* h, int B, float temperature) {
   // engine; the one-CTA engine fuses it), down, resnorm} + head {ce, chain, P, out}
   // + lm {head, merge} + verify
   const int L = B * (group_of(&h->cfg) + h->cfg.K);
-  const bool fused = !tc::use_pair_engine(L, h->np, h->np);
+  const bool fused = !tc::use_pair_engine(L, h->xp, h->np);
   const int per_layer = (fused ? 8 : 9) - (fuse_ctx(h, B) ? 1 : 0);  // one product for [y; z] when fused
   // history-KV control: + {history attention, combine} per layer + the cursor advance
   const int hist = h->H ? 2 * h->cfg.L_D + 1 : 0;
   if (h->gated)  // head: {W_h u product, sum} + K x {prep, state product, gate, r product, r, lm, merge} + final
-    return 1 + per_layer * h->cfg.L_D + hist + 2 + 7 * h->cfg.K + 1 + 1;
+                 // (+ {prep, state product, gate} of the warm-up)
+    return 1 + per_layer * h->cfg.L_D + hist + 2 + 7 * h->cfg.K + 1 + 1 + (h->cfg.head_warmup ? 3 : 0);
   return 1 + per_layer * h->cfg.L_D + hist + 4 + 2 + 1;
 }
 

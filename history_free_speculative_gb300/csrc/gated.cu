@@ -5,7 +5,9 @@
 //   f_i = sigmoid(g_i);  s_i = f_i * s_{i-1} + (1 - f_i) * tanh(c_i),  s_0 = 0;
 //   r_i = W_h [s_i; u_i] + b_h;  l_i = W_o r_i,
 //
-// one step at a time because d_i (chosen from l_i) feeds step i + 1. The two
+// one step at a time because d_i (chosen from l_i) feeds step i + 1. With the
+// warm-up (head_warmup), s_0 is one state update from zero on E_R of the token
+// before the anchor, with no output ([P1] §"官方顺序头具体算了什么"). The two
 // state products and the W_h u part run on the tensor-core GEMM engine, the
 // vocabulary projection on the LM-head kernel (K = R); these kernels do the
 // gather of E_R rows, the gating and the bookkeeping between them.
@@ -34,27 +36,30 @@ __device__ __forceinline__ void planes2(bf16* const* pl, size_t i, float v) {
 // Step i prep, one CTA per request: the previous token (the anchor at i = 1,
 // else the previous step's choice, which is also stored into cand / qs), the
 // step's RNG positions, and the product input [s_{i-1}; E_R[d_{i-1}]] as two
-// bf16 planes (fp32 precision through the tensor cores).
+// bf16 planes (fp32 precision through the tensor cores). i = 0 is the warm-up
+// step: the token before the anchor on the zero state, no bookkeeping.
 __global__ void gated_prep_kernel(GatedArgs a, int i) {
   pdl_trigger();
   pdl_wait();
   const int b = blockIdx.x, R = a.R, K = a.K;
-  int d = i == 1 ? a.anchor[b * a.G + a.G - 1] : a.cand_tmp[b];
+  int d = i == 0 ? a.anchor[b * a.G + a.G - 2] : i == 1 ? a.anchor[b * a.G + a.G - 1] : a.cand_tmp[b];
   if (d < 0 || d >= a.V) {
     if (threadIdx.x == 0) flag_status(a.status, kDevBounds);
     d = 0;
   }
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && i >= 1) {
     if (i > 1) {
       a.cand[b * K + i - 2] = a.cand_tmp[b];
       if (a.qs) a.qs[b * K + i - 2] = a.qs_tmp[b];
     }
     if (a.pos) a.pos_i[b] = a.pos[b] + (i - 1);
   }
+  // the state starts with the block (at the warm-up step when there is one)
+  const bool fresh = i == 0 || (i == 1 && !a.warm);
   for (int j = threadIdx.x; j < R; j += blockDim.x) {
     float s = 0.f;
-    if (i == 1)
-      a.s[(size_t)b * R + j] = 0.f;  // the state starts with the block
+    if (fresh)
+      a.s[(size_t)b * R + j] = 0.f;
     else
       s = a.s[(size_t)b * R + j];
     planes2(a.xp, (size_t)b * 2 * R + j, s);
@@ -132,7 +137,7 @@ cudaError_t launch_gated_sum(const float* part, const Splits& sp, int rows, int 
                              cudaStream_t s) {
   const size_t n = (size_t)rows * cols;
   int blocks = (int)((n + 255) / 256);
-  if (blocks > 152 * 8) blocks = 152 * 8;
+  if (blocks > device_sms() * 8) blocks = device_sms() * 8;
   return launch_pdl(gated_sum_kernel, dim3(blocks), dim3(256), 0, s, part, sp, rows, cols, out);
 }
 cudaError_t launch_gated_final(const GatedArgs& a, cudaStream_t s) {

@@ -374,7 +374,7 @@ long long hist_max_ctas(int num_sms) { return 8LL * num_sms; }
 
 cudaError_t launch_hist_fill(const HistFillArgs& a, cudaStream_t s) {
   const size_t n = 2 * (size_t)a.L * a.Bm * a.n_kv * a.H * a.d_h;
-  const int blocks = (int)std::min<size_t>((n + 255) / 256, 152 * 16);
+  const int blocks = (int)std::min<size_t>((n + 255) / 256, (size_t)device_sms() * 16);
   hist_fill_kernel<<<std::max(blocks, 1), 256, 0, s>>>(a);
   return cudaGetLastError();
 }

@@ -7,9 +7,24 @@
 #include "../../include/dlite.h"
 #include "common.cuh"
 
+#include <atomic>
 #include <utility>
 
 namespace dlite {
+
+// Streaming multiprocessors of the current device, queried once per device
+// (launch shapes and the planners' cost models are sized by it).
+inline int device_sms() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (!n) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+    cache[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
 
 // Launch with programmatic stream serialization (see pdl_trigger / pdl_wait).
 template <typename... KArgs, typename... Args>

@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(1024) stage_kernel(StageArgs a) {
 cudaError_t launch_stage(const StageArgs& a, bool f32, cudaStream_t s) {
   const int rows = a.B * a.m + a.B * (a.G + a.K);
   // few rows: 1024 threads per row; many: 512 (several rows per SM at once)
-  const int threads = rows <= 2 * 152 ? 1024 : 512;
+  const int threads = rows <= 2 * device_sms() ? 1024 : 512;
   if (a.D / 4 > kRowVec * threads) return cudaErrorInvalidValue;
   if (f32) return launch_pdl(stage_kernel<float>, dim3(rows), dim3(threads), 0, s, a);
   return launch_pdl(stage_kernel<bf16>, dim3(rows), dim3(threads), 0, s, a);
@@ -414,7 +414,7 @@ int attention_heads_per_cta(int n_q, int n_kv, int B) {
 cudaError_t launch_attention(const AttnArgs& a, cudaStream_t s) {
   const size_t smem = attention_smem(a.K1 ? a.K1 : a.K + 1, a.m, a.d_h, a.hq);
   const dim3 grid(a.n_q / a.hq, a.B);
-  const bool many = (int)(grid.x * grid.y) > 152;
+  const bool many = (int)(grid.x * grid.y) > device_sms();
   void (*fn)(AttnArgs) = many ? attention_kernel<2, 2> : attention_kernel<4, 1>;
   static bool attr = false;
   if (!attr) {
@@ -503,7 +503,7 @@ constexpr int kResNormCluster = 8;
 
 cudaError_t launch_resnorm(const ResNormArgs& a, cudaStream_t s) {
   // few rows: a cluster per row, so that more SMs pull the split partials
-  const int C = (a.rows * kResNormCluster <= 4 * 152 && (a.D / 4) % kResNormCluster == 0) ? kResNormCluster : 1;
+  const int C = (a.rows * kResNormCluster <= 4 * device_sms() && (a.D / 4) % kResNormCluster == 0) ? kResNormCluster : 1;
   const int n4 = a.D / 4 / C;
   int threads = (n4 + 31) / 32 * 32;
   if (threads > kRowThreads) threads = kRowThreads;
@@ -553,7 +553,7 @@ cudaError_t launch_swiglu_interleaved(const float* part, const Splits& sp, int r
                                       cudaStream_t s) {
   const size_t n4 = (size_t)rows * F / 4;
   int blocks = (int)((n4 + 255) / 256);
-  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks > device_sms() * 16) blocks = device_sms() * 16;
   return launch_pdl(swiglu_kernel, dim3(blocks), dim3(256), 0, s, part, sp, rows, F, o[0], o[1], no);
 }
 
@@ -802,7 +802,7 @@ cudaError_t launch_head_out(const float* part, int S, int rows, int D, const flo
                             bf16* const* hp, float* tap, cudaStream_t s) {
   const size_t n4 = (size_t)rows * D / 4;
   int blocks = (int)((n4 + 255) / 256);
-  if (blocks > 152 * 8) blocks = 152 * 8;
+  if (blocks > device_sms() * 8) blocks = device_sms() * 8;
   return launch_pdl(head_out_kernel, dim3(blocks), dim3(256), 0, s, part, S, rows, D, b, hs, hp[0], hp[1], tap);
 }
 
@@ -820,7 +820,7 @@ __global__ void split_kernel(const float* src, size_t n, bf16* h0, bf16* h1, flo
 
 cudaError_t launch_split(const float* src, size_t n, bf16* const* pl, float* copy, cudaStream_t s) {
   int blocks = (int)((n + 255) / 256);
-  if (blocks > 152 * 8) blocks = 152 * 8;
+  if (blocks > device_sms() * 8) blocks = device_sms() * 8;
   return launch_pdl(split_kernel, dim3(blocks), dim3(256), 0, s, src, n, pl[0], pl[1], copy);
 }
 
@@ -1337,9 +1337,10 @@ static cudaError_t launch_match_c(const VerifyArgs& a, int items, cudaStream_t s
 cudaError_t launch_match_sample(const VerifyArgs& a, cudaStream_t s) {
   const int items = a.B * ((a.kv < 0 ? a.K : a.kv) + 1);  // (request, index) rows to sample
   // the largest cluster that keeps every row in one wave (two CTAs per SM)
-  if (items * 8 <= 2 * 152) return launch_match_c<8>(a, items, s);
-  if (items * 4 <= 2 * 152) return launch_match_c<4>(a, items, s);
-  if (items * 2 <= 2 * 152) return launch_match_c<2>(a, items, s);
+  const int slots = 2 * device_sms();  // two CTAs per SM: every sampled row in one wave
+  if (items * 8 <= slots) return launch_match_c<8>(a, items, s);
+  if (items * 4 <= slots) return launch_match_c<4>(a, items, s);
+  if (items * 2 <= slots) return launch_match_c<2>(a, items, s);
   return launch_match_c<1>(a, items, s);
 }
 
@@ -1406,7 +1407,7 @@ cudaError_t launch_repack(const void* src, bool src_f32, int rows, int cols, int
                           cudaStream_t s) {
   const size_t n = (size_t)rows * cols;
   int blocks = (int)((n + 255) / 256);
-  if (blocks > 152 * 32) blocks = 152 * 32;
+  if (blocks > device_sms() * 32) blocks = device_sms() * 32;
   if (dst_ld == 0) dst_ld = cols;
   if (src_f32)
     repack_kernel<float><<<blocks, 256, 0, s>>>((const float*)src, rows, cols, src_ld, src_off, p0,
@@ -1436,7 +1437,7 @@ cudaError_t launch_repack_gate_up(const void* Wg, const void* Wu, bool src_f32, 
                                   int np, cudaStream_t s) {
   const size_t n = (size_t)2 * F * D;
   int blocks = (int)((n + 255) / 256);
-  if (blocks > 152 * 32) blocks = 152 * 32;
+  if (blocks > device_sms() * 32) blocks = device_sms() * 32;
   if (src_f32)
     repack_gate_up_kernel<float><<<blocks, 256, 0, s>>>((const float*)Wg, (const float*)Wu, F, D, p0, p1, np);
   else

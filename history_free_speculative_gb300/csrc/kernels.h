@@ -127,6 +127,7 @@ struct GatedArgs {
   float* r_step = nullptr;           // [B, R]
   bf16* rp = nullptr;                // [B, R] bf16(r) (the vocabulary product's activation)
   int* status = nullptr;
+  int warm = 0;                      // s_0 from a warm-up step on the token before the anchor
 };
 cudaError_t launch_gated_prep(const GatedArgs& a, int i, cudaStream_t s);
 cudaError_t launch_gated_gate(const GatedArgs& a, const float* part, const Splits& sp, cudaStream_t s);
@@ -154,6 +155,10 @@ cudaError_t launch_verify_sample(const VerifyArgs& a, cudaStream_t s);
 // (step 2 is launch_verify_greedy with a.tgt = a.tsamp)
 cudaError_t launch_match_sample(const VerifyArgs& a, cudaStream_t s);
 cudaError_t launch_advance(int B, const int32_t* n_commit, int64_t* pos, cudaStream_t s);
+// Bounded-wait probe: result[0] / result[1] = 1 when the warp-wide / single-thread wait on a
+// barrier nobody arrives at gave up after limit_ns (flagging the timeout bit in *status);
+// result[2] = 1 when a following kernel sees that bit at entry and skips its work.
+cudaError_t launch_wait_probe(uint64_t limit_ns, int* status, int32_t* result, cudaStream_t s);
 cudaError_t launch_shift_group(int B, int G, int K1, const int32_t* commits, const int32_t* n_commit,
                                int32_t* group, cudaStream_t s);
 cudaError_t launch_repack(const void* src, bool src_f32, int rows, int cols, int src_ld,

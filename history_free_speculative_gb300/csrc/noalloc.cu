@@ -27,6 +27,8 @@ void* g_scratch_addr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device; looked up once
 // per device (host code cannot use the symbol itself as a device pointer).
+// The cached address belongs to the device's context of that first call: it
+// does not survive cudaDeviceReset (the header says so).
 int scratch_for_current_device(unsigned long long** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DLITE_ERR_CUDA;
@@ -54,6 +56,8 @@ extern "C" int dlite_verify_sample_static(int B, int K, int V, int D, const int3
   if (B < 1 || K < 1 || K > 31 || V < 8 || V % 8 || V > 262144 || D < 4 || D % 4)
     return DLITE_ERR_INVALID_ARG;
   if (!(temperature > 0.f) || isinf(temperature)) return DLITE_ERR_INVALID_ARG;
+  // E, hs and the probability rows are read with 16-byte vector loads
+  if (((uintptr_t)E | (uintptr_t)hs | (uintptr_t)target_probs) & 15) return DLITE_ERR_INVALID_ARG;
   if ((size_t)B * (size_t)V > kResidCap) return DLITE_ERR_UNSUPPORTED_SHAPE;  // scratch too small
   unsigned long long* scratch = nullptr;
   const int rc = scratch_for_current_device(&scratch);
@@ -78,7 +82,7 @@ extern "C" int dlite_verify_sample_static(int B, int K, int V, int D, const int3
   v.commits = commits;
   v.n_commit = n_commit;
   v.next_anchor = next_anchor;
-  v.status = nullptr;
+  v.status = nullptr;  // no handle, so no status word: see the header on out-of-range candidates
   if (dlite::launch_verify_sample(v, (cudaStream_t)stream) != cudaSuccess) return DLITE_ERR_CUDA;
   return DLITE_OK;
 }

@@ -39,15 +39,16 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait on phase `parity`; false after kTimeoutNs (status flagged).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status) {
+// Bounded wait on phase `parity`; false after limit_ns (status flagged).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status,
+                                          uint64_t limit_ns = kTimeoutNs) {
   if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = gtimer();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 128; ++i)
       if (mbar_try(bar, parity)) return true;
-    if (gtimer() - t0 > kTimeoutNs) {
+    if (gtimer() - t0 > limit_ns) {
       flag_status(status, kDevTimeout);
       return false;
     }
@@ -55,14 +56,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* st
 }
 // Warp-wide bounded wait: every lane polls, lane 0's view decides, so the
 // result is uniform across the warp.
-__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, int* status) {
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, int* status,
+                                               uint64_t limit_ns = kTimeoutNs) {
   if (__shfl_sync(0xffffffffu, (int)mbar_try(bar, parity), 0)) return true;
   const uint64_t t0 = gtimer();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 64; ++i)
       if (__shfl_sync(0xffffffffu, (int)mbar_try(bar, parity), 0)) return true;
-    const int expired = __shfl_sync(0xffffffffu, (int)(gtimer() - t0 > kTimeoutNs), 0);
+    const int expired = __shfl_sync(0xffffffffu, (int)(gtimer() - t0 > limit_ns), 0);
     if (expired) {
       if ((threadIdx.x & 31) == 0) flag_status(status, kDevTimeout);
       return false;

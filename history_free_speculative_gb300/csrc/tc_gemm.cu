@@ -357,7 +357,8 @@ Plan plan(int rows, int outs, int K, int xplanes, int wplanes, bool lm, bool one
   best.ok = false;
   const int kblocks = K / 64;
   const int mt_total = (rows + 127) / 128;
-  const double bw_total = 6.5e12, l2_total = 1.6e13, mma_sm = 1.8e15 / kNumSMs;
+  const int n_sms = device_sms();
+  const double bw_total = 6.5e12, l2_total = 1.6e13, mma_sm = 1.8e15 / n_sms;
   double best_t = 1e30;
   const int combos = 1 + (xplanes == 2) + (wplanes == 2);
   const int nmax_out = ((outs + 63) / 64) * 64;  // tiled weights: rows padded to 64
@@ -380,8 +381,8 @@ Plan plan(int rows, int outs, int K, int xplanes, int wplanes, bool lm, bool one
         long units = 0;  // CTAs with work (tiles past skip_row0 x before skip_cols are skipped)
         for (int g = 0; g < groups; ++g)
           units += (long)Se * (skip_row0 > 0 && g * n_mt * 128 >= skip_row0 ? slabs - skip_cols / N : slabs);
-        const long waves = (units + kNumSMs - 1) / kNumSMs;
-        const double active = units < kNumSMs ? (double)units : (double)kNumSMs;
+        const long waves = (units + n_sms - 1) / n_sms;
+        const double active = units < n_sms ? (double)units : (double)n_sms;
         double bw_sm = bw_total / active;
         if (bw_sm > 1.2e11) bw_sm = 1.2e11;
         double l2_sm = l2_total / active;  // activation tiles come from L2, shared by all CTAs

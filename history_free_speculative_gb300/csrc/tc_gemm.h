@@ -15,7 +15,6 @@ constexpr int kThreads = 64 + 128 * kEpiGroups;  // TMA warp, MMA warp, epilogue
 // the one-CTA engine: four epilogue groups (its epilogue is on the critical path)
 constexpr int kGemmEpiGroups = 4;
 constexpr int kGemmThreads = 64 + 128 * kGemmEpiGroups;
-constexpr int kNumSMs = 152;
 constexpr size_t kSmemBudget = 226 * 1024;  // dynamic shared memory per CTA (all of it)
 constexpr size_t kTailPad = 16 * 1024;      // overhang room for a 128-row operand read
 

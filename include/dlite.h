@@ -89,6 +89,19 @@ typedef struct {
                        * (cursor + j) mod H and advances the slot's cursor by G + K. A 512-row
                        * ring is the sliding-window variant. Requires DLITE_BF16,
                        * G + K <= H <= 2^20 and (n_q / n_kv) (G + K) <= 128 */
+    int act_planes;   /* precision of the backbone activations of a DLITE_BF16 drafter:
+                       * 0 or 1 = bf16 (the fast form: z, y, q, k, v, o and the SwiGLU output
+                       * are stored as bf16); 2 = fp32-class, each stored as two bf16 planes
+                       * hi + lo (about 16 significant bits) and multiplied as two products, so
+                       * that with bf16 weights and fp32 accumulation the round follows float64
+                       * arithmetic on the same weights to ~1e-5 (about twice the tensor work
+                       * and activation traffic of the backbone products; not with history > 0).
+                       * DLITE_F32 drafters always keep fp32-class activations. */
+    int head_warmup;  /* DLITE_HEAD_GATED with anchor_group >= 2 only: 1 = warm the head's state up
+                       * on the token before the anchor ([P1] §"官方顺序头具体算了什么": when the
+                       * configuration allows, one token before the anchor gives a fixed-length
+                       * warm-up): s_0 is one state update from the zero state on E_R of the
+                       * group's second-to-last token, with no output; 0 = s_0 = 0 */
 } dlite_config;
 
 enum dlite_head_type { DLITE_HEAD_RNN = 0, DLITE_HEAD_GATED = 1 };
@@ -270,9 +283,15 @@ int dlite_verify_ex(dlite_handle *h, const dlite_verify_args *args, dlite_stream
  * 2^20 fixed-point entries (8 MiB) that every GPU loading the library holds
  * until exit; B * V above 2^20 is rejected with DLITE_ERR_UNSUPPORTED_SHAPE.
  * The first call on a device looks up that array's device address (no
- * allocation); make that first call before any stream capture. All calls
- * share the array, which keeps the last call's contents (each call rewrites
- * what it reads), so calls that overlap on the GPU race. */
+ * allocation); make that first call before any stream capture. The address
+ * is cached per device for the life of the process: after cudaDeviceReset on
+ * a device this call must not be used there again. All calls share the array,
+ * which keeps the last call's contents (each call rewrites what it reads), so
+ * calls that overlap on the GPU race.
+ * E, hs and target_probs must be 16-byte aligned (INVALID_ARG otherwise).
+ * Without a handle there is no device status word: a candidate id outside
+ * [0, V) is not reported (it is scored as id 0 and committed unchanged), so
+ * callers pass candidates from a draft of the same vocabulary. */
 int dlite_verify_sample_static(int B, int K, int V, int D, const int32_t *candidates,
                                const dlite_qstats *qstats, const float *hs, const float *E,
                                const float *target_probs, float temperature, uint64_t seed,
@@ -322,6 +341,43 @@ int dlite_round_host(dlite_handle *h, int B, const void *hidden_host, const int3
                      const float *target_probs_host, float temperature, uint64_t seed,
                      int32_t *accepted_host, int32_t *commits_host, int32_t *n_commit_host,
                      int32_t *next_anchor_host, dlite_stream_t stream);
+
+/* Synthetic target tokens for timing whole rounds with a realistic acceptance.
+ * This library holds the drafter and the verification rule, not the target
+ * model; this call stands in for the target's greedy choices in the
+ * acceptance workloads (it is not a step of the method). The acceptance model
+ * is the per-position conditional acceptance c_i whose products give the
+ * prefix survival P(A >= k) = prod c_i ([P1] §"分布重叠怎样影响平均推进量"):
+ *   target_tokens[b, j], j < K: = candidates[b, j] with probability c_j, else a
+ *                               uniform id different from it;
+ *   target_tokens[b, K]:        a uniform id (the bonus position).
+ * Draws: the words (w0, w1, w2, w3) of Philox4x32-10(counter = (0, pos[b] + j + 1
+ * (low 32 bits), b, 7), key = (seed & 0xffffffff, seed >> 32)); agreement iff
+ * ((w0 >> 9) + 1/2) 2^-23 < c_j; a disagreeing id is (d + 1 + floor(w1 (V-1) / 2^32))
+ * mod V, the bonus id floor(w1 V / 2^32).
+ *   accept_c [n_tables, B, K] float32  c per table, request and index; the call uses
+ *                                      table (*round_counter mod n_tables) and then
+ *                                      increments *round_counter (device int32; NULL:
+ *                                      table 0, nothing incremented)
+ *   candidates [B, K], pos [B] int64, target_tokens [B, K+1] int32 (out), device pointers.
+ * Out-of-range candidates are read as id 0. One single-CTA launch, stream-ordered,
+ * allocation-free. Errors: INVALID_ARG (NULL, B < 1, K outside 1..31, V < 2,
+ * n_tables < 1), CUDA. */
+int dlite_synthetic_target(int B, int K, int V, const int32_t *candidates, const float *accept_c,
+                           int n_tables, int32_t *round_counter, uint64_t seed, const int64_t *pos,
+                           int32_t *target_tokens, dlite_stream_t stream);
+
+/* Failure-detection probe of the bounded device waits (no fault is involved).
+ * Enqueues one kernel that waits on an mbarrier no thread arrives at, through
+ * the same bounded-wait helpers the tensor-core kernels use, with the limit
+ * limit_ns (1 ns .. 1 s) in place of their 2 s; each wait gives up, sets
+ * DLITE_DEV_TIMEOUT in the handle's status word and returns. Then one kernel
+ * makes the engines' entry check of that word. result [3] device int32 (out):
+ * [0] = 1 if the warp-wide wait gave up, [1] = 1 if the single-thread wait gave
+ * up, [2] = 1 if the second kernel saw the flag and would skip its work.
+ * Afterwards dlite_device_status returns DLITE_ERR_DEVICE_TIMEOUT (and clears
+ * the flag if asked). Errors: INVALID_ARG, CUDA. */
+int dlite_selftest_wait(dlite_handle *h, uint64_t limit_ns, int32_t *result, dlite_stream_t stream);
 
 /* Read (and with clear != 0, reset) the sticky device status word.
  * Synchronises `stream`. *status_out gets DLITE_DEV_* bits. Returns

@@ -74,6 +74,8 @@ def test_host_side_validation_needs_no_gpu(so):
     ("anchor_group", 9, -2),        # local token group longer than 8
     ("head_type", 2, -1),           # no such head
     ("R", 96, -2),                  # gated head: R must be a multiple of 64 (with head_type 1 below)
+    ("act_planes", 3, -1),          # activation planes: 1 (bf16) or 2 (fp32-class)
+    ("act_planes", -1, -1),
 ])
 def test_config_checks_need_no_gpu(so, field, value, code):
     """The history, group and head fields of dlite_config are checked before any CUDA call."""
@@ -104,6 +106,8 @@ def test_history_needs_bf16_and_few_query_rows(so):
     assert lib.dlite_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == -2   # fp32 drafter
     cfg.dtype = 1
     cfg.n_q, cfg.n_kv, cfg.K = 32, 1, 7   # 32 heads x 8 rows = 256 query rows per KV head
+    assert lib.dlite_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == -2
+    cfg.n_q, cfg.n_kv, cfg.K, cfg.act_planes = 4, 2, 4, 2   # the history kernels keep bf16 activations
     assert lib.dlite_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == -2
     assert lib.dlite_history_reset(None, None) == -1
     assert lib.dlite_history_read(None, 0, 0, 0, None, None, None) == -1

@@ -542,6 +542,53 @@ def test_gated_head_round_parity(name, T):
         dr.close()
 
 
+@pytest.mark.parametrize("name", ["tiny", "bf16"])
+@pytest.mark.parametrize("T", [0.0, 0.7])
+def test_gated_head_warmup_round_parity(name, T):
+    """The gated head with its state warmed up on the token before the anchor
+    (local group of 3 tokens): head vectors and candidates against the oracle;
+    and the warm-up changes the head's first vector (it is not a no-op)."""
+    G = 3
+    if name == "tiny":
+        cfg = wk.shrink(wk.TINY, R=64, head="gated", G=G, warmup=1)
+        W = wk.make_weights(cfg, 35, gain_jitter=True)
+        tol = 1e-4
+    else:
+        cfg = wk.shrink(wk.QWEN3_8B, D=512, F=1024, L_D=2, n_q=4, n_kv=2, R=128, V=4096, m=6, head="gated", G=G,
+                        warmup=1)
+        W = wk.make_weights(cfg, 36)
+        tol = HIDDEN_REL_TOL
+    # a state that matters: larger token embeddings and state weights (powers of two: exact in bf16)
+    W = dict(W, E_R=W["E_R"] * 64, W_s=W["W_s"] * 16)
+    B, seed = 12, 79
+    dr = _drafter(cfg, W, B_max=B)
+    try:
+        hidden, _, pos = wk.make_round_inputs(wk.WORKLOADS["tiny"], B=B, cfg=cfg)
+        group = torch.randint(0, cfg.V, (B, G), generator=torch.Generator().manual_seed(5), dtype=torch.int32)
+        out = dr.new_outputs(B, DEV)
+        rv = torch.empty(B, cfg.K, cfg.R, device=DEV)
+        dr.draft_round(hidden.to(DEV), group.to(DEV), T, seed, pos.to(DEV), out["cand"], out["qstats"],
+                       taps={"z": None, "x": None, "b": None, "hs": rv})
+        torch.cuda.synchronize()
+        cand, rvec = out["cand"].cpu().numpy(), rv.cpu().numpy()
+        cands, ocands, gaps = [], [], []
+        for b in range(B):
+            r = O.draft_request(hidden[b], group[b].tolist(), W, cfg, temperature=T, seed=seed, pos=int(pos[b]),
+                                request=b, mirror=(cfg.dtype == "bf16"))
+            k = cfg.K if np.array_equal(cand[b], r["cand"]) else int(np.argmax(cand[b] != r["cand"])) + 1
+            assert rel_err(rvec[b, :k], r["h"][:k]) < tol, b
+            cold = O.gated_head(O.backbone(hidden[b], group[b].tolist(), W, cfg, mirror=(cfg.dtype == "bf16")),
+                                int(group[b, -1]), W, T, seed, int(pos[b]), b)
+            e_warm, e_cold = rel_err(rvec[b, :1], r["h"][:1]), rel_err(rvec[b, :1], cold["r"][:1])
+            assert e_warm < e_cold / 4, (b, e_warm, e_cold)   # the GPU's s_0 is the warmed-up one
+            cands.append(cand[b])
+            ocands.append(r["cand"])
+            gaps.append(r["gap"])
+        check_candidates(np.stack(cands), np.stack(ocands), np.stack(gaps))
+    finally:
+        dr.close()
+
+
 def test_gated_head_sampling_verification():
     """Sampling verification with the gated head: q(v) from W_o and the head's
     r vectors kept by the handle; bit-exact against the oracle on identical inputs."""
@@ -838,26 +885,29 @@ def test_full_size_history_round_sampled_requests():
 
 def test_history_ring_memory_matches_draft_kv_formula():
     """The control's device memory grows by the draft-KV formula 2 L_D H n_kv d_h b
-    per request slot (DLite 完全拆解, §"本轮临时 K/V 仍然需要计算", eq. M_draftKV), plus a
-    fixed workspace (the block rows behind each ring, staged queries and chunk
-    partials bounded by 8 CTAs per SM) that does not grow with H."""
-    H, Bm = 65536, 4
-    cfg = _history_cfg("d128", H)
-    cfg0 = _history_cfg("d128", 0)
-    W = wk.make_weights(cfg, 43)
+    per request slot (DLite 完全拆解, §"本轮临时 K/V 仍然需要计算", eq. M_draftKV).
+    Two ring sizes: the difference of what their handles hold equals the
+    formula's difference up to the rounding of the two ring allocations (2 MiB
+    each), so the rest of the control's workspace (block rows behind each ring,
+    staged queries, chunk partials) does not grow with H; and the larger ring's
+    handle holds at least the formula more than the history-free handle."""
+    H1, H2, Bm = 32768, 65536, 4
+    cfg0, cfg1, cfg2 = (_history_cfg("d128", H) for H in (0, H1, H2))
+    W = wk.make_weights(cfg2, 43)
     Wd = wk.weights_to(W, DEV)
-    torch.cuda.synchronize()
-    free0 = torch.cuda.mem_get_info()[0]
-    d0 = binding.Drafter(cfg0, Wd, B_max=Bm)
-    torch.cuda.synchronize()
-    free1 = torch.cuda.mem_get_info()[0]
-    d1 = binding.Drafter(cfg, Wd, B_max=Bm)
-    torch.cuda.synchronize()
-    free2 = torch.cuda.mem_get_info()[0]
+    held = []
+    drs = []
     try:
-        extra = (free1 - free2) - (free0 - free1)
-        formula = 2 * cfg.L_D * H * cfg.n_kv * cfg.d_h * 2 * Bm
-        assert formula <= extra <= formula + (96 << 20), (extra, formula)
+        for cfg in (cfg0, cfg1, cfg2):
+            torch.cuda.synchronize()
+            f0 = torch.cuda.mem_get_info()[0]
+            drs.append(binding.Drafter(cfg, Wd, B_max=Bm))
+            torch.cuda.synchronize()
+            held.append(f0 - torch.cuda.mem_get_info()[0])
+        formula = lambda H: 2 * cfg2.L_D * H * cfg2.n_kv * cfg2.d_h * 2 * Bm
+        step = held[2] - held[1]
+        assert abs(step - (formula(H2) - formula(H1))) <= (4 << 20), (step, formula(H2) - formula(H1))
+        assert held[2] - held[0] >= formula(H2), (held, formula(H2))
     finally:
-        d0.close()
-        d1.close()
+        for d in drs:
+            d.close()

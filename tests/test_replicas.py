@@ -64,3 +64,14 @@ def test_single_process_reduction_is_identity():
     import bench
     assert bench.reduce_over_ranks(0.25, 7, "cpu") == (0.25, 7)
     assert bench.shard_round_index(3, 0) == 3 and bench.shard_round_index(3, 1) != 3
+
+
+def test_bench_rejects_gpus_that_disagree_with_the_launcher():
+    """Under a launcher the rank count is WORLD_SIZE; a --gpus that disagrees is an error
+    (without a launcher, --gpus N > 1 starts N ranks itself)."""
+    import subprocess
+    import sys
+    env = dict(os.environ, WORLD_SIZE="2", RANK="0", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "4", "--steps", "1"],
+                       env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0 and "WORLD_SIZE is 2" in r.stderr
