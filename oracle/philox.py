@@ -29,6 +29,7 @@ TAG_RESID = 3
 TAG_BONUS = 4
 TAG_MATCH = 5   # the target's own sample at each position (match verification)
 TAG_HIST = 6    # synthetic history K/V of the history-KV control
+TAG_TARGET = 7  # synthetic target tokens of the acceptance workloads
 HIST_SEED = 0x4849535400000001   # fixed key of the synthetic history
 
 _MASK = np.uint64(0xFFFFFFFF)
@@ -76,6 +77,13 @@ def draw(seed, c0, position, request, tag, word):
     w = np.asarray(word)
     sel = np.choose(w, out) if w.ndim else out[int(w)]
     return uniform_open(sel)
+
+
+def words(seed, c0, position, request, tag):
+    """The four raw 32-bit words of Philox(counter=(c0, pos, req, tag), key=seed)."""
+    k0, k1 = seed_key(seed)
+    return philox4x32_10(c0, np.asarray(position, dtype=np.int64).astype(np.uint64) & _MASK,
+                         request, tag, k0, k1)
 
 
 def gumbel_row(seed, position, request, V):
