@@ -33,8 +33,9 @@ Readings where the pages are silent (each is restated beside the code):
         h_i = b_i + P tanh(Q^T [b_i; h_{i-1}]),  i = 1..K,
     followed by ONE vocabulary projection l_i = E h_i.
   * Argmax ties go to the lowest token id.
-  * Sampling draws d_i by Gumbel-max on l_i/T with Philox noise; the draft
-    distribution is q_i = softmax(l_i / T).
+  * Sampling draws d_i from q_i = softmax(l_i / T) in two levels (sample_logits):
+    Gumbel-max over chunks of 16 ids on their log-mass, then the inverse CDF
+    inside the chosen chunk, all noise from Philox.
 """
 import numpy as np
 
@@ -277,16 +278,53 @@ def sequential_head(b, Q, P):
     return out
 
 
-def _pick(ell_i, temperature, seed, position, request):
-    """d from one row of logits: argmax (T = 0) or Gumbel-max on l/T with the
-    Philox noise of (position, request); returns (d, gap, lse)."""
+CHUNK = 16   # vocabulary ids per chunk of the two-level draw
+
+
+def sample_logits(ell_i, temperature, seed, position, request):
+    """The draft's choice from one row of logits l over V ids; returns (d, gap, lse).
+
+    T = 0: d = argmax l (lowest id on ties); gap = the top-2 logit gap.
+    T > 0: an exact draw from q = softmax(l / T) ([P1] §"官方顺序头具体算了什么":
+    q_i from the temperature-scaled softmax of the logits, d_i drawn from it),
+    in two levels:
+      1. chunks of CHUNK consecutive ids, chunk k = ids [16k, 16k + 16) within V,
+         with log-mass L_k = log sum_{v in k} exp(l_v / T); Gumbel-max over the
+         chunks: k* = argmax_k L_k + g_k (lowest k on ties), with
+         g_k = -log(-log u_k), u_k from word k & 3 of Philox(k >> 2, position,
+         request, TAG_GUMBEL); so P(k* = k) = exp(L_k) / sum_j exp(L_j);
+      2. inside chunk k*: the inverse CDF of exp(l_v / T - L_k*) at u' from word
+         0 of Philox(k*, position, request, TAG_PICK).
+    P(d = v) = exp(l_v / T) / sum_w exp(l_w / T). gap = the smaller of the top-2
+    gap of the chunk scores and the distance of u' from the nearest CDF step
+    of the chosen chunk (how close the draw was to going another way).
+    lse = log sum_v exp(l_v / T).
+    """
+    ell_i = f64(ell_i)
     if temperature == 0.0:
         d = int(np.argmax(ell_i))
         return d, float(_top2_gap(ell_i[None, :])[0]), float("nan")
-    s = ell_i / temperature + _ph.gumbel_row(seed, position, request, ell_i.shape[0])
-    m = float((ell_i / temperature).max())
-    lse = m + float(np.log(np.exp(ell_i / temperature - m).sum()))
-    return int(np.argmax(s)), float(_top2_gap(s[None, :])[0]), lse
+    V = ell_i.shape[0]
+    z = ell_i / temperature
+    m = float(z.max())
+    lse = m + float(np.log(np.exp(z - m).sum()))
+    n_chunks = (V + CHUNK - 1) // CHUNK
+    L = np.array([np.log(np.exp(z[k * CHUNK:(k + 1) * CHUNK] - m).sum()) + m for k in range(n_chunks)])
+    score = L + _ph.gumbel_row(seed, position, request, n_chunks)
+    k = int(np.argmax(score))
+    gap = float(_top2_gap(score[None, :])[0]) if n_chunks > 1 else float("inf")
+    u = float(_ph.draw(seed, k, position, request, _ph.TAG_PICK, 0))
+    zc = z[k * CHUNK:(k + 1) * CHUNK]
+    w = np.exp(zc - zc.max())
+    j = inverse_cdf(w, u)
+    c = np.cumsum(w) / w.sum()
+    edges = [c[j]] + ([c[j - 1]] if j > 0 else [])
+    gap = min(gap, min(abs(u - e) for e in edges))
+    return k * CHUNK + j, gap, lse
+
+
+def _pick(ell_i, temperature, seed, position, request):
+    return sample_logits(ell_i, temperature, seed, position, request)
 
 
 def gated_state_step(s_prev, token, W):
@@ -309,7 +347,7 @@ def gated_head(b, anchor_token, W, temperature=0.0, seed=0, pos=0, request=0, wa
               with the block);
         r_i = W_h [s_i; u_i] + b_h;   l_i = W_o r_i,
     and d_i is drawn from l_i like the main head's candidates (argmax, or
-    Gumbel-max on l_i / T at position pos + i) before step i + 1 reads it.
+    the two-level draw of sample_logits at position pos + i) before step i + 1 reads it.
     g is the first R outputs of W_s, c the last R; W_h acts on [s; u].
     Warm-up (the same passage: when the configuration allows, the one token
     before the anchor warms the state up for a fixed length): with warm_token,
@@ -371,9 +409,8 @@ def draft_request(hidden, anchor, W, cfg, temperature=0.0, seed=0, pos=0, reques
     """One request's draft: candidates d_1..d_K plus what verification needs.
 
     Greedy (T = 0): d_i = argmax_v l_iv (lowest id on ties).
-    Sampling (T > 0): d_i = argmax_v (l_iv / T + G_iv), G Gumbel noise from
-    Philox(c0 = v >> 2, position = pos + i, request, TAG_GUMBEL), word v & 3.
-    That is an exact draw from q_i = softmax(l_i / T) ([P1] §"从 logits 经过
+    Sampling (T > 0): d_i is the two-level draw of sample_logits at position
+    pos + i, an exact draw from q_i = softmax(l_i / T) ([P1] §"从 logits 经过
     温度缩放和 softmax,得到草稿分布 q_i").
     Returns dict(cand, logit_d, lse, gap, b, h).
     """
@@ -400,14 +437,11 @@ def draft_request(hidden, anchor, W, cfg, temperature=0.0, seed=0, pos=0, reques
         logit_d = ell[np.arange(K), cand]
         lse = np.full(K, np.nan)
     else:
-        s = np.empty_like(ell)
-        for i in range(K):
-            s[i] = ell[i] / temperature + _ph.gumbel_row(seed, pos + i + 1, request, ell.shape[1])
-        cand = np.argmax(s, axis=1)
-        gap = _top2_gap(s)
+        picks = [sample_logits(ell[i], temperature, seed, pos + i + 1, request) for i in range(K)]
+        cand = np.array([p[0] for p in picks])
+        gap = np.array([p[1] for p in picks])
         logit_d = ell[np.arange(K), cand]
-        m = (ell / temperature).max(axis=1)
-        lse = m + np.log(np.exp(ell / temperature - m[:, None]).sum(axis=1))
+        lse = np.array([p[2] for p in picks])
     if taps is not None:
         taps["b"] = b
         taps["h"] = h

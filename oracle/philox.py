@@ -30,6 +30,7 @@ TAG_BONUS = 4
 TAG_MATCH = 5   # the target's own sample at each position (match verification)
 TAG_HIST = 6    # synthetic history K/V of the history-KV control
 TAG_TARGET = 7  # synthetic target tokens of the acceptance workloads
+TAG_PICK = 8    # the draw inside the chosen vocabulary chunk (two-level sampling)
 HIST_SEED = 0x4849535400000001   # fixed key of the synthetic history
 
 _MASK = np.uint64(0xFFFFFFFF)

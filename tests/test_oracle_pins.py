@@ -60,6 +60,53 @@ def test_gumbel_max_matches_softmax():
     assert chi2 < 30.0          # 7 dof; P(chi2 > 30) ~ 1e-4
 
 
+def test_two_level_draw_matches_softmax():
+    """The draft's sampling draw (chunk Gumbel-max on the chunks' log-mass, then
+    the inverse CDF inside the chosen chunk) follows softmax(l / T): chi-square
+    over 40 ids (chunks of 16, 16 and a partial 8)."""
+    rng = np.random.default_rng(1)
+    V, T, N = 40, 0.7, 40000
+    ell = rng.normal(0, 1.0, V)
+    counts = np.zeros(V)
+    for n in range(N):
+        counts[O.sample_logits(ell, T, 77, n, 3)[0]] += 1
+    p = np.exp(ell / T - ell.max() / T)
+    p /= p.sum()
+    chi2 = ((counts - N * p) ** 2 / (N * p)).sum()
+    assert chi2 < 92.0          # 39 dof: mean 39, sd 8.8; P(chi2 > 92) < 1e-6
+
+
+def test_two_level_draw_single_chunk_is_the_inverse_cdf():
+    """With V <= 16 there is one chunk: the draw is the inverse CDF of
+    softmax(l / T) at word 0 of Philox(0, position, request, TAG_PICK)."""
+    rng = np.random.default_rng(2)
+    ell = rng.normal(0, 1.0, 12)
+    q = np.exp(ell / 0.7 - ell.max() / 0.7)
+    q /= q.sum()
+    for pos in range(200):
+        u = float(ph.draw(5, 0, pos, 4, ph.TAG_PICK, 0))
+        want = int(np.searchsorted(np.cumsum(q), u, side="right"))
+        assert O.sample_logits(ell, 0.7, 5, pos, 4)[0] == want
+
+
+def test_two_level_draw_follows_the_chunk_mass():
+    """All mass in chunk 2 (ids 32..47): every draw lands there, with the
+    within-chunk frequencies of softmax; T = 0 is the plain argmax."""
+    rng = np.random.default_rng(3)
+    ell = np.full(64, -1e3)
+    ell[32:48] = rng.normal(0, 1.0, 16)
+    counts = np.zeros(64)
+    N = 8000
+    for n in range(N):
+        counts[O.sample_logits(ell, 0.7, 9, n, 0)[0]] += 1
+    assert counts[:32].sum() == 0 and counts[48:].sum() == 0
+    p = np.exp(ell[32:48] / 0.7 - ell[32:48].max() / 0.7)
+    p /= p.sum()
+    chi2 = ((counts[32:48] - N * p) ** 2 / (N * p)).sum()
+    assert chi2 < 60.0          # 15 dof
+    assert O.sample_logits(ell, 0.0, 9, 0, 0)[0] == 32 + int(np.argmax(ell[32:48]))
+
+
 def test_draws_are_keyed_by_seed_request_position_tag():
     base = ph.draw(5, 0, 10, 2, ph.TAG_ACCEPT, 0)
     for args in [(6, 0, 10, 2, ph.TAG_ACCEPT), (5, 1, 10, 2, ph.TAG_ACCEPT),
@@ -591,8 +638,7 @@ def test_speculative_sampling_preserves_target(case):
     accepted = 0
     hows = {}
     for n in range(N):
-        s = ell / T + ph.gumbel_row(21, n + 1, 0, V)
-        d = int(np.argmax(s))
+        d = O.sample_logits(ell, T, 21, n + 1, 0)[0]
         pp = np.stack([p, np.full(V, 1.0 / V)])          # K = 1: row 0 verifies, row 1 bonus
         r = O.verify_sample([d], [ell[d]], [lse], h[None, :], E, pp, T, 21, n, 0)
         if r["A"] == 1:
@@ -603,8 +649,14 @@ def test_speculative_sampling_preserves_target(case):
         hows[r["how"]] = hows.get(r["how"], 0) + 1
     beta = np.minimum(p, q).sum()
     assert abs(accepted / N - beta) < 5 * math.sqrt(beta * (1 - beta) / N)
-    chi2 = ((counts - N * p) ** 2 / (N * p)).sum()
-    assert chi2 < 35.0                                    # 5 dof
+    # chi-square with every bin's expected count >= 5: the rarest ids pooled, smallest first
+    order = np.argsort(p)
+    n_pool = int(np.searchsorted(np.cumsum(N * p[order]), 5.0)) + 1
+    pool, rest = order[:n_pool], order[n_pool:]
+    obs = np.append(counts[rest], counts[pool].sum())
+    exp_ = np.append(N * p[rest], N * p[pool].sum())
+    chi2 = ((obs - exp_) ** 2 / exp_).sum()
+    assert chi2 < 35.0                                    # <= 5 dof; P(chi2 > 35) ~ 1e-6
     if case == "overlapping":
         assert hows.get("fallback", 0) > 0
 
