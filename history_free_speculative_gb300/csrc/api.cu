@@ -608,7 +608,7 @@ int run_seq_head(dlite_handle* h, int B, float* tap_hs, cudaStream_t s) {
 // rows of the bf16 activation x [x_cap rows, Kd] (tiled weight w [Vp, Kd]);
 // records, then the merge re-scores the finalists with the fp32 vectors vec
 // [rows, Kd] against the weight (bf16 tiled w, or w32 fp32 row-major) and
-// writes cand / qs per row. Row r draws its Gumbel noise at position
+// writes cand / qs per row. Row r draws its noise at position
 // pos[r / K_draft] + r % K_draft + 1.
 struct LmOperands {
   const bf16* x;

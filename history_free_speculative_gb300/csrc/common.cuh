@@ -56,6 +56,8 @@ constexpr uint32_t kTagGumbel = 1;
 constexpr uint32_t kTagAccept = 2;
 constexpr uint32_t kTagResid = 3;
 constexpr uint32_t kTagBonus = 4;
+constexpr uint32_t kTagPick = 8;  // the draw inside the chosen vocabulary chunk
+constexpr int kChunk = 16;        // vocabulary ids per chunk of the two-level draft draw
 constexpr int kProposals = 32;
 
 __device__ __forceinline__ uint4 philox(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,

@@ -74,9 +74,10 @@ inline Splits uniform_splits(int S) {
 }
 
 // LM-head record of a set of vocabulary columns for one row: the 4 best
-// (score, id) in descending order (greedy: logit; sampling: the base-2
-// Gumbel-max score logit log2(e)/T - log2(-log2 u)), from the bf16 product,
-// and the LSE partials of those columns in base 2.
+// (score, id) in descending order (greedy: logit and vocabulary id; sampling:
+// the base-2 chunk score log2(sum 2^(logit log2(e) / T)) - log2(-log2 u_k) and
+// the 16-id chunk k), from the bf16 product, and the LSE partials of those
+// columns in base 2.
 constexpr int kTopK = 4;
 struct LmRec {
   float sc[kTopK];

@@ -1,5 +1,6 @@
-// Persistent LM-head kernel: logits = h E^T with the argmax / Gumbel-max
-// selection and the log-sum-exp folded in; logits never reach memory.
+// Persistent LM-head kernel: logits = h E^T with the argmax / the first level
+// of the two-level draw (chunk Gumbel-max) and the log-sum-exp folded in;
+// logits never reach memory.
 //
 // Up to 128 rows of h: one CTA per SM walks the vocabulary slabs blockIdx.x,
 // blockIdx.x + grid, ... (N = 256 ids each) with one M = 128 MMA per 16-wide k

@@ -1,26 +1,32 @@
 // LM-head merge and exact re-scoring.
 //
-// The tensor-core pass scores every vocabulary id with the bf16 rounding of
-// the head state h and keeps, per row and vocabulary slab, the 4 best
-// (score, id) plus the slab's log-sum-exp partials. This kernel merges those
-// lists over all slabs in a fixed order (ties -> lowest id), then recomputes
-// the logits of the 4 finalists exactly (fp32 h against the stored weights,
-// fp32 accumulation) and decides among them. The bf16 rounding of h moves a
-// logit by ~1e-3 (D = 4096, weights ~N(0, 0.02^2)), far less than the usual
-// gap between the first and the fifth best score, so the re-scored winner is
-// the winner of the exact product; rows where the fourth finalist is within
-// kCloseCall of the first are counted as close calls.
-//
-// Sampling records are in base-2 units (score = logit log2(e) / T minus
-// log2(-log2 u), an increasing map of the Gumbel-max score; LSE partials
-// m = max logit log2(e) / T, s = sum 2^(. - m)); the finalists are re-scored
-// in natural units, logit / T - log(-log u), and the LSE is returned in
-// natural units.
+// The tensor-core pass scores the vocabulary with the bf16 rounding of the
+// head state h and keeps, per row and vocabulary walk, the 4 best
+// (score, id) plus the log-sum-exp partials. This kernel merges those lists
+// over all walks in a fixed order (ties -> lowest id), then decides among the
+// finalists with exact logits (fp32 h against the stored weights, fp32
+// accumulation). The bf16 rounding of h moves a logit by ~1e-3 (D = 4096,
+// weights ~N(0, 0.02^2)), far less than the usual gap between the first and
+// the fifth best score, so the exact decision is the decision of the exact
+// product.
+// Greedy: the entries are vocabulary ids; the 4 finalists are re-scored and
+// the best taken (rows whose fourth finalist is within kCloseCall of the first
+// are counted as close calls).
+// Sampling (the two-level draw): the entries are 16-id chunks scored in base-2
+// units (see the fold in tc_device.cuh); every finalist chunk within
+// kChunkBand of the best is re-scored exactly (16 logits each), the chunk
+// with the best exact score L_k - log(-log u_k) is chosen, and the draft token
+// is the inverse CDF of exp(l_v / T - L_k) inside it at the uniform of
+// Philox(k, position, request, tag 8) word 0 (rows with more than one chunk in
+// the band are counted as close calls). The LSE is returned in natural units.
 #include "internal.h"
 
 namespace dlite {
 
 constexpr float kCloseCall = 0.02f;  // natural score units (logit, or logit/T when sampling)
+// finalist chunks within this many natural units of the best approximate
+// chunk score are re-scored exactly (> 10x the score error of bf16 h)
+constexpr float kChunkBand = 0.05f;
 constexpr float kLog2eM = 1.4426950408889634f;
 constexpr float kLn2M = 0.6931471805599453f;
 
@@ -64,7 +70,7 @@ __device__ __forceinline__ void topk_insert(float (&sc)[kTopK], int (&id)[kTopK]
 __device__ __forceinline__ float exact_logit_part(const LmMergeArgs& a, int v, const float* h, int lo, int hi) {
   const int lane = threadIdx.x & 31;
   float acc0 = 0.f, acc1 = 0.f;
-  constexpr int kU = 16;
+  constexpr int kU = 8;
   for (int d0 = lo + lane * 4; d0 < hi; d0 += 128 * kU) {
     float4 ev[kU], hv[kU];
 #pragma unroll
@@ -126,6 +132,53 @@ __device__ __forceinline__ void warp_top4(float (&sc)[kTopK], int (&id)[kTopK], 
   }
 }
 
+// The 16 exact logits of chunk k, this warp's share: lane L of warp w takes the
+// column quads d = 4 (L + 32 (w + nw i)), i = 0, 1, ..., for 8 ids at a time
+// (the 8 rows' loads of a quad in flight together), then the lanes' sums are
+// reduced; returns this warp's partial for id t in lane t (t < 16).
+__device__ __forceinline__ float chunk_logits_part(const LmMergeArgs& a, int k, const float* h, int nw) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int kIds = kChunk / 2;
+  const int v0 = k * kChunk;
+  const int nv = min(kChunk, a.V - v0);
+  const int stride = 4 * 32 * nw;
+  float mine = 0.f;
+#pragma unroll 1
+  for (int half = 0; half < 2; ++half) {
+    float acc[kIds];
+#pragma unroll
+    for (int t = 0; t < kIds; ++t) acc[t] = 0.f;
+    for (int d = 4 * (lane + 32 * warp); d < a.D; d += stride) {
+      const float4 hv = *reinterpret_cast<const float4*>(h + d);
+      float4 ev[kIds];
+#pragma unroll
+      for (int t = 0; t < kIds; ++t) {
+        const int v = v0 + half * kIds + t;
+        ev[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (half * kIds + t < nv) {
+          if (a.Ef) {
+            ev[t] = *reinterpret_cast<const float4*>(a.Ef + (size_t)v * a.D + d);
+          } else {
+            const uint2 raw = *reinterpret_cast<const uint2*>(a.Eb + tiled_index(v, d, a.D));
+            const __nv_bfloat162 e01 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+            const __nv_bfloat162 e23 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+            ev[t] = make_float4(__low2float(e01), __high2float(e01), __low2float(e23), __high2float(e23));
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < kIds; ++t)
+        acc[t] = fmaf(ev[t].x, hv.x, fmaf(ev[t].y, hv.y, fmaf(ev[t].z, hv.z, fmaf(ev[t].w, hv.w, acc[t]))));
+    }
+#pragma unroll
+    for (int t = 0; t < kIds; ++t) {
+      const float v = warp_sum(acc[t]);
+      if (lane == half * kIds + t) mine = v;
+    }
+  }
+  return mine;
+}
+
 __device__ __forceinline__ void warp_lse(float& m, float& s) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {  // both partners form the same two terms
@@ -153,7 +206,7 @@ __device__ __forceinline__ float gumbel_f(uint32_t x) {
 }
 
 template <int kMergeWarps>
-__global__ void __launch_bounds__(kMergeWarps * 32) lm_merge_kernel(const LmMergeArgs a) {
+__global__ void __launch_bounds__(kMergeWarps * 32, 2) lm_merge_kernel(const LmMergeArgs a) {
   static_assert(kMergeWarps == 2 * kTopK, "two warps per finalist");
   // no early trigger: the verification kernel that follows would wait on
   // these SMs (its CTAs slowed this kernel by about 2x when launched early)
@@ -164,6 +217,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lm_merge_kernel(const LmMerg
   __shared__ float part[kMergeWarps];
   __shared__ int fin_id[kTopK];
   __shared__ float row_m, row_s, row_sc0, row_sc3;
+  __shared__ float chunk_l[kTopK][kChunk];  // sampling: exact logits of the finalist chunks
+  __shared__ float chunk_part[kMergeWarps][kChunk];
   const int r = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bool sampling = a.inv_T > 0.f;
@@ -217,7 +272,10 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lm_merge_kernel(const LmMerg
     if (sampling) warp_lse(m, s);
     if (lane == 0) {
 #pragma unroll
-      for (int k = 0; k < kTopK; ++k) fin_id[k] = oid[k];
+      for (int k = 0; k < kTopK; ++k) {
+        fin_id[k] = oid[k];
+        wsc[0][k] = osc[k];  // the finalists' approximate scores (warp 0's list slot is free now)
+      }
       row_m = m;
       row_s = s;
       row_sc0 = osc[0];
@@ -225,8 +283,93 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lm_merge_kernel(const LmMerg
     }
   }
   __syncthreads();
-  // exact re-scoring: warps 2k and 2k + 1 take the two halves of finalist k
   const float* h = a.h + (size_t)r * a.D;
+  if (sampling) {
+    // exact logits of the finalist chunks in the band (a prefix of the sorted
+    // finalists): every warp takes a slice of the columns of all 16 ids, the
+    // warps' partials are added in warp order
+    for (int j = 0; j < kTopK; ++j) {
+      const int k = fin_id[j];
+      if (!(k >= 0 && (long long)k * kChunk < a.V && wsc[0][j] >= row_sc0 - kChunkBand * kLog2eM)) break;
+      const float pv = chunk_logits_part(a, k, h, kMergeWarps);
+      if (lane < kChunk) chunk_part[warp][lane] = pv;
+      __syncthreads();
+      if (warp == 0 && lane < kChunk) {
+        float l = 0.f;
+#pragma unroll
+        for (int w = 0; w < kMergeWarps; ++w) l += chunk_part[w][lane];
+        chunk_l[j][lane] = l;
+      }
+      __syncthreads();
+    }
+    if (warp == 0) {
+      // lane j: the exact score of finalist chunk j; the best by a 4-lane
+      // reduction (ties -> lowest chunk id). fp32 with the accurate library
+      // exp / log (this GPU's float64 units are far too slow for a per-row
+      // tail): the decisions match the float64 oracle except where a score
+      // or a CDF step is within ~1e-6 of the deciding value.
+      const uint32_t req = (uint32_t)(r / a.K);
+      const uint32_t pos = (uint32_t)(a.pos[req] + (r % a.K) + 1);
+      const float invT = 1.f / (float)a.T;
+      float x = -INFINITY;
+      int kk = 0x7fffffff, n_in = 0;
+      if (lane < kTopK) {
+        const int kc = fin_id[lane];
+        if (kc >= 0 && (long long)kc * kChunk < a.V && wsc[0][lane] >= row_sc0 - kChunkBand * kLog2eM) {
+          const int nv = min(kChunk, a.V - kc * kChunk);
+          float mx = -INFINITY, tot = 0.f;
+          for (int t = 0; t < nv; ++t) mx = fmaxf(mx, chunk_l[lane][t] * invT);
+          for (int t = 0; t < nv; ++t) tot += expf(chunk_l[lane][t] * invT - mx);
+          const uint4 w = philox((uint32_t)kc >> 2, pos, req, kTagGumbel, a.k0, a.k1);
+          const uint32_t wx[4] = {w.x, w.y, w.z, w.w};
+          x = mx + logf(tot) + gumbel_f(wx[kc & 3]);
+          kk = kc;
+          n_in = 1;
+        }
+      }
+#pragma unroll
+      for (int o = 1; o < kTopK; o <<= 1) {
+        const float x2 = __shfl_xor_sync(0xffffffffu, x, o);
+        const int k2 = __shfl_xor_sync(0xffffffffu, kk, o);
+        if (x2 > x || (x2 == x && k2 < kk)) {
+          x = x2;
+          kk = k2;
+        }
+      }
+      n_in += __shfl_xor_sync(0xffffffffu, n_in, 1);
+      n_in += __shfl_xor_sync(0xffffffffu, n_in, 2);
+      if (lane == 0 && kk == 0x7fffffff) {  // no finalist (cannot happen with V >= 1): id 0
+        a.cand[r] = 0;
+        if (a.qs) a.qs[r].logit = 0.f;
+      } else if (lane == 0) {
+        int jw = 0;  // the finalist slot of the chosen chunk
+        for (int t = 0; t < kTopK; ++t)
+          if (fin_id[t] == kk) jw = t;
+        const int nv = min(kChunk, a.V - kk * kChunk);
+        float m2 = -INFINITY, t2 = 0.f;
+        for (int t = 0; t < nv; ++t) m2 = fmaxf(m2, chunk_l[jw][t] * invT);
+        for (int t = 0; t < nv; ++t) t2 += expf(chunk_l[jw][t] * invT - m2);
+        const float th = u01f(philox((uint32_t)kk, pos, req, kTagPick, a.k0, a.k1).x) * t2;
+        float c = 0.f;
+        int pick = nv - 1;  // the smallest id whose running sum passes the threshold
+        for (int t = 0; t + 1 < nv; ++t) {
+          c += expf(chunk_l[jw][t] * invT - m2);
+          if (c > th) {
+            pick = t;
+            break;
+          }
+        }
+        a.cand[r] = kk * kChunk + pick;
+        if (a.qs) {
+          a.qs[r].logit = chunk_l[jw][pick];
+          a.qs[r].lse = (row_m + log2f(row_s)) * kLn2M;
+        }
+        if (a.counters && n_in > 1) atomicAdd(a.counters + 4, 1ull);
+      }
+    }
+    return;
+  }
+  // greedy: exact re-scoring, warps 2k and 2k + 1 take the two halves of finalist k
   {
     const int v = fin_id[warp >> 1];
     const int half = (a.D / 2 + 3) & ~3;
@@ -237,43 +380,33 @@ __global__ void __launch_bounds__(kMergeWarps * 32) lm_merge_kernel(const LmMerg
   }
   __syncthreads();
   if (warp == 0) {  // lane k scores finalist k; the best by a 4-lane reduction (ties -> lowest id)
-    double x = -INFINITY;
-    float l = 0.f;
+    float x = -INFINITY;
     int v = 0x7fffffff;
     if (lane < kTopK) {
       const int fv = fin_id[lane];
       if (fv >= 0 && fv < a.V) {
         v = fv;
-        l = part[2 * lane] + part[2 * lane + 1];
-        x = l;
-        if (sampling) {
-          const uint32_t req = (uint32_t)(r / a.K);
-          const uint32_t pos = (uint32_t)(a.pos[req] + (r % a.K) + 1);
-          const uint4 w = philox((uint32_t)v >> 2, pos, req, kTagGumbel, a.k0, a.k1);
-          const uint32_t wx[4] = {w.x, w.y, w.z, w.w};
-          x = (double)l / a.T + (double)gumbel_f(wx[v & 3]);
-        }
+        x = part[2 * lane] + part[2 * lane + 1];
       }
     }
+    float l = x;
 #pragma unroll
     for (int o = 1; o < kTopK; o <<= 1) {
-      const double x2 = __shfl_xor_sync(0xffffffffu, x, o);
-      const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
+      const float x2 = __shfl_xor_sync(0xffffffffu, x, o);
       const int v2 = __shfl_xor_sync(0xffffffffu, v, o);
       if (x2 > x || (x2 == x && v2 < v)) {
         x = x2;
-        l = l2;
         v = v2;
       }
     }
+    l = x;
     if (lane == 0) {
       a.cand[r] = v;
       if (a.qs) {
         a.qs[r].logit = l;
-        a.qs[r].lse = sampling ? (row_m + log2f(row_s)) * kLn2M : NAN;
+        a.qs[r].lse = NAN;
       }
-      const float band = sampling ? kCloseCall * kLog2eM : kCloseCall;
-      if (a.counters && row_sc3 > row_sc0 - band) atomicAdd(a.counters + 4, 1ull);
+      if (a.counters && row_sc3 > row_sc0 - kCloseCall) atomicAdd(a.counters + 4, 1ull);
     }
   }
 }

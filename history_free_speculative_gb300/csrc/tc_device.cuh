@@ -208,13 +208,16 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 
 // ---------------------------------------------------------------- LM-head score folding
 // Every epilogue thread owns one row of h and scans its vocabulary columns in
-// increasing id order, keeping the 4 best (score, id) and the log-sum-exp
-// partials of the columns it saw. Greedy scores are the logits. Sampling
-// scores are kept in base-2 units: with l2 = logit * log2(e) / T and the same
-// uniform u as the Gumbel draw, score = l2 - log2(-log2 u) (-log2 u from
-// neg_log2_u01), which equals
-// log2(e) * (logit / T - log(-log u)) + log2(ln 2): a fixed increasing map of
-// the Gumbel-max score, so it selects the same finalists. The LSE partials are
+// increasing id order, keeping the 4 best (score, id) it saw and, when
+// sampling, the log-sum-exp partials of its columns.
+// Greedy: scores are the logits, ids the vocabulary ids.
+// Sampling (the two-level draw): each 16-id chunk k is one entry, scored in
+// base-2 units as log2(sum_{v in k} 2^(l2_v)) - log2(-log2 u_k), with
+// l2 = logit * log2(e) / T and u_k the chunk's uniform (word k & 3 of
+// Philox(k >> 2, position, request, TAG_GUMBEL)); that is
+// log2(e) (L_k - log(-log u_k)) + log2(ln 2) with L_k the chunk's natural
+// log-mass at temperature T, a fixed increasing map of the chunk's Gumbel-max
+// score, so the best entries are the finalist chunks. The LSE partials are
 // m = max l2 and s = sum 2^(l2 - m).
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -346,47 +349,32 @@ __device__ __forceinline__ void topk_push_scan(LmAcc& a, float x, int v) {
   a.id[0] = c0 ? v : i0;
 }
 
-// Fold 16 consecutive columns v0 .. v0+15 (v0 a multiple of 4) of one row, of
+// Fold 16 consecutive columns v0 .. v0+15 (v0 a multiple of 16) of one row, of
 // which the first nv (a multiple of 4) are vocabulary ids. c2s = log2(e) / T.
-// Must be called by all 32 lanes of a warp together (warp vote inside).
+// Must be called by all 32 lanes of a warp together.
 template <bool kSampling, bool kFull>
 __device__ __forceinline__ void lm_fold16(LmAcc& a, const uint32_t (&raw)[16], int v0, int nv, float c2s,
                                           const PhiloxRow& pr, uint32_t k0, uint32_t k1, bool active) {
   if (kSampling) {
-    // LSE partials; the chunk maximum is taken on the raw logits (c2s > 0)
+    // the chunk v0 / 16: its maximum, its mass relative to it, the row's LSE
+    // partials, then one noise draw and one list entry for the whole chunk
     float lmax = __uint_as_float(raw[0]);
 #pragma unroll
     for (int j = 1; j < 16; ++j)
       if (kFull || j < nv) lmax = fmaxf(lmax, __uint_as_float(raw[j]));
     const float cm = lmax * c2s;
-    if (active) {
-      if (cm > a.m) {
-        a.s *= ex2_approx(a.m - cm);
-        a.m = cm;
-      }
-      float s = 0.f;
+    float s = 0.f;
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (kFull || j < nv) s += ex2_approx(fmaf(__uint_as_float(raw[j]), c2s, -a.m));
-      a.s += s;
-    }
-    // Every 23-bit draw gives noise -log2(-log2 u) <= 23.47 in these units: a
-    // chunk whose best scaled logit is further than that below the 4th best
-    // score of every lane cannot change any list (frequent with the wide
-    // logit ranges of trained models).
-    const bool hopeless = !active || !(cm + 23.5f > a.sc[kTopK - 1]);
-    if (__all_sync(0xffffffffu, hopeless)) return;
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      if (!kFull && 4 * g >= nv) break;
-      const uint4 w = philox_row((uint32_t)(v0 + 4 * g) >> 2, pr, k0, k1);
-      const uint32_t wx[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float sc = fmaf(__uint_as_float(raw[4 * g + j]), c2s, -lg2_approx(neg_log2_u01(wx[j])));
-        if (active) topk_push_scan(a, sc, v0 + 4 * g + j);
-      }
-    }
+    for (int j = 0; j < 16; ++j)
+      if (kFull || j < nv) s += ex2_approx(fmaf(__uint_as_float(raw[j]), c2s, -cm));
+    if (!active) return;
+    const float mm = fmaxf(a.m, cm);
+    a.s = a.s * ex2_approx(a.m - mm) + s * ex2_approx(cm - mm);
+    a.m = mm;
+    const uint32_t k = (uint32_t)v0 >> 4;
+    const uint4 w = philox_row(k >> 2, pr, k0, k1);
+    const uint32_t wk = (k & 2u) ? ((k & 1u) ? w.w : w.z) : ((k & 1u) ? w.y : w.x);
+    topk_push_scan(a, cm + lg2_approx(s) - lg2_approx(neg_log2_u01(wk)), (int)k);
   } else {
     if (!active) return;
 #pragma unroll

@@ -161,8 +161,12 @@ void dlite_destroy(dlite_handle *h);
  *   anchor [B] int32              the token already chosen but not yet run
  *                                 ([B, G] with anchor_group G > 1: the local group, anchor last)
  *                                 through the target ([P1] §"锚点...")
- *   temperature                   0 = greedy argmax; > 0 = Gumbel-max draw from
- *                                 q_i = softmax(l_i / T)
+ *   temperature                   0 = greedy argmax; > 0 = an exact draw from
+ *                                 q_i = softmax(l_i / T) in two levels: Gumbel-max over
+ *                                 chunks of 16 ids on their log-mass L_k (noise: word
+ *                                 k & 3 of Philox(k >> 2, position, b, 1)), then the
+ *                                 inverse CDF inside the chosen chunk k at word 0 of
+ *                                 Philox(k, position, b, 8)
  *   seed, pos [B] int64           RNG key and per-request position offset; draft
  *                                 slot i (1..K) uses position pos[b] + i
  *                                 (ignored when temperature == 0; pos may be NULL then)
@@ -195,7 +199,7 @@ int dlite_draft_round_taps(dlite_handle *h, int B, const void *hidden, const int
  *   dlite_backbone:   hidden, anchor -> b [B, K, D] float32 (staging + L_D layers + final norm)
  *   dlite_seq_head:   b [B, K, D] float32 -> hs [B, K, D] float32 (sequential head)
  *   dlite_lm_head:    hs [B, K, D] float32 -> candidates, qstats (vocabulary
- *                     projection with the fused argmax / Gumbel-max + LSE) */
+ *                     projection with the fused argmax / two-level draw + LSE) */
 int dlite_backbone(dlite_handle *h, int B, const void *hidden, const int32_t *anchor, float *b,
                    dlite_stream_t stream);
 int dlite_seq_head(dlite_handle *h, int B, const float *b, float *hs, dlite_stream_t stream);

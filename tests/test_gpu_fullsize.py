@@ -99,8 +99,8 @@ def test_full_size_bf16_activations(name, rounds):
             for i in np.nonzero(cand[b] != mir["cand"])[0]:
                 n_bad += 1
                 ell = E @ h_gpu[b, i].astype(np.float64)   # exact logits of the GPU's own head state
-                s = ell / Tq + ph.gumbel_row(wl.rng_seed, int(pos[b]) + i + 1, b, cfg.V) if T > 0 else ell
-                assert int(np.argmax(s)) == cand[b, i], (r, b, i)
+                own = O.sample_logits(ell, Tq if T > 0 else 0.0, wl.rng_seed, int(pos[b]) + i + 1, b)[0]
+                assert own == cand[b, i], (r, b, i)
                 assert mir["gap"][i] < 0.1, (r, b, i, mir["gap"][i])   # > 5 sigma of the bf16 rounding noise
     assert n >= 1000
     assert n_bad <= 0.02 * n, (n_bad, n)

@@ -133,15 +133,11 @@ def test_lm_head_identical_inputs_multislab(midvocab, B, T):
     E = O.f64(W["E"])
     ell = O.lm_logits(hs.reshape(-1, cfg.D).numpy().astype(np.float64), E).reshape(B, cfg.K, -1)
     Tq = float(np.float32(T))
-    if T == 0.0:
-        s = ell
-    else:
-        s = ell / Tq + np.stack([[ph.gumbel_row(123, int(pos[b]) + i + 1, b, cfg.V)
-                                  for i in range(cfg.K)] for b in range(B)])
-    oc = s.argmax(axis=2)
-    part = np.partition(s, -2, axis=2)
+    picks = [[O.sample_logits(ell[b, i], Tq, 123, int(pos[b]) + i + 1, b) for i in range(cfg.K)] for b in range(B)]
+    oc = np.array([[p[0] for p in row] for row in picks])
+    gap = np.array([[p[1] for p in row] for row in picks])
     c = cand.cpu().numpy()
-    check_candidates(c, oc, part[..., -1] - part[..., -2])
+    check_candidates(c, oc, gap)
     q = qs.cpu().numpy()
     # the reported logit is the exact re-score of the chosen id
     chosen = np.take_along_axis(ell, c[..., None].astype(np.int64), 2)[..., 0]
@@ -173,14 +169,10 @@ def test_lm_head_identical_inputs_tiny(tiny, T):
     E = O.f64(W["E"])
     ell = O.lm_logits(hs.reshape(-1, cfg.D).numpy(), E).reshape(B, cfg.K, -1)
     Tq = float(np.float32(T))
-    if T == 0.0:
-        s = ell
-    else:
-        s = ell / Tq + np.stack([[ph.gumbel_row(99, int(pos[b]) + i + 1, b, cfg.V)
-                                  for i in range(cfg.K)] for b in range(B)])
-    oc = s.argmax(axis=2)
-    part = np.partition(s, -2, axis=2)
-    check_candidates(cand.cpu().numpy(), oc, part[..., -1] - part[..., -2], gap_tol=1e-4)
+    picks = [[O.sample_logits(ell[b, i], Tq, 99, int(pos[b]) + i + 1, b) for i in range(cfg.K)] for b in range(B)]
+    oc = np.array([[p[0] for p in row] for row in picks])
+    gap = np.array([[p[1] for p in row] for row in picks])
+    check_candidates(cand.cpu().numpy(), oc, gap, gap_tol=1e-4)
 
 
 def test_seq_head_identical_inputs_tiny(tiny):
