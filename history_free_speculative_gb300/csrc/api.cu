@@ -34,6 +34,13 @@ struct MapEntry {
   CUtensorMap map;
 };
 
+// Map of fp32 split-K partials [S][rows][outs] (bulk-store epilogue).
+struct OutMapEntry {
+  const void* base;
+  int S, rows, outs;
+  CUtensorMap map;
+};
+
 struct dlite_handle {
   dlite_config cfg;
   bool f32 = false;
@@ -45,6 +52,7 @@ struct dlite_handle {
   int num_sms = 0;  // SMs of the device (persistent LM-head grid)
   std::vector<void*> allocs;
   std::vector<MapEntry> maps;
+  std::vector<OutMapEntry> out_maps;
   std::vector<TunedPlan> tuned;  // plans of the B_max products, chosen by timing (tune_products)
   size_t part_cap = 0;           // floats in part
 
@@ -263,6 +271,19 @@ const CUtensorMap* get_map(dlite_handle* h, const void* base, int rows, int K, i
   return &h->maps.back().map;
 }
 
+const CUtensorMap* get_out_map(dlite_handle* h, const void* base, int S, int rows, int outs) {
+  for (const OutMapEntry& e : h->out_maps)
+    if (e.base == base && e.S == S && e.rows == rows && e.outs == outs) return &e.map;
+  OutMapEntry e;
+  e.base = base;
+  e.S = S;
+  e.rows = rows;
+  e.outs = outs;
+  if (!tc::make_out_map(&e.map, base, S, rows, outs)) return nullptr;
+  h->out_maps.push_back(e);
+  return &h->out_maps.back().map;
+}
+
 // One launch of the one-CTA engine with plan pl (partials, or the SwiGLU output when act is set).
 int launch_onecta(dlite_handle* h, const tc::Plan& pl, const Operand& X, const Operand& W, int rows, int outs,
                   float* part, cudaStream_t s, bf16* const* act, int act_planes, int skip_row0, int skip_cols) {
@@ -285,13 +306,17 @@ int launch_onecta(dlite_handle* h, const tc::Plan& pl, const Operand& X, const O
   prm.status = h->status;
   prm.skip_row0 = skip_row0;
   prm.skip_cols = skip_cols;
+  const CUtensorMap* out = nullptr;
   if (act) {
     prm.mode = 2;
     prm.act[0] = act[0];
     prm.act[1] = act_planes == 2 ? act[1] : nullptr;
     prm.act_planes = act_planes;
+  } else {
+    out = get_out_map(h, part, pl.S, rows, outs);  // partials leave through bulk tensor stores
+    if (!out) return DLITE_ERR_CUDA;
   }
-  CK(tc::launch(pl, x0, x1, w0, w1, prm, s));
+  CK(tc::launch(pl, x0, x1, w0, w1, prm, s, out));
   return DLITE_OK;
 }
 
@@ -1597,8 +1622,10 @@ int dlite_selftest_gemm(int rows, int outs, int K, int xplanes, int wplanes, con
   prm.x_box = xb;
   prm.part = part;
   prm.status = status;
+  CUtensorMap mo;
+  if (!tc::make_out_map(&mo, part, pl.S, rows, outs)) return DLITE_ERR_CUDA;
   CK(tc::launch(pl, &mx0, xplanes == 2 ? &mx1 : nullptr, &mw0, wplanes == 2 ? &mw1 : nullptr, prm,
-                (cudaStream_t)stream));
+                (cudaStream_t)stream, &mo));
   return pl.S;
 }
 

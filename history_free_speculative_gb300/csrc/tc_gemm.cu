@@ -24,7 +24,7 @@ template <int NMT, int XP, int WP>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap mx0, const __grid_constant__ CUtensorMap mx1,
                    const __grid_constant__ CUtensorMap mw0, const __grid_constant__ CUtensorMap mw1,
-                   const TcParams p) {
+                   const __grid_constant__ CUtensorMap mo, const TcParams p) {
   // Shared memory: [barriers | pad to 1 KB] [stage 0] ... [stage S-1] [kTailPad].
   // Stage: [activation slots: NMT x XP x a_slot] [weight planes: WP x N rows x 128 B].
   // An activation slot holds only the x_box loaded rows; the 128-row MMA operand
@@ -178,7 +178,41 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int mt = 0; mt < NMT; ++mt) {
         const int r = m0 + mt * 128 + q * 32 + lane;
         const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(mt * p.N);
-        if (p.mode == 0) {
+        if (p.mode == 0 && p.tma_out && ncol % 32 == 0) {
+          // lane = row of a 32 x 32 box staged in this warp's 4 KB of the idle
+          // stage memory (128-byte swizzle: 16-byte chunk j of row L at chunk
+          // j ^ (L & 7), so the lanes' stores spread over the banks), written
+          // by one bulk tensor store; rows past p.rows are clipped by the map
+          const uint32_t stg = su32(smem + (size_t)(warp - 2) * 4096);
+          const int row0 = m0 + mt * 128 + q * 32;
+          for (int c = c_lo; c < c_hi; c += 32) {
+            uint32_t v0[16], v1[16];
+            tmem_ld16_nowait(tbase + c, v0);
+            tmem_ld16_nowait(tbase + c + 16, v1);
+            tmem_wait_ld();
+            if (lane == 0) bulk_wait_read0();  // the previous box has left the buffer
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const uint32_t a = stg + (uint32_t)lane * 128u + (uint32_t)((j ^ (lane & 7)) * 16);
+              const uint32_t w0 = j < 4 ? v0[4 * j] : v1[4 * (j - 4)];
+              const uint32_t w1 = j < 4 ? v0[4 * j + 1] : v1[4 * (j - 4) + 1];
+              const uint32_t w2 = j < 4 ? v0[4 * j + 2] : v1[4 * (j - 4) + 2];
+              const uint32_t w3 = j < 4 ? v0[4 * j + 3] : v1[4 * (j - 4) + 3];
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w0), "r"(w1), "r"(w2),
+                           "r"(w3)
+                           : "memory");
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0 && row0 < p.rows && o0 + c < p.outs) {
+              tma_store_3d(&mo, stg, o0 + c, row0, split);
+              bulk_commit();
+            }
+          }
+          if (lane == 0) bulk_wait0();  // performed before the CTA ends
+          __syncwarp();
+        } else if (p.mode == 0) {
           // lane = row: each lane stores its row's 16 columns per chunk as four
           // 16-byte stores straight from the TMEM registers (measured faster than
           // a shared-memory transpose into full 128-byte rows: the epilogue is
@@ -330,6 +364,18 @@ bool make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_out_map(CUtensorMap* m, const void* base, int S, int rows, int outs) {
+  EncodeTiledFn fn = encoder();
+  if (!fn || !base || ((uintptr_t)base & 15) || S < 1 || rows < 1 || outs < 8 || outs % 4) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)outs, (cuuint64_t)rows, (cuuint64_t)S};
+  cuuint64_t strides[2] = {(cuuint64_t)outs * 4, (cuuint64_t)rows * outs * 4};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map_tiled(CUtensorMap* m, const void* base, int rows, int K, int box_rows) {
   EncodeTiledFn fn = encoder();
   if (!fn || !base || ((uintptr_t)base & 15) || K % 64 || rows % 64 || box_rows % 64 || box_rows < 64 ||
@@ -453,15 +499,15 @@ std::vector<Plan> plan_candidates(int rows, int outs, int K, int xplanes, int wp
 }
 
 size_t smem_bytes(const Plan& pl) {
-  // the epilogue reuses the first 32 KB of the stage memory as transpose buffers
+  // the epilogue reuses the first 64 KB of the stage memory as staging boxes (4 KB per warp)
   size_t stage_mem = (size_t)pl.stages * pl.stage_bytes + kTailPad;
-  if (stage_mem < 32768) stage_mem = 32768;
+  if (stage_mem < 65536) stage_mem = 65536;
   return 1024 /* align */ + 1024 /* barriers */ + stage_mem;
 }
 
 typedef void (*KernelFn)(const __grid_constant__ CUtensorMap, const __grid_constant__ CUtensorMap,
                          const __grid_constant__ CUtensorMap, const __grid_constant__ CUtensorMap,
-                         const TcParams);
+                         const __grid_constant__ CUtensorMap, const TcParams);
 
 template <int NMT>
 static KernelFn pick_planes(int xp, int wp) {
@@ -482,7 +528,7 @@ static KernelFn pick(int nmt, int xp, int wp) {
 }
 
 cudaError_t launch(const Plan& pl, const CUtensorMap* x0, const CUtensorMap* x1, const CUtensorMap* w0,
-                   const CUtensorMap* w1, TcParams prm, cudaStream_t s) {
+                   const CUtensorMap* w1, TcParams prm, cudaStream_t s, const CUtensorMap* out) {
   KernelFn fn = pick(pl.n_mt, prm.xplanes, prm.wplanes);
   if (!fn) return cudaErrorInvalidValue;
   static bool attr[5][3] = {};
@@ -500,9 +546,10 @@ cudaError_t launch(const Plan& pl, const CUtensorMap* x0, const CUtensorMap* x1,
   prm.stages = pl.stages;
   prm.stage_bytes = pl.stage_bytes;
   prm.tmem_cols = (uint32_t)pl.tmem_cols;
+  prm.tma_out = (out && prm.mode == 0) ? 1 : 0;
   dim3 grid((prm.outs + pl.N - 1) / pl.N, pl.S, pl.groups);
   return launch_pdl(fn, grid, dim3(kGemmThreads), smem_bytes(pl), s, *x0, x1 ? *x1 : *x0, *w0,
-                    w1 ? *w1 : *w0, prm);
+                    w1 ? *w1 : *w0, out ? *out : *x0, prm);
 }
 
 }  // namespace tc

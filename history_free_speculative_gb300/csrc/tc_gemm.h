@@ -47,6 +47,7 @@ struct TcParams {
   const int64_t* pos = nullptr;
   int K_draft = 1;
   int* status = nullptr;
+  int tma_out = 0;         // mode 0: partials leave through bulk tensor stores (the out map)
   // mode 0: a CTA whose rows all lie at or past skip_row0 (> 0) and whose
   // columns all lie before skip_cols does nothing (a product over stacked
   // operands whose lower rows need only the upper columns)
@@ -58,6 +59,9 @@ bool make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows);
 // Tensor map of a bf16 weight in the tiled layout (rows a multiple of 64), box = one
 // k block of box_rows (a multiple of 64) rows.
 bool make_map_tiled(CUtensorMap* m, const void* base, int rows, int K, int box_rows);
+// Tensor map of fp32 split-K partials part[S][rows][outs] for 32-row x 32-column
+// bulk stores (128-byte swizzle): rows and columns past the extents are not written.
+bool make_out_map(CUtensorMap* m, const void* base, int S, int rows, int outs);
 // lm or one_split: no k splits (the LM head; products whose epilogue needs the full sums)
 // skip_row0 / skip_cols: the tiles TcParams::skip_row0 / skip_cols describe do no work
 Plan plan(int rows, int outs, int K, int xplanes, int wplanes, bool lm, bool one_split = false, int skip_row0 = 0,
@@ -145,8 +149,9 @@ LmPlan lm_plan_persistent(int rows, int outs, int K, int num_sms);
 size_t lm_smem_bytes(const LmPlan& pl);
 cudaError_t launch_lm_persistent(const LmPlan& pl, const CUtensorMap* x0, const CUtensorMap* x1,
                                  const CUtensorMap* w, LmParams prm, cudaStream_t s);
+// out: the partials' map (make_out_map) for mode 0, or null (16-byte stores from registers)
 cudaError_t launch(const Plan& pl, const CUtensorMap* x0, const CUtensorMap* x1, const CUtensorMap* w0,
-                   const CUtensorMap* w1, TcParams prm, cudaStream_t s);
+                   const CUtensorMap* w1, TcParams prm, cudaStream_t s, const CUtensorMap* out = nullptr);
 
 }  // namespace tc
 }  // namespace dlite
