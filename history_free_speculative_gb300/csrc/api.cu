@@ -336,26 +336,6 @@ int gemm(dlite_handle* h, const char* name, const Operand& X, const Operand& W, 
          bool* fused = nullptr, int skip_row0 = 0, int skip_cols = 0) {
   if (fused) *fused = false;
   const bool skipping = skip_row0 > 0;  // tiles to skip: the one-CTA engine
-  // few rows: persistent stream-K over the weights (the gate/up product keeps
-  // the one-CTA engine, whose epilogue applies the SwiGLU)
-  if (!act && !skipping && tc::use_stream_engine(rows, X.n, W.n)) {
-    const tc::StreamPlan sp = tc::stream_plan(rows, outs, X.K, h->num_sms);
-    if (sp.ok) {
-      h->maps.reserve(h->maps.size() + 4);
-      const CUtensorMap* x0 = get_map(h, X.p[0], X.rows, X.K, sp.x_box);
-      const CUtensorMap* w0 = get_map(h, W.p[0], W.rows, W.K, sp.N, true);
-      if (!x0 || !w0) return DLITE_ERR_CUDA;
-      tc::StreamParams prm;
-      prm.rows = rows;
-      prm.outs = outs;
-      prm.part = part;
-      prm.status = h->status;
-      if (sp_out) *sp_out = tc::stream_splits(sp);
-      CK(tc::launch_stream(sp, x0, w0, prm, s));
-      mark(h, name);
-      return DLITE_OK;
-    }
-  }
   if (!skipping && tc::use_pair_engine(rows, X.n, W.n)) {  // 2-SM MMAs
     const tc::PairPlan pp = tc::pair_plan(rows, outs, X.K, h->num_sms);
     if (pp.ok) {
@@ -402,19 +382,15 @@ tc::Plan lm_plan(dlite_handle* h, int rows) {
 }
 
 // bf16 drafters store the context rows z behind the local rows y in one
-// buffer, and a single product [y; z] W_qkv^T serves both, one launch instead
-// of two: 1 = few rows, on the stream-K engine (the query columns of the
-// context rows are computed and ignored); 2 = more rows, on the one-CTA
-// engine, whose tiles of context rows x query columns are skipped.
-// 0 = two products (fp32 drafters).
-static int ctx_route(const dlite_handle* h, int B) {
+// buffer, and a single product [y; z] W_qkv^T on the one-CTA engine serves
+// both, one launch instead of two: its tiles of context rows x query columns
+// are skipped. fp32-class drafters run two products.
+static bool fuse_ctx(const dlite_handle* h, int B) {
   const dlite_config& c = h->cfg;
   const int rows = B * (group_of(&c) + c.K) + B * c.m;
-  if (h->np != 1 || h->xp != 1) return 0;
-  if (tc::use_stream_engine(rows, 1, 1)) return tc::stream_plan(rows, h->qd + 2 * h->kvd, c.D, h->num_sms).ok;
-  return tc::plan(rows, h->qd + 2 * h->kvd, c.D, 1, 1, false).ok ? 2 : 0;
+  if (h->np != 1 || h->xp != 1) return false;
+  return tc::plan(rows, h->qd + 2 * h->kvd, c.D, 1, 1, false, false, B * (group_of(&c) + c.K), h->qd).ok;
 }
-static bool fuse_ctx(const dlite_handle* h, int B) { return ctx_route(h, B) != 0; }
 
 // History-KV control, layer l: split-KV attention of the block's queries over
 // the ring and the block, then the merge into h->o and the ring append.
@@ -498,10 +474,9 @@ int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anch
     Splits S1, S2;
     AttnArgs at;
     if (fused_ctx) {
-      const bool skip = ctx_route(h, B) == 2;
       RUN(gemm(h, "gemm_qkv", opnd(h->y, h->xp, h->Lcap + h->Ccap, c.D),
                opnd(w.Wqkv, h->np, h->qd + 2 * h->kvd, c.D), L + C, h->qd + 2 * h->kvd, h->part, &S1, s,
-               nullptr, 1, nullptr, skip ? L : 0, skip ? h->qd : 0));
+               nullptr, 1, nullptr, L, h->qd));
       at.part_ctx = h->part;
       at.sp_ctx = S1;
       at.ctx_row0 = L;
@@ -599,6 +574,41 @@ int run_backbone(dlite_handle* h, int B, const void* hidden, const int32_t* anch
   return DLITE_OK;
 }
 
+// out32 = res + X W^T on the one-CTA engine with one k split, written as fp32
+// and as two bf16 planes by the product's epilogue (no partials, no second
+// kernel); DLITE_ERR_UNSUPPORTED_SHAPE when no single-split plan fits.
+int gemm_residual(dlite_handle* h, const char* name, const Operand& X, const Operand& W, int rows, int outs,
+                  const float* res, float* out32, bf16* const* planes, float* tap, cudaStream_t s) {
+  if (outs % 16) return DLITE_ERR_UNSUPPORTED_SHAPE;
+  const tc::Plan pl = tc::plan(rows, outs, X.K, X.n, W.n, false, true);
+  if (!pl.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
+  const int xb = tc::x_box_rows(rows);
+  h->maps.reserve(h->maps.size() + 4);
+  const CUtensorMap* x0 = get_map(h, X.p[0], X.rows, X.K, xb);
+  const CUtensorMap* x1 = X.n == 2 ? get_map(h, X.p[1], X.rows, X.K, xb) : nullptr;
+  const CUtensorMap* w0 = get_map(h, W.p[0], W.rows, W.K, pl.N, true);
+  const CUtensorMap* w1 = W.n == 2 ? get_map(h, W.p[1], W.rows, W.K, pl.N, true) : nullptr;
+  if (!x0 || !w0 || (X.n == 2 && !x1) || (W.n == 2 && !w1)) return DLITE_ERR_CUDA;
+  tc::TcParams prm;
+  prm.rows = rows;
+  prm.outs = outs;
+  prm.K = X.K;
+  prm.xplanes = X.n;
+  prm.wplanes = W.n;
+  prm.mode = 3;
+  prm.x_box = xb;
+  prm.res = res;
+  prm.out32 = out32;
+  prm.tap32 = tap;
+  prm.act[0] = planes[0];
+  prm.act[1] = planes[1];
+  prm.act_planes = 2;
+  prm.status = h->status;
+  CK(tc::launch(pl, x0, x1, w0, w1, prm, s));
+  mark(h, name);
+  return DLITE_OK;
+}
+
 // b (h->b, h->bp) -> hs (h->hs, h->hp)
 int run_seq_head(dlite_handle* h, int B, float* tap_hs, cudaStream_t s) {
   const dlite_config& c = h->cfg;
@@ -622,6 +632,11 @@ int run_seq_head(dlite_handle* h, int B, float* tap_hs, cudaStream_t s) {
   ch.Bg = chain_group_size(c.R, B);
   CK(launch_head_chain(ch, s));
   mark(h, "head_chain");
+  // few rows: h = b + t P^T straight from the product's epilogue (fp32 and the bf16
+  // planes of the LM head); with more rows a single k split leaves too few CTAs
+  const int rc = rows > 64 ? DLITE_ERR_UNSUPPORTED_SHAPE : gemm_residual(h, "gemm_head_p", opnd(h->tp, 2, h->Hcap, h->Rp), opnd(h->P, h->np, c.D, h->Rp),
+                               rows, c.D, h->b, h->hs, h->hp, tap_hs, s);
+  if (rc != DLITE_ERR_UNSUPPORTED_SHAPE) return rc;
   RUN(gemm(h, "gemm_head_p", opnd(h->tp, 2, h->Hcap, h->Rp), opnd(h->P, h->np, c.D, h->Rp), rows, c.D,
            h->part, &S, s));
   CK(launch_head_out(h->part, S.S, rows, c.D, h->b, h->hs, h->hp, tap_hs, s));
@@ -876,15 +891,13 @@ static int tune_products(dlite_handle* h) {
   std::vector<Site> sites;
   const LayerW& w = h->layer[0];
   const int qkv = h->qd + 2 * h->kvd;
-  if (ctx_route(h, B) == 2)
+  if (fuse_ctx(h, B))
     sites.push_back({opnd(h->y, 1, h->Lcap + h->Ccap, c.D), opnd(w.Wqkv, 1, qkv, c.D), L + C, qkv, nullptr, L, h->qd});
   sites.push_back({opnd(h->o, 1, h->Lcap, h->qd), opnd(w.Wo, 1, c.D, h->qd), L, c.D, nullptr, 0, 0});
   sites.push_back({opnd(h->y, 1, h->Lcap, c.D), opnd(w.Wgu, 1, 2 * c.F, c.D), L, 2 * c.F, h->a, 0, 0});
   sites.push_back({opnd(h->a, 1, h->Lcap, c.F), opnd(w.Wd, 1, c.D, c.F), L, c.D, nullptr, 0, 0});
-  if (!h->gated) {
+  if (!h->gated)
     sites.push_back({opnd(h->bp, 2, h->Hcap, c.D), opnd(h->Wce, 1, 2 * h->Rp, c.D), Hr, 2 * h->Rp, nullptr, 0, 0});
-    sites.push_back({opnd(h->tp, 2, h->Hcap, h->Rp), opnd(h->P, 1, c.D, h->Rp), Hr, c.D, nullptr, 0, 0});
-  }
   const size_t flush_bytes = (size_t)256 << 20;  // twice the L2
   void* flush = nullptr;
   if (cudaMalloc(&flush, flush_bytes) != cudaSuccess) {
@@ -900,11 +913,9 @@ static int tune_products(dlite_handle* h) {
   for (const Site& st : sites) {
     if (rc) break;
     const bool skipping = st.skip_row0 > 0;
-    const bool stream = !st.act && !skipping && tc::use_stream_engine(st.rows, st.X.n, st.W.n) &&
-                        tc::stream_plan(st.rows, st.outs, st.X.K, h->num_sms).ok;
-    const bool pair = !stream && !skipping && tc::use_pair_engine(st.rows, st.X.n, st.W.n) &&
+    const bool pair = !skipping && tc::use_pair_engine(st.rows, st.X.n, st.W.n) &&
                       tc::pair_plan(st.rows, st.outs, st.X.K, h->num_sms).ok;
-    if (stream || pair) continue;  // another engine serves this product
+    if (pair) continue;  // the pair engine serves this product
     TunedPlan best;
     float best_ms = 1e30f;
     for (const tc::Plan& pl : tc::plan_candidates(st.rows, st.outs, st.X.K, st.X.n, st.W.n, st.act != nullptr)) {
@@ -1093,15 +1104,9 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
       const size_t v = (size_t)pl.S * st[0] * st[1];
       pe = v > pe ? v : pe;
       const tc::PairPlan pp = tc::pair_plan(st[0], st[1], st[2], h->num_sms);
-      const tc::StreamPlan sq = tc::stream_plan(st[0], st[1], st[2], h->num_sms);
-      if (sq.ok && tc::use_stream_engine(st[0], st[3], h->np))
-        pe = (size_t)sq.S * st[0] * st[1] > pe ? (size_t)sq.S * st[0] * st[1] : pe;
       if (pp.ok && tc::use_pair_engine(st[0], st[3], h->np)) pe = (size_t)pp.S * st[0] * st[1] > pe ? (size_t)pp.S * st[0] * st[1] : pe;  // planes
     }
-    if (ctx_route(h, B) == 1) {
-      const tc::StreamPlan sf = tc::stream_plan(L + C, h->qd + 2 * h->kvd, D, h->num_sms);
-      pe = (size_t)sf.S * (L + C) * (h->qd + 2 * h->kvd) > pe ? (size_t)sf.S * (L + C) * (h->qd + 2 * h->kvd) : pe;
-    } else if (ctx_route(h, B) == 2) {
+    if (fuse_ctx(h, B)) {
       const tc::Plan pf = tc::plan(L + C, h->qd + 2 * h->kvd, D, 1, 1, false, false, L, h->qd);
       pe = std::max(pe, (size_t)pf.S * (L + C) * (h->qd + 2 * h->kvd));
     }
@@ -1110,9 +1115,6 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
     const size_t v2 = (size_t)pc.S * C * 2 * h->kvd;
     pe2 = v2 > pe2 ? v2 : pe2;
     const tc::PairPlan pc2 = tc::pair_plan(C, 2 * h->kvd, D, h->num_sms);
-    const tc::StreamPlan sc2 = tc::stream_plan(C, 2 * h->kvd, D, h->num_sms);
-    if (sc2.ok && tc::use_stream_engine(C, h->xp, h->np))
-      pe2 = (size_t)sc2.S * C * 2 * h->kvd > pe2 ? (size_t)sc2.S * C * 2 * h->kvd : pe2;
     if (pc2.ok && tc::use_pair_engine(C, h->xp, h->np)) pe2 = (size_t)pc2.S * C * 2 * h->kvd > pe2 ? (size_t)pc2.S * C * 2 * h->kvd : pe2;
     const tc::Plan pl = lm_plan(h, H);
     if (!pl.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
@@ -1127,7 +1129,7 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
   {  // the timed plan selection at B_max may pick up to 4 splits for the layer products
     const int L = Bm * (group_of(&c) + c.K), C = Bm * c.m;
     pe = std::max(pe, (size_t)4 * L * std::max(h->qd + 2 * h->kvd, D));
-    if (ctx_route(h, Bm) == 2) pe = std::max(pe, (size_t)4 * (L + C) * (h->qd + 2 * h->kvd));
+    if (fuse_ctx(h, Bm)) pe = std::max(pe, (size_t)4 * (L + C) * (h->qd + 2 * h->kvd));
   }
   AL(h->part, pe);
   h->part_cap = pe;
@@ -1551,24 +1553,6 @@ int dlite_selftest_gemm(int rows, int outs, int K, int xplanes, int wplanes, con
   if ((xplanes == 2 && !X1) || (wplanes == 2 && !W1)) return DLITE_ERR_INVALID_ARG;
   if (xplanes == 1 && wplanes == 2) return DLITE_ERR_INVALID_ARG;  // plane products x0w0 (+x1w0) (+x0w1)
   const int wrows = (outs + 63) / 64 * 64;
-  if (!plan_override && tc::use_stream_engine(rows, xplanes, wplanes)) {  // the round's route
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return DLITE_ERR_CUDA;
-    const tc::StreamPlan sp = tc::stream_plan(rows, outs, K, sms);
-    if (sp.ok) {
-      CUtensorMap mx, mw;
-      if (!tc::make_map(&mx, X0, x_rows, K, sp.x_box) || !tc::make_map_tiled(&mw, W0, wrows, K, sp.N))
-        return DLITE_ERR_CUDA;
-      tc::StreamParams prm;
-      prm.rows = rows;
-      prm.outs = outs;
-      prm.part = part;
-      prm.status = status;
-      CK(tc::launch_stream(sp, &mx, &mw, prm, (cudaStream_t)stream));
-      return sp.S;
-    }
-  }
   if (!plan_override && tc::use_pair_engine(rows, xplanes, wplanes)) {  // the round's route
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -1693,7 +1677,10 @@ int dlite_launch_count(dlite_handle* h, int B, float temperature) {
   if (h->gated)  // head: {W_h u product, sum} + K x {prep, state product, gate, r product, r, lm, merge} + final
                  // (+ {prep, state product, gate} of the warm-up)
     return 1 + per_layer * h->cfg.L_D + hist + 2 + 7 * h->cfg.K + 1 + 1 + (h->cfg.head_warmup ? 3 : 0);
-  return 1 + per_layer * h->cfg.L_D + hist + 4 + 2 + 1;
+  // head {ce, chain, P + residual} (+ out when no single-split plan fits the P product)
+  const int head = B * h->cfg.K <= 64 && tc::plan(B * h->cfg.K, h->cfg.D, h->Rp, 2, h->np, false, true).ok &&
+                   h->cfg.D % 16 == 0 ? 3 : 4;
+  return 1 + per_layer * h->cfg.L_D + hist + head + 2 + 1;
 }
 
 }  // extern "C"

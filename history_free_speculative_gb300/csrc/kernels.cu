@@ -69,6 +69,34 @@ __device__ __forceinline__ float4 sum_splits4(const float* base, size_t stride, 
   return acc;
 }
 
+// One float4 of a split-K product: its first plane, the plane stride, the planes.
+struct SplitSrc {
+  const float* p = nullptr;
+  size_t stride = 0;
+  int n = 0;
+};
+// Two such sums at once: up to kDepth loads of each in flight together, each
+// sum added in plane order from zero (the same result as sum_splits4).
+template <int kDepth>
+__device__ __forceinline__ void sum_splits4x2(const SplitSrc& s0, const SplitSrc& s1, float4& r0, float4& r1) {
+  r0 = make_float4(0.f, 0.f, 0.f, 0.f);
+  r1 = r0;
+  const int nmax = s0.n > s1.n ? s0.n : s1.n;
+  for (int s = 0; s < nmax; s += kDepth) {
+    float4 t0[kDepth], t1[kDepth];
+#pragma unroll
+    for (int k = 0; k < kDepth; ++k) {
+      if (s + k < s0.n) t0[k] = *reinterpret_cast<const float4*>(s0.p + (size_t)(s + k) * s0.stride);
+      if (s + k < s1.n) t1[k] = *reinterpret_cast<const float4*>(s1.p + (size_t)(s + k) * s1.stride);
+    }
+#pragma unroll
+    for (int k = 0; k < kDepth; ++k) {
+      if (s + k < s0.n) r0 = f4add(r0, t0[k]);
+      if (s + k < s1.n) r1 = f4add(r1, t1[k]);
+    }
+  }
+}
+
 __device__ __forceinline__ void store4_planes(bf16* const* pl, int n, size_t i, float4 v) {
   store_planes(pl, n, i, v.x);
   store_planes(pl, n, i + 1, v.y);
@@ -218,36 +246,64 @@ __global__ void __launch_bounds__(kAttnThreads, kMinCtas) attention_kernel(AttnA
   float* ps = vs + Tkp * LD;   // [QRp][LP] scores, then probabilities
   const size_t sl = (size_t)(a.loc_rows ? a.loc_rows : a.B * K1) * ldl;
   const size_t sc = (size_t)(a.ctx_rows ? a.ctx_rows : a.B * a.m) * ldc;
-  auto loc4 = [&](int row, int col) {
-    return sum_splits4<kDepth>(a.part_loc + (size_t)(b * K1 + row) * ldl + col, sl,
-                               splits_at(a.sp_loc, b * K1 + row, col));
-  };
-  auto ctx4 = [&](int row, int col) {
-    const int r = a.ctx_row0 + b * a.m + row, c = a.ctx_col0 + col;
-    return sum_splits4<kDepth>(a.part_ctx + (size_t)r * ldc + c, sc, splits_at(a.sp_ctx, r, c));
-  };
   auto rnd4 = [&](float4 v) {
     return a.round_bf16 ? make_float4(round_bf16(v.x), round_bf16(v.y), round_bf16(v.z), round_bf16(v.w)) : v;
   };
   const int h4 = half / 4, d4 = dh / 4;
   const int nq = G * K1 * d4, nk = K1 * d4, nv = K1 * d4, nc = a.m * d4;
-  // 1) every float4 of the block's rows summed over the split planes (one
-  //    split sum per item keeps the registers low: two CTAs per SM)
-  for (int idx = threadIdx.x; idx < nq + nk + nv + 2 * nc; idx += blockDim.x) {
+  // the source (first split plane, plane stride, planes) and the shared-memory
+  // destination of item idx: a float4 of a query, local key / value or context
+  // key / value row; values are rounded like the keys and queries (after RoPE)
+  auto item = [&](int idx, SplitSrc& src, float*& dst, bool& rnd) {
+    int row, col;
+    bool ctx = false;
+    rnd = false;
     if (idx < nq) {  // queries of the group's heads (rotated below)
-      const int d = (idx % d4) * 4, r = idx / d4, hh = r / K1, i = r % K1;
-      *reinterpret_cast<float4*>(qs + r * LD + d) = loc4(i, (h0 + hh) * dh + d);
+      const int d = (idx % d4) * 4, r = idx / d4, hh = r / K1;
+      row = r % K1, col = (h0 + hh) * dh + d;
+      dst = qs + r * LD + d;
     } else if (idx < nq + nk) {  // local keys (rotated below)
-      const int t = idx - nq, d = (t % d4) * 4, i = t / d4;
-      *reinterpret_cast<float4*>(ks + (a.m + i) * LD + d) = loc4(i, qd + g * dh + d);
+      const int t = idx - nq, d = (t % d4) * 4;
+      row = t / d4, col = qd + g * dh + d;
+      dst = ks + (a.m + row) * LD + d;
     } else if (idx < nq + nk + nv) {  // local values
-      const int t = idx - nq - nk, d = (t % d4) * 4, i = t / d4;
-      *reinterpret_cast<float4*>(vs + (a.m + i) * LD + d) = rnd4(loc4(i, qd + kvd + g * dh + d));
+      const int t = idx - nq - nk, d = (t % d4) * 4;
+      row = t / d4, col = qd + kvd + g * dh + d;
+      dst = vs + (a.m + row) * LD + d;
+      rnd = true;
     } else {  // context keys / values: local position 0, no rotation
-      const int t = idx - nq - nk - nv, kv = t / nc, r = t % nc, d = (r % d4) * 4, j = r / d4;
-      float* dst = (kv ? vs : ks) + j * LD + d;
-      *reinterpret_cast<float4*>(dst) = rnd4(ctx4(j, kv * kvd + g * dh + d));
+      const int t = idx - nq - nk - nv, kv = t / nc, r = t % nc, d = (r % d4) * 4;
+      row = r / d4, col = kv * kvd + g * dh + d;
+      dst = (kv ? vs : ks) + row * LD + d;
+      ctx = true;
+      rnd = true;
     }
+    if (ctx) {
+      const int rr = a.ctx_row0 + b * a.m + row, cc = a.ctx_col0 + col;
+      src.p = a.part_ctx + (size_t)rr * ldc + cc;
+      src.stride = sc;
+      src.n = splits_at(a.sp_ctx, rr, cc);
+    } else {
+      src.p = a.part_loc + (size_t)(b * K1 + row) * ldl + col;
+      src.stride = sl;
+      src.n = splits_at(a.sp_loc, b * K1 + row, col);
+    }
+  };
+  // 1) every float4 of the block's rows summed over the split planes, two
+  //    items per thread at a time with both items' plane loads in flight
+  const int n_items = nq + nk + nv + 2 * nc;
+  for (int idx = threadIdx.x; idx < n_items; idx += 2 * blockDim.x) {
+    SplitSrc s0, s1;
+    float *d0, *d1 = nullptr;
+    bool r0, r1 = false;
+    item(idx, s0, d0, r0);
+    const bool two = idx + (int)blockDim.x < n_items;
+    if (two) item(idx + blockDim.x, s1, d1, r1);
+    else s1.n = 0;
+    float4 v0, v1;
+    sum_splits4x2<kDepth>(s0, s1, v0, v1);
+    *reinterpret_cast<float4*>(d0) = r0 ? rnd4(v0) : v0;
+    if (two) *reinterpret_cast<float4*>(d1) = r1 ? rnd4(v1) : v1;
   }
   __syncthreads();
   // padding rows of the tensor-core tiles hold zeros

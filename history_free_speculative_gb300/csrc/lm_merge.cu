@@ -67,10 +67,10 @@ __device__ __forceinline__ void topk_insert(float (&sc)[kTopK], int (&id)[kTopK]
 
 // Partial exact logit of id v over columns [lo, hi) (fp32 accumulation; the
 // warp's lanes take 4 columns each per 128, all loads issued before use).
+template <int kU>
 __device__ __forceinline__ float exact_logit_part(const LmMergeArgs& a, int v, const float* h, int lo, int hi) {
   const int lane = threadIdx.x & 31;
   float acc0 = 0.f, acc1 = 0.f;
-  constexpr int kU = 8;
   for (int d0 = lo + lane * 4; d0 < hi; d0 += 128 * kU) {
     float4 ev[kU], hv[kU];
 #pragma unroll
@@ -205,11 +205,15 @@ __device__ __forceinline__ float gumbel_f(uint32_t x) {
   return -logf(nl);
 }
 
-template <int kMergeWarps>
-__global__ void __launch_bounds__(kMergeWarps * 32, 2) lm_merge_kernel(const LmMergeArgs a) {
+// kSampling: the sampling form (<= 128 registers: two CTAs per SM, as many rows
+// as there are; no early launch of the successor: the sampling verification's
+// CTAs waiting on these SMs slowed this kernel by about 2x); the greedy form
+// (few rows in practice; deeper loads for the finalists, the successor may
+// launch early).
+template <int kMergeWarps, bool kSampling>
+__global__ void __launch_bounds__(kMergeWarps * 32, kSampling ? 2 : 1) lm_merge_kernel(const LmMergeArgs a) {
   static_assert(kMergeWarps == 2 * kTopK, "two warps per finalist");
-  // no early trigger: the verification kernel that follows would wait on
-  // these SMs (its CTAs slowed this kernel by about 2x when launched early)
+  if (!kSampling) pdl_trigger();
   pdl_wait();
   __shared__ float wsc[kMergeWarps][kTopK];
   __shared__ int wid[kMergeWarps][kTopK];
@@ -221,7 +225,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 2) lm_merge_kernel(const LmM
   __shared__ float chunk_part[kMergeWarps][kChunk];
   const int r = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const bool sampling = a.inv_T > 0.f;
+  constexpr bool sampling = kSampling;
   float sc[kTopK];
   int id[kTopK];
 #pragma unroll
@@ -284,7 +288,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 2) lm_merge_kernel(const LmM
   }
   __syncthreads();
   const float* h = a.h + (size_t)r * a.D;
-  if (sampling) {
+  if constexpr (kSampling) {
     // exact logits of the finalist chunks in the band (a prefix of the sorted
     // finalists): every warp takes a slice of the columns of all 16 ids, the
     // warps' partials are added in warp order
@@ -375,7 +379,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 2) lm_merge_kernel(const LmM
     const int half = (a.D / 2 + 3) & ~3;
     const int lo = (warp & 1) ? half : 0, hi = (warp & 1) ? a.D : half;
     float p = 0.f;
-    if (v >= 0 && v < a.V) p = exact_logit_part(a, v, h, lo, hi);  // fewer than kTopK ids on tiny vocabularies
+    if (v >= 0 && v < a.V) p = exact_logit_part<16>(a, v, h, lo, hi);  // fewer than kTopK ids on tiny vocabularies
     if (lane == 0) part[warp] = p;
   }
   __syncthreads();
@@ -412,7 +416,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 2) lm_merge_kernel(const LmM
 }
 
 cudaError_t launch_lm_merge(const LmMergeArgs& a, cudaStream_t s) {
-  return launch_pdl(lm_merge_kernel<2 * kTopK>, dim3(a.rows), dim3(2 * kTopK * 32), 0, s, a);
+  if (a.inv_T > 0.f) return launch_pdl(lm_merge_kernel<2 * kTopK, true>, dim3(a.rows), dim3(2 * kTopK * 32), 0, s, a);
+  return launch_pdl(lm_merge_kernel<2 * kTopK, false>, dim3(a.rows), dim3(2 * kTopK * 32), 0, s, a);
 }
 
 }  // namespace dlite

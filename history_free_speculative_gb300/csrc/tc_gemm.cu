@@ -237,6 +237,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               }
             }
           }
+        } else if (p.mode == 3) {
+          // residual: lane = row stores res + product of its row's 16 columns per
+          // chunk as fp32 (and the tap) and as the hi / lo bf16 planes
+          for (int c = c_lo; c < c_hi; c += 16) {
+            uint32_t v0[16];
+            tmem_ld16_nowait(tbase + c, v0);
+            tmem_wait_ld();
+            if (r < p.rows && o0 + c < p.outs) {
+              const size_t idx = (size_t)r * p.outs + o0 + c;  // outs is a multiple of 16 here
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const float4 b4 = *reinterpret_cast<const float4*>(p.res + idx + 4 * k);
+                const float4 v = make_float4(b4.x + __uint_as_float(v0[4 * k]), b4.y + __uint_as_float(v0[4 * k + 1]),
+                                             b4.z + __uint_as_float(v0[4 * k + 2]),
+                                             b4.w + __uint_as_float(v0[4 * k + 3]));
+                *reinterpret_cast<float4*>(p.out32 + idx + 4 * k) = v;
+                if (p.tap32) *reinterpret_cast<float4*>(p.tap32 + idx + 4 * k) = v;
+                bf16 h[4], l[4];
+                split_bf16(v.x, h[0], l[0]);
+                split_bf16(v.y, h[1], l[1]);
+                split_bf16(v.z, h[2], l[2]);
+                split_bf16(v.w, h[3], l[3]);
+                *reinterpret_cast<uint2*>(p.act[0] + idx + 4 * k) = *reinterpret_cast<const uint2*>(h);
+                *reinterpret_cast<uint2*>(p.act[1] + idx + 4 * k) = *reinterpret_cast<const uint2*>(l);
+              }
+            }
+          }
         } else if (p.mode == 2) {
           // SwiGLU: the slab's columns come in blocks of 64, [32 gate | 32 up] of the
           // same 32 features; lane = row stores a = silu(gate) * up of its row's 32

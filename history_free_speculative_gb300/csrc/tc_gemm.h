@@ -37,7 +37,8 @@ struct TcParams {
   uint32_t stage_bytes = 0, tmem_cols = 32;
   int x_box = 128;         // rows of each activation tile load (<= 128, multiple of 8)
   int mode = 0;            // 0: fp32 partials [split][rows][outs]; 1: LM-head records;
-                           // 2: SwiGLU of gate / up columns interleaved in blocks of 32 (one split)
+                           // 2: SwiGLU of gate / up columns interleaved in blocks of 32 (one split);
+                           // 3: out32 = res + product as fp32 and as two bf16 planes act[0..1] (one split)
   float* part = nullptr;
   bf16* act[2] = {nullptr, nullptr};  // mode 2: a = silu(gate) * up, [rows, outs / 2] bf16 planes
   int act_planes = 1;
@@ -48,6 +49,9 @@ struct TcParams {
   int K_draft = 1;
   int* status = nullptr;
   int tma_out = 0;         // mode 0: partials leave through bulk tensor stores (the out map)
+  const float* res = nullptr;  // mode 3: [rows, outs] addend
+  float* out32 = nullptr;      // mode 3: [rows, outs] result
+  float* tap32 = nullptr;      // mode 3: optional copy of the result
   // mode 0: a CTA whose rows all lie at or past skip_row0 (> 0) and whose
   // columns all lie before skip_cols does nothing (a product over stacked
   // operands whose lower rows need only the upper columns)
@@ -113,31 +117,6 @@ struct PairParams {
   float* part = nullptr;
   int* status = nullptr;
 };
-// Persistent stream-K GEMM for <= 128 rows (bf16 operands): grid = G CTAs (one
-// per SM); W maps with N-row boxes, X maps with x_box-row boxes; partials laid
-// out as stream_splits() describes.
-struct StreamPlan {
-  bool ok = false;
-  int N = 0, x_box = 0, kblocks = 0, slabs = 0, stages = 0, G = 0, S = 1;
-  uint32_t stage_bytes = 0;
-  size_t tail_pad = 0;
-  long long U = 0;
-};
-struct StreamParams {
-  int rows = 0, outs = 0;
-  int kblocks = 0, stages = 0, x_box = 8, G = 1;
-  uint32_t stage_bytes = 0;
-  long long U = 1;
-  float* part = nullptr;
-  int* status = nullptr;
-};
-bool use_stream_engine(int rows, int xplanes, int wplanes);
-StreamPlan stream_plan(int rows, int outs, int K, int num_sms);
-Splits stream_splits(const StreamPlan& pl);
-size_t stream_smem_bytes(const StreamPlan& pl);
-cudaError_t launch_stream(const StreamPlan& pl, const CUtensorMap* x, const CUtensorMap* w, StreamParams prm,
-                          cudaStream_t s);
-
 bool use_pair_engine(int rows, int xplanes, int wplanes);
 PairPlan pair_plan(int rows, int outs, int K, int num_sms);
 Splits pair_splits(const PairPlan& pl);

@@ -420,7 +420,7 @@ int dlite_stage_times(dlite_handle *h, int B, const void *hidden, const int32_t 
  * hold 16 * rows * outs floats; the sum over the returned number of splits
  * (> 0) is the product. `status` is a device int receiving DLITE_DEV_* bits.
  * plan_override: NULL selects what the round uses (one bf16 plane on each side
- * and more than 128 rows: the CTA-pair engine with 2-SM MMAs; otherwise the
+ * and more than 512 rows: the CTA-pair engine with 2-SM MMAs; otherwise the
  * one-CTA engine with the planner's tiling); a host int[3] {slab width N,
  * k splits, pipeline stages} (0 = planner's choice) forces the one-CTA engine
  * with that tiling, for sweeps.

@@ -33,3 +33,32 @@ def f64_weights(W):
     out = {k: f64(v) for k, v in W.items() if k != "layers"}
     out["layers"] = [{k: f64(v) for k, v in l.items()} for l in W["layers"]]
     return out
+
+
+def check_candidates_bf16(cand, ocand, ogap, E, h_gpu, h_mir, own_choice, T=0.0, max_frac=0.02):
+    """Candidates of a drafter with bf16 backbone activations against the mirror oracle.
+
+    Both round the activations to bf16 at the same points, but once an input of
+    one rounding differs in its last fp32 bits (another accumulation order) the
+    two sides' rounding decisions decorrelate: the head states differ by a
+    bf16-noise amount and a near-tie can go either way. Each mismatch must
+    (1) be the exact choice of the drafter's own head state, own_choice(n, i,
+    E h_gpu[n, i]) in float64, and (2) sit where the mirror's gap is within
+    reach of the head-state difference: a logit shift of at most
+    s = max_v |E (h_gpu - h_mir)| moves a greedy top-2 gap by at most 2 s, a
+    chunk-score gap of the two-level draw by at most 2 s / T and a CDF step
+    inside a chunk by at most exp(2 s / T) - 1. At most max_frac of the
+    candidates may differ (one on samples under 1 / max_frac).
+    """
+    cand, ocand, ogap = np.asarray(cand), np.asarray(ocand), np.asarray(ogap)
+    E = np.asarray(E, dtype=np.float64)
+    bad = np.argwhere(cand != ocand)
+    for n, i in bad:
+        hg = np.asarray(h_gpu[n][i], dtype=np.float64)
+        assert own_choice(n, i, E @ hg) == cand[n, i], ("not the exact choice of its own head state", n, i)
+        s = float(np.abs(E @ (hg - np.asarray(h_mir[n][i], dtype=np.float64))).max())
+        reach = 2.0 * s if T == 0 else float(np.expm1(2.0 * s / T))
+        assert ogap[n, i] < reach, ("a gap the head-state difference cannot bridge", n, i, ogap[n, i], reach)
+    allowed = max(1, int(max_frac * cand.size))
+    assert len(bad) <= allowed, f"{len(bad)} of {cand.size} candidates differ"
+    return len(bad)

@@ -94,3 +94,4 @@ def test_engine_plans_match_float64(N, S, rows):
     scale = np.sqrt(K) * np.abs(w64).max() * np.abs(x64).max()
     assert np.isfinite(got).all()
     assert np.abs(got - ref).max() <= 1e-5 * scale
+

@@ -15,7 +15,7 @@ from history_free_speculative_gb300 import binding
 from history_free_speculative_gb300 import workload as wk
 from oracle import dlite_oracle as O
 from oracle import philox as ph
-from parity import HIDDEN_REL_TOL, check_candidates, f64_weights, rel_err
+from parity import HIDDEN_REL_TOL, check_candidates, check_candidates_bf16, f64_weights, rel_err
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -778,7 +778,9 @@ def test_history_fill_matches_oracle(name):
 @pytest.mark.parametrize("name,H", [("d128", 300), ("d128", 64), ("d64", 200), ("d64", 12), ("d128wide", 150)])
 def test_history_round_parity(name, H):
     """Three rounds of the history-KV control (the 12-row ring wraps): hidden rows and candidates against
-    the oracle drafter attending over its own ring, then each ring after the
+    the oracle drafter attending over its own ring (bf16 activations: a differing
+    candidate must be the exact choice of the drafter's own head state at a
+    near-tie that the head-state difference explains), then each ring after the
     append (slots no round has written bit-exact, the written rows within the
     hidden tolerance: the appended rows are the drafter's own) and the cursors."""
     cfg = _history_cfg(name, H)
@@ -787,6 +789,7 @@ def test_history_round_parity(name, H):
     B = 4
     dr = _drafter(cfg, W, B_max=B)
     K1 = cfg.G + cfg.K
+    E64 = O.f64(W["E"])
     try:
         hist = [O.HistoryCache(cfg, H, b) for b in range(B)]
         written = np.zeros((B, H), dtype=bool)
@@ -802,7 +805,7 @@ def test_history_round_parity(name, H):
                            taps=taps)
             torch.cuda.synchronize()
             cursor0 = [hc.cursor for hc in hist]
-            cands, ocands, gaps = [], [], []
+            cands, ocands, gaps, hmir = [], [], [], []
             for b in range(B):
                 t = {}
                 r = O.draft_request(hidden[b], int(anchor[b]), W, cfg, taps=t, mirror=True, history=hist[b])
@@ -812,7 +815,9 @@ def test_history_round_parity(name, H):
                 cands.append(out["cand"][b].cpu().numpy())
                 ocands.append(r["cand"])
                 gaps.append(r["gap"])
-            check_candidates(np.stack(cands), np.stack(ocands), np.stack(gaps))
+                hmir.append(t["h"])
+            check_candidates_bf16(np.stack(cands), np.stack(ocands), np.stack(gaps), E64,
+                                  taps["hs"].cpu().numpy(), hmir, lambda n, i, ell: int(np.argmax(ell)))
             for b in range(B):
                 written[b, (cursor0[b] + np.arange(K1)) % H] = True   # rows of this and earlier rounds
                 slots, keep = written[b], ~written[b]
