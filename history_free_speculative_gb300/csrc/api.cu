@@ -69,9 +69,9 @@ struct dlite_handle {
   const bf16 *Ws[2] = {nullptr, nullptr}, *Whs[2] = {nullptr, nullptr}, *Whu[2] = {nullptr, nullptr},
              *Wo[2] = {nullptr, nullptr};     // tiled planes: [2R, 2R], [R, R], [R, D], [Vp, R]
   float *ER32 = nullptr, *bs32 = nullptr, *bh32 = nullptr, *Wo32 = nullptr;  // fp32 (Wo32: fp32 drafters)
-  int Bcap = 0;                             // B_max padded to 128 (activation rows of the step products)
+  int Bcap = 0;                             // B_max padded to 128 (rows of the vocabulary product's r operand)
   float *g_s = nullptr, *g_hu = nullptr, *g_r = nullptr, *g_rstep = nullptr;
-  bf16 *g_xp[2] = {nullptr, nullptr}, *g_sp[2] = {nullptr, nullptr}, *g_rp = nullptr;
+  bf16* g_rp = nullptr;
   int32_t* g_cand = nullptr;
   dlite_qstats* g_qs = nullptr;
   int64_t* g_pos = nullptr;
@@ -783,10 +783,11 @@ int run_gated_head(dlite_handle* h, int B, const int32_t* anchor, float temperat
   g.bh = h->bh32;
   g.hu = h->g_hu;
   g.s = h->g_s;
-  g.xp[0] = h->g_xp[0];
-  g.xp[1] = h->g_xp[1];
-  g.sp[0] = h->g_sp[0];
-  g.sp[1] = h->g_sp[1];
+  g.Ws[0] = h->Ws[0];
+  g.Ws[1] = h->Ws[1];
+  g.Whs[0] = h->Whs[0];
+  g.Whs[1] = h->Whs[1];
+  g.np = h->np;
   g.r_all = h->g_r;
   g.r_step = h->g_rstep;
   g.rp = h->g_rp;
@@ -801,22 +802,13 @@ int run_gated_head(dlite_handle* h, int B, const int32_t* anchor, float temperat
   op.K_draft = 1;
   g.warm = c.head_warmup;
   if (c.head_warmup) {  // s_0: one state update from zero on the token before the anchor, no output
-    CK(launch_gated_prep(g, 0, s));
-    mark(h, "gated_prep");
-    RUN(gemm(h, "gemm_gated_s", opnd(h->g_xp, 2, h->Bcap, 2 * R), opnd(h->Ws, h->np, 2 * R, 2 * R), B, 2 * R,
-             h->part, &S, s));
-    CK(launch_gated_gate(g, h->part, S, s));
-    mark(h, "gated_gate");
+    CK(launch_gated_state(g, 0, s));
+    mark(h, "gated_state");
   }
   for (int i = 1; i <= K; ++i) {
-    CK(launch_gated_prep(g, i, s));
-    mark(h, "gated_prep");
-    RUN(gemm(h, "gemm_gated_s", opnd(h->g_xp, 2, h->Bcap, 2 * R), opnd(h->Ws, h->np, 2 * R, 2 * R), B, 2 * R,
-             h->part, &S, s));
-    CK(launch_gated_gate(g, h->part, S, s));
-    mark(h, "gated_gate");
-    RUN(gemm(h, "gemm_gated_r", opnd(h->g_sp, 2, h->Bcap, R), opnd(h->Whs, h->np, R, R), B, R, h->part, &S, s));
-    CK(launch_gated_r(g, i, h->part, S, s));
+    CK(launch_gated_state(g, i, s));
+    mark(h, "gated_state");
+    CK(launch_gated_r(g, i, s));
     mark(h, "gated_r");
     RUN(run_lm_core(h, B, op, temperature, seed, pos ? h->g_pos : nullptr, h->g_cand, qs ? h->g_qs : nullptr, s));
   }
@@ -1092,12 +1084,10 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
   size_t pe = 0, pe2 = 0, lme = 0;
   for (int B = 1; B <= Bm; ++B) {
     const int L = B * (group_of(&c) + c.K), C = B * c.m, H = B * c.K;
-    const int sites[9][4] = {{L, h->qd + 2 * h->kvd, D, h->xp}, {L, D, h->qd, h->xp},
+    const int sites[7][4] = {{L, h->qd + 2 * h->kvd, D, h->xp}, {L, D, h->qd, h->xp},
                              {L, 2 * F, D, h->xp},               {L, D, F, h->xp},
                              {H, 2 * h->Rp, D, 2},               {H, D, h->Rp, 2},
-                             // the gated head's products (sized whatever the head type)
-                             {H, h->Rp, D, 2},                   {B, 2 * h->Rp, 2 * h->Rp, 2},
-                             {B, h->Rp, h->Rp, 2}};
+                             {H, h->Rp, D, 2}};  // the gated head's W_h u product (sized whatever the head type)
     for (auto& st : sites) {
       const tc::Plan pl = tc::plan(st[0], st[1], st[2], st[3], h->np, false);
       if (!pl.ok) return DLITE_ERR_UNSUPPORTED_SHAPE;
@@ -1139,16 +1129,10 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
   AL(h->tsamp, (size_t)Bm * (c.K + 1));
   if (h->gated) {
     const size_t Bc = (size_t)h->Bcap;
-    AL(h->g_s, (size_t)Bm * R);
+    AL(h->g_s, (size_t)2 * Bm * R);
     AL(h->g_hu, (size_t)Bm * c.K * R);
     AL(h->g_r, (size_t)Bm * c.K * R);
     AL(h->g_rstep, (size_t)Bm * R);
-    for (int p = 0; p < 2; ++p) {
-      AL(h->g_xp[p], Bc * 2 * R);
-      CK(cudaMemset(h->g_xp[p], 0, Bc * 2 * R * 2));
-      AL(h->g_sp[p], Bc * R);
-      CK(cudaMemset(h->g_sp[p], 0, Bc * R * 2));
-    }
     AL(h->g_rp, Bc * R);
     CK(cudaMemset(h->g_rp, 0, Bc * R * 2));
     AL(h->g_cand, (size_t)Bm);
@@ -1674,9 +1658,8 @@ int dlite_launch_count(dlite_handle* h, int B, float temperature) {
   const int per_layer = (fused ? 8 : 9) - (fuse_ctx(h, B) ? 1 : 0);  // one product for [y; z] when fused
   // history-KV control: + {history attention, combine} per layer + the cursor advance
   const int hist = h->H ? 2 * h->cfg.L_D + 1 : 0;
-  if (h->gated)  // head: {W_h u product, sum} + K x {prep, state product, gate, r product, r, lm, merge} + final
-                 // (+ {prep, state product, gate} of the warm-up)
-    return 1 + per_layer * h->cfg.L_D + hist + 2 + 7 * h->cfg.K + 1 + 1 + (h->cfg.head_warmup ? 3 : 0);
+  if (h->gated)  // head: {W_h u product, sum} + K x {state, r, lm, merge} + final (+ the warm-up's state)
+    return 1 + per_layer * h->cfg.L_D + hist + 2 + 4 * h->cfg.K + 1 + (h->cfg.head_warmup ? 1 : 0);
   // head {ce, chain, P + residual} (+ out when no single-split plan fits the P product)
   const int head = B * h->cfg.K <= 64 && tc::plan(B * h->cfg.K, h->cfg.D, h->Rp, 2, h->np, false, true).ok &&
                    h->cfg.D % 16 == 0 ? 3 : 4;

@@ -7,12 +7,13 @@
 //
 // one step at a time because d_i (chosen from l_i) feeds step i + 1. With the
 // warm-up (head_warmup), s_0 is one state update from zero on E_R of the token
-// before the anchor, with no output ([P1] §"官方顺序头具体算了什么"). The two
-// state products and the W_h u part run on the tensor-core GEMM engine, the
-// vocabulary projection on the LM-head kernel (K = R); these kernels do the
-// gather of E_R rows, the gating and the bookkeeping between them.
+// before the anchor, with no output ([P1] §"官方顺序头具体算了什么"). The W_h u
+// part of all K steps runs once on the tensor-core GEMM engine and the
+// vocabulary projection on the LM-head kernel (K = R); each step's state
+// update and r are one small kernel each (below).
 #include "internal.h"
 #include "kernels.h"
+#include "tc_device.cuh"
 
 namespace dlite {
 
@@ -24,80 +25,293 @@ __device__ __forceinline__ float split_sum(const float* part, size_t stride, int
   return acc;
 }
 
-__device__ __forceinline__ void planes2(bf16* const* pl, size_t i, float v) {
-  bf16 hi, lo;
-  split_bf16(v, hi, lo);
-  pl[0][i] = hi;
-  pl[1][i] = lo;
+}  // namespace
+
+// ---------------------------------------------------------------- the step kernels
+// With B requests the two step products are B x 2R x 2R (state) and B x R x R
+// (r): a few tens of MFMA on weights of 2 MB and 0.5 MB (R = 512, bf16), which
+// the vocabulary stream between the steps evicts from L2. Their cost is the
+// latency of fetching those weights, so each runs as one small kernel over a
+// grid of (FB features) x (4 requests) CTAs whose first act, before waiting
+// for the previous kernel, is to request its whole weight slice (FB rows of
+// every 64-column tile: one contiguous run each) with bulk copies into shared
+// memory; the arithmetic then runs on the CUDA cores from shared memory. The
+// state kernel takes the previous token, stages [s_{i-1}; E_R(d_{i-1})], forms
+// [g | c] for its FB features and writes s_i; the r kernel forms r_i for its
+// FB features. Lane (q, ch) of a warp reads the 16-byte chunk ch of row q of a
+// 4-row group (a quarter-warp reads one 128-byte row: no bank conflicts) and
+// keeps the partial sums of every (row, request) of its chunks; a reduce-
+// scatter over the 8 lanes of a row and a sum over the warps in warp order
+// give the products. Weights are read as fp32 (the sum of their bf16 planes).
+// The state is double-buffered by step parity: a step reads all of s_{i-1}
+// while its CTAs write s_i.
+constexpr int kStepRows = 4;   // requests per CTA
+constexpr int kStepWarps = 8;  // the warps split the 64-column tiles
+
+namespace {
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float (&w)[8]) {
+  const uint32_t v[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    w[2 * e] = __uint_as_float(v[e] << 16);
+    w[2 * e + 1] = __uint_as_float(v[e] & 0xffff0000u);
+  }
+}
+
+// 8 weights of a staged row chunk (np bf16 planes, plane stride in elements) as fp32
+template <int NP>
+__device__ __forceinline__ void smem_w8(const bf16* w0, size_t plane_stride, float (&w)[8]) {
+  bf16x8_to_f32(*reinterpret_cast<const uint4*>(w0), w);
+  if (NP == 2) {
+    float lo[8];
+    bf16x8_to_f32(*reinterpret_cast<const uint4*>(w0 + plane_stride), lo);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) w[e] += lo[e];
+  }
+}
+
+__device__ __forceinline__ float dot8(const float (&w)[8], const float (&x)[8]) {
+  float acc = w[0] * x[0];
+#pragma unroll
+  for (int e = 1; e < 8; ++e) acc = fmaf(w[e], x[e], acc);
+  return acc;
+}
+
+// Sum v over the 8 lanes that share lane >> 3, leaving each lane NV / 8 of the
+// sums: lane with chunk index ch keeps indices base + k, k < NV / 8, where
+// base = (ch >> 2 & 1) NV / 2 + (ch >> 1 & 1) NV / 4 + (ch & 1) NV / 8.
+template <int NV>
+__device__ __forceinline__ void reduce_scatter8(float (&v)[NV], int ch) {
+#pragma unroll
+  for (int st = 0; st < 3; ++st) {
+    const int half = NV >> (st + 1);
+    const int bit = (ch >> (2 - st)) & 1;
+#pragma unroll
+    for (int k = 0; k < half; ++k) {
+      const float keep = bit ? v[half + k] : v[k];
+      const float send = bit ? v[k] : v[half + k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 4 >> st);
+    }
+  }
+}
+
+// Request rows r0 .. r0 + FB - 1 of every 64-column tile of a tiled [*, cols]
+// matrix (np planes) into dst [plane][tile][FB][64]; thread 0 only.
+template <int NP, int FB>
+__device__ __forceinline__ void request_slice(const bf16* const* W, int r0, int cols, bf16* dst, uint32_t bar,
+                                              int n_tiles_before) {
+  const int nkt = cols / 64;
+  for (int p = 0; p < NP; ++p)
+    for (int t = 0; t < nkt; ++t)
+      tc::bulk_load(tc::su32(dst + ((size_t)(p * n_tiles_before) + t) * FB * 64),
+                    W[p] + tiled_index((size_t)r0, (size_t)t * 64, (size_t)cols), FB * 128, bar);
 }
 
 }  // namespace
 
-// Step i prep, one CTA per request: the previous token (the anchor at i = 1,
-// else the previous step's choice, which is also stored into cand / qs), the
-// step's RNG positions, and the product input [s_{i-1}; E_R[d_{i-1}]] as two
-// bf16 planes (fp32 precision through the tensor cores). i = 0 is the warm-up
-// step: the token before the anchor on the zero state, no bookkeeping.
-__global__ void gated_prep_kernel(GatedArgs a, int i) {
+// Step i (0: the warm-up on the token before the anchor, no output; 1: the
+// anchor; then the previous step's choice, which is also stored into cand / qs):
+// [g | c] = W_s [s_{i-1}; E_R(d_{i-1})] + b_s, s_i = f s_{i-1} + (1 - f) tanh(c).
+// Shared memory: [NP][g | c][2R / 64][FB][64] bf16, [4][2R] fp32 inputs,
+// [8][2][FB][4] fp32 warp sums.
+template <int NP>
+__global__ void __launch_bounds__(kStepWarps * 32) gated_state_kernel(GatedArgs a, int i) {
+  constexpr int FB = 32 / NP;  // features per CTA
+  constexpr int NV = 2 * FB;   // partial sums per lane: (g | c) x (FB / 4 rows) x 4 requests
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int tok[kStepRows];
+  __shared__ int ok_s;
+  const int R = a.R, R2 = 2 * R, K = a.K, nkt = R2 / 64;
+  bf16* wsm = reinterpret_cast<bf16*>(smem);
+  const size_t plane = (size_t)2 * nkt * FB * 64;  // elements per staged plane
+  float* xs = reinterpret_cast<float*>(smem + NP * plane * 2);
+  float* red = xs + kStepRows * R2;
+  const int j0 = blockIdx.x * FB, b0 = blockIdx.y * kStepRows;
+  const int nb = min(kStepRows, a.B - b0);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = lane >> 3, ch = lane & 7;
+  const uint32_t bar_a = tc::su32(&bar);
+  if (threadIdx.x == 0) {  // the weights do not depend on the previous kernel
+    tc::mbar_init(bar_a, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    tc::mbar_expect_tx(bar_a, (uint32_t)(NP * 2 * nkt * FB * 128));
+    for (int gc = 0; gc < 2; ++gc)  // g rows j0.., c rows R + j0..
+      request_slice<NP, FB>(a.Ws, gc * R + j0, R2, wsm + (size_t)gc * nkt * FB * 64, bar_a, 2 * nkt);
+  }
   pdl_trigger();
   pdl_wait();
-  const int b = blockIdx.x, R = a.R, K = a.K;
-  int d = i == 0 ? a.anchor[b * a.G + a.G - 2] : i == 1 ? a.anchor[b * a.G + a.G - 1] : a.cand_tmp[b];
-  if (d < 0 || d >= a.V) {
-    if (threadIdx.x == 0) flag_status(a.status, kDevBounds);
-    d = 0;
+  if (threadIdx.x < kStepRows) {
+    const int b = b0 + threadIdx.x;
+    int d = 0;
+    if (b < a.B) {
+      d = i == 0 ? a.anchor[b * a.G + a.G - 2] : i == 1 ? a.anchor[b * a.G + a.G - 1] : a.cand_tmp[b];
+      if (d < 0 || d >= a.V) {
+        flag_status(a.status, kDevBounds);
+        d = 0;
+      }
+    }
+    tok[threadIdx.x] = d;
   }
-  if (threadIdx.x == 0 && i >= 1) {
+  if (blockIdx.x == 0 && threadIdx.x < nb && i >= 1) {  // the step's bookkeeping, once per request
+    const int b = b0 + threadIdx.x;
     if (i > 1) {
       a.cand[b * K + i - 2] = a.cand_tmp[b];
       if (a.qs) a.qs[b * K + i - 2] = a.qs_tmp[b];
     }
     if (a.pos) a.pos_i[b] = a.pos[b] + (i - 1);
   }
+  __syncthreads();
   // the state starts with the block (at the warm-up step when there is one)
   const bool fresh = i == 0 || (i == 1 && !a.warm);
-  for (int j = threadIdx.x; j < R; j += blockDim.x) {
-    float s = 0.f;
-    if (fresh)
-      a.s[(size_t)b * R + j] = 0.f;
-    else
-      s = a.s[(size_t)b * R + j];
-    planes2(a.xp, (size_t)b * 2 * R + j, s);
-    planes2(a.xp, (size_t)b * 2 * R + R + j, a.ER[(size_t)d * R + j]);
+  const float* s_prev = a.s + (size_t)((i & 1) ^ 1) * a.B * R;
+  for (int e = threadIdx.x; e < kStepRows * R2 / 4; e += blockDim.x) {
+    const int r = e / (R2 / 4), k = (e % (R2 / 4)) * 4;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r < nb) {
+      if (k >= R)
+        v = *reinterpret_cast<const float4*>(a.ER + (size_t)tok[r] * R + k - R);
+      else if (!fresh)
+        v = *reinterpret_cast<const float4*>(s_prev + (size_t)(b0 + r) * R + k);
+    }
+    *reinterpret_cast<float4*>(xs + r * R2 + k) = v;
+  }
+  if (threadIdx.x == 0) ok_s = tc::mbar_wait(bar_a, 0, a.status);
+  __syncthreads();
+  if (!ok_s) {  // the weights did not arrive in time (status flagged): let the copies land, then leave
+    if (threadIdx.x == 0) tc::mbar_wait(bar_a, 0, nullptr);
+    return;
+  }
+  float v[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) v[k] = 0.f;
+  for (int t = warp; t < nkt; t += kStepWarps) {
+    float x[kStepRows][8];
+#pragma unroll
+    for (int b = 0; b < kStepRows; ++b) {
+      const float4 x0 = *reinterpret_cast<const float4*>(xs + b * R2 + t * 64 + ch * 8);
+      const float4 x1 = *reinterpret_cast<const float4*>(xs + b * R2 + t * 64 + ch * 8 + 4);
+      x[b][0] = x0.x, x[b][1] = x0.y, x[b][2] = x0.z, x[b][3] = x0.w;
+      x[b][4] = x1.x, x[b][5] = x1.y, x[b][6] = x1.z, x[b][7] = x1.w;
+    }
+#pragma unroll
+    for (int gc = 0; gc < 2; ++gc)
+#pragma unroll
+      for (int rg = 0; rg < FB / 4; ++rg) {
+        float w[8];
+        smem_w8<NP>(wsm + ((size_t)gc * nkt + t) * FB * 64 + (rg * 4 + q) * 64 + ch * 8, plane, w);
+#pragma unroll
+        for (int b = 0; b < kStepRows; ++b) v[(gc * (FB / 4) + rg) * 4 + b] += dot8(w, x[b]);
+      }
+  }
+  reduce_scatter8<NV>(v, ch);
+#pragma unroll
+  for (int k = 0; k < NV / 8; ++k) {
+    const int idx = ((ch >> 2) & 1) * (NV / 2) + ((ch >> 1) & 1) * (NV / 4) + (ch & 1) * (NV / 8) + k;
+    const int gc = idx / FB, rg = (idx % FB) / 4, b = idx % 4;
+    red[((warp * 2 + gc) * FB + rg * 4 + q) * kStepRows + b] = v[k];
+  }
+  __syncthreads();
+  if (threadIdx.x < FB * kStepRows) {
+    const int l = threadIdx.x / kStepRows, r = threadIdx.x % kStepRows;
+    if (r < nb) {
+      float g = 0.f, c = 0.f;
+#pragma unroll
+      for (int w = 0; w < kStepWarps; ++w) {
+        g += red[((w * 2 + 0) * FB + l) * kStepRows + r];
+        c += red[((w * 2 + 1) * FB + l) * kStepRows + r];
+      }
+      const int j = j0 + l;
+      g += a.bs[j];
+      c += a.bs[R + j];
+      const float f = 1.f / (1.f + expf(-g));
+      const float sp = xs[r * R2 + j];  // s_{i-1}[j] (zero for a fresh state)
+      a.s[(size_t)(i & 1) * a.B * R + (size_t)(b0 + r) * R + j] = f * sp + (1.f - f) * tanhf(c);
+    }
   }
 }
 
-// [g | c] = sum of the split planes + b_s; s_i = f s_{i-1} + (1 - f) tanh(c)
-__global__ void gated_gate_kernel(GatedArgs a, const float* part, Splits sp) {
-  pdl_trigger();
-  pdl_wait();
-  const int b = blockIdx.x, R = a.R;
-  const size_t stride = (size_t)a.B * 2 * R;
-  for (int j = threadIdx.x; j < R; j += blockDim.x) {
-    const size_t ig = (size_t)b * 2 * R + j, ic = ig + R;
-    const float g = split_sum(part, stride, splits_at(sp, b, j), ig) + a.bs[j];
-    const float c = split_sum(part, stride, splits_at(sp, b, R + j), ic) + a.bs[R + j];
-    const float f = 1.f / (1.f + expf(-g));
-    const float s = f * a.s[(size_t)b * R + j] + (1.f - f) * tanhf(c);
-    a.s[(size_t)b * R + j] = s;
-    planes2(a.sp, (size_t)b * R + j, s);
-  }
-}
-
-// r_i = W_hs s_i (split planes) + (W_hu u_i) + b_h: kept in fp32 (all steps, for
+// r_i = W_hs s_i + (W_hu u_i) + b_h: kept in fp32 (all steps, for
 // verification; this step's, for the exact re-scoring) and as the bf16
-// activation of the vocabulary projection
-__global__ void gated_r_kernel(GatedArgs a, int i, const float* part, Splits sp) {
+// activation of the vocabulary projection. Shared memory: [NP][R / 64][FB][64]
+// bf16, [4][R] fp32 states, [8][FB][4] fp32 warp sums.
+template <int NP>
+__global__ void __launch_bounds__(kStepWarps * 32) gated_r_kernel(GatedArgs a, int i) {
+  constexpr int FB = 32 / NP;
+  constexpr int NV = FB;  // (FB / 4 rows) x 4 requests
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int ok_s;
+  const int R = a.R, K = a.K, nkt = R / 64;
+  bf16* wsm = reinterpret_cast<bf16*>(smem);
+  const size_t plane = (size_t)nkt * FB * 64;
+  float* xs = reinterpret_cast<float*>(smem + NP * plane * 2);
+  float* red = xs + kStepRows * R;
+  const int j0 = blockIdx.x * FB, b0 = blockIdx.y * kStepRows;
+  const int nb = min(kStepRows, a.B - b0);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = lane >> 3, ch = lane & 7;
+  const uint32_t bar_a = tc::su32(&bar);
+  if (threadIdx.x == 0) {
+    tc::mbar_init(bar_a, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    tc::mbar_expect_tx(bar_a, (uint32_t)(NP * nkt * FB * 128));
+    request_slice<NP, FB>(a.Whs, j0, R, wsm, bar_a, nkt);
+  }
   pdl_trigger();
   pdl_wait();
-  const int b = blockIdx.x, R = a.R, K = a.K;
-  const size_t stride = (size_t)a.B * R;
-  for (int j = threadIdx.x; j < R; j += blockDim.x) {
-    const size_t row = (size_t)b * K + i - 1;
-    const float r = split_sum(part, stride, splits_at(sp, b, j), (size_t)b * R + j) + a.hu[row * R + j] + a.bh[j];
-    a.r_all[row * R + j] = r;
-    a.r_step[(size_t)b * R + j] = r;
-    a.rp[(size_t)b * R + j] = __float2bfloat16_rn(r);
+  const float* s_i = a.s + (size_t)(i & 1) * a.B * R;
+  for (int e = threadIdx.x; e < kStepRows * R / 4; e += blockDim.x) {
+    const int r = e / (R / 4), k = (e % (R / 4)) * 4;
+    const float4 v = r < nb ? *reinterpret_cast<const float4*>(s_i + (size_t)(b0 + r) * R + k)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+    *reinterpret_cast<float4*>(xs + r * R + k) = v;
+  }
+  if (threadIdx.x == 0) ok_s = tc::mbar_wait(bar_a, 0, a.status);
+  __syncthreads();
+  if (!ok_s) {
+    if (threadIdx.x == 0) tc::mbar_wait(bar_a, 0, nullptr);
+    return;
+  }
+  float v[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) v[k] = 0.f;
+  for (int t = warp; t < nkt; t += kStepWarps) {
+    float x[kStepRows][8];
+#pragma unroll
+    for (int b = 0; b < kStepRows; ++b) {
+      const float4 x0 = *reinterpret_cast<const float4*>(xs + b * R + t * 64 + ch * 8);
+      const float4 x1 = *reinterpret_cast<const float4*>(xs + b * R + t * 64 + ch * 8 + 4);
+      x[b][0] = x0.x, x[b][1] = x0.y, x[b][2] = x0.z, x[b][3] = x0.w;
+      x[b][4] = x1.x, x[b][5] = x1.y, x[b][6] = x1.z, x[b][7] = x1.w;
+    }
+#pragma unroll
+    for (int rg = 0; rg < FB / 4; ++rg) {
+      float w[8];
+      smem_w8<NP>(wsm + (size_t)t * FB * 64 + (rg * 4 + q) * 64 + ch * 8, plane, w);
+#pragma unroll
+      for (int b = 0; b < kStepRows; ++b) v[rg * 4 + b] += dot8(w, x[b]);
+    }
+  }
+  reduce_scatter8<NV>(v, ch);
+#pragma unroll
+  for (int k = 0; k < NV / 8; ++k) {
+    const int idx = ((ch >> 2) & 1) * (NV / 2) + ((ch >> 1) & 1) * (NV / 4) + (ch & 1) * (NV / 8) + k;
+    red[(warp * FB + (idx / 4) * 4 + q) * kStepRows + idx % 4] = v[k];
+  }
+  __syncthreads();
+  if (threadIdx.x < FB * kStepRows) {
+    const int l = threadIdx.x / kStepRows, r = threadIdx.x % kStepRows;
+    if (r < nb) {
+      float acc = 0.f;
+#pragma unroll
+      for (int w = 0; w < kStepWarps; ++w) acc += red[(w * FB + l) * kStepRows + r];
+      const int b = b0 + r, j = j0 + l;
+      const size_t row = (size_t)b * K + i - 1;
+      acc += a.hu[row * R + j] + a.bh[j];
+      a.r_all[row * R + j] = acc;
+      a.r_step[(size_t)b * R + j] = acc;
+      a.rp[(size_t)b * R + j] = __float2bfloat16_rn(acc);
+    }
   }
 }
 
@@ -122,16 +336,32 @@ __global__ void gated_final_kernel(GatedArgs a) {
   if (a.qs) a.qs[b * a.K + a.K - 1] = a.qs_tmp[b];
 }
 
-static int gated_threads(int R) { return R >= 512 ? 512 : (R + 31) / 32 * 32; }
+static size_t state_smem(int R, int np) {
+  const int fb = 32 / np;
+  return (size_t)np * 2 * (2 * R / 64) * fb * 128 + (size_t)kStepRows * 2 * R * 4 + (size_t)kStepWarps * 2 * fb * kStepRows * 4;
+}
+static size_t r_smem(int R, int np) {
+  const int fb = 32 / np;
+  return (size_t)np * (R / 64) * fb * 128 + (size_t)kStepRows * R * 4 + (size_t)kStepWarps * fb * kStepRows * 4;
+}
 
-cudaError_t launch_gated_prep(const GatedArgs& a, int i, cudaStream_t s) {
-  return launch_pdl(gated_prep_kernel, dim3(a.B), dim3(gated_threads(a.R)), 0, s, a, i);
+cudaError_t launch_gated_state(const GatedArgs& a, int i, cudaStream_t s) {
+  if (a.R > 512 || a.R % 64 || a.B < 1 || a.np < 1 || a.np > 2) return cudaErrorInvalidValue;
+  const size_t sm = state_smem(a.R, a.np);
+  auto fn = a.np == 1 ? gated_state_kernel<1> : gated_state_kernel<2>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(fn, dim3(a.R / (32 / a.np), (a.B + kStepRows - 1) / kStepRows), dim3(kStepWarps * 32), sm, s,
+                    a, i);
 }
-cudaError_t launch_gated_gate(const GatedArgs& a, const float* part, const Splits& sp, cudaStream_t s) {
-  return launch_pdl(gated_gate_kernel, dim3(a.B), dim3(gated_threads(a.R)), 0, s, a, part, sp);
-}
-cudaError_t launch_gated_r(const GatedArgs& a, int i, const float* part, const Splits& sp, cudaStream_t s) {
-  return launch_pdl(gated_r_kernel, dim3(a.B), dim3(gated_threads(a.R)), 0, s, a, i, part, sp);
+cudaError_t launch_gated_r(const GatedArgs& a, int i, cudaStream_t s) {
+  if (a.R > 512 || a.R % 64 || a.B < 1 || a.np < 1 || a.np > 2) return cudaErrorInvalidValue;
+  const size_t sm = r_smem(a.R, a.np);
+  auto fn = a.np == 1 ? gated_r_kernel<1> : gated_r_kernel<2>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(fn, dim3(a.R / (32 / a.np), (a.B + kStepRows - 1) / kStepRows), dim3(kStepWarps * 32), sm, s,
+                    a, i);
 }
 cudaError_t launch_gated_sum(const float* part, const Splits& sp, int rows, int cols, float* out,
                              cudaStream_t s) {

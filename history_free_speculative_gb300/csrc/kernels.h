@@ -120,18 +120,18 @@ struct GatedArgs {
   const float* bs = nullptr;         // [2R]
   const float* bh = nullptr;         // [R]
   const float* hu = nullptr;         // [B*K, R] W_h[:, R:] u_i
-  float* s = nullptr;                // [B, R] state
-  bf16* xp[2] = {nullptr, nullptr};  // [B, 2R] planes of [s; v]
-  bf16* sp[2] = {nullptr, nullptr};  // [B, R] planes of s
+  float* s = nullptr;                // [2][B, R] state, double-buffered by step parity
+  const bf16* Ws[2] = {nullptr, nullptr};   // W_s [2R, 2R], tiled bf16 planes
+  const bf16* Whs[2] = {nullptr, nullptr};  // W_h[:, :R] [R, R], tiled bf16 planes
+  int np = 1;                               // weight planes
   float* r_all = nullptr;            // [B*K, R]
   float* r_step = nullptr;           // [B, R]
   bf16* rp = nullptr;                // [B, R] bf16(r) (the vocabulary product's activation)
   int* status = nullptr;
   int warm = 0;                      // s_0 from a warm-up step on the token before the anchor
 };
-cudaError_t launch_gated_prep(const GatedArgs& a, int i, cudaStream_t s);
-cudaError_t launch_gated_gate(const GatedArgs& a, const float* part, const Splits& sp, cudaStream_t s);
-cudaError_t launch_gated_r(const GatedArgs& a, int i, const float* part, const Splits& sp, cudaStream_t s);
+cudaError_t launch_gated_state(const GatedArgs& a, int i, cudaStream_t s);
+cudaError_t launch_gated_r(const GatedArgs& a, int i, cudaStream_t s);
 cudaError_t launch_gated_sum(const float* part, const Splits& sp, int rows, int cols, float* out,
                              cudaStream_t s);
 cudaError_t launch_gated_final(const GatedArgs& a, cudaStream_t s);

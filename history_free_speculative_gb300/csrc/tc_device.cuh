@@ -90,6 +90,13 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t sr
       "r"(src), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
+// 1-D bulk copy global -> shared (both 16-byte aligned, bytes a multiple of 16),
+// completing on mbarrier `bar` (expect_tx beforehand).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until this thread's bulk stores have finished reading shared memory (the
 // buffer may be rewritten) / have been performed completely.
