@@ -179,6 +179,58 @@ __device__ __forceinline__ float chunk_logits_part(const LmMergeArgs& a, int k, 
   return mine;
 }
 
+// Short rows (D <= 512, the gated head's W_o product): the exact logits of
+// every finalist chunk in the band at once, into chunk_l[j][t]. The n_band x 16
+// ids are dealt to the warps round-robin, four ids of a warp at a time with all
+// their loads in flight (one round trip for the usual one or two chunks,
+// instead of one per chunk and half-chunk); lanes take 4-column quads.
+__device__ __forceinline__ void band_logits_short(const LmMergeArgs& a, const int* fin, int n_band, const float* h,
+                                                  float (*chunk_l)[kChunk], int nw) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float4 hv[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int d = 4 * lane + 128 * u;
+    hv[u] = d < a.D ? *reinterpret_cast<const float4*>(h + d) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  const int n_ids = n_band * kChunk;
+  for (int i0 = warp; i0 < n_ids; i0 += 4 * nw) {
+    float acc[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      acc[t] = 0.f;
+      const int ii = i0 + t * nw, j = ii / kChunk, tt = ii % kChunk;
+      const int v = (ii < n_ids ? fin[j] : 0) * kChunk + tt;
+      if (ii >= n_ids || v >= a.V) continue;
+      float4 ev[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int d = 4 * lane + 128 * u;
+        ev[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (d < a.D) {
+          if (a.Ef) {
+            ev[u] = *reinterpret_cast<const float4*>(a.Ef + (size_t)v * a.D + d);
+          } else {
+            const uint2 raw = *reinterpret_cast<const uint2*>(a.Eb + tiled_index(v, d, a.D));
+            const __nv_bfloat162 e01 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+            const __nv_bfloat162 e23 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+            ev[u] = make_float4(__low2float(e01), __high2float(e01), __low2float(e23), __high2float(e23));
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        acc[t] = fmaf(ev[u].x, hv[u].x, fmaf(ev[u].y, hv[u].y, fmaf(ev[u].z, hv[u].z, fmaf(ev[u].w, hv[u].w, acc[t]))));
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int ii = i0 + t * nw;
+      const float sum = warp_sum(acc[t]);
+      if (lane == 0 && ii < n_ids) chunk_l[ii / kChunk][ii % kChunk] = sum;
+    }
+  }
+}
+
 __device__ __forceinline__ void warp_lse(float& m, float& s) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {  // both partners form the same two terms
@@ -207,9 +259,10 @@ __device__ __forceinline__ float gumbel_f(uint32_t x) {
 
 // kSampling: the sampling form (<= 128 registers: two CTAs per SM, as many rows
 // as there are; no early launch of the successor: the sampling verification's
-// CTAs waiting on these SMs slowed this kernel by about 2x); the greedy form
-// (few rows in practice; deeper loads for the finalists, the successor may
-// launch early).
+// CTAs waiting on these SMs slowed this kernel by about 2x, and so did the
+// gated head's next step with the vocabulary stream behind it); the greedy
+// form (few rows in practice; deeper loads for the finalists, the successor
+// may launch early).
 template <int kMergeWarps, bool kSampling>
 __global__ void __launch_bounds__(kMergeWarps * 32, kSampling ? 2 : 1) lm_merge_kernel(const LmMergeArgs a) {
   static_assert(kMergeWarps == 2 * kTopK, "two warps per finalist");
@@ -290,11 +343,19 @@ __global__ void __launch_bounds__(kMergeWarps * 32, kSampling ? 2 : 1) lm_merge_
   const float* h = a.h + (size_t)r * a.D;
   if constexpr (kSampling) {
     // exact logits of the finalist chunks in the band (a prefix of the sorted
-    // finalists): every warp takes a slice of the columns of all 16 ids, the
-    // warps' partials are added in warp order
-    for (int j = 0; j < kTopK; ++j) {
+    // finalists): short rows all at once; otherwise chunk by chunk, every warp
+    // taking a slice of the columns of all 16 ids, the warps' partials added in
+    // warp order
+    int n_band = 0;
+    while (n_band < kTopK && fin_id[n_band] >= 0 && (long long)fin_id[n_band] * kChunk < a.V &&
+           wsc[0][n_band] >= row_sc0 - kChunkBand * kLog2eM)
+      ++n_band;
+    if (a.D <= 512) {
+      band_logits_short(a, fin_id, n_band, h, chunk_l, kMergeWarps);
+      __syncthreads();
+    }
+    for (int j = 0; j < (a.D <= 512 ? 0 : n_band); ++j) {
       const int k = fin_id[j];
-      if (!(k >= 0 && (long long)k * kChunk < a.V && wsc[0][j] >= row_sc0 - kChunkBand * kLog2eM)) break;
       const float pv = chunk_logits_part(a, k, h, kMergeWarps);
       if (lane < kChunk) chunk_part[warp][lane] = pv;
       __syncthreads();
