@@ -148,27 +148,45 @@ __device__ __forceinline__ float chunk_logits_part(const LmMergeArgs& a, int k, 
     float acc[kIds];
 #pragma unroll
     for (int t = 0; t < kIds; ++t) acc[t] = 0.f;
-    for (int d = 4 * (lane + 32 * warp); d < a.D; d += stride) {
-      const float4 hv = *reinterpret_cast<const float4*>(h + d);
-      float4 ev[kIds];
+    if (!a.Ef) {
+      // bf16 weights: up to four quads per id in flight, kept as raw bf16 pairs
+      // (32 x 8 bytes per lane) until the arithmetic, one round trip per half
+      // at D <= 4096
+      for (int d0 = 4 * (lane + 32 * warp); d0 < a.D; d0 += 4 * stride) {
+        uint2 raw[4][kIds];
+        float4 hv[4];
 #pragma unroll
-      for (int t = 0; t < kIds; ++t) {
-        const int v = v0 + half * kIds + t;
-        ev[t] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (half * kIds + t < nv) {
-          if (a.Ef) {
-            ev[t] = *reinterpret_cast<const float4*>(a.Ef + (size_t)v * a.D + d);
-          } else {
-            const uint2 raw = *reinterpret_cast<const uint2*>(a.Eb + tiled_index(v, d, a.D));
-            const __nv_bfloat162 e01 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-            const __nv_bfloat162 e23 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
-            ev[t] = make_float4(__low2float(e01), __high2float(e01), __low2float(e23), __high2float(e23));
-          }
+        for (int u = 0; u < 4; ++u) {
+          const int d = d0 + u * stride;
+          hv[u] = d < a.D ? *reinterpret_cast<const float4*>(h + d) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int t = 0; t < kIds; ++t)
+            raw[u][t] = d < a.D && half * kIds + t < nv
+                            ? *reinterpret_cast<const uint2*>(a.Eb + tiled_index(v0 + half * kIds + t, d, a.D))
+                            : make_uint2(0u, 0u);
         }
-      }
 #pragma unroll
-      for (int t = 0; t < kIds; ++t)
-        acc[t] = fmaf(ev[t].x, hv.x, fmaf(ev[t].y, hv.y, fmaf(ev[t].z, hv.z, fmaf(ev[t].w, hv.w, acc[t]))));
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int t = 0; t < kIds; ++t) {
+            const float4 e = make_float4(__uint_as_float(raw[u][t].x << 16), __uint_as_float(raw[u][t].x & 0xffff0000u),
+                                         __uint_as_float(raw[u][t].y << 16), __uint_as_float(raw[u][t].y & 0xffff0000u));
+            acc[t] = fmaf(e.x, hv[u].x, fmaf(e.y, hv[u].y, fmaf(e.z, hv[u].z, fmaf(e.w, hv[u].w, acc[t]))));
+          }
+      }
+    } else {
+      for (int d = 4 * (lane + 32 * warp); d < a.D; d += stride) {
+        const float4 hv = *reinterpret_cast<const float4*>(h + d);
+        float4 ev[kIds];
+#pragma unroll
+        for (int t = 0; t < kIds; ++t)
+          ev[t] = half * kIds + t < nv
+                      ? *reinterpret_cast<const float4*>(a.Ef + (size_t)(v0 + half * kIds + t) * a.D + d)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int t = 0; t < kIds; ++t)
+          acc[t] = fmaf(ev[t].x, hv.x, fmaf(ev[t].y, hv.y, fmaf(ev[t].z, hv.z, fmaf(ev[t].w, hv.w, acc[t]))));
+      }
     }
 #pragma unroll
     for (int t = 0; t < kIds; ++t) {

@@ -445,8 +445,11 @@ Plan plan(int rows, int outs, int K, int xplanes, int wplanes, bool lm, bool one
       if (stages > 8) stages = 8;
       if (stages < 2) continue;
       const int slabs = (outs + N - 1) / N;
-      // at most 4 k-splits: every consumer sums the splits on its critical path
-      const int smax = (lm || one_split) ? 1 : (kblocks < 4 ? kblocks : 4);
+      // at most 4 k-splits (every consumer sums the splits on its critical path),
+      // up to 16 for few rows, whose partial planes are small: a weight stream
+      // then needs the splits to fill the SMs with wide slabs
+      const int scap = rows <= 64 ? 16 : 4;
+      const int smax = (lm || one_split) ? 1 : (kblocks < scap ? kblocks : scap);
       for (int S = 1; S <= smax; ++S) {
         const int kbps = (kblocks + S - 1) / S;
         const int Se = (kblocks + kbps - 1) / kbps;
@@ -503,7 +506,8 @@ std::vector<Plan> plan_candidates(int rows, int outs, int K, int xplanes, int wp
       int stages = (int)((kSmemBudget - 2048 - kTailPad) / sb);
       if (stages > 8) stages = 8;
       if (stages < 2) continue;
-      const int smax = one_split ? 1 : (kblocks < 4 ? kblocks : 4);
+      const int scap = rows <= 64 ? 16 : 4;
+      const int smax = one_split ? 1 : (kblocks < scap ? kblocks : scap);
       for (int S = 1; S <= smax; ++S) {
         const int kbps = (kblocks + S - 1) / S;
         if ((kblocks + kbps - 1) / kbps != S) continue;
