@@ -576,9 +576,10 @@ cudaError_t launch_resnorm(const ResNormArgs& a, cudaStream_t s) {
   attrs[1].val.clusterDim.z = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
-  // a cluster per row: few CTAs, deep loads; else two CTAs per SM (all rows in one wave)
+  // a cluster per row: few CTAs, deep loads (every plane of a few-row product, up
+  // to 8, in flight at once); else two CTAs per SM (all rows in one wave)
   if (n4 > threads * (C > 1 ? 1 : kRowVec)) return cudaErrorInvalidValue;
-  return C > 1 ? cudaLaunchKernelEx(&cfg, resnorm_kernel<4, 1, 1>, a)
+  return C > 1 ? cudaLaunchKernelEx(&cfg, resnorm_kernel<8, 1, 1>, a)
                : cudaLaunchKernelEx(&cfg, resnorm_kernel<2, 2, kRowVec>, a);
 }
 
