@@ -95,3 +95,27 @@ def test_engine_plans_match_float64(N, S, rows):
     assert np.isfinite(got).all()
     assert np.abs(got - ref).max() <= 1e-5 * scale
 
+
+
+@pytest.mark.parametrize("rows,K,N,S", [(8, 4096, 256, 8), (8, 12288, 192, 16), (21, 4096, 128, 6), (64, 2048, 256, 12)])
+def test_engine_few_rows_many_splits_match_float64(rows, K, N, S):
+    """Few-row products take up to 16 k splits (wide slabs over all SMs): the planes
+    of every split count sum to the float64 product."""
+    outs = 1000 if N != 256 else 4096
+    g = torch.Generator().manual_seed(rows * 5 + K + N + S)
+    x_rows = 128
+    X = torch.randn(x_rows, K, generator=g)
+    X[rows:] = float("nan")
+    W = torch.randn(outs, K, generator=g) * 0.05
+    Xp = [p.to(DEV) for p in _planes(X, 1)]
+    Wp = [p.to(DEV) for p in _planes(W, 1)]
+    got, st = binding.selftest_gemm(Xp, [_tiled(p) for p in Wp], rows=rows, outs=outs, plan=(N, S, 0))
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    x64 = Xp[0][:rows].double().cpu().numpy()
+    w64 = Wp[0].double().cpu().numpy()
+    ref = x64 @ w64.T
+    got = got.double().cpu().numpy()
+    scale = np.sqrt(K) * np.abs(w64).max() * np.abs(x64).max()
+    assert np.isfinite(got).all()
+    assert np.abs(got - ref).max() <= 1e-5 * scale
