@@ -117,7 +117,7 @@ __device__ __forceinline__ float4 load4(const bf16* p) {
   return make_float4(__low2float(a), __high2float(a), __low2float(b), __high2float(b));
 }
 
-template <typename T>
+template <typename T, int kVec>  // kVec: float4 chunks of a row per thread at most
 __global__ void __launch_bounds__(1024) stage_kernel(StageArgs a) {
   pdl_trigger();
   pdl_wait();
@@ -125,13 +125,13 @@ __global__ void __launch_bounds__(1024) stage_kernel(StageArgs a) {
   const int row = blockIdx.x;
   const int D = a.D, n4 = D / 4;
   const int nz = a.B * a.m;
-  float4 v[kRowVec];
+  float4 v[kVec];
   float ss = 0.f;
   if (row < nz) {
     const int b = row / a.m, j = row % a.m;
     const T* h = reinterpret_cast<const T*>(a.hidden) + ((size_t)b * a.m + j) * D;
 #pragma unroll
-    for (int k = 0; k < kRowVec; ++k) {
+    for (int k = 0; k < kVec; ++k) {
       const int i = threadIdx.x + k * blockDim.x;
       if (i < n4) {
         v[k] = f4add(load4(h + 4 * i), load4(a.e_depth + (size_t)j * D + 4 * i));
@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(1024) stage_kernel(StageArgs a) {
     ss = block_sum(ss, red);
     const float inv = rsqrtf(ss / D + a.eps);
 #pragma unroll
-    for (int k = 0; k < kRowVec; ++k) {
+    for (int k = 0; k < kVec; ++k) {
       const int i = threadIdx.x + k * blockDim.x;
       if (i < n4) {
         const float4 g = load4(a.g_stage + 4 * i);
@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(1024) stage_kernel(StageArgs a) {
     }
     const T* E = reinterpret_cast<const T*>(a.E);
 #pragma unroll
-    for (int k = 0; k < kRowVec; ++k) {
+    for (int k = 0; k < kVec; ++k) {
       const int i = threadIdx.x + k * blockDim.x;
       if (i < n4) {
         v[k] = (i0 < a.G) ? load4(E + (a.E_tiled ? tiled_index(tok, 4 * i, D) : (size_t)tok * D + 4 * i))
@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(1024) stage_kernel(StageArgs a) {
     ss = block_sum(ss, red);
     const float inv = rsqrtf(ss / D + a.eps);
 #pragma unroll
-    for (int k = 0; k < kRowVec; ++k) {
+    for (int k = 0; k < kVec; ++k) {
       const int i = threadIdx.x + k * blockDim.x;
       if (i < n4) {
         const float4 g = load4(a.g_attn0 + 4 * i);
@@ -190,11 +190,17 @@ __global__ void __launch_bounds__(1024) stage_kernel(StageArgs a) {
 
 cudaError_t launch_stage(const StageArgs& a, bool f32, cudaStream_t s) {
   const int rows = a.B * a.m + a.B * (a.G + a.K);
-  // few rows: 1024 threads per row; many: 512 (several rows per SM at once)
-  const int threads = rows <= 2 * device_sms() ? 1024 : 512;
-  if (a.D / 4 > kRowVec * threads) return cudaErrorInvalidValue;
-  if (f32) return launch_pdl(stage_kernel<float>, dim3(rows), dim3(threads), 0, s, a);
-  return launch_pdl(stage_kernel<bf16>, dim3(rows), dim3(threads), 0, s, a);
+  // few rows: 1024 threads per row; many: 256 threads with four float4 of the
+  // row each (D <= 4096; few registers, so that every row runs in one wave:
+  // 704 rows at B = 32 took two waves of 512-thread CTAs), else 512
+  if (rows <= 2 * device_sms() || a.D / 4 > 4 * 256) {
+    const int threads = rows <= 2 * device_sms() ? 1024 : 512;
+    if (a.D / 4 > kRowVec * threads) return cudaErrorInvalidValue;
+    if (f32) return launch_pdl(stage_kernel<float, kRowVec>, dim3(rows), dim3(threads), 0, s, a);
+    return launch_pdl(stage_kernel<bf16, kRowVec>, dim3(rows), dim3(threads), 0, s, a);
+  }
+  if (f32) return launch_pdl(stage_kernel<float, 4>, dim3(rows), dim3(256), 0, s, a);
+  return launch_pdl(stage_kernel<bf16, 4>, dim3(rows), dim3(256), 0, s, a);
 }
 
 // ---------------------------------------------------------------- K2b: block attention
