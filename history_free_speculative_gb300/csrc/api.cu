@@ -66,6 +66,7 @@ struct dlite_handle {
   float* Mt = nullptr;                      // [R, R] Q_h P in the chain's register image
   // gated token-feedback head (head_type 1)
   bool gated = false;
+  int gated_clusters = 0;  // fused-step clusters (R / 32 CTAs, 4 requests each) the device runs at once
   const bf16 *Ws[2] = {nullptr, nullptr}, *Whs[2] = {nullptr, nullptr}, *Whu[2] = {nullptr, nullptr},
              *Wo[2] = {nullptr, nullptr};     // tiled planes: [2R, 2R], [R, R], [R, D], [Vp, R]
   float *ER32 = nullptr, *bs32 = nullptr, *bh32 = nullptr, *Wo32 = nullptr;  // fp32 (Wo32: fp32 drafters)
@@ -379,6 +380,12 @@ void seed_key(uint64_t seed, uint32_t* k0, uint32_t* k1) {
 // LM head: one bf16 plane of h and of E; the merge re-scores the finalists exactly.
 tc::Plan lm_plan(dlite_handle* h, int rows) {
   return tc::plan(rows, h->cfg.V, h->cfg.D, 1, 1, true);
+}
+
+// The gated head's fused step (state and r in one launch) when every one of its
+// clusters (4 requests each) is resident at once.
+static bool gated_fused(const dlite_handle* h, int B) {
+  return h->gated_clusters > 0 && (B + 3) / 4 <= h->gated_clusters;
 }
 
 // bf16 drafters store the context rows z behind the local rows y in one
@@ -802,14 +809,20 @@ int run_gated_head(dlite_handle* h, int B, const int32_t* anchor, float temperat
   op.K_draft = 1;
   g.warm = c.head_warmup;
   if (c.head_warmup) {  // s_0: one state update from zero on the token before the anchor, no output
-    CK(launch_gated_state(g, 0, s));
+    CK(launch_gated_state(g, 0, false, s));
     mark(h, "gated_state");
   }
+  // the step's r in the state kernel's launch when all its clusters run at
+  // once (in waves they were slower than the two launches: 0.96 vs 0.90 ms
+  // per round at B = 32)
+  const bool fused = gated_fused(h, B);
   for (int i = 1; i <= K; ++i) {
-    CK(launch_gated_state(g, i, s));
+    CK(launch_gated_state(g, i, fused, s));
     mark(h, "gated_state");
-    CK(launch_gated_r(g, i, s));
-    mark(h, "gated_r");
+    if (!fused) {
+      CK(launch_gated_r(g, i, s));
+      mark(h, "gated_r");
+    }
     RUN(run_lm_core(h, B, op, temperature, seed, pos ? h->g_pos : nullptr, h->g_cand, qs ? h->g_qs : nullptr, s));
   }
   CK(launch_gated_final(g, s));
@@ -1186,6 +1199,13 @@ static int create_impl(dlite_handle* h, const dlite_weights* w) {
     AL(h->hpart_o, prow * c.d_h);
     AL(h->hpart_ml, prow * 2);
     RUN(dlite_history_reset(h, nullptr));
+  }
+  if (h->gated) {  // the fused step needs a co-resident cluster of R / 32 CTAs
+    GatedArgs ga;
+    ga.B = c.B_max;
+    ga.R = c.R;
+    ga.np = h->np;
+    h->gated_clusters = gated_step_clusters(ga);
   }
   CK(cudaDeviceSynchronize());
   RUN(tune_products(h));
@@ -1658,8 +1678,9 @@ int dlite_launch_count(dlite_handle* h, int B, float temperature) {
   const int per_layer = (fused ? 8 : 9) - (fuse_ctx(h, B) ? 1 : 0);  // one product for [y; z] when fused
   // history-KV control: + {history attention, combine} per layer + the cursor advance
   const int hist = h->H ? 2 * h->cfg.L_D + 1 : 0;
-  if (h->gated)  // head: {W_h u product, sum} + K x {state, r, lm, merge} + final (+ the warm-up's state)
-    return 1 + per_layer * h->cfg.L_D + hist + 2 + 4 * h->cfg.K + 1 + (h->cfg.head_warmup ? 1 : 0);
+  if (h->gated)  // head: {W_h u product, sum} + K x {state (+ r), lm, merge} + final (+ the warm-up's state)
+    return 1 + per_layer * h->cfg.L_D + hist + 2 + (gated_fused(h, B) ? 3 : 4) * h->cfg.K + 1 +
+           (h->cfg.head_warmup ? 1 : 0);
   // head {ce, chain, P + residual} (+ out when no single-split plan fits the P product)
   const int head = B * h->cfg.K <= 64 && tc::plan(B * h->cfg.K, h->cfg.D, h->Rp, 2, h->np, false, true).ok &&
                    h->cfg.D % 16 == 0 ? 3 : 4;

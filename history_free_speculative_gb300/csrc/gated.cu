@@ -110,168 +110,19 @@ __device__ __forceinline__ void request_slice(const bf16* const* W, int r0, int 
 
 }  // namespace
 
-// Step i (0: the warm-up on the token before the anchor, no output; 1: the
-// anchor; then the previous step's choice, which is also stored into cand / qs):
-// [g | c] = W_s [s_{i-1}; E_R(d_{i-1})] + b_s, s_i = f s_{i-1} + (1 - f) tanh(c).
-// Shared memory: [NP][g | c][2R / 64][FB][64] bf16, [4][2R] fp32 inputs,
-// [8][2][FB][4] fp32 warp sums.
-template <int NP>
-__global__ void __launch_bounds__(kStepWarps * 32) gated_state_kernel(GatedArgs a, int i) {
-  constexpr int FB = 32 / NP;  // features per CTA
-  constexpr int NV = 2 * FB;   // partial sums per lane: (g | c) x (FB / 4 rows) x 4 requests
-  extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t bar;
-  __shared__ int tok[kStepRows];
-  __shared__ int ok_s;
-  const int R = a.R, R2 = 2 * R, K = a.K, nkt = R2 / 64;
-  bf16* wsm = reinterpret_cast<bf16*>(smem);
-  const size_t plane = (size_t)2 * nkt * FB * 64;  // elements per staged plane
-  float* xs = reinterpret_cast<float*>(smem + NP * plane * 2);
-  float* red = xs + kStepRows * R2;
-  const int j0 = blockIdx.x * FB, b0 = blockIdx.y * kStepRows;
-  const int nb = min(kStepRows, a.B - b0);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = lane >> 3, ch = lane & 7;
-  const uint32_t bar_a = tc::su32(&bar);
-  if (threadIdx.x == 0) {  // the weights do not depend on the previous kernel
-    tc::mbar_init(bar_a, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    tc::mbar_expect_tx(bar_a, (uint32_t)(NP * 2 * nkt * FB * 128));
-    for (int gc = 0; gc < 2; ++gc)  // g rows j0.., c rows R + j0..
-      request_slice<NP, FB>(a.Ws, gc * R + j0, R2, wsm + (size_t)gc * nkt * FB * 64, bar_a, 2 * nkt);
-  }
-  pdl_trigger();
-  pdl_wait();
-  if (threadIdx.x < kStepRows) {
-    const int b = b0 + threadIdx.x;
-    int d = 0;
-    if (b < a.B) {
-      d = i == 0 ? a.anchor[b * a.G + a.G - 2] : i == 1 ? a.anchor[b * a.G + a.G - 1] : a.cand_tmp[b];
-      if (d < 0 || d >= a.V) {
-        flag_status(a.status, kDevBounds);
-        d = 0;
-      }
-    }
-    tok[threadIdx.x] = d;
-  }
-  if (blockIdx.x == 0 && threadIdx.x < nb && i >= 1) {  // the step's bookkeeping, once per request
-    const int b = b0 + threadIdx.x;
-    if (i > 1) {
-      a.cand[b * K + i - 2] = a.cand_tmp[b];
-      if (a.qs) a.qs[b * K + i - 2] = a.qs_tmp[b];
-    }
-    if (a.pos) a.pos_i[b] = a.pos[b] + (i - 1);
-  }
-  __syncthreads();
-  // the state starts with the block (at the warm-up step when there is one)
-  const bool fresh = i == 0 || (i == 1 && !a.warm);
-  const float* s_prev = a.s + (size_t)((i & 1) ^ 1) * a.B * R;
-  for (int e = threadIdx.x; e < kStepRows * R2 / 4; e += blockDim.x) {
-    const int r = e / (R2 / 4), k = (e % (R2 / 4)) * 4;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (r < nb) {
-      if (k >= R)
-        v = *reinterpret_cast<const float4*>(a.ER + (size_t)tok[r] * R + k - R);
-      else if (!fresh)
-        v = *reinterpret_cast<const float4*>(s_prev + (size_t)(b0 + r) * R + k);
-    }
-    *reinterpret_cast<float4*>(xs + r * R2 + k) = v;
-  }
-  if (threadIdx.x == 0) ok_s = tc::mbar_wait(bar_a, 0, a.status);
-  __syncthreads();
-  if (!ok_s) {  // the weights did not arrive in time (status flagged): let the copies land, then leave
-    if (threadIdx.x == 0) tc::mbar_wait(bar_a, 0, nullptr);
-    return;
-  }
-  float v[NV];
-#pragma unroll
-  for (int k = 0; k < NV; ++k) v[k] = 0.f;
-  for (int t = warp; t < nkt; t += kStepWarps) {
-    float x[kStepRows][8];
-#pragma unroll
-    for (int b = 0; b < kStepRows; ++b) {
-      const float4 x0 = *reinterpret_cast<const float4*>(xs + b * R2 + t * 64 + ch * 8);
-      const float4 x1 = *reinterpret_cast<const float4*>(xs + b * R2 + t * 64 + ch * 8 + 4);
-      x[b][0] = x0.x, x[b][1] = x0.y, x[b][2] = x0.z, x[b][3] = x0.w;
-      x[b][4] = x1.x, x[b][5] = x1.y, x[b][6] = x1.z, x[b][7] = x1.w;
-    }
-#pragma unroll
-    for (int gc = 0; gc < 2; ++gc)
-#pragma unroll
-      for (int rg = 0; rg < FB / 4; ++rg) {
-        float w[8];
-        smem_w8<NP>(wsm + ((size_t)gc * nkt + t) * FB * 64 + (rg * 4 + q) * 64 + ch * 8, plane, w);
-#pragma unroll
-        for (int b = 0; b < kStepRows; ++b) v[(gc * (FB / 4) + rg) * 4 + b] += dot8(w, x[b]);
-      }
-  }
-  reduce_scatter8<NV>(v, ch);
-#pragma unroll
-  for (int k = 0; k < NV / 8; ++k) {
-    const int idx = ((ch >> 2) & 1) * (NV / 2) + ((ch >> 1) & 1) * (NV / 4) + (ch & 1) * (NV / 8) + k;
-    const int gc = idx / FB, rg = (idx % FB) / 4, b = idx % 4;
-    red[((warp * 2 + gc) * FB + rg * 4 + q) * kStepRows + b] = v[k];
-  }
-  __syncthreads();
-  if (threadIdx.x < FB * kStepRows) {
-    const int l = threadIdx.x / kStepRows, r = threadIdx.x % kStepRows;
-    if (r < nb) {
-      float g = 0.f, c = 0.f;
-#pragma unroll
-      for (int w = 0; w < kStepWarps; ++w) {
-        g += red[((w * 2 + 0) * FB + l) * kStepRows + r];
-        c += red[((w * 2 + 1) * FB + l) * kStepRows + r];
-      }
-      const int j = j0 + l;
-      g += a.bs[j];
-      c += a.bs[R + j];
-      const float f = 1.f / (1.f + expf(-g));
-      const float sp = xs[r * R2 + j];  // s_{i-1}[j] (zero for a fresh state)
-      a.s[(size_t)(i & 1) * a.B * R + (size_t)(b0 + r) * R + j] = f * sp + (1.f - f) * tanhf(c);
-    }
-  }
-}
-
-// r_i = W_hs s_i + (W_hu u_i) + b_h: kept in fp32 (all steps, for
+// r_i = W_hs s_i + (W_hu u_i) + b_h for features j0 .. j0 + FB - 1 of requests
+// b0 .. b0 + nb - 1, from the staged states xs [4][R] (fp32) and the staged
+// weight slice wsm [NP][R / 64][FB][64]: kept in fp32 (all steps, for
 // verification; this step's, for the exact re-scoring) and as the bf16
-// activation of the vocabulary projection. Shared memory: [NP][R / 64][FB][64]
-// bf16, [4][R] fp32 states, [8][FB][4] fp32 warp sums.
+// activation of the vocabulary projection. Every thread of the CTA calls it.
 template <int NP>
-__global__ void __launch_bounds__(kStepWarps * 32) gated_r_kernel(GatedArgs a, int i) {
+__device__ __forceinline__ void r_product(const GatedArgs& a, int i, const float* xs, const bf16* wsm, float* red,
+                                          int j0, int b0, int nb) {
   constexpr int FB = 32 / NP;
   constexpr int NV = FB;  // (FB / 4 rows) x 4 requests
-  extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t bar;
-  __shared__ int ok_s;
   const int R = a.R, K = a.K, nkt = R / 64;
-  bf16* wsm = reinterpret_cast<bf16*>(smem);
   const size_t plane = (size_t)nkt * FB * 64;
-  float* xs = reinterpret_cast<float*>(smem + NP * plane * 2);
-  float* red = xs + kStepRows * R;
-  const int j0 = blockIdx.x * FB, b0 = blockIdx.y * kStepRows;
-  const int nb = min(kStepRows, a.B - b0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = lane >> 3, ch = lane & 7;
-  const uint32_t bar_a = tc::su32(&bar);
-  if (threadIdx.x == 0) {
-    tc::mbar_init(bar_a, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    tc::mbar_expect_tx(bar_a, (uint32_t)(NP * nkt * FB * 128));
-    request_slice<NP, FB>(a.Whs, j0, R, wsm, bar_a, nkt);
-  }
-  pdl_trigger();
-  pdl_wait();
-  const float* s_i = a.s + (size_t)(i & 1) * a.B * R;
-  for (int e = threadIdx.x; e < kStepRows * R / 4; e += blockDim.x) {
-    const int r = e / (R / 4), k = (e % (R / 4)) * 4;
-    const float4 v = r < nb ? *reinterpret_cast<const float4*>(s_i + (size_t)(b0 + r) * R + k)
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-    *reinterpret_cast<float4*>(xs + r * R + k) = v;
-  }
-  if (threadIdx.x == 0) ok_s = tc::mbar_wait(bar_a, 0, a.status);
-  __syncthreads();
-  if (!ok_s) {
-    if (threadIdx.x == 0) tc::mbar_wait(bar_a, 0, nullptr);
-    return;
-  }
   float v[NV];
 #pragma unroll
   for (int k = 0; k < NV; ++k) v[k] = 0.f;
@@ -315,6 +166,194 @@ __global__ void __launch_bounds__(kStepWarps * 32) gated_r_kernel(GatedArgs a, i
   }
 }
 
+// Step i (0: the warm-up on the token before the anchor, no output; 1: the
+// anchor; then the previous step's choice, which is also stored into cand / qs):
+// [g | c] = W_s [s_{i-1}; E_R(d_{i-1})] + b_s, s_i = f s_{i-1} + (1 - f) tanh(c).
+// kR (one bf16 weight plane): the step's r as well, in the same launch. The
+// grid's x extent (R / 32 feature blocks) is then one thread-block cluster:
+// every CTA sends its slice of s_i to all CTAs of the cluster (distributed
+// shared memory), one cluster barrier, and each CTA forms r for its 32
+// features from the whole s_i with its W_hs slice, requested at the start
+// with the W_s slice. Same arithmetic and order as the separate r kernel.
+// Shared memory: [NP][g | c][2R / 64][FB][64] bf16, (kR) [R / 64][FB][64] bf16,
+// [4][2R] fp32 inputs, [8][2][FB][4] fp32 warp sums, (kR) [4][R] fp32 s_i and
+// [8][FB][4] fp32 warp sums.
+template <int NP, bool kR>
+__global__ void __launch_bounds__(kStepWarps * 32) gated_state_kernel(GatedArgs a, int i) {
+  static_assert(!kR || NP == 1, "the fused step keeps one weight plane");
+  constexpr int FB = 32 / NP;  // features per CTA
+  constexpr int NV = 2 * FB;   // partial sums per lane: (g | c) x (FB / 4 rows) x 4 requests
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int tok[kStepRows];
+  __shared__ int ok_s;
+  const int R = a.R, R2 = 2 * R, K = a.K, nkt = R2 / 64;
+  const bool with_r = kR && i >= 1;  // the warm-up step has no output
+  bf16* wsm = reinterpret_cast<bf16*>(smem);
+  const size_t plane = (size_t)2 * nkt * FB * 64;  // elements per staged plane
+  bf16* whs = wsm + NP * plane;                     // (kR) the W_hs slice
+  const size_t whs_elems = kR ? (size_t)(R / 64) * FB * 64 : 0;
+  float* xs = reinterpret_cast<float*>(whs + whs_elems);
+  float* red = xs + kStepRows * R2;
+  float* s_all = red + kStepWarps * 2 * FB * kStepRows;  // (kR)
+  float* red_r = s_all + kStepRows * R;                 // (kR)
+  const int j0 = blockIdx.x * FB, b0 = blockIdx.y * kStepRows;
+  const int nb = min(kStepRows, a.B - b0);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = lane >> 3, ch = lane & 7;
+  const uint32_t bar_a = tc::su32(&bar);
+  if (threadIdx.x == 0) {  // the weights do not depend on the previous kernel
+    tc::mbar_init(bar_a, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    tc::mbar_expect_tx(bar_a, (uint32_t)(NP * 2 * nkt * FB * 128 + (with_r ? (R / 64) * FB * 128 : 0)));
+    for (int gc = 0; gc < 2; ++gc)  // g rows j0.., c rows R + j0..
+      request_slice<NP, FB>(a.Ws, gc * R + j0, R2, wsm + (size_t)gc * nkt * FB * 64, bar_a, 2 * nkt);
+    if (with_r) request_slice<1, FB>(a.Whs, j0, R, whs, bar_a, R / 64);
+  }
+  pdl_trigger();
+  pdl_wait();
+  if (threadIdx.x < kStepRows) {
+    const int b = b0 + threadIdx.x;
+    int d = 0;
+    if (b < a.B) {
+      d = i == 0 ? a.anchor[b * a.G + a.G - 2] : i == 1 ? a.anchor[b * a.G + a.G - 1] : a.cand_tmp[b];
+      if (d < 0 || d >= a.V) {
+        flag_status(a.status, kDevBounds);
+        d = 0;
+      }
+    }
+    tok[threadIdx.x] = d;
+  }
+  if (blockIdx.x == 0 && threadIdx.x < nb && i >= 1) {  // the step's bookkeeping, once per request
+    const int b = b0 + threadIdx.x;
+    if (i > 1) {
+      a.cand[b * K + i - 2] = a.cand_tmp[b];
+      if (a.qs) a.qs[b * K + i - 2] = a.qs_tmp[b];
+    }
+    if (a.pos) a.pos_i[b] = a.pos[b] + (i - 1);
+  }
+  __syncthreads();
+  // the state starts with the block (at the warm-up step when there is one)
+  const bool fresh = i == 0 || (i == 1 && !a.warm);
+  const float* s_prev = a.s + (size_t)((i & 1) ^ 1) * a.B * R;
+  for (int e = threadIdx.x; e < kStepRows * R2 / 4; e += blockDim.x) {
+    const int r = e / (R2 / 4), k = (e % (R2 / 4)) * 4;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r < nb) {
+      if (k >= R)
+        v = *reinterpret_cast<const float4*>(a.ER + (size_t)tok[r] * R + k - R);
+      else if (!fresh)
+        v = *reinterpret_cast<const float4*>(s_prev + (size_t)(b0 + r) * R + k);
+    }
+    *reinterpret_cast<float4*>(xs + r * R2 + k) = v;
+  }
+  if (threadIdx.x == 0) ok_s = tc::mbar_wait(bar_a, 0, a.status);
+  __syncthreads();
+  // after a wait that gave up (status flagged) the CTA lets its copies land and
+  // skips the arithmetic; with the fused r it still takes the cluster barrier
+  const bool ok = ok_s != 0;
+  if (!ok && threadIdx.x == 0) tc::mbar_wait(bar_a, 0, nullptr);
+  if (ok) {
+    float v[NV];
+#pragma unroll
+    for (int k = 0; k < NV; ++k) v[k] = 0.f;
+    for (int t = warp; t < nkt; t += kStepWarps) {
+      float x[kStepRows][8];
+#pragma unroll
+      for (int b = 0; b < kStepRows; ++b) {
+        const float4 x0 = *reinterpret_cast<const float4*>(xs + b * R2 + t * 64 + ch * 8);
+        const float4 x1 = *reinterpret_cast<const float4*>(xs + b * R2 + t * 64 + ch * 8 + 4);
+        x[b][0] = x0.x, x[b][1] = x0.y, x[b][2] = x0.z, x[b][3] = x0.w;
+        x[b][4] = x1.x, x[b][5] = x1.y, x[b][6] = x1.z, x[b][7] = x1.w;
+      }
+#pragma unroll
+      for (int gc = 0; gc < 2; ++gc)
+#pragma unroll
+        for (int rg = 0; rg < FB / 4; ++rg) {
+          float w[8];
+          smem_w8<NP>(wsm + ((size_t)gc * nkt + t) * FB * 64 + (rg * 4 + q) * 64 + ch * 8, plane, w);
+#pragma unroll
+          for (int b = 0; b < kStepRows; ++b) v[(gc * (FB / 4) + rg) * 4 + b] += dot8(w, x[b]);
+        }
+    }
+    reduce_scatter8<NV>(v, ch);
+#pragma unroll
+    for (int k = 0; k < NV / 8; ++k) {
+      const int idx = ((ch >> 2) & 1) * (NV / 2) + ((ch >> 1) & 1) * (NV / 4) + (ch & 1) * (NV / 8) + k;
+      const int gc = idx / FB, rg = (idx % FB) / 4, b = idx % 4;
+      red[((warp * 2 + gc) * FB + rg * 4 + q) * kStepRows + b] = v[k];
+    }
+  }
+  __syncthreads();
+  if (ok && threadIdx.x < FB * kStepRows) {
+    const int l = threadIdx.x / kStepRows, r = threadIdx.x % kStepRows;
+    float s_new = 0.f;  // rows past the batch contribute zeros to the fused r
+    if (r < nb) {
+      float g = 0.f, c = 0.f;
+#pragma unroll
+      for (int w = 0; w < kStepWarps; ++w) {
+        g += red[((w * 2 + 0) * FB + l) * kStepRows + r];
+        c += red[((w * 2 + 1) * FB + l) * kStepRows + r];
+      }
+      const int j = j0 + l;
+      g += a.bs[j];
+      c += a.bs[R + j];
+      const float f = 1.f / (1.f + expf(-g));
+      const float sp = xs[r * R2 + j];  // s_{i-1}[j] (zero for a fresh state)
+      s_new = f * sp + (1.f - f) * tanhf(c);
+      a.s[(size_t)(i & 1) * a.B * R + (size_t)(b0 + r) * R + j] = s_new;
+    }
+    if (with_r) {  // this feature of s_i into every CTA of the cluster
+      const uint32_t dst = tc::su32(s_all + r * R + j0 + l);
+      for (int rank = 0; rank < (int)gridDim.x; ++rank)
+        asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(tc::map_to_rank(dst, (uint32_t)rank)), "f"(s_new)
+                     : "memory");
+    }
+  }
+  if (with_r) {
+    tc::cluster_sync_all();  // every slice of s_i has arrived (and no CTA writes remotely any more)
+    if (ok) r_product<1>(a, i, s_all, whs, red_r, j0, b0, nb);
+  }
+}
+
+// The separate r kernel (two weight planes, or no cluster of R / 32 CTAs).
+template <int NP>
+__global__ void __launch_bounds__(kStepWarps * 32) gated_r_kernel(GatedArgs a, int i) {
+  constexpr int FB = 32 / NP;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int ok_s;
+  const int R = a.R, nkt = R / 64;
+  bf16* wsm = reinterpret_cast<bf16*>(smem);
+  const size_t plane = (size_t)nkt * FB * 64;
+  float* xs = reinterpret_cast<float*>(smem + NP * plane * 2);
+  float* red = xs + kStepRows * R;
+  const int j0 = blockIdx.x * FB, b0 = blockIdx.y * kStepRows;
+  const int nb = min(kStepRows, a.B - b0);
+  const uint32_t bar_a = tc::su32(&bar);
+  if (threadIdx.x == 0) {
+    tc::mbar_init(bar_a, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    tc::mbar_expect_tx(bar_a, (uint32_t)(NP * nkt * FB * 128));
+    request_slice<NP, FB>(a.Whs, j0, R, wsm, bar_a, nkt);
+  }
+  pdl_trigger();
+  pdl_wait();
+  const float* s_i = a.s + (size_t)(i & 1) * a.B * R;
+  for (int e = threadIdx.x; e < kStepRows * R / 4; e += blockDim.x) {
+    const int r = e / (R / 4), k = (e % (R / 4)) * 4;
+    const float4 v = r < nb ? *reinterpret_cast<const float4*>(s_i + (size_t)(b0 + r) * R + k)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+    *reinterpret_cast<float4*>(xs + r * R + k) = v;
+  }
+  if (threadIdx.x == 0) ok_s = tc::mbar_wait(bar_a, 0, a.status);
+  __syncthreads();
+  if (!ok_s) {
+    if (threadIdx.x == 0) tc::mbar_wait(bar_a, 0, nullptr);
+    return;
+  }
+  r_product<NP>(a, i, xs, wsm, red, j0, b0, nb);
+}
+
 // out[r][c] = sum of the split planes of a rows x cols product
 __global__ void gated_sum_kernel(const float* part, Splits sp, int rows, int cols, float* out) {
   pdl_trigger();
@@ -336,23 +375,66 @@ __global__ void gated_final_kernel(GatedArgs a) {
   if (a.qs) a.qs[b * a.K + a.K - 1] = a.qs_tmp[b];
 }
 
-static size_t state_smem(int R, int np) {
+static size_t state_smem(int R, int np, bool fused) {
   const int fb = 32 / np;
-  return (size_t)np * 2 * (2 * R / 64) * fb * 128 + (size_t)kStepRows * 2 * R * 4 + (size_t)kStepWarps * 2 * fb * kStepRows * 4;
+  size_t b = (size_t)np * 2 * (2 * R / 64) * fb * 128 + (size_t)kStepRows * 2 * R * 4 +
+             (size_t)kStepWarps * 2 * fb * kStepRows * 4;
+  if (fused) b += (size_t)(R / 64) * fb * 128 + (size_t)kStepRows * R * 4 + (size_t)kStepWarps * fb * kStepRows * 4;
+  return b;
 }
 static size_t r_smem(int R, int np) {
   const int fb = 32 / np;
   return (size_t)np * (R / 64) * fb * 128 + (size_t)kStepRows * R * 4 + (size_t)kStepWarps * fb * kStepRows * 4;
 }
 
-cudaError_t launch_gated_state(const GatedArgs& a, int i, cudaStream_t s) {
-  if (a.R > 512 || a.R % 64 || a.B < 1 || a.np < 1 || a.np > 2) return cudaErrorInvalidValue;
-  const size_t sm = state_smem(a.R, a.np);
-  auto fn = a.np == 1 ? gated_state_kernel<1> : gated_state_kernel<2>;
+static cudaLaunchConfig_t step_config(const GatedArgs& a, bool fused, size_t sm, cudaStream_t s,
+                                      cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.R / (32 / a.np), (a.B + kStepRows - 1) / kStepRows);
+  cfg.blockDim = dim3(kStepWarps * 32);
+  cfg.dynamicSmemBytes = sm;
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = fused ? a.R / 32 : 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = fused ? 2 : 1;
+  return cfg;
+}
+
+int gated_step_clusters(const GatedArgs& a) {
+  if (a.np != 1 || a.R > 512 || a.R % 64 || a.B < 1) return 0;
+  auto fn = gated_state_kernel<1, true>;
+  const size_t sm = state_smem(a.R, 1, true);
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) != cudaSuccess ||
+      (a.R / 32 > 8 && cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = step_config(a, true, sm, nullptr, attr);
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+cudaError_t launch_gated_state(const GatedArgs& a, int i, bool fused, cudaStream_t s) {
+  if (a.R > 512 || a.R % 64 || a.B < 1 || a.np < 1 || a.np > 2 || (fused && a.np != 1)) return cudaErrorInvalidValue;
+  const size_t sm = state_smem(a.R, a.np, fused);
+  auto fn = fused ? gated_state_kernel<1, true> : a.np == 1 ? gated_state_kernel<1, false> : gated_state_kernel<2, false>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e == cudaSuccess && fused && a.R / 32 > 8)
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
-  return launch_pdl(fn, dim3(a.R / (32 / a.np), (a.B + kStepRows - 1) / kStepRows), dim3(kStepWarps * 32), sm, s,
-                    a, i);
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = step_config(a, fused, sm, s, attr);
+  return cudaLaunchKernelEx(&cfg, fn, a, i);
 }
 cudaError_t launch_gated_r(const GatedArgs& a, int i, cudaStream_t s) {
   if (a.R > 512 || a.R % 64 || a.B < 1 || a.np < 1 || a.np > 2) return cudaErrorInvalidValue;

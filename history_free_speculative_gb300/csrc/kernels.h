@@ -130,8 +130,12 @@ struct GatedArgs {
   int* status = nullptr;
   int warm = 0;                      // s_0 from a warm-up step on the token before the anchor
 };
-cudaError_t launch_gated_state(const GatedArgs& a, int i, cudaStream_t s);
+// fused: the step's r in the same launch (one weight plane; a cluster of R / 32
+// CTAs per group of 4 requests). gated_step_clusters: how many such clusters
+// the device runs at once (0: the fused form is unavailable)
+cudaError_t launch_gated_state(const GatedArgs& a, int i, bool fused, cudaStream_t s);
 cudaError_t launch_gated_r(const GatedArgs& a, int i, cudaStream_t s);
+int gated_step_clusters(const GatedArgs& a);
 cudaError_t launch_gated_sum(const float* part, const Splits& sp, int rows, int cols, float* out,
                              cudaStream_t s);
 cudaError_t launch_gated_final(const GatedArgs& a, cudaStream_t s);
