@@ -510,15 +510,23 @@ __global__ void __launch_bounds__(kRowThreads, kMinCtas) resnorm_kernel(ResNormA
   const size_t stride = (size_t)a.rows * D;
   float4 v[kVec];
   float ss = 0.f;
+  // every load of the thread first (no store in between that the compiler would
+  // have to order them after), then the stores
 #pragma unroll
   for (int k = 0; k < kVec; ++k) {
     const int i = i0 + threadIdx.x + k * blockDim.x;
     if (i < i0 + n4) {
-      float4 x = *reinterpret_cast<const float4*>(a.x + (size_t)r * D + 4 * i);
-      x = f4add(x, sum_splits4<kDepth>(a.part + (size_t)r * D + 4 * i, stride, splits_at(a.sp, r, 4 * i)));
+      const float4 x = *reinterpret_cast<const float4*>(a.x + (size_t)r * D + 4 * i);
+      v[k] = f4add(x, sum_splits4<kDepth>(a.part + (size_t)r * D + 4 * i, stride, splits_at(a.sp, r, 4 * i)));
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kVec; ++k) {
+    const int i = i0 + threadIdx.x + k * blockDim.x;
+    if (i < i0 + n4) {
+      const float4 x = v[k];
       *reinterpret_cast<float4*>(a.x + (size_t)r * D + 4 * i) = x;
       if (a.tap_x) *reinterpret_cast<float4*>(a.tap_x + (size_t)r * D + 4 * i) = x;
-      v[k] = x;
       ss += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
     }
   }
@@ -585,8 +593,11 @@ cudaError_t launch_resnorm(const ResNormArgs& a, cudaStream_t s) {
   // a cluster per row: few CTAs, deep loads (every plane of a few-row product, up
   // to 8, in flight at once); else two CTAs per SM (all rows in one wave)
   if (n4 > threads * (C > 1 ? 1 : kRowVec)) return cudaErrorInvalidValue;
-  return C > 1 ? cudaLaunchKernelEx(&cfg, resnorm_kernel<8, 1, 1>, a)
-               : cudaLaunchKernelEx(&cfg, resnorm_kernel<2, 2, kRowVec>, a);
+  if (C > 1) return cudaLaunchKernelEx(&cfg, resnorm_kernel<8, 1, 1>, a);
+  // one CTA per row: as many float4 per thread as the row needs, so that every
+  // split plane's load of them can be in flight at once within the registers
+  if (n4 <= 2 * threads) return cudaLaunchKernelEx(&cfg, resnorm_kernel<4, 2, 2>, a);
+  return cudaLaunchKernelEx(&cfg, resnorm_kernel<2, 2, kRowVec>, a);
 }
 
 // ---------------------------------------------------------------- SwiGLU epilogue
