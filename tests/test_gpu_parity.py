@@ -486,21 +486,31 @@ def test_shift_group_matches_oracle(small_v):
 
 # ---------------------------------------------------------------- gated token-feedback head
 
-@pytest.mark.parametrize("name", ["tiny", "bf16"])
+@pytest.mark.parametrize("name", ["tiny", "bf16", "bf16-r512-b32"])
 @pytest.mark.parametrize("T", [0.0, 0.7])
 def test_gated_head_round_parity(name, T):
     """The official gated head: per-step vectors r_i and candidates (greedy and
-    sampled, token fed back each step) against the oracle."""
+    sampled, token fed back each step) against the oracle. With one weight plane
+    the step's r runs in the state kernel's launch when all its clusters (R / 32
+    CTAs, 4 requests each) are resident at once: R = 128 with 12 requests takes
+    that form; R = 512 with 32 requests (eight 16-CTA clusters) the two launches
+    on devices that hold fewer clusters at once."""
+    B = 12
     if name == "tiny":
         cfg = wk.shrink(wk.TINY, R=64, head="gated")
         W = wk.make_weights(cfg, 31, gain_jitter=True)
         tol = 1e-4
-    else:
+    elif name == "bf16":
         cfg = wk.shrink(wk.QWEN3_8B, D=512, F=1024, L_D=2, n_q=4, n_kv=2, R=128, V=4096, m=6, head="gated")
         W = wk.make_weights(cfg, 32)
         tol = HIDDEN_REL_TOL
+    else:
+        cfg = wk.shrink(wk.QWEN3_8B, D=512, F=1024, L_D=1, n_q=4, n_kv=2, R=512, V=4096, m=6, head="gated")
+        W = wk.make_weights(cfg, 33)
+        tol = HIDDEN_REL_TOL
+        B = 32
     wl = wk.WORKLOADS["tiny"]
-    B, seed = 12, 77
+    seed = 77
     dr = _drafter(cfg, W, B_max=B)
     try:
         hidden, anchor, pos = wk.make_round_inputs(wl, B=B, cfg=cfg)
