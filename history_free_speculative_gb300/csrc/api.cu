@@ -1585,7 +1585,8 @@ int dlite_selftest_gemm(int rows, int outs, int K, int xplanes, int wplanes, con
       pl.S = (pl.kblocks + pl.kb_per_split - 1) / pl.kb_per_split;
     }
     pl.stage_bytes = (uint32_t)wplanes * pl.N * 128 + (uint32_t)pl.n_mt * xplanes * tc::a_slot_bytes(tc::x_box_rows(rows));
-    int stmax = (int)((tc::kSmemBudget - 2048 - tc::kTailPad) / pl.stage_bytes);
+    pl.tail_pad = tc::x_box_rows(rows) < 128 ? (uint32_t)tc::kTailPad : 0u;
+    int stmax = (int)((tc::kSmemBudget - 2048 - pl.tail_pad) / pl.stage_bytes);
     pl.stages = plan_override[2] ? plan_override[2] : (stmax > 8 ? 8 : stmax);
     int cols = 32;
     while (cols < pl.N * pl.n_mt) cols <<= 1;

@@ -25,11 +25,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap mx0, const __grid_constant__ CUtensorMap mx1,
                    const __grid_constant__ CUtensorMap mw0, const __grid_constant__ CUtensorMap mw1,
                    const __grid_constant__ CUtensorMap mo, const TcParams p) {
-  // Shared memory: [barriers | pad to 1 KB] [stage 0] ... [stage S-1] [kTailPad].
+  // Shared memory: [barriers | pad to 1 KB] [stage 0] ... [stage S-1] [tail pad].
   // Stage: [activation slots: NMT x XP x a_slot] [weight planes: WP x N rows x 128 B].
-  // An activation slot holds only the x_box loaded rows; the 128-row MMA operand
-  // overhangs into the following bytes (stale data feeding only unused TMEM lanes),
-  // and the tail pad keeps that overhang inside the allocation.
+  // An activation slot holds only the x_box loaded rows; with fewer than 128 the
+  // 128-row MMA operand overhangs into the following bytes (stale data feeding
+  // only unused TMEM lanes), and the tail pad keeps that overhang inside the
+  // allocation (full 128-row slots need none: one more stage fits).
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)base;
@@ -441,7 +442,8 @@ Plan plan(int rows, int outs, int K, int xplanes, int wplanes, bool lm, bool one
     for (int N = 64; N <= 256; N += 64) {
       if (N * n_mt > 512 || N > nmax_out) continue;  // weight buffers hold >= nmax_out rows
       const uint32_t sb = (uint32_t)wplanes * N * 128 + (uint32_t)n_mt * xplanes * a_slot_bytes(x_box_rows(rows));
-      int stages = (int)((kSmemBudget - 2048 - kTailPad) / sb);
+      const uint32_t pad = x_box_rows(rows) < 128 ? (uint32_t)kTailPad : 0u;
+      int stages = (int)((kSmemBudget - 2048 - pad) / sb);
       if (stages > 8) stages = 8;
       if (stages < 2) continue;
       const int slabs = (outs + N - 1) / N;
@@ -481,6 +483,7 @@ Plan plan(int rows, int outs, int K, int xplanes, int wplanes, bool lm, bool one
           best.groups = groups;
           best.stages = stages;
           best.stage_bytes = sb;
+          best.tail_pad = pad;
           best.tmem_cols = next_pow2_cols(N * n_mt);
         }
       }
@@ -503,7 +506,8 @@ std::vector<Plan> plan_candidates(int rows, int outs, int K, int xplanes, int wp
     for (int N = 64; N <= 256; N += 64) {
       if (N * n_mt > 512 || N > nmax_out) continue;
       const uint32_t sb = (uint32_t)wplanes * N * 128 + (uint32_t)n_mt * xplanes * a_slot_bytes(x_box_rows(rows));
-      int stages = (int)((kSmemBudget - 2048 - kTailPad) / sb);
+      const uint32_t pad = x_box_rows(rows) < 128 ? (uint32_t)kTailPad : 0u;
+      int stages = (int)((kSmemBudget - 2048 - pad) / sb);
       if (stages > 8) stages = 8;
       if (stages < 2) continue;
       const int scap = rows <= 64 ? 16 : 4;
@@ -521,6 +525,7 @@ std::vector<Plan> plan_candidates(int rows, int outs, int K, int xplanes, int wp
         p.groups = groups;
         p.stages = stages;
         p.stage_bytes = sb;
+        p.tail_pad = pad;
         p.tmem_cols = next_pow2_cols(N * n_mt);
         out.push_back(p);
       }
@@ -531,7 +536,7 @@ std::vector<Plan> plan_candidates(int rows, int outs, int K, int xplanes, int wp
 
 size_t smem_bytes(const Plan& pl) {
   // the epilogue reuses the first 64 KB of the stage memory as staging boxes (4 KB per warp)
-  size_t stage_mem = (size_t)pl.stages * pl.stage_bytes + kTailPad;
+  size_t stage_mem = (size_t)pl.stages * pl.stage_bytes + pl.tail_pad;
   if (stage_mem < 65536) stage_mem = 65536;
   return 1024 /* align */ + 1024 /* barriers */ + stage_mem;
 }

@@ -16,7 +16,7 @@ constexpr int kThreads = 64 + 128 * kEpiGroups;  // TMA warp, MMA warp, epilogue
 constexpr int kGemmEpiGroups = 4;
 constexpr int kGemmThreads = 64 + 128 * kGemmEpiGroups;
 constexpr size_t kSmemBudget = 226 * 1024;  // dynamic shared memory per CTA (all of it)
-constexpr size_t kTailPad = 16 * 1024;      // overhang room for a 128-row operand read
+constexpr size_t kTailPad = 16 * 1024;      // overhang room for a 128-row operand read of a short slot
 
 struct Plan {
   bool ok = false;
@@ -29,6 +29,7 @@ struct Plan {
   int stages = 2;
   uint32_t stage_bytes = 0;
   int tmem_cols = 32;
+  uint32_t tail_pad = 0;  // behind the last stage when the activation slots hold < 128 rows
 };
 
 struct TcParams {
