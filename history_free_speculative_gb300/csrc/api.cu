@@ -922,11 +922,16 @@ static int tune_products(dlite_handle* h) {
                       tc::pair_plan(st.rows, st.outs, st.X.K, h->num_sms).ok;
     if (pair) continue;  // the pair engine serves this product
     TunedPlan best;
-    float best_ms = 1e30f;
+    float best_ms = 1e30f, model_ms = 1e30f;
+    // the analytical plan stays unless a timed one beats it clearly: one cold
+    // launch per candidate is noisy, and near-equal tilings flipped from one
+    // handle to the next
+    const tc::Plan model = tc::plan(st.rows, st.outs, st.X.K, st.X.n, st.W.n, false, st.act != nullptr,
+                                    st.skip_row0, st.skip_cols);
     for (const tc::Plan& pl : tc::plan_candidates(st.rows, st.outs, st.X.K, st.X.n, st.W.n, st.act != nullptr)) {
       if (!st.act && (size_t)pl.S * st.rows * st.outs > h->part_cap) continue;
       float t = 1e30f;
-      for (int rep = 0; rep < 2 && !rc; ++rep) {
+      for (int rep = 0; rep < 3 && !rc; ++rep) {
         float ms = 0.f;
         // weights from HBM, activations L2-resident (as written by the previous kernel of a round)
         bool ok = cudaMemsetAsync(flush, rep, flush_bytes, s) == cudaSuccess;
@@ -944,12 +949,14 @@ static int tune_products(dlite_handle* h) {
         }
         t = std::min(t, ms);
       }
+      if (!rc && model.ok && pl.N == model.N && pl.S == model.S && pl.n_mt == model.n_mt && pl.groups == model.groups)
+        model_ms = t;
       if (!rc && t < best_ms) {
         best_ms = t;
         best = {st.rows, st.outs, st.X.K, st.X.n, st.W.n, st.act != nullptr, st.skip_row0, st.skip_cols, pl};
       }
     }
-    if (!rc && best_ms < 1e29f) h->tuned.push_back(best);
+    if (!rc && best_ms < 1e29f && best_ms < 0.97f * model_ms) h->tuned.push_back(best);
   }
   if (e0) cudaEventDestroy(e0);
   if (e1) cudaEventDestroy(e1);
