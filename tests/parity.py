@@ -62,3 +62,19 @@ def check_candidates_bf16(cand, ocand, ogap, E, h_gpu, h_mir, own_choice, T=0.0,
     allowed = max(1, int(max_frac * cand.size))
     assert len(bad) <= allowed, f"{len(bad)} of {cand.size} candidates differ"
     return len(bad)
+
+
+def check_fed_back_candidates(cand, ocand, ogap, E, h_gpu, h_mir, own_choice, T=0.0, bf16=True):
+    """Candidates of a head that feeds each step's token into the next step (the
+    gated head): after a request's first differing token the two sides draft from
+    different prefixes, so the positions past it are not compared; the first
+    difference itself is checked like any other (check_candidates_bf16 for bf16
+    activations, the tie band otherwise)."""
+    cand, ocand = np.array(cand), np.asarray(ocand)
+    for n in range(cand.shape[0]):
+        bad = np.nonzero(cand[n] != ocand[n])[0]
+        if len(bad):
+            cand[n, bad[0] + 1:] = ocand[n, bad[0] + 1:]
+    if bf16:
+        return check_candidates_bf16(cand, ocand, ogap, E, h_gpu, h_mir, own_choice, T)
+    return check_candidates(cand, ocand, ogap)

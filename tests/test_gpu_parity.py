@@ -15,7 +15,7 @@ from history_free_speculative_gb300 import binding
 from history_free_speculative_gb300 import workload as wk
 from oracle import dlite_oracle as O
 from oracle import philox as ph
-from parity import HIDDEN_REL_TOL, check_candidates, check_candidates_bf16, f64_weights, rel_err
+from parity import HIDDEN_REL_TOL, check_candidates, check_candidates_bf16, check_fed_back_candidates, f64_weights, rel_err
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -446,7 +446,7 @@ def test_group_round_parity(name, G):
                 "hs": torch.empty(B, cfg.K, cfg.D, device=DEV)}
         dr.draft_round(hidden.to(DEV), groups.to(DEV), 0.0, 0, pos.to(DEV), out["cand"], out["qstats"], taps=taps)
         torch.cuda.synchronize()
-        cands, ocands, gaps = [], [], []
+        cands, ocands, gaps, hmir = [], [], [], []
         for b in range(B):
             t = {}
             r = O.draft_request(hidden[b], groups[b].numpy(), W, cfg, taps=t, mirror=(cfg.dtype == "bf16"))
@@ -456,7 +456,12 @@ def test_group_round_parity(name, G):
             cands.append(out["cand"][b].cpu().numpy())
             ocands.append(r["cand"])
             gaps.append(r["gap"])
-        check_candidates(np.stack(cands), np.stack(ocands), np.stack(gaps))
+            hmir.append(t["h"])
+        if cfg.dtype == "bf16":   # a flip must be the own head state's exact choice at a bridgeable gap
+            check_candidates_bf16(np.stack(cands), np.stack(ocands), np.stack(gaps), O.f64(W["E"]),
+                                  taps["hs"].cpu().numpy(), hmir, lambda n, i, ell: int(np.argmax(ell)))
+        else:
+            check_candidates(np.stack(cands), np.stack(ocands), np.stack(gaps))
     finally:
         dr.close()
 
@@ -525,7 +530,7 @@ def test_gated_head_round_parity(name, T):
         torch.cuda.synchronize()
         cand = out["cand"].cpu().numpy()
         qs = out["qstats"].cpu().numpy()
-        cands, ocands, gaps = [], [], []
+        cands, ocands, gaps, hmir = [], [], [], []
         for b in range(B):
             r = O.draft_request(hidden[b], int(anchor[b]), W, cfg, temperature=T, seed=seed, pos=int(pos[b]),
                                 request=b, mirror=(cfg.dtype == "bf16"))
@@ -539,7 +544,11 @@ def test_gated_head_round_parity(name, T):
             cands.append(cand[b])
             ocands.append(r["cand"])
             gaps.append(r["gap"])
-        check_candidates(np.stack(cands), np.stack(ocands), np.stack(gaps))
+            hmir.append(r["h"])
+        Tq = float(np.float32(T))
+        own = lambda n, i, ell: O.sample_logits(ell, Tq if T > 0 else 0.0, seed, int(pos[n]) + i + 1, n)[0]
+        check_fed_back_candidates(np.stack(cands), np.stack(ocands), np.stack(gaps), O.f64(W["W_o"]),
+                                  taps["hs"].cpu().numpy(), hmir, own, T=Tq, bf16=cfg.dtype == "bf16")
     finally:
         dr.close()
 
@@ -573,7 +582,7 @@ def test_gated_head_warmup_round_parity(name, T):
                        taps={"z": None, "x": None, "b": None, "hs": rv})
         torch.cuda.synchronize()
         cand, rvec = out["cand"].cpu().numpy(), rv.cpu().numpy()
-        cands, ocands, gaps = [], [], []
+        cands, ocands, gaps, hmir = [], [], [], []
         for b in range(B):
             r = O.draft_request(hidden[b], group[b].tolist(), W, cfg, temperature=T, seed=seed, pos=int(pos[b]),
                                 request=b, mirror=(cfg.dtype == "bf16"))
@@ -586,7 +595,11 @@ def test_gated_head_warmup_round_parity(name, T):
             cands.append(cand[b])
             ocands.append(r["cand"])
             gaps.append(r["gap"])
-        check_candidates(np.stack(cands), np.stack(ocands), np.stack(gaps))
+            hmir.append(r["h"])
+        Tq = float(np.float32(T))
+        own = lambda n, i, ell: O.sample_logits(ell, Tq if T > 0 else 0.0, seed, int(pos[n]) + i + 1, n)[0]
+        check_fed_back_candidates(np.stack(cands), np.stack(ocands), np.stack(gaps), O.f64(W["W_o"]), rvec, hmir,
+                                  own, T=Tq, bf16=cfg.dtype == "bf16")
     finally:
         dr.close()
 
@@ -722,7 +735,9 @@ def test_round_host_sampling_matches_device_path(tiny):
 @pytest.mark.parametrize("name", ["qwen3-4b-b1", "qwen3-8b-b32"])
 def test_full_size_round_sampled_requests(name):
     """Full-size drafter in the bench's launch configuration; the oracle checks
-    two sampled requests end to end (pure for hidden states, mirror for tokens)."""
+    two sampled requests end to end (pure for hidden states, mirror for tokens;
+    a differing token must be the exact choice of the drafter's own head state
+    at a gap within reach of the head-state difference)."""
     wl = wk.WORKLOADS[name]
     cfg = wl.cfg
     B = wl.B
@@ -741,18 +756,26 @@ def test_full_size_round_sampled_requests(name):
     del W
     dr_cand = out["cand"].cpu().numpy()
     sample = [0, B - 1] if B > 1 else [0]
-    cands, ocands, gaps = [], [], []
+    cands, ocands, gaps, hgpu, hmir = [], [], [], [], []
     for b in sample:
         pure = O.draft_request(hidden[b].cpu(), int(anchor[b]), Wc, cfg, temperature=T,
                                seed=wl.rng_seed, pos=int(pos[b]), request=b, mirror=False)
+        tm = {}
         mir = O.draft_request(hidden[b].cpu(), int(anchor[b]), Wc, cfg, temperature=T,
-                              seed=wl.rng_seed, pos=int(pos[b]), request=b, mirror=True)
+                              seed=wl.rng_seed, pos=int(pos[b]), request=b, mirror=True, taps=tm)
         assert rel_err(taps["b"][b].cpu(), pure["b"]) < HIDDEN_REL_TOL
         assert rel_err(taps["hs"][b].cpu(), pure["h"]) < HIDDEN_REL_TOL
         cands.append(dr_cand[b])
         ocands.append(mir["cand"])
         gaps.append(mir["gap"])
-    check_candidates(np.stack(cands), np.stack(ocands), np.stack(gaps))
+        hgpu.append(taps["hs"][b].cpu().numpy())
+        hmir.append(tm["h"])
+    # bf16 activations: a differing candidate must be the exact choice of the
+    # drafter's own head state, at a gap the head-state difference can bridge
+    Tq = float(np.float32(T))
+    own = lambda n, i, ell: O.sample_logits(ell, Tq if T > 0 else 0.0, wl.rng_seed,
+                                            int(pos[sample[n]]) + i + 1, sample[n])[0]
+    check_candidates_bf16(np.stack(cands), np.stack(ocands), np.stack(gaps), Wc["E"], hgpu, hmir, own, T=Tq)
     dr.close()
 
 
@@ -853,7 +876,9 @@ def test_full_size_history_round_sampled_requests():
     """The 8B-shape history-KV control at B = 8 with an 8192-row ring, in the
     bench's launch configuration: two sampled requests against the oracle
     drafter attending over its own ring (pure for hidden states, mirror for
-    tokens), and their rings after the append."""
+    tokens; a differing token must be the exact choice of the drafter's own
+    head state at a gap within reach of the head-state difference), and their
+    rings after the append."""
     H = 8192
     wl = wk.WORKLOADS["qwen3-8b-history"]
     cfg = wk.shrink(wl.cfg, history=H)
@@ -863,30 +888,36 @@ def test_full_size_history_round_sampled_requests():
     dr = binding.Drafter(cfg, W, B_max=B)
     hidden, anchor, pos = wk.make_round_inputs(wl, device=DEV)
     out = dr.new_outputs(B, DEV)
-    taps = {"b": torch.empty(B, cfg.K, cfg.D, device=DEV)}
+    taps = {"b": torch.empty(B, cfg.K, cfg.D, device=DEV), "hs": torch.empty(B, cfg.K, cfg.D, device=DEV)}
     dr.draft_round(hidden, anchor, 0.0, wl.rng_seed, pos, out["cand"], out["qstats"], taps=taps)
     torch.cuda.synchronize()
     rc, st = dr.device_status()
     assert rc == 0 and st == 0
     Wc = f64_weights(wk.weights_to(W, "cpu"))
     del W
-    cands, ocands, gaps = [], [], []
+    cands, ocands, gaps, hgpu, hmir = [], [], [], [], []
     for b in (1, B - 1):
         hp = O.HistoryCache(cfg, H, b)
         hm = O.HistoryCache(cfg, H, b)
         pure = O.draft_request(hidden[b].cpu(), int(anchor[b]), Wc, cfg, mirror=False, history=hp)
-        mir = O.draft_request(hidden[b].cpu(), int(anchor[b]), Wc, cfg, mirror=True, history=hm)
+        tm = {}
+        mir = O.draft_request(hidden[b].cpu(), int(anchor[b]), Wc, cfg, mirror=True, history=hm, taps=tm)
         assert rel_err(taps["b"][b].cpu(), pure["b"]) < HIDDEN_REL_TOL
         cands.append(out["cand"][b].cpu().numpy())
         ocands.append(mir["cand"])
         gaps.append(mir["gap"])
+        hgpu.append(taps["hs"][b].cpu().numpy())
+        hmir.append(tm["h"])
         for l in range(cfg.L_D):
             ring, cur = dr.history_read(l, b, 0)
             got = ring.float().cpu().numpy().transpose(1, 0, 2)
             assert cur == K1 and hm.cursor == K1
             assert np.array_equal(got[K1:], hm.k[l][K1:])
             assert rel_err(got[:K1], hm.k[l][:K1]) < HIDDEN_REL_TOL
-    check_candidates(np.stack(cands), np.stack(ocands), np.stack(gaps))
+    # bf16 activations: a differing candidate must be the exact choice of the
+    # drafter's own head state, at a gap the head-state difference can bridge
+    check_candidates_bf16(np.stack(cands), np.stack(ocands), np.stack(gaps), Wc["E"], hgpu, hmir,
+                          lambda n, i, ell: int(np.argmax(ell)))
     dr.close()
 
 
