@@ -131,19 +131,21 @@ __global__ void __launch_bounds__(kLmThreads, 1)
                                 : kWTile + (uint32_t)x_box * 128u * (p.rep ? 4u : 1u);
     const uint32_t fullb = PAIR ? map_to_rank(full0, 0) : full0;
     const CUtensorMap* mx = tile ? &mx1 : &mx0;
-    auto load_w = [&](int i, int s) {
+    // One lane issues every copy, so its per-stage instruction latency bounds
+    // the stream: the stage, its phase, the k block and the slab advance by
+    // increments (integer division by a runtime divisor costs tens of cycles).
+    auto load_w = [&](int s, int kb, int slab) {
       const uint32_t st = su32(smem + (size_t)s * p.stage_bytes);
-      const int slab = unit + (i / nkb) * n_units;
       if (!PAIR || tile == 0) mbar_expect_tx(full0 + 8 * s, bytes);
-      const int kb = (i % nkb + rot) % nkb, wrow = (slab * N + tile * (int)kWRows) >> 6;
+      const int wrow = (slab * N + tile * (int)kWRows) >> 6;
       if (PAIR)
         tma_load_4d_pair(st + wofs, &mw, fullb + 8 * s, kb, wrow);
       else
         tma_load_4d(st + wofs, &mw, fullb + 8 * s, kb, wrow);
     };
-    auto load_x = [&](int i, int s) {
+    auto load_x = [&](int s, int kb) {
       const uint32_t st = su32(smem + (size_t)s * p.stage_bytes);
-      const int kx = ((i % nkb + rot) % nkb) * 64;
+      const int kx = kb * 64;
       if (PAIR)
         tma_load_2d_pair(st, mx, fullb + 8 * s, kx, tile * 128);
       else if (p.rep)  // one copy of the rows per TMEM lane quadrant
@@ -155,27 +157,55 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     // before waiting for h.
     const int total = n_mine * nkb;
     const int pre = total < p.stages ? total : p.stages;
-    if (lane == 0)
-      for (int i = 0; i < pre; ++i) load_w(i, i);
+    if (lane == 0) {
+      int kb = rot, j = 0, slab = unit;
+      for (int i = 0; i < pre; ++i) {
+        load_w(i, kb, slab);
+        if (++kb == nkb) kb = 0;
+        if (++j == nkb) {
+          j = 0;
+          slab += n_units;
+        }
+      }
+    }
     __syncwarp();
     pdl_wait();
-    if (lane == 0)
-      for (int i = 0; i < pre; ++i) load_x(i, i);
+    if (lane == 0) {
+      int kb = rot;
+      for (int i = 0; i < pre; ++i) {
+        load_x(i, kb);
+        if (++kb == nkb) kb = 0;
+      }
+    }
     __syncwarp();
+    // cursor of copy i = pre: stage s (phase ph of its use), k block kb, the
+    // j-th block of the slab
+    int s = pre % p.stages, j = pre % nkb;
+    int kb = (j + rot) % nkb, slab = unit + (pre / nkb) * n_units;
+    uint32_t ph = (uint32_t)(pre / p.stages) & 1u;
     int issued = pre;
     bool ok = true;
     for (int i = pre; i < total; ++i) {
-      const int s = i % p.stages;
-      if (!mbar_wait_warp(empty0 + 8 * s, (uint32_t)(i / p.stages - 1) & 1, p.status)) {
+      // the slot's previous use (copy i - stages) had the other phase
+      if (!mbar_wait_warp(empty0 + 8 * s, ph ^ 1u, p.status)) {
         ok = false;
         break;
       }
       if (lane == 0) {
-        load_w(i, s);
-        load_x(i, s);
+        load_w(s, kb, slab);
+        load_x(s, kb);
       }
       __syncwarp();
       issued = i + 1;
+      if (++s == p.stages) {
+        s = 0;
+        ph ^= 1u;
+      }
+      if (++kb == nkb) kb = 0;
+      if (++j == nkb) {
+        j = 0;
+        slab += n_units;
+      }
     }
     if (!ok && (!PAIR || tile == 0)) {  // let the copies still in flight land before the CTA exits
       for (int i = issued - p.stages < 0 ? 0 : issued - p.stages; i < issued; ++i)
@@ -188,16 +218,16 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     const uint64_t wbase = (uint64_t)(a_slot_bytes(p.rep ? 128 : p.x_box0) >> 4);
     const uint64_t desc0 = sw128_desc(su32(smem));
     const uint64_t sdelta = (uint64_t)(p.stage_bytes >> 4);
-    int i = 0;
+    int s = 0;  // stage of the next k block and the phase of its use
+    uint32_t ph = 0;
     bool ok = true;
     for (int t = 0; t < n_mine && ok; ++t) {
       const int b = t & 1;
       if (t >= 2 && !mbar_wait_warp(acce0 + 8 * b, (uint32_t)((t >> 1) - 1) & 1, p.status)) break;
       fence_after();
       const uint32_t dcol = tmem + (uint32_t)b * kAccCols;
-      for (int j = 0; j < nkb; ++j, ++i) {
-        const int s = i % p.stages;
-        if (!mbar_wait_warp(full0 + 8 * s, (uint32_t)(i / p.stages) & 1, p.status)) {
+      for (int j = 0; j < nkb; ++j) {
+        if (!mbar_wait_warp(full0 + 8 * s, ph, p.status)) {
           ok = false;
           break;
         }
@@ -220,6 +250,10 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             umma_commit(empty0 + 8 * s);
         }
         __syncwarp();
+        if (++s == p.stages) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
       if (ok && lane == 0) {
         if (PAIR)

@@ -85,19 +85,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t a_slot = a_slot_bytes(p.x_box);
     // k blocks in a per-CTA rotated order: concurrent CTAs fetch different
     // activation tiles instead of all hitting the same L2 lines
-    auto load_w = [&](int i, int s) {
+    // One lane issues every copy, so its per-stage instruction latency bounds
+    // the stream: stage, phase and k block advance by increments (integer
+    // division by a runtime divisor costs tens of cycles). kr = (i + rot) % nkb.
+    auto load_w = [&](int kr, int s) {
       const uint32_t st = su32(smem + (size_t)s * p.stage_bytes);
       const uint32_t fb = full0 + 8 * s;
-      const int kb = kb0 + (i + rot) % nkb;
+      const int kb = kb0 + kr;
       mbar_expect_tx(fb, bytes);
       const uint32_t wst = st + (uint32_t)(NMT * XP) * a_slot;
       tma_load_4d(wst, &mw0, fb, kb, o0 >> 6);
       if (WP == 2) tma_load_4d(wst + wtile, &mw1, fb, kb, o0 >> 6);
     };
-    auto load_x = [&](int i, int s) {
+    auto load_x = [&](int kr, int s) {
       const uint32_t st = su32(smem + (size_t)s * p.stage_bytes);
       const uint32_t fb = full0 + 8 * s;
-      const int kx = (kb0 + (i + rot) % nkb) * 64;
+      const int kx = (kb0 + kr) * 64;
 #pragma unroll
       for (int mt = 0; mt < NMT; ++mt)
 #pragma unroll
@@ -108,21 +111,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // weight tiles before waiting for it, then the activations.
     const int pre = nkb < p.stages ? nkb : p.stages;
     if (lane == 0)
-      for (int i = 0; i < pre; ++i) load_w(i, i);
+      for (int i = 0, kr = rot; i < pre; ++i) {
+        load_w(kr, i);
+        if (++kr == nkb) kr = 0;
+      }
     __syncwarp();
     pdl_wait();
     if (lane == 0)
-      for (int i = 0; i < pre; ++i) load_x(i, i);
+      for (int i = 0, kr = rot; i < pre; ++i) {
+        load_x(kr, i);
+        if (++kr == nkb) kr = 0;
+      }
     __syncwarp();
+    // cursor of copy i = pre: stage s, the phase ph of its use, k block kr
+    int s = pre == p.stages ? 0 : pre, kr = pre + rot >= nkb ? pre + rot - nkb : pre + rot;
+    uint32_t ph = pre == p.stages ? 1u : 0u;
     for (int i = pre; i < nkb; ++i) {
-      const int s = i % p.stages;
-      const uint32_t it = (uint32_t)(i / p.stages);
-      if (!mbar_wait_warp(empty0 + 8 * s, (it - 1) & 1, p.status)) break;
+      // the slot's previous use (copy i - stages) had the other phase
+      if (!mbar_wait_warp(empty0 + 8 * s, ph ^ 1u, p.status)) break;
       if (lane == 0) {
-        load_w(i, s);
-        load_x(i, s);
+        load_w(kr, s);
+        load_x(kr, s);
       }
       __syncwarp();
+      if (++s == p.stages) {
+        s = 0;
+        ph ^= 1u;
+      }
+      if (++kr == nkb) kr = 0;
     }
   } else if (warp == 1) {  // ---------------- MMA issuer
     constexpr int kCombos = 1 + (XP == 2) + (WP == 2);
@@ -136,10 +152,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint64_t aslot = (uint64_t)(a_slot >> 4);
     const uint64_t desc0 = sw128_desc(su32(smem));
     const uint64_t sdelta = (uint64_t)(p.stage_bytes >> 4);
+    int s = 0;  // stage of k block i and the phase of its use
+    uint32_t ph = 0;
     for (int i = 0; i < nkb; ++i) {
-      const int s = i % p.stages;
-      const uint32_t it = (uint32_t)(i / p.stages);
-      if (!mbar_wait_warp(full0 + 8 * s, it & 1, p.status)) break;
+      if (!mbar_wait_warp(full0 + 8 * s, ph, p.status)) break;
       fence_after();
       if (lane == 0) {
         const uint64_t a0 = desc0 + sdelta * (uint64_t)s;
@@ -163,6 +179,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         umma_commit(empty0 + 8 * s);
       }
       __syncwarp();
+      if (++s == p.stages) {
+        s = 0;
+        ph ^= 1u;
+      }
     }
     if (lane == 0) umma_commit(accf);
     __syncwarp();

@@ -35,7 +35,7 @@ constexpr uint32_t kPairStage = 2 * kATile;  // this CTA's X tile + W tile per k
 constexpr uint32_t kPairStaging = 0;  // the epilogue stores from registers: no staging area
 
 struct Segment {
-  int tile, kb_lo, n, plane;
+  int tile, kb_lo, n, plane, slab, group;
 };
 // Next segment of the unit range [u, end) of worker `pair`: the units up to the
 // end of the current tile; plane = pair - (worker owning the tile's first unit).
@@ -48,6 +48,8 @@ __device__ __forceinline__ bool next_segment(const PairParams& p, long long& u, 
   const long long lim = (tile + 1) * p.kblocks < end ? (tile + 1) * p.kblocks : end;
   sg.n = (int)(lim - u);
   sg.plane = pair - (int)(((tile * p.kblocks + 1) * p.G - 1) / p.U);
+  sg.slab = sg.tile % p.slabs;
+  sg.group = sg.tile / p.slabs;
   u = lim;
   return true;
 }
@@ -101,16 +103,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {  // ---------------- TMA producer (both CTAs)
     const uint32_t full_leader = map_to_rank(full0, 0);
-    auto load = [&](const Segment& sg, int j, int i, bool weights, bool acts) {
-      const int s = i % p.stages;
+    // One lane issues every copy, so its per-stage instruction latency bounds
+    // the stream: the stage and its phase advance by increments (integer
+    // division by a runtime divisor costs tens of cycles).
+    auto load = [&](const Segment& sg, int j, int s, bool weights, bool acts) {
       const uint32_t st = su32(smem + (size_t)s * kPairStage);
       const int kb = sg.kb_lo + j;
-      const int slab = sg.tile % p.slabs, group = sg.tile / p.slabs;
       if (weights) {
         if (rank == 0) mbar_expect_tx(full0 + 8 * s, 2u * kPairStage);
-        tma_load_4d_pair(st + kATile, &mw, full_leader + 8 * s, kb, (slab * kPairN + (int)rank * 128) >> 6);
+        tma_load_4d_pair(st + kATile, &mw, full_leader + 8 * s, kb, (sg.slab * kPairN + (int)rank * 128) >> 6);
       }
-      if (acts) tma_load_2d_pair(st, &mx, full_leader + 8 * s, kb * 64, group * 256 + (int)rank * 128);
+      if (acts) tma_load_2d_pair(st, &mx, full_leader + 8 * s, kb * 64, sg.group * 256 + (int)rank * 128);
     };
     // weights do not depend on the previous kernel: request the first stages'
     // weight tiles before waiting for it, then their activation tiles
@@ -132,18 +135,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     long long u = u_begin;
     Segment sg;
-    int i = 0;
+    int i = 0, s = 0;  // copy i goes to stage s in the phase ph of its use
+    uint32_t ph = 0;
     bool ok = true;
     while (ok && next_segment(p, u, u_end, pair, sg)) {
       for (int j = 0; j < sg.n; ++j, ++i) {
-        if (i < p.stages) continue;  // issued above
-        const int s = i % p.stages;
-        if (!mbar_wait_warp(empty0 + 8 * s, (uint32_t)(i / p.stages - 1) & 1, p.status)) {
-          ok = false;
-          break;
+        if (i >= p.stages) {  // the first stages were issued above
+          // the slot's previous use (copy i - stages) had the other phase
+          if (!mbar_wait_warp(empty0 + 8 * s, ph ^ 1u, p.status)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) load(sg, j, s, true, true);
+          __syncwarp();
         }
-        if (lane == 0) load(sg, j, i, true, true);
-        __syncwarp();
+        if (++s == p.stages) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
     }
   } else if (warp == 1) {  // ---------------- MMA issuer (rank 0)
@@ -154,16 +163,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t wofs = (uint64_t)(kATile >> 4);
       long long u = u_begin;
       Segment sg;
-      int i = 0, t = 0;
+      int t = 0, s = 0;  // stage of the next k block and the phase of its use
+      uint32_t ph = 0;
       bool ok = true;
       while (ok && next_segment(p, u, u_end, pair, sg)) {
         const int b = t & 1;
         if (t >= 2 && !mbar_wait_warp(acce0 + 8 * b, (uint32_t)((t >> 1) - 1) & 1, p.status)) break;
         fence_after();
         const uint32_t dcol = tmem + (uint32_t)b * kPairN;
-        for (int j = 0; j < sg.n; ++j, ++i) {
-          const int s = i % p.stages;
-          if (!mbar_wait_warp(full0 + 8 * s, (uint32_t)(i / p.stages) & 1, p.status)) {
+        for (int j = 0; j < sg.n; ++j) {
+          if (!mbar_wait_warp(full0 + 8 * s, ph, p.status)) {
             ok = false;
             break;
           }
@@ -177,6 +186,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_commit_pair(empty0 + 8 * s);
           }
           __syncwarp();
+          if (++s == p.stages) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
         // also after an expired wait, so that both epilogues run to the end
         if (lane == 0) umma_commit_pair(accf0 + 8 * b);
