@@ -311,7 +311,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const int j = 8 * k + 2 * e + t2;
                     const float g = __uint_as_float(j < 16 ? g0[j] : g1[j - 16]);
                     const float u = __uint_as_float(j < 16 ? u0[j] : u1[j - 16]);
-                    a2[t2] = g / (1.f + expf(-g)) * u;
+                    // fast exponential and division (a few ulp of fp32, far below the
+                    // bf16 rounding of the stored activation): this epilogue runs after
+                    // the last product of the tile, unhidden; silu -> -0 when exp overflows
+                    a2[t2] = __fdividef(g, 1.f + __expf(-g)) * u;
                   }
                   bf16 h0, l0, h1, l1;
                   if (p.act_planes == 2) {
